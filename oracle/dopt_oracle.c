@@ -1,0 +1,496 @@
+/*
+ * Oracle for the ZeRO-1 distributed-optimizer step over a contiguous flat
+ * gradient/parameter buffer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is a plain, slow, single-threaded CPU
+ * statement of what the step computes.  Only the test suite, the smoke check
+ * and the benchmark's CPU-baseline leg may build or call it.  It shares no
+ * code, header or table with the CUDA library; the two are compared against
+ * each other element by element.
+ *
+ * Sources (page titles and sections):
+ *  [P1]  "04 · 分布式优化器" (Megatron-LM distributed optimizer)
+ *        §2  the flat grad buffer cut into buckets; each bucket split into
+ *            DP equal contiguous ranges, rank r owning range r.
+ *        §3  the ownership demo: 1000 elements, DP 4, shard 250, rank 1 owns
+ *            [250, 500); a param overlapping my range contributes the slice
+ *            intersect(param range, my range).
+ *        §4.1 Range(start, end) with normalize (rebase); the four ranges
+ *            gbuf_world, gbuf_world_in_bucket, gbuf_local, param; every
+ *            bucket size must divide by DP; rank r's range starts at
+ *            r * (bucket size / DP).
+ *        §4.2 reduce-scatter of each bucket: each rank keeps its 1/DP part.
+ *        §4.3 the shard's grad goes to the fp32 main grad sliced by the
+ *            "param" range; Adam runs on the shard only; the updated main
+ *            shard is written back at gbuf_world_in_bucket.
+ *        §4.4 all-gather of param_data gives every rank the full params.
+ *        §5  gradient_scaling_factor multiplies the grads before the
+ *            communication; padding keeps every bucket divisible by DP.
+ *  [P2]  "distributed_training" tutorial, "AllReduce" (reduce-scatter then
+ *        all-gather equals all-reduce) and §8.2 mixed precision (bf16 model
+ *        params, fp32 master weights).
+ *
+ * Readings where the pages leave a step open (each one is listed in the
+ * design notes of the repository):
+ *  R1  Params sit at consecutive offsets in the order given; no per-param
+ *      alignment.
+ *  R2  Buckets are greedy: params are appended to the open bucket, which is
+ *      closed as soon as its unpadded element count reaches bucket_elems
+ *      (bucket_elems == 0: a single bucket).  A param never spans buckets.
+ *      A bucket that holds at least one param is emitted.
+ *  R3  Each bucket is padded at its end to a multiple of D * pad_unit; later
+ *      buckets shift by that padding.  Padding belongs to no param and is
+ *      never read or written by the step.
+ *  R4  gbuf_world of a piece is the piece's own global range (all four
+ *      ranges of a piece have the same length and differ by a translation).
+ *  R5  Scaling: every replica element is widened to fp32 and multiplied by
+ *      the fp32 scaling factor (one rounding) before the reduction; the
+ *      reduction is fp32 in rank order, acc = x_0, acc = acc + x_r.
+ *      The reduced fp32 value feeds Adam directly (no rounding to bf16).
+ *  R6  Adam is AdamW with bias correction and decoupled decay, in fp32,
+ *      each operation rounded once, in this order:
+ *        m = b1*m + (1-b1)*g
+ *        v = b2*v + (1-b2)*(g*g)
+ *        w = w * (1 - lr*wd)                (only where the param decays)
+ *        w = w - step_size * (m / (sqrt(v)/bc2_sqrt + eps))
+ *      with step_size = lr/(1-b1^t) and bc2_sqrt = sqrt(1-b2^t).  The
+ *      per-step scalars (1-b1), (1-b2), (1-lr*wd), step_size, bc2_sqrt are
+ *      evaluated in double from the float hyper-parameters and rounded to
+ *      float once.
+ *  R7  Model params are bf16; fp32 -> bf16 is round-to-nearest-even, NaN
+ *      stays a quiet NaN.
+ *  R8  The all-gather copies every rank's owned elements (its pieces) from
+ *      its own replica into all other replicas; padding is not copied.
+ *
+ * Windows: the step can be restricted to global buffer indices [w0, w1).
+ * All buffer-indexed arrays passed to orc_step are then window-relative
+ * (element i lives at index i - w0).  Elements are independent, so a window
+ * gives exactly the values of the full computation.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_OK 0
+#define ORC_E_ARG (-1)
+#define ORC_E_LAYOUT (-2)
+#define ORC_E_NOMEM (-6)
+
+/* Range(start, end): half-open interval [start, end) ([P1] §4.1). */
+typedef struct {
+    int64_t start;
+    int64_t end;
+} orc_range;
+
+/* One (param, rank) piece with its four ranges ([P1] §4.1 table). */
+typedef struct {
+    orc_range gbuf_world;
+    orc_range gbuf_world_in_bucket;
+    orc_range gbuf_local;
+    orc_range param;
+    int32_t param_id;
+    int32_t bucket_id;
+    int32_t rank;
+    int32_t unused;
+} orc_piece;
+
+/* Range.normalize: the same interval translated to begin at `start`. */
+static orc_range orc_normalize(orc_range r, int64_t start)
+{
+    orc_range out;
+    out.start = start;
+    out.end = start + (r.end - r.start);
+    return out;
+}
+
+static int64_t orc_max(int64_t a, int64_t b) { return a > b ? a : b; }
+static int64_t orc_min(int64_t a, int64_t b) { return a < b ? a : b; }
+
+/* ------------------------------------------------------------------------ */
+/* Layout: flat buffer, greedy buckets, padding (R1-R3).                    */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * param_start/param_end/param_bucket: [n].  bucket_start/bucket_end: room for
+ * n buckets (a bucket holds at least one param).  Returns ORC_OK or an error.
+ */
+int orc_layout(const int64_t *sizes, int32_t n, int32_t D, int64_t bucket_elems,
+               int32_t pad_unit, int64_t *param_start, int64_t *param_end,
+               int32_t *param_bucket, int64_t *bucket_start, int64_t *bucket_end,
+               int32_t *n_buckets_out, int64_t *numel_out)
+{
+    if (n < 0 || D < 1 || pad_unit < 1 || bucket_elems < 0)
+        return ORC_E_ARG;
+    for (int32_t p = 0; p < n; ++p)
+        if (sizes[p] < 0)
+            return ORC_E_ARG;
+
+    int64_t unit = (int64_t)D * (int64_t)pad_unit;
+    int64_t open_start = 0;  /* where the open bucket begins */
+    int64_t open_count = 0;  /* unpadded elements in the open bucket */
+    int32_t open_params = 0; /* params in the open bucket */
+    int32_t nb = 0;
+
+    for (int32_t p = 0; p < n; ++p) {
+        param_start[p] = open_start + open_count;
+        param_end[p] = param_start[p] + sizes[p];
+        param_bucket[p] = nb;
+        open_count += sizes[p];
+        open_params += 1;
+        if (bucket_elems > 0 && open_count >= bucket_elems) {
+            int64_t padded = (open_count + unit - 1) / unit * unit;
+            bucket_start[nb] = open_start;
+            bucket_end[nb] = open_start + padded;
+            nb += 1;
+            open_start += padded;
+            open_count = 0;
+            open_params = 0;
+        }
+    }
+    if (open_params > 0) {
+        int64_t padded = (open_count + unit - 1) / unit * unit;
+        bucket_start[nb] = open_start;
+        bucket_end[nb] = open_start + padded;
+        nb += 1;
+        open_start += padded;
+    }
+    *n_buckets_out = nb;
+    *numel_out = open_start;
+    return ORC_OK;
+}
+
+/* Rank r's range in bucket k: [start + r*S, start + (r+1)*S), S = size/D
+ * ([P1] §4.1, the per-rank ranges of each bucket). */
+static int orc_rank_range(int64_t b_start, int64_t b_end, int32_t D, int32_t r,
+                          orc_range *out)
+{
+    int64_t size = b_end - b_start;
+    if (size % D != 0)
+        return ORC_E_LAYOUT; /* the bucket-divides-by-DP assertion */
+    int64_t S = size / D;
+    out->start = b_start + (int64_t)r * S;
+    out->end = out->start + S;
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Four-way range map ([P1] §3 demo loop and §4.1).                         */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * For every bucket k, every rank r and every param p of bucket k (in order),
+ * the overlap of p's buffer range with r's range gives one piece.  Pieces are
+ * emitted sorted by (bucket, rank, gbuf_world.start).  `pieces` needs room
+ * for n + D * n_buckets entries.
+ */
+int orc_pieces(int32_t n, const int64_t *param_start, const int64_t *param_end,
+               const int32_t *param_bucket, int32_t nb, const int64_t *bucket_start,
+               const int64_t *bucket_end, int32_t D, orc_piece *pieces,
+               int32_t *n_pieces_out)
+{
+    int32_t np = 0;
+    for (int32_t k = 0; k < nb; ++k) {
+        for (int32_t r = 0; r < D; ++r) {
+            orc_range mine;
+            int rc = orc_rank_range(bucket_start[k], bucket_end[k], D, r, &mine);
+            if (rc != ORC_OK)
+                return rc;
+            for (int32_t p = 0; p < n; ++p) {
+                if (param_bucket[p] != k)
+                    continue;
+                int64_t x = orc_max(param_start[p], mine.start);
+                int64_t y = orc_min(param_end[p], mine.end);
+                if (x >= y)
+                    continue;
+                orc_piece pc;
+                memset(&pc, 0, sizeof pc);
+                pc.gbuf_world.start = x;
+                pc.gbuf_world.end = y;
+                pc.gbuf_world_in_bucket = orc_normalize(pc.gbuf_world, x - bucket_start[k]);
+                pc.gbuf_local = orc_normalize(pc.gbuf_world, x - mine.start);
+                pc.param = orc_normalize(pc.gbuf_world, x - param_start[p]);
+                pc.param_id = p;
+                pc.bucket_id = k;
+                pc.rank = r;
+                pieces[np++] = pc;
+            }
+        }
+    }
+    *n_pieces_out = np;
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* bf16 helpers (R7).                                                       */
+/* ------------------------------------------------------------------------ */
+
+static float orc_bits_to_f32(uint32_t u)
+{
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+static uint32_t orc_f32_to_bits(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return u;
+}
+
+float orc_bf16_to_f32(uint16_t h) { return orc_bits_to_f32((uint32_t)h << 16); }
+
+/* Round to nearest, ties to even, on the 16 dropped bits; NaN -> quiet NaN. */
+uint16_t orc_f32_to_bf16(float f)
+{
+    uint32_t u = orc_f32_to_bits(f);
+    if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu) != 0)
+        return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t lower = u & 0xffffu;
+    uint32_t upper = u >> 16;
+    if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u)))
+        upper += 1u; /* may carry into the exponent: overflow gives inf */
+    return (uint16_t)upper;
+}
+
+/* ------------------------------------------------------------------------ */
+/* The step ([P1] §4.2-§4.4, readings R5-R8).                               */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    float lr, beta1, beta2, eps, weight_decay, grad_scale;
+} orc_adam;
+
+/* Per-step scalars, each evaluated in double and rounded to float once (R6). */
+typedef struct {
+    float b1, b2, one_minus_b1, one_minus_b2, decay, step_size, bc2_sqrt, eps, scale;
+} orc_scalars;
+
+static orc_scalars orc_make_scalars(const orc_adam *c, int64_t t)
+{
+    orc_scalars s;
+    double lr = c->lr, b1 = c->beta1, b2 = c->beta2, wd = c->weight_decay;
+    s.b1 = c->beta1;
+    s.b2 = c->beta2;
+    s.one_minus_b1 = (float)(1.0 - b1);
+    s.one_minus_b2 = (float)(1.0 - b2);
+    s.decay = (float)(1.0 - lr * wd);
+    s.step_size = (float)(lr / (1.0 - pow(b1, (double)t)));
+    s.bc2_sqrt = (float)sqrt(1.0 - pow(b2, (double)t));
+    s.eps = c->eps;
+    s.scale = c->grad_scale;
+    return s;
+}
+
+/* Element i of replica r, widened to fp32. */
+static float orc_grad(const void *const *grads, int32_t grad_is_f32, int32_t r, int64_t idx)
+{
+    if (grad_is_f32)
+        return ((const float *)grads[r])[idx];
+    return orc_bf16_to_f32(((const uint16_t *)grads[r])[idx]);
+}
+
+/* One AdamW update of a single element (R6), fp32, one rounding per op. */
+static void orc_adamw(const orc_scalars *s, int decays, float g, float *w, float *m, float *v)
+{
+    float mm = *m, vv = *v, ww = *w;
+    float t1 = s->b1 * mm;
+    float t2 = s->one_minus_b1 * g;
+    mm = t1 + t2;
+    float gg = g * g;
+    float t3 = s->b2 * vv;
+    float t4 = s->one_minus_b2 * gg;
+    vv = t3 + t4;
+    if (decays)
+        ww = ww * s->decay;
+    float root = sqrtf(vv);
+    float corrected = root / s->bc2_sqrt;
+    float denom = corrected + s->eps;
+    float ratio = mm / denom;
+    float delta = s->step_size * ratio;
+    ww = ww - delta;
+    *m = mm;
+    *v = vv;
+    *w = ww;
+}
+
+/*
+ * One optimizer step for all D simulated ranks, restricted to the window
+ * [w0, w1) of global buffer indices.
+ *
+ *   grads[D]        replica gradient buffers (bf16 bits or fp32), read only
+ *   master, exp_avg, exp_avg_sq   fp32, buffer-indexed (element i of the
+ *                   fp32 main params of the param that owns i)
+ *   params[D]       replica bf16 param buffers (bits)
+ *   gather          nonzero: all-gather into every replica (R8); zero: only
+ *                   the owning rank's replica receives its updated shard
+ *   main_grad_out   nullable: the reduce-scattered fp32 main grad of each
+ *                   owned element, buffer-indexed
+ *
+ * All buffer-indexed arrays are window-relative.  Returns ORC_OK or an error.
+ */
+int orc_step(const int64_t *sizes, int32_t n, const uint8_t *wd_mask, int32_t D,
+             int64_t bucket_elems, int32_t pad_unit, const orc_adam *cfg, int64_t step,
+             int32_t grad_is_f32, const void *const *grads, float *master, float *exp_avg,
+             float *exp_avg_sq, uint16_t *const *params, int32_t gather,
+             float *main_grad_out, int64_t w0, int64_t w1)
+{
+    if (step < 1 || w0 < 0 || w1 < w0)
+        return ORC_E_ARG;
+
+    int rc = ORC_OK;
+    int64_t *pstart = NULL, *pend = NULL, *bstart = NULL, *bend = NULL;
+    int32_t *pbucket = NULL;
+    orc_piece *pieces = NULL;
+    float *shard = NULL;
+    int32_t nb = 0, npieces = 0;
+    int64_t numel = 0;
+    size_t cap = (size_t)(n > 0 ? n : 1);
+
+    pstart = (int64_t *)malloc(cap * sizeof *pstart);
+    pend = (int64_t *)malloc(cap * sizeof *pend);
+    pbucket = (int32_t *)malloc(cap * sizeof *pbucket);
+    bstart = (int64_t *)malloc(cap * sizeof *bstart);
+    bend = (int64_t *)malloc(cap * sizeof *bend);
+    if (!pstart || !pend || !pbucket || !bstart || !bend) {
+        rc = ORC_E_NOMEM;
+        goto done;
+    }
+    rc = orc_layout(sizes, n, D, bucket_elems, pad_unit, pstart, pend, pbucket, bstart,
+                    bend, &nb, &numel);
+    if (rc != ORC_OK)
+        goto done;
+    if (w1 > numel) {
+        rc = ORC_E_ARG;
+        goto done;
+    }
+    pieces = (orc_piece *)malloc(((size_t)n + (size_t)D * (size_t)nb + 1) * sizeof *pieces);
+    if (!pieces) {
+        rc = ORC_E_NOMEM;
+        goto done;
+    }
+    rc = orc_pieces(n, pstart, pend, pbucket, nb, bstart, bend, D, pieces, &npieces);
+    if (rc != ORC_OK)
+        goto done;
+
+    orc_scalars sc = orc_make_scalars(cfg, step);
+
+    int32_t first_piece = 0;
+    for (int32_t k = 0; k < nb; ++k) {
+        for (int32_t r = 0; r < D; ++r) {
+            orc_range mine = {0, 0};
+            rc = orc_rank_range(bstart[k], bend[k], D, r, &mine);
+            if (rc != ORC_OK)
+                goto done;
+            int64_t S = mine.end - mine.start;
+
+            /* Reduce-scatter ([P1] §4.2, §5; R5): rank r keeps the scaled,
+             * rank-ordered fp32 sum of its range over all D replicas. */
+            free(shard);
+            shard = (float *)malloc((size_t)(S > 0 ? S : 1) * sizeof *shard);
+            if (!shard) {
+                rc = ORC_E_NOMEM;
+                goto done;
+            }
+            int64_t j_lo = orc_max(0, w0 - mine.start);
+            int64_t j_hi = orc_min(S, w1 - mine.start);
+            for (int64_t j = j_lo; j < j_hi; ++j) {
+                int64_t i = mine.start + j;
+                float acc = sc.scale * orc_grad(grads, grad_is_f32, 0, i - w0);
+                for (int32_t q = 1; q < D; ++q) {
+                    float x = sc.scale * orc_grad(grads, grad_is_f32, q, i - w0);
+                    acc = acc + x;
+                }
+                shard[j] = acc;
+            }
+
+            /* This rank's pieces are contiguous in the piece list. */
+            int32_t last_piece = first_piece;
+            while (last_piece < npieces && pieces[last_piece].bucket_id == k &&
+                   pieces[last_piece].rank == r)
+                ++last_piece;
+
+            for (int32_t pi = first_piece; pi < last_piece; ++pi) {
+                const orc_piece *pc = &pieces[pi];
+                int32_t p = pc->param_id;
+                int decays = wd_mask ? (wd_mask[p] != 0) : 1;
+                int64_t t_lo = orc_max(0, w0 - pc->gbuf_world.start);
+                int64_t t_hi = orc_min(pc->gbuf_world.end, w1) - pc->gbuf_world.start;
+                for (int64_t t = t_lo; t < t_hi; ++t) {
+                    int64_t i = pc->gbuf_world.start + t;
+                    /* main grad: the shard sliced by gbuf_local ([P1] §4.3) */
+                    float g = shard[pc->gbuf_local.start + t];
+                    /* main param: the param's fp32 copy sliced by the "param"
+                     * range; stored buffer-indexed at the param's offset. */
+                    int64_t mi = pstart[p] + pc->param.start + t;
+                    orc_adamw(&sc, decays, g, &master[mi - w0], &exp_avg[mi - w0],
+                              &exp_avg_sq[mi - w0]);
+                    /* write-back into rank r's bucket view at
+                     * gbuf_world_in_bucket ([P1] §4.3) */
+                    int64_t bi = bstart[k] + pc->gbuf_world_in_bucket.start + t;
+                    params[r][bi - w0] = orc_f32_to_bf16(master[mi - w0]);
+                    if (main_grad_out)
+                        main_grad_out[i - w0] = g;
+                }
+            }
+
+            /* All-gather ([P1] §4.4; R8): rank r's owned elements go from its
+             * replica to every other replica. */
+            if (gather) {
+                for (int32_t pi = first_piece; pi < last_piece; ++pi) {
+                    const orc_piece *pc = &pieces[pi];
+                    int64_t i_lo = orc_max(pc->gbuf_world.start, w0);
+                    int64_t i_hi = orc_min(pc->gbuf_world.end, w1);
+                    for (int64_t i = i_lo; i < i_hi; ++i) {
+                        for (int32_t q = 0; q < D; ++q)
+                            if (q != r)
+                                params[q][i - w0] = params[r][i - w0];
+                    }
+                }
+            }
+            first_piece = last_piece;
+        }
+    }
+
+done:
+    free(shard);
+    free(pieces);
+    free(pstart);
+    free(pend);
+    free(pbucket);
+    free(bstart);
+    free(bend);
+    return rc;
+}
+
+/* Convenience for tests: the layout and pieces in one call.  Sizes of the
+ * outputs as in orc_layout / orc_pieces. */
+int orc_range_map(const int64_t *sizes, int32_t n, int32_t D, int64_t bucket_elems,
+                  int32_t pad_unit, int64_t *param_start, int64_t *param_end,
+                  int32_t *param_bucket, int64_t *bucket_start, int64_t *bucket_end,
+                  int32_t *n_buckets_out, int64_t *numel_out, orc_piece *pieces,
+                  int32_t *n_pieces_out)
+{
+    int rc = orc_layout(sizes, n, D, bucket_elems, pad_unit, param_start, param_end,
+                        param_bucket, bucket_start, bucket_end, n_buckets_out, numel_out);
+    if (rc != ORC_OK)
+        return rc;
+    return orc_pieces(n, param_start, param_end, param_bucket, *n_buckets_out, bucket_start,
+                      bucket_end, D, pieces, n_pieces_out);
+}
+
+/* The per-step scalars, for tests that pin them. */
+void orc_step_scalars(const orc_adam *cfg, int64_t step, float *out9)
+{
+    orc_scalars s = orc_make_scalars(cfg, step);
+    out9[0] = s.b1;
+    out9[1] = s.b2;
+    out9[2] = s.one_minus_b1;
+    out9[3] = s.one_minus_b2;
+    out9[4] = s.decay;
+    out9[5] = s.step_size;
+    out9[6] = s.bc2_sqrt;
+    out9[7] = s.eps;
+    out9[8] = s.scale;
+}

@@ -1,0 +1,93 @@
+"""Plant plausible mistakes in a copy of the oracle and check that the pins
+catch every one of them.  Each mutant is compiled to a temporary library and
+its pins run in a subprocess, so an out-of-range access in a mutant shows up
+as a failure rather than taking down the test run."""
+import os
+import subprocess
+import sys
+import tempfile
+
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+# (name, text in dopt_oracle.c, replacement)
+MUTANTS = [
+    ("no_scale_rank0", "float acc = sc.scale * orc_grad(grads, grad_is_f32, 0, i - w0);",
+     "float acc = orc_grad(grads, grad_is_f32, 0, i - w0);"),
+    ("skip_last_rank", "for (int32_t q = 1; q < D; ++q) {", "for (int32_t q = 1; q < D - 1; ++q) {"),
+    ("update_sign", "ww = ww - delta;", "ww = ww + delta;"),
+    ("no_bias_correction1", "s.step_size = (float)(lr / (1.0 - pow(b1, (double)t)));",
+     "s.step_size = (float)lr;"),
+    ("no_bias_correction2", "s.bc2_sqrt = (float)sqrt(1.0 - pow(b2, (double)t));",
+     "s.bc2_sqrt = 1.0f;"),
+    ("eps_inside_sqrt", "float root = sqrtf(vv);", "float root = sqrtf(vv + s->eps);"),
+    ("m_uses_beta2", "float t1 = s->b1 * mm;", "float t1 = s->b2 * mm;"),
+    ("m_uses_one_minus_beta2", "float t2 = s->one_minus_b1 * g;", "float t2 = s->one_minus_b2 * g;"),
+    ("v_not_squared", "float gg = g * g;", "float gg = g;"),
+    ("no_weight_decay", "ww = ww * s->decay;", "ww = ww;"),
+    ("decay_sign", "s.decay = (float)(1.0 - lr * wd);", "s.decay = (float)(1.0 + lr * wd);"),
+    ("wd_ignores_mask", "int decays = wd_mask ? (wd_mask[p] != 0) : 1;", "int decays = 1;"),
+    ("grad_via_bucket_range", "float g = shard[pc->gbuf_local.start + t];",
+     "float g = shard[pc->gbuf_world_in_bucket.start + t];"),
+    ("master_via_local_range", "int64_t mi = pstart[p] + pc->param.start + t;",
+     "int64_t mi = pstart[p] + pc->gbuf_local.start + t;"),
+    ("writeback_via_local_range", "int64_t bi = bstart[k] + pc->gbuf_world_in_bucket.start + t;",
+     "int64_t bi = bstart[k] + pc->gbuf_local.start + t;"),
+    ("master_drops_piece_offset", "int64_t mi = pstart[p] + pc->param.start + t;",
+     "int64_t mi = pstart[p] + t;"),
+    ("writeback_drops_bucket_base", "int64_t bi = bstart[k] + pc->gbuf_world_in_bucket.start + t;",
+     "int64_t bi = pc->gbuf_world_in_bucket.start + t;"),
+    ("rank_range_shifted", "out->start = b_start + (int64_t)r * S;",
+     "out->start = b_start + (int64_t)r * S + (r > 0);"),
+    ("pad_ignores_D", "int64_t unit = (int64_t)D * (int64_t)pad_unit;", "int64_t unit = (int64_t)pad_unit;"),
+    ("bucket_closes_late", "if (bucket_elems > 0 && open_count >= bucket_elems) {",
+     "if (bucket_elems > 0 && open_count > bucket_elems) {"),
+    ("local_range_from_bucket", "pc.gbuf_local = orc_normalize(pc.gbuf_world, x - mine.start);",
+     "pc.gbuf_local = orc_normalize(pc.gbuf_world, x - bucket_start[k]);"),
+    ("no_gather", "if (gather) {", "if (0) {"),
+    ("bf16_truncates", "if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u)))", "if (0)"),
+    ("bf16_ties_away", "if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u)))",
+     "if (lower >= 0x8000u)"),
+]
+
+RUNNER = r"""
+import sys, traceback
+sys.path.insert(0, {root!r}); sys.path.insert(0, {tests!r})
+import oracle, pins
+lib = oracle.load({path!r})
+failed = []
+for pin in pins.ALL_PINS:
+    try:
+        pin(lib)
+    except BaseException as e:
+        failed.append(pin.__name__)
+print("FAILED_PINS", ",".join(failed))
+sys.exit(1 if failed else 0)
+"""
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(name, old, new, tmp_path):
+    with open(os.path.join(ROOT, "oracle", "dopt_oracle.c")) as f:
+        src = f.read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    mutated = tmp_path / "mutant.c"
+    mutated.write_text(src.replace(old, new))
+    so = tmp_path / "libmutant.so"
+    oracle._compile(str(mutated), str(so))
+    code = RUNNER.format(root=ROOT, tests=os.path.join(ROOT, "tests"), path=str(so))
+    res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True,
+                         timeout=600)
+    assert res.returncode != 0, f"mutant {name} passed every pin:\n{res.stdout}\n{res.stderr}"
+
+
+def test_runner_passes_unmutated_oracle():
+    """Control: the same runner on the unmodified oracle reports no failure."""
+    code = RUNNER.format(root=ROOT, tests=os.path.join(ROOT, "tests"), path=oracle.build())
+    res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True,
+                         timeout=600)
+    assert res.returncode == 0, res.stdout + res.stderr
+    assert "FAILED_PINS \n" in res.stdout or res.stdout.strip() == "FAILED_PINS"
