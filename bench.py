@@ -1,0 +1,411 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused ZeRO-1 distributed-optimizer step on GB300.
+
+One step = one dopt_step launch: reduce-scatter of the D bf16 grad replicas
+(scaled, fp32, rank order), fp32 main grads through the range map, AdamW
+with bias correction on fp32 master/m/v, bf16 write-back and all-gather into
+the D param replicas, over every bucket of the GPT-2-small-shaped flat
+buffer (124,439,808 elements, D=8, 40 Mi buckets padded to multiples of
+D*64).  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (plain C, one thread) on a bounded
+window of the same workload, on the host cores.  With N>1 (torchrun, one
+rank per GPU) every rank runs its own replica of the workload: the step has
+no data exchange between GPUs, so the ranks only meet for the timing
+barrier and the max-over-ranks reduction.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from zero_distributed_optimizer_gb300 import workloads as W  # noqa: E402
+
+METRIC = "fused RS+AdamW+gather elements/s and HBM GB/s (% of ~8 TB/s), 1 GB300"
+UNIT = "elements/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "dopt_step_kernel_gpt2_small.md")
+KERNEL_SOURCES = [os.path.join(ROOT, "zero_distributed_optimizer_gb300", "csrc", f)
+                  for f in ("step.cu", "dopt_internal.h")]
+CPU_SAMPLE_ELEMS = 1 << 21
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Max of a per-rank number over all ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def read_profile_traffic():
+    """dram bytes per launch of the step kernel from the committed ncu
+    summary, or None if there is none or the kernel changed since."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu_index), "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        inside = [p for t, p in self.samples if t0 - 0.15 <= t <= t1 + 0.15]
+        note = "samples during the timed region"
+        if not inside:
+            mid = 0.5 * (t0 + t1)
+            inside = [min(self.samples, key=lambda s: abs(s[0] - mid))[1]]
+            note = "timed region shorter than the sampling period: nearest sample"
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[2]) for p in inside if num(p[2]) is not None]
+        smax = [num(p[3]) for p in inside if num(p[3]) is not None]
+        power = [num(p[4]) for p in inside if num(p[4]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4)
+                          if p[6 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "reasons": reasons, "samples": len(inside), "note": note}
+
+
+def cpu_oracle_rate(w: W.Workload, seconds: float = 12.0, max_steps: int = 40, grads_src=None,
+                    state_src=None, sample=CPU_SAMPLE_ELEMS):
+    """Elements/s of the oracle (as it stands, one host thread) stepping the
+    first `sample` buffer elements of the workload, repeated for about
+    `seconds` seconds."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from dataclasses import asdict
+
+    from zero_distributed_optimizer_gb300.binding import AdamConfig
+
+    oracle.build()
+    adam = oracle.make_adam(**asdict(AdamConfig(**w.adam_kwargs())))
+    if grads_src is None:
+        grads_src = W.make_grads(w, sample, 1, "cpu")
+        state_src = W.make_state(w, sample, "cpu")
+
+    def host(t):
+        t = t[:sample].detach().cpu().contiguous()
+        if t.dtype == torch.bfloat16:
+            return t.view(torch.int16).numpy().view(np.uint16).copy()
+        return t.numpy().copy()
+
+    grads = [host(g) for g in grads_src]
+    master, m, v = (host(x) for x in state_src)
+    params = [np.zeros(sample, np.uint16) for _ in range(w.D)]
+    sizes, wd = list(w.sizes), list(w.wd_mask)
+    steps = 0
+    t0 = time.perf_counter()
+    while steps < max_steps and (time.perf_counter() - t0) < seconds:
+        oracle.step(sizes, wd, w.D, w.bucket_elems, w.pad_unit, adam, steps + 1, grads, master,
+                    m, v, params, window=(0, sample))
+        steps += 1
+    dt = time.perf_counter() - t0
+    return sample * steps / dt, steps, dt
+
+
+def run_reference(args):
+    """The oracle arm: rank 0 alone times the CPU oracle on a bounded window."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = W.gpt2_small()
+    import torch
+
+    grads_src = W.make_grads(w, CPU_SAMPLE_ELEMS, 1, "cpu")
+    state_src = W.make_state(w, CPU_SAMPLE_ELEMS, "cpu")
+    cpu_oracle_rate(w, seconds=1e9, max_steps=max(1, args.warmup), grads_src=grads_src,
+                    state_src=state_src)
+    rate, steps, dt = cpu_oracle_rate(w, seconds=1e9, max_steps=args.steps, grads_src=grads_src,
+                                      state_src=state_src)
+    sample = (f"first {CPU_SAMPLE_ELEMS} elements of the {w.name} buffer (D={w.D}), "
+              f"{steps} oracle steps, one host thread")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": world,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / max(steps, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "N": w.numel, "D": w.D, "bucket_elems": w.bucket_elems,
+                   "pad_unit": w.pad_unit, "grad_dtype": w.grad_dtype,
+                   "sample_elems": CPU_SAMPLE_ELEMS},
+        "cpu_baseline": {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "torch": torch.__version__,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+
+    from zero_distributed_optimizer_gb300 import binding as B
+    from zero_distributed_optimizer_gb300 import build as libbuild
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    device = torch.device("cuda", torch.cuda.current_device())
+    if rank == 0:
+        libbuild.build()
+    if world > 1:
+        torch.distributed.barrier()
+
+    w = W.gpt2_small()
+    L = B.dopt_build_range_map(list(w.sizes), w.D, w.bucket_elems, w.pad_unit,
+                               list(w.wd_mask)).to_device()
+    N = L.padded_numel
+    master, m, v = W.make_state(w, N, device)
+    params = W.make_params(master, w.D)
+    grads = W.make_grads(w, N, 1, device)
+    adam = B.AdamConfig(**w.adam_kwargs())
+    stream = torch.cuda.current_stream()
+
+    def step(t):
+        B.dopt_step(L, adam, t, grads, master, m, v, params, gather=True, stream=stream)
+
+    t = 0
+    for _ in range(max(args.warmup, 3)):
+        t += 1
+        step(t)
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    # let the sampler come up and the clocks settle under the same load
+    settle_end = time.time() + 0.4
+    while time.time() < settle_end:
+        t += 1
+        step(t)
+        torch.cuda.synchronize()
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    h0 = time.time()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        t += 1
+        step(t)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    h1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    sampler.stop()
+    ms_local = ev0.elapsed_time(ev1)
+    ms_total = max_over_ranks(ms_local, world, device)
+    ms_per_step = ms_total / args.steps
+
+    elems = w.numel
+    value = world * elems * args.steps / (ms_total / 1e3)
+    bytes_per_launch = elems * w.algorithmic_bytes_per_element()
+    gbs = bytes_per_launch / (ms_per_step / 1e3) / 1e9
+    peak, peak_kind = measured_hbm_peak()
+    traffic = read_profile_traffic()
+
+    # end to end through the public API: grads from pinned host memory,
+    # updated params (replica 0) back to pinned host memory, every step
+    e2e = None
+    if not args.no_e2e:
+        host_grads = [g.cpu().pin_memory() for g in grads]
+        host_out = torch.empty(N, dtype=torch.bfloat16).pin_memory()
+        dev_stage = [torch.empty_like(g) for g in grads]
+        k_e2e = max(3, min(args.steps, 20))
+        for _ in range(2):
+            t += 1
+            B.step_from_host(L, adam, t, host_grads, dev_stage, master, m, v, params, host_out,
+                             stream=stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(k_e2e):
+            t += 1
+            B.step_from_host(L, adam, t, host_grads, dev_stage, master, m, v, params, host_out,
+                             stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, device)
+        e2e = {"value": world * elems * k_e2e / (e2e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in host_grads),
+               "d2h_bytes_per_step": host_out.numel() * host_out.element_size(),
+               "steps": k_e2e, "ms_per_step": e2e_ms / k_e2e,
+               "path": "binding.step_from_host: pinned H2D of D grad replicas, dopt_step, "
+                       "D2H of param replica 0"}
+        del host_grads, host_out, dev_stage
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, steps_done, dt = cpu_oracle_rate(w, seconds=args.cpu_seconds, grads_src=grads,
+                                               state_src=(master, m, v))
+        cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"first {CPU_SAMPLE_ELEMS} elements of the {w.name} buffer, "
+                         f"{steps_done} oracle steps in {dt:.1f} s, one host thread"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": w.name, "N": elems, "padded_numel": N, "D": w.D,
+                       "bucket_elems": w.bucket_elems, "pad_unit": w.pad_unit,
+                       "n_buckets": L.n_buckets, "grad_dtype": w.grad_dtype,
+                       "state_dtype": "f32", "param_dtype": "bf16",
+                       "bytes_per_element": w.algorithmic_bytes_per_element(),
+                       "l2": "working set %.1f GB > 129 MB L2, no flush" % (
+                           (N * (w.D * w.grad_bytes + 12 + 2 * w.D)) / 1e9),
+                       "parallelism": "replicas" if world > 1 else "single"},
+            "hbm_gbs": gbs, "pct_of_8tbs": gbs / NOMINAL_HBM_GBS,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                         "frac": gbs / peak, "peak_kind": peak_kind,
+                         "traffic": traffic,
+                         "algorithmic_bytes_per_launch": bytes_per_launch},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": args.steps,
+            "clocks": sampler.summary(h0, h1),
+            "torch": torch.__version__,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,228 @@
+/*
+ * dopt: the ZeRO-1 distributed-optimizer step over a contiguous flat
+ * gradient/parameter buffer, on one GPU, with D data-parallel ranks held as
+ * D replica buffers in device memory.
+ *
+ * The operations follow the Megatron-LM distributed-optimizer page
+ * ("04 · 分布式优化器"):
+ *   - the flat buffer cut into buckets, each bucket split into D equal
+ *     contiguous ranges, rank r owning range r (§2, §3);
+ *   - Range and the four ranges of every (param, rank) piece (§4.1);
+ *   - the bucket-wise reduce-scatter of the grads, scaled first (§4.2, §5);
+ *   - the shard going to fp32 main grads, Adam on the shard, the write-back
+ *     of the updated shard into the param buffer (§4.3);
+ *   - the all-gather of the params (§4.4).
+ *
+ * Conventions
+ *   - Every call returns DOPT_OK (0) or a negative DOPT_E_* code; the text
+ *     of the last error on the calling thread is dopt_last_error().
+ *   - Device buffers belong to the caller.  The library owns a dopt_layout
+ *     and its device tables and frees both in dopt_layout_free.
+ *   - dopt_step and dopt_gather are asynchronous on `stream` (a
+ *     cudaStream_t; NULL is the legacy default stream).  They check their
+ *     arguments on the host before anything is queued, report launch errors
+ *     through cudaGetLastError, and never allocate or synchronise.  Faults
+ *     inside a kernel surface at the caller's next synchronisation.
+ *   - Buffer-indexed arrays hold one element per position of the padded
+ *     buffer (padded_numel elements).  Padding positions belong to no param;
+ *     the step neither reads nor writes them in any buffer.
+ */
+#ifndef DOPT_H
+#define DOPT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define DOPT_OK 0
+#define DOPT_E_ARG (-1)    /* invalid argument (null, out of range) */
+#define DOPT_E_LAYOUT (-2) /* a bucket does not divide by D (page 1, §4.1 and §5) */
+#define DOPT_E_ALIGN (-3)  /* a device pointer is not 16-byte aligned */
+#define DOPT_E_CUDA (-4)   /* a CUDA runtime call failed */
+#define DOPT_E_STATE (-5)  /* the layout has no device tables on this device */
+#define DOPT_E_NOMEM (-6)  /* host allocation failed */
+
+/* Largest number of simulated data-parallel ranks. */
+#define DOPT_MAX_D 64
+
+/* Range(start, end): the half-open interval [start, end) (page 1, §4.1). */
+typedef struct {
+    int64_t start;
+    int64_t end;
+} dopt_range;
+
+/*
+ * One (param, rank) piece: the part of a param that falls in one rank's
+ * range of its bucket, with the four ranges of page 1, §4.1:
+ *   gbuf_world            the piece's range in the whole flat buffer
+ *   gbuf_world_in_bucket  the same, relative to the start of its bucket
+ *   gbuf_local            the same, relative to the start of the rank's range
+ *   param                 the same, relative to the start of the param
+ * All four have the same length; they differ by a translation.
+ */
+typedef struct {
+    dopt_range gbuf_world;
+    dopt_range gbuf_world_in_bucket;
+    dopt_range gbuf_local;
+    dopt_range param;
+    int32_t param_id;
+    int32_t bucket_id;
+    int32_t rank;
+    int32_t reserved;
+} dopt_piece;
+
+/*
+ * Layout parameters.
+ *   D             simulated data-parallel ranks, 1..DOPT_MAX_D
+ *   pad_unit      every bucket is padded at its end to a multiple of
+ *                 D * pad_unit elements (>= 1)
+ *   bucket_elems  a bucket is closed as soon as its unpadded element count
+ *                 reaches bucket_elems; 0 puts all params in one bucket
+ */
+typedef struct {
+    int32_t D;
+    int32_t pad_unit;
+    int64_t bucket_elems;
+} dopt_layout_cfg;
+
+/*
+ * AdamW hyper-parameters.  grad_scale is the gradient scaling factor applied
+ * to every replica's grads before the reduction (page 1, §5).
+ * Valid ranges: lr >= 0, 0 <= beta1 < 1, 0 <= beta2 < 1, eps >= 0,
+ * weight_decay >= 0, grad_scale finite.
+ */
+typedef struct {
+    float lr;
+    float beta1;
+    float beta2;
+    float eps;
+    float weight_decay;
+    float grad_scale;
+} dopt_adam_cfg;
+
+/* Gradient element type of the replica buffers. */
+typedef enum { DOPT_BF16 = 0, DOPT_FP32 = 1 } dopt_dtype;
+
+/* dopt_step flags. */
+#define DOPT_STEP_GATHER 1u /* fuse the all-gather: write all D replicas */
+
+typedef struct dopt_layout dopt_layout;
+
+/*
+ * Build the flat-buffer layout and its four-way range map (page 1, §2, §3,
+ * §4.1, §5).
+ *
+ *   param_sizes[n_params]  element count of each param (>= 0), in buffer
+ *                          order; params sit at consecutive offsets.
+ *   wd_mask[n_params]      nullable; nonzero where the param takes weight
+ *                          decay (NULL: every param does).
+ *   cfg                    D, pad_unit, bucket_elems (see dopt_layout_cfg).
+ *   out                    receives a new layout; free it with
+ *                          dopt_layout_free.
+ *
+ * Buckets are greedy: params are appended to the open bucket, which closes
+ * as soon as its unpadded count reaches bucket_elems; a param never spans
+ * two buckets; each bucket is padded to a multiple of D * pad_unit, and rank
+ * r owns [start + r*S, start + (r+1)*S) of it with S = size / D.
+ * Host only: makes no CUDA call.  Errors: DOPT_E_ARG, DOPT_E_NOMEM.
+ */
+int dopt_build_range_map(const int64_t *param_sizes, int32_t n_params, const uint8_t *wd_mask,
+                         const dopt_layout_cfg *cfg, dopt_layout **out);
+
+/* Sizes of a layout: padded buffer length, bucket and piece counts.  Any
+ * output pointer may be NULL.  Host only. */
+int dopt_layout_query(const dopt_layout *layout, int64_t *padded_numel, int32_t *n_buckets,
+                      int32_t *n_pieces);
+
+/* Copy the n_buckets bucket ranges (padded, in buffer order). Host only. */
+int dopt_layout_buckets(const dopt_layout *layout, dopt_range *buckets);
+
+/* Copy the n_pieces pieces, sorted by (bucket, rank, gbuf_world.start).
+ * Host only. */
+int dopt_layout_pieces(const dopt_layout *layout, dopt_piece *pieces);
+
+/* Copy each param's full range in the buffer ([n_params]). Host only. */
+int dopt_layout_param_ranges(const dopt_layout *layout, dopt_range *params);
+
+/*
+ * Copy the layout's kernel tables (owned runs of the buffer and a per-tile
+ * index into them) to the current CUDA device.  Allocates device memory
+ * once; must precede dopt_step / dopt_gather on that device and any stream
+ * capture.  Calling it again on the same device is a no-op; on another
+ * device it moves the tables there.  Synchronous.  Errors: DOPT_E_ARG,
+ * DOPT_E_CUDA.
+ */
+int dopt_layout_to_device(dopt_layout *layout);
+
+/* Free a layout and its device tables.  NULL is ignored. */
+void dopt_layout_free(dopt_layout *layout);
+
+/*
+ * One distributed-optimizer step for all D simulated ranks, fused into one
+ * kernel launch over the whole buffer (page 1, §4.2-§4.4):
+ *
+ *   for every owned element i (rank q owns it, param p holds it):
+ *     g      = fp32 sum over r = 0..D-1, in rank order, of
+ *              grad_scale * float(grad_replicas[r][i])   (each op rounded)
+ *     m      = beta1*m + (1-beta1)*g
+ *     v      = beta2*v + (1-beta2)*(g*g)
+ *     w      = w * (1 - lr*weight_decay)          (only if p decays)
+ *     w      = w - step_size * (m / (sqrt(v)/bc2_sqrt + eps))
+ *     param_replicas[r][i] = bf16_rne(w)   for every r (DOPT_STEP_GATHER)
+ *                                          or for r = q only (no flag)
+ *     main_grad_out[i] = g                 (when main_grad_out is not NULL)
+ *   with step_size = lr / (1 - beta1^step), bc2_sqrt = sqrt(1 - beta2^step)
+ *   and the scalars (1-beta1), (1-beta2), (1-lr*wd), step_size, bc2_sqrt
+ *   evaluated in double on the host and rounded to float once.  Every fp32
+ *   multiply, add, divide and square root is rounded on its own (no fused
+ *   multiply-add).
+ *
+ *   layout          built by dopt_build_range_map, tables on this device
+ *   cfg             AdamW hyper-parameters (host pointer)
+ *   step            1-based step count t
+ *   grad_replicas   host array of D device pointers, each padded_numel
+ *                   elements of grad_dtype; read only
+ *   master, exp_avg, exp_avg_sq
+ *                   device fp32, padded_numel elements each, buffer-indexed
+ *                   (the union of all D ranks' shards); updated in place
+ *   param_replicas  host array of D device pointers, bf16, padded_numel each
+ *   flags           0 or DOPT_STEP_GATHER
+ *   main_grad_out   nullable device fp32[padded_numel]: the reduce-scattered
+ *                   fp32 main grad of every owned element
+ *   stream          CUDA stream to launch on
+ *
+ * Every device pointer must be 16-byte aligned (DOPT_E_ALIGN otherwise).
+ * The D grad replicas must not overlap any output.  Errors: DOPT_E_ARG,
+ * DOPT_E_ALIGN, DOPT_E_STATE, DOPT_E_CUDA.
+ */
+int dopt_step(const dopt_layout *layout, const dopt_adam_cfg *cfg, int64_t step,
+              const void *const *grad_replicas, dopt_dtype grad_dtype, float *master,
+              float *exp_avg, float *exp_avg_sq, void *const *param_replicas, uint32_t flags,
+              float *main_grad_out, cudaStream_t stream);
+
+/*
+ * The all-gather of the params on its own (page 1, §4.4): for every rank q
+ * and every element q owns, copy param_replicas[q][i] into every other
+ * replica.  Padding is not copied.  param_replicas: host array of D device
+ * bf16 pointers (16-byte aligned).  Asynchronous on `stream`.
+ * Errors: DOPT_E_ARG, DOPT_E_ALIGN, DOPT_E_STATE, DOPT_E_CUDA.
+ */
+int dopt_gather(const dopt_layout *layout, void *const *param_replicas, cudaStream_t stream);
+
+/* Text of the last error raised on the calling thread ("" if none). */
+const char *dopt_last_error(void);
+
+/* Library version string. */
+const char *dopt_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DOPT_H */

@@ -190,15 +190,16 @@ int orc_pieces(int32_t n, const int64_t *param_start, const int64_t *param_end,
                int32_t *n_pieces_out)
 {
     int32_t np = 0;
+    int32_t first = 0; /* the params of bucket k are consecutive from here */
     for (int32_t k = 0; k < nb; ++k) {
+        while (first < n && param_bucket[first] < k)
+            ++first;
         for (int32_t r = 0; r < D; ++r) {
             orc_range mine;
             int rc = orc_rank_range(bucket_start[k], bucket_end[k], D, r, &mine);
             if (rc != ORC_OK)
                 return rc;
-            for (int32_t p = 0; p < n; ++p) {
-                if (param_bucket[p] != k)
-                    continue;
+            for (int32_t p = first; p < n && param_bucket[p] == k; ++p) {
                 int64_t x = orc_max(param_start[p], mine.start);
                 int64_t y = orc_min(param_end[p], mine.end);
                 if (x >= y)

@@ -1,0 +1,169 @@
+"""Host-side checks of libdopt.so that need no GPU: the library loads and
+exports every function include/*.h declares; the range map it builds is
+bit-exact with the oracle's; invalid arguments are refused before any CUDA
+call is made."""
+import ctypes
+import glob
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import pins
+from zero_distributed_optimizer_gb300 import binding as B
+from zero_distributed_optimizer_gb300 import build as libbuild
+from zero_distributed_optimizer_gb300 import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return B.lib()
+
+
+def declared_functions():
+    names = set()
+    for path in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(path).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w\s\*]*?\b(dopt_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("dopt_build_range_map", "dopt_step", "dopt_gather", "dopt_layout_free",
+                     "dopt_last_error"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(B.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(raw, n)]
+    assert not missing, missing
+    assert "sm_103a" in B.version()
+
+
+def _lib_layout(sizes, D, bucket, pad, wd=None):
+    return B.dopt_build_range_map(sizes, D, bucket_elems=bucket, pad_unit=pad, wd_mask=wd)
+
+
+def _compare_with_oracle(sizes, D, bucket, pad):
+    L = _lib_layout(sizes, D, bucket, pad)
+    O = oracle.range_map(sizes, D, bucket, pad)
+    assert L.padded_numel == O.numel
+    assert L.buckets() == list(zip(O.bucket_start.tolist(), O.bucket_end.tolist()))
+    assert L.param_ranges() == list(zip(O.param_start.tolist(), O.param_end.tolist()))
+    assert L.pieces() == O.pieces
+    return L
+
+
+def test_range_map_matches_oracle_tiny(lib):
+    for sizes, D, bucket, pad in pins.random_tiny_layouts(400, seed=99):
+        _compare_with_oracle(sizes, D, bucket, pad)
+
+
+def test_range_map_page1_example(lib):
+    L = _compare_with_oracle([130, 260, 90, 310, 210], 4, 0, 1)
+    assert [pc for pc in L.pieces() if pc["rank"] == 1][0]["gbuf_world"] == (250, 390)
+
+
+@pytest.mark.parametrize("w", W.all_configs(), ids=lambda w: w.name)
+def test_range_map_matches_oracle_configs(lib, w):
+    _compare_with_oracle(list(w.sizes), w.D, w.bucket_elems, w.pad_unit)
+
+
+def test_range_map_matches_oracle_sweep(lib):
+    for D in W.SWEEP_D:
+        for b in W.SWEEP_BUCKET_MI:
+            w = W.sweep_256m(D, b)
+            _compare_with_oracle(list(w.sizes), w.D, w.bucket_elems, w.pad_unit)
+
+
+def test_range_map_larger_random(lib):
+    rng = np.random.default_rng(5)
+    for _ in range(30):
+        n = int(rng.integers(1, 300))
+        sizes = [int(x) for x in rng.integers(0, 5000, n)]
+        D = int(rng.integers(1, 65))
+        bucket = int(rng.choice([0, int(rng.integers(1, 50000))]))
+        pad = int(rng.integers(1, 130))
+        _compare_with_oracle(sizes, D, bucket, pad)
+
+
+def test_layout_errors(lib):
+    for sizes, D, bucket, pad in (([4], 0, 0, 1), ([4], 65, 0, 1), ([4, -1], 2, 0, 1),
+                                  ([4], 2, 0, 0), ([4], 2, -1, 1)):
+        with pytest.raises(B.DoptError) as e:
+            _lib_layout(sizes, D, bucket, pad)
+        assert e.value.code == B.DOPT_E_ARG
+        assert B.lib().dopt_last_error().decode().startswith("dopt_build_range_map")
+    out = ctypes.c_void_p()
+    assert B.lib().dopt_build_range_map(None, 3, None, None, ctypes.byref(out)) == B.DOPT_E_ARG
+    assert B.lib().dopt_build_range_map(None, 0, None, None, None) == B.DOPT_E_ARG
+
+
+def test_empty_layouts(lib):
+    L = _lib_layout([], 4, 0, 1)
+    assert L.padded_numel == 0 and L.n_buckets == 0 and L.n_pieces == 0
+    L = _lib_layout([0, 0], 3, 0, 2)
+    assert L.padded_numel == 0 and L.n_buckets == 1 and L.n_pieces == 0
+
+
+def _raw_step(L, ptr_grads, ptr_state, ptr_params, step=1, flags=1, dtype=B.DOPT_BF16, cfg=None,
+              main_grad=None):
+    D = L.D
+    cfg = cfg or B.AdamConfig().to_c()
+    gp = (ctypes.c_void_p * D)(*ptr_grads)
+    pp = (ctypes.c_void_p * D)(*ptr_params)
+    return B.lib().dopt_step(L.handle, ctypes.byref(cfg), step, gp, dtype, ptr_state[0],
+                             ptr_state[1], ptr_state[2], pp, flags, main_grad, None)
+
+
+def test_step_argument_checks_before_cuda(lib):
+    """Refusals that come before the library touches CUDA (no GPU needed):
+    the fake pointers below are never dereferenced."""
+    L = _lib_layout([100, 30], 2, 0, 8)
+    good = [0x10000, 0x20000]
+    state = [0x30000, 0x40000, 0x50000]
+    assert _raw_step(L, good, state, good, step=0) == B.DOPT_E_ARG
+    assert _raw_step(L, good, state, good, flags=4) == B.DOPT_E_ARG
+    assert _raw_step(L, good, state, good, dtype=7) == B.DOPT_E_ARG
+    assert _raw_step(L, [0x10000, 0], state, good) == B.DOPT_E_ARG
+    assert _raw_step(L, [0x10000, 0x20002], state, good) == B.DOPT_E_ALIGN
+    assert _raw_step(L, good, [0x30000, 0x40008, 0x50000], good) == B.DOPT_E_ALIGN
+    assert _raw_step(L, good, state, good, main_grad=0x60004) == B.DOPT_E_ALIGN
+    bad_cfg = B.AdamConfig(beta1=1.0).to_c()
+    assert _raw_step(L, good, state, good, cfg=bad_cfg) == B.DOPT_E_ARG
+    bad_cfg = B.AdamConfig(lr=float("nan")).to_c()
+    assert _raw_step(L, good, state, good, cfg=bad_cfg) == B.DOPT_E_ARG
+    assert B.lib().dopt_step(None, None, 1, None, 0, None, None, None, None, 1, None, None) == B.DOPT_E_ARG
+    # an empty layout is a no-op that never needs the device
+    E = _lib_layout([], 2, 0, 1)
+    assert _raw_step(E, good, state, good) == B.DOPT_OK
+    # with valid arguments the next check needs the device tables
+    rc = _raw_step(L, good, state, good)
+    assert rc in (B.DOPT_E_STATE, B.DOPT_E_CUDA)
+    assert B.lib().dopt_last_error().decode()
+
+
+def test_gather_argument_checks_before_cuda(lib):
+    L = _lib_layout([100, 30], 2, 0, 8)
+    pp = (ctypes.c_void_p * 2)(0x10000, 0x20001)
+    assert B.lib().dopt_gather(L.handle, pp, None) == B.DOPT_E_ALIGN
+    pp = (ctypes.c_void_p * 2)(0x10000, 0)
+    assert B.lib().dopt_gather(L.handle, pp, None) == B.DOPT_E_ARG
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+
+    L = _lib_layout([16], 1, 0, 1)
+    t = torch.zeros(16)
+    with pytest.raises(B.DoptError):
+        B.dopt_step(L, B.AdamConfig(), 1, [t.bfloat16()], t, t.clone(), t.clone(), [t.bfloat16()])

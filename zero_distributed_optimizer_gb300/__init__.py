@@ -1,0 +1,27 @@
+"""GB300-native ZeRO-1 distributed-optimizer step (Megatron-style, flat buffer).
+
+The work runs in libdopt.so (hand-written sm_103a CUDA kernels behind the C
+ABI declared in include/dopt.h); this package is its thin Python binding.
+The library is loaded on first use and every call raises if it is missing.
+"""
+from .binding import (  # noqa: F401
+    DOPT_BF16,
+    DOPT_E_ALIGN,
+    DOPT_E_ARG,
+    DOPT_E_CUDA,
+    DOPT_E_LAYOUT,
+    DOPT_E_NOMEM,
+    DOPT_E_STATE,
+    DOPT_FP32,
+    DOPT_MAX_D,
+    DOPT_OK,
+    DOPT_STEP_GATHER,
+    AdamConfig,
+    DoptError,
+    Layout,
+    dopt_build_range_map,
+    dopt_gather,
+    dopt_step,
+    step_from_host,
+    version,
+)

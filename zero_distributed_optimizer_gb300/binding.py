@@ -1,0 +1,316 @@
+"""Python binding of the dopt C ABI (include/dopt.h): argument marshalling only.
+
+Every function here checks what the C ABI cannot (tensor device, dtype,
+length, contiguity) and passes raw pointers and sizes to libdopt.so; all of
+the step's work runs in the library's CUDA kernels.  There is no fallback:
+if libdopt.so is missing or fails to load, every call raises.
+
+Names follow the C entry points: ``dopt_build_range_map``, ``dopt_step``,
+``dopt_gather``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libdopt.so")
+
+DOPT_OK = 0
+DOPT_E_ARG = -1
+DOPT_E_LAYOUT = -2
+DOPT_E_ALIGN = -3
+DOPT_E_CUDA = -4
+DOPT_E_STATE = -5
+DOPT_E_NOMEM = -6
+DOPT_MAX_D = 64
+DOPT_BF16 = 0
+DOPT_FP32 = 1
+DOPT_STEP_GATHER = 1
+
+_ERROR_NAMES = {DOPT_E_ARG: "DOPT_E_ARG", DOPT_E_LAYOUT: "DOPT_E_LAYOUT",
+                DOPT_E_ALIGN: "DOPT_E_ALIGN", DOPT_E_CUDA: "DOPT_E_CUDA",
+                DOPT_E_STATE: "DOPT_E_STATE", DOPT_E_NOMEM: "DOPT_E_NOMEM"}
+
+
+class DoptError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"{_ERROR_NAMES.get(code, code)}: {message}")
+        self.code = code
+
+
+class dopt_range(ctypes.Structure):
+    _fields_ = [("start", ctypes.c_int64), ("end", ctypes.c_int64)]
+
+
+class dopt_piece(ctypes.Structure):
+    _fields_ = [("gbuf_world", dopt_range), ("gbuf_world_in_bucket", dopt_range),
+                ("gbuf_local", dopt_range), ("param", dopt_range), ("param_id", ctypes.c_int32),
+                ("bucket_id", ctypes.c_int32), ("rank", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+class dopt_layout_cfg(ctypes.Structure):
+    _fields_ = [("D", ctypes.c_int32), ("pad_unit", ctypes.c_int32),
+                ("bucket_elems", ctypes.c_int64)]
+
+
+class dopt_adam_cfg(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
+                ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float),
+                ("grad_scale", ctypes.c_float)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def _declare(lib):
+    P = ctypes.POINTER
+    vp = ctypes.c_void_p
+    lib.dopt_build_range_map.restype = ctypes.c_int
+    lib.dopt_build_range_map.argtypes = [P(ctypes.c_int64), ctypes.c_int32, P(ctypes.c_uint8),
+                                         P(dopt_layout_cfg), P(vp)]
+    lib.dopt_layout_query.restype = ctypes.c_int
+    lib.dopt_layout_query.argtypes = [vp, P(ctypes.c_int64), P(ctypes.c_int32), P(ctypes.c_int32)]
+    lib.dopt_layout_buckets.restype = ctypes.c_int
+    lib.dopt_layout_buckets.argtypes = [vp, P(dopt_range)]
+    lib.dopt_layout_pieces.restype = ctypes.c_int
+    lib.dopt_layout_pieces.argtypes = [vp, P(dopt_piece)]
+    lib.dopt_layout_param_ranges.restype = ctypes.c_int
+    lib.dopt_layout_param_ranges.argtypes = [vp, P(dopt_range)]
+    lib.dopt_layout_to_device.restype = ctypes.c_int
+    lib.dopt_layout_to_device.argtypes = [vp]
+    lib.dopt_layout_free.restype = None
+    lib.dopt_layout_free.argtypes = [vp]
+    lib.dopt_step.restype = ctypes.c_int
+    lib.dopt_step.argtypes = [vp, P(dopt_adam_cfg), ctypes.c_int64, P(vp), ctypes.c_int, vp, vp,
+                              vp, P(vp), ctypes.c_uint32, vp, vp]
+    lib.dopt_gather.restype = ctypes.c_int
+    lib.dopt_gather.argtypes = [vp, P(vp), vp]
+    lib.dopt_last_error.restype = ctypes.c_char_p
+    lib.dopt_last_error.argtypes = []
+    lib.dopt_version.restype = ctypes.c_char_p
+    lib.dopt_version.argtypes = []
+
+
+def lib():
+    """The loaded libdopt.so.  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(
+                    f"{LIB_PATH} is missing: build it with "
+                    "`python -m zero_distributed_optimizer_gb300.build` (no fallback exists)")
+            handle = ctypes.CDLL(LIB_PATH)
+            _declare(handle)
+            _lib = handle
+        return _lib
+
+
+def _check(rc: int):
+    if rc != DOPT_OK:
+        raise DoptError(rc, lib().dopt_last_error().decode(errors="replace"))
+
+
+@dataclass(frozen=True)
+class AdamConfig:
+    lr: float = 1e-3
+    beta1: float = 0.9
+    beta2: float = 0.95
+    eps: float = 1e-8
+    weight_decay: float = 0.1
+    grad_scale: float = 1.0
+
+    def to_c(self) -> dopt_adam_cfg:
+        return dopt_adam_cfg(self.lr, self.beta1, self.beta2, self.eps, self.weight_decay,
+                             self.grad_scale)
+
+
+class Layout:
+    """Owner of a dopt_layout handle (freed with the object)."""
+
+    def __init__(self, handle: int, D: int, n_params: int):
+        self._h = ctypes.c_void_p(handle)
+        self.D = D
+        self.n_params = n_params
+        numel = ctypes.c_int64()
+        nb = ctypes.c_int32()
+        npc = ctypes.c_int32()
+        _check(lib().dopt_layout_query(self._h, ctypes.byref(numel), ctypes.byref(nb),
+                                       ctypes.byref(npc)))
+        self.padded_numel = int(numel.value)
+        self.n_buckets = int(nb.value)
+        self.n_pieces = int(npc.value)
+        self._device = None
+
+    @property
+    def handle(self) -> ctypes.c_void_p:
+        if not self._h:
+            raise DoptError(DOPT_E_ARG, "layout already freed")
+        return self._h
+
+    def buckets(self) -> list:
+        arr = (dopt_range * max(self.n_buckets, 1))()
+        _check(lib().dopt_layout_buckets(self.handle, arr))
+        return [(arr[i].start, arr[i].end) for i in range(self.n_buckets)]
+
+    def param_ranges(self) -> list:
+        arr = (dopt_range * max(self.n_params, 1))()
+        _check(lib().dopt_layout_param_ranges(self.handle, arr))
+        return [(arr[i].start, arr[i].end) for i in range(self.n_params)]
+
+    def pieces(self) -> list:
+        arr = (dopt_piece * max(self.n_pieces, 1))()
+        _check(lib().dopt_layout_pieces(self.handle, arr))
+        out = []
+        for i in range(self.n_pieces):
+            pc = arr[i]
+            out.append({
+                "gbuf_world": (pc.gbuf_world.start, pc.gbuf_world.end),
+                "gbuf_world_in_bucket": (pc.gbuf_world_in_bucket.start, pc.gbuf_world_in_bucket.end),
+                "gbuf_local": (pc.gbuf_local.start, pc.gbuf_local.end),
+                "param": (pc.param.start, pc.param.end),
+                "param_id": pc.param_id, "bucket_id": pc.bucket_id, "rank": pc.rank,
+            })
+        return out
+
+    def to_device(self, device=None) -> "Layout":
+        """Copy the kernel tables to `device` (default: the current device)."""
+        import torch
+
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+        with torch.cuda.device(dev):
+            _check(lib().dopt_layout_to_device(self.handle))
+        self._device = dev
+        return self
+
+    def free(self):
+        if self._h:
+            lib().dopt_layout_free(self._h)
+            self._h = ctypes.c_void_p(None)
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+
+def dopt_build_range_map(param_sizes, D: int, bucket_elems: int = 0, pad_unit: int = 1,
+                         wd_mask=None) -> Layout:
+    """Flat-buffer layout and four-way range map (host only, no CUDA call)."""
+    n = len(param_sizes)
+    sizes = (ctypes.c_int64 * max(n, 1))(*[int(s) for s in param_sizes])
+    wd = None
+    if wd_mask is not None:
+        if len(wd_mask) != n:
+            raise DoptError(DOPT_E_ARG, "wd_mask length differs from param_sizes")
+        wd = (ctypes.c_uint8 * max(n, 1))(*[1 if x else 0 for x in wd_mask])
+    cfg = dopt_layout_cfg(int(D), int(pad_unit), int(bucket_elems))
+    out = ctypes.c_void_p()
+    _check(lib().dopt_build_range_map(sizes, n, wd, ctypes.byref(cfg), ctypes.byref(out)))
+    return Layout(out.value, int(D), n)
+
+
+def _stream_handle(stream):
+    import torch
+
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check_tensor(t, name, dtype, numel, device):
+    if t.device != device:
+        raise DoptError(DOPT_E_ARG, f"{name} is on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise DoptError(DOPT_E_ARG, f"{name} has dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous() or t.numel() < numel:
+        raise DoptError(DOPT_E_ARG, f"{name} must be contiguous with >= {numel} elements")
+
+
+def dopt_step(layout: Layout, adam: AdamConfig, step: int, grad_replicas, master, exp_avg,
+              exp_avg_sq, param_replicas, gather: bool = True, main_grad_out=None,
+              stream=None) -> None:
+    """One fused ZeRO-1 step (reduce-scatter, AdamW, write-back, all-gather).
+
+    grad_replicas: D bf16 or fp32 CUDA tensors; master/exp_avg/exp_avg_sq:
+    fp32; param_replicas: D bf16; main_grad_out: optional fp32.  Each holds
+    at least layout.padded_numel elements.  Asynchronous on `stream`
+    (default: torch's current stream).
+    """
+    import torch
+
+    D = layout.D
+    if len(grad_replicas) != D or len(param_replicas) != D:
+        raise DoptError(DOPT_E_ARG, f"need {D} grad and {D} param replicas")
+    N = layout.padded_numel
+    device = master.device
+    if device.type != "cuda":
+        raise DoptError(DOPT_E_ARG, "dopt_step needs CUDA tensors (no CPU path exists)")
+    gdt = grad_replicas[0].dtype
+    if gdt not in (torch.bfloat16, torch.float32):
+        raise DoptError(DOPT_E_ARG, f"grad dtype {gdt} is not bf16 or fp32")
+    for i, g in enumerate(grad_replicas):
+        _check_tensor(g, f"grad_replicas[{i}]", gdt, N, device)
+    for name, t in (("master", master), ("exp_avg", exp_avg), ("exp_avg_sq", exp_avg_sq)):
+        _check_tensor(t, name, torch.float32, N, device)
+    for i, p in enumerate(param_replicas):
+        _check_tensor(p, f"param_replicas[{i}]", torch.bfloat16, N, device)
+    if main_grad_out is not None:
+        _check_tensor(main_grad_out, "main_grad_out", torch.float32, N, device)
+    gp = (ctypes.c_void_p * D)(*[g.data_ptr() for g in grad_replicas])
+    pp = (ctypes.c_void_p * D)(*[p.data_ptr() for p in param_replicas])
+    cfg = adam.to_c()
+    with torch.cuda.device(device):
+        _check(lib().dopt_step(
+            layout.handle, ctypes.byref(cfg), int(step), gp,
+            DOPT_BF16 if gdt == torch.bfloat16 else DOPT_FP32, master.data_ptr(),
+            exp_avg.data_ptr(), exp_avg_sq.data_ptr(), pp, DOPT_STEP_GATHER if gather else 0,
+            None if main_grad_out is None else main_grad_out.data_ptr(), _stream_handle(stream)))
+
+
+def dopt_gather(layout: Layout, param_replicas, stream=None) -> None:
+    """The all-gather alone: every rank's owned elements into every replica."""
+    import torch
+
+    D = layout.D
+    if len(param_replicas) != D:
+        raise DoptError(DOPT_E_ARG, f"need {D} param replicas")
+    device = param_replicas[0].device
+    if device.type != "cuda":
+        raise DoptError(DOPT_E_ARG, "dopt_gather needs CUDA tensors")
+    for i, p in enumerate(param_replicas):
+        _check_tensor(p, f"param_replicas[{i}]", torch.bfloat16, layout.padded_numel, device)
+    pp = (ctypes.c_void_p * D)(*[p.data_ptr() for p in param_replicas])
+    with torch.cuda.device(device):
+        _check(lib().dopt_gather(layout.handle, pp, _stream_handle(stream)))
+
+
+def version() -> str:
+    return lib().dopt_version().decode()
+
+
+def step_from_host(layout: Layout, adam: AdamConfig, step: int, host_grads, dev_grads, master,
+                   exp_avg, exp_avg_sq, param_replicas, host_params_out=None, stream=None) -> None:
+    """The step for a caller whose grads sit in (pinned) host memory: copy the
+    D host grad replicas into the device buffers `dev_grads`, run dopt_step
+    with the all-gather, and copy replica 0 of the updated params back into
+    `host_params_out` (if given).  Everything is queued on `stream`; the
+    caller synchronises before reading `host_params_out`."""
+    import torch
+
+    s = torch.cuda.current_stream() if stream is None else stream
+    with torch.cuda.stream(s):
+        for h, d in zip(host_grads, dev_grads):
+            d.copy_(h, non_blocking=True)
+        dopt_step(layout, adam, step, dev_grads, master, exp_avg, exp_avg_sq, param_replicas,
+                  gather=True, stream=s)
+        if host_params_out is not None:
+            host_params_out.copy_(param_replicas[0], non_blocking=True)

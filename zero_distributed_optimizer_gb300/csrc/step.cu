@@ -1,0 +1,473 @@
+// Fused ZeRO-1 distributed-optimizer step for sm_103a, and the standalone
+// all-gather (Megatron-LM distributed-optimizer page, §4.2-§4.4).
+//
+// Work split.  With all D ranks held on one device, every owned element i
+// is independent: rank q's reduce-scatter reads the D replicas at i, its
+// Adam reads and writes the fp32 master/m/v at i (the four-way range map
+// composes to the identity on the buffer index, because main params are
+// stored buffer-indexed), and the write-back plus all-gather writes the D
+// param replicas at i.  So one launch covers the whole buffer, all buckets
+// and all ranks, in tiles of 2048 elements (256 threads x 8 elements).
+//
+// Per element the only facts needed are "owned or padding", "decays or
+// not" and the owner rank.  They come from the run table (maximal owned
+// stretches with one rank and one decay flag).  Each CTA gets the first run
+// of its tile from a host-built index; each warp then finds the first run
+// of its own 256 elements with one ballot over 32 run ends, and each thread
+// walks forward to its 8 elements.  An 8-element vector that lies inside one
+// run goes through 128-bit loads and stores; a vector that straddles a run
+// edge (param with another decay flag, a rank edge, padding) is done element
+// by element and never touches padding.
+//
+// Arithmetic.  Every fp32 operation uses the round-to-nearest intrinsics
+// (__fmul_rn, __fadd_rn, __fsub_rn, __fdiv_rn, __fsqrt_rn), so no multiply
+// and add are fused and divide and square root are IEEE; the rank order of
+// the reduction is the loop order.
+#include <cmath>
+#include <cstdint>
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "dopt_internal.h"
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kVec = 8;
+static_assert(kThreads * kVec == kDoptTileElems, "tile size must match the host table");
+
+struct Scalars {
+    float b1, b2, omb1, omb2, decay, step_size, bc2_sqrt, eps, scale;
+};
+
+struct StepArgs {
+    const void *grads[DOPT_MAX_D];
+    void *params[DOPT_MAX_D];
+    float *master;
+    float *exp_avg;
+    float *exp_avg_sq;
+    float *main_grad_out;
+    const int64_t *run_start;
+    const int64_t *run_end;
+    const int32_t *run_meta;
+    const int32_t *tile_run;
+    int64_t numel;
+    int32_t n_runs;
+    int32_t D;
+    int32_t gather;
+    Scalars sc;
+};
+
+struct GatherArgs {
+    void *params[DOPT_MAX_D];
+    const int64_t *run_start;
+    const int64_t *run_end;
+    const int32_t *run_meta;
+    const int32_t *tile_run;
+    int64_t numel;
+    int32_t n_runs;
+    int32_t D;
+};
+
+// ---------------------------------------------------------------------------
+// Small device helpers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4 &raw, float (&f)[8]) {
+    f[0] = bf16_lo(raw.x);
+    f[1] = bf16_hi(raw.x);
+    f[2] = bf16_lo(raw.y);
+    f[3] = bf16_hi(raw.y);
+    f[4] = bf16_lo(raw.z);
+    f[5] = bf16_hi(raw.z);
+    f[6] = bf16_lo(raw.w);
+    f[7] = bf16_hi(raw.w);
+}
+
+// Two floats to two bf16 (round to nearest even), element 0 in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ uint16_t to_bf16_bits(float x) {
+    __nv_bfloat16 h = __float2bfloat16_rn(x);
+    return *reinterpret_cast<uint16_t *>(&h);
+}
+
+__device__ __forceinline__ uint4 ld_stream(const void *p) {
+    return __ldcs(reinterpret_cast<const uint4 *>(p));
+}
+__device__ __forceinline__ void st_stream(void *p, const uint4 &v) {
+    __stcs(reinterpret_cast<uint4 *>(p), v);
+}
+__device__ __forceinline__ float4 ld_stream_f4(const float *p) {
+    return __ldcs(reinterpret_cast<const float4 *>(p));
+}
+__device__ __forceinline__ void st_stream_f4(float *p, const float4 &v) {
+    __stcs(reinterpret_cast<float4 *>(p), v);
+}
+
+// One AdamW update of one element, each operation rounded on its own.
+__device__ __forceinline__ void adamw(const Scalars &s, float decay, float g, float &w, float &m,
+                                      float &v) {
+    m = __fadd_rn(__fmul_rn(s.b1, m), __fmul_rn(s.omb1, g));
+    const float gg = __fmul_rn(g, g);
+    v = __fadd_rn(__fmul_rn(s.b2, v), __fmul_rn(s.omb2, gg));
+    w = __fmul_rn(w, decay);
+    const float denom = __fadd_rn(__fdiv_rn(__fsqrt_rn(v), s.bc2_sqrt), s.eps);
+    w = __fsub_rn(w, __fmul_rn(s.step_size, __fdiv_rn(m, denom)));
+}
+
+// First run (index >= j) whose end lies beyond `pos`: one ballot over 32
+// consecutive run ends per iteration.  All 32 lanes must call it.
+__device__ __forceinline__ int warp_first_run(const int64_t *run_end, int n_runs, int j,
+                                              int64_t pos, int lane) {
+    for (;;) {
+        const int idx = j + lane;
+        const bool ended = idx < n_runs && run_end[idx] <= pos;
+        const unsigned mask = __ballot_sync(0xffffffffu, ended);
+        j += __popc(mask);
+        if (mask != 0xffffffffu) return j;
+    }
+}
+
+template <typename G>
+__device__ __forceinline__ float load_grad_scalar(const void *base, int64_t i) {
+    if constexpr (sizeof(G) == 2)
+        return __uint_as_float(uint32_t(__ldcs(static_cast<const unsigned short *>(base) + i)) << 16);
+    else
+        return __ldcs(static_cast<const float *>(base) + i);
+}
+
+// Load the 8 grads of replica r at e0 (bf16: one 16-byte load; fp32: two).
+template <typename G>
+struct GradVec;
+
+template <>
+struct GradVec<__nv_bfloat16> {
+    uint4 a;
+    __device__ __forceinline__ void load(const void *base, int64_t e0) {
+        a = ld_stream(static_cast<const __nv_bfloat16 *>(base) + e0);
+    }
+    __device__ __forceinline__ void get(float (&f)[8]) const { unpack_bf16x8(a, f); }
+};
+
+template <>
+struct GradVec<float> {
+    float4 a, b;
+    __device__ __forceinline__ void load(const void *base, int64_t e0) {
+        const float *p = static_cast<const float *>(base) + e0;
+        a = ld_stream_f4(p);
+        b = ld_stream_f4(p + 4);
+    }
+    __device__ __forceinline__ void get(float (&f)[8]) const {
+        f[0] = a.x, f[1] = a.y, f[2] = a.z, f[3] = a.w;
+        f[4] = b.x, f[5] = b.y, f[6] = b.z, f[7] = b.w;
+    }
+};
+
+// Scaled rank-order fp32 reduction of 8 elements over the D replicas.
+template <typename G, int DC>
+__device__ __forceinline__ void reduce_vec(const StepArgs &a, int64_t e0, float (&acc)[8]) {
+    const float scale = a.sc.scale;
+    if constexpr (DC > 0) {
+        GradVec<G> g[DC];
+#pragma unroll
+        for (int r = 0; r < DC; ++r) g[r].load(a.grads[r], e0);
+#pragma unroll
+        for (int r = 0; r < DC; ++r) {
+            float f[8];
+            g[r].get(f);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float x = __fmul_rn(scale, f[k]);
+                acc[k] = r == 0 ? x : __fadd_rn(acc[k], x);
+            }
+        }
+    } else {
+        constexpr int kBatch = 4;
+        for (int r0 = 0; r0 < a.D; r0 += kBatch) {
+            GradVec<G> g[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u)
+                if (r0 + u < a.D) g[u].load(a.grads[r0 + u], e0);
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                if (r0 + u >= a.D) break;
+                float f[8];
+                g[u].get(f);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float x = __fmul_rn(scale, f[k]);
+                    acc[k] = (r0 + u) == 0 ? x : __fadd_rn(acc[k], x);
+                }
+            }
+        }
+    }
+}
+
+// A vector of 8 owned elements of one run.
+template <typename G, int DC>
+__device__ __forceinline__ void full_vector(const StepArgs &a, int64_t e0, int32_t meta) {
+    float acc[8];
+    reduce_vec<G, DC>(a, e0, acc);
+
+    const float4 w0 = ld_stream_f4(a.master + e0), w1 = ld_stream_f4(a.master + e0 + 4);
+    const float4 m0 = ld_stream_f4(a.exp_avg + e0), m1 = ld_stream_f4(a.exp_avg + e0 + 4);
+    const float4 v0 = ld_stream_f4(a.exp_avg_sq + e0), v1 = ld_stream_f4(a.exp_avg_sq + e0 + 4);
+    float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+    float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    const float decay = (meta & kRunDecays) ? a.sc.decay : 1.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) adamw(a.sc, decay, acc[k], w[k], m[k], v[k]);
+
+    st_stream_f4(a.master + e0, make_float4(w[0], w[1], w[2], w[3]));
+    st_stream_f4(a.master + e0 + 4, make_float4(w[4], w[5], w[6], w[7]));
+    st_stream_f4(a.exp_avg + e0, make_float4(m[0], m[1], m[2], m[3]));
+    st_stream_f4(a.exp_avg + e0 + 4, make_float4(m[4], m[5], m[6], m[7]));
+    st_stream_f4(a.exp_avg_sq + e0, make_float4(v[0], v[1], v[2], v[3]));
+    st_stream_f4(a.exp_avg_sq + e0 + 4, make_float4(v[4], v[5], v[6], v[7]));
+    if (a.main_grad_out) {
+        st_stream_f4(a.main_grad_out + e0, make_float4(acc[0], acc[1], acc[2], acc[3]));
+        st_stream_f4(a.main_grad_out + e0 + 4, make_float4(acc[4], acc[5], acc[6], acc[7]));
+    }
+
+    const uint4 packed = make_uint4(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]),
+                                    pack_bf16x2(w[4], w[5]), pack_bf16x2(w[6], w[7]));
+    if (a.gather) {
+        if constexpr (DC > 0) {
+#pragma unroll
+            for (int r = 0; r < DC; ++r)
+                st_stream(static_cast<__nv_bfloat16 *>(a.params[r]) + e0, packed);
+        } else {
+            for (int r = 0; r < a.D; ++r)
+                st_stream(static_cast<__nv_bfloat16 *>(a.params[r]) + e0, packed);
+        }
+    } else {
+        const int q = meta >> kRunRankShift;
+        st_stream(static_cast<__nv_bfloat16 *>(a.params[q]) + e0, packed);
+    }
+}
+
+// A vector that straddles a run edge: element by element, owned ones only.
+template <typename G, int DC>
+__device__ __noinline__ void mixed_vector(const StepArgs &a, int64_t e0, int j) {
+    const int D = DC > 0 ? DC : a.D;
+    for (int k = 0; k < kVec; ++k) {
+        const int64_t e = e0 + k;
+        if (e >= a.numel) return;
+        while (j < a.n_runs && a.run_end[j] <= e) ++j;
+        if (j >= a.n_runs) return;
+        if (a.run_start[j] > e) continue;  // padding
+        const int32_t meta = a.run_meta[j];
+        float g = 0.0f;
+        for (int r = 0; r < D; ++r) {
+            const float x = __fmul_rn(a.sc.scale, load_grad_scalar<G>(a.grads[r], e));
+            g = r == 0 ? x : __fadd_rn(g, x);
+        }
+        float w = a.master[e], m = a.exp_avg[e], v = a.exp_avg_sq[e];
+        adamw(a.sc, (meta & kRunDecays) ? a.sc.decay : 1.0f, g, w, m, v);
+        a.master[e] = w;
+        a.exp_avg[e] = m;
+        a.exp_avg_sq[e] = v;
+        if (a.main_grad_out) a.main_grad_out[e] = g;
+        const uint16_t bits = to_bf16_bits(w);
+        if (a.gather) {
+            for (int r = 0; r < D; ++r) static_cast<uint16_t *>(a.params[r])[e] = bits;
+        } else {
+            static_cast<uint16_t *>(a.params[meta >> kRunRankShift])[e] = bits;
+        }
+    }
+}
+
+template <typename G, int DC>
+__global__ void __launch_bounds__(kThreads) dopt_step_kernel(const __grid_constant__ StepArgs a) {
+    const int64_t tile_begin = int64_t(blockIdx.x) * kDoptTileElems;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp_begin = tile_begin + int64_t(threadIdx.x & ~31) * kVec;
+    const int64_t e0 = tile_begin + int64_t(threadIdx.x) * kVec;
+    int j = warp_first_run(a.run_end, a.n_runs, a.tile_run[blockIdx.x], warp_begin, lane);
+    if (e0 >= a.numel) return;
+    while (j < a.n_runs && a.run_end[j] <= e0) ++j;
+    if (j >= a.n_runs) return;
+    const int64_t rs = a.run_start[j];
+    if (rs >= e0 + kVec) return;  // all padding
+    if (rs <= e0 && e0 + kVec <= a.run_end[j])
+        full_vector<G, DC>(a, e0, a.run_meta[j]);
+    else
+        mixed_vector<G, DC>(a, e0, j);
+}
+
+__global__ void __launch_bounds__(kThreads) dopt_gather_kernel(const __grid_constant__ GatherArgs a) {
+    const int64_t tile_begin = int64_t(blockIdx.x) * kDoptTileElems;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp_begin = tile_begin + int64_t(threadIdx.x & ~31) * kVec;
+    const int64_t e0 = tile_begin + int64_t(threadIdx.x) * kVec;
+    int j = warp_first_run(a.run_end, a.n_runs, a.tile_run[blockIdx.x], warp_begin, lane);
+    if (e0 >= a.numel) return;
+    while (j < a.n_runs && a.run_end[j] <= e0) ++j;
+    if (j >= a.n_runs) return;
+    const int64_t rs = a.run_start[j];
+    if (rs >= e0 + kVec) return;
+    if (rs <= e0 && e0 + kVec <= a.run_end[j]) {
+        const int q = a.run_meta[j] >> kRunRankShift;
+        const uint4 val = ld_stream(static_cast<const __nv_bfloat16 *>(a.params[q]) + e0);
+        for (int r = 0; r < a.D; ++r)
+            if (r != q) st_stream(static_cast<__nv_bfloat16 *>(a.params[r]) + e0, val);
+        return;
+    }
+    for (int k = 0; k < kVec; ++k) {
+        const int64_t e = e0 + k;
+        if (e >= a.numel) return;
+        while (j < a.n_runs && a.run_end[j] <= e) ++j;
+        if (j >= a.n_runs) return;
+        if (a.run_start[j] > e) continue;
+        const int q = a.run_meta[j] >> kRunRankShift;
+        const uint16_t bits = static_cast<const uint16_t *>(a.params[q])[e];
+        for (int r = 0; r < a.D; ++r)
+            if (r != q) static_cast<uint16_t *>(a.params[r])[e] = bits;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+
+Scalars make_scalars(const dopt_adam_cfg &c, int64_t t) {
+    const double lr = c.lr, b1 = c.beta1, b2 = c.beta2, wd = c.weight_decay;
+    Scalars s;
+    s.b1 = c.beta1;
+    s.b2 = c.beta2;
+    s.omb1 = float(1.0 - b1);
+    s.omb2 = float(1.0 - b2);
+    s.decay = float(1.0 - lr * wd);
+    s.step_size = float(lr / (1.0 - std::pow(b1, double(t))));
+    s.bc2_sqrt = float(std::sqrt(1.0 - std::pow(b2, double(t))));
+    s.eps = c.eps;
+    s.scale = c.grad_scale;
+    return s;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+using StepKernel = void (*)(StepArgs);
+
+template <typename G>
+StepKernel pick_step_kernel(int D) {
+    switch (D) {
+        case 1: return dopt_step_kernel<G, 1>;
+        case 2: return dopt_step_kernel<G, 2>;
+        case 4: return dopt_step_kernel<G, 4>;
+        case 8: return dopt_step_kernel<G, 8>;
+        case 16: return dopt_step_kernel<G, 16>;
+        default: return dopt_step_kernel<G, 0>;
+    }
+}
+
+int check_device_tables(const dopt_layout *L, const char *who) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return dopt::fail(DOPT_E_CUDA, "%s: cudaGetDevice: %s", who, cudaGetErrorString(e));
+    if (L->device != dev || !L->d_block)
+        return dopt::fail(DOPT_E_STATE,
+                          "%s: layout tables are not on device %d (call dopt_layout_to_device)",
+                          who, dev);
+    return DOPT_OK;
+}
+
+}  // namespace
+
+extern "C" int dopt_step(const dopt_layout *L, const dopt_adam_cfg *cfg, int64_t step,
+                         const void *const *grad_replicas, dopt_dtype grad_dtype, float *master,
+                         float *exp_avg, float *exp_avg_sq, void *const *param_replicas,
+                         uint32_t flags, float *main_grad_out, cudaStream_t stream) {
+    using dopt::fail;
+    dopt::clear_error();
+    if (!L || !cfg || !grad_replicas || !param_replicas || !master || !exp_avg || !exp_avg_sq)
+        return fail(DOPT_E_ARG, "dopt_step: NULL argument");
+    if (step < 1) return fail(DOPT_E_ARG, "dopt_step: step=%lld < 1", (long long)step);
+    if (grad_dtype != DOPT_BF16 && grad_dtype != DOPT_FP32)
+        return fail(DOPT_E_ARG, "dopt_step: unknown grad dtype %d", int(grad_dtype));
+    if (flags & ~uint32_t(DOPT_STEP_GATHER))
+        return fail(DOPT_E_ARG, "dopt_step: unknown flags 0x%x", flags);
+    if (!(cfg->lr >= 0.0f) || !std::isfinite(cfg->lr) || !(cfg->beta1 >= 0.0f && cfg->beta1 < 1.0f) ||
+        !(cfg->beta2 >= 0.0f && cfg->beta2 < 1.0f) || !(cfg->eps >= 0.0f) || !std::isfinite(cfg->eps) ||
+        !(cfg->weight_decay >= 0.0f) || !std::isfinite(cfg->weight_decay) ||
+        !std::isfinite(cfg->grad_scale))
+        return fail(DOPT_E_ARG, "dopt_step: hyper-parameter out of range");
+    const int D = L->cfg.D;
+    for (int r = 0; r < D; ++r) {
+        if (!grad_replicas[r] || !param_replicas[r])
+            return fail(DOPT_E_ARG, "dopt_step: replica %d pointer is NULL", r);
+        if (!aligned16(grad_replicas[r]) || !aligned16(param_replicas[r]))
+            return fail(DOPT_E_ALIGN, "dopt_step: replica %d pointer is not 16-byte aligned", r);
+    }
+    if (!aligned16(master) || !aligned16(exp_avg) || !aligned16(exp_avg_sq) ||
+        (main_grad_out && !aligned16(main_grad_out)))
+        return fail(DOPT_E_ALIGN, "dopt_step: state pointer is not 16-byte aligned");
+    if (L->run_start.empty()) return DOPT_OK;  // nothing owned: nothing to do
+    int rc = check_device_tables(L, "dopt_step");
+    if (rc != DOPT_OK) return rc;
+
+    StepArgs a{};
+    for (int r = 0; r < D; ++r) {
+        a.grads[r] = grad_replicas[r];
+        a.params[r] = param_replicas[r];
+    }
+    a.master = master;
+    a.exp_avg = exp_avg;
+    a.exp_avg_sq = exp_avg_sq;
+    a.main_grad_out = main_grad_out;
+    a.run_start = L->d_run_start;
+    a.run_end = L->d_run_end;
+    a.run_meta = L->d_run_meta;
+    a.tile_run = L->d_tile_run;
+    a.numel = L->numel;
+    a.n_runs = int32_t(L->run_start.size());
+    a.D = D;
+    a.gather = (flags & DOPT_STEP_GATHER) ? 1 : 0;
+    a.sc = make_scalars(*cfg, step);
+
+    const unsigned grid = unsigned((L->numel + kDoptTileElems - 1) / kDoptTileElems);
+    StepKernel k = grad_dtype == DOPT_BF16 ? pick_step_kernel<__nv_bfloat16>(D)
+                                           : pick_step_kernel<float>(D);
+    k<<<grid, kThreads, 0, stream>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(DOPT_E_CUDA, "dopt_step launch: %s", cudaGetErrorString(e));
+    return DOPT_OK;
+}
+
+extern "C" int dopt_gather(const dopt_layout *L, void *const *param_replicas, cudaStream_t stream) {
+    using dopt::fail;
+    dopt::clear_error();
+    if (!L || !param_replicas) return fail(DOPT_E_ARG, "dopt_gather: NULL argument");
+    const int D = L->cfg.D;
+    for (int r = 0; r < D; ++r) {
+        if (!param_replicas[r]) return fail(DOPT_E_ARG, "dopt_gather: replica %d is NULL", r);
+        if (!aligned16(param_replicas[r]))
+            return fail(DOPT_E_ALIGN, "dopt_gather: replica %d is not 16-byte aligned", r);
+    }
+    if (L->run_start.empty() || D == 1) return DOPT_OK;
+    int rc = check_device_tables(L, "dopt_gather");
+    if (rc != DOPT_OK) return rc;
+    GatherArgs a{};
+    for (int r = 0; r < D; ++r) a.params[r] = param_replicas[r];
+    a.run_start = L->d_run_start;
+    a.run_end = L->d_run_end;
+    a.run_meta = L->d_run_meta;
+    a.tile_run = L->d_tile_run;
+    a.numel = L->numel;
+    a.n_runs = int32_t(L->run_start.size());
+    a.D = D;
+    const unsigned grid = unsigned((L->numel + kDoptTileElems - 1) / kDoptTileElems);
+    dopt_gather_kernel<<<grid, kThreads, 0, stream>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(DOPT_E_CUDA, "dopt_gather launch: %s", cudaGetErrorString(e));
+    return DOPT_OK;
+}

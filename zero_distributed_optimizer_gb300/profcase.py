@@ -1,0 +1,95 @@
+"""Run a few launches of the fused step on one workload, for profilers.
+
+    python -m zero_distributed_optimizer_gb300.profcase --workload gpt2_small \
+        [--max-elems N] [--warmup W] [--launches K] [--gather-kernel]
+
+--max-elems keeps the leading params of the workload whose total stays
+within N elements, so that a profiler capture can run on a smaller buffer of
+the same shape mix.  Inputs come from the seeded workload generators.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def truncated(w, max_elems):
+    if not max_elems or w.numel <= max_elems:
+        return w
+    sizes, wd, total = [], [], 0
+    for s, d in zip(w.sizes, w.wd_mask):
+        if total + s > max_elems:
+            if not sizes:  # a single param larger than the cap: cut it
+                sizes.append(max_elems)
+                wd.append(d)
+            break
+        sizes.append(s)
+        wd.append(d)
+        total += s
+    return w.with_(name=f"{w.name}_first{sum(sizes)}", sizes=tuple(sizes), wd_mask=tuple(wd))
+
+
+def main(argv=None):
+    import torch
+
+    from zero_distributed_optimizer_gb300 import binding as B
+    from zero_distributed_optimizer_gb300 import build as libbuild
+    from zero_distributed_optimizer_gb300 import workloads as W
+
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", default="gpt2_small",
+                    choices=["toy_1000", "gpt2_small", "llama_1p3b", "sweep_256m", "moe_many_small"])
+    ap.add_argument("--D", type=int, default=8, help="sweep_256m only")
+    ap.add_argument("--bucket-mi", type=int, default=64, help="sweep_256m only")
+    ap.add_argument("--max-elems", type=int, default=0)
+    ap.add_argument("--warmup", type=int, default=2)
+    ap.add_argument("--launches", type=int, default=3)
+    ap.add_argument("--gather-kernel", action="store_true",
+                    help="time dopt_gather instead of the fused step")
+    args = ap.parse_args(argv)
+
+    libbuild.build()
+    if args.workload == "sweep_256m":
+        w = W.sweep_256m(args.D, args.bucket_mi)
+    else:
+        w = getattr(W, args.workload)()
+    w = truncated(w, args.max_elems)
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    L = B.dopt_build_range_map(list(w.sizes), w.D, w.bucket_elems, w.pad_unit,
+                               list(w.wd_mask)).to_device(dev)
+    N = L.padded_numel
+    master, m, v = W.make_state(w, N, dev)
+    params = W.make_params(master, w.D)
+    grads = W.make_grads(w, N, 1, dev)
+    adam = B.AdamConfig(**w.adam_kwargs())
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    t = 0
+    for i in range(args.warmup + args.launches):
+        if i == args.warmup:
+            ev[0].record()
+        t += 1
+        if args.gather_kernel:
+            B.dopt_gather(L, params)
+        else:
+            B.dopt_step(L, adam, t, grads, master, m, v, params)
+    ev[1].record()
+    torch.cuda.synchronize()
+    ms = ev[0].elapsed_time(ev[1]) / max(args.launches, 1)
+    bytes_per = w.numel * (2 * w.D if args.gather_kernel else w.algorithmic_bytes_per_element())
+    print(json.dumps({"workload": w.name, "N": w.numel, "padded_numel": N, "D": w.D,
+                      "kernel": "dopt_gather_kernel" if args.gather_kernel else "dopt_step_kernel",
+                      "launches": args.launches, "ms_per_launch": ms,
+                      "algorithmic_bytes_per_launch": bytes_per,
+                      "gbs": bytes_per / (ms / 1e3) / 1e9}))
+
+
+if __name__ == "__main__":
+    main()

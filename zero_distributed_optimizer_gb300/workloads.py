@@ -256,3 +256,29 @@ def make_params(master, D: int):
 
     p = master.to(torch.bfloat16)
     return [p.clone() for _ in range(D)]
+
+
+def random_case(numel: int, D: int, steps: int, grad_dtype: str = "bf16", seed: int = 0):
+    """Seeded inputs for a small parity case (CPU tensors): fp32 master/m/v,
+    D distinct random bf16 replicas (so untouched padding is visible) and
+    per-step grads mixing magnitudes: N(0, 1e-3), 1% near 1, 1% zeros and
+    1% below eps (1e-10)."""
+    import torch
+
+    g = _gen(torch, "cpu", seed_of("random_case", numel, D, seed))
+    master = torch.randn(numel, generator=g) * 0.02
+    m = torch.randn(numel, generator=g) * 1e-4
+    v = (torch.randn(numel, generator=g) * 1e-6).abs()
+    params = [(torch.randn(numel, generator=g) * 0.02).to(torch.bfloat16) for _ in range(D)]
+    grads = []
+    for _ in range(steps):
+        per_rank = []
+        for _ in range(D):
+            x = torch.randn(numel, generator=g) * 1e-3
+            u = torch.rand(numel, generator=g)
+            x = torch.where(u < 0.01, x * 1000, x)
+            x = torch.where((u >= 0.01) & (u < 0.02), torch.zeros_like(x), x)
+            x = torch.where((u >= 0.02) & (u < 0.03), x * 1e-7, x)
+            per_rank.append(x.to(torch.bfloat16) if grad_dtype == "bf16" else x)
+        grads.append(per_rank)
+    return master, m, v, params, grads
