@@ -108,8 +108,15 @@ def _declare(lib) -> None:
         i64p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32,
         ctypes.POINTER(Adam), ctypes.c_int64, ctypes.c_int32, ctypes.POINTER(ctypes.c_void_p),
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p),
-        ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+        ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_float,
     ]
+    lib.orc_grad_norm_sq.restype = ctypes.c_int
+    lib.orc_grad_norm_sq.argtypes = [i64p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
+                                     ctypes.c_int32, ctypes.c_float, ctypes.c_int32,
+                                     ctypes.POINTER(ctypes.c_void_p), ctypes.c_int64,
+                                     ctypes.c_int64, ctypes.POINTER(ctypes.c_double)]
+    lib.orc_clip_coef.restype = ctypes.c_float
+    lib.orc_clip_coef.argtypes = [ctypes.c_double, ctypes.c_float]
     lib.orc_f32_to_bf16.restype = ctypes.c_uint16
     lib.orc_f32_to_bf16.argtypes = [ctypes.c_float]
     lib.orc_bf16_to_f32.restype = ctypes.c_float
@@ -220,14 +227,15 @@ def make_adam(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, grad_s
 
 def step(sizes, wd_mask, D: int, bucket_elems: int, pad_unit: int, adam: Adam, t: int,
          grads, master, exp_avg, exp_avg_sq, params, gather: bool = True,
-         main_grad_out=None, window=None, lib=None) -> None:
+         main_grad_out=None, window=None, clip_coef: float = 1.0, lib=None) -> None:
     """One ZeRO-1 step for all D simulated ranks, in place on numpy arrays.
 
     grads: D arrays (uint16 bf16 bits or float32); master/exp_avg/exp_avg_sq:
     float32; params: D uint16 arrays (bf16 bits); main_grad_out: optional
     float32.  All are buffer-indexed and cover ``window = (w0, w1)`` (default:
     the whole padded buffer).  Follows page 1 §4.2 (reduce-scatter), §4.3
-    (main grads, Adam, write-back) and §4.4 (all-gather).
+    (main grads, Adam, write-back) and §4.4 (all-gather).  ``clip_coef``
+    (from :func:`clip_coef`) multiplies every reduced grad before Adam.
     """
     lib = lib or load()
     sizes_a, sizes_p = _i64(sizes)
@@ -263,9 +271,36 @@ def step(sizes, wd_mask, D: int, bucket_elems: int, pad_unit: int, adam: Adam, t
                       pad_unit, ctypes.byref(adam), t, int(grad_is_f32), gp,
                       master.ctypes.data, exp_avg.ctypes.data, exp_avg_sq.ctypes.data, pp,
                       int(bool(gather)),
-                      None if main_grad_out is None else main_grad_out.ctypes.data, w0, w1)
+                      None if main_grad_out is None else main_grad_out.ctypes.data, w0, w1,
+                      float(clip_coef))
     if rc != ORC_OK:
         raise OracleError(f"orc_step failed: {rc}")
+
+
+def grad_norm_sq(sizes, D: int, bucket_elems: int, pad_unit: int, grad_scale: float, grads,
+                 window=None, lib=None) -> float:
+    """Sum of squares of the reduced grads over the owned elements of the
+    window (tutorial §8.3 global norm), accumulated in double."""
+    lib = lib or load()
+    sizes_a, sizes_p = _i64(sizes)
+    grad_is_f32 = grads[0].dtype == np.float32
+    span = len(grads[0])
+    w0, w1 = (0, span) if window is None else (int(window[0]), int(window[1]))
+    if w1 - w0 != span or len(grads) != D:
+        raise OracleError("grads must be D arrays of the window length")
+    gp = (ctypes.c_void_p * D)(*[g.ctypes.data for g in grads])
+    out = ctypes.c_double(0.0)
+    rc = lib.orc_grad_norm_sq(sizes_p, len(sizes_a), D, bucket_elems, pad_unit,
+                              float(grad_scale), int(grad_is_f32), gp, w0, w1, ctypes.byref(out))
+    if rc != ORC_OK:
+        raise OracleError(f"orc_grad_norm_sq failed: {rc}")
+    return float(out.value)
+
+
+def clip_coef(norm_sq: float, max_norm: float, lib=None) -> float:
+    """min(1, max_norm / (sqrt(norm_sq) + 1e-6)), rounded to float once."""
+    lib = lib or load()
+    return float(lib.orc_clip_coef(float(norm_sq), float(max_norm)))
 
 
 def f32_to_bf16(x, lib=None) -> np.ndarray:

@@ -27,8 +27,8 @@
  *        §5  gradient_scaling_factor multiplies the grads before the
  *            communication; padding keeps every bucket divisible by DP.
  *  [P2]  "distributed_training" tutorial, "AllReduce" (reduce-scatter then
- *        all-gather equals all-reduce) and §8.2 mixed precision (bf16 model
- *        params, fp32 master weights).
+ *        all-gather equals all-reduce), §8.2 mixed precision (bf16 model
+ *        params, fp32 master weights) and §8.3 global norm clipping.
  *
  * Readings where the pages leave a step open (each one is listed in the
  * design notes of the repository):
@@ -61,6 +61,12 @@
  *      stays a quiet NaN.
  *  R8  The all-gather copies every rank's owned elements (its pieces) from
  *      its own replica into all other replicas; padding is not copied.
+ *  R9  Global-norm clipping ([P2] §8.3: the norm sqrt(sum ||g||^2) over all
+ *      shards, needed before the optimizer update): norm^2 is the sum of the
+ *      squares of the reduced fp32 grads of all owned elements, accumulated
+ *      in double; the coefficient is min(1, max_norm / (norm + 1e-6)),
+ *      evaluated in double and rounded to float once; each reduced grad is
+ *      multiplied by it (one fp32 rounding) before Adam.
  *
  * Windows: the step can be restricted to global buffer indices [w0, w1).
  * All buffer-indexed arrays passed to orc_step are then window-relative
@@ -292,6 +298,19 @@ static float orc_grad(const void *const *grads, int32_t grad_is_f32, int32_t r, 
     return orc_bf16_to_f32(((const uint16_t *)grads[r])[idx]);
 }
 
+/* The reduced grad of buffer element idx (R5): rank-order fp32 sum of the
+ * scaled replicas.  `idx` is window-relative. */
+static float orc_reduce_element(const void *const *grads, int32_t grad_is_f32, int32_t D,
+                                float scale, int64_t idx)
+{
+    float acc = scale * orc_grad(grads, grad_is_f32, 0, idx);
+    for (int32_t q = 1; q < D; ++q) {
+        float x = scale * orc_grad(grads, grad_is_f32, q, idx);
+        acc = acc + x;
+    }
+    return acc;
+}
+
 /* One AdamW update of a single element (R6), fp32, one rounding per op. */
 static void orc_adamw(const orc_scalars *s, int decays, float g, float *w, float *m, float *v)
 {
@@ -327,7 +346,9 @@ static void orc_adamw(const orc_scalars *s, int decays, float g, float *w, float
  *   gather          nonzero: all-gather into every replica (R8); zero: only
  *                   the owning rank's replica receives its updated shard
  *   main_grad_out   nullable: the reduce-scattered fp32 main grad of each
- *                   owned element, buffer-indexed
+ *                   owned element, buffer-indexed (before clipping)
+ *   clip_coef       global-norm clipping coefficient (orc_clip_coef); 1.0
+ *                   when no clipping is wanted
  *
  * All buffer-indexed arrays are window-relative.  Returns ORC_OK or an error.
  */
@@ -335,7 +356,7 @@ int orc_step(const int64_t *sizes, int32_t n, const uint8_t *wd_mask, int32_t D,
              int64_t bucket_elems, int32_t pad_unit, const orc_adam *cfg, int64_t step,
              int32_t grad_is_f32, const void *const *grads, float *master, float *exp_avg,
              float *exp_avg_sq, uint16_t *const *params, int32_t gather,
-             float *main_grad_out, int64_t w0, int64_t w1)
+             float *main_grad_out, int64_t w0, int64_t w1, float clip_coef)
 {
     if (step < 1 || w0 < 0 || w1 < w0)
         return ORC_E_ARG;
@@ -398,12 +419,7 @@ int orc_step(const int64_t *sizes, int32_t n, const uint8_t *wd_mask, int32_t D,
             int64_t j_hi = orc_min(S, w1 - mine.start);
             for (int64_t j = j_lo; j < j_hi; ++j) {
                 int64_t i = mine.start + j;
-                float acc = sc.scale * orc_grad(grads, grad_is_f32, 0, i - w0);
-                for (int32_t q = 1; q < D; ++q) {
-                    float x = sc.scale * orc_grad(grads, grad_is_f32, q, i - w0);
-                    acc = acc + x;
-                }
-                shard[j] = acc;
+                shard[j] = orc_reduce_element(grads, grad_is_f32, D, sc.scale, i - w0);
             }
 
             /* This rank's pieces are contiguous in the piece list. */
@@ -422,10 +438,13 @@ int orc_step(const int64_t *sizes, int32_t n, const uint8_t *wd_mask, int32_t D,
                     int64_t i = pc->gbuf_world.start + t;
                     /* main grad: the shard sliced by gbuf_local ([P1] §4.3) */
                     float g = shard[pc->gbuf_local.start + t];
+                    /* global-norm clipping (R9): one fp32 multiply; a
+                     * coefficient of exactly 1 leaves g unchanged */
+                    float gc = g * clip_coef;
                     /* main param: the param's fp32 copy sliced by the "param"
                      * range; stored buffer-indexed at the param's offset. */
                     int64_t mi = pstart[p] + pc->param.start + t;
-                    orc_adamw(&sc, decays, g, &master[mi - w0], &exp_avg[mi - w0],
+                    orc_adamw(&sc, decays, gc, &master[mi - w0], &exp_avg[mi - w0],
                               &exp_avg_sq[mi - w0]);
                     /* write-back into rank r's bucket view at
                      * gbuf_world_in_bucket ([P1] §4.3) */
@@ -463,6 +482,78 @@ done:
     free(bstart);
     free(bend);
     return rc;
+}
+
+/*
+ * Sum of squares of the reduced grads over the owned elements of the window
+ * [w0, w1) (R9), in piece order, accumulated in double.  Grad arrays are
+ * window-relative.  Summing the results of disjoint windows that cover the
+ * buffer gives the global norm^2.
+ */
+int orc_grad_norm_sq(const int64_t *sizes, int32_t n, int32_t D, int64_t bucket_elems,
+                     int32_t pad_unit, float grad_scale, int32_t grad_is_f32,
+                     const void *const *grads, int64_t w0, int64_t w1, double *out)
+{
+    if (w0 < 0 || w1 < w0 || !out)
+        return ORC_E_ARG;
+    int rc = ORC_OK;
+    size_t cap = (size_t)(n > 0 ? n : 1);
+    int64_t *pstart = (int64_t *)malloc(cap * sizeof *pstart);
+    int64_t *pend = (int64_t *)malloc(cap * sizeof *pend);
+    int32_t *pbucket = (int32_t *)malloc(cap * sizeof *pbucket);
+    int64_t *bstart = (int64_t *)malloc(cap * sizeof *bstart);
+    int64_t *bend = (int64_t *)malloc(cap * sizeof *bend);
+    orc_piece *pieces = NULL;
+    int32_t nb = 0, npieces = 0;
+    int64_t numel = 0;
+    double sum = 0.0;
+    if (!pstart || !pend || !pbucket || !bstart || !bend) {
+        rc = ORC_E_NOMEM;
+        goto done;
+    }
+    rc = orc_layout(sizes, n, D, bucket_elems, pad_unit, pstart, pend, pbucket, bstart, bend,
+                    &nb, &numel);
+    if (rc != ORC_OK)
+        goto done;
+    if (w1 > numel) {
+        rc = ORC_E_ARG;
+        goto done;
+    }
+    pieces = (orc_piece *)malloc(((size_t)n + (size_t)D * (size_t)nb + 1) * sizeof *pieces);
+    if (!pieces) {
+        rc = ORC_E_NOMEM;
+        goto done;
+    }
+    rc = orc_pieces(n, pstart, pend, pbucket, nb, bstart, bend, D, pieces, &npieces);
+    if (rc != ORC_OK)
+        goto done;
+    for (int32_t pi = 0; pi < npieces; ++pi) {
+        int64_t i_lo = orc_max(pieces[pi].gbuf_world.start, w0);
+        int64_t i_hi = orc_min(pieces[pi].gbuf_world.end, w1);
+        for (int64_t i = i_lo; i < i_hi; ++i) {
+            double g = (double)orc_reduce_element(grads, grad_is_f32, D, grad_scale, i - w0);
+            sum += g * g;
+        }
+    }
+    *out = sum;
+done:
+    free(pieces);
+    free(pstart);
+    free(pend);
+    free(pbucket);
+    free(bstart);
+    free(bend);
+    return rc;
+}
+
+/* Clipping coefficient from the global norm^2 (R9). */
+float orc_clip_coef(double norm_sq, float max_norm)
+{
+    double norm = sqrt(norm_sq);
+    double coef = (double)max_norm / (norm + 1e-6);
+    if (coef > 1.0)
+        coef = 1.0;
+    return (float)coef;
 }
 
 /* Convenience for tests: the layout and pieces in one call.  Sizes of the

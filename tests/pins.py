@@ -499,6 +499,151 @@ def pin_window_equals_full(lib):
             assert np.array_equal(a, b[w0:w1])
 
 
+# ---------------------------------------------------------------------------
+# Global-norm clipping pins (tutorial §8.3)
+# ---------------------------------------------------------------------------
+
+def pin_clip_norm_closed_form(lib):
+    """norm^2 of four reduced grads of 1.5 (D=2, two halves of 0.75) is 9;
+    with max_norm at least the norm the coefficient is exactly 1."""
+    D = 2
+    grads = [_bf16_bits_of(np.array([0.75] * 4, np.float32)) for _ in range(D)]
+    nsq = oracle.grad_norm_sq([4], D, 0, 1, 1.0, grads, lib=lib)
+    assert nsq == 9.0, nsq
+    assert oracle.clip_coef(nsq, 3.5, lib=lib) == 1.0
+    assert oracle.clip_coef(nsq, 1e9, lib=lib) == 1.0
+    assert 0.0 < oracle.clip_coef(nsq, 1.5, lib=lib) < 0.5
+    # padding is not part of the norm
+    grads_p = [_bf16_bits_of(np.array([0.75] * 4 + [100.0] * 2, np.float32)) for _ in range(D)]
+    assert oracle.grad_norm_sq([4], D, 0, 3, 1.0, grads_p, lib=lib) == 9.0
+
+
+def _clip_vs_torch(lib, grad_std, steps=3, seed=13):
+    import torch
+
+    sizes = [50, 13, 200, 7]
+    wd_mask = [1, 0, 1, 1]
+    n = sum(sizes)
+    adam_f = dict(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1)
+    master, m, v = _state(n, seed, m_scale=1e-4, v_scale=1e-6)
+    params = _params_from(master, 1)
+    rng = np.random.default_rng(seed)
+    t_params, groups = [], {0: [], 1: []}
+    off = 0
+    for size, w in zip(sizes, wd_mask):
+        p = torch.tensor(master[off:off + size].astype(np.float64), requires_grad=True)
+        t_params.append((p, off, size))
+        groups[w].append(p)
+        off += size
+    opt = torch.optim.AdamW(
+        [{"params": groups[1], "weight_decay": _f32(adam_f["weight_decay"])},
+         {"params": groups[0], "weight_decay": 0.0}],
+        lr=_f32(adam_f["lr"]), betas=(_f32(adam_f["beta1"]), _f32(adam_f["beta2"])),
+        eps=_f32(adam_f["eps"]), foreach=False)
+    for p, o, size in t_params:
+        opt.state[p] = {"step": torch.tensor(0.0),
+                        "exp_avg": torch.tensor(m[o:o + size].astype(np.float64)),
+                        "exp_avg_sq": torch.tensor(v[o:o + size].astype(np.float64))}
+    adam = oracle.make_adam(grad_scale=1.0, **adam_f)
+    u = 2.0 ** -24
+    b1 = _f32(adam_f["beta1"])
+    mag_m = np.abs(m.astype(np.float64))
+    for t in range(1, steps + 1):
+        g = rng.normal(0, grad_std, n).astype(np.float32)
+        bits = (g.view(np.uint32) >> 16).astype(np.uint16)
+        gf = _bits_to_f32(bits).astype(np.float64)
+        max_norm = 0.5 * float(np.sqrt(np.sum(gf * gf)))
+        nsq = oracle.grad_norm_sq(sizes, 1, 0, 1, 1.0, [bits], lib=lib)
+        coef = oracle.clip_coef(nsq, max_norm, lib=lib)
+        oracle.step(sizes, wd_mask, 1, 0, 1, adam, t, [bits], master, m, v, params,
+                    clip_coef=coef, lib=lib)
+        for p, o, size in t_params:
+            p.grad = torch.tensor(gf[o:o + size])
+        total = torch.nn.utils.clip_grad_norm_([p for p, _, _ in t_params], max_norm)
+        assert abs(np.sqrt(nsq) - float(total)) <= 1e-12 * float(total)
+        opt.step()
+        gclip = np.concatenate([p.grad.numpy() for p, _, _ in t_params])
+        mag_m = b1 * mag_m + (1 - b1) * np.abs(gclip)
+    ref_w = np.concatenate([p.detach().numpy() for p, _, _ in t_params])
+    ref_m = np.concatenate([opt.state[p]["exp_avg"].numpy() for p, _, _ in t_params])
+    ref_v = np.concatenate([opt.state[p]["exp_avg_sq"].numpy() for p, _, _ in t_params])
+    np.testing.assert_allclose(master, ref_w, rtol=2e-6, atol=1e-9)
+    assert np.all(np.abs(m - ref_m) <= 2e-6 * np.abs(ref_m) + 8 * u * steps * mag_m)
+    np.testing.assert_allclose(v, ref_v, rtol=4e-6, atol=1e-20)
+
+
+def pin_clip_d1_matches_torch(lib):
+    """D=1 with clipping equals PyTorch's clip_grad_norm_ followed by AdamW
+    (float64), for a large norm and for a norm small enough that the 1e-6
+    in the coefficient's denominator matters."""
+    _clip_vs_torch(lib, grad_std=1.0, seed=13)
+    _clip_vs_torch(lib, grad_std=1e-5, seed=14)
+
+
+def pin_clip_off_equals_plain_step(lib):
+    """A coefficient of 1 (norm below max_norm) leaves the step bitwise equal
+    to the step without clipping."""
+    sizes, wd = [100, 27, 300], [1, 0, 1]
+    D, pad = 4, 2
+    L = oracle.range_map(sizes, D, 0, pad, lib=lib)
+    N = L.numel
+    rng = np.random.default_rng(2)
+    grads = [_bf16_bits_of((rng.integers(-50, 50, N) / 256).astype(np.float32)) for _ in range(D)]
+    nsq = oracle.grad_norm_sq(sizes, D, 0, pad, 0.25, grads, lib=lib)
+    coef = oracle.clip_coef(nsq, 2.0 * float(np.sqrt(nsq)) + 1.0, lib=lib)
+    assert coef == 1.0
+    a = list(_state(N, 3, 1e-4, 1e-6)) + [_params_from(_state(N, 3)[0], D)]
+    b = [x.copy() for x in a[:3]] + [[p.copy() for p in a[3]]]
+    adam = oracle.make_adam(grad_scale=0.25)
+    oracle.step(sizes, wd, D, 0, pad, adam, 1, grads, a[0], a[1], a[2], a[3], lib=lib)
+    oracle.step(sizes, wd, D, 0, pad, adam, 1, grads, b[0], b[1], b[2], b[3], clip_coef=coef,
+                lib=lib)
+    for x, y in zip(a[:3], b[:3]):
+        assert np.array_equal(x.view(np.uint32), y.view(np.uint32))
+
+
+def pin_clip_d_independence(lib):
+    """With clipping engaged, integer-valued grads still give results that
+    are bitwise independent of D: the reduced grads are the same, their
+    squares are exact in double and so is their sum, in any order."""
+    rng = np.random.default_rng(23)
+    sizes = [33, 7, 129, 64]
+    wd = [1, 0, 1, 1]
+    n = sum(sizes)
+    G = rng.integers(-64, 65, n).astype(np.float32)
+    base = None
+    for D, pad in ((1, 1), (2, 3), (4, 1), (8, 2), (16, 1)):
+        L = oracle.range_map(sizes, D, 0, pad, lib=lib)
+        N = L.numel
+        master, m, v = np.zeros(N, np.float32), np.zeros(N, np.float32), np.zeros(N, np.float32)
+        m0, _, _ = _state(n, 31)
+        grads = []
+        for r in range(D):
+            g = np.zeros(N, np.float32)
+            off = 0
+            for p, size in enumerate(sizes):
+                s0 = int(L.param_start[p])
+                g[s0:s0 + size] = (G[off:off + size] + (2 * r - (D - 1)) * 2) / 1024.0
+                master[s0:s0 + size] = m0[off:off + size]
+                off += size
+            grads.append(_bf16_bits_of(g))
+        params = _params_from(master, D)
+        nsq = oracle.grad_norm_sq(sizes, D, 0, pad, 1.0 / D, grads, lib=lib)
+        coef = oracle.clip_coef(nsq, 0.25 * float(np.sqrt(nsq)), lib=lib)
+        assert coef < 1.0
+        oracle.step(sizes, wd, D, 0, pad, oracle.make_adam(grad_scale=1.0 / D), 1, grads, master,
+                    m, v, params, clip_coef=coef, lib=lib)
+        res = [(master[int(L.param_start[p]):int(L.param_end[p])].copy(),
+                m[int(L.param_start[p]):int(L.param_end[p])].copy()) for p in range(len(sizes))]
+        if base is None:
+            base = (nsq, coef, res)
+            continue
+        assert nsq == base[0] and coef == base[1], D
+        for (a, b), (c, d) in zip(res, base[2]):
+            assert np.array_equal(a.view(np.uint32), c.view(np.uint32))
+            assert np.array_equal(b.view(np.uint32), d.view(np.uint32))
+
+
 ALL_PINS = [
     pin_page1_ownership,
     pin_brute_force_range_maps,
@@ -512,4 +657,8 @@ ALL_PINS = [
     pin_bf16_rounding,
     pin_gather_and_padding,
     pin_window_equals_full,
+    pin_clip_norm_closed_form,
+    pin_clip_d1_matches_torch,
+    pin_clip_off_equals_plain_step,
+    pin_clip_d_independence,
 ]

@@ -15,8 +15,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 # (name, text in dopt_oracle.c, replacement)
 MUTANTS = [
-    ("no_scale_rank0", "float acc = sc.scale * orc_grad(grads, grad_is_f32, 0, i - w0);",
-     "float acc = orc_grad(grads, grad_is_f32, 0, i - w0);"),
+    ("no_scale_rank0", "float acc = scale * orc_grad(grads, grad_is_f32, 0, idx);",
+     "float acc = orc_grad(grads, grad_is_f32, 0, idx);"),
     ("skip_last_rank", "for (int32_t q = 1; q < D; ++q) {", "for (int32_t q = 1; q < D - 1; ++q) {"),
     ("update_sign", "ww = ww - delta;", "ww = ww + delta;"),
     ("no_bias_correction1", "s.step_size = (float)(lr / (1.0 - pow(b1, (double)t)));",
@@ -48,6 +48,12 @@ MUTANTS = [
     ("local_range_from_bucket", "pc.gbuf_local = orc_normalize(pc.gbuf_world, x - mine.start);",
      "pc.gbuf_local = orc_normalize(pc.gbuf_world, x - bucket_start[k]);"),
     ("no_gather", "if (gather) {", "if (0) {"),
+    ("clip_not_applied", "float gc = g * clip_coef;", "float gc = g;"),
+    ("norm_not_squared", "sum += g * g;", "sum += g < 0 ? -g : g;"),
+    ("clip_no_sqrt", "double norm = sqrt(norm_sq);", "double norm = norm_sq;"),
+    ("clip_no_upper_bound", "if (coef > 1.0)", "if (coef > 2.0)"),
+    ("clip_eps_dropped", "double coef = (double)max_norm / (norm + 1e-6);",
+     "double coef = (double)max_norm / norm;"),
     ("bf16_truncates", "if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u)))", "if (0)"),
     ("bf16_ties_away", "if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u)))",
      "if (lower >= 0x8000u)"),
