@@ -215,6 +215,42 @@ int dopt_step(const dopt_layout *layout, const dopt_adam_cfg *cfg, int64_t step,
  */
 int dopt_gather(const dopt_layout *layout, void *const *param_replicas, cudaStream_t stream);
 
+/* Bytes of device workspace that dopt_step_clipped needs (16-byte aligned). */
+#define DOPT_CLIP_WORKSPACE_BYTES 16384
+
+/*
+ * The step with global grad-norm clipping (distributed-training tutorial,
+ * §8.3: the norm sqrt(sum ||g||^2) over every rank's shard is needed before
+ * the optimizer update).  Two launches on `stream`:
+ *
+ *   1. the fused reduce-scatter writes every owned element's reduced fp32
+ *      grad g (as in dopt_step) into main_grad, and the global
+ *      norm^2 = sum of g^2 over all owned elements is accumulated (fp32
+ *      squares summed per 8 elements, then in fp64); the coefficient
+ *      c = min(1, max_norm / (norm + 1e-6)) is evaluated in fp64 and rounded
+ *      to float;
+ *   2. the AdamW step, write-back and (with DOPT_STEP_GATHER) all-gather of
+ *      dopt_step, with g replaced by fl(g * c).
+ *
+ *   max_norm    > 0, finite
+ *   main_grad   device fp32[padded_numel], written: the reduced grads
+ *               before clipping (padding untouched)
+ *   workspace   device, DOPT_CLIP_WORKSPACE_BYTES, 16-byte aligned, owned by
+ *               the caller; holds per-CTA partial sums between the launches;
+ *               calls that share a workspace must not overlap on the GPU
+ *   norm_out    nullable device float[2]: [0] = global norm, [1] = c
+ *   other arguments as in dopt_step.
+ *
+ * The norm's fp32 squares and pairwise sums differ from an exact sum by at
+ * most a few units in the 24th bit, so c is within ~2e-7 relative of the
+ * exactly rounded coefficient.  Errors: as dopt_step.
+ */
+int dopt_step_clipped(const dopt_layout *layout, const dopt_adam_cfg *cfg, int64_t step,
+                      float max_norm, const void *const *grad_replicas, dopt_dtype grad_dtype,
+                      float *master, float *exp_avg, float *exp_avg_sq,
+                      void *const *param_replicas, uint32_t flags, float *main_grad,
+                      void *workspace, float *norm_out, cudaStream_t stream);
+
 /* Text of the last error raised on the calling thread ("" if none). */
 const char *dopt_last_error(void);
 

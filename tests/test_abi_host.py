@@ -167,3 +167,23 @@ def test_binding_refuses_cpu_tensors(lib):
     t = torch.zeros(16)
     with pytest.raises(B.DoptError):
         B.dopt_step(L, B.AdamConfig(), 1, [t.bfloat16()], t, t.clone(), t.clone(), [t.bfloat16()])
+
+
+def test_clipped_step_argument_checks_before_cuda(lib):
+    L = _lib_layout([100, 30], 2, 0, 8)
+    cfg = B.AdamConfig().to_c()
+    gp = (ctypes.c_void_p * 2)(0x10000, 0x20000)
+
+    def call(max_norm=1.0, main=0x70000, ws=0x80000, norm_out=None):
+        return B.lib().dopt_step_clipped(L.handle, ctypes.byref(cfg), 1, max_norm, gp, 0,
+                                         0x30000, 0x40000, 0x50000, gp, 1, main, ws, norm_out,
+                                         None)
+
+    assert call(main=None) == B.DOPT_E_ARG
+    assert call(ws=None) == B.DOPT_E_ARG
+    assert call(max_norm=0.0) == B.DOPT_E_ARG
+    assert call(max_norm=float("inf")) == B.DOPT_E_ARG
+    assert call(ws=0x80004) == B.DOPT_E_ALIGN
+    assert call(main=0x70004) == B.DOPT_E_ALIGN
+    assert call(norm_out=0x90004) == B.DOPT_E_ALIGN
+    assert call() in (B.DOPT_E_STATE, B.DOPT_E_CUDA)

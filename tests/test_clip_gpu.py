@@ -1,0 +1,176 @@
+"""Parity of the clipped step (global grad-norm clipping before AdamW) with
+the oracle.
+
+The oracle's norm^2 is an fp64 sum in piece order; the device sums fp32
+squares pairwise per 8 elements and then in fp64, so the two norms differ by
+at most a few units in the 24th bit (relative error <= 4 * 2^-24 from the
+square and the three pairwise additions).  The coefficient therefore agrees
+to ~2e-7 relative, a clipped grad to an ulp or two, which keeps master/m/v
+inside the 1e-6 relative (+1e-7) tolerance and params inside 1 bf16 ulp."""
+from dataclasses import asdict
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity import assert_bf16_close, assert_f32_close, sample_windows, t2np_bf16, t2np_f32
+from zero_distributed_optimizer_gb300 import binding as B
+from zero_distributed_optimizer_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+NORM_RTOL = 1e-6
+
+
+def _run_small(sizes, wd, D, bucket, pad, grad_dtype, steps, clip_frac, seed):
+    L = B.dopt_build_range_map(sizes, D, bucket, pad, wd).to_device()
+    N = L.padded_numel
+    master, m, v, params, grads = W.random_case(N, D, steps, grad_dtype, seed)
+    h = [master.numpy().copy(), m.numpy().copy(), v.numpy().copy()]
+    hp = [t2np_bf16(p).copy() for p in params]
+    d = [master.to(DEV), m.to(DEV), v.to(DEV)]
+    dp = [p.to(DEV) for p in params]
+    mg = torch.full((N,), -9.0, device=DEV)
+    hmg = np.full(N, -9.0, np.float32)
+    ws = B.clip_workspace(DEV)
+    norm_out = torch.zeros(2, device=DEV)
+    adam = B.AdamConfig(grad_scale=1.0 / D)
+    oadam = oracle.make_adam(**asdict(adam))
+    for i in range(steps):
+        t = i + 1
+        hg = [t2np_bf16(g) if grad_dtype == "bf16" else g.numpy().copy() for g in grads[i]]
+        nsq = oracle.grad_norm_sq(sizes, D, bucket, pad, adam.grad_scale, hg)
+        max_norm = clip_frac * float(np.sqrt(nsq)) if nsq > 0 else 1.0
+        coef = oracle.clip_coef(nsq, max_norm)
+        B.dopt_step_clipped(L, adam, t, max_norm, [g.to(DEV) for g in grads[i]], *d, dp, mg, ws,
+                            norm_out=norm_out)
+        oracle.step(sizes, wd, D, bucket, pad, oadam, t, hg, *h, hp, main_grad_out=hmg,
+                    clip_coef=coef)
+        torch.cuda.synchronize()
+        got_norm, got_coef = norm_out.tolist()
+        assert abs(got_norm - np.sqrt(nsq)) <= NORM_RTOL * np.sqrt(nsq) + 1e-30
+        assert abs(got_coef - coef) <= NORM_RTOL * coef
+        if clip_frac >= 1.0:
+            assert got_coef == 1.0 and coef == 1.0
+    assert_f32_close(t2np_f32(d[0]), h[0], "master")
+    assert_f32_close(t2np_f32(d[1]), h[1], "exp_avg")
+    assert_f32_close(t2np_f32(d[2]), h[2], "exp_avg_sq")
+    assert_f32_close(t2np_f32(mg), hmg, "main_grad")
+    for r in range(D):
+        assert_bf16_close(t2np_bf16(dp[r]), hp[r], f"param{r}")
+
+
+CLIP_CASES = [
+    ([130, 260, 90, 310, 210], None, 4, 0, 1),
+    ([5000, 1, 7, 300, 20000, 3, 9999], [1, 0, 1, 0, 1, 1, 0], 8, 0, 1),
+    ([4096, 333, 12345, 8, 77777], [0, 1, 1, 0, 1], 3, 20000, 1),
+    ([65536, 1000, 65536], [1, 0, 1], 16, 0, 64),
+    ([123457, 99], [1, 0], 64, 0, 1),
+    ([64] * 300 + [5000], None, 2, 4096, 64),
+    ([600000, 17, 300001], [1, 0, 1], 8, 400000, 64),  # many CTAs' partials
+]
+
+
+@pytest.mark.parametrize("grad_dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("case", range(len(CLIP_CASES)))
+def test_clipped_parity_small(case, grad_dtype):
+    sizes, wd, D, bucket, pad = CLIP_CASES[case]
+    _run_small(sizes, wd, D, bucket, pad, grad_dtype, steps=2, clip_frac=0.3, seed=100 + case)
+
+
+def test_no_clipping_when_norm_is_small():
+    sizes, wd, D = [20000, 7, 3000], [1, 0, 1], 4
+    _run_small(sizes, wd, D, 0, 8, "bf16", steps=2, clip_frac=4.0, seed=7)
+
+
+def test_clipped_with_large_max_norm_equals_plain_step():
+    """A coefficient of exactly 1 gives the plain step bit for bit."""
+    sizes, wd, D = [50000, 13, 7001], [1, 0, 1], 8
+    L = B.dopt_build_range_map(sizes, D, 0, 64, wd).to_device()
+    N = L.padded_numel
+    master, m, v, params, grads = W.random_case(N, D, 1, "bf16", 3)
+    a = [master.to(DEV), m.to(DEV), v.to(DEV)]
+    b = [x.clone() for x in a]
+    pa = [p.to(DEV) for p in params]
+    pb = [p.clone() for p in pa]
+    g = [x.to(DEV) for x in grads[0]]
+    adam = B.AdamConfig(grad_scale=0.125)
+    B.dopt_step(L, adam, 1, g, *a, pa)
+    B.dopt_step_clipped(L, adam, 1, 1e30, g, *b, pb, torch.empty(N, device=DEV),
+                        B.clip_workspace(DEV))
+    torch.cuda.synchronize()
+    for x, y in zip(a + pa, b + pb):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+
+
+def test_clipped_workspace_reuse_and_side_stream():
+    """The workspace is reset by every call: repeated calls on one workspace,
+    on a side stream, give the same result as fresh workspaces."""
+    sizes, wd, D = [300000, 5, 70000], [1, 0, 1], 4
+    L = B.dopt_build_range_map(sizes, D, 0, 8, wd).to_device()
+    N = L.padded_numel
+    master, m, v, params, grads = W.random_case(N, D, 3, "bf16", 4)
+    a = [master.to(DEV), m.to(DEV), v.to(DEV)]
+    b = [x.clone() for x in a]
+    pa = [p.to(DEV) for p in params]
+    pb = [p.clone() for p in pa]
+    mg = torch.empty(N, device=DEV)
+    ws = B.clip_workspace(DEV)
+    s = torch.cuda.Stream()
+    adam = B.AdamConfig(grad_scale=0.25)
+    for i in range(3):
+        g = [x.to(DEV) for x in grads[i]]
+        B.dopt_step_clipped(L, adam, i + 1, 0.01, g, *a, pa, mg, B.clip_workspace(DEV))
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            B.dopt_step_clipped(L, adam, i + 1, 0.01, g, *b, pb, mg, ws, stream=s)
+        s.synchronize()
+    for x, y in zip(a + pa, b + pb):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+
+
+def test_clipped_gpt2_small_full_size():
+    """The GPT-2-small layout at full size, 3 steps with clipping engaged:
+    the oracle computes the global norm over the whole buffer and steps
+    sampled windows."""
+    w = W.gpt2_small()
+    steps = 3
+    L = B.dopt_build_range_map(list(w.sizes), w.D, w.bucket_elems, w.pad_unit,
+                               list(w.wd_mask)).to_device()
+    O = oracle.range_map(list(w.sizes), w.D, w.bucket_elems, w.pad_unit)
+    N = L.padded_numel
+    wins = sample_windows(L.buckets(), O.pieces, N, seed=77, n_edges=24, n_random=6)
+    master, m, v = W.make_state(w, N, DEV)
+    params = W.make_params(master, w.D)
+    host = [[t2np_f32(master[a:b]).copy(), t2np_f32(m[a:b]).copy(), t2np_f32(v[a:b]).copy(),
+             [t2np_bf16(p[a:b]).copy() for p in params]] for a, b in wins]
+    mg = torch.empty(N, device=DEV)
+    ws = B.clip_workspace(DEV)
+    norm_out = torch.zeros(2, device=DEV)
+    adam = B.AdamConfig(**w.adam_kwargs())
+    oadam = oracle.make_adam(**asdict(adam))
+    for t in range(1, steps + 1):
+        grads = W.make_grads(w, N, t, DEV)
+        hg_full = [t2np_bf16(g) for g in grads]
+        nsq = oracle.grad_norm_sq(list(w.sizes), w.D, w.bucket_elems, w.pad_unit, w.grad_scale,
+                                  hg_full)
+        max_norm = 0.5 * float(np.sqrt(nsq))
+        coef = oracle.clip_coef(nsq, max_norm)
+        B.dopt_step_clipped(L, adam, t, max_norm, grads, master, m, v, params, mg, ws,
+                            norm_out=norm_out)
+        for (a, b), hs in zip(wins, host):
+            oracle.step(list(w.sizes), list(w.wd_mask), w.D, w.bucket_elems, w.pad_unit, oadam, t,
+                        [x[a:b].copy() for x in hg_full], hs[0], hs[1], hs[2], hs[3],
+                        window=(a, b), clip_coef=coef)
+        torch.cuda.synchronize()
+        got_norm, got_coef = norm_out.tolist()
+        assert abs(got_norm - np.sqrt(nsq)) <= NORM_RTOL * np.sqrt(nsq)
+        assert abs(got_coef - coef) <= NORM_RTOL * coef
+        del grads, hg_full
+    for (a, b), hs in zip(wins, host):
+        assert_f32_close(t2np_f32(master[a:b]), hs[0], f"master[{a}:{b}]")
+        assert_f32_close(t2np_f32(m[a:b]), hs[1], f"m[{a}:{b}]")
+        assert_f32_close(t2np_f32(v[a:b]), hs[2], f"v[{a}:{b}]")
+        for r in range(w.D):
+            assert_bf16_close(t2np_bf16(params[r][a:b]), hs[3][r], f"param{r}[{a}:{b}]")

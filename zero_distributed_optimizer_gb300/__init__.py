@@ -6,6 +6,7 @@ The library is loaded on first use and every call raises if it is missing.
 """
 from .binding import (  # noqa: F401
     DOPT_BF16,
+    DOPT_CLIP_WORKSPACE_BYTES,
     DOPT_E_ALIGN,
     DOPT_E_ARG,
     DOPT_E_CUDA,
@@ -22,6 +23,8 @@ from .binding import (  # noqa: F401
     dopt_build_range_map,
     dopt_gather,
     dopt_step,
+    dopt_step_clipped,
+    clip_workspace,
     step_from_host,
     version,
 )

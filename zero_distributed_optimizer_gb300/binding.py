@@ -29,6 +29,7 @@ DOPT_MAX_D = 64
 DOPT_BF16 = 0
 DOPT_FP32 = 1
 DOPT_STEP_GATHER = 1
+DOPT_CLIP_WORKSPACE_BYTES = 16384
 
 _ERROR_NAMES = {DOPT_E_ARG: "DOPT_E_ARG", DOPT_E_LAYOUT: "DOPT_E_LAYOUT",
                 DOPT_E_ALIGN: "DOPT_E_ALIGN", DOPT_E_CUDA: "DOPT_E_CUDA",
@@ -88,6 +89,10 @@ def _declare(lib):
     lib.dopt_step.restype = ctypes.c_int
     lib.dopt_step.argtypes = [vp, P(dopt_adam_cfg), ctypes.c_int64, P(vp), ctypes.c_int, vp, vp,
                               vp, P(vp), ctypes.c_uint32, vp, vp]
+    lib.dopt_step_clipped.restype = ctypes.c_int
+    lib.dopt_step_clipped.argtypes = [vp, P(dopt_adam_cfg), ctypes.c_int64, ctypes.c_float, P(vp),
+                                      ctypes.c_int, vp, vp, vp, P(vp), ctypes.c_uint32, vp, vp,
+                                      vp, vp]
     lib.dopt_gather.restype = ctypes.c_int
     lib.dopt_gather.argtypes = [vp, P(vp), vp]
     lib.dopt_last_error.restype = ctypes.c_char_p
@@ -274,6 +279,57 @@ def dopt_step(layout: Layout, adam: AdamConfig, step: int, grad_replicas, master
             DOPT_BF16 if gdt == torch.bfloat16 else DOPT_FP32, master.data_ptr(),
             exp_avg.data_ptr(), exp_avg_sq.data_ptr(), pp, DOPT_STEP_GATHER if gather else 0,
             None if main_grad_out is None else main_grad_out.data_ptr(), _stream_handle(stream)))
+
+
+def clip_workspace(device=None):
+    """A device workspace for dopt_step_clipped (DOPT_CLIP_WORKSPACE_BYTES)."""
+    import torch
+
+    return torch.zeros(DOPT_CLIP_WORKSPACE_BYTES, dtype=torch.uint8,
+                       device=device if device is not None else "cuda")
+
+
+def dopt_step_clipped(layout: Layout, adam: AdamConfig, step: int, max_norm: float,
+                      grad_replicas, master, exp_avg, exp_avg_sq, param_replicas, main_grad,
+                      workspace, gather: bool = True, norm_out=None, stream=None) -> None:
+    """The step with global grad-norm clipping (two launches).
+
+    main_grad: fp32 CUDA tensor of >= padded_numel elements (receives the
+    reduced grads before clipping); workspace: from :func:`clip_workspace`;
+    norm_out: optional fp32 CUDA tensor of 2 elements (norm, coefficient).
+    """
+    import torch
+
+    D = layout.D
+    if len(grad_replicas) != D or len(param_replicas) != D:
+        raise DoptError(DOPT_E_ARG, f"need {D} grad and {D} param replicas")
+    N = layout.padded_numel
+    device = master.device
+    if device.type != "cuda":
+        raise DoptError(DOPT_E_ARG, "dopt_step_clipped needs CUDA tensors (no CPU path exists)")
+    gdt = grad_replicas[0].dtype
+    if gdt not in (torch.bfloat16, torch.float32):
+        raise DoptError(DOPT_E_ARG, f"grad dtype {gdt} is not bf16 or fp32")
+    for i, g in enumerate(grad_replicas):
+        _check_tensor(g, f"grad_replicas[{i}]", gdt, N, device)
+    for name, t in (("master", master), ("exp_avg", exp_avg), ("exp_avg_sq", exp_avg_sq),
+                    ("main_grad", main_grad)):
+        _check_tensor(t, name, torch.float32, N, device)
+    for i, p in enumerate(param_replicas):
+        _check_tensor(p, f"param_replicas[{i}]", torch.bfloat16, N, device)
+    _check_tensor(workspace, "workspace", torch.uint8, DOPT_CLIP_WORKSPACE_BYTES, device)
+    if norm_out is not None:
+        _check_tensor(norm_out, "norm_out", torch.float32, 2, device)
+    gp = (ctypes.c_void_p * D)(*[g.data_ptr() for g in grad_replicas])
+    pp = (ctypes.c_void_p * D)(*[p.data_ptr() for p in param_replicas])
+    cfg = adam.to_c()
+    with torch.cuda.device(device):
+        _check(lib().dopt_step_clipped(
+            layout.handle, ctypes.byref(cfg), int(step), float(max_norm), gp,
+            DOPT_BF16 if gdt == torch.bfloat16 else DOPT_FP32, master.data_ptr(),
+            exp_avg.data_ptr(), exp_avg_sq.data_ptr(), pp, DOPT_STEP_GATHER if gather else 0,
+            main_grad.data_ptr(), workspace.data_ptr(),
+            None if norm_out is None else norm_out.data_ptr(), _stream_handle(stream)))
 
 
 def dopt_gather(layout: Layout, param_replicas, stream=None) -> None:

@@ -23,6 +23,7 @@
 // (__fmul_rn, __fadd_rn, __fsub_rn, __fdiv_rn, __fsqrt_rn), so no multiply
 // and add are fused and divide and square root are IEEE; the rank order of
 // the reduction is the loop order.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 
@@ -35,6 +36,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kVec = 8;
+constexpr int kMaxClipCtas = 1024;
 static_assert(kThreads * kVec == kDoptTileElems, "tile size must match the host table");
 
 struct Scalars {
@@ -48,6 +50,8 @@ struct StepArgs {
     float *exp_avg;
     float *exp_avg_sq;
     float *main_grad_out;
+    const float *main_grad_in;  // clipped step: the reduced grads
+    const float *clip_coef;     // clipped step: device scalar
     const int64_t *run_start;
     const int64_t *run_end;
     const int32_t *run_meta;
@@ -57,6 +61,34 @@ struct StepArgs {
     int32_t D;
     int32_t gather;
     Scalars sc;
+};
+
+// Workspace of the clipped step (device memory, DOPT_CLIP_WORKSPACE_BYTES).
+struct ClipWorkspace {
+    unsigned int ticket;  // CTAs done; zeroed before every launch
+    unsigned int pad0;
+    double norm_sq;
+    float norm;
+    float coef;
+    unsigned char pad1[40];
+    double partial[kMaxClipCtas];
+};
+static_assert(sizeof(ClipWorkspace) <= DOPT_CLIP_WORKSPACE_BYTES, "workspace size");
+
+struct NormArgs {
+    const void *grads[DOPT_MAX_D];
+    float *main_grad;
+    ClipWorkspace *ws;
+    float *norm_out;
+    const int64_t *run_start;
+    const int64_t *run_end;
+    const int32_t *tile_run;
+    int64_t numel;
+    int64_t n_tiles;
+    int32_t n_runs;
+    int32_t D;
+    float scale;
+    float max_norm;
 };
 
 struct GatherArgs {
@@ -172,9 +204,9 @@ struct GradVec<float> {
 };
 
 // Scaled rank-order fp32 reduction of 8 elements over the D replicas.
-template <typename G, int DC>
-__device__ __forceinline__ void reduce_vec(const StepArgs &a, int64_t e0, float (&acc)[8]) {
-    const float scale = a.sc.scale;
+template <typename G, int DC, typename Args>
+__device__ __forceinline__ void reduce_vec(const Args &a, float scale, int64_t e0,
+                                           float (&acc)[8]) {
     if constexpr (DC > 0) {
         GradVec<G> g[DC];
 #pragma unroll
@@ -211,11 +243,32 @@ __device__ __forceinline__ void reduce_vec(const StepArgs &a, int64_t e0, float 
     }
 }
 
-// A vector of 8 owned elements of one run.
-template <typename G, int DC>
+// Scaled rank-order fp32 reduction of one element over the D replicas.
+template <typename G>
+__device__ __forceinline__ float reduce_scalar(const void *const *grads, int D, float scale,
+                                               int64_t e) {
+    float g = 0.0f;
+    for (int r = 0; r < D; ++r) {
+        const float x = __fmul_rn(scale, load_grad_scalar<G>(grads[r], e));
+        g = r == 0 ? x : __fadd_rn(g, x);
+    }
+    return g;
+}
+
+// A vector of 8 owned elements of one run.  kFromMain: the reduced grads
+// come from main_grad_in, times the clipping coefficient.
+template <typename G, int DC, bool kFromMain>
 __device__ __forceinline__ void full_vector(const StepArgs &a, int64_t e0, int32_t meta) {
     float acc[8];
-    reduce_vec<G, DC>(a, e0, acc);
+    if constexpr (kFromMain) {
+        const float coef = *a.clip_coef;
+        const float4 g0 = ld_stream_f4(a.main_grad_in + e0), g1 = ld_stream_f4(a.main_grad_in + e0 + 4);
+        const float f[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc[k] = __fmul_rn(f[k], coef);
+    } else {
+        reduce_vec<G, DC>(a, a.sc.scale, e0, acc);
+    }
 
     const float4 w0 = ld_stream_f4(a.master + e0), w1 = ld_stream_f4(a.master + e0 + 4);
     const float4 m0 = ld_stream_f4(a.exp_avg + e0), m1 = ld_stream_f4(a.exp_avg + e0 + 4);
@@ -233,7 +286,7 @@ __device__ __forceinline__ void full_vector(const StepArgs &a, int64_t e0, int32
     st_stream_f4(a.exp_avg + e0 + 4, make_float4(m[4], m[5], m[6], m[7]));
     st_stream_f4(a.exp_avg_sq + e0, make_float4(v[0], v[1], v[2], v[3]));
     st_stream_f4(a.exp_avg_sq + e0 + 4, make_float4(v[4], v[5], v[6], v[7]));
-    if (a.main_grad_out) {
+    if (!kFromMain && a.main_grad_out) {
         st_stream_f4(a.main_grad_out + e0, make_float4(acc[0], acc[1], acc[2], acc[3]));
         st_stream_f4(a.main_grad_out + e0 + 4, make_float4(acc[4], acc[5], acc[6], acc[7]));
     }
@@ -256,7 +309,7 @@ __device__ __forceinline__ void full_vector(const StepArgs &a, int64_t e0, int32
 }
 
 // A vector that straddles a run edge: element by element, owned ones only.
-template <typename G, int DC>
+template <typename G, int DC, bool kFromMain>
 __device__ __noinline__ void mixed_vector(const StepArgs &a, int64_t e0, int j) {
     const int D = DC > 0 ? DC : a.D;
     for (int k = 0; k < kVec; ++k) {
@@ -266,17 +319,17 @@ __device__ __noinline__ void mixed_vector(const StepArgs &a, int64_t e0, int j) 
         if (j >= a.n_runs) return;
         if (a.run_start[j] > e) continue;  // padding
         const int32_t meta = a.run_meta[j];
-        float g = 0.0f;
-        for (int r = 0; r < D; ++r) {
-            const float x = __fmul_rn(a.sc.scale, load_grad_scalar<G>(a.grads[r], e));
-            g = r == 0 ? x : __fadd_rn(g, x);
-        }
+        float g;
+        if constexpr (kFromMain)
+            g = __fmul_rn(a.main_grad_in[e], *a.clip_coef);
+        else
+            g = reduce_scalar<G>(a.grads, D, a.sc.scale, e);
         float w = a.master[e], m = a.exp_avg[e], v = a.exp_avg_sq[e];
         adamw(a.sc, (meta & kRunDecays) ? a.sc.decay : 1.0f, g, w, m, v);
         a.master[e] = w;
         a.exp_avg[e] = m;
         a.exp_avg_sq[e] = v;
-        if (a.main_grad_out) a.main_grad_out[e] = g;
+        if (!kFromMain && a.main_grad_out) a.main_grad_out[e] = g;
         const uint16_t bits = to_bf16_bits(w);
         if (a.gather) {
             for (int r = 0; r < D; ++r) static_cast<uint16_t *>(a.params[r])[e] = bits;
@@ -286,7 +339,7 @@ __device__ __noinline__ void mixed_vector(const StepArgs &a, int64_t e0, int j) 
     }
 }
 
-template <typename G, int DC>
+template <typename G, int DC, bool kFromMain>
 __global__ void __launch_bounds__(kThreads) dopt_step_kernel(const __grid_constant__ StepArgs a) {
     const int64_t tile_begin = int64_t(blockIdx.x) * kDoptTileElems;
     const int lane = threadIdx.x & 31;
@@ -299,9 +352,91 @@ __global__ void __launch_bounds__(kThreads) dopt_step_kernel(const __grid_consta
     const int64_t rs = a.run_start[j];
     if (rs >= e0 + kVec) return;  // all padding
     if (rs <= e0 && e0 + kVec <= a.run_end[j])
-        full_vector<G, DC>(a, e0, a.run_meta[j]);
+        full_vector<G, DC, kFromMain>(a, e0, a.run_meta[j]);
     else
-        mixed_vector<G, DC>(a, e0, j);
+        mixed_vector<G, DC, kFromMain>(a, e0, j);
+}
+
+// Deterministic sum over a warp (fixed shuffle tree); the result is in lane 0.
+__device__ __forceinline__ double warp_sum(double v) {
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Pass 1 of the clipped step: the fused reduce-scatter writes the fp32 main
+// grads and every CTA accumulates the sum of their squares over the tiles it
+// visits (fp32 squares summed pairwise per 8-element vector, then one fp64
+// add per vector).  Each CTA leaves one fp64 partial; the CTA that finishes
+// last (atomic ticket, nobody waits) adds the partials in CTA order and
+// writes the norm and the clipping coefficient
+// min(1, max_norm / (norm + 1e-6)).
+template <typename G, int DC>
+__global__ void __launch_bounds__(kThreads) dopt_rs_norm_kernel(const __grid_constant__ NormArgs a) {
+    const int lane = threadIdx.x & 31;
+    double local = 0.0;
+    for (int64_t tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x) {
+        const int64_t tile_begin = tile * kDoptTileElems;
+        const int64_t warp_begin = tile_begin + int64_t(threadIdx.x & ~31) * kVec;
+        const int64_t e0 = tile_begin + int64_t(threadIdx.x) * kVec;
+        int j = warp_first_run(a.run_end, a.n_runs, a.tile_run[tile], warp_begin, lane);
+        if (e0 >= a.numel) continue;
+        while (j < a.n_runs && a.run_end[j] <= e0) ++j;
+        if (j >= a.n_runs || a.run_start[j] >= e0 + kVec) continue;
+        if (a.run_start[j] <= e0 && e0 + kVec <= a.run_end[j]) {
+            float acc[8];
+            reduce_vec<G, DC>(a, a.scale, e0, acc);
+            st_stream_f4(a.main_grad + e0, make_float4(acc[0], acc[1], acc[2], acc[3]));
+            st_stream_f4(a.main_grad + e0 + 4, make_float4(acc[4], acc[5], acc[6], acc[7]));
+            float sq[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) sq[k] = __fmul_rn(acc[k], acc[k]);
+            const float s01 = __fadd_rn(sq[0], sq[1]), s23 = __fadd_rn(sq[2], sq[3]);
+            const float s45 = __fadd_rn(sq[4], sq[5]), s67 = __fadd_rn(sq[6], sq[7]);
+            local += double(__fadd_rn(__fadd_rn(s01, s23), __fadd_rn(s45, s67)));
+            continue;
+        }
+        const int D = DC > 0 ? DC : a.D;
+        for (int k = 0; k < kVec; ++k) {
+            const int64_t e = e0 + k;
+            if (e >= a.numel) break;
+            while (j < a.n_runs && a.run_end[j] <= e) ++j;
+            if (j >= a.n_runs) break;
+            if (a.run_start[j] > e) continue;
+            const float g = reduce_scalar<G>(a.grads, D, a.scale, e);
+            a.main_grad[e] = g;
+            local += double(__fmul_rn(g, g));
+        }
+    }
+    __shared__ double warp_part[kThreads / 32];
+    __shared__ bool last;
+    local = warp_sum(local);
+    if (lane == 0) warp_part[threadIdx.x >> 5] = local;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double cta = 0.0;
+        for (int w = 0; w < kThreads / 32; ++w) cta += warp_part[w];
+        a.ws->partial[blockIdx.x] = cta;
+        __threadfence();
+        last = atomicAdd(&a.ws->ticket, 1u) == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!last || threadIdx.x >= 32) return;
+    __threadfence();
+    double v = 0.0;
+    for (int i = lane; i < int(gridDim.x); i += 32) v += __ldcg(&a.ws->partial[i]);
+    v = warp_sum(v);
+    if (lane == 0) {
+        const double norm = sqrt(v);
+        double coef = double(a.max_norm) / (norm + 1e-6);
+        if (coef > 1.0) coef = 1.0;
+        a.ws->norm_sq = v;
+        a.ws->norm = float(norm);
+        a.ws->coef = float(coef);
+        if (a.norm_out) {
+            a.norm_out[0] = float(norm);
+            a.norm_out[1] = float(coef);
+        }
+    }
 }
 
 __global__ void __launch_bounds__(kThreads) dopt_gather_kernel(const __grid_constant__ GatherArgs a) {
@@ -357,17 +492,47 @@ Scalars make_scalars(const dopt_adam_cfg &c, int64_t t) {
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 using StepKernel = void (*)(StepArgs);
+using NormKernel = void (*)(NormArgs);
 
-template <typename G>
+template <typename G, bool kFromMain>
 StepKernel pick_step_kernel(int D) {
     switch (D) {
-        case 1: return dopt_step_kernel<G, 1>;
-        case 2: return dopt_step_kernel<G, 2>;
-        case 4: return dopt_step_kernel<G, 4>;
-        case 8: return dopt_step_kernel<G, 8>;
-        case 16: return dopt_step_kernel<G, 16>;
-        default: return dopt_step_kernel<G, 0>;
+        case 1: return dopt_step_kernel<G, 1, kFromMain>;
+        case 2: return dopt_step_kernel<G, 2, kFromMain>;
+        case 4: return dopt_step_kernel<G, 4, kFromMain>;
+        case 8: return dopt_step_kernel<G, 8, kFromMain>;
+        case 16: return dopt_step_kernel<G, 16, kFromMain>;
+        default: return dopt_step_kernel<G, 0, kFromMain>;
     }
+}
+
+template <typename G>
+NormKernel pick_norm_kernel(int D) {
+    switch (D) {
+        case 1: return dopt_rs_norm_kernel<G, 1>;
+        case 2: return dopt_rs_norm_kernel<G, 2>;
+        case 4: return dopt_rs_norm_kernel<G, 4>;
+        case 8: return dopt_rs_norm_kernel<G, 8>;
+        case 16: return dopt_rs_norm_kernel<G, 16>;
+        default: return dopt_rs_norm_kernel<G, 0>;
+    }
+}
+
+// Grid of the persistent norm pass: every SM full, at most kMaxClipCtas.
+int norm_grid(NormKernel k, int64_t n_tiles, int device) {
+    int sms = 0, per_sm = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, 0) != cudaSuccess) {
+        cudaGetLastError();
+        sms = 1;
+        per_sm = 1;
+    }
+    // a whole number of CTAs per SM, so that every SM gets the same share
+    const int per_sm_cap = std::max(1, kMaxClipCtas / std::max(sms, 1));
+    int64_t g = int64_t(std::max(sms, 1)) * std::min(std::max(per_sm, 1), per_sm_cap);
+    g = std::min<int64_t>(g, kMaxClipCtas);
+    g = std::min<int64_t>(g, std::max<int64_t>(n_tiles, 1));
+    return int(g);
 }
 
 int check_device_tables(const dopt_layout *L, const char *who) {
@@ -381,41 +546,42 @@ int check_device_tables(const dopt_layout *L, const char *who) {
     return DOPT_OK;
 }
 
-}  // namespace
-
-extern "C" int dopt_step(const dopt_layout *L, const dopt_adam_cfg *cfg, int64_t step,
-                         const void *const *grad_replicas, dopt_dtype grad_dtype, float *master,
-                         float *exp_avg, float *exp_avg_sq, void *const *param_replicas,
-                         uint32_t flags, float *main_grad_out, cudaStream_t stream) {
+// Host checks shared by the step entry points; nothing is queued before
+// they pass.
+int check_step_args(const char *who, const dopt_layout *L, const dopt_adam_cfg *cfg,
+                    int64_t step, const void *const *grad_replicas, dopt_dtype grad_dtype,
+                    const float *master, const float *exp_avg, const float *exp_avg_sq,
+                    void *const *param_replicas, uint32_t flags, const float *main_grad) {
     using dopt::fail;
-    dopt::clear_error();
     if (!L || !cfg || !grad_replicas || !param_replicas || !master || !exp_avg || !exp_avg_sq)
-        return fail(DOPT_E_ARG, "dopt_step: NULL argument");
-    if (step < 1) return fail(DOPT_E_ARG, "dopt_step: step=%lld < 1", (long long)step);
+        return fail(DOPT_E_ARG, "%s: NULL argument", who);
+    if (step < 1) return fail(DOPT_E_ARG, "%s: step=%lld < 1", who, (long long)step);
     if (grad_dtype != DOPT_BF16 && grad_dtype != DOPT_FP32)
-        return fail(DOPT_E_ARG, "dopt_step: unknown grad dtype %d", int(grad_dtype));
+        return fail(DOPT_E_ARG, "%s: unknown grad dtype %d", who, int(grad_dtype));
     if (flags & ~uint32_t(DOPT_STEP_GATHER))
-        return fail(DOPT_E_ARG, "dopt_step: unknown flags 0x%x", flags);
+        return fail(DOPT_E_ARG, "%s: unknown flags 0x%x", who, flags);
     if (!(cfg->lr >= 0.0f) || !std::isfinite(cfg->lr) || !(cfg->beta1 >= 0.0f && cfg->beta1 < 1.0f) ||
         !(cfg->beta2 >= 0.0f && cfg->beta2 < 1.0f) || !(cfg->eps >= 0.0f) || !std::isfinite(cfg->eps) ||
         !(cfg->weight_decay >= 0.0f) || !std::isfinite(cfg->weight_decay) ||
         !std::isfinite(cfg->grad_scale))
-        return fail(DOPT_E_ARG, "dopt_step: hyper-parameter out of range");
+        return fail(DOPT_E_ARG, "%s: hyper-parameter out of range", who);
     const int D = L->cfg.D;
     for (int r = 0; r < D; ++r) {
         if (!grad_replicas[r] || !param_replicas[r])
-            return fail(DOPT_E_ARG, "dopt_step: replica %d pointer is NULL", r);
+            return fail(DOPT_E_ARG, "%s: replica %d pointer is NULL", who, r);
         if (!aligned16(grad_replicas[r]) || !aligned16(param_replicas[r]))
-            return fail(DOPT_E_ALIGN, "dopt_step: replica %d pointer is not 16-byte aligned", r);
+            return fail(DOPT_E_ALIGN, "%s: replica %d pointer is not 16-byte aligned", who, r);
     }
     if (!aligned16(master) || !aligned16(exp_avg) || !aligned16(exp_avg_sq) ||
-        (main_grad_out && !aligned16(main_grad_out)))
-        return fail(DOPT_E_ALIGN, "dopt_step: state pointer is not 16-byte aligned");
-    if (L->run_start.empty()) return DOPT_OK;  // nothing owned: nothing to do
-    int rc = check_device_tables(L, "dopt_step");
-    if (rc != DOPT_OK) return rc;
+        (main_grad && !aligned16(main_grad)))
+        return fail(DOPT_E_ALIGN, "%s: state pointer is not 16-byte aligned", who);
+    return DOPT_OK;
+}
 
-    StepArgs a{};
+void fill_step_args(StepArgs &a, const dopt_layout *L, const dopt_adam_cfg *cfg, int64_t step,
+                    const void *const *grad_replicas, float *master, float *exp_avg,
+                    float *exp_avg_sq, void *const *param_replicas, uint32_t flags) {
+    const int D = L->cfg.D;
     for (int r = 0; r < D; ++r) {
         a.grads[r] = grad_replicas[r];
         a.params[r] = param_replicas[r];
@@ -423,7 +589,6 @@ extern "C" int dopt_step(const dopt_layout *L, const dopt_adam_cfg *cfg, int64_t
     a.master = master;
     a.exp_avg = exp_avg;
     a.exp_avg_sq = exp_avg_sq;
-    a.main_grad_out = main_grad_out;
     a.run_start = L->d_run_start;
     a.run_end = L->d_run_end;
     a.run_meta = L->d_run_meta;
@@ -433,14 +598,106 @@ extern "C" int dopt_step(const dopt_layout *L, const dopt_adam_cfg *cfg, int64_t
     a.D = D;
     a.gather = (flags & DOPT_STEP_GATHER) ? 1 : 0;
     a.sc = make_scalars(*cfg, step);
+}
+
+// The two launches of the clipped step, with the workspace given as a
+// device address.
+int launch_clipped(const char *who, const dopt_layout *L, const dopt_adam_cfg *cfg,
+                   int64_t step, float max_norm, const void *const *grad_replicas,
+                   dopt_dtype grad_dtype, float *master, float *exp_avg, float *exp_avg_sq,
+                   void *const *param_replicas, uint32_t flags, float *main_grad,
+                   ClipWorkspace *ws, float *norm_out, cudaStream_t stream) {
+    using dopt::fail;
+    NormArgs na{};
+    const int D = L->cfg.D;
+    for (int r = 0; r < D; ++r) na.grads[r] = grad_replicas[r];
+    na.main_grad = main_grad;
+    na.ws = ws;
+    na.norm_out = norm_out;
+    na.run_start = L->d_run_start;
+    na.run_end = L->d_run_end;
+    na.tile_run = L->d_tile_run;
+    na.numel = L->numel;
+    na.n_tiles = (L->numel + kDoptTileElems - 1) / kDoptTileElems;
+    na.n_runs = int32_t(L->run_start.size());
+    na.D = D;
+    na.scale = cfg->grad_scale;
+    na.max_norm = max_norm;
+    NormKernel nk = grad_dtype == DOPT_BF16 ? pick_norm_kernel<__nv_bfloat16>(D)
+                                            : pick_norm_kernel<float>(D);
+    const int grid_a = norm_grid(nk, na.n_tiles, L->device);
+    cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(unsigned int), stream);
+    if (e != cudaSuccess) return fail(DOPT_E_CUDA, "%s: workspace reset: %s", who, cudaGetErrorString(e));
+    nk<<<grid_a, kThreads, 0, stream>>>(na);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(DOPT_E_CUDA, "%s: norm launch: %s", who, cudaGetErrorString(e));
+
+    StepArgs a{};
+    fill_step_args(a, L, cfg, step, grad_replicas, master, exp_avg, exp_avg_sq, param_replicas,
+                   flags);
+    a.main_grad_in = main_grad;
+    a.clip_coef = &ws->coef;
+    const unsigned grid = unsigned((L->numel + kDoptTileElems - 1) / kDoptTileElems);
+    StepKernel k = pick_step_kernel<float, true>(D);
+    k<<<grid, kThreads, 0, stream>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(DOPT_E_CUDA, "%s: step launch: %s", who, cudaGetErrorString(e));
+    return DOPT_OK;
+}
+
+}  // namespace
+
+extern "C" int dopt_step(const dopt_layout *L, const dopt_adam_cfg *cfg, int64_t step,
+                         const void *const *grad_replicas, dopt_dtype grad_dtype, float *master,
+                         float *exp_avg, float *exp_avg_sq, void *const *param_replicas,
+                         uint32_t flags, float *main_grad_out, cudaStream_t stream) {
+    using dopt::fail;
+    dopt::clear_error();
+    int rc = check_step_args("dopt_step", L, cfg, step, grad_replicas, grad_dtype, master,
+                             exp_avg, exp_avg_sq, param_replicas, flags, main_grad_out);
+    if (rc != DOPT_OK) return rc;
+    const int D = L->cfg.D;
+    if (L->run_start.empty()) return DOPT_OK;  // nothing owned: nothing to do
+    rc = check_device_tables(L, "dopt_step");
+    if (rc != DOPT_OK) return rc;
+
+    StepArgs a{};
+    fill_step_args(a, L, cfg, step, grad_replicas, master, exp_avg, exp_avg_sq, param_replicas,
+                   flags);
+    a.main_grad_out = main_grad_out;
 
     const unsigned grid = unsigned((L->numel + kDoptTileElems - 1) / kDoptTileElems);
-    StepKernel k = grad_dtype == DOPT_BF16 ? pick_step_kernel<__nv_bfloat16>(D)
-                                           : pick_step_kernel<float>(D);
+    StepKernel k = grad_dtype == DOPT_BF16 ? pick_step_kernel<__nv_bfloat16, false>(D)
+                                           : pick_step_kernel<float, false>(D);
     k<<<grid, kThreads, 0, stream>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(DOPT_E_CUDA, "dopt_step launch: %s", cudaGetErrorString(e));
     return DOPT_OK;
+}
+
+extern "C" int dopt_step_clipped(const dopt_layout *L, const dopt_adam_cfg *cfg, int64_t step,
+                                 float max_norm, const void *const *grad_replicas,
+                                 dopt_dtype grad_dtype, float *master, float *exp_avg,
+                                 float *exp_avg_sq, void *const *param_replicas, uint32_t flags,
+                                 float *main_grad, void *workspace, float *norm_out,
+                                 cudaStream_t stream) {
+    using dopt::fail;
+    dopt::clear_error();
+    int rc = check_step_args("dopt_step_clipped", L, cfg, step, grad_replicas, grad_dtype,
+                             master, exp_avg, exp_avg_sq, param_replicas, flags, main_grad);
+    if (rc != DOPT_OK) return rc;
+    if (!main_grad || !workspace)
+        return fail(DOPT_E_ARG, "dopt_step_clipped: main_grad and workspace are required");
+    if (!aligned16(workspace) || (norm_out && (reinterpret_cast<uintptr_t>(norm_out) & 7u)))
+        return fail(DOPT_E_ALIGN, "dopt_step_clipped: workspace or norm_out misaligned");
+    if (!(max_norm > 0.0f) || !std::isfinite(max_norm))
+        return fail(DOPT_E_ARG, "dopt_step_clipped: max_norm must be positive and finite");
+    if (L->run_start.empty()) return DOPT_OK;
+    rc = check_device_tables(L, "dopt_step_clipped");
+    if (rc != DOPT_OK) return rc;
+    return launch_clipped("dopt_step_clipped", L, cfg, step, max_norm, grad_replicas, grad_dtype,
+                          master, exp_avg, exp_avg_sq, param_replicas, flags, main_grad,
+                          static_cast<ClipWorkspace *>(workspace), norm_out, stream);
 }
 
 extern "C" int dopt_gather(const dopt_layout *L, void *const *param_replicas, cudaStream_t stream) {
