@@ -251,6 +251,53 @@ int dopt_step_clipped(const dopt_layout *layout, const dopt_adam_cfg *cfg, int64
                       void *const *param_replicas, uint32_t flags, float *main_grad,
                       void *workspace, float *norm_out, cudaStream_t stream);
 
+/* Size of the static device scratch behind dopt_step_clipped_noalloc. */
+#define DOPT_NOALLOC_SCRATCH_BYTES 16384
+
+/*
+ * dopt_step_clipped for callers that cannot allocate device memory on the
+ * step's path.  The pages have no counterpart: this entry point exists for
+ * such callers, not for the method.
+ *
+ * Who needs it: code whose device memory belongs to a framework's caching
+ * allocator (a raw cudaMalloc would bypass that allocator's budget and
+ * bookkeeping), and training loops that cannot take the device-wide
+ * synchronisation that cudaFree, and a cudaMalloc that has to grow the
+ * heap, can cause.  Such a caller cannot hand dopt_step_clipped a fresh
+ * workspace, so this variant keeps the norm pass's scratch (per-CTA partial
+ * sums, the finishing ticket, norm and coefficient) in a file-scope
+ * `static __device__` array of DOPT_NOALLOC_SCRATCH_BYTES inside the
+ * library.  Every GPU that loads the library holds that array until the
+ * process exits.
+ *
+ * The entry point calls no cudaMalloc, cudaFree or other allocating
+ * routine.  The caller still passes all inputs and outputs (main_grad
+ * included), and the layout's device tables must already be on the device
+ * (dopt_layout_to_device, which allocates, belongs to set-up).
+ *
+ * Set-up: the first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current and remembers it; make
+ * that first call on each device before any stream capture.
+ *
+ * Sharing: every call on a device uses the same array, which keeps the last
+ * call's contents.  Each call zeroes the ticket that must start at zero
+ * (a 4-byte cudaMemsetAsync on `stream`); the rest is overwritten before it
+ * is read.  Calls whose executions overlap on the GPU (other streams, other
+ * layouts, other threads) race on the array: the caller must order them.
+ *
+ * Limit: the norm pass needs 64 bytes plus 8 bytes per CTA, at most 1024
+ * CTAs (8,256 bytes), whatever the buffer size; a launch that would need
+ * more than DOPT_NOALLOC_SCRATCH_BYTES is refused with DOPT_E_ARG.
+ *
+ * Arguments, results and errors otherwise as dopt_step_clipped (without
+ * `workspace`).
+ */
+int dopt_step_clipped_noalloc(const dopt_layout *layout, const dopt_adam_cfg *cfg, int64_t step,
+                              float max_norm, const void *const *grad_replicas,
+                              dopt_dtype grad_dtype, float *master, float *exp_avg,
+                              float *exp_avg_sq, void *const *param_replicas, uint32_t flags,
+                              float *main_grad, float *norm_out, cudaStream_t stream);
+
 /* Text of the last error raised on the calling thread ("" if none). */
 const char *dopt_last_error(void);
 

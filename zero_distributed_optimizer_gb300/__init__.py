@@ -24,6 +24,7 @@ from .binding import (  # noqa: F401
     dopt_gather,
     dopt_step,
     dopt_step_clipped,
+    dopt_step_clipped_noalloc,
     clip_workspace,
     step_from_host,
     version,

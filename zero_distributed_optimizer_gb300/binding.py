@@ -93,6 +93,10 @@ def _declare(lib):
     lib.dopt_step_clipped.argtypes = [vp, P(dopt_adam_cfg), ctypes.c_int64, ctypes.c_float, P(vp),
                                       ctypes.c_int, vp, vp, vp, P(vp), ctypes.c_uint32, vp, vp,
                                       vp, vp]
+    lib.dopt_step_clipped_noalloc.restype = ctypes.c_int
+    lib.dopt_step_clipped_noalloc.argtypes = [vp, P(dopt_adam_cfg), ctypes.c_int64, ctypes.c_float,
+                                              P(vp), ctypes.c_int, vp, vp, vp, P(vp),
+                                              ctypes.c_uint32, vp, vp, vp]
     lib.dopt_gather.restype = ctypes.c_int
     lib.dopt_gather.argtypes = [vp, P(vp), vp]
     lib.dopt_last_error.restype = ctypes.c_char_p
@@ -330,6 +334,47 @@ def dopt_step_clipped(layout: Layout, adam: AdamConfig, step: int, max_norm: flo
             exp_avg.data_ptr(), exp_avg_sq.data_ptr(), pp, DOPT_STEP_GATHER if gather else 0,
             main_grad.data_ptr(), workspace.data_ptr(),
             None if norm_out is None else norm_out.data_ptr(), _stream_handle(stream)))
+
+
+def dopt_step_clipped_noalloc(layout: Layout, adam: AdamConfig, step: int, max_norm: float,
+                              grad_replicas, master, exp_avg, exp_avg_sq, param_replicas,
+                              main_grad, gather: bool = True, norm_out=None, stream=None) -> None:
+    """dopt_step_clipped without a workspace argument, for callers that must
+    not allocate device memory on the step's path: the scratch lives in a
+    static device array inside libdopt.so, shared by every call on a device
+    (calls that overlap on the GPU race on it).  The first call on a device
+    looks up that array's address; make it before any stream capture."""
+    import torch
+
+    D = layout.D
+    if len(grad_replicas) != D or len(param_replicas) != D:
+        raise DoptError(DOPT_E_ARG, f"need {D} grad and {D} param replicas")
+    N = layout.padded_numel
+    device = master.device
+    if device.type != "cuda":
+        raise DoptError(DOPT_E_ARG, "dopt_step_clipped_noalloc needs CUDA tensors")
+    gdt = grad_replicas[0].dtype
+    if gdt not in (torch.bfloat16, torch.float32):
+        raise DoptError(DOPT_E_ARG, f"grad dtype {gdt} is not bf16 or fp32")
+    for i, g in enumerate(grad_replicas):
+        _check_tensor(g, f"grad_replicas[{i}]", gdt, N, device)
+    for name, t in (("master", master), ("exp_avg", exp_avg), ("exp_avg_sq", exp_avg_sq),
+                    ("main_grad", main_grad)):
+        _check_tensor(t, name, torch.float32, N, device)
+    for i, p in enumerate(param_replicas):
+        _check_tensor(p, f"param_replicas[{i}]", torch.bfloat16, N, device)
+    if norm_out is not None:
+        _check_tensor(norm_out, "norm_out", torch.float32, 2, device)
+    gp = (ctypes.c_void_p * D)(*[g.data_ptr() for g in grad_replicas])
+    pp = (ctypes.c_void_p * D)(*[p.data_ptr() for p in param_replicas])
+    cfg = adam.to_c()
+    with torch.cuda.device(device):
+        _check(lib().dopt_step_clipped_noalloc(
+            layout.handle, ctypes.byref(cfg), int(step), float(max_norm), gp,
+            DOPT_BF16 if gdt == torch.bfloat16 else DOPT_FP32, master.data_ptr(),
+            exp_avg.data_ptr(), exp_avg_sq.data_ptr(), pp, DOPT_STEP_GATHER if gather else 0,
+            main_grad.data_ptr(), None if norm_out is None else norm_out.data_ptr(),
+            _stream_handle(stream)))
 
 
 def dopt_gather(layout: Layout, param_replicas, stream=None) -> None:

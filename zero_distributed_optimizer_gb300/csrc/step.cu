@@ -25,7 +25,9 @@
 // the reduction is the loop order.
 #include <algorithm>
 #include <cmath>
+#include <cstddef>
 #include <cstdint>
+#include <mutex>
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -602,6 +604,10 @@ void fill_step_args(StepArgs &a, const dopt_layout *L, const dopt_adam_cfg *cfg,
 
 // The two launches of the clipped step, with the workspace given as a
 // device address.
+NormKernel norm_kernel_for(dopt_dtype grad_dtype, int D) {
+    return grad_dtype == DOPT_BF16 ? pick_norm_kernel<__nv_bfloat16>(D) : pick_norm_kernel<float>(D);
+}
+
 int launch_clipped(const char *who, const dopt_layout *L, const dopt_adam_cfg *cfg,
                    int64_t step, float max_norm, const void *const *grad_replicas,
                    dopt_dtype grad_dtype, float *master, float *exp_avg, float *exp_avg_sq,
@@ -623,8 +629,7 @@ int launch_clipped(const char *who, const dopt_layout *L, const dopt_adam_cfg *c
     na.D = D;
     na.scale = cfg->grad_scale;
     na.max_norm = max_norm;
-    NormKernel nk = grad_dtype == DOPT_BF16 ? pick_norm_kernel<__nv_bfloat16>(D)
-                                            : pick_norm_kernel<float>(D);
+    NormKernel nk = norm_kernel_for(grad_dtype, D);
     const int grid_a = norm_grid(nk, na.n_tiles, L->device);
     cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(unsigned int), stream);
     if (e != cudaSuccess) return fail(DOPT_E_CUDA, "%s: workspace reset: %s", who, cudaGetErrorString(e));
@@ -698,6 +703,75 @@ extern "C" int dopt_step_clipped(const dopt_layout *L, const dopt_adam_cfg *cfg,
     return launch_clipped("dopt_step_clipped", L, cfg, step, max_norm, grad_replicas, grad_dtype,
                           master, exp_avg, exp_avg_sq, param_replicas, flags, main_grad,
                           static_cast<ClipWorkspace *>(workspace), norm_out, stream);
+}
+
+// ---------------------------------------------------------------------------
+// dopt_step_clipped_noalloc: the same two launches with the scratch in a
+// static device array instead of a caller workspace (see dopt.h).
+// ---------------------------------------------------------------------------
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[DOPT_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void *g_scratch_address[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device.  In host code the array's name only stands for the symbol; the
+// kernels must get this address.
+int noalloc_scratch(int device, void **out) {
+    using dopt::fail;
+    if (device < 0 || device >= kMaxDevices)
+        return fail(DOPT_E_ARG, "dopt_step_clipped_noalloc: device %d out of range", device);
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!g_scratch_address[device]) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p)
+            return fail(DOPT_E_CUDA, "dopt_step_clipped_noalloc: cudaGetSymbolAddress: %s",
+                        cudaGetErrorString(e));
+        g_scratch_address[device] = p;
+    }
+    *out = g_scratch_address[device];
+    return DOPT_OK;
+}
+
+}  // namespace
+
+extern "C" int dopt_step_clipped_noalloc(const dopt_layout *L, const dopt_adam_cfg *cfg,
+                                         int64_t step, float max_norm,
+                                         const void *const *grad_replicas, dopt_dtype grad_dtype,
+                                         float *master, float *exp_avg, float *exp_avg_sq,
+                                         void *const *param_replicas, uint32_t flags,
+                                         float *main_grad, float *norm_out, cudaStream_t stream) {
+    using dopt::fail;
+    dopt::clear_error();
+    const char *who = "dopt_step_clipped_noalloc";
+    int rc = check_step_args(who, L, cfg, step, grad_replicas, grad_dtype, master, exp_avg,
+                             exp_avg_sq, param_replicas, flags, main_grad);
+    if (rc != DOPT_OK) return rc;
+    if (!main_grad) return fail(DOPT_E_ARG, "%s: main_grad is required", who);
+    if (norm_out && (reinterpret_cast<uintptr_t>(norm_out) & 7u))
+        return fail(DOPT_E_ALIGN, "%s: norm_out misaligned", who);
+    if (!(max_norm > 0.0f) || !std::isfinite(max_norm))
+        return fail(DOPT_E_ARG, "%s: max_norm must be positive and finite", who);
+    if (L->run_start.empty()) return DOPT_OK;
+    rc = check_device_tables(L, who);
+    if (rc != DOPT_OK) return rc;
+    const int64_t n_tiles = (L->numel + kDoptTileElems - 1) / kDoptTileElems;
+    const int grid_a = norm_grid(norm_kernel_for(grad_dtype, L->cfg.D), n_tiles, L->device);
+    const size_t need = offsetof(ClipWorkspace, partial) + size_t(grid_a) * sizeof(double);
+    if (need > sizeof(g_noalloc_scratch))
+        return fail(DOPT_E_ARG, "%s: the norm pass needs %zu bytes of scratch (%d CTAs), the "
+                    "static scratch holds %zu", who, need, grid_a, sizeof(g_noalloc_scratch));
+    void *scratch = nullptr;
+    rc = noalloc_scratch(L->device, &scratch);
+    if (rc != DOPT_OK) return rc;
+    return launch_clipped(who, L, cfg, step, max_norm, grad_replicas, grad_dtype, master, exp_avg,
+                          exp_avg_sq, param_replicas, flags, main_grad,
+                          static_cast<ClipWorkspace *>(scratch), norm_out, stream);
 }
 
 extern "C" int dopt_gather(const dopt_layout *L, void *const *param_replicas, cudaStream_t stream) {
