@@ -1,7 +1,7 @@
 """Run a few launches of the fused step on one workload, for profilers.
 
     python -m zero_distributed_optimizer_gb300.profcase --workload gpt2_small \
-        [--max-elems N] [--warmup W] [--launches K] [--gather-kernel]
+        [--max-elems N] [--warmup W] [--launches K] [--mode step|gather|clipped]
 
 --max-elems keeps the leading params of the workload whose total stays
 within N elements, so that a profiler capture can run on a smaller buffer of
@@ -50,8 +50,8 @@ def main(argv=None):
     ap.add_argument("--max-elems", type=int, default=0)
     ap.add_argument("--warmup", type=int, default=2)
     ap.add_argument("--launches", type=int, default=3)
-    ap.add_argument("--gather-kernel", action="store_true",
-                    help="time dopt_gather instead of the fused step")
+    ap.add_argument("--mode", choices=["step", "gather", "clipped"], default="step",
+                    help="the fused step, dopt_gather alone, or the clipped step")
     args = ap.parse_args(argv)
 
     libbuild.build()
@@ -69,6 +69,9 @@ def main(argv=None):
     params = W.make_params(master, w.D)
     grads = W.make_grads(w, N, 1, dev)
     adam = B.AdamConfig(**w.adam_kwargs())
+    if args.mode == "clipped":
+        main_grad = torch.empty(N, device=dev)
+        ws = B.clip_workspace(dev)
     torch.cuda.synchronize()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     t = 0
@@ -76,16 +79,20 @@ def main(argv=None):
         if i == args.warmup:
             ev[0].record()
         t += 1
-        if args.gather_kernel:
+        if args.mode == "gather":
             B.dopt_gather(L, params)
+        elif args.mode == "clipped":
+            B.dopt_step_clipped(L, adam, t, 1.0, grads, master, m, v, params, main_grad, ws)
         else:
             B.dopt_step(L, adam, t, grads, master, m, v, params)
     ev[1].record()
     torch.cuda.synchronize()
     ms = ev[0].elapsed_time(ev[1]) / max(args.launches, 1)
-    bytes_per = w.numel * (2 * w.D if args.gather_kernel else w.algorithmic_bytes_per_element())
+    per_elem = {"gather": 2 * w.D, "step": w.algorithmic_bytes_per_element(),
+                "clipped": w.algorithmic_bytes_per_element() + 8}[args.mode]
+    bytes_per = w.numel * per_elem
     print(json.dumps({"workload": w.name, "N": w.numel, "padded_numel": N, "D": w.D,
-                      "kernel": "dopt_gather_kernel" if args.gather_kernel else "dopt_step_kernel",
+                      "mode": args.mode,
                       "launches": args.launches, "ms_per_launch": ms,
                       "algorithmic_bytes_per_launch": bytes_per,
                       "gbs": bytes_per / (ms / 1e3) / 1e9}))
