@@ -115,6 +115,10 @@ def _declare(lib) -> None:
                                      ctypes.c_int32, ctypes.c_float, ctypes.c_int32,
                                      ctypes.POINTER(ctypes.c_void_p), ctypes.c_int64,
                                      ctypes.c_int64, ctypes.POINTER(ctypes.c_double)]
+    lib.orc_allreduce.restype = ctypes.c_int
+    lib.orc_allreduce.argtypes = [i64p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
+                                  ctypes.c_int32, ctypes.c_float, ctypes.c_int32,
+                                  ctypes.POINTER(ctypes.c_void_p), ctypes.c_int64, ctypes.c_int64]
     lib.orc_clip_coef.restype = ctypes.c_float
     lib.orc_clip_coef.argtypes = [ctypes.c_double, ctypes.c_float]
     lib.orc_f32_to_bf16.restype = ctypes.c_uint16
@@ -295,6 +299,28 @@ def grad_norm_sq(sizes, D: int, bucket_elems: int, pad_unit: int, grad_scale: fl
     if rc != ORC_OK:
         raise OracleError(f"orc_grad_norm_sq failed: {rc}")
     return float(out.value)
+
+
+def allreduce(sizes, D: int, bucket_elems: int, pad_unit: int, grad_scale: float, grads,
+              window=None, lib=None) -> None:
+    """All-reduce of the grads in place (page 1 §5 force_all_reduce; the
+    tutorial's AllReduce = reduce-scatter + all-gather): every replica gets
+    the reduced grad at every owned element, rounded to the grad type."""
+    lib = lib or load()
+    sizes_a, sizes_p = _i64(sizes)
+    grad_is_f32 = grads[0].dtype == np.float32
+    span = len(grads[0])
+    w0, w1 = (0, span) if window is None else (int(window[0]), int(window[1]))
+    if w1 - w0 != span or len(grads) != D:
+        raise OracleError("grads must be D arrays of the window length")
+    for g in grads:
+        if g.dtype != (np.float32 if grad_is_f32 else np.uint16) or not g.flags.c_contiguous:
+            raise OracleError("grads must be contiguous, all uint16 or all float32")
+    gp = (ctypes.c_void_p * D)(*[g.ctypes.data for g in grads])
+    rc = lib.orc_allreduce(sizes_p, len(sizes_a), D, bucket_elems, pad_unit, float(grad_scale),
+                           int(grad_is_f32), gp, w0, w1)
+    if rc != ORC_OK:
+        raise OracleError(f"orc_allreduce failed: {rc}")
 
 
 def clip_coef(norm_sq: float, max_norm: float, lib=None) -> float:

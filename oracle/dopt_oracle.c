@@ -67,6 +67,10 @@
  *      in double; the coefficient is min(1, max_norm / (norm + 1e-6)),
  *      evaluated in double and rounded to float once; each reduced grad is
  *      multiplied by it (one fp32 rounding) before Adam.
+ *  R10 force_all_reduce ([P1] §5) leaves the optimizer step unchanged (each
+ *      rank still updates its own shard from the same reduced grads) and
+ *      additionally gives every replica's grad buffer the whole reduced grad,
+ *      rounded to the grad type.
  *
  * Windows: the step can be restricted to global buffer indices [w0, w1).
  * All buffer-indexed arrays passed to orc_step are then window-relative
@@ -537,6 +541,106 @@ int orc_grad_norm_sq(const int64_t *sizes, int32_t n, int32_t D, int64_t bucket_
     }
     *out = sum;
 done:
+    free(pieces);
+    free(pstart);
+    free(pend);
+    free(pbucket);
+    free(bstart);
+    free(bend);
+    return rc;
+}
+
+/*
+ * All-reduce of the grads ([P1] §5, force_all_reduce: every rank keeps the
+ * whole reduced grad instead of its shard; [P2] "AllReduce": a
+ * reduce-scatter followed by an all-gather).  For every (bucket, rank) the
+ * shard is reduced as in the step (R5) and then written into every
+ * replica's grad buffer at the shard's owned elements, rounded to the grad
+ * type (R7 for bf16; fp32 stays as is) (R10).  Padding is not written.
+ * grads are window-relative and are overwritten.
+ */
+int orc_allreduce(const int64_t *sizes, int32_t n, int32_t D, int64_t bucket_elems,
+                  int32_t pad_unit, float grad_scale, int32_t grad_is_f32, void *const *grads,
+                  int64_t w0, int64_t w1)
+{
+    if (w0 < 0 || w1 < w0)
+        return ORC_E_ARG;
+    int rc = ORC_OK;
+    size_t cap = (size_t)(n > 0 ? n : 1);
+    int64_t *pstart = (int64_t *)malloc(cap * sizeof *pstart);
+    int64_t *pend = (int64_t *)malloc(cap * sizeof *pend);
+    int32_t *pbucket = (int32_t *)malloc(cap * sizeof *pbucket);
+    int64_t *bstart = (int64_t *)malloc(cap * sizeof *bstart);
+    int64_t *bend = (int64_t *)malloc(cap * sizeof *bend);
+    orc_piece *pieces = NULL;
+    float *shard = NULL;
+    int32_t nb = 0, npieces = 0;
+    int64_t numel = 0;
+    if (!pstart || !pend || !pbucket || !bstart || !bend) {
+        rc = ORC_E_NOMEM;
+        goto done;
+    }
+    rc = orc_layout(sizes, n, D, bucket_elems, pad_unit, pstart, pend, pbucket, bstart, bend,
+                    &nb, &numel);
+    if (rc != ORC_OK)
+        goto done;
+    if (w1 > numel) {
+        rc = ORC_E_ARG;
+        goto done;
+    }
+    pieces = (orc_piece *)malloc(((size_t)n + (size_t)D * (size_t)nb + 1) * sizeof *pieces);
+    if (!pieces) {
+        rc = ORC_E_NOMEM;
+        goto done;
+    }
+    rc = orc_pieces(n, pstart, pend, pbucket, nb, bstart, bend, D, pieces, &npieces);
+    if (rc != ORC_OK)
+        goto done;
+    int32_t first_piece = 0;
+    for (int32_t k = 0; k < nb; ++k) {
+        for (int32_t r = 0; r < D; ++r) {
+            orc_range mine = {0, 0};
+            rc = orc_rank_range(bstart[k], bend[k], D, r, &mine);
+            if (rc != ORC_OK)
+                goto done;
+            int64_t S = mine.end - mine.start;
+            /* reduce-scatter: rank r's shard */
+            free(shard);
+            shard = (float *)malloc((size_t)(S > 0 ? S : 1) * sizeof *shard);
+            if (!shard) {
+                rc = ORC_E_NOMEM;
+                goto done;
+            }
+            int64_t j_lo = orc_max(0, w0 - mine.start);
+            int64_t j_hi = orc_min(S, w1 - mine.start);
+            for (int64_t j = j_lo; j < j_hi; ++j)
+                shard[j] = orc_reduce_element((const void *const *)grads, grad_is_f32, D,
+                                              grad_scale, mine.start + j - w0);
+            int32_t last_piece = first_piece;
+            while (last_piece < npieces && pieces[last_piece].bucket_id == k &&
+                   pieces[last_piece].rank == r)
+                ++last_piece;
+            /* all-gather of the shard into every replica's grad buffer */
+            for (int32_t pi = first_piece; pi < last_piece; ++pi) {
+                const orc_piece *pc = &pieces[pi];
+                int64_t t_lo = orc_max(0, w0 - pc->gbuf_world.start);
+                int64_t t_hi = orc_min(pc->gbuf_world.end, w1) - pc->gbuf_world.start;
+                for (int64_t t = t_lo; t < t_hi; ++t) {
+                    int64_t i = pc->gbuf_world.start + t;
+                    float reduced = shard[pc->gbuf_local.start + t];
+                    for (int32_t q = 0; q < D; ++q) {
+                        if (grad_is_f32)
+                            ((float *)grads[q])[i - w0] = reduced;
+                        else
+                            ((uint16_t *)grads[q])[i - w0] = orc_f32_to_bf16(reduced);
+                    }
+                }
+            }
+            first_piece = last_piece;
+        }
+    }
+done:
+    free(shard);
     free(pieces);
     free(pstart);
     free(pend);

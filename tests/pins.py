@@ -644,6 +644,76 @@ def pin_clip_d_independence(lib):
             assert np.array_equal(b.view(np.uint32), d.view(np.uint32))
 
 
+# ---------------------------------------------------------------------------
+# All-reduce pins (page 1 §5 force_all_reduce; tutorial "AllReduce")
+# ---------------------------------------------------------------------------
+
+def pin_allreduce_every_rank(lib):
+    """Tutorial "AllReduce": [1,2], [2,3], [3,3] -> [6,8] on every rank, in
+    bf16 and in fp32 grad buffers; padding untouched."""
+    g = _golden("allreduce_example.json")
+    D = len(g["ranks_in"])
+    for dtype in ("bf16", "fp32"):
+        vals = [np.array(list(r) + [-2.0], np.float32) for r in g["ranks_in"]]
+        grads = [(_bf16_bits_of(x) if dtype == "bf16" else x.copy()) for x in vals]
+        oracle.allreduce([2], D, 0, 1, 1.0, grads, lib=lib)
+        for x in grads:
+            f = _bits_to_f32(x) if dtype == "bf16" else x
+            assert f[:2].tolist() == [float(v) for v in g["every_rank_out"]], f
+            assert f[2] == -2.0
+
+
+def pin_allreduce_is_rs_then_gather(lib, cases=30, seed=41):
+    """All-reduce equals the concatenated reduce-scatter shards copied to
+    every rank: each replica's buffer becomes the main grads the step
+    reports (exact integer inputs), and the step is unchanged by it."""
+    rng = np.random.default_rng(seed)
+    for sizes, D, bucket, pad in random_tiny_layouts(cases, seed):
+        if not sizes or sum(sizes) == 0:
+            continue
+        L = oracle.range_map(sizes, D, bucket, pad, lib=lib)
+        N = L.numel
+        ints = [rng.integers(-30, 31, N) for _ in range(D)]
+        grads = [_bf16_bits_of(x.astype(np.float32) / 4) for x in ints]
+        before = [x.copy() for x in grads]
+        master, m, v = _state(N, 5)
+        params = _params_from(master, D)
+        mg = np.full(N, 7.0, np.float32)
+        oracle.step(sizes, None, D, bucket, pad, oracle.make_adam(grad_scale=0.5), 1, grads,
+                    master, m, v, params, main_grad_out=mg, lib=lib)
+        oracle.allreduce(sizes, D, bucket, pad, 0.5, grads, lib=lib)
+        owned = np.zeros(N, bool)
+        for p in range(len(sizes)):
+            owned[L.param_start[p]:L.param_end[p]] = True
+        for x, x0 in zip(grads, before):
+            assert np.array_equal(_bits_to_f32(x)[owned], mg[owned])
+            assert np.array_equal(x[~owned], x0[~owned])
+
+
+def pin_allreduce_rounds_to_nearest_even(lib):
+    """The all-reduced bf16 buffer is the round-to-nearest-even of the fp32
+    reduced grads (PyTorch's conversion of the step's main grads), with sums
+    that need rounding."""
+    import torch
+
+    rng = np.random.default_rng(8)
+    sizes, D, pad = [500, 333], 3, 1
+    L = oracle.range_map(sizes, D, 0, pad, lib=lib)
+    N = L.numel
+    grads = [(rng.normal(0, 1, N).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+             for _ in range(D)]
+    master, m, v = _state(N, 9)
+    mg = np.zeros(N, np.float32)
+    oracle.step(sizes, None, D, 0, pad, oracle.make_adam(grad_scale=1.0), 1, grads, master, m, v,
+                _params_from(master, D), main_grad_out=mg, lib=lib)
+    oracle.allreduce(sizes, D, 0, pad, 1.0, grads, lib=lib)
+    want = torch.tensor(mg).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    n = sum(sizes)  # one bucket: the owned elements come first, then padding
+    assert np.count_nonzero(_bits_to_f32(want[:n]) != mg[:n]) > n // 4  # rounding happens
+    for x in grads:
+        assert np.array_equal(x[:n], want[:n])
+
+
 ALL_PINS = [
     pin_page1_ownership,
     pin_brute_force_range_maps,
@@ -661,4 +731,7 @@ ALL_PINS = [
     pin_clip_d1_matches_torch,
     pin_clip_off_equals_plain_step,
     pin_clip_d_independence,
+    pin_allreduce_every_rank,
+    pin_allreduce_is_rs_then_gather,
+    pin_allreduce_rounds_to_nearest_even,
 ]

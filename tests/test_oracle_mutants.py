@@ -48,6 +48,12 @@ MUTANTS = [
     ("local_range_from_bucket", "pc.gbuf_local = orc_normalize(pc.gbuf_world, x - mine.start);",
      "pc.gbuf_local = orc_normalize(pc.gbuf_world, x - bucket_start[k]);"),
     ("no_gather", "if (gather) {", "if (0) {"),
+    ("allreduce_skips_own_rank", "for (int32_t q = 0; q < D; ++q) {\n                        if (grad_is_f32)",
+     "for (int32_t q = 0; q < D; ++q) {\n                        if (q == r) continue;\n                        if (grad_is_f32)"),
+    ("allreduce_truncates_bf16", "((uint16_t *)grads[q])[i - w0] = orc_f32_to_bf16(reduced);",
+     "((uint16_t *)grads[q])[i - w0] = (uint16_t)(orc_f32_to_bits(reduced) >> 16);"),
+    ("allreduce_via_bucket_range", "float reduced = shard[pc->gbuf_local.start + t];",
+     "float reduced = shard[pc->gbuf_world_in_bucket.start + t];"),
     ("clip_not_applied", "float gc = g * clip_coef;", "float gc = g;"),
     ("norm_not_squared", "sum += g * g;", "sum += g < 0 ? -g : g;"),
     ("clip_no_sqrt", "double norm = sqrt(norm_sq);", "double norm = norm_sq;"),
