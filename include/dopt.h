@@ -207,6 +207,51 @@ int dopt_step(const dopt_layout *layout, const dopt_adam_cfg *cfg, int64_t step,
               float *main_grad_out, cudaStream_t stream);
 
 /*
+ * The step over the contiguous bucket range [first_bucket, first_bucket +
+ * n_buckets) only, one launch.  The per-bucket form of the distributed
+ * optimizer page's pipeline (§2, §4.2: each bucket's reduce-scatter starts
+ * as soon as the bucket is full, so its update can follow on its own): the
+ * caller may launch the buckets one by one, on one or several streams, in
+ * any order; together they give exactly dopt_step's result, since every
+ * element belongs to one bucket.  Arguments otherwise as dopt_step (buffers
+ * are still whole-buffer pointers).  n_buckets = 0 is a no-op.
+ * Errors: as dopt_step, and DOPT_E_ARG for a range outside the layout.
+ */
+int dopt_step_buckets(const dopt_layout *layout, const dopt_adam_cfg *cfg, int64_t step,
+                      int32_t first_bucket, int32_t n_buckets, const void *const *grad_replicas,
+                      dopt_dtype grad_dtype, float *master, float *exp_avg, float *exp_avg_sq,
+                      void *const *param_replicas, uint32_t flags, float *main_grad_out,
+                      cudaStream_t stream);
+
+/*
+ * The all-reduce of the grads on its own (page 1, §5, force_all_reduce: all
+ * ranks keep the whole reduced grad, e.g. to save full weight grads;
+ * distributed-training tutorial, "AllReduce" = reduce-scatter followed by
+ * all-gather).  For every owned element i:
+ *     g = fp32 sum over r in rank order of grad_scale * float(grad_replicas[r][i])
+ *     grad_replicas[r][i] = g rounded to the grad type (bf16: nearest even)
+ * for every r, in place.  Padding is not written.
+ *   grad_replicas  host array of D device pointers (16-byte aligned),
+ *                  padded_numel elements of grad_dtype each; read and written
+ * Asynchronous on `stream`.  Errors: DOPT_E_ARG, DOPT_E_ALIGN, DOPT_E_STATE,
+ * DOPT_E_CUDA.
+ */
+int dopt_allreduce(const dopt_layout *layout, void *const *grad_replicas, dopt_dtype grad_dtype,
+                   float grad_scale, cudaStream_t stream);
+
+/*
+ * dopt_step with force_all_reduce (page 1, §5): the same step, one launch,
+ * which also writes the reduced grad of every owned element into every grad
+ * replica, as dopt_allreduce does (the Adam update uses the fp32 reduced
+ * grad, unchanged).  grad_replicas are read and then written.  Arguments and
+ * errors otherwise as dopt_step.
+ */
+int dopt_step_allreduce(const dopt_layout *layout, const dopt_adam_cfg *cfg, int64_t step,
+                        void *const *grad_replicas, dopt_dtype grad_dtype, float *master,
+                        float *exp_avg, float *exp_avg_sq, void *const *param_replicas,
+                        uint32_t flags, float *main_grad_out, cudaStream_t stream);
+
+/*
  * The all-gather of the params on its own (page 1, §4.4): for every rank q
  * and every element q owns, copy param_replicas[q][i] into every other
  * replica.  Padding is not copied.  param_replicas: host array of D device

@@ -187,3 +187,28 @@ def test_clipped_step_argument_checks_before_cuda(lib):
     assert call(main=0x70004) == B.DOPT_E_ALIGN
     assert call(norm_out=0x90004) == B.DOPT_E_ALIGN
     assert call() in (B.DOPT_E_STATE, B.DOPT_E_CUDA)
+
+
+def test_bucket_and_allreduce_argument_checks_before_cuda(lib):
+    L = _lib_layout([100, 50, 60], 2, 40, 8)
+    assert L.n_buckets == 3
+    cfg = B.AdamConfig().to_c()
+    gp = (ctypes.c_void_p * 2)(0x10000, 0x20000)
+
+    def buckets(first, count):
+        return B.lib().dopt_step_buckets(L.handle, ctypes.byref(cfg), 1, first, count, gp, 0,
+                                         0x30000, 0x40000, 0x50000, gp, 1, None, None)
+
+    assert buckets(-1, 1) == B.DOPT_E_ARG
+    assert buckets(0, 4) == B.DOPT_E_ARG
+    assert buckets(3, 1) == B.DOPT_E_ARG
+    assert buckets(1, -1) == B.DOPT_E_ARG
+    assert buckets(3, 0) == B.DOPT_OK  # an empty range needs no device
+    assert buckets(1, 2) in (B.DOPT_E_STATE, B.DOPT_E_CUDA)
+    assert B.lib().dopt_allreduce(L.handle, gp, 5, 1.0, None) == B.DOPT_E_ARG
+    assert B.lib().dopt_allreduce(L.handle, gp, 0, float("nan"), None) == B.DOPT_E_ARG
+    bad = (ctypes.c_void_p * 2)(0x10000, 0x20008)
+    assert B.lib().dopt_allreduce(L.handle, bad, 0, 1.0, None) == B.DOPT_E_ALIGN
+    assert B.lib().dopt_allreduce(L.handle, gp, 0, 1.0, None) in (B.DOPT_E_STATE, B.DOPT_E_CUDA)
+    assert B.lib().dopt_step_allreduce(L.handle, ctypes.byref(cfg), 0, gp, 0, 0x30000, 0x40000,
+                                       0x50000, gp, 1, None, None) == B.DOPT_E_ARG

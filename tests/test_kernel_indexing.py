@@ -1,12 +1,14 @@
-"""CPU model of the step kernel's work split, checked before any GPU run.
+"""CPU model of the kernels' work split, checked before any GPU run.
 
-The model follows the kernel's decomposition: 2048-element tiles, a per-tile
-first-run index, a per-warp ballot over 32 run ends, a per-thread walk, the
-8-element vector path inside one run and the element path at run edges.  It
-checks that every owned element is visited exactly once, that no padding
-element is visited, and that every 8-element vector access lies inside the
-buffer.  The run table is rebuilt here from the pieces with the kernel's
-merge rule (touching pieces with the same owner rank and decay flag)."""
+The model follows the kernels' decomposition: a launch covers a run view
+(runs [run_begin, run_limit) and the tiles from tile0 that span them),
+2048-element tiles, a per-tile first-run index, a per-warp ballot over 32 run
+ends, a per-thread walk, the 8-element vector path inside one run and the
+element path at run edges.  It checks that every owned element of the view
+is visited exactly once, that nothing outside it is visited, and that every
+8-element vector access lies inside the buffer.  The run table is rebuilt
+here from the pieces with the library's rule (touching pieces of one bucket
+with the same owner rank and decay flag merge)."""
 import numpy as np
 import pytest
 
@@ -16,41 +18,55 @@ from zero_distributed_optimizer_gb300 import binding as B
 TILE, THREADS, VEC = 2048, 256, 8
 
 
-def runs_from_pieces(pieces, decays):
-    runs = []
+def runs_from_pieces(pieces, decays, n_buckets):
+    runs, bucket_run, last_bucket = [], [0] * (n_buckets + 1), -1
     for pc in pieces:
         meta = (1 if decays[pc["param_id"]] else 0) | (pc["rank"] << 8)
         a, b = pc["gbuf_world"]
-        if runs and runs[-1][1] == a and runs[-1][2] == meta:
+        if runs and runs[-1][1] == a and runs[-1][2] == meta and last_bucket == pc["bucket_id"]:
             runs[-1][1] = b
         else:
+            for k in range(last_bucket + 1, pc["bucket_id"] + 1):
+                bucket_run[k] = len(runs)
+            last_bucket = pc["bucket_id"]
             runs.append([a, b, meta])
-    return runs
+    for k in range(last_bucket + 1, n_buckets + 1):
+        bucket_run[k] = len(runs)
+    return runs, bucket_run
 
 
-def simulate(numel, runs):
-    nr = len(runs)
+def tile_index(numel, runs):
+    n_tiles = (numel + TILE - 1) // TILE
+    out, j = [], 0
+    for t in range(n_tiles + 1):
+        while j < len(runs) and runs[j][1] <= t * TILE:
+            j += 1
+        out.append(j)
+    return out
+
+
+def view(runs, bucket_run, first, count):
+    lo_run, hi_run = bucket_run[first], bucket_run[first + count]
+    if lo_run >= hi_run:
+        return lo_run, hi_run, 0, 0
+    tile0 = runs[lo_run][0] // TILE
+    tiles = (runs[hi_run - 1][1] + TILE - 1) // TILE - tile0
+    return lo_run, hi_run, tile0, tiles
+
+
+def simulate(numel, runs, tile_run, run_begin, run_limit, tile0, tiles, visits):
     start = [r[0] for r in runs]
     end = [r[1] for r in runs]
-    visits = np.zeros(numel, np.int32)
     vector_accesses = 0
-    n_tiles = (numel + TILE - 1) // TILE
-    tile_run = []
-    j = 0
-    for t in range(n_tiles + 1):
-        while j < nr and end[j] <= t * TILE:
-            j += 1
-        tile_run.append(j)
-    for tile in range(n_tiles):
+    for b in range(tiles):
+        tile = tile0 + b
+        assert tile < len(tile_run) - 1
         for warp in range(THREADS // 32):
             wb = tile * TILE + warp * 32 * VEC
-            j = tile_run[tile]
-            while True:
-                c = 0
-                for lane in range(32):
-                    idx = j + lane
-                    if idx < nr and end[idx] <= wb:
-                        c += 1
+            j = max(tile_run[tile], run_begin)
+            while True:  # the ballot over 32 run ends
+                c = sum(1 for lane in range(32)
+                        if j + lane < run_limit and end[j + lane] <= wb)
                 j += c
                 if c < 32:
                     break
@@ -59,9 +75,9 @@ def simulate(numel, runs):
                 if e0 >= numel:
                     continue
                 jj = j
-                while jj < nr and end[jj] <= e0:
+                while jj < run_limit and end[jj] <= e0:
                     jj += 1
-                if jj >= nr or start[jj] >= e0 + VEC:
+                if jj >= run_limit or start[jj] >= e0 + VEC:
                     continue
                 if start[jj] <= e0 and e0 + VEC <= end[jj]:
                     assert e0 % VEC == 0 and e0 + VEC <= numel
@@ -72,27 +88,43 @@ def simulate(numel, runs):
                     e = e0 + k
                     if e >= numel:
                         break
-                    while jj < nr and end[jj] <= e:
+                    while jj < run_limit and end[jj] <= e:
                         jj += 1
-                    if jj >= nr:
+                    if jj >= run_limit:
                         break
                     if start[jj] > e:
                         continue
                     visits[e] += 1
-    return visits, vector_accesses
+    return vector_accesses
 
 
 def check_layout(sizes, D, bucket, pad, wd=None):
     L = B.dopt_build_range_map(sizes, D, bucket, pad, wd)
     decays = wd if wd is not None else [1] * len(sizes)
-    runs = runs_from_pieces(L.pieces(), decays)
+    runs, bucket_run = runs_from_pieces(L.pieces(), decays, L.n_buckets)
     for (a, b, _), (c, d, _) in zip(runs, runs[1:]):
         assert a < b <= c < d  # sorted, disjoint, non-empty
-    visits, nvec = simulate(L.padded_numel, runs)
-    owned = np.zeros(L.padded_numel, np.int32)
+    N = L.padded_numel
+    tr = tile_index(N, runs)
+    owned = np.zeros(N, np.int32)
     for a, b in L.param_ranges():
         owned[a:b] = 1
+    # one launch over every bucket
+    visits = np.zeros(N, np.int32)
+    nvec = simulate(N, runs, tr, *view(runs, bucket_run, 0, L.n_buckets), visits)
     assert np.array_equal(visits, owned)
+    # one launch per bucket, and one over a middle range of buckets
+    visits = np.zeros(N, np.int32)
+    for k in range(L.n_buckets):
+        simulate(N, runs, tr, *view(runs, bucket_run, k, 1), visits)
+    assert np.array_equal(visits, owned)
+    if L.n_buckets >= 3:
+        visits = np.zeros(N, np.int32)
+        simulate(N, runs, tr, *view(runs, bucket_run, 1, L.n_buckets - 2), visits)
+        mid = np.zeros(N, np.int32)
+        buckets = L.buckets()
+        mid[buckets[1][0]:buckets[-2][1]] = owned[buckets[1][0]:buckets[-2][1]]
+        assert np.array_equal(visits, mid)
     return nvec
 
 
@@ -113,6 +145,9 @@ def test_tiny_layouts():
     ([123457, 99], 64, 0, 1, [1, 0]),
     ([0, 500, 0, 0, 1200, 0], 4, 0, 1, None),
     ([3] * 2000, 16, 0, 1, [1, 0] * 1000),  # more than 32 runs per warp
+    ([1000, 3, 2000, 5, 700], 1, 1000, 1, None),  # D=1: buckets touch, runs must not merge
+    ([300000, 5, 70001, 4096, 123], 8, 100000, 64, [1, 0, 1, 1, 0]),
+    ([5000, 7000, 3000, 9000, 4000], 4, 6000, 8, None),
 ])
 def test_parity_layouts(case):
     sizes, D, bucket, pad, wd = case

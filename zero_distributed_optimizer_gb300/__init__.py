@@ -20,9 +20,12 @@ from .binding import (  # noqa: F401
     AdamConfig,
     DoptError,
     Layout,
+    dopt_allreduce,
     dopt_build_range_map,
     dopt_gather,
     dopt_step,
+    dopt_step_allreduce,
+    dopt_step_buckets,
     dopt_step_clipped,
     dopt_step_clipped_noalloc,
     clip_workspace,

@@ -97,6 +97,15 @@ def _declare(lib):
     lib.dopt_step_clipped_noalloc.argtypes = [vp, P(dopt_adam_cfg), ctypes.c_int64, ctypes.c_float,
                                               P(vp), ctypes.c_int, vp, vp, vp, P(vp),
                                               ctypes.c_uint32, vp, vp, vp]
+    lib.dopt_step_buckets.restype = ctypes.c_int
+    lib.dopt_step_buckets.argtypes = [vp, P(dopt_adam_cfg), ctypes.c_int64, ctypes.c_int32,
+                                      ctypes.c_int32, P(vp), ctypes.c_int, vp, vp, vp, P(vp),
+                                      ctypes.c_uint32, vp, vp]
+    lib.dopt_step_allreduce.restype = ctypes.c_int
+    lib.dopt_step_allreduce.argtypes = [vp, P(dopt_adam_cfg), ctypes.c_int64, P(vp), ctypes.c_int,
+                                        vp, vp, vp, P(vp), ctypes.c_uint32, vp, vp]
+    lib.dopt_allreduce.restype = ctypes.c_int
+    lib.dopt_allreduce.argtypes = [vp, P(vp), ctypes.c_int, ctypes.c_float, vp]
     lib.dopt_gather.restype = ctypes.c_int
     lib.dopt_gather.argtypes = [vp, P(vp), vp]
     lib.dopt_last_error.restype = ctypes.c_char_p
@@ -242,6 +251,91 @@ def _check_tensor(t, name, dtype, numel, device):
         raise DoptError(DOPT_E_ARG, f"{name} has dtype {t.dtype}, expected {dtype}")
     if not t.is_contiguous() or t.numel() < numel:
         raise DoptError(DOPT_E_ARG, f"{name} must be contiguous with >= {numel} elements")
+
+
+def _step_pointers(layout: Layout, grad_replicas, master, exp_avg, exp_avg_sq, param_replicas,
+                   main_grad_out):
+    import torch
+
+    D = layout.D
+    if len(grad_replicas) != D or len(param_replicas) != D:
+        raise DoptError(DOPT_E_ARG, f"need {D} grad and {D} param replicas")
+    N = layout.padded_numel
+    device = master.device
+    if device.type != "cuda":
+        raise DoptError(DOPT_E_ARG, "the step needs CUDA tensors (no CPU path exists)")
+    gdt = grad_replicas[0].dtype
+    if gdt not in (torch.bfloat16, torch.float32):
+        raise DoptError(DOPT_E_ARG, f"grad dtype {gdt} is not bf16 or fp32")
+    for i, g in enumerate(grad_replicas):
+        _check_tensor(g, f"grad_replicas[{i}]", gdt, N, device)
+    for name, t in (("master", master), ("exp_avg", exp_avg), ("exp_avg_sq", exp_avg_sq)):
+        _check_tensor(t, name, torch.float32, N, device)
+    for i, p in enumerate(param_replicas):
+        _check_tensor(p, f"param_replicas[{i}]", torch.bfloat16, N, device)
+    if main_grad_out is not None:
+        _check_tensor(main_grad_out, "main_grad_out", torch.float32, N, device)
+    gp = (ctypes.c_void_p * D)(*[g.data_ptr() for g in grad_replicas])
+    pp = (ctypes.c_void_p * D)(*[p.data_ptr() for p in param_replicas])
+    dt = DOPT_BF16 if gdt == torch.bfloat16 else DOPT_FP32
+    mg = None if main_grad_out is None else main_grad_out.data_ptr()
+    return device, gp, pp, dt, mg
+
+
+def dopt_step_buckets(layout: Layout, adam: AdamConfig, step: int, first_bucket: int,
+                      n_buckets: int, grad_replicas, master, exp_avg, exp_avg_sq,
+                      param_replicas, gather: bool = True, main_grad_out=None,
+                      stream=None) -> None:
+    """The step over buckets [first_bucket, first_bucket + n_buckets) only."""
+    import torch
+
+    device, gp, pp, dt, mg = _step_pointers(layout, grad_replicas, master, exp_avg, exp_avg_sq,
+                                            param_replicas, main_grad_out)
+    cfg = adam.to_c()
+    with torch.cuda.device(device):
+        _check(lib().dopt_step_buckets(
+            layout.handle, ctypes.byref(cfg), int(step), int(first_bucket), int(n_buckets), gp,
+            dt, master.data_ptr(), exp_avg.data_ptr(), exp_avg_sq.data_ptr(), pp,
+            DOPT_STEP_GATHER if gather else 0, mg, _stream_handle(stream)))
+
+
+def dopt_step_allreduce(layout: Layout, adam: AdamConfig, step: int, grad_replicas, master,
+                        exp_avg, exp_avg_sq, param_replicas, gather: bool = True,
+                        main_grad_out=None, stream=None) -> None:
+    """The step that also all-reduces the grads in place (force_all_reduce)."""
+    import torch
+
+    device, gp, pp, dt, mg = _step_pointers(layout, grad_replicas, master, exp_avg, exp_avg_sq,
+                                            param_replicas, main_grad_out)
+    cfg = adam.to_c()
+    with torch.cuda.device(device):
+        _check(lib().dopt_step_allreduce(
+            layout.handle, ctypes.byref(cfg), int(step), gp, dt, master.data_ptr(),
+            exp_avg.data_ptr(), exp_avg_sq.data_ptr(), pp, DOPT_STEP_GATHER if gather else 0, mg,
+            _stream_handle(stream)))
+
+
+def dopt_allreduce(layout: Layout, grad_replicas, grad_scale: float, stream=None) -> None:
+    """All-reduce of the D grad replicas in place (scaled, fp32 rank order,
+    rounded back to the grad type)."""
+    import torch
+
+    D = layout.D
+    if len(grad_replicas) != D:
+        raise DoptError(DOPT_E_ARG, f"need {D} grad replicas")
+    device = grad_replicas[0].device
+    if device.type != "cuda":
+        raise DoptError(DOPT_E_ARG, "dopt_allreduce needs CUDA tensors")
+    gdt = grad_replicas[0].dtype
+    if gdt not in (torch.bfloat16, torch.float32):
+        raise DoptError(DOPT_E_ARG, f"grad dtype {gdt} is not bf16 or fp32")
+    for i, g in enumerate(grad_replicas):
+        _check_tensor(g, f"grad_replicas[{i}]", gdt, layout.padded_numel, device)
+    gp = (ctypes.c_void_p * D)(*[g.data_ptr() for g in grad_replicas])
+    with torch.cuda.device(device):
+        _check(lib().dopt_allreduce(layout.handle, gp,
+                                    DOPT_BF16 if gdt == torch.bfloat16 else DOPT_FP32,
+                                    float(grad_scale), _stream_handle(stream)))
 
 
 def dopt_step(layout: Layout, adam: AdamConfig, step: int, grad_replicas, master, exp_avg,

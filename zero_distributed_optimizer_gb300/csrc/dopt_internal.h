@@ -26,12 +26,15 @@ struct dopt_layout {
     std::vector<dopt_range> buckets;
     std::vector<dopt_piece> pieces;
 
-    // Kernel tables.  A run is a maximal stretch of owned elements with one
-    // owner rank, one bucket and one weight-decay flag; the gaps between runs
-    // are padding.  tile_run[t] is the first run ending after tile t's start.
+    // Kernel tables.  A run is a maximal stretch of owned elements of one
+    // bucket with one owner rank and one weight-decay flag; the gaps between
+    // runs are padding.  tile_run[t] is the first run ending after tile t's start.
     std::vector<int64_t> run_start, run_end;
     std::vector<int32_t> run_meta;
     std::vector<int32_t> tile_run;
+    // bucket_run[k] is the first run of bucket k; bucket_run[n_buckets] is
+    // the run count.  Runs never cross a bucket boundary.
+    std::vector<int32_t> bucket_run;
 
     // Device copies (one allocation), valid on `device` once uploaded.
     int device = -1;

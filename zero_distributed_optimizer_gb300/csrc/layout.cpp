@@ -90,23 +90,33 @@ void bucket_pieces(dopt_layout &L, int32_t k, int32_t p_begin, int32_t p_end) {
     }
 }
 
-// Runs for the kernel: consecutive pieces that touch and share the owner
-// rank and the decay flag are merged (the kernel needs nothing else per
-// element).
+// Runs for the kernel: consecutive pieces of one bucket that touch and
+// share the owner rank and the decay flag are merged (the kernel needs
+// nothing else per element).  Runs stay inside their bucket, so that a
+// launch can cover any contiguous range of buckets.
 void build_runs(dopt_layout &L) {
+    const int32_t nb = int32_t(L.buckets.size());
+    L.bucket_run.assign(size_t(nb) + 1, 0);
+    int32_t run_bucket = -1;
     for (const dopt_piece &pc : L.pieces) {
         int32_t meta = (L.param_decays[size_t(pc.param_id)] ? kRunDecays : 0) |
                        (pc.rank << kRunRankShift);
         bool extend = !L.run_end.empty() && L.run_end.back() == pc.gbuf_world.start &&
-                      L.run_meta.back() == meta;
+                      L.run_meta.back() == meta && run_bucket == pc.bucket_id;
         if (extend) {
             L.run_end.back() = pc.gbuf_world.end;
         } else {
+            // buckets between the last run's and this one own no run
+            for (int32_t k = run_bucket + 1; k <= pc.bucket_id; ++k)
+                L.bucket_run[size_t(k)] = int32_t(L.run_start.size());
+            run_bucket = pc.bucket_id;
             L.run_start.push_back(pc.gbuf_world.start);
             L.run_end.push_back(pc.gbuf_world.end);
             L.run_meta.push_back(meta);
         }
     }
+    for (int32_t k = run_bucket + 1; k <= nb; ++k)
+        L.bucket_run[size_t(k)] = int32_t(L.run_start.size());
     const int64_t n_tiles = (L.numel + kDoptTileElems - 1) / kDoptTileElems;
     L.tile_run.resize(size_t(n_tiles) + 1);
     size_t j = 0;

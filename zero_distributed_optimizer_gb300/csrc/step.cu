@@ -1,23 +1,27 @@
-// Fused ZeRO-1 distributed-optimizer step for sm_103a, and the standalone
-// all-gather (Megatron-LM distributed-optimizer page, §4.2-§4.4).
+// Fused ZeRO-1 distributed-optimizer step for sm_103a, the clipped step,
+// the all-reduce and the standalone all-gather (Megatron-LM
+// distributed-optimizer page, §4.2-§4.4 and §5; distributed-training
+// tutorial, "AllReduce" and §8.3).
 //
 // Work split.  With all D ranks held on one device, every owned element i
 // is independent: rank q's reduce-scatter reads the D replicas at i, its
 // Adam reads and writes the fp32 master/m/v at i (the four-way range map
 // composes to the identity on the buffer index, because main params are
 // stored buffer-indexed), and the write-back plus all-gather writes the D
-// param replicas at i.  So one launch covers the whole buffer, all buckets
-// and all ranks, in tiles of 2048 elements (256 threads x 8 elements).
+// param replicas at i.  So one launch covers any set of buckets (all of them
+// for dopt_step), in tiles of 2048 elements (256 threads x 8 elements).
 //
 // Per element the only facts needed are "owned or padding", "decays or
 // not" and the owner rank.  They come from the run table (maximal owned
-// stretches with one rank and one decay flag).  Each CTA gets the first run
-// of its tile from a host-built index; each warp then finds the first run
-// of its own 256 elements with one ballot over 32 run ends, and each thread
-// walks forward to its 8 elements.  An 8-element vector that lies inside one
-// run goes through 128-bit loads and stores; a vector that straddles a run
-// edge (param with another decay flag, a rank edge, padding) is done element
-// by element and never touches padding.
+// stretches of one bucket with one rank and one decay flag).  A launch
+// covers a contiguous range of runs (a RunView); each CTA gets the first run
+// of its tile from a host-built index, each warp finds the first run of its
+// own 256 elements with one ballot over 32 run ends, and each thread walks
+// forward to its 8 elements.  An 8-element vector inside one run goes
+// through 128-bit loads and stores; a vector that straddles a run edge
+// (param with another decay flag, a rank edge, padding, the edge of the
+// launch's range) is done element by element and touches owned elements of
+// the range only.
 //
 // Arithmetic.  Every fp32 operation uses the round-to-nearest intrinsics
 // (__fmul_rn, __fadd_rn, __fsub_rn, __fdiv_rn, __fsqrt_rn), so no multiply
@@ -45,6 +49,27 @@ struct Scalars {
     float b1, b2, omb1, omb2, decay, step_size, bc2_sqrt, eps, scale;
 };
 
+// The part of the run table one launch covers: runs [run_begin, run_limit)
+// and tiles from tile0 on.  Elements outside those runs are left alone.
+struct RunView {
+    const int64_t *run_start;
+    const int64_t *run_end;
+    const int32_t *run_meta;
+    const int32_t *tile_run;
+    int64_t numel;
+    int64_t tile0;
+    int32_t run_begin;
+    int32_t run_limit;
+};
+
+// What the step kernel does with the reduced grads.
+enum StepMode : int {
+    kPlain = 0,       // reduce the replicas, Adam
+    kFromMain = 1,    // read main_grad_in times the clipping coefficient, Adam
+    kWriteGrads = 2,  // reduce the replicas, write the reduced grads back into
+                      // every replica (all-reduce), Adam
+};
+
 struct StepArgs {
     const void *grads[DOPT_MAX_D];
     void *params[DOPT_MAX_D];
@@ -52,14 +77,9 @@ struct StepArgs {
     float *exp_avg;
     float *exp_avg_sq;
     float *main_grad_out;
-    const float *main_grad_in;  // clipped step: the reduced grads
-    const float *clip_coef;     // clipped step: device scalar
-    const int64_t *run_start;
-    const int64_t *run_end;
-    const int32_t *run_meta;
-    const int32_t *tile_run;
-    int64_t numel;
-    int32_t n_runs;
+    const float *main_grad_in;  // kFromMain: the reduced grads
+    const float *clip_coef;     // kFromMain: device scalar
+    RunView rv;
     int32_t D;
     int32_t gather;
     Scalars sc;
@@ -76,18 +96,15 @@ struct ClipWorkspace {
     double partial[kMaxClipCtas];
 };
 static_assert(sizeof(ClipWorkspace) <= DOPT_CLIP_WORKSPACE_BYTES, "workspace size");
+static_assert(sizeof(ClipWorkspace) <= DOPT_NOALLOC_SCRATCH_BYTES, "scratch size");
 
 struct NormArgs {
     const void *grads[DOPT_MAX_D];
     float *main_grad;
     ClipWorkspace *ws;
     float *norm_out;
-    const int64_t *run_start;
-    const int64_t *run_end;
-    const int32_t *tile_run;
-    int64_t numel;
+    RunView rv;
     int64_t n_tiles;
-    int32_t n_runs;
     int32_t D;
     float scale;
     float max_norm;
@@ -95,13 +112,18 @@ struct NormArgs {
 
 struct GatherArgs {
     void *params[DOPT_MAX_D];
-    const int64_t *run_start;
-    const int64_t *run_end;
-    const int32_t *run_meta;
-    const int32_t *tile_run;
-    int64_t numel;
-    int32_t n_runs;
+    RunView rv;
     int32_t D;
+};
+
+// The grads are read, reduced and written back in place (each element by
+// the one thread that read it), so the pointers are stored as const and
+// cast back for the stores.
+struct AllReduceArgs {
+    const void *grads[DOPT_MAX_D];
+    RunView rv;
+    int32_t D;
+    float scale;
 };
 
 // ---------------------------------------------------------------------------
@@ -126,6 +148,11 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4 &raw, float (&f)[8]) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ uint4 pack_bf16x8(const float (&f)[8]) {
+    return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                      pack_bf16x2(f[6], f[7]));
 }
 
 __device__ __forceinline__ uint16_t to_bf16_bits(float x) {
@@ -157,17 +184,51 @@ __device__ __forceinline__ void adamw(const Scalars &s, float decay, float g, fl
     w = __fsub_rn(w, __fmul_rn(s.step_size, __fdiv_rn(m, denom)));
 }
 
-// First run (index >= j) whose end lies beyond `pos`: one ballot over 32
-// consecutive run ends per iteration.  All 32 lanes must call it.
-__device__ __forceinline__ int warp_first_run(const int64_t *run_end, int n_runs, int j,
+// First run (index >= j, < limit) whose end lies beyond `pos`: one ballot
+// over 32 consecutive run ends per iteration.  All 32 lanes must call it.
+__device__ __forceinline__ int warp_first_run(const int64_t *run_end, int limit, int j,
                                               int64_t pos, int lane) {
     for (;;) {
         const int idx = j + lane;
-        const bool ended = idx < n_runs && run_end[idx] <= pos;
+        const bool ended = idx < limit && run_end[idx] <= pos;
         const unsigned mask = __ballot_sync(0xffffffffu, ended);
         j += __popc(mask);
         if (mask != 0xffffffffu) return j;
     }
+}
+
+// Where a thread's 8-element vector at e0 of `tile` stands in the view:
+// kNone (nothing of the view in it), kFull (inside one run) or kMixed; `j`
+// is the first run of the view ending after e0.  All lanes must call it.
+enum VecKind : int { kNone = 0, kFull = 1, kMixed = 2 };
+
+__device__ __forceinline__ VecKind locate(const RunView &v, int64_t tile, int64_t e0, int &j) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp_begin = tile * kDoptTileElems + int64_t(threadIdx.x & ~31) * kVec;
+    j = warp_first_run(v.run_end, v.run_limit, max(v.tile_run[tile], v.run_begin), warp_begin,
+                       lane);
+    if (e0 >= v.numel) return kNone;
+    while (j < v.run_limit && v.run_end[j] <= e0) ++j;
+    if (j >= v.run_limit) return kNone;
+    const int64_t rs = v.run_start[j];
+    if (rs >= e0 + kVec) return kNone;
+    return (rs <= e0 && e0 + kVec <= v.run_end[j]) ? kFull : kMixed;
+}
+
+// For the element path: advance j to the run holding e; false if e is not
+// owned in the view (padding, or outside its runs).  Sets `done` once no
+// run of the view is left.
+__device__ __forceinline__ bool owned_at(const RunView &v, int64_t e, int &j, bool &done) {
+    if (e >= v.numel) {
+        done = true;
+        return false;
+    }
+    while (j < v.run_limit && v.run_end[j] <= e) ++j;
+    if (j >= v.run_limit) {
+        done = true;
+        return false;
+    }
+    return v.run_start[j] <= e;
 }
 
 template <typename G>
@@ -176,6 +237,14 @@ __device__ __forceinline__ float load_grad_scalar(const void *base, int64_t i) {
         return __uint_as_float(uint32_t(__ldcs(static_cast<const unsigned short *>(base) + i)) << 16);
     else
         return __ldcs(static_cast<const float *>(base) + i);
+}
+
+template <typename G>
+__device__ __forceinline__ void store_grad_scalar(const void *base, int64_t i, float g) {
+    if constexpr (sizeof(G) == 2)
+        static_cast<uint16_t *>(const_cast<void *>(base))[i] = to_bf16_bits(g);
+    else
+        static_cast<float *>(const_cast<void *>(base))[i] = g;
 }
 
 // Load the 8 grads of replica r at e0 (bf16: one 16-byte load; fp32: two).
@@ -189,6 +258,10 @@ struct GradVec<__nv_bfloat16> {
         a = ld_stream(static_cast<const __nv_bfloat16 *>(base) + e0);
     }
     __device__ __forceinline__ void get(float (&f)[8]) const { unpack_bf16x8(a, f); }
+    // the 8 reduced grads, rounded to bf16, into replica `base` at e0
+    __device__ __forceinline__ static void store(const void *base, int64_t e0, const float (&f)[8]) {
+        st_stream(static_cast<__nv_bfloat16 *>(const_cast<void *>(base)) + e0, pack_bf16x8(f));
+    }
 };
 
 template <>
@@ -202,6 +275,11 @@ struct GradVec<float> {
     __device__ __forceinline__ void get(float (&f)[8]) const {
         f[0] = a.x, f[1] = a.y, f[2] = a.z, f[3] = a.w;
         f[4] = b.x, f[5] = b.y, f[6] = b.z, f[7] = b.w;
+    }
+    __device__ __forceinline__ static void store(const void *base, int64_t e0, const float (&f)[8]) {
+        float *p = static_cast<float *>(const_cast<void *>(base)) + e0;
+        st_stream_f4(p, make_float4(f[0], f[1], f[2], f[3]));
+        st_stream_f4(p + 4, make_float4(f[4], f[5], f[6], f[7]));
     }
 };
 
@@ -257,12 +335,28 @@ __device__ __forceinline__ float reduce_scalar(const void *const *grads, int D, 
     return g;
 }
 
-// A vector of 8 owned elements of one run.  kFromMain: the reduced grads
-// come from main_grad_in, times the clipping coefficient.
-template <typename G, int DC, bool kFromMain>
+// The reduced grads of 8 elements written into every replica, rounded to
+// the grad type (the all-reduce's all-gather half).
+template <typename G, int DC>
+__device__ __forceinline__ void write_grads_vec(const void *const *grads, int D_rt, int64_t e0,
+                                                const float (&acc)[8]) {
+    if constexpr (DC > 0) {
+#pragma unroll
+        for (int r = 0; r < DC; ++r) GradVec<G>::store(grads[r], e0, acc);
+    } else {
+        for (int r = 0; r < D_rt; ++r) GradVec<G>::store(grads[r], e0, acc);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// The step kernel
+// ---------------------------------------------------------------------------
+
+// A vector of 8 owned elements of one run.
+template <typename G, int DC, int MODE>
 __device__ __forceinline__ void full_vector(const StepArgs &a, int64_t e0, int32_t meta) {
     float acc[8];
-    if constexpr (kFromMain) {
+    if constexpr (MODE == kFromMain) {
         const float coef = *a.clip_coef;
         const float4 g0 = ld_stream_f4(a.main_grad_in + e0), g1 = ld_stream_f4(a.main_grad_in + e0 + 4);
         const float f[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
@@ -271,6 +365,7 @@ __device__ __forceinline__ void full_vector(const StepArgs &a, int64_t e0, int32
     } else {
         reduce_vec<G, DC>(a, a.sc.scale, e0, acc);
     }
+    if constexpr (MODE == kWriteGrads) write_grads_vec<G, DC>(a.grads, a.D, e0, acc);
 
     const float4 w0 = ld_stream_f4(a.master + e0), w1 = ld_stream_f4(a.master + e0 + 4);
     const float4 m0 = ld_stream_f4(a.exp_avg + e0), m1 = ld_stream_f4(a.exp_avg + e0 + 4);
@@ -288,13 +383,12 @@ __device__ __forceinline__ void full_vector(const StepArgs &a, int64_t e0, int32
     st_stream_f4(a.exp_avg + e0 + 4, make_float4(m[4], m[5], m[6], m[7]));
     st_stream_f4(a.exp_avg_sq + e0, make_float4(v[0], v[1], v[2], v[3]));
     st_stream_f4(a.exp_avg_sq + e0 + 4, make_float4(v[4], v[5], v[6], v[7]));
-    if (!kFromMain && a.main_grad_out) {
+    if (MODE != kFromMain && a.main_grad_out) {
         st_stream_f4(a.main_grad_out + e0, make_float4(acc[0], acc[1], acc[2], acc[3]));
         st_stream_f4(a.main_grad_out + e0 + 4, make_float4(acc[4], acc[5], acc[6], acc[7]));
     }
 
-    const uint4 packed = make_uint4(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]),
-                                    pack_bf16x2(w[4], w[5]), pack_bf16x2(w[6], w[7]));
+    const uint4 packed = pack_bf16x8(w);
     if (a.gather) {
         if constexpr (DC > 0) {
 #pragma unroll
@@ -311,27 +405,27 @@ __device__ __forceinline__ void full_vector(const StepArgs &a, int64_t e0, int32
 }
 
 // A vector that straddles a run edge: element by element, owned ones only.
-template <typename G, int DC, bool kFromMain>
+template <typename G, int DC, int MODE>
 __device__ __noinline__ void mixed_vector(const StepArgs &a, int64_t e0, int j) {
     const int D = DC > 0 ? DC : a.D;
-    for (int k = 0; k < kVec; ++k) {
+    bool done = false;
+    for (int k = 0; k < kVec && !done; ++k) {
         const int64_t e = e0 + k;
-        if (e >= a.numel) return;
-        while (j < a.n_runs && a.run_end[j] <= e) ++j;
-        if (j >= a.n_runs) return;
-        if (a.run_start[j] > e) continue;  // padding
-        const int32_t meta = a.run_meta[j];
+        if (!owned_at(a.rv, e, j, done)) continue;
+        const int32_t meta = a.rv.run_meta[j];
         float g;
-        if constexpr (kFromMain)
+        if constexpr (MODE == kFromMain)
             g = __fmul_rn(a.main_grad_in[e], *a.clip_coef);
         else
             g = reduce_scalar<G>(a.grads, D, a.sc.scale, e);
+        if constexpr (MODE == kWriteGrads)
+            for (int r = 0; r < D; ++r) store_grad_scalar<G>(a.grads[r], e, g);
         float w = a.master[e], m = a.exp_avg[e], v = a.exp_avg_sq[e];
         adamw(a.sc, (meta & kRunDecays) ? a.sc.decay : 1.0f, g, w, m, v);
         a.master[e] = w;
         a.exp_avg[e] = m;
         a.exp_avg_sq[e] = v;
-        if (!kFromMain && a.main_grad_out) a.main_grad_out[e] = g;
+        if (MODE != kFromMain && a.main_grad_out) a.main_grad_out[e] = g;
         const uint16_t bits = to_bf16_bits(w);
         if (a.gather) {
             for (int r = 0; r < D; ++r) static_cast<uint16_t *>(a.params[r])[e] = bits;
@@ -341,23 +435,48 @@ __device__ __noinline__ void mixed_vector(const StepArgs &a, int64_t e0, int j) 
     }
 }
 
-template <typename G, int DC, bool kFromMain>
+template <typename G, int DC, int MODE>
 __global__ void __launch_bounds__(kThreads) dopt_step_kernel(const __grid_constant__ StepArgs a) {
-    const int64_t tile_begin = int64_t(blockIdx.x) * kDoptTileElems;
-    const int lane = threadIdx.x & 31;
-    const int64_t warp_begin = tile_begin + int64_t(threadIdx.x & ~31) * kVec;
-    const int64_t e0 = tile_begin + int64_t(threadIdx.x) * kVec;
-    int j = warp_first_run(a.run_end, a.n_runs, a.tile_run[blockIdx.x], warp_begin, lane);
-    if (e0 >= a.numel) return;
-    while (j < a.n_runs && a.run_end[j] <= e0) ++j;
-    if (j >= a.n_runs) return;
-    const int64_t rs = a.run_start[j];
-    if (rs >= e0 + kVec) return;  // all padding
-    if (rs <= e0 && e0 + kVec <= a.run_end[j])
-        full_vector<G, DC, kFromMain>(a, e0, a.run_meta[j]);
-    else
-        mixed_vector<G, DC, kFromMain>(a, e0, j);
+    const int64_t tile = a.rv.tile0 + blockIdx.x;
+    const int64_t e0 = tile * kDoptTileElems + int64_t(threadIdx.x) * kVec;
+    int j;
+    const VecKind kind = locate(a.rv, tile, e0, j);
+    if (kind == kFull)
+        full_vector<G, DC, MODE>(a, e0, a.rv.run_meta[j]);
+    else if (kind == kMixed)
+        mixed_vector<G, DC, MODE>(a, e0, j);
 }
+
+// ---------------------------------------------------------------------------
+// The all-reduce kernel: reduce, then write the reduced grads into every
+// replica, rounded to the grad type.
+// ---------------------------------------------------------------------------
+
+template <typename G, int DC>
+__global__ void __launch_bounds__(kThreads) dopt_allreduce_kernel(const __grid_constant__ AllReduceArgs a) {
+    const int64_t tile = a.rv.tile0 + blockIdx.x;
+    const int64_t e0 = tile * kDoptTileElems + int64_t(threadIdx.x) * kVec;
+    int j;
+    const VecKind kind = locate(a.rv, tile, e0, j);
+    if (kind == kFull) {
+        float acc[8];
+        reduce_vec<G, DC>(a, a.scale, e0, acc);
+        write_grads_vec<G, DC>(a.grads, a.D, e0, acc);
+    } else if (kind == kMixed) {
+        const int D = DC > 0 ? DC : a.D;
+        bool done = false;
+        for (int k = 0; k < kVec && !done; ++k) {
+            const int64_t e = e0 + k;
+            if (!owned_at(a.rv, e, j, done)) continue;
+            const float g = reduce_scalar<G>(a.grads, D, a.scale, e);
+            for (int r = 0; r < D; ++r) store_grad_scalar<G>(a.grads[r], e, g);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Pass 1 of the clipped step
+// ---------------------------------------------------------------------------
 
 // Deterministic sum over a warp (fixed shuffle tree); the result is in lane 0.
 __device__ __forceinline__ double warp_sum(double v) {
@@ -365,26 +484,22 @@ __device__ __forceinline__ double warp_sum(double v) {
     return v;
 }
 
-// Pass 1 of the clipped step: the fused reduce-scatter writes the fp32 main
-// grads and every CTA accumulates the sum of their squares over the tiles it
-// visits (fp32 squares summed pairwise per 8-element vector, then one fp64
-// add per vector).  Each CTA leaves one fp64 partial; the CTA that finishes
-// last (atomic ticket, nobody waits) adds the partials in CTA order and
-// writes the norm and the clipping coefficient
-// min(1, max_norm / (norm + 1e-6)).
+// The fused reduce-scatter writes the fp32 main grads and every CTA
+// accumulates the sum of their squares over the tiles it visits (fp32
+// squares summed pairwise per 8-element vector, then one fp64 add per
+// vector).  Each CTA leaves one fp64 partial; the CTA that finishes last
+// (atomic ticket, nobody waits) adds the partials in CTA order and writes the
+// norm and the clipping coefficient min(1, max_norm / (norm + 1e-6)).
 template <typename G, int DC>
 __global__ void __launch_bounds__(kThreads) dopt_rs_norm_kernel(const __grid_constant__ NormArgs a) {
     const int lane = threadIdx.x & 31;
     double local = 0.0;
-    for (int64_t tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x) {
-        const int64_t tile_begin = tile * kDoptTileElems;
-        const int64_t warp_begin = tile_begin + int64_t(threadIdx.x & ~31) * kVec;
-        const int64_t e0 = tile_begin + int64_t(threadIdx.x) * kVec;
-        int j = warp_first_run(a.run_end, a.n_runs, a.tile_run[tile], warp_begin, lane);
-        if (e0 >= a.numel) continue;
-        while (j < a.n_runs && a.run_end[j] <= e0) ++j;
-        if (j >= a.n_runs || a.run_start[j] >= e0 + kVec) continue;
-        if (a.run_start[j] <= e0 && e0 + kVec <= a.run_end[j]) {
+    for (int64_t t = blockIdx.x; t < a.n_tiles; t += gridDim.x) {
+        const int64_t tile = a.rv.tile0 + t;
+        const int64_t e0 = tile * kDoptTileElems + int64_t(threadIdx.x) * kVec;
+        int j;
+        const VecKind kind = locate(a.rv, tile, e0, j);
+        if (kind == kFull) {
             float acc[8];
             reduce_vec<G, DC>(a, a.scale, e0, acc);
             st_stream_f4(a.main_grad + e0, make_float4(acc[0], acc[1], acc[2], acc[3]));
@@ -395,18 +510,16 @@ __global__ void __launch_bounds__(kThreads) dopt_rs_norm_kernel(const __grid_con
             const float s01 = __fadd_rn(sq[0], sq[1]), s23 = __fadd_rn(sq[2], sq[3]);
             const float s45 = __fadd_rn(sq[4], sq[5]), s67 = __fadd_rn(sq[6], sq[7]);
             local += double(__fadd_rn(__fadd_rn(s01, s23), __fadd_rn(s45, s67)));
-            continue;
-        }
-        const int D = DC > 0 ? DC : a.D;
-        for (int k = 0; k < kVec; ++k) {
-            const int64_t e = e0 + k;
-            if (e >= a.numel) break;
-            while (j < a.n_runs && a.run_end[j] <= e) ++j;
-            if (j >= a.n_runs) break;
-            if (a.run_start[j] > e) continue;
-            const float g = reduce_scalar<G>(a.grads, D, a.scale, e);
-            a.main_grad[e] = g;
-            local += double(__fmul_rn(g, g));
+        } else if (kind == kMixed) {
+            const int D = DC > 0 ? DC : a.D;
+            bool done = false;
+            for (int k = 0; k < kVec && !done; ++k) {
+                const int64_t e = e0 + k;
+                if (!owned_at(a.rv, e, j, done)) continue;
+                const float g = reduce_scalar<G>(a.grads, D, a.scale, e);
+                a.main_grad[e] = g;
+                local += double(__fmul_rn(g, g));
+            }
         }
     }
     __shared__ double warp_part[kThreads / 32];
@@ -441,34 +554,30 @@ __global__ void __launch_bounds__(kThreads) dopt_rs_norm_kernel(const __grid_con
     }
 }
 
+// ---------------------------------------------------------------------------
+// The gather kernel: each rank's owned elements from its replica to all.
+// ---------------------------------------------------------------------------
+
 __global__ void __launch_bounds__(kThreads) dopt_gather_kernel(const __grid_constant__ GatherArgs a) {
-    const int64_t tile_begin = int64_t(blockIdx.x) * kDoptTileElems;
-    const int lane = threadIdx.x & 31;
-    const int64_t warp_begin = tile_begin + int64_t(threadIdx.x & ~31) * kVec;
-    const int64_t e0 = tile_begin + int64_t(threadIdx.x) * kVec;
-    int j = warp_first_run(a.run_end, a.n_runs, a.tile_run[blockIdx.x], warp_begin, lane);
-    if (e0 >= a.numel) return;
-    while (j < a.n_runs && a.run_end[j] <= e0) ++j;
-    if (j >= a.n_runs) return;
-    const int64_t rs = a.run_start[j];
-    if (rs >= e0 + kVec) return;
-    if (rs <= e0 && e0 + kVec <= a.run_end[j]) {
-        const int q = a.run_meta[j] >> kRunRankShift;
+    const int64_t tile = a.rv.tile0 + blockIdx.x;
+    const int64_t e0 = tile * kDoptTileElems + int64_t(threadIdx.x) * kVec;
+    int j;
+    const VecKind kind = locate(a.rv, tile, e0, j);
+    if (kind == kFull) {
+        const int q = a.rv.run_meta[j] >> kRunRankShift;
         const uint4 val = ld_stream(static_cast<const __nv_bfloat16 *>(a.params[q]) + e0);
         for (int r = 0; r < a.D; ++r)
             if (r != q) st_stream(static_cast<__nv_bfloat16 *>(a.params[r]) + e0, val);
-        return;
-    }
-    for (int k = 0; k < kVec; ++k) {
-        const int64_t e = e0 + k;
-        if (e >= a.numel) return;
-        while (j < a.n_runs && a.run_end[j] <= e) ++j;
-        if (j >= a.n_runs) return;
-        if (a.run_start[j] > e) continue;
-        const int q = a.run_meta[j] >> kRunRankShift;
-        const uint16_t bits = static_cast<const uint16_t *>(a.params[q])[e];
-        for (int r = 0; r < a.D; ++r)
-            if (r != q) static_cast<uint16_t *>(a.params[r])[e] = bits;
+    } else if (kind == kMixed) {
+        bool done = false;
+        for (int k = 0; k < kVec && !done; ++k) {
+            const int64_t e = e0 + k;
+            if (!owned_at(a.rv, e, j, done)) continue;
+            const int q = a.rv.run_meta[j] >> kRunRankShift;
+            const uint16_t bits = static_cast<const uint16_t *>(a.params[q])[e];
+            for (int r = 0; r < a.D; ++r)
+                if (r != q) static_cast<uint16_t *>(a.params[r])[e] = bits;
+        }
     }
 }
 
@@ -493,19 +602,50 @@ Scalars make_scalars(const dopt_adam_cfg &c, int64_t t) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The run view of buckets [first, first + count) and the number of tiles a
+// launch over it needs (0: nothing owned there).
+RunView make_view(const dopt_layout *L, int32_t first, int32_t count, int64_t *tiles) {
+    RunView v{};
+    v.run_start = L->d_run_start;
+    v.run_end = L->d_run_end;
+    v.run_meta = L->d_run_meta;
+    v.tile_run = L->d_tile_run;
+    v.numel = L->numel;
+    v.run_begin = L->bucket_run[size_t(first)];
+    v.run_limit = L->bucket_run[size_t(first + count)];
+    *tiles = 0;
+    if (v.run_begin >= v.run_limit) return v;
+    const int64_t lo = L->run_start[size_t(v.run_begin)];
+    const int64_t hi = L->run_end[size_t(v.run_limit - 1)];
+    v.tile0 = lo / kDoptTileElems;
+    *tiles = (hi + kDoptTileElems - 1) / kDoptTileElems - v.tile0;
+    return v;
+}
+
+RunView whole_view(const dopt_layout *L, int64_t *tiles) {
+    return make_view(L, 0, int32_t(L->buckets.size()), tiles);
+}
+
 using StepKernel = void (*)(StepArgs);
 using NormKernel = void (*)(NormArgs);
+using AllReduceKernel = void (*)(AllReduceArgs);
 
-template <typename G, bool kFromMain>
+template <typename G, int MODE>
 StepKernel pick_step_kernel(int D) {
     switch (D) {
-        case 1: return dopt_step_kernel<G, 1, kFromMain>;
-        case 2: return dopt_step_kernel<G, 2, kFromMain>;
-        case 4: return dopt_step_kernel<G, 4, kFromMain>;
-        case 8: return dopt_step_kernel<G, 8, kFromMain>;
-        case 16: return dopt_step_kernel<G, 16, kFromMain>;
-        default: return dopt_step_kernel<G, 0, kFromMain>;
+        case 1: return dopt_step_kernel<G, 1, MODE>;
+        case 2: return dopt_step_kernel<G, 2, MODE>;
+        case 4: return dopt_step_kernel<G, 4, MODE>;
+        case 8: return dopt_step_kernel<G, 8, MODE>;
+        case 16: return dopt_step_kernel<G, 16, MODE>;
+        default: return dopt_step_kernel<G, 0, MODE>;
     }
+}
+
+template <int MODE>
+StepKernel step_kernel_for(dopt_dtype grad_dtype, int D) {
+    return grad_dtype == DOPT_BF16 ? pick_step_kernel<__nv_bfloat16, MODE>(D)
+                                   : pick_step_kernel<float, MODE>(D);
 }
 
 template <typename G>
@@ -517,6 +657,22 @@ NormKernel pick_norm_kernel(int D) {
         case 8: return dopt_rs_norm_kernel<G, 8>;
         case 16: return dopt_rs_norm_kernel<G, 16>;
         default: return dopt_rs_norm_kernel<G, 0>;
+    }
+}
+
+NormKernel norm_kernel_for(dopt_dtype grad_dtype, int D) {
+    return grad_dtype == DOPT_BF16 ? pick_norm_kernel<__nv_bfloat16>(D) : pick_norm_kernel<float>(D);
+}
+
+template <typename G>
+AllReduceKernel pick_allreduce_kernel(int D) {
+    switch (D) {
+        case 1: return dopt_allreduce_kernel<G, 1>;
+        case 2: return dopt_allreduce_kernel<G, 2>;
+        case 4: return dopt_allreduce_kernel<G, 4>;
+        case 8: return dopt_allreduce_kernel<G, 8>;
+        case 16: return dopt_allreduce_kernel<G, 16>;
+        default: return dopt_allreduce_kernel<G, 0>;
     }
 }
 
@@ -548,6 +704,16 @@ int check_device_tables(const dopt_layout *L, const char *who) {
     return DOPT_OK;
 }
 
+int check_replicas(const char *who, int D, const void *const *ptrs) {
+    using dopt::fail;
+    for (int r = 0; r < D; ++r) {
+        if (!ptrs[r]) return fail(DOPT_E_ARG, "%s: replica %d pointer is NULL", who, r);
+        if (!aligned16(ptrs[r]))
+            return fail(DOPT_E_ALIGN, "%s: replica %d pointer is not 16-byte aligned", who, r);
+    }
+    return DOPT_OK;
+}
+
 // Host checks shared by the step entry points; nothing is queued before
 // they pass.
 int check_step_args(const char *who, const dopt_layout *L, const dopt_adam_cfg *cfg,
@@ -568,12 +734,10 @@ int check_step_args(const char *who, const dopt_layout *L, const dopt_adam_cfg *
         !std::isfinite(cfg->grad_scale))
         return fail(DOPT_E_ARG, "%s: hyper-parameter out of range", who);
     const int D = L->cfg.D;
-    for (int r = 0; r < D; ++r) {
-        if (!grad_replicas[r] || !param_replicas[r])
-            return fail(DOPT_E_ARG, "%s: replica %d pointer is NULL", who, r);
-        if (!aligned16(grad_replicas[r]) || !aligned16(param_replicas[r]))
-            return fail(DOPT_E_ALIGN, "%s: replica %d pointer is not 16-byte aligned", who, r);
-    }
+    int rc = check_replicas(who, D, grad_replicas);
+    if (rc != DOPT_OK) return rc;
+    rc = check_replicas(who, D, const_cast<const void *const *>(param_replicas));
+    if (rc != DOPT_OK) return rc;
     if (!aligned16(master) || !aligned16(exp_avg) || !aligned16(exp_avg_sq) ||
         (main_grad && !aligned16(main_grad)))
         return fail(DOPT_E_ALIGN, "%s: state pointer is not 16-byte aligned", who);
@@ -591,23 +755,40 @@ void fill_step_args(StepArgs &a, const dopt_layout *L, const dopt_adam_cfg *cfg,
     a.master = master;
     a.exp_avg = exp_avg;
     a.exp_avg_sq = exp_avg_sq;
-    a.run_start = L->d_run_start;
-    a.run_end = L->d_run_end;
-    a.run_meta = L->d_run_meta;
-    a.tile_run = L->d_tile_run;
-    a.numel = L->numel;
-    a.n_runs = int32_t(L->run_start.size());
     a.D = D;
     a.gather = (flags & DOPT_STEP_GATHER) ? 1 : 0;
     a.sc = make_scalars(*cfg, step);
 }
 
-// The two launches of the clipped step, with the workspace given as a
-// device address.
-NormKernel norm_kernel_for(dopt_dtype grad_dtype, int D) {
-    return grad_dtype == DOPT_BF16 ? pick_norm_kernel<__nv_bfloat16>(D) : pick_norm_kernel<float>(D);
+int launch_error(const char *who, const char *what) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return dopt::fail(DOPT_E_CUDA, "%s: %s launch: %s", who, what, cudaGetErrorString(e));
+    return DOPT_OK;
 }
 
+// One step launch (plain or all-reduce mode) over buckets [first, first+count).
+template <int MODE>
+int launch_step(const char *who, const dopt_layout *L, const dopt_adam_cfg *cfg, int64_t step,
+                int32_t first, int32_t count, const void *const *grad_replicas,
+                dopt_dtype grad_dtype, float *master, float *exp_avg, float *exp_avg_sq,
+                void *const *param_replicas, uint32_t flags, float *main_grad_out,
+                cudaStream_t stream) {
+    int64_t tiles = 0;
+    StepArgs a{};
+    a.rv = make_view(L, first, count, &tiles);
+    if (tiles == 0) return DOPT_OK;
+    int rc = check_device_tables(L, who);
+    if (rc != DOPT_OK) return rc;
+    fill_step_args(a, L, cfg, step, grad_replicas, master, exp_avg, exp_avg_sq, param_replicas,
+                   flags);
+    a.main_grad_out = main_grad_out;
+    StepKernel k = step_kernel_for<MODE>(grad_dtype, L->cfg.D);
+    k<<<unsigned(tiles), kThreads, 0, stream>>>(a);
+    return launch_error(who, "step");
+}
+
+// The two launches of the clipped step, with the workspace given as a
+// device address.
 int launch_clipped(const char *who, const dopt_layout *L, const dopt_adam_cfg *cfg,
                    int64_t step, float max_norm, const void *const *grad_replicas,
                    dopt_dtype grad_dtype, float *master, float *exp_avg, float *exp_avg_sq,
@@ -620,12 +801,7 @@ int launch_clipped(const char *who, const dopt_layout *L, const dopt_adam_cfg *c
     na.main_grad = main_grad;
     na.ws = ws;
     na.norm_out = norm_out;
-    na.run_start = L->d_run_start;
-    na.run_end = L->d_run_end;
-    na.tile_run = L->d_tile_run;
-    na.numel = L->numel;
-    na.n_tiles = (L->numel + kDoptTileElems - 1) / kDoptTileElems;
-    na.n_runs = int32_t(L->run_start.size());
+    na.rv = whole_view(L, &na.n_tiles);
     na.D = D;
     na.scale = cfg->grad_scale;
     na.max_norm = max_norm;
@@ -634,50 +810,115 @@ int launch_clipped(const char *who, const dopt_layout *L, const dopt_adam_cfg *c
     cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(unsigned int), stream);
     if (e != cudaSuccess) return fail(DOPT_E_CUDA, "%s: workspace reset: %s", who, cudaGetErrorString(e));
     nk<<<grid_a, kThreads, 0, stream>>>(na);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return fail(DOPT_E_CUDA, "%s: norm launch: %s", who, cudaGetErrorString(e));
+    int rc = launch_error(who, "norm");
+    if (rc != DOPT_OK) return rc;
 
     StepArgs a{};
+    int64_t tiles = 0;
+    a.rv = whole_view(L, &tiles);
     fill_step_args(a, L, cfg, step, grad_replicas, master, exp_avg, exp_avg_sq, param_replicas,
                    flags);
     a.main_grad_in = main_grad;
     a.clip_coef = &ws->coef;
-    const unsigned grid = unsigned((L->numel + kDoptTileElems - 1) / kDoptTileElems);
-    StepKernel k = pick_step_kernel<float, true>(D);
-    k<<<grid, kThreads, 0, stream>>>(a);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return fail(DOPT_E_CUDA, "%s: step launch: %s", who, cudaGetErrorString(e));
+    StepKernel k = pick_step_kernel<float, kFromMain>(D);
+    k<<<unsigned(tiles), kThreads, 0, stream>>>(a);
+    return launch_error(who, "step");
+}
+
+// Checks of the clipped entry points beyond the step's own.
+int check_clip_args(const char *who, const float *main_grad, const float *norm_out,
+                    float max_norm) {
+    using dopt::fail;
+    if (!main_grad) return fail(DOPT_E_ARG, "%s: main_grad is required", who);
+    if (norm_out && (reinterpret_cast<uintptr_t>(norm_out) & 7u))
+        return fail(DOPT_E_ALIGN, "%s: norm_out misaligned", who);
+    if (!(max_norm > 0.0f) || !std::isfinite(max_norm))
+        return fail(DOPT_E_ARG, "%s: max_norm must be positive and finite", who);
     return DOPT_OK;
 }
 
 }  // namespace
 
+// ---------------------------------------------------------------------------
+// Entry points
+// ---------------------------------------------------------------------------
+
 extern "C" int dopt_step(const dopt_layout *L, const dopt_adam_cfg *cfg, int64_t step,
                          const void *const *grad_replicas, dopt_dtype grad_dtype, float *master,
                          float *exp_avg, float *exp_avg_sq, void *const *param_replicas,
                          uint32_t flags, float *main_grad_out, cudaStream_t stream) {
+    dopt::clear_error();
+    const char *who = "dopt_step";
+    int rc = check_step_args(who, L, cfg, step, grad_replicas, grad_dtype, master, exp_avg,
+                             exp_avg_sq, param_replicas, flags, main_grad_out);
+    if (rc != DOPT_OK) return rc;
+    return launch_step<kPlain>(who, L, cfg, step, 0, int32_t(L->buckets.size()), grad_replicas,
+                               grad_dtype, master, exp_avg, exp_avg_sq, param_replicas, flags,
+                               main_grad_out, stream);
+}
+
+extern "C" int dopt_step_buckets(const dopt_layout *L, const dopt_adam_cfg *cfg, int64_t step,
+                                 int32_t first_bucket, int32_t n_buckets,
+                                 const void *const *grad_replicas, dopt_dtype grad_dtype,
+                                 float *master, float *exp_avg, float *exp_avg_sq,
+                                 void *const *param_replicas, uint32_t flags,
+                                 float *main_grad_out, cudaStream_t stream) {
     using dopt::fail;
     dopt::clear_error();
-    int rc = check_step_args("dopt_step", L, cfg, step, grad_replicas, grad_dtype, master,
-                             exp_avg, exp_avg_sq, param_replicas, flags, main_grad_out);
+    const char *who = "dopt_step_buckets";
+    int rc = check_step_args(who, L, cfg, step, grad_replicas, grad_dtype, master, exp_avg,
+                             exp_avg_sq, param_replicas, flags, main_grad_out);
     if (rc != DOPT_OK) return rc;
+    const int32_t nb = int32_t(L->buckets.size());
+    if (first_bucket < 0 || n_buckets < 0 || first_bucket > nb || n_buckets > nb - first_bucket)
+        return fail(DOPT_E_ARG, "%s: buckets [%d, %d+%d) outside 0..%d", who, first_bucket,
+                    first_bucket, n_buckets, nb);
+    return launch_step<kPlain>(who, L, cfg, step, first_bucket, n_buckets, grad_replicas,
+                               grad_dtype, master, exp_avg, exp_avg_sq, param_replicas, flags,
+                               main_grad_out, stream);
+}
+
+extern "C" int dopt_step_allreduce(const dopt_layout *L, const dopt_adam_cfg *cfg, int64_t step,
+                                   void *const *grad_replicas, dopt_dtype grad_dtype,
+                                   float *master, float *exp_avg, float *exp_avg_sq,
+                                   void *const *param_replicas, uint32_t flags,
+                                   float *main_grad_out, cudaStream_t stream) {
+    dopt::clear_error();
+    const char *who = "dopt_step_allreduce";
+    const void *const *grads = const_cast<const void *const *>(grad_replicas);
+    int rc = check_step_args(who, L, cfg, step, grads, grad_dtype, master, exp_avg, exp_avg_sq,
+                             param_replicas, flags, main_grad_out);
+    if (rc != DOPT_OK) return rc;
+    return launch_step<kWriteGrads>(who, L, cfg, step, 0, int32_t(L->buckets.size()), grads,
+                                    grad_dtype, master, exp_avg, exp_avg_sq, param_replicas,
+                                    flags, main_grad_out, stream);
+}
+
+extern "C" int dopt_allreduce(const dopt_layout *L, void *const *grad_replicas,
+                              dopt_dtype grad_dtype, float grad_scale, cudaStream_t stream) {
+    using dopt::fail;
+    dopt::clear_error();
+    const char *who = "dopt_allreduce";
+    if (!L || !grad_replicas) return fail(DOPT_E_ARG, "%s: NULL argument", who);
+    if (grad_dtype != DOPT_BF16 && grad_dtype != DOPT_FP32)
+        return fail(DOPT_E_ARG, "%s: unknown grad dtype %d", who, int(grad_dtype));
+    if (!std::isfinite(grad_scale)) return fail(DOPT_E_ARG, "%s: grad_scale not finite", who);
     const int D = L->cfg.D;
-    if (L->run_start.empty()) return DOPT_OK;  // nothing owned: nothing to do
-    rc = check_device_tables(L, "dopt_step");
+    int rc = check_replicas(who, D, const_cast<const void *const *>(grad_replicas));
     if (rc != DOPT_OK) return rc;
-
-    StepArgs a{};
-    fill_step_args(a, L, cfg, step, grad_replicas, master, exp_avg, exp_avg_sq, param_replicas,
-                   flags);
-    a.main_grad_out = main_grad_out;
-
-    const unsigned grid = unsigned((L->numel + kDoptTileElems - 1) / kDoptTileElems);
-    StepKernel k = grad_dtype == DOPT_BF16 ? pick_step_kernel<__nv_bfloat16, false>(D)
-                                           : pick_step_kernel<float, false>(D);
-    k<<<grid, kThreads, 0, stream>>>(a);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return fail(DOPT_E_CUDA, "dopt_step launch: %s", cudaGetErrorString(e));
-    return DOPT_OK;
+    AllReduceArgs a{};
+    int64_t tiles = 0;
+    a.rv = whole_view(L, &tiles);
+    if (tiles == 0) return DOPT_OK;
+    rc = check_device_tables(L, who);
+    if (rc != DOPT_OK) return rc;
+    for (int r = 0; r < D; ++r) a.grads[r] = grad_replicas[r];
+    a.D = D;
+    a.scale = grad_scale;
+    AllReduceKernel k = grad_dtype == DOPT_BF16 ? pick_allreduce_kernel<__nv_bfloat16>(D)
+                                                : pick_allreduce_kernel<float>(D);
+    k<<<unsigned(tiles), kThreads, 0, stream>>>(a);
+    return launch_error(who, "all-reduce");
 }
 
 extern "C" int dopt_step_clipped(const dopt_layout *L, const dopt_adam_cfg *cfg, int64_t step,
@@ -688,20 +929,19 @@ extern "C" int dopt_step_clipped(const dopt_layout *L, const dopt_adam_cfg *cfg,
                                  cudaStream_t stream) {
     using dopt::fail;
     dopt::clear_error();
-    int rc = check_step_args("dopt_step_clipped", L, cfg, step, grad_replicas, grad_dtype,
-                             master, exp_avg, exp_avg_sq, param_replicas, flags, main_grad);
+    const char *who = "dopt_step_clipped";
+    int rc = check_step_args(who, L, cfg, step, grad_replicas, grad_dtype, master, exp_avg,
+                             exp_avg_sq, param_replicas, flags, main_grad);
     if (rc != DOPT_OK) return rc;
-    if (!main_grad || !workspace)
-        return fail(DOPT_E_ARG, "dopt_step_clipped: main_grad and workspace are required");
-    if (!aligned16(workspace) || (norm_out && (reinterpret_cast<uintptr_t>(norm_out) & 7u)))
-        return fail(DOPT_E_ALIGN, "dopt_step_clipped: workspace or norm_out misaligned");
-    if (!(max_norm > 0.0f) || !std::isfinite(max_norm))
-        return fail(DOPT_E_ARG, "dopt_step_clipped: max_norm must be positive and finite");
+    rc = check_clip_args(who, main_grad, norm_out, max_norm);
+    if (rc != DOPT_OK) return rc;
+    if (!workspace) return fail(DOPT_E_ARG, "%s: workspace is required", who);
+    if (!aligned16(workspace)) return fail(DOPT_E_ALIGN, "%s: workspace misaligned", who);
     if (L->run_start.empty()) return DOPT_OK;
-    rc = check_device_tables(L, "dopt_step_clipped");
+    rc = check_device_tables(L, who);
     if (rc != DOPT_OK) return rc;
-    return launch_clipped("dopt_step_clipped", L, cfg, step, max_norm, grad_replicas, grad_dtype,
-                          master, exp_avg, exp_avg_sq, param_replicas, flags, main_grad,
+    return launch_clipped(who, L, cfg, step, max_norm, grad_replicas, grad_dtype, master,
+                          exp_avg, exp_avg_sq, param_replicas, flags, main_grad,
                           static_cast<ClipWorkspace *>(workspace), norm_out, stream);
 }
 
@@ -752,11 +992,8 @@ extern "C" int dopt_step_clipped_noalloc(const dopt_layout *L, const dopt_adam_c
     int rc = check_step_args(who, L, cfg, step, grad_replicas, grad_dtype, master, exp_avg,
                              exp_avg_sq, param_replicas, flags, main_grad);
     if (rc != DOPT_OK) return rc;
-    if (!main_grad) return fail(DOPT_E_ARG, "%s: main_grad is required", who);
-    if (norm_out && (reinterpret_cast<uintptr_t>(norm_out) & 7u))
-        return fail(DOPT_E_ALIGN, "%s: norm_out misaligned", who);
-    if (!(max_norm > 0.0f) || !std::isfinite(max_norm))
-        return fail(DOPT_E_ARG, "%s: max_norm must be positive and finite", who);
+    rc = check_clip_args(who, main_grad, norm_out, max_norm);
+    if (rc != DOPT_OK) return rc;
     if (L->run_start.empty()) return DOPT_OK;
     rc = check_device_tables(L, who);
     if (rc != DOPT_OK) return rc;
@@ -777,28 +1014,20 @@ extern "C" int dopt_step_clipped_noalloc(const dopt_layout *L, const dopt_adam_c
 extern "C" int dopt_gather(const dopt_layout *L, void *const *param_replicas, cudaStream_t stream) {
     using dopt::fail;
     dopt::clear_error();
-    if (!L || !param_replicas) return fail(DOPT_E_ARG, "dopt_gather: NULL argument");
+    const char *who = "dopt_gather";
+    if (!L || !param_replicas) return fail(DOPT_E_ARG, "%s: NULL argument", who);
     const int D = L->cfg.D;
-    for (int r = 0; r < D; ++r) {
-        if (!param_replicas[r]) return fail(DOPT_E_ARG, "dopt_gather: replica %d is NULL", r);
-        if (!aligned16(param_replicas[r]))
-            return fail(DOPT_E_ALIGN, "dopt_gather: replica %d is not 16-byte aligned", r);
-    }
-    if (L->run_start.empty() || D == 1) return DOPT_OK;
-    int rc = check_device_tables(L, "dopt_gather");
+    int rc = check_replicas(who, D, const_cast<const void *const *>(param_replicas));
     if (rc != DOPT_OK) return rc;
+    if (D == 1) return DOPT_OK;
     GatherArgs a{};
+    int64_t tiles = 0;
+    a.rv = whole_view(L, &tiles);
+    if (tiles == 0) return DOPT_OK;
+    rc = check_device_tables(L, who);
+    if (rc != DOPT_OK) return rc;
     for (int r = 0; r < D; ++r) a.params[r] = param_replicas[r];
-    a.run_start = L->d_run_start;
-    a.run_end = L->d_run_end;
-    a.run_meta = L->d_run_meta;
-    a.tile_run = L->d_tile_run;
-    a.numel = L->numel;
-    a.n_runs = int32_t(L->run_start.size());
     a.D = D;
-    const unsigned grid = unsigned((L->numel + kDoptTileElems - 1) / kDoptTileElems);
-    dopt_gather_kernel<<<grid, kThreads, 0, stream>>>(a);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return fail(DOPT_E_CUDA, "dopt_gather launch: %s", cudaGetErrorString(e));
-    return DOPT_OK;
+    dopt_gather_kernel<<<unsigned(tiles), kThreads, 0, stream>>>(a);
+    return launch_error(who, "gather");
 }

@@ -1,7 +1,7 @@
 """Run a few launches of the fused step on one workload, for profilers.
 
     python -m zero_distributed_optimizer_gb300.profcase --workload gpt2_small \
-        [--max-elems N] [--warmup W] [--launches K] [--mode step|gather|clipped]
+        [--max-elems N] [--warmup W] [--launches K] [--mode MODE]
 
 --max-elems keeps the leading params of the workload whose total stays
 within N elements, so that a profiler capture can run on a smaller buffer of
@@ -50,8 +50,11 @@ def main(argv=None):
     ap.add_argument("--max-elems", type=int, default=0)
     ap.add_argument("--warmup", type=int, default=2)
     ap.add_argument("--launches", type=int, default=3)
-    ap.add_argument("--mode", choices=["step", "gather", "clipped"], default="step",
-                    help="the fused step, dopt_gather alone, or the clipped step")
+    ap.add_argument("--mode", default="step",
+                    choices=["step", "gather", "clipped", "buckets", "allreduce", "step_allreduce"],
+                    help="the fused step, dopt_gather alone, the clipped step, the step as "
+                         "one launch per bucket, dopt_allreduce alone, or the step with "
+                         "force_all_reduce")
     args = ap.parse_args(argv)
 
     libbuild.build()
@@ -81,6 +84,13 @@ def main(argv=None):
         t += 1
         if args.mode == "gather":
             B.dopt_gather(L, params)
+        elif args.mode == "buckets":
+            for k in range(L.n_buckets):
+                B.dopt_step_buckets(L, adam, t, k, 1, grads, master, m, v, params)
+        elif args.mode == "allreduce":
+            B.dopt_allreduce(L, grads, 1.0)
+        elif args.mode == "step_allreduce":
+            B.dopt_step_allreduce(L, adam, t, grads, master, m, v, params)
         elif args.mode == "clipped":
             B.dopt_step_clipped(L, adam, t, 1.0, grads, master, m, v, params, main_grad, ws)
         else:
@@ -88,11 +98,13 @@ def main(argv=None):
     ev[1].record()
     torch.cuda.synchronize()
     ms = ev[0].elapsed_time(ev[1]) / max(args.launches, 1)
-    per_elem = {"gather": 2 * w.D, "step": w.algorithmic_bytes_per_element(),
-                "clipped": w.algorithmic_bytes_per_element() + 8}[args.mode]
+    step_bytes = w.algorithmic_bytes_per_element()
+    per_elem = {"gather": 2 * w.D, "step": step_bytes, "buckets": step_bytes,
+                "clipped": step_bytes + 8, "allreduce": 2 * w.D * w.grad_bytes,
+                "step_allreduce": step_bytes + w.D * w.grad_bytes}[args.mode]
     bytes_per = w.numel * per_elem
     print(json.dumps({"workload": w.name, "N": w.numel, "padded_numel": N, "D": w.D,
-                      "mode": args.mode,
+                      "mode": args.mode, "n_buckets": L.n_buckets,
                       "launches": args.launches, "ms_per_launch": ms,
                       "algorithmic_bytes_per_launch": bytes_per,
                       "gbs": bytes_per / (ms / 1e3) / 1e9}))
