@@ -105,18 +105,21 @@ def _declare(lib) -> None:
                                   ctypes.POINTER(Piece), i32p]
     lib.orc_step.restype = ctypes.c_int
     lib.orc_step.argtypes = [
-        i64p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32,
+        i64p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
+        ctypes.c_int32,
         ctypes.POINTER(Adam), ctypes.c_int64, ctypes.c_int32, ctypes.POINTER(ctypes.c_void_p),
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p),
         ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_float,
     ]
     lib.orc_grad_norm_sq.restype = ctypes.c_int
-    lib.orc_grad_norm_sq.argtypes = [i64p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
+    lib.orc_grad_norm_sq.argtypes = [i64p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                     ctypes.c_int64,
                                      ctypes.c_int32, ctypes.c_float, ctypes.c_int32,
                                      ctypes.POINTER(ctypes.c_void_p), ctypes.c_int64,
                                      ctypes.c_int64, ctypes.POINTER(ctypes.c_double)]
     lib.orc_allreduce.restype = ctypes.c_int
-    lib.orc_allreduce.argtypes = [i64p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
+    lib.orc_allreduce.argtypes = [i64p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                  ctypes.c_int64,
                                   ctypes.c_int32, ctypes.c_float, ctypes.c_int32,
                                   ctypes.POINTER(ctypes.c_void_p), ctypes.c_int64, ctypes.c_int64]
     lib.orc_clip_coef.restype = ctypes.c_float
@@ -231,7 +234,8 @@ def make_adam(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, grad_s
 
 def step(sizes, wd_mask, D: int, bucket_elems: int, pad_unit: int, adam: Adam, t: int,
          grads, master, exp_avg, exp_avg_sq, params, gather: bool = True,
-         main_grad_out=None, window=None, clip_coef: float = 1.0, lib=None) -> None:
+         main_grad_out=None, window=None, clip_coef: float = 1.0, instances: int = 1,
+         lib=None) -> None:
     """One ZeRO-1 step for all D simulated ranks, in place on numpy arrays.
 
     grads: D arrays (uint16 bf16 bits or float32); master/exp_avg/exp_avg_sq:
@@ -240,6 +244,8 @@ def step(sizes, wd_mask, D: int, bucket_elems: int, pad_unit: int, adam: Adam, t
     the whole padded buffer).  Follows page 1 §4.2 (reduce-scatter), §4.3
     (main grads, Adam, write-back) and §4.4 (all-gather).  ``clip_coef``
     (from :func:`clip_coef`) multiplies every reduced grad before Adam.
+    ``instances`` > 1 splits the D ranks into that many optimizer instances
+    (page 1 §5): reduce-scatter inside each, then a sum across instances.
     """
     lib = lib or load()
     sizes_a, sizes_p = _i64(sizes)
@@ -271,7 +277,8 @@ def step(sizes, wd_mask, D: int, bucket_elems: int, pad_unit: int, adam: Adam, t
         wd = np.ascontiguousarray(wd_mask, dtype=np.uint8)
     gp = (ctypes.c_void_p * D)(*[g.ctypes.data for g in grads])
     pp = (ctypes.c_void_p * D)(*[p.ctypes.data for p in params])
-    rc = lib.orc_step(sizes_p, n, None if wd is None else wd.ctypes.data, D, bucket_elems,
+    rc = lib.orc_step(sizes_p, n, None if wd is None else wd.ctypes.data, D, int(instances),
+                      bucket_elems,
                       pad_unit, ctypes.byref(adam), t, int(grad_is_f32), gp,
                       master.ctypes.data, exp_avg.ctypes.data, exp_avg_sq.ctypes.data, pp,
                       int(bool(gather)),
@@ -282,7 +289,7 @@ def step(sizes, wd_mask, D: int, bucket_elems: int, pad_unit: int, adam: Adam, t
 
 
 def grad_norm_sq(sizes, D: int, bucket_elems: int, pad_unit: int, grad_scale: float, grads,
-                 window=None, lib=None) -> float:
+                 window=None, instances: int = 1, lib=None) -> float:
     """Sum of squares of the reduced grads over the owned elements of the
     window (tutorial §8.3 global norm), accumulated in double."""
     lib = lib or load()
@@ -294,7 +301,7 @@ def grad_norm_sq(sizes, D: int, bucket_elems: int, pad_unit: int, grad_scale: fl
         raise OracleError("grads must be D arrays of the window length")
     gp = (ctypes.c_void_p * D)(*[g.ctypes.data for g in grads])
     out = ctypes.c_double(0.0)
-    rc = lib.orc_grad_norm_sq(sizes_p, len(sizes_a), D, bucket_elems, pad_unit,
+    rc = lib.orc_grad_norm_sq(sizes_p, len(sizes_a), D, int(instances), bucket_elems, pad_unit,
                               float(grad_scale), int(grad_is_f32), gp, w0, w1, ctypes.byref(out))
     if rc != ORC_OK:
         raise OracleError(f"orc_grad_norm_sq failed: {rc}")
@@ -302,7 +309,7 @@ def grad_norm_sq(sizes, D: int, bucket_elems: int, pad_unit: int, grad_scale: fl
 
 
 def allreduce(sizes, D: int, bucket_elems: int, pad_unit: int, grad_scale: float, grads,
-              window=None, lib=None) -> None:
+              window=None, instances: int = 1, lib=None) -> None:
     """All-reduce of the grads in place (page 1 §5 force_all_reduce; the
     tutorial's AllReduce = reduce-scatter + all-gather): every replica gets
     the reduced grad at every owned element, rounded to the grad type."""
@@ -317,7 +324,8 @@ def allreduce(sizes, D: int, bucket_elems: int, pad_unit: int, grad_scale: float
         if g.dtype != (np.float32 if grad_is_f32 else np.uint16) or not g.flags.c_contiguous:
             raise OracleError("grads must be contiguous, all uint16 or all float32")
     gp = (ctypes.c_void_p * D)(*[g.ctypes.data for g in grads])
-    rc = lib.orc_allreduce(sizes_p, len(sizes_a), D, bucket_elems, pad_unit, float(grad_scale),
+    rc = lib.orc_allreduce(sizes_p, len(sizes_a), D, int(instances), bucket_elems, pad_unit,
+                           float(grad_scale),
                            int(grad_is_f32), gp, w0, w1)
     if rc != ORC_OK:
         raise OracleError(f"orc_allreduce failed: {rc}")

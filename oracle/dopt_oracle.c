@@ -67,6 +67,16 @@
  *      in double; the coefficient is min(1, max_norm / (norm + 1e-6)),
  *      evaluated in double and rounded to float once; each reduced grad is
  *      multiplied by it (one fp32 rounding) before Adam.
+ *  R11 num_distributed_optimizer_instances ([P1] §5: the reduce-scatter
+ *      stays inside an instance, an all-reduce across instances follows):
+ *      the D ranks form `instances` groups of R = D / instances consecutive
+ *      ranks; buckets are padded to and split into R ranges; each element's
+ *      grad is, per instance, the rank-order fp32 sum of its R scaled
+ *      replicas, and these sums are added in instance order.  Rank r of
+ *      every instance computes the same update from the same state, so one
+ *      copy of the optimizer state stands for all of them; the write-back
+ *      goes to rank r of every instance and the all-gather runs inside each
+ *      instance.
  *  R10 force_all_reduce ([P1] §5) leaves the optimizer step unchanged (each
  *      rank still updates its own shard from the same reduced grads) and
  *      additionally gives every replica's grad buffer the whole reduced grad,
@@ -302,15 +312,24 @@ static float orc_grad(const void *const *grads, int32_t grad_is_f32, int32_t r, 
     return orc_bf16_to_f32(((const uint16_t *)grads[r])[idx]);
 }
 
-/* The reduced grad of buffer element idx (R5): rank-order fp32 sum of the
- * scaled replicas.  `idx` is window-relative. */
+/* The reduced grad of buffer element idx (R5, R11): inside each instance,
+ * the rank-order fp32 sum of its R = D / instances scaled replicas (the
+ * reduce-scatter within the instance); then the instances' sums added in
+ * instance order (the all-reduce across instances).  With one instance this
+ * is the plain rank-order sum.  `idx` is window-relative. */
 static float orc_reduce_element(const void *const *grads, int32_t grad_is_f32, int32_t D,
-                                float scale, int64_t idx)
+                                int32_t instances, float scale, int64_t idx)
 {
-    float acc = scale * orc_grad(grads, grad_is_f32, 0, idx);
-    for (int32_t q = 1; q < D; ++q) {
-        float x = scale * orc_grad(grads, grad_is_f32, q, idx);
-        acc = acc + x;
+    int32_t R = D / instances;
+    float acc = 0.0f;
+    for (int32_t inst = 0; inst < instances; ++inst) {
+        int32_t first = inst * R;
+        float part = scale * orc_grad(grads, grad_is_f32, first, idx);
+        for (int32_t q = first + 1; q < first + R; ++q) {
+            float x = scale * orc_grad(grads, grad_is_f32, q, idx);
+            part = part + x;
+        }
+        acc = (inst == 0) ? part : acc + part;
     }
     return acc;
 }
@@ -353,17 +372,22 @@ static void orc_adamw(const orc_scalars *s, int decays, float g, float *w, float
  *                   owned element, buffer-indexed (before clipping)
  *   clip_coef       global-norm clipping coefficient (orc_clip_coef); 1.0
  *                   when no clipping is wanted
+ *   instances       optimizer instances (R11); D must divide by it; 1 is
+ *                   the plain step
  *
  * All buffer-indexed arrays are window-relative.  Returns ORC_OK or an error.
  */
 int orc_step(const int64_t *sizes, int32_t n, const uint8_t *wd_mask, int32_t D,
-             int64_t bucket_elems, int32_t pad_unit, const orc_adam *cfg, int64_t step,
+             int32_t instances, int64_t bucket_elems, int32_t pad_unit,
+             const orc_adam *cfg, int64_t step,
              int32_t grad_is_f32, const void *const *grads, float *master, float *exp_avg,
              float *exp_avg_sq, uint16_t *const *params, int32_t gather,
              float *main_grad_out, int64_t w0, int64_t w1, float clip_coef)
 {
-    if (step < 1 || w0 < 0 || w1 < w0)
+    if (step < 1 || w0 < 0 || w1 < w0 || instances < 1 || D % instances != 0)
         return ORC_E_ARG;
+    /* R ranks per instance shard each bucket (R11) */
+    int32_t R = D / instances;
 
     int rc = ORC_OK;
     int64_t *pstart = NULL, *pend = NULL, *bstart = NULL, *bend = NULL;
@@ -383,7 +407,7 @@ int orc_step(const int64_t *sizes, int32_t n, const uint8_t *wd_mask, int32_t D,
         rc = ORC_E_NOMEM;
         goto done;
     }
-    rc = orc_layout(sizes, n, D, bucket_elems, pad_unit, pstart, pend, pbucket, bstart,
+    rc = orc_layout(sizes, n, R, bucket_elems, pad_unit, pstart, pend, pbucket, bstart,
                     bend, &nb, &numel);
     if (rc != ORC_OK)
         goto done;
@@ -391,12 +415,12 @@ int orc_step(const int64_t *sizes, int32_t n, const uint8_t *wd_mask, int32_t D,
         rc = ORC_E_ARG;
         goto done;
     }
-    pieces = (orc_piece *)malloc(((size_t)n + (size_t)D * (size_t)nb + 1) * sizeof *pieces);
+    pieces = (orc_piece *)malloc(((size_t)n + (size_t)R * (size_t)nb + 1) * sizeof *pieces);
     if (!pieces) {
         rc = ORC_E_NOMEM;
         goto done;
     }
-    rc = orc_pieces(n, pstart, pend, pbucket, nb, bstart, bend, D, pieces, &npieces);
+    rc = orc_pieces(n, pstart, pend, pbucket, nb, bstart, bend, R, pieces, &npieces);
     if (rc != ORC_OK)
         goto done;
 
@@ -404,15 +428,15 @@ int orc_step(const int64_t *sizes, int32_t n, const uint8_t *wd_mask, int32_t D,
 
     int32_t first_piece = 0;
     for (int32_t k = 0; k < nb; ++k) {
-        for (int32_t r = 0; r < D; ++r) {
+        for (int32_t r = 0; r < R; ++r) {
             orc_range mine = {0, 0};
-            rc = orc_rank_range(bstart[k], bend[k], D, r, &mine);
+            rc = orc_rank_range(bstart[k], bend[k], R, r, &mine);
             if (rc != ORC_OK)
                 goto done;
             int64_t S = mine.end - mine.start;
 
-            /* Reduce-scatter ([P1] §4.2, §5; R5): rank r keeps the scaled,
-             * rank-ordered fp32 sum of its range over all D replicas. */
+            /* Reduce-scatter ([P1] §4.2, §5; R5, R11): rank r keeps the
+             * scaled fp32 sum of its range over all D replicas. */
             free(shard);
             shard = (float *)malloc((size_t)(S > 0 ? S : 1) * sizeof *shard);
             if (!shard) {
@@ -423,7 +447,8 @@ int orc_step(const int64_t *sizes, int32_t n, const uint8_t *wd_mask, int32_t D,
             int64_t j_hi = orc_min(S, w1 - mine.start);
             for (int64_t j = j_lo; j < j_hi; ++j) {
                 int64_t i = mine.start + j;
-                shard[j] = orc_reduce_element(grads, grad_is_f32, D, sc.scale, i - w0);
+                shard[j] = orc_reduce_element(grads, grad_is_f32, D, instances, sc.scale,
+                                              i - w0);
             }
 
             /* This rank's pieces are contiguous in the piece list. */
@@ -451,25 +476,30 @@ int orc_step(const int64_t *sizes, int32_t n, const uint8_t *wd_mask, int32_t D,
                     orc_adamw(&sc, decays, gc, &master[mi - w0], &exp_avg[mi - w0],
                               &exp_avg_sq[mi - w0]);
                     /* write-back into rank r's bucket view at
-                     * gbuf_world_in_bucket ([P1] §4.3) */
+                     * gbuf_world_in_bucket ([P1] §4.3); rank r of every
+                     * instance holds the same update (R11) */
                     int64_t bi = bstart[k] + pc->gbuf_world_in_bucket.start + t;
-                    params[r][bi - w0] = orc_f32_to_bf16(master[mi - w0]);
+                    uint16_t updated = orc_f32_to_bf16(master[mi - w0]);
+                    for (int32_t inst = 0; inst < instances; ++inst)
+                        params[inst * R + r][bi - w0] = updated;
                     if (main_grad_out)
                         main_grad_out[i - w0] = g;
                 }
             }
 
-            /* All-gather ([P1] §4.4; R8): rank r's owned elements go from its
-             * replica to every other replica. */
+            /* All-gather ([P1] §4.4; R8): inside each instance, rank r's
+             * owned elements go from its replica to the instance's other
+             * replicas. */
             if (gather) {
                 for (int32_t pi = first_piece; pi < last_piece; ++pi) {
                     const orc_piece *pc = &pieces[pi];
                     int64_t i_lo = orc_max(pc->gbuf_world.start, w0);
                     int64_t i_hi = orc_min(pc->gbuf_world.end, w1);
                     for (int64_t i = i_lo; i < i_hi; ++i) {
-                        for (int32_t q = 0; q < D; ++q)
-                            if (q != r)
-                                params[q][i - w0] = params[r][i - w0];
+                        for (int32_t inst = 0; inst < instances; ++inst)
+                            for (int32_t q = 0; q < R; ++q)
+                                if (q != r)
+                                    params[inst * R + q][i - w0] = params[inst * R + r][i - w0];
                     }
                 }
             }
@@ -494,12 +524,14 @@ done:
  * window-relative.  Summing the results of disjoint windows that cover the
  * buffer gives the global norm^2.
  */
-int orc_grad_norm_sq(const int64_t *sizes, int32_t n, int32_t D, int64_t bucket_elems,
-                     int32_t pad_unit, float grad_scale, int32_t grad_is_f32,
-                     const void *const *grads, int64_t w0, int64_t w1, double *out)
+int orc_grad_norm_sq(const int64_t *sizes, int32_t n, int32_t D, int32_t instances,
+                     int64_t bucket_elems, int32_t pad_unit, float grad_scale,
+                     int32_t grad_is_f32, const void *const *grads, int64_t w0, int64_t w1,
+                     double *out)
 {
-    if (w0 < 0 || w1 < w0 || !out)
+    if (w0 < 0 || w1 < w0 || !out || instances < 1 || D % instances != 0)
         return ORC_E_ARG;
+    int32_t R = D / instances;
     int rc = ORC_OK;
     size_t cap = (size_t)(n > 0 ? n : 1);
     int64_t *pstart = (int64_t *)malloc(cap * sizeof *pstart);
@@ -515,7 +547,7 @@ int orc_grad_norm_sq(const int64_t *sizes, int32_t n, int32_t D, int64_t bucket_
         rc = ORC_E_NOMEM;
         goto done;
     }
-    rc = orc_layout(sizes, n, D, bucket_elems, pad_unit, pstart, pend, pbucket, bstart, bend,
+    rc = orc_layout(sizes, n, R, bucket_elems, pad_unit, pstart, pend, pbucket, bstart, bend,
                     &nb, &numel);
     if (rc != ORC_OK)
         goto done;
@@ -523,19 +555,20 @@ int orc_grad_norm_sq(const int64_t *sizes, int32_t n, int32_t D, int64_t bucket_
         rc = ORC_E_ARG;
         goto done;
     }
-    pieces = (orc_piece *)malloc(((size_t)n + (size_t)D * (size_t)nb + 1) * sizeof *pieces);
+    pieces = (orc_piece *)malloc(((size_t)n + (size_t)R * (size_t)nb + 1) * sizeof *pieces);
     if (!pieces) {
         rc = ORC_E_NOMEM;
         goto done;
     }
-    rc = orc_pieces(n, pstart, pend, pbucket, nb, bstart, bend, D, pieces, &npieces);
+    rc = orc_pieces(n, pstart, pend, pbucket, nb, bstart, bend, R, pieces, &npieces);
     if (rc != ORC_OK)
         goto done;
     for (int32_t pi = 0; pi < npieces; ++pi) {
         int64_t i_lo = orc_max(pieces[pi].gbuf_world.start, w0);
         int64_t i_hi = orc_min(pieces[pi].gbuf_world.end, w1);
         for (int64_t i = i_lo; i < i_hi; ++i) {
-            double g = (double)orc_reduce_element(grads, grad_is_f32, D, grad_scale, i - w0);
+            double g = (double)orc_reduce_element(grads, grad_is_f32, D, instances, grad_scale,
+                                                  i - w0);
             sum += g * g;
         }
     }
@@ -559,12 +592,13 @@ done:
  * type (R7 for bf16; fp32 stays as is) (R10).  Padding is not written.
  * grads are window-relative and are overwritten.
  */
-int orc_allreduce(const int64_t *sizes, int32_t n, int32_t D, int64_t bucket_elems,
-                  int32_t pad_unit, float grad_scale, int32_t grad_is_f32, void *const *grads,
-                  int64_t w0, int64_t w1)
+int orc_allreduce(const int64_t *sizes, int32_t n, int32_t D, int32_t instances,
+                  int64_t bucket_elems, int32_t pad_unit, float grad_scale, int32_t grad_is_f32,
+                  void *const *grads, int64_t w0, int64_t w1)
 {
-    if (w0 < 0 || w1 < w0)
+    if (w0 < 0 || w1 < w0 || instances < 1 || D % instances != 0)
         return ORC_E_ARG;
+    int32_t R = D / instances;
     int rc = ORC_OK;
     size_t cap = (size_t)(n > 0 ? n : 1);
     int64_t *pstart = (int64_t *)malloc(cap * sizeof *pstart);
@@ -580,7 +614,7 @@ int orc_allreduce(const int64_t *sizes, int32_t n, int32_t D, int64_t bucket_ele
         rc = ORC_E_NOMEM;
         goto done;
     }
-    rc = orc_layout(sizes, n, D, bucket_elems, pad_unit, pstart, pend, pbucket, bstart, bend,
+    rc = orc_layout(sizes, n, R, bucket_elems, pad_unit, pstart, pend, pbucket, bstart, bend,
                     &nb, &numel);
     if (rc != ORC_OK)
         goto done;
@@ -588,19 +622,19 @@ int orc_allreduce(const int64_t *sizes, int32_t n, int32_t D, int64_t bucket_ele
         rc = ORC_E_ARG;
         goto done;
     }
-    pieces = (orc_piece *)malloc(((size_t)n + (size_t)D * (size_t)nb + 1) * sizeof *pieces);
+    pieces = (orc_piece *)malloc(((size_t)n + (size_t)R * (size_t)nb + 1) * sizeof *pieces);
     if (!pieces) {
         rc = ORC_E_NOMEM;
         goto done;
     }
-    rc = orc_pieces(n, pstart, pend, pbucket, nb, bstart, bend, D, pieces, &npieces);
+    rc = orc_pieces(n, pstart, pend, pbucket, nb, bstart, bend, R, pieces, &npieces);
     if (rc != ORC_OK)
         goto done;
     int32_t first_piece = 0;
     for (int32_t k = 0; k < nb; ++k) {
-        for (int32_t r = 0; r < D; ++r) {
+        for (int32_t r = 0; r < R; ++r) {
             orc_range mine = {0, 0};
-            rc = orc_rank_range(bstart[k], bend[k], D, r, &mine);
+            rc = orc_rank_range(bstart[k], bend[k], R, r, &mine);
             if (rc != ORC_OK)
                 goto done;
             int64_t S = mine.end - mine.start;
@@ -615,7 +649,7 @@ int orc_allreduce(const int64_t *sizes, int32_t n, int32_t D, int64_t bucket_ele
             int64_t j_hi = orc_min(S, w1 - mine.start);
             for (int64_t j = j_lo; j < j_hi; ++j)
                 shard[j] = orc_reduce_element((const void *const *)grads, grad_is_f32, D,
-                                              grad_scale, mine.start + j - w0);
+                                              instances, grad_scale, mine.start + j - w0);
             int32_t last_piece = first_piece;
             while (last_piece < npieces && pieces[last_piece].bucket_id == k &&
                    pieces[last_piece].rank == r)

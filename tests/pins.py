@@ -714,6 +714,102 @@ def pin_allreduce_rounds_to_nearest_even(lib):
         assert np.array_equal(x[:n], want[:n])
 
 
+# ---------------------------------------------------------------------------
+# Optimizer instances (page 1 §5, num_distributed_optimizer_instances > 1)
+# ---------------------------------------------------------------------------
+
+def pin_instances_hierarchical_order(lib):
+    """Page 1 §5: with several optimizer instances the reduce-scatter stays
+    inside an instance and an all-reduce across instances follows.  D=4 in 2
+    instances, fp32 grads 2^24, 1 | 1, -2^24 at one element: the instance
+    sums are 2^24 (1 + 2^24 is a tie, to even) and 1 - 2^24, their sum is 1;
+    one instance (the flat rank-order sum) gives 0."""
+    vals = [2.0 ** 24, 1.0, 1.0, -(2.0 ** 24)]
+    for instances, R, want in ((2, 2, 1.0), (1, 4, 0.0)):
+        grads = [np.array([x] + [0.0] * (R - 1), np.float32) for x in vals]
+        master, m, v = _state(R, 2)
+        out = np.full(R, 99.0, np.float32)
+        oracle.step([1], None, 4, 0, 1, oracle.make_adam(grad_scale=1.0), 1, grads, master, m,
+                    v, _params_from(master, 4), main_grad_out=out, instances=instances, lib=lib)
+        assert out[0] == want, (instances, out)
+        assert oracle.grad_norm_sq([1], 4, 0, 1, 1.0, grads, instances=instances,
+                                   lib=lib) == want * want
+
+
+def pin_instances_factorizations(lib):
+    """Integer-valued grads make every grouping exact: D=8 as 1, 2, 4 or 8
+    instances gives bitwise the same master, m, v and params per param."""
+    rng = np.random.default_rng(29)
+    sizes = [33, 7, 129, 64, 1, 90]
+    wd = [1, 0, 1, 1, 0, 1]
+    n = sum(sizes)
+    G = rng.integers(-64, 65, n).astype(np.float32)
+    D = 8
+    base = None
+    for instances in (1, 2, 4, 8):
+        R = D // instances
+        L = oracle.range_map(sizes, R, 0, 1, lib=lib)
+        N = L.numel
+        m0, _, _ = _state(n, 31)
+        master = np.zeros(N, np.float32)
+        m = np.zeros(N, np.float32)
+        v = np.zeros(N, np.float32)
+        grads = []
+        for r in range(D):
+            g = np.zeros(N, np.float32)
+            off = 0
+            for p, size in enumerate(sizes):
+                s0 = int(L.param_start[p])
+                g[s0:s0 + size] = (G[off:off + size] + (2 * r - (D - 1)) * 2) / 1024.0
+                master[s0:s0 + size] = m0[off:off + size]
+                off += size
+            grads.append(_bf16_bits_of(g))
+        params = _params_from(master, D)
+        oracle.step(sizes, wd, D, 0, 1, oracle.make_adam(grad_scale=1.0 / D), 1, grads, master,
+                    m, v, params, instances=instances, lib=lib)
+        res = []
+        for p in range(len(sizes)):
+            a, b = int(L.param_start[p]), int(L.param_end[p])
+            res.append([master[a:b].view(np.uint32).copy(), m[a:b].view(np.uint32).copy(),
+                        v[a:b].view(np.uint32).copy()] + [x[a:b].copy() for x in params])
+        if base is None:
+            base = res
+            continue
+        for x, y in zip(res, base):
+            for a, b in zip(x, y):
+                assert np.array_equal(a, b), instances
+
+
+def pin_instances_write_back_and_gather(lib):
+    """Without the gather only rank r of every instance holds the update of
+    the elements rank r owns; the gather spreads it inside each instance."""
+    sizes, D, instances = [37, 50], 6, 2
+    R = D // instances
+    L = oracle.range_map(sizes, R, 0, 1, lib=lib)
+    N = L.numel
+    rng = np.random.default_rng(4)
+    grads = [_bf16_bits_of(rng.integers(-8, 9, N).astype(np.float32)) for _ in range(D)]
+    for gather in (False, True):
+        master, m, v = _state(N, 6)
+        params = [(np.arange(N, dtype=np.uint16) * 3 + r) for r in range(D)]
+        before = [p.copy() for p in params]
+        oracle.step(sizes, None, D, 0, 1, oracle.make_adam(grad_scale=1.0 / D), 1, grads, master,
+                    m, v, params, gather=gather, instances=instances, lib=lib)
+        want = oracle.f32_to_bf16(master, lib=lib)
+        S = N // R
+        for rep in range(D):
+            r = rep % R
+            mine = np.zeros(N, bool)
+            mine[r * S:(r + 1) * S] = True
+            owned = np.zeros(N, bool)
+            owned[:sum(sizes)] = True
+            if gather:
+                assert np.array_equal(params[rep][owned], want[owned])
+            else:
+                assert np.array_equal(params[rep][owned & mine], want[owned & mine])
+                assert np.array_equal(params[rep][owned & ~mine], before[rep][owned & ~mine])
+
+
 ALL_PINS = [
     pin_page1_ownership,
     pin_brute_force_range_maps,
@@ -734,4 +830,7 @@ ALL_PINS = [
     pin_allreduce_every_rank,
     pin_allreduce_is_rs_then_gather,
     pin_allreduce_rounds_to_nearest_even,
+    pin_instances_hierarchical_order,
+    pin_instances_factorizations,
+    pin_instances_write_back_and_gather,
 ]

@@ -15,9 +15,15 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 # (name, text in dopt_oracle.c, replacement)
 MUTANTS = [
-    ("no_scale_rank0", "float acc = scale * orc_grad(grads, grad_is_f32, 0, idx);",
-     "float acc = orc_grad(grads, grad_is_f32, 0, idx);"),
-    ("skip_last_rank", "for (int32_t q = 1; q < D; ++q) {", "for (int32_t q = 1; q < D - 1; ++q) {"),
+    ("no_scale_first_rank", "float part = scale * orc_grad(grads, grad_is_f32, first, idx);",
+     "float part = orc_grad(grads, grad_is_f32, first, idx);"),
+    ("skip_last_rank", "for (int32_t q = first + 1; q < first + R; ++q) {",
+     "for (int32_t q = first + 1; q < first + R - 1; ++q) {"),
+    ("skip_last_instance", "for (int32_t inst = 0; inst < instances; ++inst) {\n        int32_t first",
+     "for (int32_t inst = 0; inst < instances - 1 || inst == 0; ++inst) {\n        int32_t first"),
+    ("writeback_first_instance_only",
+     "for (int32_t inst = 0; inst < instances; ++inst)\n                        params[inst * R + r][bi - w0] = updated;",
+     "params[r][bi - w0] = updated;"),
     ("update_sign", "ww = ww - delta;", "ww = ww + delta;"),
     ("no_bias_correction1", "s.step_size = (float)(lr / (1.0 - pow(b1, (double)t)));",
      "s.step_size = (float)lr;"),
