@@ -42,7 +42,7 @@ extern "C" {
 /* Status codes. */
 #define DOPT_OK 0
 #define DOPT_E_ARG (-1)    /* invalid argument (null, out of range) */
-#define DOPT_E_LAYOUT (-2) /* a bucket does not divide by D (page 1, §4.1 and §5) */
+#define DOPT_E_LAYOUT (-2) /* a bucket does not divide by R (page 1, §4.1 and §5) */
 #define DOPT_E_ALIGN (-3)  /* a device pointer is not 16-byte aligned */
 #define DOPT_E_CUDA (-4)   /* a CUDA runtime call failed */
 #define DOPT_E_STATE (-5)  /* the layout has no device tables on this device */
@@ -79,16 +79,28 @@ typedef struct {
 
 /*
  * Layout parameters.
- *   D             simulated data-parallel ranks, 1..DOPT_MAX_D
+ *   D             simulated data-parallel ranks (replica buffers),
+ *                 1..DOPT_MAX_D
  *   pad_unit      every bucket is padded at its end to a multiple of
- *                 D * pad_unit elements (>= 1)
+ *                 R * pad_unit elements (>= 1), R = D / instances
  *   bucket_elems  a bucket is closed as soon as its unpadded element count
  *                 reaches bucket_elems; 0 puts all params in one bucket
+ *   instances     distributed-optimizer instances (page 1, §5,
+ *                 num_distributed_optimizer_instances); 0 or 1: one
+ *                 instance.  D must divide by it.  The ranks form
+ *                 `instances` groups of R = D / instances consecutive ranks;
+ *                 each bucket is split into R ranges, rank r of every group
+ *                 owning range r; the grads are reduced inside each group in
+ *                 rank order and the groups' sums are then added in group
+ *                 order (the all-reduce across instances).
+ *   reserved      must be 0
  */
 typedef struct {
     int32_t D;
     int32_t pad_unit;
     int64_t bucket_elems;
+    int32_t instances;
+    int32_t reserved;
 } dopt_layout_cfg;
 
 /*
@@ -128,8 +140,10 @@ typedef struct dopt_layout dopt_layout;
  *
  * Buckets are greedy: params are appended to the open bucket, which closes
  * as soon as its unpadded count reaches bucket_elems; a param never spans
- * two buckets; each bucket is padded to a multiple of D * pad_unit, and rank
- * r owns [start + r*S, start + (r+1)*S) of it with S = size / D.
+ * two buckets; each bucket is padded to a multiple of R * pad_unit, and rank
+ * r (of each instance) owns [start + r*S, start + (r+1)*S) of it with
+ * S = size / R, R = D / instances.  Pieces carry the rank inside the
+ * instance (0..R-1).
  * Host only: makes no CUDA call.  Errors: DOPT_E_ARG, DOPT_E_NOMEM.
  */
 int dopt_build_range_map(const int64_t *param_sizes, int32_t n_params, const uint8_t *wd_mask,
@@ -169,13 +183,17 @@ void dopt_layout_free(dopt_layout *layout);
  *
  *   for every owned element i (rank q owns it, param p holds it):
  *     g      = fp32 sum over r = 0..D-1, in rank order, of
- *              grad_scale * float(grad_replicas[r][i])   (each op rounded)
+ *              grad_scale * float(grad_replicas[r][i])   (each op rounded);
+ *              with several instances, the rank-order sum inside each
+ *              instance, then those sums in instance order
  *     m      = beta1*m + (1-beta1)*g
  *     v      = beta2*v + (1-beta2)*(g*g)
  *     w      = w * (1 - lr*weight_decay)          (only if p decays)
  *     w      = w - step_size * (m / (sqrt(v)/bc2_sqrt + eps))
  *     param_replicas[r][i] = bf16_rne(w)   for every r (DOPT_STEP_GATHER)
- *                                          or for r = q only (no flag)
+ *                                          or, without the flag, for the
+ *                                          replica of rank q in every
+ *                                          instance
  *     main_grad_out[i] = g                 (when main_grad_out is not NULL)
  *   with step_size = lr / (1 - beta1^step), bc2_sqrt = sqrt(1 - beta2^step)
  *   and the scalars (1-beta1), (1-beta2), (1-lr*wd), step_size, bc2_sqrt
@@ -254,7 +272,7 @@ int dopt_step_allreduce(const dopt_layout *layout, const dopt_adam_cfg *cfg, int
 /*
  * The all-gather of the params on its own (page 1, §4.4): for every rank q
  * and every element q owns, copy param_replicas[q][i] into every other
- * replica.  Padding is not copied.  param_replicas: host array of D device
+ * replica of q's instance.  Padding is not copied.  param_replicas: host array of D device
  * bf16 pointers (16-byte aligned).  Asynchronous on `stream`.
  * Errors: DOPT_E_ARG, DOPT_E_ALIGN, DOPT_E_STATE, DOPT_E_CUDA.
  */

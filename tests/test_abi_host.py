@@ -212,3 +212,34 @@ def test_bucket_and_allreduce_argument_checks_before_cuda(lib):
     assert B.lib().dopt_allreduce(L.handle, gp, 0, 1.0, None) in (B.DOPT_E_STATE, B.DOPT_E_CUDA)
     assert B.lib().dopt_step_allreduce(L.handle, ctypes.byref(cfg), 0, gp, 0, 0x30000, 0x40000,
                                        0x50000, gp, 1, None, None) == B.DOPT_E_ARG
+
+
+@pytest.mark.parametrize("D,instances", [(8, 2), (8, 4), (8, 8), (6, 3), (16, 4), (12, 2)])
+def test_range_map_with_instances_matches_oracle(lib, D, instances):
+    """With several optimizer instances the buckets are sharded R = D/I
+    ways: the layout equals the oracle's for R ranks."""
+    rng = np.random.default_rng(D * 10 + instances)
+    R = D // instances
+    for _ in range(20):
+        n = int(rng.integers(1, 40))
+        sizes = [int(x) for x in rng.integers(0, 3000, n)]
+        bucket = int(rng.choice([0, int(rng.integers(1, 9000))]))
+        pad = int(rng.integers(1, 70))
+        L = B.dopt_build_range_map(sizes, D, bucket, pad, instances=instances)
+        O = oracle.range_map(sizes, R, bucket, pad)
+        assert L.R == R and L.padded_numel == O.numel
+        assert L.buckets() == list(zip(O.bucket_start.tolist(), O.bucket_end.tolist()))
+        assert L.pieces() == O.pieces
+
+
+def test_instances_errors(lib):
+    for D, instances in ((8, 3), (4, -1), (6, 4)):
+        with pytest.raises(B.DoptError) as e:
+            B.dopt_build_range_map([10, 20], D, 0, 1, instances=instances)
+        assert e.value.code == B.DOPT_E_ARG
+    cfg = B.dopt_layout_cfg(4, 1, 0, 1, 7)  # reserved must be 0
+    out = ctypes.c_void_p()
+    sizes = (ctypes.c_int64 * 1)(10)
+    assert B.lib().dopt_build_range_map(sizes, 1, None, ctypes.byref(cfg), ctypes.byref(out)) == B.DOPT_E_ARG
+    L = B.dopt_build_range_map([10, 20], 8, 0, 1, instances=0)  # 0 means one instance
+    assert L.padded_numel == B.dopt_build_range_map([10, 20], 8, 0, 1).padded_numel

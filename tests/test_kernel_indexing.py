@@ -98,8 +98,8 @@ def simulate(numel, runs, tile_run, run_begin, run_limit, tile0, tiles, visits):
     return vector_accesses
 
 
-def check_layout(sizes, D, bucket, pad, wd=None):
-    L = B.dopt_build_range_map(sizes, D, bucket, pad, wd)
+def check_layout(sizes, D, bucket, pad, wd=None, instances=1):
+    L = B.dopt_build_range_map(sizes, D, bucket, pad, wd, instances=instances)
     decays = wd if wd is not None else [1] * len(sizes)
     runs, bucket_run = runs_from_pieces(L.pieces(), decays, L.n_buckets)
     for (a, b, _), (c, d, _) in zip(runs, runs[1:]):
@@ -159,3 +159,11 @@ def test_vector_path_dominates_on_aligned_layouts():
     sizes = [8 * 1000, 8 * 333, 8 * 2049]
     nvec = check_layout(sizes, 4, 0, 8)
     assert nvec == sum(sizes) // 8
+
+
+@pytest.mark.parametrize("D,instances", [(8, 2), (6, 3), (16, 4), (8, 8)])
+def test_instance_layouts(D, instances):
+    """Layouts sharded R = D / instances ways (runs carry the rank inside the
+    instance)."""
+    check_layout([5000, 1, 7, 300, 20000, 3, 9999], D, 0, 1, [1, 0, 1, 0, 1, 1, 0], instances)
+    check_layout([31000, 17, 64000, 5], D, 30000, 3, [1, 0, 1, 0], instances)

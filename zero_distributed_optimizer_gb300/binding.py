@@ -55,7 +55,8 @@ class dopt_piece(ctypes.Structure):
 
 class dopt_layout_cfg(ctypes.Structure):
     _fields_ = [("D", ctypes.c_int32), ("pad_unit", ctypes.c_int32),
-                ("bucket_elems", ctypes.c_int64)]
+                ("bucket_elems", ctypes.c_int64), ("instances", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 class dopt_adam_cfg(ctypes.Structure):
@@ -151,9 +152,11 @@ class AdamConfig:
 class Layout:
     """Owner of a dopt_layout handle (freed with the object)."""
 
-    def __init__(self, handle: int, D: int, n_params: int):
+    def __init__(self, handle: int, D: int, n_params: int, instances: int = 1):
         self._h = ctypes.c_void_p(handle)
         self.D = D
+        self.instances = instances
+        self.R = D // instances  # ranks per instance: the shard count of a bucket
         self.n_params = n_params
         numel = ctypes.c_int64()
         nb = ctypes.c_int32()
@@ -219,8 +222,10 @@ class Layout:
 
 
 def dopt_build_range_map(param_sizes, D: int, bucket_elems: int = 0, pad_unit: int = 1,
-                         wd_mask=None) -> Layout:
-    """Flat-buffer layout and four-way range map (host only, no CUDA call)."""
+                         wd_mask=None, instances: int = 1) -> Layout:
+    """Flat-buffer layout and four-way range map (host only, no CUDA call).
+    ``instances`` > 1 groups the D ranks into that many optimizer instances
+    of D // instances ranks each (page 1 §5)."""
     n = len(param_sizes)
     sizes = (ctypes.c_int64 * max(n, 1))(*[int(s) for s in param_sizes])
     wd = None
@@ -228,10 +233,10 @@ def dopt_build_range_map(param_sizes, D: int, bucket_elems: int = 0, pad_unit: i
         if len(wd_mask) != n:
             raise DoptError(DOPT_E_ARG, "wd_mask length differs from param_sizes")
         wd = (ctypes.c_uint8 * max(n, 1))(*[1 if x else 0 for x in wd_mask])
-    cfg = dopt_layout_cfg(int(D), int(pad_unit), int(bucket_elems))
+    cfg = dopt_layout_cfg(int(D), int(pad_unit), int(bucket_elems), int(instances), 0)
     out = ctypes.c_void_p()
     _check(lib().dopt_build_range_map(sizes, n, wd, ctypes.byref(cfg), ctypes.byref(out)))
-    return Layout(out.value, int(D), n)
+    return Layout(out.value, int(D), n, max(int(instances), 1))
 
 
 def _stream_handle(stream):

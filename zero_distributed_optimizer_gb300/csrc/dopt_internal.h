@@ -12,13 +12,14 @@
 constexpr int64_t kDoptTileElems = 2048;
 
 // Run metadata bits: bit 0 = the run's params take weight decay; bits 8..15
-// = the rank that owns the run.
+// = the rank (inside its instance) that owns the run.
 constexpr int32_t kRunDecays = 1;
 constexpr int kRunRankShift = 8;
 
 struct dopt_layout {
-    dopt_layout_cfg cfg{};
-    int64_t numel = 0;  // padded buffer length
+    dopt_layout_cfg cfg{};  // instances normalised to >= 1
+    int32_t R = 1;          // ranks per instance (D / instances)
+    int64_t numel = 0;      // padded buffer length
 
     std::vector<int64_t> param_start, param_end;
     std::vector<int32_t> param_bucket;

@@ -30,9 +30,9 @@ namespace {
 
 // Greedy buckets and padding: params at consecutive offsets; the open
 // bucket closes once its unpadded count reaches bucket_elems; each bucket
-// is padded to a multiple of D * pad_unit (page 1, §2 and §5).
+// is padded to a multiple of R * pad_unit (page 1, §2 and §5).
 void place_params(dopt_layout &L, const int64_t *sizes, int32_t n) {
-    const int64_t unit = int64_t(L.cfg.D) * L.cfg.pad_unit;
+    const int64_t unit = int64_t(L.R) * L.cfg.pad_unit;
     L.param_start.resize(n);
     L.param_end.resize(n);
     L.param_bucket.resize(n);
@@ -64,11 +64,11 @@ void place_params(dopt_layout &L, const int64_t *sizes, int32_t n) {
 // with the current rank's range and advances whichever ends first.
 void bucket_pieces(dopt_layout &L, int32_t k, int32_t p_begin, int32_t p_end) {
     const dopt_range b = L.buckets[size_t(k)];
-    const int32_t D = L.cfg.D;
-    const int64_t S = (b.end - b.start) / D;
+    const int32_t R = L.R;
+    const int64_t S = (b.end - b.start) / R;
     if (S == 0) return;
     int32_t p = p_begin, r = 0;
-    while (p < p_end && r < D) {
+    while (p < p_end && r < R) {
         const int64_t lo = b.start + r * S, hi = lo + S;
         const int64_t a = L.param_start[size_t(p)], e = L.param_end[size_t(p)];
         const int64_t x = std::max(a, lo), y = std::min(e, hi);
@@ -163,6 +163,10 @@ int dopt_build_range_map(const int64_t *param_sizes, int32_t n_params, const uin
         return fail(DOPT_E_ARG, "dopt_build_range_map: pad_unit=%d < 1", cfg->pad_unit);
     if (cfg->bucket_elems < 0)
         return fail(DOPT_E_ARG, "dopt_build_range_map: bucket_elems < 0");
+    const int32_t instances = cfg->instances == 0 ? 1 : cfg->instances;
+    if (instances < 1 || cfg->D % instances != 0 || cfg->reserved != 0)
+        return fail(DOPT_E_ARG, "dopt_build_range_map: instances=%d does not divide D=%d",
+                    cfg->instances, cfg->D);
     int64_t total = 0;
     for (int32_t p = 0; p < n_params; ++p) {
         if (param_sizes[p] < 0)
@@ -176,15 +180,18 @@ int dopt_build_range_map(const int64_t *param_sizes, int32_t n_params, const uin
     try {
         L = new dopt_layout();
         L->cfg = *cfg;
+        L->cfg.instances = instances;
+        L->R = cfg->D / instances;
         L->param_decays.assign(size_t(n_params), 1);
         if (wd_mask)
             for (int32_t p = 0; p < n_params; ++p) L->param_decays[size_t(p)] = wd_mask[p] ? 1 : 0;
         place_params(*L, param_sizes, n_params);
         for (const dopt_range &b : L->buckets)
-            if ((b.end - b.start) % cfg->D != 0) {
+            if ((b.end - b.start) % L->R != 0) {
+                const int32_t R = L->R;
                 delete L;
-                return fail(DOPT_E_LAYOUT, "bucket [%lld, %lld) does not divide by D=%d",
-                            (long long)b.start, (long long)b.end, cfg->D);
+                return fail(DOPT_E_LAYOUT, "bucket [%lld, %lld) does not divide by R=%d",
+                            (long long)b.start, (long long)b.end, R);
             }
         if ((L->numel + kDoptTileElems - 1) / kDoptTileElems >= (int64_t(1) << 31)) {
             delete L;

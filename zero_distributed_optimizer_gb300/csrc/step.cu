@@ -81,6 +81,7 @@ struct StepArgs {
     const float *clip_coef;     // kFromMain: device scalar
     RunView rv;
     int32_t D;
+    int32_t R;  // ranks per instance (D with one instance)
     int32_t gather;
     Scalars sc;
 };
@@ -106,6 +107,7 @@ struct NormArgs {
     RunView rv;
     int64_t n_tiles;
     int32_t D;
+    int32_t R;
     float scale;
     float max_norm;
 };
@@ -114,6 +116,7 @@ struct GatherArgs {
     void *params[DOPT_MAX_D];
     RunView rv;
     int32_t D;
+    int32_t R;
 };
 
 // The grads are read, reduced and written back in place (each element by
@@ -123,6 +126,7 @@ struct AllReduceArgs {
     const void *grads[DOPT_MAX_D];
     RunView rv;
     int32_t D;
+    int32_t R;
     float scale;
 };
 
@@ -283,7 +287,11 @@ struct GradVec<float> {
     }
 };
 
-// Scaled rank-order fp32 reduction of 8 elements over the D replicas.
+// Scaled rank-order fp32 reduction of 8 elements over the D replicas.  The
+// compile-time-D form serves one instance; the run-time form reduces each
+// group of R consecutive replicas in rank order and adds the groups' sums in
+// group order (several optimizer instances; with R = D the last group's sum
+// is copied, so the result is the plain rank-order sum).
 template <typename G, int DC, typename Args>
 __device__ __forceinline__ void reduce_vec(const Args &a, float scale, int64_t e0,
                                            float (&acc)[8]) {
@@ -303,6 +311,8 @@ __device__ __forceinline__ void reduce_vec(const Args &a, float scale, int64_t e
         }
     } else {
         constexpr int kBatch = 4;
+        float part[8];
+        int in_group = 0;  // position of the next replica inside its group
         for (int r0 = 0; r0 < a.D; r0 += kBatch) {
             GradVec<G> g[kBatch];
 #pragma unroll
@@ -310,27 +320,37 @@ __device__ __forceinline__ void reduce_vec(const Args &a, float scale, int64_t e
                 if (r0 + u < a.D) g[u].load(a.grads[r0 + u], e0);
 #pragma unroll
             for (int u = 0; u < kBatch; ++u) {
-                if (r0 + u >= a.D) break;
+                const int r = r0 + u;
+                if (r >= a.D) break;
                 float f[8];
                 g[u].get(f);
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const float x = __fmul_rn(scale, f[k]);
-                    acc[k] = (r0 + u) == 0 ? x : __fadd_rn(acc[k], x);
+                    part[k] = in_group == 0 ? x : __fadd_rn(part[k], x);
+                }
+                if (++in_group == a.R) {
+                    in_group = 0;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        acc[k] = r + 1 == a.R ? part[k] : __fadd_rn(acc[k], part[k]);
                 }
             }
         }
     }
 }
 
-// Scaled rank-order fp32 reduction of one element over the D replicas.
+// The same reduction for one element: groups of R replicas in rank order,
+// then the groups' sums in group order.
 template <typename G>
-__device__ __forceinline__ float reduce_scalar(const void *const *grads, int D, float scale,
-                                               int64_t e) {
-    float g = 0.0f;
+__device__ __forceinline__ float reduce_scalar(const void *const *grads, int D, int R,
+                                               float scale, int64_t e) {
+    float g = 0.0f, part = 0.0f;
     for (int r = 0; r < D; ++r) {
         const float x = __fmul_rn(scale, load_grad_scalar<G>(grads[r], e));
-        g = r == 0 ? x : __fadd_rn(g, x);
+        const int in_group = r % R;
+        part = in_group == 0 ? x : __fadd_rn(part, x);
+        if (in_group == R - 1) g = r + 1 == R ? part : __fadd_rn(g, part);
     }
     return g;
 }
@@ -400,7 +420,8 @@ __device__ __forceinline__ void full_vector(const StepArgs &a, int64_t e0, int32
         }
     } else {
         const int q = meta >> kRunRankShift;
-        st_stream(static_cast<__nv_bfloat16 *>(a.params[q]) + e0, packed);
+        for (int r = q; r < a.D; r += a.R)
+            st_stream(static_cast<__nv_bfloat16 *>(a.params[r]) + e0, packed);
     }
 }
 
@@ -417,7 +438,7 @@ __device__ __noinline__ void mixed_vector(const StepArgs &a, int64_t e0, int j) 
         if constexpr (MODE == kFromMain)
             g = __fmul_rn(a.main_grad_in[e], *a.clip_coef);
         else
-            g = reduce_scalar<G>(a.grads, D, a.sc.scale, e);
+            g = reduce_scalar<G>(a.grads, D, a.R, a.sc.scale, e);
         if constexpr (MODE == kWriteGrads)
             for (int r = 0; r < D; ++r) store_grad_scalar<G>(a.grads[r], e, g);
         float w = a.master[e], m = a.exp_avg[e], v = a.exp_avg_sq[e];
@@ -430,7 +451,8 @@ __device__ __noinline__ void mixed_vector(const StepArgs &a, int64_t e0, int j) 
         if (a.gather) {
             for (int r = 0; r < D; ++r) static_cast<uint16_t *>(a.params[r])[e] = bits;
         } else {
-            static_cast<uint16_t *>(a.params[meta >> kRunRankShift])[e] = bits;
+            for (int r = meta >> kRunRankShift; r < D; r += a.R)
+                static_cast<uint16_t *>(a.params[r])[e] = bits;
         }
     }
 }
@@ -468,7 +490,7 @@ __global__ void __launch_bounds__(kThreads) dopt_allreduce_kernel(const __grid_c
         for (int k = 0; k < kVec && !done; ++k) {
             const int64_t e = e0 + k;
             if (!owned_at(a.rv, e, j, done)) continue;
-            const float g = reduce_scalar<G>(a.grads, D, a.scale, e);
+            const float g = reduce_scalar<G>(a.grads, D, a.R, a.scale, e);
             for (int r = 0; r < D; ++r) store_grad_scalar<G>(a.grads[r], e, g);
         }
     }
@@ -516,7 +538,7 @@ __global__ void __launch_bounds__(kThreads) dopt_rs_norm_kernel(const __grid_con
             for (int k = 0; k < kVec && !done; ++k) {
                 const int64_t e = e0 + k;
                 if (!owned_at(a.rv, e, j, done)) continue;
-                const float g = reduce_scalar<G>(a.grads, D, a.scale, e);
+                const float g = reduce_scalar<G>(a.grads, D, a.R, a.scale, e);
                 a.main_grad[e] = g;
                 local += double(__fmul_rn(g, g));
             }
@@ -565,18 +587,22 @@ __global__ void __launch_bounds__(kThreads) dopt_gather_kernel(const __grid_cons
     const VecKind kind = locate(a.rv, tile, e0, j);
     if (kind == kFull) {
         const int q = a.rv.run_meta[j] >> kRunRankShift;
-        const uint4 val = ld_stream(static_cast<const __nv_bfloat16 *>(a.params[q]) + e0);
-        for (int r = 0; r < a.D; ++r)
-            if (r != q) st_stream(static_cast<__nv_bfloat16 *>(a.params[r]) + e0, val);
+        for (int base = 0; base < a.D; base += a.R) {
+            const uint4 val = ld_stream(static_cast<const __nv_bfloat16 *>(a.params[base + q]) + e0);
+            for (int r = base; r < base + a.R; ++r)
+                if (r != base + q) st_stream(static_cast<__nv_bfloat16 *>(a.params[r]) + e0, val);
+        }
     } else if (kind == kMixed) {
         bool done = false;
         for (int k = 0; k < kVec && !done; ++k) {
             const int64_t e = e0 + k;
             if (!owned_at(a.rv, e, j, done)) continue;
             const int q = a.rv.run_meta[j] >> kRunRankShift;
-            const uint16_t bits = static_cast<const uint16_t *>(a.params[q])[e];
-            for (int r = 0; r < a.D; ++r)
-                if (r != q) static_cast<uint16_t *>(a.params[r])[e] = bits;
+            for (int base = 0; base < a.D; base += a.R) {
+                const uint16_t bits = static_cast<const uint16_t *>(a.params[base + q])[e];
+                for (int r = base; r < base + a.R; ++r)
+                    if (r != base + q) static_cast<uint16_t *>(a.params[r])[e] = bits;
+            }
         }
     }
 }
@@ -641,6 +667,10 @@ StepKernel pick_step_kernel(int D) {
         default: return dopt_step_kernel<G, 0, MODE>;
     }
 }
+
+// The compile-time-D kernels serve one instance only; several instances
+// take the run-time form, which reduces group by group.
+int kernel_D(const dopt_layout *L) { return L->cfg.instances > 1 ? 0 : L->cfg.D; }
 
 template <int MODE>
 StepKernel step_kernel_for(dopt_dtype grad_dtype, int D) {
@@ -756,6 +786,7 @@ void fill_step_args(StepArgs &a, const dopt_layout *L, const dopt_adam_cfg *cfg,
     a.exp_avg = exp_avg;
     a.exp_avg_sq = exp_avg_sq;
     a.D = D;
+    a.R = L->R;
     a.gather = (flags & DOPT_STEP_GATHER) ? 1 : 0;
     a.sc = make_scalars(*cfg, step);
 }
@@ -782,7 +813,7 @@ int launch_step(const char *who, const dopt_layout *L, const dopt_adam_cfg *cfg,
     fill_step_args(a, L, cfg, step, grad_replicas, master, exp_avg, exp_avg_sq, param_replicas,
                    flags);
     a.main_grad_out = main_grad_out;
-    StepKernel k = step_kernel_for<MODE>(grad_dtype, L->cfg.D);
+    StepKernel k = step_kernel_for<MODE>(grad_dtype, kernel_D(L));
     k<<<unsigned(tiles), kThreads, 0, stream>>>(a);
     return launch_error(who, "step");
 }
@@ -803,9 +834,10 @@ int launch_clipped(const char *who, const dopt_layout *L, const dopt_adam_cfg *c
     na.norm_out = norm_out;
     na.rv = whole_view(L, &na.n_tiles);
     na.D = D;
+    na.R = L->R;
     na.scale = cfg->grad_scale;
     na.max_norm = max_norm;
-    NormKernel nk = norm_kernel_for(grad_dtype, D);
+    NormKernel nk = norm_kernel_for(grad_dtype, kernel_D(L));
     const int grid_a = norm_grid(nk, na.n_tiles, L->device);
     cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(unsigned int), stream);
     if (e != cudaSuccess) return fail(DOPT_E_CUDA, "%s: workspace reset: %s", who, cudaGetErrorString(e));
@@ -820,7 +852,7 @@ int launch_clipped(const char *who, const dopt_layout *L, const dopt_adam_cfg *c
                    flags);
     a.main_grad_in = main_grad;
     a.clip_coef = &ws->coef;
-    StepKernel k = pick_step_kernel<float, kFromMain>(D);
+    StepKernel k = pick_step_kernel<float, kFromMain>(kernel_D(L));
     k<<<unsigned(tiles), kThreads, 0, stream>>>(a);
     return launch_error(who, "step");
 }
@@ -914,9 +946,10 @@ extern "C" int dopt_allreduce(const dopt_layout *L, void *const *grad_replicas,
     if (rc != DOPT_OK) return rc;
     for (int r = 0; r < D; ++r) a.grads[r] = grad_replicas[r];
     a.D = D;
+    a.R = L->R;
     a.scale = grad_scale;
-    AllReduceKernel k = grad_dtype == DOPT_BF16 ? pick_allreduce_kernel<__nv_bfloat16>(D)
-                                                : pick_allreduce_kernel<float>(D);
+    AllReduceKernel k = grad_dtype == DOPT_BF16 ? pick_allreduce_kernel<__nv_bfloat16>(kernel_D(L))
+                                                : pick_allreduce_kernel<float>(kernel_D(L));
     k<<<unsigned(tiles), kThreads, 0, stream>>>(a);
     return launch_error(who, "all-reduce");
 }
@@ -998,7 +1031,7 @@ extern "C" int dopt_step_clipped_noalloc(const dopt_layout *L, const dopt_adam_c
     rc = check_device_tables(L, who);
     if (rc != DOPT_OK) return rc;
     const int64_t n_tiles = (L->numel + kDoptTileElems - 1) / kDoptTileElems;
-    const int grid_a = norm_grid(norm_kernel_for(grad_dtype, L->cfg.D), n_tiles, L->device);
+    const int grid_a = norm_grid(norm_kernel_for(grad_dtype, kernel_D(L)), n_tiles, L->device);
     const size_t need = offsetof(ClipWorkspace, partial) + size_t(grid_a) * sizeof(double);
     if (need > sizeof(g_noalloc_scratch))
         return fail(DOPT_E_ARG, "%s: the norm pass needs %zu bytes of scratch (%d CTAs), the "
@@ -1019,7 +1052,7 @@ extern "C" int dopt_gather(const dopt_layout *L, void *const *param_replicas, cu
     const int D = L->cfg.D;
     int rc = check_replicas(who, D, const_cast<const void *const *>(param_replicas));
     if (rc != DOPT_OK) return rc;
-    if (D == 1) return DOPT_OK;
+    if (L->R == 1) return DOPT_OK;  // every rank is alone in its instance
     GatherArgs a{};
     int64_t tiles = 0;
     a.rv = whole_view(L, &tiles);
@@ -1028,6 +1061,7 @@ extern "C" int dopt_gather(const dopt_layout *L, void *const *param_replicas, cu
     if (rc != DOPT_OK) return rc;
     for (int r = 0; r < D; ++r) a.params[r] = param_replicas[r];
     a.D = D;
+    a.R = L->R;
     dopt_gather_kernel<<<unsigned(tiles), kThreads, 0, stream>>>(a);
     return launch_error(who, "gather");
 }
