@@ -55,6 +55,8 @@ def main(argv=None):
                     help="the fused step, dopt_gather alone, the clipped step, the step as "
                          "one launch per bucket, dopt_allreduce alone, or the step with "
                          "force_all_reduce")
+    ap.add_argument("--streams", type=int, default=1,
+                    help="buckets mode: bucket k is launched on stream k mod STREAMS")
     args = ap.parse_args(argv)
 
     libbuild.build()
@@ -75,6 +77,7 @@ def main(argv=None):
     if args.mode == "clipped":
         main_grad = torch.empty(N, device=dev)
         ws = B.clip_workspace(dev)
+    streams = [torch.cuda.current_stream()] + [torch.cuda.Stream(dev) for _ in range(args.streams - 1)]
     torch.cuda.synchronize()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     t = 0
@@ -85,8 +88,18 @@ def main(argv=None):
         if args.mode == "gather":
             B.dopt_gather(L, params)
         elif args.mode == "buckets":
+            # fork the side streams off the main one, launch, join them back
+            fork = torch.cuda.Event()
+            fork.record(streams[0])
+            for s_ in streams[1:]:
+                s_.wait_event(fork)
             for k in range(L.n_buckets):
-                B.dopt_step_buckets(L, adam, t, k, 1, grads, master, m, v, params)
+                s_ = streams[k % len(streams)]
+                B.dopt_step_buckets(L, adam, t, k, 1, grads, master, m, v, params, stream=s_)
+            for s_ in streams[1:]:
+                join = torch.cuda.Event()
+                join.record(s_)
+                streams[0].wait_event(join)
         elif args.mode == "allreduce":
             B.dopt_allreduce(L, grads, 1.0)
         elif args.mode == "step_allreduce":
@@ -104,7 +117,7 @@ def main(argv=None):
                 "step_allreduce": step_bytes + w.D * w.grad_bytes}[args.mode]
     bytes_per = w.numel * per_elem
     print(json.dumps({"workload": w.name, "N": w.numel, "padded_numel": N, "D": w.D,
-                      "mode": args.mode, "n_buckets": L.n_buckets,
+                      "mode": args.mode, "n_buckets": L.n_buckets, "streams": args.streams,
                       "launches": args.launches, "ms_per_launch": ms,
                       "algorithmic_bytes_per_launch": bytes_per,
                       "gbs": bytes_per / (ms / 1e3) / 1e9}))
