@@ -123,6 +123,17 @@ typedef enum { DOPT_BF16 = 0, DOPT_FP32 = 1 } dopt_dtype;
 
 /* dopt_step flags. */
 #define DOPT_STEP_GATHER 1u /* fuse the all-gather: write all D replicas */
+/*
+ * The grad replicas are pinned host buffers (cudaHostAlloc, or
+ * cudaHostRegister'ed) that the device reads in place over the host link,
+ * instead of device buffers: no staging copy and no device memory for the
+ * grads.  Each pointer is resolved with cudaPointerGetAttributes; anything
+ * that is not registered host memory with a device mapping is refused with
+ * DOPT_E_ARG before any launch.  Accepted by dopt_step, dopt_step_buckets,
+ * dopt_step_allreduce (which then writes the host buffers) and
+ * dopt_step_clipped.
+ */
+#define DOPT_STEP_HOST_GRADS 2u
 
 typedef struct dopt_layout dopt_layout;
 
@@ -210,7 +221,7 @@ void dopt_layout_free(dopt_layout *layout);
  *                   device fp32, padded_numel elements each, buffer-indexed
  *                   (the union of all D ranks' shards); updated in place
  *   param_replicas  host array of D device pointers, bf16, padded_numel each
- *   flags           0 or DOPT_STEP_GATHER
+ *   flags           DOPT_STEP_GATHER and/or DOPT_STEP_HOST_GRADS
  *   main_grad_out   nullable device fp32[padded_numel]: the reduce-scattered
  *                   fp32 main grad of every owned element
  *   stream          CUDA stream to launch on

@@ -28,6 +28,9 @@ def run_workload(w: W.Workload, seed: int = 0, steps=None, n_edges=48, n_random=
     assert L.padded_numel == O.numel and L.pieces() == O.pieces  # bit-exact range map
     N = L.padded_numel
     wins = sample_windows(L.buckets(), O.pieces, N, seed, n_edges=n_edges, n_random=n_random)
+    if N > (1 << 31):  # both sides of the int32 element boundary
+        from parity import merge_windows
+        wins = merge_windows(wins + [((1 << 31) - 4096, (1 << 31) + 4096)], N)
     master, m, v = W.make_state(w, N, DEV)
     params = W.make_params(master, w.D)
     host = []
@@ -81,3 +84,15 @@ def test_sweep_256m_full_size(D, bucket_mi):
 def test_moe_many_small_fp32_grads_full_size():
     compared, _ = run_workload(W.moe_many_small(), seed=5)
     assert compared > 500_000
+
+
+def test_beyond_two_billion_elements():
+    """A buffer of more than 2^31 elements (element offsets beyond int32),
+    D=1, bf16 grads, two buckets: sampled windows, including both sides of
+    element 2^31, match the oracle."""
+    big = (1 << 31) + 12345
+    w = W.Workload("beyond_2g", (big // 2, 3, big - big // 2 - 3), (1, 0, 1), D=1,
+                   bucket_elems=big // 2, pad_unit=64, grad_dtype="bf16",
+                   grad_dist="normal1e-3", m_init="zero", v_init="zero", steps=2)
+    compared, _ = run_workload(w, seed=9, n_edges=16, n_random=4)
+    assert compared > 100_000

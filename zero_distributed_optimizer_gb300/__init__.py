@@ -17,6 +17,7 @@ from .binding import (  # noqa: F401
     DOPT_MAX_D,
     DOPT_OK,
     DOPT_STEP_GATHER,
+    DOPT_STEP_HOST_GRADS,
     AdamConfig,
     DoptError,
     Layout,

@@ -29,6 +29,7 @@ DOPT_MAX_D = 64
 DOPT_BF16 = 0
 DOPT_FP32 = 1
 DOPT_STEP_GATHER = 1
+DOPT_STEP_HOST_GRADS = 2
 DOPT_CLIP_WORKSPACE_BYTES = 16384
 
 _ERROR_NAMES = {DOPT_E_ARG: "DOPT_E_ARG", DOPT_E_LAYOUT: "DOPT_E_LAYOUT",
@@ -258,8 +259,20 @@ def _check_tensor(t, name, dtype, numel, device):
         raise DoptError(DOPT_E_ARG, f"{name} must be contiguous with >= {numel} elements")
 
 
+def _check_grads(grad_replicas, gdt, N, device, host_grads):
+    """Device grads on the step's device, or (host_grads) pinned CPU tensors
+    that the library reads in place."""
+    for i, g in enumerate(grad_replicas):
+        if host_grads:
+            if g.device.type != "cpu" or not g.is_pinned():
+                raise DoptError(DOPT_E_ARG, f"grad_replicas[{i}] must be a pinned CPU tensor")
+            _check_tensor(g, f"grad_replicas[{i}]", gdt, N, g.device)
+        else:
+            _check_tensor(g, f"grad_replicas[{i}]", gdt, N, device)
+
+
 def _step_pointers(layout: Layout, grad_replicas, master, exp_avg, exp_avg_sq, param_replicas,
-                   main_grad_out):
+                   main_grad_out, host_grads=False):
     import torch
 
     D = layout.D
@@ -272,8 +285,7 @@ def _step_pointers(layout: Layout, grad_replicas, master, exp_avg, exp_avg_sq, p
     gdt = grad_replicas[0].dtype
     if gdt not in (torch.bfloat16, torch.float32):
         raise DoptError(DOPT_E_ARG, f"grad dtype {gdt} is not bf16 or fp32")
-    for i, g in enumerate(grad_replicas):
-        _check_tensor(g, f"grad_replicas[{i}]", gdt, N, device)
+    _check_grads(grad_replicas, gdt, N, device, host_grads)
     for name, t in (("master", master), ("exp_avg", exp_avg), ("exp_avg_sq", exp_avg_sq)):
         _check_tensor(t, name, torch.float32, N, device)
     for i, p in enumerate(param_replicas):
@@ -290,18 +302,19 @@ def _step_pointers(layout: Layout, grad_replicas, master, exp_avg, exp_avg_sq, p
 def dopt_step_buckets(layout: Layout, adam: AdamConfig, step: int, first_bucket: int,
                       n_buckets: int, grad_replicas, master, exp_avg, exp_avg_sq,
                       param_replicas, gather: bool = True, main_grad_out=None,
-                      stream=None) -> None:
+                      stream=None, host_grads: bool = False) -> None:
     """The step over buckets [first_bucket, first_bucket + n_buckets) only."""
     import torch
 
     device, gp, pp, dt, mg = _step_pointers(layout, grad_replicas, master, exp_avg, exp_avg_sq,
-                                            param_replicas, main_grad_out)
+                                            param_replicas, main_grad_out, host_grads)
+    flags = (DOPT_STEP_GATHER if gather else 0) | (DOPT_STEP_HOST_GRADS if host_grads else 0)
     cfg = adam.to_c()
     with torch.cuda.device(device):
         _check(lib().dopt_step_buckets(
             layout.handle, ctypes.byref(cfg), int(step), int(first_bucket), int(n_buckets), gp,
-            dt, master.data_ptr(), exp_avg.data_ptr(), exp_avg_sq.data_ptr(), pp,
-            DOPT_STEP_GATHER if gather else 0, mg, _stream_handle(stream)))
+            dt, master.data_ptr(), exp_avg.data_ptr(), exp_avg_sq.data_ptr(), pp, flags, mg,
+            _stream_handle(stream)))
 
 
 def dopt_step_allreduce(layout: Layout, adam: AdamConfig, step: int, grad_replicas, master,
@@ -345,43 +358,25 @@ def dopt_allreduce(layout: Layout, grad_replicas, grad_scale: float, stream=None
 
 def dopt_step(layout: Layout, adam: AdamConfig, step: int, grad_replicas, master, exp_avg,
               exp_avg_sq, param_replicas, gather: bool = True, main_grad_out=None,
-              stream=None) -> None:
+              stream=None, host_grads: bool = False) -> None:
     """One fused ZeRO-1 step (reduce-scatter, AdamW, write-back, all-gather).
 
-    grad_replicas: D bf16 or fp32 CUDA tensors; master/exp_avg/exp_avg_sq:
-    fp32; param_replicas: D bf16; main_grad_out: optional fp32.  Each holds
-    at least layout.padded_numel elements.  Asynchronous on `stream`
-    (default: torch's current stream).
+    grad_replicas: D bf16 or fp32 CUDA tensors (or, with host_grads, pinned
+    CPU tensors the kernel reads in place); master/exp_avg/exp_avg_sq: fp32;
+    param_replicas: D bf16; main_grad_out: optional fp32.  Each holds at
+    least layout.padded_numel elements.  Asynchronous on `stream` (default:
+    torch's current stream).
     """
     import torch
 
-    D = layout.D
-    if len(grad_replicas) != D or len(param_replicas) != D:
-        raise DoptError(DOPT_E_ARG, f"need {D} grad and {D} param replicas")
-    N = layout.padded_numel
-    device = master.device
-    if device.type != "cuda":
-        raise DoptError(DOPT_E_ARG, "dopt_step needs CUDA tensors (no CPU path exists)")
-    gdt = grad_replicas[0].dtype
-    if gdt not in (torch.bfloat16, torch.float32):
-        raise DoptError(DOPT_E_ARG, f"grad dtype {gdt} is not bf16 or fp32")
-    for i, g in enumerate(grad_replicas):
-        _check_tensor(g, f"grad_replicas[{i}]", gdt, N, device)
-    for name, t in (("master", master), ("exp_avg", exp_avg), ("exp_avg_sq", exp_avg_sq)):
-        _check_tensor(t, name, torch.float32, N, device)
-    for i, p in enumerate(param_replicas):
-        _check_tensor(p, f"param_replicas[{i}]", torch.bfloat16, N, device)
-    if main_grad_out is not None:
-        _check_tensor(main_grad_out, "main_grad_out", torch.float32, N, device)
-    gp = (ctypes.c_void_p * D)(*[g.data_ptr() for g in grad_replicas])
-    pp = (ctypes.c_void_p * D)(*[p.data_ptr() for p in param_replicas])
+    device, gp, pp, dt, mg = _step_pointers(layout, grad_replicas, master, exp_avg, exp_avg_sq,
+                                            param_replicas, main_grad_out, host_grads)
+    flags = (DOPT_STEP_GATHER if gather else 0) | (DOPT_STEP_HOST_GRADS if host_grads else 0)
     cfg = adam.to_c()
     with torch.cuda.device(device):
-        _check(lib().dopt_step(
-            layout.handle, ctypes.byref(cfg), int(step), gp,
-            DOPT_BF16 if gdt == torch.bfloat16 else DOPT_FP32, master.data_ptr(),
-            exp_avg.data_ptr(), exp_avg_sq.data_ptr(), pp, DOPT_STEP_GATHER if gather else 0,
-            None if main_grad_out is None else main_grad_out.data_ptr(), _stream_handle(stream)))
+        _check(lib().dopt_step(layout.handle, ctypes.byref(cfg), int(step), gp, dt,
+                               master.data_ptr(), exp_avg.data_ptr(), exp_avg_sq.data_ptr(), pp,
+                               flags, mg, _stream_handle(stream)))
 
 
 def clip_workspace(device=None):
@@ -498,19 +493,27 @@ def version() -> str:
 
 
 def step_from_host(layout: Layout, adam: AdamConfig, step: int, host_grads, dev_grads, master,
-                   exp_avg, exp_avg_sq, param_replicas, host_params_out=None, stream=None) -> None:
-    """The step for a caller whose grads sit in (pinned) host memory: copy the
-    D host grad replicas into the device buffers `dev_grads`, run dopt_step
-    with the all-gather, and copy replica 0 of the updated params back into
-    `host_params_out` (if given).  Everything is queued on `stream`; the
-    caller synchronises before reading `host_params_out`."""
+                   exp_avg, exp_avg_sq, param_replicas, host_params_out=None, stream=None,
+                   zero_copy: bool = False) -> None:
+    """The step for a caller whose grads sit in pinned host memory.
+
+    Staged (default): copy the D host grad replicas into the device buffers
+    `dev_grads`, then run dopt_step.  zero_copy: the kernel reads the pinned
+    host replicas in place over the host link (DOPT_STEP_HOST_GRADS);
+    `dev_grads` is not used.  Either way replica 0 of the updated params is
+    copied back into `host_params_out` (if given).  Everything is queued on
+    `stream`; the caller synchronises before reading `host_params_out`."""
     import torch
 
     s = torch.cuda.current_stream() if stream is None else stream
     with torch.cuda.stream(s):
-        for h, d in zip(host_grads, dev_grads):
-            d.copy_(h, non_blocking=True)
-        dopt_step(layout, adam, step, dev_grads, master, exp_avg, exp_avg_sq, param_replicas,
-                  gather=True, stream=s)
+        if zero_copy:
+            dopt_step(layout, adam, step, host_grads, master, exp_avg, exp_avg_sq, param_replicas,
+                      gather=True, stream=s, host_grads=True)
+        else:
+            for h, d in zip(host_grads, dev_grads):
+                d.copy_(h, non_blocking=True)
+            dopt_step(layout, adam, step, dev_grads, master, exp_avg, exp_avg_sq,
+                      param_replicas, gather=True, stream=s)
         if host_params_out is not None:
             host_params_out.copy_(param_replicas[0], non_blocking=True)

@@ -756,7 +756,7 @@ int check_step_args(const char *who, const dopt_layout *L, const dopt_adam_cfg *
     if (step < 1) return fail(DOPT_E_ARG, "%s: step=%lld < 1", who, (long long)step);
     if (grad_dtype != DOPT_BF16 && grad_dtype != DOPT_FP32)
         return fail(DOPT_E_ARG, "%s: unknown grad dtype %d", who, int(grad_dtype));
-    if (flags & ~uint32_t(DOPT_STEP_GATHER))
+    if (flags & ~uint32_t(DOPT_STEP_GATHER | DOPT_STEP_HOST_GRADS))
         return fail(DOPT_E_ARG, "%s: unknown flags 0x%x", who, flags);
     if (!(cfg->lr >= 0.0f) || !std::isfinite(cfg->lr) || !(cfg->beta1 >= 0.0f && cfg->beta1 < 1.0f) ||
         !(cfg->beta2 >= 0.0f && cfg->beta2 < 1.0f) || !(cfg->eps >= 0.0f) || !std::isfinite(cfg->eps) ||
@@ -771,6 +771,33 @@ int check_step_args(const char *who, const dopt_layout *L, const dopt_adam_cfg *
     if (!aligned16(master) || !aligned16(exp_avg) || !aligned16(exp_avg_sq) ||
         (main_grad && !aligned16(main_grad)))
         return fail(DOPT_E_ALIGN, "%s: state pointer is not 16-byte aligned", who);
+    return DOPT_OK;
+}
+
+// With DOPT_STEP_HOST_GRADS the grad pointers are pinned host buffers: each
+// is replaced by the device's mapping of it, and anything else is refused.
+int resolve_grads(const char *who, int D, const void *const *grad_replicas, uint32_t flags,
+                  const void **out) {
+    using dopt::fail;
+    for (int r = 0; r < D; ++r) out[r] = grad_replicas[r];
+    if (!(flags & DOPT_STEP_HOST_GRADS)) return DOPT_OK;
+    for (int r = 0; r < D; ++r) {
+        cudaPointerAttributes at{};
+        cudaError_t e = cudaPointerGetAttributes(&at, grad_replicas[r]);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(DOPT_E_ARG, "%s: grad replica %d: cudaPointerGetAttributes: %s", who, r,
+                        cudaGetErrorString(e));
+        }
+        if (at.type != cudaMemoryTypeHost || !at.devicePointer)
+            return fail(DOPT_E_ARG, "%s: grad replica %d is not pinned host memory mapped to the "
+                        "device", who, r);
+        const char *base = static_cast<const char *>(at.devicePointer);
+        out[r] = base + (static_cast<const char *>(grad_replicas[r]) -
+                         static_cast<const char *>(at.hostPointer));
+        if (!aligned16(out[r]))
+            return fail(DOPT_E_ALIGN, "%s: grad replica %d mapping is not 16-byte aligned", who, r);
+    }
     return DOPT_OK;
 }
 
@@ -810,8 +837,10 @@ int launch_step(const char *who, const dopt_layout *L, const dopt_adam_cfg *cfg,
     if (tiles == 0) return DOPT_OK;
     int rc = check_device_tables(L, who);
     if (rc != DOPT_OK) return rc;
-    fill_step_args(a, L, cfg, step, grad_replicas, master, exp_avg, exp_avg_sq, param_replicas,
-                   flags);
+    const void *grads[DOPT_MAX_D];
+    rc = resolve_grads(who, L->cfg.D, grad_replicas, flags, grads);
+    if (rc != DOPT_OK) return rc;
+    fill_step_args(a, L, cfg, step, grads, master, exp_avg, exp_avg_sq, param_replicas, flags);
     a.main_grad_out = main_grad_out;
     StepKernel k = step_kernel_for<MODE>(grad_dtype, kernel_D(L));
     k<<<unsigned(tiles), kThreads, 0, stream>>>(a);
@@ -828,7 +857,10 @@ int launch_clipped(const char *who, const dopt_layout *L, const dopt_adam_cfg *c
     using dopt::fail;
     NormArgs na{};
     const int D = L->cfg.D;
-    for (int r = 0; r < D; ++r) na.grads[r] = grad_replicas[r];
+    const void *grads[DOPT_MAX_D];
+    int rc = resolve_grads(who, D, grad_replicas, flags, grads);
+    if (rc != DOPT_OK) return rc;
+    for (int r = 0; r < D; ++r) na.grads[r] = grads[r];
     na.main_grad = main_grad;
     na.ws = ws;
     na.norm_out = norm_out;
@@ -842,14 +874,13 @@ int launch_clipped(const char *who, const dopt_layout *L, const dopt_adam_cfg *c
     cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(unsigned int), stream);
     if (e != cudaSuccess) return fail(DOPT_E_CUDA, "%s: workspace reset: %s", who, cudaGetErrorString(e));
     nk<<<grid_a, kThreads, 0, stream>>>(na);
-    int rc = launch_error(who, "norm");
+    rc = launch_error(who, "norm");
     if (rc != DOPT_OK) return rc;
 
     StepArgs a{};
     int64_t tiles = 0;
     a.rv = whole_view(L, &tiles);
-    fill_step_args(a, L, cfg, step, grad_replicas, master, exp_avg, exp_avg_sq, param_replicas,
-                   flags);
+    fill_step_args(a, L, cfg, step, grads, master, exp_avg, exp_avg_sq, param_replicas, flags);
     a.main_grad_in = main_grad;
     a.clip_coef = &ws->coef;
     StepKernel k = pick_step_kernel<float, kFromMain>(kernel_D(L));

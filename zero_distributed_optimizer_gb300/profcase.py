@@ -51,7 +51,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=2)
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--mode", default="step",
-                    choices=["step", "gather", "clipped", "buckets", "allreduce", "step_allreduce"],
+                    choices=["step", "gather", "clipped", "buckets", "buckets_graph", "allreduce",
+                             "step_allreduce"],
                     help="the fused step, dopt_gather alone, the clipped step, the step as "
                          "one launch per bucket, dopt_allreduce alone, or the step with "
                          "force_all_reduce")
@@ -78,6 +79,36 @@ def main(argv=None):
         main_grad = torch.empty(N, device=dev)
         ws = B.clip_workspace(dev)
     streams = [torch.cuda.current_stream()] + [torch.cuda.Stream(dev) for _ in range(args.streams - 1)]
+
+    def bucket_launches(t):
+        # fork the side streams off the main one, launch, join them back
+        fork = torch.cuda.Event()
+        fork.record(streams[0])
+        for s_ in streams[1:]:
+            s_.wait_event(fork)
+        for k in range(L.n_buckets):
+            s_ = streams[k % len(streams)]
+            B.dopt_step_buckets(L, adam, t, k, 1, grads, master, m, v, params, stream=s_)
+        for s_ in streams[1:]:
+            join = torch.cuda.Event()
+            join.record(s_)
+            streams[0].wait_event(join)
+
+    graph = None
+    if args.mode == "buckets_graph":
+        # the per-bucket launches of one step recorded once and replayed: the
+        # replays repeat the same step count (same bias corrections); they
+        # time the device side of per-bucket stepping without host submission
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            streams[0] = side
+            bucket_launches(1)  # warm-up outside the capture
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=side):
+                bucket_launches(1)
+        torch.cuda.current_stream().wait_stream(side)
+        streams[0] = torch.cuda.current_stream()
     torch.cuda.synchronize()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     t = 0
@@ -88,18 +119,9 @@ def main(argv=None):
         if args.mode == "gather":
             B.dopt_gather(L, params)
         elif args.mode == "buckets":
-            # fork the side streams off the main one, launch, join them back
-            fork = torch.cuda.Event()
-            fork.record(streams[0])
-            for s_ in streams[1:]:
-                s_.wait_event(fork)
-            for k in range(L.n_buckets):
-                s_ = streams[k % len(streams)]
-                B.dopt_step_buckets(L, adam, t, k, 1, grads, master, m, v, params, stream=s_)
-            for s_ in streams[1:]:
-                join = torch.cuda.Event()
-                join.record(s_)
-                streams[0].wait_event(join)
+            bucket_launches(t)
+        elif args.mode == "buckets_graph":
+            graph.replay()
         elif args.mode == "allreduce":
             B.dopt_allreduce(L, grads, 1.0)
         elif args.mode == "step_allreduce":
@@ -113,6 +135,7 @@ def main(argv=None):
     ms = ev[0].elapsed_time(ev[1]) / max(args.launches, 1)
     step_bytes = w.algorithmic_bytes_per_element()
     per_elem = {"gather": 2 * w.D, "step": step_bytes, "buckets": step_bytes,
+                "buckets_graph": step_bytes,
                 "clipped": step_bytes + 8, "allreduce": 2 * w.D * w.grad_bytes,
                 "step_allreduce": step_bytes + w.D * w.grad_bytes}[args.mode]
     bytes_per = w.numel * per_elem
