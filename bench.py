@@ -39,7 +39,7 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "dopt_step_kernel_gpt2_small.md")
 KERNEL_SOURCES = [os.path.join(ROOT, "zero_distributed_optimizer_gb300", "csrc", f)
-                  for f in ("step.cu", "dopt_internal.h")]
+                  for f in ("kernels.cuh", "dopt_internal.h")]
 CPU_SAMPLE_ELEMS = 1 << 21
 
 

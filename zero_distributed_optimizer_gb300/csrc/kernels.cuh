@@ -1,0 +1,607 @@
+#pragma once
+// Device code of the fused ZeRO-1 distributed-optimizer step for sm_103a,
+// the clipped step, the all-reduce and the standalone all-gather (Megatron-LM
+// distributed-optimizer page, §4.2-§4.4 and §5; distributed-training
+// tutorial, "AllReduce" and §8.3).  Included by step.cu only.
+//
+// Work split.  With all D ranks held on one device, every owned element i
+// is independent: rank q's reduce-scatter reads the D replicas at i, its
+// Adam reads and writes the fp32 master/m/v at i (the four-way range map
+// composes to the identity on the buffer index, because main params are
+// stored buffer-indexed), and the write-back plus all-gather writes the D
+// param replicas at i.  So one launch covers any set of buckets (all of them
+// for dopt_step), in tiles of 2048 elements (256 threads x 8 elements).
+//
+// Per element the only facts needed are "owned or padding", "decays or
+// not" and the owner rank.  They come from the run table (maximal owned
+// stretches of one bucket with one rank and one decay flag).  A launch
+// covers a contiguous range of runs (a RunView); each CTA gets the first run
+// of its tile from a host-built index, each warp finds the first run of its
+// own 256 elements with one ballot over 32 run ends, and each thread walks
+// forward to its 8 elements.  An 8-element vector inside one run goes
+// through 128-bit loads and stores; a vector that straddles a run edge
+// (param with another decay flag, a rank edge, padding, the edge of the
+// launch's range) is done element by element and touches owned elements of
+// the range only.
+//
+// Arithmetic.  Every fp32 operation uses the round-to-nearest intrinsics
+// (__fmul_rn, __fadd_rn, __fsub_rn, __fdiv_rn, __fsqrt_rn), so no multiply
+// and add are fused and divide and square root are IEEE; the rank order of
+// the reduction is the loop order.
+#include <cstdint>
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "dopt_internal.h"
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kVec = 8;
+constexpr int kMaxClipCtas = 1024;
+static_assert(kThreads * kVec == kDoptTileElems, "tile size must match the host table");
+
+struct Scalars {
+    float b1, b2, omb1, omb2, decay, step_size, bc2_sqrt, eps, scale;
+};
+
+// The part of the run table one launch covers: runs [run_begin, run_limit)
+// and tiles from tile0 on.  Elements outside those runs are left alone.
+struct RunView {
+    const int64_t *run_start;
+    const int64_t *run_end;
+    const int32_t *run_meta;
+    const int32_t *tile_run;
+    int64_t numel;
+    int64_t tile0;
+    int32_t run_begin;
+    int32_t run_limit;
+};
+
+// What the step kernel does with the reduced grads.
+enum StepMode : int {
+    kPlain = 0,       // reduce the replicas, Adam
+    kFromMain = 1,    // read main_grad_in times the clipping coefficient, Adam
+    kWriteGrads = 2,  // reduce the replicas, write the reduced grads back into
+                      // every replica (all-reduce), Adam
+};
+
+struct StepArgs {
+    const void *grads[DOPT_MAX_D];
+    void *params[DOPT_MAX_D];
+    float *master;
+    float *exp_avg;
+    float *exp_avg_sq;
+    float *main_grad_out;
+    const float *main_grad_in;  // kFromMain: the reduced grads
+    const float *clip_coef;     // kFromMain: device scalar
+    RunView rv;
+    int32_t D;
+    int32_t R;  // ranks per instance (D with one instance)
+    int32_t gather;
+    Scalars sc;
+};
+
+// Workspace of the clipped step (device memory, DOPT_CLIP_WORKSPACE_BYTES).
+struct ClipWorkspace {
+    unsigned int ticket;  // CTAs done; zeroed before every launch
+    unsigned int pad0;
+    double norm_sq;
+    float norm;
+    float coef;
+    unsigned char pad1[40];
+    double partial[kMaxClipCtas];
+};
+static_assert(sizeof(ClipWorkspace) <= DOPT_CLIP_WORKSPACE_BYTES, "workspace size");
+static_assert(sizeof(ClipWorkspace) <= DOPT_NOALLOC_SCRATCH_BYTES, "scratch size");
+
+struct NormArgs {
+    const void *grads[DOPT_MAX_D];
+    float *main_grad;
+    ClipWorkspace *ws;
+    float *norm_out;
+    RunView rv;
+    int64_t n_tiles;
+    int32_t D;
+    int32_t R;
+    float scale;
+    float max_norm;
+};
+
+struct GatherArgs {
+    void *params[DOPT_MAX_D];
+    RunView rv;
+    int32_t D;
+    int32_t R;
+};
+
+// The grads are read, reduced and written back in place (each element by
+// the one thread that read it), so the pointers are stored as const and
+// cast back for the stores.
+struct AllReduceArgs {
+    const void *grads[DOPT_MAX_D];
+    RunView rv;
+    int32_t D;
+    int32_t R;
+    float scale;
+};
+
+// ---------------------------------------------------------------------------
+// Small device helpers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4 &raw, float (&f)[8]) {
+    f[0] = bf16_lo(raw.x);
+    f[1] = bf16_hi(raw.x);
+    f[2] = bf16_lo(raw.y);
+    f[3] = bf16_hi(raw.y);
+    f[4] = bf16_lo(raw.z);
+    f[5] = bf16_hi(raw.z);
+    f[6] = bf16_lo(raw.w);
+    f[7] = bf16_hi(raw.w);
+}
+
+// Two floats to two bf16 (round to nearest even), element 0 in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ uint4 pack_bf16x8(const float (&f)[8]) {
+    return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                      pack_bf16x2(f[6], f[7]));
+}
+
+__device__ __forceinline__ uint16_t to_bf16_bits(float x) {
+    __nv_bfloat16 h = __float2bfloat16_rn(x);
+    return *reinterpret_cast<uint16_t *>(&h);
+}
+
+__device__ __forceinline__ uint4 ld_stream(const void *p) {
+    return __ldcs(reinterpret_cast<const uint4 *>(p));
+}
+__device__ __forceinline__ void st_stream(void *p, const uint4 &v) {
+    __stcs(reinterpret_cast<uint4 *>(p), v);
+}
+__device__ __forceinline__ float4 ld_stream_f4(const float *p) {
+    return __ldcs(reinterpret_cast<const float4 *>(p));
+}
+__device__ __forceinline__ void st_stream_f4(float *p, const float4 &v) {
+    __stcs(reinterpret_cast<float4 *>(p), v);
+}
+
+// One AdamW update of one element, each operation rounded on its own.
+__device__ __forceinline__ void adamw(const Scalars &s, float decay, float g, float &w, float &m,
+                                      float &v) {
+    m = __fadd_rn(__fmul_rn(s.b1, m), __fmul_rn(s.omb1, g));
+    const float gg = __fmul_rn(g, g);
+    v = __fadd_rn(__fmul_rn(s.b2, v), __fmul_rn(s.omb2, gg));
+    w = __fmul_rn(w, decay);
+    const float denom = __fadd_rn(__fdiv_rn(__fsqrt_rn(v), s.bc2_sqrt), s.eps);
+    w = __fsub_rn(w, __fmul_rn(s.step_size, __fdiv_rn(m, denom)));
+}
+
+// First run (index >= j, < limit) whose end lies beyond `pos`: one ballot
+// over 32 consecutive run ends per iteration.  All 32 lanes must call it.
+__device__ __forceinline__ int warp_first_run(const int64_t *run_end, int limit, int j,
+                                              int64_t pos, int lane) {
+    for (;;) {
+        const int idx = j + lane;
+        const bool ended = idx < limit && run_end[idx] <= pos;
+        const unsigned mask = __ballot_sync(0xffffffffu, ended);
+        j += __popc(mask);
+        if (mask != 0xffffffffu) return j;
+    }
+}
+
+// Where a thread's 8-element vector at e0 of `tile` stands in the view:
+// kNone (nothing of the view in it), kFull (inside one run) or kMixed; `j`
+// is the first run of the view ending after e0.  All lanes must call it.
+enum VecKind : int { kNone = 0, kFull = 1, kMixed = 2 };
+
+__device__ __forceinline__ VecKind locate(const RunView &v, int64_t tile, int64_t e0, int &j) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp_begin = tile * kDoptTileElems + int64_t(threadIdx.x & ~31) * kVec;
+    j = warp_first_run(v.run_end, v.run_limit, max(v.tile_run[tile], v.run_begin), warp_begin,
+                       lane);
+    if (e0 >= v.numel) return kNone;
+    while (j < v.run_limit && v.run_end[j] <= e0) ++j;
+    if (j >= v.run_limit) return kNone;
+    const int64_t rs = v.run_start[j];
+    if (rs >= e0 + kVec) return kNone;
+    return (rs <= e0 && e0 + kVec <= v.run_end[j]) ? kFull : kMixed;
+}
+
+// For the element path: advance j to the run holding e; false if e is not
+// owned in the view (padding, or outside its runs).  Sets `done` once no
+// run of the view is left.
+__device__ __forceinline__ bool owned_at(const RunView &v, int64_t e, int &j, bool &done) {
+    if (e >= v.numel) {
+        done = true;
+        return false;
+    }
+    while (j < v.run_limit && v.run_end[j] <= e) ++j;
+    if (j >= v.run_limit) {
+        done = true;
+        return false;
+    }
+    return v.run_start[j] <= e;
+}
+
+template <typename G>
+__device__ __forceinline__ float load_grad_scalar(const void *base, int64_t i) {
+    if constexpr (sizeof(G) == 2)
+        return __uint_as_float(uint32_t(__ldcs(static_cast<const unsigned short *>(base) + i)) << 16);
+    else
+        return __ldcs(static_cast<const float *>(base) + i);
+}
+
+template <typename G>
+__device__ __forceinline__ void store_grad_scalar(const void *base, int64_t i, float g) {
+    if constexpr (sizeof(G) == 2)
+        static_cast<uint16_t *>(const_cast<void *>(base))[i] = to_bf16_bits(g);
+    else
+        static_cast<float *>(const_cast<void *>(base))[i] = g;
+}
+
+// Load the 8 grads of replica r at e0 (bf16: one 16-byte load; fp32: two).
+template <typename G>
+struct GradVec;
+
+template <>
+struct GradVec<__nv_bfloat16> {
+    uint4 a;
+    __device__ __forceinline__ void load(const void *base, int64_t e0) {
+        a = ld_stream(static_cast<const __nv_bfloat16 *>(base) + e0);
+    }
+    __device__ __forceinline__ void get(float (&f)[8]) const { unpack_bf16x8(a, f); }
+    // the 8 reduced grads, rounded to bf16, into replica `base` at e0
+    __device__ __forceinline__ static void store(const void *base, int64_t e0, const float (&f)[8]) {
+        st_stream(static_cast<__nv_bfloat16 *>(const_cast<void *>(base)) + e0, pack_bf16x8(f));
+    }
+};
+
+template <>
+struct GradVec<float> {
+    float4 a, b;
+    __device__ __forceinline__ void load(const void *base, int64_t e0) {
+        const float *p = static_cast<const float *>(base) + e0;
+        a = ld_stream_f4(p);
+        b = ld_stream_f4(p + 4);
+    }
+    __device__ __forceinline__ void get(float (&f)[8]) const {
+        f[0] = a.x, f[1] = a.y, f[2] = a.z, f[3] = a.w;
+        f[4] = b.x, f[5] = b.y, f[6] = b.z, f[7] = b.w;
+    }
+    __device__ __forceinline__ static void store(const void *base, int64_t e0, const float (&f)[8]) {
+        float *p = static_cast<float *>(const_cast<void *>(base)) + e0;
+        st_stream_f4(p, make_float4(f[0], f[1], f[2], f[3]));
+        st_stream_f4(p + 4, make_float4(f[4], f[5], f[6], f[7]));
+    }
+};
+
+// Scaled rank-order fp32 reduction of 8 elements over the D replicas.  The
+// compile-time-D form serves one instance; the run-time form reduces each
+// group of R consecutive replicas in rank order and adds the groups' sums in
+// group order (several optimizer instances; with R = D the last group's sum
+// is copied, so the result is the plain rank-order sum).
+template <typename G, int DC, typename Args>
+__device__ __forceinline__ void reduce_vec(const Args &a, float scale, int64_t e0,
+                                           float (&acc)[8]) {
+    if constexpr (DC > 0) {
+        GradVec<G> g[DC];
+#pragma unroll
+        for (int r = 0; r < DC; ++r) g[r].load(a.grads[r], e0);
+#pragma unroll
+        for (int r = 0; r < DC; ++r) {
+            float f[8];
+            g[r].get(f);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float x = __fmul_rn(scale, f[k]);
+                acc[k] = r == 0 ? x : __fadd_rn(acc[k], x);
+            }
+        }
+    } else {
+        constexpr int kBatch = 4;
+        float part[8];
+        int in_group = 0;  // position of the next replica inside its group
+        for (int r0 = 0; r0 < a.D; r0 += kBatch) {
+            GradVec<G> g[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u)
+                if (r0 + u < a.D) g[u].load(a.grads[r0 + u], e0);
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int r = r0 + u;
+                if (r >= a.D) break;
+                float f[8];
+                g[u].get(f);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float x = __fmul_rn(scale, f[k]);
+                    part[k] = in_group == 0 ? x : __fadd_rn(part[k], x);
+                }
+                if (++in_group == a.R) {
+                    in_group = 0;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        acc[k] = r + 1 == a.R ? part[k] : __fadd_rn(acc[k], part[k]);
+                }
+            }
+        }
+    }
+}
+
+// The same reduction for one element: groups of R replicas in rank order,
+// then the groups' sums in group order.
+template <typename G>
+__device__ __forceinline__ float reduce_scalar(const void *const *grads, int D, int R,
+                                               float scale, int64_t e) {
+    float g = 0.0f, part = 0.0f;
+    for (int r = 0; r < D; ++r) {
+        const float x = __fmul_rn(scale, load_grad_scalar<G>(grads[r], e));
+        const int in_group = r % R;
+        part = in_group == 0 ? x : __fadd_rn(part, x);
+        if (in_group == R - 1) g = r + 1 == R ? part : __fadd_rn(g, part);
+    }
+    return g;
+}
+
+// The reduced grads of 8 elements written into every replica, rounded to
+// the grad type (the all-reduce's all-gather half).
+template <typename G, int DC>
+__device__ __forceinline__ void write_grads_vec(const void *const *grads, int D_rt, int64_t e0,
+                                                const float (&acc)[8]) {
+    if constexpr (DC > 0) {
+#pragma unroll
+        for (int r = 0; r < DC; ++r) GradVec<G>::store(grads[r], e0, acc);
+    } else {
+        for (int r = 0; r < D_rt; ++r) GradVec<G>::store(grads[r], e0, acc);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// The step kernel
+// ---------------------------------------------------------------------------
+
+// A vector of 8 owned elements of one run.
+template <typename G, int DC, int MODE>
+__device__ __forceinline__ void full_vector(const StepArgs &a, int64_t e0, int32_t meta) {
+    float acc[8];
+    if constexpr (MODE == kFromMain) {
+        const float coef = *a.clip_coef;
+        const float4 g0 = ld_stream_f4(a.main_grad_in + e0), g1 = ld_stream_f4(a.main_grad_in + e0 + 4);
+        const float f[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc[k] = __fmul_rn(f[k], coef);
+    } else {
+        reduce_vec<G, DC>(a, a.sc.scale, e0, acc);
+    }
+    if constexpr (MODE == kWriteGrads) write_grads_vec<G, DC>(a.grads, a.D, e0, acc);
+
+    const float4 w0 = ld_stream_f4(a.master + e0), w1 = ld_stream_f4(a.master + e0 + 4);
+    const float4 m0 = ld_stream_f4(a.exp_avg + e0), m1 = ld_stream_f4(a.exp_avg + e0 + 4);
+    const float4 v0 = ld_stream_f4(a.exp_avg_sq + e0), v1 = ld_stream_f4(a.exp_avg_sq + e0 + 4);
+    float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+    float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    const float decay = (meta & kRunDecays) ? a.sc.decay : 1.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) adamw(a.sc, decay, acc[k], w[k], m[k], v[k]);
+
+    st_stream_f4(a.master + e0, make_float4(w[0], w[1], w[2], w[3]));
+    st_stream_f4(a.master + e0 + 4, make_float4(w[4], w[5], w[6], w[7]));
+    st_stream_f4(a.exp_avg + e0, make_float4(m[0], m[1], m[2], m[3]));
+    st_stream_f4(a.exp_avg + e0 + 4, make_float4(m[4], m[5], m[6], m[7]));
+    st_stream_f4(a.exp_avg_sq + e0, make_float4(v[0], v[1], v[2], v[3]));
+    st_stream_f4(a.exp_avg_sq + e0 + 4, make_float4(v[4], v[5], v[6], v[7]));
+    if (MODE != kFromMain && a.main_grad_out) {
+        st_stream_f4(a.main_grad_out + e0, make_float4(acc[0], acc[1], acc[2], acc[3]));
+        st_stream_f4(a.main_grad_out + e0 + 4, make_float4(acc[4], acc[5], acc[6], acc[7]));
+    }
+
+    const uint4 packed = pack_bf16x8(w);
+    if (a.gather) {
+        if constexpr (DC > 0) {
+#pragma unroll
+            for (int r = 0; r < DC; ++r)
+                st_stream(static_cast<__nv_bfloat16 *>(a.params[r]) + e0, packed);
+        } else {
+            for (int r = 0; r < a.D; ++r)
+                st_stream(static_cast<__nv_bfloat16 *>(a.params[r]) + e0, packed);
+        }
+    } else {
+        const int q = meta >> kRunRankShift;
+        for (int r = q; r < a.D; r += a.R)
+            st_stream(static_cast<__nv_bfloat16 *>(a.params[r]) + e0, packed);
+    }
+}
+
+// A vector that straddles a run edge: element by element, owned ones only.
+template <typename G, int DC, int MODE>
+__device__ __noinline__ void mixed_vector(const StepArgs &a, int64_t e0, int j) {
+    const int D = DC > 0 ? DC : a.D;
+    bool done = false;
+    for (int k = 0; k < kVec && !done; ++k) {
+        const int64_t e = e0 + k;
+        if (!owned_at(a.rv, e, j, done)) continue;
+        const int32_t meta = a.rv.run_meta[j];
+        float g;
+        if constexpr (MODE == kFromMain)
+            g = __fmul_rn(a.main_grad_in[e], *a.clip_coef);
+        else
+            g = reduce_scalar<G>(a.grads, D, a.R, a.sc.scale, e);
+        if constexpr (MODE == kWriteGrads)
+            for (int r = 0; r < D; ++r) store_grad_scalar<G>(a.grads[r], e, g);
+        float w = a.master[e], m = a.exp_avg[e], v = a.exp_avg_sq[e];
+        adamw(a.sc, (meta & kRunDecays) ? a.sc.decay : 1.0f, g, w, m, v);
+        a.master[e] = w;
+        a.exp_avg[e] = m;
+        a.exp_avg_sq[e] = v;
+        if (MODE != kFromMain && a.main_grad_out) a.main_grad_out[e] = g;
+        const uint16_t bits = to_bf16_bits(w);
+        if (a.gather) {
+            for (int r = 0; r < D; ++r) static_cast<uint16_t *>(a.params[r])[e] = bits;
+        } else {
+            for (int r = meta >> kRunRankShift; r < D; r += a.R)
+                static_cast<uint16_t *>(a.params[r])[e] = bits;
+        }
+    }
+}
+
+template <typename G, int DC, int MODE>
+__global__ void __launch_bounds__(kThreads) dopt_step_kernel(const __grid_constant__ StepArgs a) {
+    const int64_t tile = a.rv.tile0 + blockIdx.x;
+    const int64_t e0 = tile * kDoptTileElems + int64_t(threadIdx.x) * kVec;
+    int j;
+    const VecKind kind = locate(a.rv, tile, e0, j);
+    if (kind == kFull)
+        full_vector<G, DC, MODE>(a, e0, a.rv.run_meta[j]);
+    else if (kind == kMixed)
+        mixed_vector<G, DC, MODE>(a, e0, j);
+}
+
+// ---------------------------------------------------------------------------
+// The all-reduce kernel: reduce, then write the reduced grads into every
+// replica, rounded to the grad type.
+// ---------------------------------------------------------------------------
+
+template <typename G, int DC>
+__global__ void __launch_bounds__(kThreads) dopt_allreduce_kernel(const __grid_constant__ AllReduceArgs a) {
+    const int64_t tile = a.rv.tile0 + blockIdx.x;
+    const int64_t e0 = tile * kDoptTileElems + int64_t(threadIdx.x) * kVec;
+    int j;
+    const VecKind kind = locate(a.rv, tile, e0, j);
+    if (kind == kFull) {
+        float acc[8];
+        reduce_vec<G, DC>(a, a.scale, e0, acc);
+        write_grads_vec<G, DC>(a.grads, a.D, e0, acc);
+    } else if (kind == kMixed) {
+        const int D = DC > 0 ? DC : a.D;
+        bool done = false;
+        for (int k = 0; k < kVec && !done; ++k) {
+            const int64_t e = e0 + k;
+            if (!owned_at(a.rv, e, j, done)) continue;
+            const float g = reduce_scalar<G>(a.grads, D, a.R, a.scale, e);
+            for (int r = 0; r < D; ++r) store_grad_scalar<G>(a.grads[r], e, g);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Pass 1 of the clipped step
+// ---------------------------------------------------------------------------
+
+// Deterministic sum over a warp (fixed shuffle tree); the result is in lane 0.
+__device__ __forceinline__ double warp_sum(double v) {
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// The fused reduce-scatter writes the fp32 main grads and every CTA
+// accumulates the sum of their squares over the tiles it visits (fp32
+// squares summed pairwise per 8-element vector, then one fp64 add per
+// vector).  Each CTA leaves one fp64 partial; the CTA that finishes last
+// (atomic ticket, nobody waits) adds the partials in CTA order and writes the
+// norm and the clipping coefficient min(1, max_norm / (norm + 1e-6)).
+template <typename G, int DC>
+__global__ void __launch_bounds__(kThreads) dopt_rs_norm_kernel(const __grid_constant__ NormArgs a) {
+    const int lane = threadIdx.x & 31;
+    double local = 0.0;
+    for (int64_t t = blockIdx.x; t < a.n_tiles; t += gridDim.x) {
+        const int64_t tile = a.rv.tile0 + t;
+        const int64_t e0 = tile * kDoptTileElems + int64_t(threadIdx.x) * kVec;
+        int j;
+        const VecKind kind = locate(a.rv, tile, e0, j);
+        if (kind == kFull) {
+            float acc[8];
+            reduce_vec<G, DC>(a, a.scale, e0, acc);
+            st_stream_f4(a.main_grad + e0, make_float4(acc[0], acc[1], acc[2], acc[3]));
+            st_stream_f4(a.main_grad + e0 + 4, make_float4(acc[4], acc[5], acc[6], acc[7]));
+            float sq[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) sq[k] = __fmul_rn(acc[k], acc[k]);
+            const float s01 = __fadd_rn(sq[0], sq[1]), s23 = __fadd_rn(sq[2], sq[3]);
+            const float s45 = __fadd_rn(sq[4], sq[5]), s67 = __fadd_rn(sq[6], sq[7]);
+            local += double(__fadd_rn(__fadd_rn(s01, s23), __fadd_rn(s45, s67)));
+        } else if (kind == kMixed) {
+            const int D = DC > 0 ? DC : a.D;
+            bool done = false;
+            for (int k = 0; k < kVec && !done; ++k) {
+                const int64_t e = e0 + k;
+                if (!owned_at(a.rv, e, j, done)) continue;
+                const float g = reduce_scalar<G>(a.grads, D, a.R, a.scale, e);
+                a.main_grad[e] = g;
+                local += double(__fmul_rn(g, g));
+            }
+        }
+    }
+    __shared__ double warp_part[kThreads / 32];
+    __shared__ bool last;
+    local = warp_sum(local);
+    if (lane == 0) warp_part[threadIdx.x >> 5] = local;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double cta = 0.0;
+        for (int w = 0; w < kThreads / 32; ++w) cta += warp_part[w];
+        a.ws->partial[blockIdx.x] = cta;
+        __threadfence();
+        last = atomicAdd(&a.ws->ticket, 1u) == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!last || threadIdx.x >= 32) return;
+    __threadfence();
+    double v = 0.0;
+    for (int i = lane; i < int(gridDim.x); i += 32) v += __ldcg(&a.ws->partial[i]);
+    v = warp_sum(v);
+    if (lane == 0) {
+        const double norm = sqrt(v);
+        double coef = double(a.max_norm) / (norm + 1e-6);
+        if (coef > 1.0) coef = 1.0;
+        a.ws->norm_sq = v;
+        a.ws->norm = float(norm);
+        a.ws->coef = float(coef);
+        if (a.norm_out) {
+            a.norm_out[0] = float(norm);
+            a.norm_out[1] = float(coef);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// The gather kernel: each rank's owned elements from its replica to all.
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(kThreads) dopt_gather_kernel(const __grid_constant__ GatherArgs a) {
+    const int64_t tile = a.rv.tile0 + blockIdx.x;
+    const int64_t e0 = tile * kDoptTileElems + int64_t(threadIdx.x) * kVec;
+    int j;
+    const VecKind kind = locate(a.rv, tile, e0, j);
+    if (kind == kFull) {
+        const int q = a.rv.run_meta[j] >> kRunRankShift;
+        for (int base = 0; base < a.D; base += a.R) {
+            const uint4 val = ld_stream(static_cast<const __nv_bfloat16 *>(a.params[base + q]) + e0);
+            for (int r = base; r < base + a.R; ++r)
+                if (r != base + q) st_stream(static_cast<__nv_bfloat16 *>(a.params[r]) + e0, val);
+        }
+    } else if (kind == kMixed) {
+        bool done = false;
+        for (int k = 0; k < kVec && !done; ++k) {
+            const int64_t e = e0 + k;
+            if (!owned_at(a.rv, e, j, done)) continue;
+            const int q = a.rv.run_meta[j] >> kRunRankShift;
+            for (int base = 0; base < a.D; base += a.R) {
+                const uint16_t bits = static_cast<const uint16_t *>(a.params[base + q])[e];
+                for (int r = base; r < base + a.R; ++r)
+                    if (r != base + q) static_cast<uint16_t *>(a.params[r])[e] = bits;
+            }
+        }
+    }
+}
+
+}  // namespace
