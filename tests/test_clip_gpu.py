@@ -174,3 +174,27 @@ def test_clipped_gpt2_small_full_size():
         assert_f32_close(t2np_f32(v[a:b]), hs[2], f"v[{a}:{b}]")
         for r in range(w.D):
             assert_bf16_close(t2np_bf16(params[r][a:b]), hs[3][r], f"param{r}[{a}:{b}]")
+
+
+def test_clipped_step_is_deterministic():
+    """The norm's partial sums are added in a fixed order (per-CTA partials
+    in CTA order), so two runs from the same inputs are bitwise equal."""
+    sizes, wd, D = [700000, 5, 300001], [1, 0, 1], 8
+    L = B.dopt_build_range_map(sizes, D, 0, 64, wd).to_device()
+    N = L.padded_numel
+    master, m, v, params, grads = W.random_case(N, D, 2, "bf16", 12)
+    runs = []
+    for _ in range(2):
+        d = [master.to(DEV), m.to(DEV), v.to(DEV)]
+        dp = [p.to(DEV) for p in params]
+        norm_out = torch.zeros(2, device=DEV)
+        ws = B.clip_workspace(DEV)
+        mg = torch.empty(N, device=DEV)
+        for i in range(2):
+            B.dopt_step_clipped(L, B.AdamConfig(grad_scale=0.125), i + 1, 0.01,
+                                [g.to(DEV) for g in grads[i]], *d, dp, mg, ws, norm_out=norm_out)
+        torch.cuda.synchronize()
+        runs.append(d + dp + [norm_out])
+    for x, y in zip(*runs):
+        assert torch.equal(x.view(torch.int16) if x.dtype == torch.bfloat16 else x.view(torch.int32),
+                           y.view(torch.int16) if y.dtype == torch.bfloat16 else y.view(torch.int32))
