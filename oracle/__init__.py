@@ -110,13 +110,15 @@ def _declare(lib) -> None:
         ctypes.POINTER(Adam), ctypes.c_int64, ctypes.c_int32, ctypes.POINTER(ctypes.c_void_p),
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p),
         ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_float,
+        ctypes.c_int32,
     ]
     lib.orc_grad_norm_sq.restype = ctypes.c_int
     lib.orc_grad_norm_sq.argtypes = [i64p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                      ctypes.c_int64,
                                      ctypes.c_int32, ctypes.c_float, ctypes.c_int32,
                                      ctypes.POINTER(ctypes.c_void_p), ctypes.c_int64,
-                                     ctypes.c_int64, ctypes.POINTER(ctypes.c_double)]
+                                     ctypes.c_int64, ctypes.c_int32,
+                                     ctypes.POINTER(ctypes.c_double)]
     lib.orc_allreduce.restype = ctypes.c_int
     lib.orc_allreduce.argtypes = [i64p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                   ctypes.c_int64,
@@ -235,7 +237,7 @@ def make_adam(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, grad_s
 def step(sizes, wd_mask, D: int, bucket_elems: int, pad_unit: int, adam: Adam, t: int,
          grads, master, exp_avg, exp_avg_sq, params, gather: bool = True,
          main_grad_out=None, window=None, clip_coef: float = 1.0, instances: int = 1,
-         lib=None) -> None:
+         round_grad: bool = False, lib=None) -> None:
     """One ZeRO-1 step for all D simulated ranks, in place on numpy arrays.
 
     grads: D arrays (uint16 bf16 bits or float32); master/exp_avg/exp_avg_sq:
@@ -246,6 +248,7 @@ def step(sizes, wd_mask, D: int, bucket_elems: int, pad_unit: int, adam: Adam, t
     (from :func:`clip_coef`) multiplies every reduced grad before Adam.
     ``instances`` > 1 splits the D ranks into that many optimizer instances
     (page 1 §5): reduce-scatter inside each, then a sum across instances.
+    ``round_grad`` rounds every reduced grad to the grad type first.
     """
     lib = lib or load()
     sizes_a, sizes_p = _i64(sizes)
@@ -283,13 +286,13 @@ def step(sizes, wd_mask, D: int, bucket_elems: int, pad_unit: int, adam: Adam, t
                       master.ctypes.data, exp_avg.ctypes.data, exp_avg_sq.ctypes.data, pp,
                       int(bool(gather)),
                       None if main_grad_out is None else main_grad_out.ctypes.data, w0, w1,
-                      float(clip_coef))
+                      float(clip_coef), int(bool(round_grad)))
     if rc != ORC_OK:
         raise OracleError(f"orc_step failed: {rc}")
 
 
 def grad_norm_sq(sizes, D: int, bucket_elems: int, pad_unit: int, grad_scale: float, grads,
-                 window=None, instances: int = 1, lib=None) -> float:
+                 window=None, instances: int = 1, round_grad: bool = False, lib=None) -> float:
     """Sum of squares of the reduced grads over the owned elements of the
     window (tutorial §8.3 global norm), accumulated in double."""
     lib = lib or load()
@@ -302,7 +305,8 @@ def grad_norm_sq(sizes, D: int, bucket_elems: int, pad_unit: int, grad_scale: fl
     gp = (ctypes.c_void_p * D)(*[g.ctypes.data for g in grads])
     out = ctypes.c_double(0.0)
     rc = lib.orc_grad_norm_sq(sizes_p, len(sizes_a), D, int(instances), bucket_elems, pad_unit,
-                              float(grad_scale), int(grad_is_f32), gp, w0, w1, ctypes.byref(out))
+                              float(grad_scale), int(grad_is_f32), gp, w0, w1,
+                              int(bool(round_grad)), ctypes.byref(out))
     if rc != ORC_OK:
         raise OracleError(f"orc_grad_norm_sq failed: {rc}")
     return float(out.value)

@@ -77,6 +77,11 @@
  *      copy of the optimizer state stands for all of them; the write-back
  *      goes to rank r of every instance and the all-gather runs inside each
  *      instance.
+ *  R12 Optional (off by default): Megatron's reduce-scatter lands in the grad
+ *      buffer ([P1] §4.2-§4.3: the shard is copied from the buffer to the
+ *      main grads), so with that option the reduced grad is rounded to the
+ *      grad type (bf16: R7) before clipping and Adam, and the norm is taken
+ *      over the rounded grads.
  *  R10 force_all_reduce ([P1] §5) leaves the optimizer step unchanged (each
  *      rank still updates its own shard from the same reduced grads) and
  *      additionally gives every replica's grad buffer the whole reduced grad,
@@ -334,6 +339,13 @@ static float orc_reduce_element(const void *const *grads, int32_t grad_is_f32, i
     return acc;
 }
 
+/* The reduced grad rounded to the grad buffer's type (R12): bf16 rounds to
+ * nearest even (R7), fp32 stays as is. */
+static float orc_round_to_grad_type(float g, int32_t grad_is_f32)
+{
+    return grad_is_f32 ? g : orc_bf16_to_f32(orc_f32_to_bf16(g));
+}
+
 /* One AdamW update of a single element (R6), fp32, one rounding per op. */
 static void orc_adamw(const orc_scalars *s, int decays, float g, float *w, float *m, float *v)
 {
@@ -374,6 +386,9 @@ static void orc_adamw(const orc_scalars *s, int decays, float g, float *w, float
  *                   when no clipping is wanted
  *   instances       optimizer instances (R11); D must divide by it; 1 is
  *                   the plain step
+ *   round_grad      nonzero: the reduced grad is rounded to the grad type
+ *                   before clipping and Adam (R12); main_grad_out then
+ *                   reports the rounded value
  *
  * All buffer-indexed arrays are window-relative.  Returns ORC_OK or an error.
  */
@@ -382,7 +397,8 @@ int orc_step(const int64_t *sizes, int32_t n, const uint8_t *wd_mask, int32_t D,
              const orc_adam *cfg, int64_t step,
              int32_t grad_is_f32, const void *const *grads, float *master, float *exp_avg,
              float *exp_avg_sq, uint16_t *const *params, int32_t gather,
-             float *main_grad_out, int64_t w0, int64_t w1, float clip_coef)
+             float *main_grad_out, int64_t w0, int64_t w1, float clip_coef,
+             int32_t round_grad)
 {
     if (step < 1 || w0 < 0 || w1 < w0 || instances < 1 || D % instances != 0)
         return ORC_E_ARG;
@@ -467,6 +483,9 @@ int orc_step(const int64_t *sizes, int32_t n, const uint8_t *wd_mask, int32_t D,
                     int64_t i = pc->gbuf_world.start + t;
                     /* main grad: the shard sliced by gbuf_local ([P1] §4.3) */
                     float g = shard[pc->gbuf_local.start + t];
+                    /* the reduced grad in the grad buffer's type (R12) */
+                    if (round_grad)
+                        g = orc_round_to_grad_type(g, grad_is_f32);
                     /* global-norm clipping (R9): one fp32 multiply; a
                      * coefficient of exactly 1 leaves g unchanged */
                     float gc = g * clip_coef;
@@ -527,7 +546,7 @@ done:
 int orc_grad_norm_sq(const int64_t *sizes, int32_t n, int32_t D, int32_t instances,
                      int64_t bucket_elems, int32_t pad_unit, float grad_scale,
                      int32_t grad_is_f32, const void *const *grads, int64_t w0, int64_t w1,
-                     double *out)
+                     int32_t round_grad, double *out)
 {
     if (w0 < 0 || w1 < w0 || !out || instances < 1 || D % instances != 0)
         return ORC_E_ARG;
@@ -567,8 +586,10 @@ int orc_grad_norm_sq(const int64_t *sizes, int32_t n, int32_t D, int32_t instanc
         int64_t i_lo = orc_max(pieces[pi].gbuf_world.start, w0);
         int64_t i_hi = orc_min(pieces[pi].gbuf_world.end, w1);
         for (int64_t i = i_lo; i < i_hi; ++i) {
-            double g = (double)orc_reduce_element(grads, grad_is_f32, D, instances, grad_scale,
-                                                  i - w0);
+            float r = orc_reduce_element(grads, grad_is_f32, D, instances, grad_scale, i - w0);
+            if (round_grad)
+                r = orc_round_to_grad_type(r, grad_is_f32);
+            double g = (double)r;
             sum += g * g;
         }
     }

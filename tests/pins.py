@@ -810,6 +810,61 @@ def pin_instances_write_back_and_gather(lib):
                 assert np.array_equal(params[rep][owned & ~mine], before[rep][owned & ~mine])
 
 
+# ---------------------------------------------------------------------------
+# Reduced grad rounded to the grad type (optional reading)
+# ---------------------------------------------------------------------------
+
+def pin_round_grad(lib):
+    """With round_grad the reduced grads are rounded to the grad type: the
+    reported main grads are PyTorch's bf16 rounding of the unrounded ones;
+    the step equals a D=1 step fed those rounded values with scaling 1; the
+    norm is the sum of their squares; fp32 grads are left as they are."""
+    import torch
+
+    sizes, wd, D, pad = [300, 41, 129], [1, 0, 1], 3, 2
+    L = oracle.range_map(sizes, D, 0, pad, lib=lib)
+    N = L.numel
+    rng = np.random.default_rng(77)
+    grads = [(rng.normal(0, 1, N).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+             for _ in range(D)]
+    adam = oracle.make_adam(grad_scale=0.3)  # not a power of two: sums need rounding
+    master0, m0, v0 = _state(N, 13, 1e-4, 1e-6)
+    runs = {}
+    for rg in (False, True):
+        master, m, v = master0.copy(), m0.copy(), v0.copy()
+        params = _params_from(master0, D)
+        mg = np.zeros(N, np.float32)
+        oracle.step(sizes, wd, D, 0, pad, adam, 1, grads, master, m, v, params, main_grad_out=mg,
+                    round_grad=rg, lib=lib)
+        runs[rg] = (master, m, v, params, mg)
+    owned = np.zeros(N, bool)
+    for p in range(len(sizes)):
+        owned[L.param_start[p]:L.param_end[p]] = True
+    want = torch.tensor(runs[False][4]).to(torch.bfloat16).float().numpy()
+    assert np.array_equal(runs[True][4][owned], want[owned])
+    assert np.count_nonzero(want[owned] != runs[False][4][owned]) > owned.sum() // 2
+    # a D=1 step on the rounded values (exact in bf16, scaling 1) is the same step
+    bits = (want.view(np.uint32) >> 16).astype(np.uint16)
+    master, m, v = master0.copy(), m0.copy(), v0.copy()
+    params = _params_from(master0, 1)
+    L1 = oracle.range_map(sizes, 1, 0, 1, lib=lib)
+    assert L1.numel == sum(sizes)
+    idx = np.flatnonzero(owned)
+    sub = [a[idx].copy() for a in (master, m, v)]
+    oracle.step(sizes, wd, 1, 0, 1, oracle.make_adam(grad_scale=1.0), 1, [bits[idx].copy()],
+                *sub, [params[0][idx].copy()], lib=lib)
+    for a, b in zip(sub, runs[True][:3]):
+        assert np.array_equal(a.view(np.uint32), b[idx].view(np.uint32))
+    nsq = oracle.grad_norm_sq(sizes, D, 0, pad, 0.3, grads, round_grad=True, lib=lib)
+    ref = float(np.sum(want[owned].astype(np.float64) ** 2))
+    assert abs(nsq - ref) <= 1e-12 * ref
+    # fp32 grads: the grad type is fp32, nothing to round
+    g32 = [rng.normal(0, 1, N).astype(np.float32) for _ in range(D)]
+    a = oracle.grad_norm_sq(sizes, D, 0, pad, 0.3, g32, lib=lib)
+    b = oracle.grad_norm_sq(sizes, D, 0, pad, 0.3, g32, round_grad=True, lib=lib)
+    assert a == b
+
+
 ALL_PINS = [
     pin_page1_ownership,
     pin_brute_force_range_maps,
@@ -833,4 +888,5 @@ ALL_PINS = [
     pin_instances_hierarchical_order,
     pin_instances_factorizations,
     pin_instances_write_back_and_gather,
+    pin_round_grad,
 ]

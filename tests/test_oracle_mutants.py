@@ -60,6 +60,12 @@ MUTANTS = [
      "((uint16_t *)grads[q])[i - w0] = (uint16_t)(orc_f32_to_bits(reduced) >> 16);"),
     ("allreduce_via_bucket_range", "float reduced = shard[pc->gbuf_local.start + t];",
      "float reduced = shard[pc->gbuf_world_in_bucket.start + t];"),
+    ("round_grad_ignored", "if (round_grad)\n                        g = orc_round_to_grad_type(g, grad_is_f32);",
+     "if (0)\n                        g = orc_round_to_grad_type(g, grad_is_f32);"),
+    ("round_grad_norm_unrounded", "if (round_grad)\n                r = orc_round_to_grad_type(r, grad_is_f32);",
+     "if (0)\n                r = orc_round_to_grad_type(r, grad_is_f32);"),
+    ("round_grad_truncates", "return grad_is_f32 ? g : orc_bf16_to_f32(orc_f32_to_bf16(g));",
+     "return grad_is_f32 ? g : orc_bits_to_f32(orc_f32_to_bits(g) & 0xffff0000u);"),
     ("clip_not_applied", "float gc = g * clip_coef;", "float gc = g;"),
     ("norm_not_squared", "sum += g * g;", "sum += g < 0 ? -g : g;"),
     ("clip_no_sqrt", "double norm = sqrt(norm_sq);", "double norm = norm_sq;"),
