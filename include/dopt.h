@@ -134,6 +134,15 @@ typedef enum { DOPT_BF16 = 0, DOPT_FP32 = 1 } dopt_dtype;
  * dopt_step_clipped.
  */
 #define DOPT_STEP_HOST_GRADS 2u
+/*
+ * Round each reduced grad to the grad type before clipping and Adam (bf16:
+ * nearest even; fp32 grads are unchanged), as when the reduce-scatter writes
+ * into the grad buffer and the optimizer copies the shard from there (page
+ * 1, §4.2-§4.3).  main_grad_out / main_grad then hold the rounded values and
+ * the clipped step's norm is taken over them.  Without the flag the fp32
+ * sum feeds Adam directly.  Accepted by every step entry point.
+ */
+#define DOPT_STEP_ROUND_GRAD 4u
 
 typedef struct dopt_layout dopt_layout;
 
@@ -221,7 +230,7 @@ void dopt_layout_free(dopt_layout *layout);
  *                   device fp32, padded_numel elements each, buffer-indexed
  *                   (the union of all D ranks' shards); updated in place
  *   param_replicas  host array of D device pointers, bf16, padded_numel each
- *   flags           DOPT_STEP_GATHER and/or DOPT_STEP_HOST_GRADS
+ *   flags           DOPT_STEP_GATHER, DOPT_STEP_HOST_GRADS, DOPT_STEP_ROUND_GRAD
  *   main_grad_out   nullable device fp32[padded_numel]: the reduce-scattered
  *                   fp32 main grad of every owned element
  *   stream          CUDA stream to launch on

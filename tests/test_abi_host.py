@@ -132,7 +132,7 @@ def test_step_argument_checks_before_cuda(lib):
     good = [0x10000, 0x20000]
     state = [0x30000, 0x40000, 0x50000]
     assert _raw_step(L, good, state, good, step=0) == B.DOPT_E_ARG
-    assert _raw_step(L, good, state, good, flags=4) == B.DOPT_E_ARG
+    assert _raw_step(L, good, state, good, flags=8) == B.DOPT_E_ARG
     assert _raw_step(L, good, state, good, dtype=7) == B.DOPT_E_ARG
     assert _raw_step(L, [0x10000, 0], state, good) == B.DOPT_E_ARG
     assert _raw_step(L, [0x10000, 0x20002], state, good) == B.DOPT_E_ALIGN

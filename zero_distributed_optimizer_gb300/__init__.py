@@ -18,6 +18,7 @@ from .binding import (  # noqa: F401
     DOPT_OK,
     DOPT_STEP_GATHER,
     DOPT_STEP_HOST_GRADS,
+    DOPT_STEP_ROUND_GRAD,
     AdamConfig,
     DoptError,
     Layout,

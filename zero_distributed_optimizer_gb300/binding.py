@@ -30,6 +30,7 @@ DOPT_BF16 = 0
 DOPT_FP32 = 1
 DOPT_STEP_GATHER = 1
 DOPT_STEP_HOST_GRADS = 2
+DOPT_STEP_ROUND_GRAD = 4
 DOPT_CLIP_WORKSPACE_BYTES = 16384
 
 _ERROR_NAMES = {DOPT_E_ARG: "DOPT_E_ARG", DOPT_E_LAYOUT: "DOPT_E_LAYOUT",
@@ -259,6 +260,11 @@ def _check_tensor(t, name, dtype, numel, device):
         raise DoptError(DOPT_E_ARG, f"{name} must be contiguous with >= {numel} elements")
 
 
+def _flags(gather: bool, host_grads: bool = False, round_grad: bool = False) -> int:
+    return ((DOPT_STEP_GATHER if gather else 0) | (DOPT_STEP_HOST_GRADS if host_grads else 0)
+            | (DOPT_STEP_ROUND_GRAD if round_grad else 0))
+
+
 def _check_grads(grad_replicas, gdt, N, device, host_grads):
     """Device grads on the step's device, or (host_grads) pinned CPU tensors
     that the library reads in place."""
@@ -302,13 +308,13 @@ def _step_pointers(layout: Layout, grad_replicas, master, exp_avg, exp_avg_sq, p
 def dopt_step_buckets(layout: Layout, adam: AdamConfig, step: int, first_bucket: int,
                       n_buckets: int, grad_replicas, master, exp_avg, exp_avg_sq,
                       param_replicas, gather: bool = True, main_grad_out=None,
-                      stream=None, host_grads: bool = False) -> None:
+                      stream=None, host_grads: bool = False, round_grad: bool = False) -> None:
     """The step over buckets [first_bucket, first_bucket + n_buckets) only."""
     import torch
 
     device, gp, pp, dt, mg = _step_pointers(layout, grad_replicas, master, exp_avg, exp_avg_sq,
                                             param_replicas, main_grad_out, host_grads)
-    flags = (DOPT_STEP_GATHER if gather else 0) | (DOPT_STEP_HOST_GRADS if host_grads else 0)
+    flags = _flags(gather, host_grads, round_grad)
     cfg = adam.to_c()
     with torch.cuda.device(device):
         _check(lib().dopt_step_buckets(
@@ -319,7 +325,7 @@ def dopt_step_buckets(layout: Layout, adam: AdamConfig, step: int, first_bucket:
 
 def dopt_step_allreduce(layout: Layout, adam: AdamConfig, step: int, grad_replicas, master,
                         exp_avg, exp_avg_sq, param_replicas, gather: bool = True,
-                        main_grad_out=None, stream=None) -> None:
+                        main_grad_out=None, stream=None, round_grad: bool = False) -> None:
     """The step that also all-reduces the grads in place (force_all_reduce)."""
     import torch
 
@@ -329,8 +335,8 @@ def dopt_step_allreduce(layout: Layout, adam: AdamConfig, step: int, grad_replic
     with torch.cuda.device(device):
         _check(lib().dopt_step_allreduce(
             layout.handle, ctypes.byref(cfg), int(step), gp, dt, master.data_ptr(),
-            exp_avg.data_ptr(), exp_avg_sq.data_ptr(), pp, DOPT_STEP_GATHER if gather else 0, mg,
-            _stream_handle(stream)))
+            exp_avg.data_ptr(), exp_avg_sq.data_ptr(), pp, _flags(gather, round_grad=round_grad),
+            mg, _stream_handle(stream)))
 
 
 def dopt_allreduce(layout: Layout, grad_replicas, grad_scale: float, stream=None) -> None:
@@ -358,7 +364,7 @@ def dopt_allreduce(layout: Layout, grad_replicas, grad_scale: float, stream=None
 
 def dopt_step(layout: Layout, adam: AdamConfig, step: int, grad_replicas, master, exp_avg,
               exp_avg_sq, param_replicas, gather: bool = True, main_grad_out=None,
-              stream=None, host_grads: bool = False) -> None:
+              stream=None, host_grads: bool = False, round_grad: bool = False) -> None:
     """One fused ZeRO-1 step (reduce-scatter, AdamW, write-back, all-gather).
 
     grad_replicas: D bf16 or fp32 CUDA tensors (or, with host_grads, pinned
@@ -371,7 +377,7 @@ def dopt_step(layout: Layout, adam: AdamConfig, step: int, grad_replicas, master
 
     device, gp, pp, dt, mg = _step_pointers(layout, grad_replicas, master, exp_avg, exp_avg_sq,
                                             param_replicas, main_grad_out, host_grads)
-    flags = (DOPT_STEP_GATHER if gather else 0) | (DOPT_STEP_HOST_GRADS if host_grads else 0)
+    flags = _flags(gather, host_grads, round_grad)
     cfg = adam.to_c()
     with torch.cuda.device(device):
         _check(lib().dopt_step(layout.handle, ctypes.byref(cfg), int(step), gp, dt,
@@ -389,7 +395,8 @@ def clip_workspace(device=None):
 
 def dopt_step_clipped(layout: Layout, adam: AdamConfig, step: int, max_norm: float,
                       grad_replicas, master, exp_avg, exp_avg_sq, param_replicas, main_grad,
-                      workspace, gather: bool = True, norm_out=None, stream=None) -> None:
+                      workspace, gather: bool = True, norm_out=None, stream=None,
+                      round_grad: bool = False) -> None:
     """The step with global grad-norm clipping (two launches).
 
     main_grad: fp32 CUDA tensor of >= padded_numel elements (receives the
@@ -425,7 +432,7 @@ def dopt_step_clipped(layout: Layout, adam: AdamConfig, step: int, max_norm: flo
         _check(lib().dopt_step_clipped(
             layout.handle, ctypes.byref(cfg), int(step), float(max_norm), gp,
             DOPT_BF16 if gdt == torch.bfloat16 else DOPT_FP32, master.data_ptr(),
-            exp_avg.data_ptr(), exp_avg_sq.data_ptr(), pp, DOPT_STEP_GATHER if gather else 0,
+            exp_avg.data_ptr(), exp_avg_sq.data_ptr(), pp, _flags(gather, round_grad=round_grad),
             main_grad.data_ptr(), workspace.data_ptr(),
             None if norm_out is None else norm_out.data_ptr(), _stream_handle(stream)))
 

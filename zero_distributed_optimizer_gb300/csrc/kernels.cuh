@@ -80,6 +80,7 @@ struct StepArgs {
     int32_t D;
     int32_t R;  // ranks per instance (D with one instance)
     int32_t gather;
+    int32_t round_grad;  // round the reduced grad to the grad type first
     Scalars sc;
 };
 
@@ -105,6 +106,7 @@ struct NormArgs {
     int64_t n_tiles;
     int32_t D;
     int32_t R;
+    int32_t round_grad;
     float scale;
     float max_norm;
 };
@@ -159,6 +161,22 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&f)[8]) {
 __device__ __forceinline__ uint16_t to_bf16_bits(float x) {
     __nv_bfloat16 h = __float2bfloat16_rn(x);
     return *reinterpret_cast<uint16_t *>(&h);
+}
+
+// A reduced grad in the grad buffer's type: bf16 rounds to nearest even,
+// fp32 is already in its type.
+template <typename G>
+__device__ __forceinline__ float to_grad_type(float g) {
+    if constexpr (sizeof(G) == 2)
+        return __uint_as_float(uint32_t(to_bf16_bits(g)) << 16);
+    else
+        return g;
+}
+
+template <typename G>
+__device__ __forceinline__ void to_grad_type8(float (&acc)[8]) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc[k] = to_grad_type<G>(acc[k]);
 }
 
 __device__ __forceinline__ uint4 ld_stream(const void *p) {
@@ -381,6 +399,7 @@ __device__ __forceinline__ void full_vector(const StepArgs &a, int64_t e0, int32
         for (int k = 0; k < 8; ++k) acc[k] = __fmul_rn(f[k], coef);
     } else {
         reduce_vec<G, DC>(a, a.sc.scale, e0, acc);
+        if (a.round_grad) to_grad_type8<G>(acc);
     }
     if constexpr (MODE == kWriteGrads) write_grads_vec<G, DC>(a.grads, a.D, e0, acc);
 
@@ -432,10 +451,12 @@ __device__ __noinline__ void mixed_vector(const StepArgs &a, int64_t e0, int j) 
         if (!owned_at(a.rv, e, j, done)) continue;
         const int32_t meta = a.rv.run_meta[j];
         float g;
-        if constexpr (MODE == kFromMain)
+        if constexpr (MODE == kFromMain) {
             g = __fmul_rn(a.main_grad_in[e], *a.clip_coef);
-        else
+        } else {
             g = reduce_scalar<G>(a.grads, D, a.R, a.sc.scale, e);
+            if (a.round_grad) g = to_grad_type<G>(g);
+        }
         if constexpr (MODE == kWriteGrads)
             for (int r = 0; r < D; ++r) store_grad_scalar<G>(a.grads[r], e, g);
         float w = a.master[e], m = a.exp_avg[e], v = a.exp_avg_sq[e];
@@ -521,6 +542,7 @@ __global__ void __launch_bounds__(kThreads) dopt_rs_norm_kernel(const __grid_con
         if (kind == kFull) {
             float acc[8];
             reduce_vec<G, DC>(a, a.scale, e0, acc);
+            if (a.round_grad) to_grad_type8<G>(acc);
             st_stream_f4(a.main_grad + e0, make_float4(acc[0], acc[1], acc[2], acc[3]));
             st_stream_f4(a.main_grad + e0 + 4, make_float4(acc[4], acc[5], acc[6], acc[7]));
             float sq[8];
@@ -535,7 +557,8 @@ __global__ void __launch_bounds__(kThreads) dopt_rs_norm_kernel(const __grid_con
             for (int k = 0; k < kVec && !done; ++k) {
                 const int64_t e = e0 + k;
                 if (!owned_at(a.rv, e, j, done)) continue;
-                const float g = reduce_scalar<G>(a.grads, D, a.R, a.scale, e);
+                float g = reduce_scalar<G>(a.grads, D, a.R, a.scale, e);
+                if (a.round_grad) g = to_grad_type<G>(g);
                 a.main_grad[e] = g;
                 local += double(__fmul_rn(g, g));
             }

@@ -165,7 +165,7 @@ int check_step_args(const char *who, const dopt_layout *L, const dopt_adam_cfg *
     if (step < 1) return fail(DOPT_E_ARG, "%s: step=%lld < 1", who, (long long)step);
     if (grad_dtype != DOPT_BF16 && grad_dtype != DOPT_FP32)
         return fail(DOPT_E_ARG, "%s: unknown grad dtype %d", who, int(grad_dtype));
-    if (flags & ~uint32_t(DOPT_STEP_GATHER | DOPT_STEP_HOST_GRADS))
+    if (flags & ~uint32_t(DOPT_STEP_GATHER | DOPT_STEP_HOST_GRADS | DOPT_STEP_ROUND_GRAD))
         return fail(DOPT_E_ARG, "%s: unknown flags 0x%x", who, flags);
     if (!(cfg->lr >= 0.0f) || !std::isfinite(cfg->lr) || !(cfg->beta1 >= 0.0f && cfg->beta1 < 1.0f) ||
         !(cfg->beta2 >= 0.0f && cfg->beta2 < 1.0f) || !(cfg->eps >= 0.0f) || !std::isfinite(cfg->eps) ||
@@ -224,6 +224,7 @@ void fill_step_args(StepArgs &a, const dopt_layout *L, const dopt_adam_cfg *cfg,
     a.D = D;
     a.R = L->R;
     a.gather = (flags & DOPT_STEP_GATHER) ? 1 : 0;
+    a.round_grad = (flags & DOPT_STEP_ROUND_GRAD) ? 1 : 0;
     a.sc = make_scalars(*cfg, step);
 }
 
@@ -276,6 +277,7 @@ int launch_clipped(const char *who, const dopt_layout *L, const dopt_adam_cfg *c
     na.rv = whole_view(L, &na.n_tiles);
     na.D = D;
     na.R = L->R;
+    na.round_grad = (flags & DOPT_STEP_ROUND_GRAD) ? 1 : 0;
     na.scale = cfg->grad_scale;
     na.max_norm = max_norm;
     NormKernel nk = norm_kernel_for(grad_dtype, kernel_D(L));
