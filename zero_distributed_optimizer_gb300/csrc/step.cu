@@ -6,15 +6,24 @@
 #include <cstddef>
 #include <cstdint>
 #include <mutex>
+#include <vector>
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "dopt_internal.h"
 
 #include "kernels.cuh"
 
 namespace {
+
+// A named range around each entry point for timeline profilers (a no-op
+// when no profiler is attached).
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+};
 
 // ---------------------------------------------------------------------------
 // Host side
@@ -115,15 +124,38 @@ AllReduceKernel pick_allreduce_kernel(int D) {
     }
 }
 
+// SMs and resident CTAs per SM of a norm kernel on a device, asked once.
+struct GridInfo {
+    NormKernel kernel;
+    int device;
+    int sms;
+    int per_sm;
+};
+std::mutex g_grid_mutex;
+std::vector<GridInfo> g_grid_info;
+
+void sm_occupancy(NormKernel k, int device, int *sms, int *per_sm) {
+    std::lock_guard<std::mutex> lock(g_grid_mutex);
+    for (const GridInfo &g : g_grid_info)
+        if (g.kernel == k && g.device == device) {
+            *sms = g.sms;
+            *per_sm = g.per_sm;
+            return;
+        }
+    if (cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, k, kThreads, 0) != cudaSuccess) {
+        cudaGetLastError();
+        *sms = 1;
+        *per_sm = 1;
+        return;  // not cached: asked again next time
+    }
+    g_grid_info.push_back(GridInfo{k, device, *sms, *per_sm});
+}
+
 // Grid of the persistent norm pass: every SM full, at most kMaxClipCtas.
 int norm_grid(NormKernel k, int64_t n_tiles, int device) {
     int sms = 0, per_sm = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, 0) != cudaSuccess) {
-        cudaGetLastError();
-        sms = 1;
-        per_sm = 1;
-    }
+    sm_occupancy(k, device, &sms, &per_sm);
     // a whole number of CTAs per SM, so that every SM gets the same share
     const int per_sm_cap = std::max(1, kMaxClipCtas / std::max(sms, 1));
     int64_t g = int64_t(std::max(sms, 1)) * std::min(std::max(per_sm, 1), per_sm_cap);
@@ -323,6 +355,7 @@ extern "C" int dopt_step(const dopt_layout *L, const dopt_adam_cfg *cfg, int64_t
                          uint32_t flags, float *main_grad_out, cudaStream_t stream) {
     dopt::clear_error();
     const char *who = "dopt_step";
+    NvtxRange range(who);
     int rc = check_step_args(who, L, cfg, step, grad_replicas, grad_dtype, master, exp_avg,
                              exp_avg_sq, param_replicas, flags, main_grad_out);
     if (rc != DOPT_OK) return rc;
@@ -340,6 +373,7 @@ extern "C" int dopt_step_buckets(const dopt_layout *L, const dopt_adam_cfg *cfg,
     using dopt::fail;
     dopt::clear_error();
     const char *who = "dopt_step_buckets";
+    NvtxRange range(who);
     int rc = check_step_args(who, L, cfg, step, grad_replicas, grad_dtype, master, exp_avg,
                              exp_avg_sq, param_replicas, flags, main_grad_out);
     if (rc != DOPT_OK) return rc;
@@ -359,6 +393,7 @@ extern "C" int dopt_step_allreduce(const dopt_layout *L, const dopt_adam_cfg *cf
                                    float *main_grad_out, cudaStream_t stream) {
     dopt::clear_error();
     const char *who = "dopt_step_allreduce";
+    NvtxRange range(who);
     const void *const *grads = const_cast<const void *const *>(grad_replicas);
     int rc = check_step_args(who, L, cfg, step, grads, grad_dtype, master, exp_avg, exp_avg_sq,
                              param_replicas, flags, main_grad_out);
@@ -373,6 +408,7 @@ extern "C" int dopt_allreduce(const dopt_layout *L, void *const *grad_replicas,
     using dopt::fail;
     dopt::clear_error();
     const char *who = "dopt_allreduce";
+    NvtxRange range(who);
     if (!L || !grad_replicas) return fail(DOPT_E_ARG, "%s: NULL argument", who);
     if (grad_dtype != DOPT_BF16 && grad_dtype != DOPT_FP32)
         return fail(DOPT_E_ARG, "%s: unknown grad dtype %d", who, int(grad_dtype));
@@ -405,6 +441,7 @@ extern "C" int dopt_step_clipped(const dopt_layout *L, const dopt_adam_cfg *cfg,
     using dopt::fail;
     dopt::clear_error();
     const char *who = "dopt_step_clipped";
+    NvtxRange range(who);
     int rc = check_step_args(who, L, cfg, step, grad_replicas, grad_dtype, master, exp_avg,
                              exp_avg_sq, param_replicas, flags, main_grad);
     if (rc != DOPT_OK) return rc;
@@ -464,6 +501,7 @@ extern "C" int dopt_step_clipped_noalloc(const dopt_layout *L, const dopt_adam_c
     using dopt::fail;
     dopt::clear_error();
     const char *who = "dopt_step_clipped_noalloc";
+    NvtxRange range(who);
     int rc = check_step_args(who, L, cfg, step, grad_replicas, grad_dtype, master, exp_avg,
                              exp_avg_sq, param_replicas, flags, main_grad);
     if (rc != DOPT_OK) return rc;
@@ -490,6 +528,7 @@ extern "C" int dopt_gather(const dopt_layout *L, void *const *param_replicas, cu
     using dopt::fail;
     dopt::clear_error();
     const char *who = "dopt_gather";
+    NvtxRange range(who);
     if (!L || !param_replicas) return fail(DOPT_E_ARG, "%s: NULL argument", who);
     const int D = L->cfg.D;
     int rc = check_replicas(who, D, const_cast<const void *const *>(param_replicas));
