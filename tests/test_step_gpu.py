@@ -268,3 +268,28 @@ def test_device_errors():
     assert e.value.code == B.DOPT_E_ALIGN
     B.dopt_step(L, B.AdamConfig(), 1, g, *st, p)  # the context is still usable
     torch.cuda.synchronize()
+
+
+def test_step_plan_equals_per_call_binding():
+    """A StepPlan (arguments checked once) gives the same results as the
+    per-call binding, for whole steps and for bucket launches."""
+    sizes, wd, D = [30000, 7, 20000, 513, 9000], [1, 0, 1, 0, 1], 4
+    L = B.dopt_build_range_map(sizes, D, 15000, 8, wd).to_device()
+    N = L.padded_numel
+    master, m, v, params, grads = W.random_case(N, D, 2, "bf16", 33)
+    a = [master.to(DEV), m.to(DEV), v.to(DEV)]
+    b = [x.clone() for x in a]
+    pa = [p.to(DEV) for p in params]
+    pb = [p.clone() for p in pa]
+    ga = [g.to(DEV) for g in grads[0]]
+    gb = [g.clone() for g in ga]
+    adam = B.AdamConfig(grad_scale=0.25)
+    plan = B.StepPlan(L, adam, gb, *b, pb)
+    B.dopt_step(L, adam, 1, ga, *a, pa)
+    plan.step(1)
+    for k in range(L.n_buckets):
+        B.dopt_step_buckets(L, adam, 2, k, 1, ga, *a, pa)
+        plan.step_buckets(2, k)
+    torch.cuda.synchronize()
+    for x, y in zip(a + pa, b + pb):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16))

@@ -22,6 +22,7 @@ from .binding import (  # noqa: F401
     AdamConfig,
     DoptError,
     Layout,
+    StepPlan,
     dopt_allreduce,
     dopt_build_range_map,
     dopt_gather,

@@ -385,6 +385,45 @@ def dopt_step(layout: Layout, adam: AdamConfig, step: int, grad_replicas, master
                                flags, mg, _stream_handle(stream)))
 
 
+class StepPlan:
+    """The arguments of repeated steps over the same buffers, checked and
+    marshalled once: each ``step`` / ``step_buckets`` is then one call into
+    the library (the per-call checks of :func:`dopt_step` cost more host time
+    than a small launch).  The plan keeps the tensors alive; the caller must
+    not reallocate them while the plan is in use."""
+
+    def __init__(self, layout: Layout, adam: AdamConfig, grad_replicas, master, exp_avg,
+                 exp_avg_sq, param_replicas, gather: bool = True, main_grad_out=None,
+                 host_grads: bool = False, round_grad: bool = False, stream=None):
+        import torch
+
+        self.device, self._gp, self._pp, self._dt, self._mg = _step_pointers(
+            layout, grad_replicas, master, exp_avg, exp_avg_sq, param_replicas, main_grad_out,
+            host_grads)
+        self.layout = layout
+        self._keep = (list(grad_replicas), master, exp_avg, exp_avg_sq, list(param_replicas),
+                      main_grad_out)
+        self._state = (master.data_ptr(), exp_avg.data_ptr(), exp_avg_sq.data_ptr())
+        self._flags = _flags(gather, host_grads, round_grad)
+        self._cfg = adam.to_c()
+        with torch.cuda.device(self.device):
+            self._stream = _stream_handle(stream)
+        self._lib = lib()
+
+    def step(self, step: int) -> None:
+        """dopt_step on the planned buffers."""
+        _check(self._lib.dopt_step(self.layout.handle, ctypes.byref(self._cfg), int(step), self._gp,
+                                   self._dt, *self._state, self._pp, self._flags, self._mg,
+                                   self._stream))
+
+    def step_buckets(self, step: int, first_bucket: int, n_buckets: int = 1, stream=None) -> None:
+        """dopt_step_buckets on the planned buffers (optionally another stream)."""
+        st = self._stream if stream is None else _stream_handle(stream)
+        _check(self._lib.dopt_step_buckets(self.layout.handle, ctypes.byref(self._cfg), int(step),
+                                           int(first_bucket), int(n_buckets), self._gp, self._dt,
+                                           *self._state, self._pp, self._flags, self._mg, st))
+
+
 def clip_workspace(device=None):
     """A device workspace for dopt_step_clipped (DOPT_CLIP_WORKSPACE_BYTES)."""
     import torch

@@ -58,6 +58,8 @@ def main(argv=None):
                          "force_all_reduce")
     ap.add_argument("--streams", type=int, default=1,
                     help="buckets mode: bucket k is launched on stream k mod STREAMS")
+    ap.add_argument("--plan", action="store_true",
+                    help="step and buckets modes: launch through a StepPlan")
     args = ap.parse_args(argv)
 
     libbuild.build()
@@ -79,6 +81,7 @@ def main(argv=None):
         main_grad = torch.empty(N, device=dev)
         ws = B.clip_workspace(dev)
     streams = [torch.cuda.current_stream()] + [torch.cuda.Stream(dev) for _ in range(args.streams - 1)]
+    plan = B.StepPlan(L, adam, grads, master, m, v, params) if args.plan else None
 
     def bucket_launches(t):
         # fork the side streams off the main one, launch, join them back
@@ -88,7 +91,10 @@ def main(argv=None):
             s_.wait_event(fork)
         for k in range(L.n_buckets):
             s_ = streams[k % len(streams)]
-            B.dopt_step_buckets(L, adam, t, k, 1, grads, master, m, v, params, stream=s_)
+            if plan is not None:
+                plan.step_buckets(t, k, 1, stream=s_)
+            else:
+                B.dopt_step_buckets(L, adam, t, k, 1, grads, master, m, v, params, stream=s_)
         for s_ in streams[1:]:
             join = torch.cuda.Event()
             join.record(s_)
@@ -128,6 +134,8 @@ def main(argv=None):
             B.dopt_step_allreduce(L, adam, t, grads, master, m, v, params)
         elif args.mode == "clipped":
             B.dopt_step_clipped(L, adam, t, 1.0, grads, master, m, v, params, main_grad, ws)
+        elif plan is not None:
+            plan.step(t)
         else:
             B.dopt_step(L, adam, t, grads, master, m, v, params)
     ev[1].record()
@@ -140,7 +148,7 @@ def main(argv=None):
                 "step_allreduce": step_bytes + w.D * w.grad_bytes}[args.mode]
     bytes_per = w.numel * per_elem
     print(json.dumps({"workload": w.name, "N": w.numel, "padded_numel": N, "D": w.D,
-                      "mode": args.mode, "n_buckets": L.n_buckets, "streams": args.streams,
+                      "mode": args.mode, "n_buckets": L.n_buckets, "streams": args.streams, "plan": args.plan,
                       "launches": args.launches, "ms_per_launch": ms,
                       "algorithmic_bytes_per_launch": bytes_per,
                       "gbs": bytes_per / (ms / 1e3) / 1e9}))
