@@ -132,3 +132,26 @@ def test_host_grads_refuses_unpinned_memory():
                                B.DOPT_STEP_GATHER | B.DOPT_STEP_HOST_GRADS, None, None)
         assert rc == B.DOPT_E_ARG, rc
     torch.cuda.synchronize()  # the context is still usable
+
+
+def test_host_stepper_results():
+    """The pipelined stepper gives the same state and, after synchronize,
+    the same host copy of the params as step_from_host, step by step."""
+    D = 4
+    L, N, master, m, v, params, grads = _setup([400000, 3, 12345], [1, 0, 1], D, 0, 64, "bf16", 9)
+    a = [master.to(DEV), m.to(DEV), v.to(DEV)]
+    b = [x.clone() for x in a]
+    pa = [p.to(DEV) for p in params]
+    pb = [p.clone() for p in pa]
+    outa = torch.empty(N, dtype=torch.bfloat16).pin_memory()
+    outb = torch.empty(N, dtype=torch.bfloat16).pin_memory()
+    adam = B.AdamConfig(grad_scale=0.25)
+    stepper = B.HostStepper(L, adam, *b, pb, outb)
+    for i in range(2):
+        host = [g.contiguous().pin_memory() for g in grads[i]]
+        B.step_from_host(L, adam, i + 1, host, None, *a, pa, outa, zero_copy=True)
+        stepper.step(i + 1, host)
+        stepper.synchronize()
+        torch.cuda.synchronize()
+        assert torch.equal(outa.view(torch.int16), outb.view(torch.int16))
+    _eq(a + pa, b + pb)

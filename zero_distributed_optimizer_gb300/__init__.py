@@ -21,6 +21,7 @@ from .binding import (  # noqa: F401
     DOPT_STEP_ROUND_GRAD,
     AdamConfig,
     DoptError,
+    HostStepper,
     Layout,
     StepPlan,
     dopt_allreduce,

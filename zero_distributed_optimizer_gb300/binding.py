@@ -424,6 +424,56 @@ class StepPlan:
                                            *self._state, self._pp, self._flags, self._mg, st))
 
 
+class HostStepper:
+    """Steps whose grads arrive in pinned host memory and whose result (param
+    replica 0) goes back to pinned host memory, pipelined: every step reads
+    the host grads in place (DOPT_STEP_HOST_GRADS), copies replica 0 to a
+    device staging buffer, and returns it to `host_params_out` on a side
+    stream while the next step runs.  `host_params_out` holds the result of
+    the latest step once :meth:`synchronize` (or a device-wide sync) has
+    returned; reading it earlier races with the copy."""
+
+    def __init__(self, layout: Layout, adam: AdamConfig, master, exp_avg, exp_avg_sq,
+                 param_replicas, host_params_out, stream=None):
+        import torch
+
+        if host_params_out.device.type != "cpu" or not host_params_out.is_pinned():
+            raise DoptError(DOPT_E_ARG, "host_params_out must be a pinned CPU tensor")
+        _check_tensor(host_params_out, "host_params_out", torch.bfloat16, layout.padded_numel,
+                      host_params_out.device)
+        self.layout, self.adam = layout, adam
+        self.state = (master, exp_avg, exp_avg_sq)
+        self.params = list(param_replicas)
+        self.out = host_params_out
+        self.device = master.device
+        self.stream = torch.cuda.current_stream(self.device) if stream is None else stream
+        self.copy_stream = torch.cuda.Stream(self.device)
+        self.stage = torch.empty_like(self.params[0])
+        self.copied = None
+
+    def step(self, step: int, host_grads) -> None:
+        import torch
+
+        with torch.cuda.stream(self.stream):
+            dopt_step(self.layout, self.adam, step, host_grads, *self.state, self.params,
+                      gather=True, stream=self.stream, host_grads=True)
+            if self.copied is not None:  # the staging buffer is free again
+                self.stream.wait_event(self.copied)
+            self.stage.copy_(self.params[0], non_blocking=True)
+            ready = torch.cuda.Event()
+            ready.record(self.stream)
+        self.copy_stream.wait_event(ready)
+        with torch.cuda.stream(self.copy_stream):
+            self.out.copy_(self.stage, non_blocking=True)
+            self.copied = torch.cuda.Event()
+            self.copied.record(self.copy_stream)
+
+    def synchronize(self) -> None:
+        """Make the caller's stream wait for the last result copy."""
+        if self.copied is not None:
+            self.stream.wait_event(self.copied)
+
+
 def clip_workspace(device=None):
     """A device workspace for dopt_step_clipped (DOPT_CLIP_WORKSPACE_BYTES)."""
     import torch
