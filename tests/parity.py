@@ -105,3 +105,32 @@ def sample_windows(buckets, pieces, numel, seed, n_edges=48, n_random=12, rand_l
         a = int(rng.integers(0, max(1, numel - rand_len)))
         wins.append((a, a + rand_len))
     return merge_windows(wins, numel)
+
+
+def oracle_step_whole(sizes, wd_mask, D, bucket_elems, pad_unit, adam, t, grads, master,
+                      exp_avg, exp_avg_sq, params, main_grad_out=None, threads=None, **kw):
+    """The oracle's step over a whole buffer, cut into disjoint windows that
+    host threads step at the same time.  Every output element depends on
+    its own inputs alone and the ctypes call releases the GIL, so the
+    result equals one call over the whole buffer bit for bit (a CPU test
+    checks that)."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+
+    n = len(master)
+    k = max(1, min(threads or os.cpu_count() or 1, 32))
+    cuts = [n * i // k for i in range(k + 1)]
+
+    def one(i):
+        a, b = cuts[i], cuts[i + 1]
+        if a == b:
+            return
+        oracle.step(sizes, wd_mask, D, bucket_elems, pad_unit, adam, t, [g[a:b] for g in grads],
+                    master[a:b], exp_avg[a:b], exp_avg_sq[a:b], [p[a:b] for p in params],
+                    main_grad_out=None if main_grad_out is None else main_grad_out[a:b],
+                    window=(a, b), **kw)
+
+    with ThreadPoolExecutor(k) as ex:
+        list(ex.map(one, range(k)))
