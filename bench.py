@@ -10,8 +10,8 @@ D*64).  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
---impl reference times the CPU oracle (plain C, one thread) on a bounded
-window of the same workload, on the host cores.  With N>1 (torchrun, one
+--impl reference times the CPU oracle (plain C, run on every host core over
+disjoint windows) on a bounded sample of the same workload.  With N>1 (torchrun, one
 rank per GPU) every rank runs its own replica of the workload: the step has
 no data exchange between GPUs, so the ranks only meet for the timing
 barrier and the max-over-ranks reduction.
@@ -183,16 +183,19 @@ class ClockSampler:
 
 
 def cpu_oracle_rate(w: W.Workload, seconds: float = 12.0, max_steps: int = 40, grads_src=None,
-                    state_src=None, sample=CPU_SAMPLE_ELEMS):
-    """Elements/s of the oracle (as it stands, one host thread) stepping the
-    first `sample` buffer elements of the workload, repeated for about
-    `seconds` seconds."""
+                    state_src=None, sample=CPU_SAMPLE_ELEMS, threads: int = 1):
+    """Elements/s of the oracle (as it stands) stepping the first `sample`
+    buffer elements of the workload, repeated for about `seconds` seconds.
+    With threads > 1 the sample is cut into that many disjoint windows and
+    each host thread steps one (the oracle's C call releases the GIL and
+    every element depends on its own inputs alone)."""
+    from concurrent.futures import ThreadPoolExecutor
+    from dataclasses import asdict
+
     import numpy as np
     import torch
 
     import oracle
-    from dataclasses import asdict
-
     from zero_distributed_optimizer_gb300.binding import AdamConfig
 
     oracle.build()
@@ -212,14 +215,30 @@ def cpu_oracle_rate(w: W.Workload, seconds: float = 12.0, max_steps: int = 40, g
     master, m, v = (host(x) for x in state_src)
     params = [np.zeros(sample, np.uint16) for _ in range(w.D)]
     sizes, wd = list(w.sizes), list(w.wd_mask)
+    threads = max(1, min(threads, sample))
+    cuts = [sample * i // threads for i in range(threads + 1)]
+
+    def window(i, t):
+        a, b = cuts[i], cuts[i + 1]
+        oracle.step(sizes, wd, w.D, w.bucket_elems, w.pad_unit, adam, t,
+                    [g[a:b] for g in grads], master[a:b], m[a:b], v[a:b],
+                    [p[a:b] for p in params], window=(a, b))
+
     steps = 0
-    t0 = time.perf_counter()
-    while steps < max_steps and (time.perf_counter() - t0) < seconds:
-        oracle.step(sizes, wd, w.D, w.bucket_elems, w.pad_unit, adam, steps + 1, grads, master,
-                    m, v, params, window=(0, sample))
-        steps += 1
-    dt = time.perf_counter() - t0
+    with ThreadPoolExecutor(threads) as ex:
+        t0 = time.perf_counter()
+        while steps < max_steps and (time.perf_counter() - t0) < seconds:
+            list(ex.map(window, range(threads), [steps + 1] * threads))
+            steps += 1
+        dt = time.perf_counter() - t0
     return sample * steps / dt, steps, dt, sample
+
+
+def host_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
 
 
 WORKLOADS = ("gpt2_small", "toy_1000", "llama_1p3b", "sweep_256m", "moe_many_small")
@@ -240,14 +259,17 @@ def run_reference(args):
     w = workload_by_name(args.workload)
     import torch
 
-    grads_src = W.make_grads(w, CPU_SAMPLE_ELEMS, 1, "cpu")
-    state_src = W.make_state(w, CPU_SAMPLE_ELEMS, "cpu")
+    threads = args.cpu_threads or host_threads()
+    elems = CPU_SAMPLE_ELEMS * threads
+    grads_src = W.make_grads(w, elems, 1, "cpu")
+    state_src = W.make_state(w, elems, "cpu")
     cpu_oracle_rate(w, seconds=1e9, max_steps=max(1, args.warmup), grads_src=grads_src,
-                    state_src=state_src)
+                    state_src=state_src, sample=elems, threads=threads)
     rate, steps, dt, used = cpu_oracle_rate(w, seconds=1e9, max_steps=args.steps,
-                                            grads_src=grads_src, state_src=state_src)
+                                            grads_src=grads_src, state_src=state_src,
+                                            sample=elems, threads=threads)
     sample = (f"first {used} elements of the {w.name} buffer (D={w.D}), "
-              f"{steps} oracle steps, one host thread")
+              f"{steps} oracle steps, {threads} host threads on disjoint windows")
     line = {
         "impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": world,
         "steps": steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / max(steps, 1),
@@ -256,7 +278,7 @@ def run_reference(args):
         "config": {"workload": w.name, "N": w.numel, "D": w.D, "bucket_elems": w.bucket_elems,
                    "pad_unit": w.pad_unit, "grad_dtype": w.grad_dtype,
                    "sample_elems": used},
-        "cpu_baseline": {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "torch": torch.__version__,
@@ -394,11 +416,18 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, steps_done, dt, used = cpu_oracle_rate(w, seconds=args.cpu_seconds,
-                                                     grads_src=grads, state_src=(master, m, v))
-        cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"first {used} elements of the {w.name} buffer, "
-                         f"{steps_done} oracle steps in {dt:.1f} s, one host thread"}
+        threads = args.cpu_threads or host_threads()
+        rate1, steps1, dt1, used1 = cpu_oracle_rate(w, seconds=args.cpu_seconds / 2,
+                                                    grads_src=grads, state_src=(master, m, v))
+        rate, steps_done, dt, used = cpu_oracle_rate(
+            w, seconds=args.cpu_seconds / 2, grads_src=grads, state_src=(master, m, v),
+            sample=CPU_SAMPLE_ELEMS * threads, threads=threads)
+        cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"first {used} elements of the {w.name} buffer, {steps_done} oracle "
+                         f"steps in {dt:.1f} s, {threads} host threads on disjoint windows",
+               "one_thread": {"value": rate1, "cores": 1,
+                              "sample": f"first {used1} elements, {steps1} oracle steps in "
+                                        f"{dt1:.1f} s"}}
 
     if rank == 0:
         line = {
@@ -439,7 +468,10 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="wall time of the CPU-baseline legs (one thread, all threads)")
+    ap.add_argument("--cpu-threads", type=int, default=0,
+                    help="host threads of the oracle runs (0: every core this process may use)")
     ap.add_argument("--workload", choices=WORKLOADS, default="gpt2_small",
                     help="the GPT-2-small layout is the configuration of the reported metric")
     args = ap.parse_args(argv)
