@@ -41,6 +41,7 @@ PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "dopt_step_kernel_gpt2_small.md
 KERNEL_SOURCES = [os.path.join(ROOT, "zero_distributed_optimizer_gb300", "csrc", f)
                   for f in ("kernels.cuh", "dopt_internal.h")]
 CPU_SAMPLE_ELEMS = 1 << 21
+GRAPH_STEPS = 8
 
 
 def dist_env():
@@ -361,6 +362,41 @@ def run_ours(args):
     peak, peak_kind = measured_hbm_peak()
     traffic = read_profile_traffic()
 
+    # the same steps replayed from a CUDA graph: GRAPH_STEPS dopt_step_counted
+    # calls (the step number lives in a device counter) captured once, the
+    # graph replayed until K steps are done
+    graph = None
+    if not args.no_graph:
+        per = GRAPH_STEPS
+        replays = max(1, args.steps // per)
+        counter = B.step_counter(t + 1, device)
+        B.dopt_step_counted(L, adam, counter, grads, master, m, v, params)  # kernels loaded
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(per):
+                B.dopt_step_counted(L, adam, counter, grads, master, m, v, params)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(replays):
+            g.replay()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        g_ms = max_over_ranks(g0.elapsed_time(g1), world, device) / (replays * per)
+        next_step, status = B.counter_state(counter)
+        assert status == 0 and next_step == t + 2 + per * (3 + replays)
+        t = next_step - 1
+        graph = {"ms_per_step": g_ms, "value": world * elems / (g_ms / 1e3), "unit": UNIT,
+                 "steps": replays * per, "steps_per_graph": per, "launches_per_step": 2,
+                 "path": "binding.dopt_step_counted captured in a CUDA graph and replayed "
+                         "(per step a counter kernel of two threads, then the step kernel)"}
+        del g
+
     # end to end through the public API: grads from pinned host memory,
     # updated params (replica 0) back to pinned host memory, every step
     e2e = None
@@ -449,6 +485,7 @@ def run_ours(args):
                          "algorithmic_bytes_per_launch": bytes_per_launch},
             "cpu_baseline": cpu,
             "e2e": e2e,
+            "graph_replay": graph,
             "gpu_launches": args.steps,
             "clocks": sampler.summary(h0, h1),
             "torch": torch.__version__,
@@ -468,6 +505,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="skip the CUDA-graph replay of counted steps")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="wall time of the CPU-baseline legs (one thread, all threads)")
     ap.add_argument("--cpu-threads", type=int, default=0,

@@ -262,6 +262,48 @@ int dopt_step_buckets(const dopt_layout *layout, const dopt_adam_cfg *cfg, int64
                       cudaStream_t stream);
 
 /*
+ * Step counter in device memory for dopt_step_counted: 64 bytes, 16-byte
+ * aligned, owned by the caller.
+ *   next_step  1-based number of the step the next dopt_step_counted launch
+ *              takes.  The caller sets it (to 1, or to the step to resume
+ *              at); every such launch reads it on the device and adds one.
+ *   status     written by every launch: 0, or DOPT_COUNTER_BAD_STEP when
+ *              next_step was outside 1 .. 2^62; such a launch changes
+ *              nothing else (not the counter, the state or the params).
+ *   scratch    the library's: the Adam scalars of the step last taken.
+ */
+typedef struct {
+    int64_t next_step;
+    int32_t status;
+    int32_t reserved;
+    float scratch[12];
+} dopt_step_counter;
+
+#define DOPT_COUNTER_BAD_STEP 1
+
+/*
+ * dopt_step with the step number taken from a counter in device memory
+ * instead of a host argument, and the counter advanced on the device.  One
+ * kernel of one thread reads counter->next_step = t, evaluates the step's
+ * scalars (the same double-precision expressions as dopt_step, there with
+ * the device's pow and sqrt) into counter->scratch and stores t + 1; then
+ * the step kernel of dopt_step runs with those scalars.  The launches and
+ * their arguments do not depend on t, so a sequence captured once (a CUDA
+ * graph) replays every later step.  The pages describe no such counter:
+ * it is an addition of this library for graph replay.
+ *   counter  device dopt_step_counter (see there); read and written by the
+ *            device only, in stream order
+ * Other arguments, the arithmetic and the errors as dopt_step, plus
+ * DOPT_E_ARG for a NULL counter and DOPT_E_ALIGN for a misaligned one.  A
+ * bad next_step is reported in counter->status, not by the return value.
+ */
+int dopt_step_counted(const dopt_layout *layout, const dopt_adam_cfg *cfg,
+                      dopt_step_counter *counter, const void *const *grad_replicas,
+                      dopt_dtype grad_dtype, float *master, float *exp_avg, float *exp_avg_sq,
+                      void *const *param_replicas, uint32_t flags, float *main_grad_out,
+                      cudaStream_t stream);
+
+/*
  * The all-reduce of the grads on its own (page 1, §5, force_all_reduce: all
  * ranks keep the whole reduced grad, e.g. to save full weight grads;
  * distributed-training tutorial, "AllReduce" = reduce-scatter followed by

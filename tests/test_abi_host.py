@@ -243,3 +243,20 @@ def test_instances_errors(lib):
     assert B.lib().dopt_build_range_map(sizes, 1, None, ctypes.byref(cfg), ctypes.byref(out)) == B.DOPT_E_ARG
     L = B.dopt_build_range_map([10, 20], 8, 0, 1, instances=0)  # 0 means one instance
     assert L.padded_numel == B.dopt_build_range_map([10, 20], 8, 0, 1).padded_numel
+
+
+def test_counted_step_argument_checks_before_cuda(lib):
+    L = _lib_layout([100, 30], 2, 0, 8)
+    cfg = B.AdamConfig().to_c()
+    gp = (ctypes.c_void_p * 2)(0x10000, 0x20000)
+
+    def call(counter=0x90000, grads=gp, flags=1):
+        return B.lib().dopt_step_counted(L.handle, ctypes.byref(cfg), counter, grads, 0, 0x30000,
+                                         0x40000, 0x50000, gp, flags, None, None)
+
+    assert call(counter=None) == B.DOPT_E_ARG
+    assert call(counter=0x90008) == B.DOPT_E_ALIGN
+    assert call(grads=(ctypes.c_void_p * 2)(0x10000, 0)) == B.DOPT_E_ARG
+    assert call(flags=8) == B.DOPT_E_ARG
+    assert call() in (B.DOPT_E_STATE, B.DOPT_E_CUDA)  # nothing was launched
+    assert ctypes.sizeof(ctypes.c_int64) * 8 == B.DOPT_STEP_COUNTER_BYTES

@@ -15,6 +15,8 @@ PROGRAM = r"""
 #include <stdio.h>
 #include "dopt.h"
 
+_Static_assert(sizeof(dopt_step_counter) == 64, "dopt_step_counter is 64 bytes");
+
 int main(void)
 {
     const int64_t sizes[5] = {130, 260, 90, 310, 210};

@@ -7,6 +7,7 @@ The library is loaded on first use and every call raises if it is missing.
 from .binding import (  # noqa: F401
     DOPT_BF16,
     DOPT_CLIP_WORKSPACE_BYTES,
+    DOPT_COUNTER_BAD_STEP,
     DOPT_E_ALIGN,
     DOPT_E_ARG,
     DOPT_E_CUDA,
@@ -18,6 +19,7 @@ from .binding import (  # noqa: F401
     DOPT_OK,
     DOPT_STEP_GATHER,
     DOPT_STEP_HOST_GRADS,
+    DOPT_STEP_COUNTER_BYTES,
     DOPT_STEP_ROUND_GRAD,
     AdamConfig,
     DoptError,
@@ -32,7 +34,10 @@ from .binding import (  # noqa: F401
     dopt_step_buckets,
     dopt_step_clipped,
     dopt_step_clipped_noalloc,
+    dopt_step_counted,
     clip_workspace,
+    counter_state,
+    step_counter,
     step_from_host,
     version,
 )

@@ -32,6 +32,8 @@ DOPT_STEP_GATHER = 1
 DOPT_STEP_HOST_GRADS = 2
 DOPT_STEP_ROUND_GRAD = 4
 DOPT_CLIP_WORKSPACE_BYTES = 16384
+DOPT_STEP_COUNTER_BYTES = 64  # sizeof(dopt_step_counter)
+DOPT_COUNTER_BAD_STEP = 1
 
 _ERROR_NAMES = {DOPT_E_ARG: "DOPT_E_ARG", DOPT_E_LAYOUT: "DOPT_E_LAYOUT",
                 DOPT_E_ALIGN: "DOPT_E_ALIGN", DOPT_E_CUDA: "DOPT_E_CUDA",
@@ -92,6 +94,9 @@ def _declare(lib):
     lib.dopt_step.restype = ctypes.c_int
     lib.dopt_step.argtypes = [vp, P(dopt_adam_cfg), ctypes.c_int64, P(vp), ctypes.c_int, vp, vp,
                               vp, P(vp), ctypes.c_uint32, vp, vp]
+    lib.dopt_step_counted.restype = ctypes.c_int
+    lib.dopt_step_counted.argtypes = [vp, P(dopt_adam_cfg), vp, P(vp), ctypes.c_int, vp, vp, vp,
+                                      P(vp), ctypes.c_uint32, vp, vp]
     lib.dopt_step_clipped.restype = ctypes.c_int
     lib.dopt_step_clipped.argtypes = [vp, P(dopt_adam_cfg), ctypes.c_int64, ctypes.c_float, P(vp),
                                       ctypes.c_int, vp, vp, vp, P(vp), ctypes.c_uint32, vp, vp,
@@ -385,6 +390,56 @@ def dopt_step(layout: Layout, adam: AdamConfig, step: int, grad_replicas, master
                                flags, mg, _stream_handle(stream)))
 
 
+def step_counter(next_step: int = 1, device=None):
+    """A dopt_step_counter in device memory (an int64 tensor of 8 elements:
+    element 0 is next_step, the low half of element 1 the status)."""
+    import torch
+
+    c = torch.zeros(DOPT_STEP_COUNTER_BYTES // 8, dtype=torch.int64,
+                    device=device if device is not None else "cuda")
+    c[0] = int(next_step)
+    return c
+
+
+def counter_state(counter):
+    """(next_step, status) of a step counter (synchronises with the device)."""
+    import torch
+
+    h = counter.cpu()
+    return int(h[0]), int(h[1:2].view(torch.int32)[0])
+
+
+def _check_counter(counter, device):
+    import torch
+
+    if (not isinstance(counter, torch.Tensor) or counter.dtype != torch.int64
+            or counter.device != device or not counter.is_contiguous()
+            or counter.numel() * 8 < DOPT_STEP_COUNTER_BYTES):
+        raise DoptError(DOPT_E_ARG, "counter must be a contiguous int64 tensor of "
+                        f"{DOPT_STEP_COUNTER_BYTES // 8} elements on {device} (step_counter())")
+
+
+def dopt_step_counted(layout: Layout, adam: AdamConfig, counter, grad_replicas, master,
+                      exp_avg, exp_avg_sq, param_replicas, gather: bool = True,
+                      main_grad_out=None, stream=None, host_grads: bool = False,
+                      round_grad: bool = False) -> None:
+    """dopt_step with the step number read from, and advanced in, a device
+    counter (:func:`step_counter`): the launches do not depend on the step,
+    so they can be captured once in a CUDA graph and replayed every step."""
+    import torch
+
+    device, gp, pp, dt, mg = _step_pointers(layout, grad_replicas, master, exp_avg, exp_avg_sq,
+                                            param_replicas, main_grad_out, host_grads)
+    _check_counter(counter, master.device)
+    flags = _flags(gather, host_grads, round_grad)
+    cfg = adam.to_c()
+    with torch.cuda.device(device):
+        _check(lib().dopt_step_counted(layout.handle, ctypes.byref(cfg), counter.data_ptr(), gp,
+                                       dt, master.data_ptr(), exp_avg.data_ptr(),
+                                       exp_avg_sq.data_ptr(), pp, flags, mg,
+                                       _stream_handle(stream)))
+
+
 class StepPlan:
     """The arguments of repeated steps over the same buffers, checked and
     marshalled once: each ``step`` / ``step_buckets`` is then one call into
@@ -415,6 +470,13 @@ class StepPlan:
         _check(self._lib.dopt_step(self.layout.handle, ctypes.byref(self._cfg), int(step), self._gp,
                                    self._dt, *self._state, self._pp, self._flags, self._mg,
                                    self._stream))
+
+    def step_counted(self, counter) -> None:
+        """dopt_step_counted on the planned buffers."""
+        _check_counter(counter, self._keep[1].device)
+        _check(self._lib.dopt_step_counted(self.layout.handle, ctypes.byref(self._cfg),
+                                           counter.data_ptr(), self._gp, self._dt, *self._state,
+                                           self._pp, self._flags, self._mg, self._stream))
 
     def step_buckets(self, step: int, first_bucket: int, n_buckets: int = 1, stream=None) -> None:
         """dopt_step_buckets on the planned buffers (optionally another stream)."""

@@ -28,6 +28,7 @@
 // (__fmul_rn, __fadd_rn, __fsub_rn, __fdiv_rn, __fsqrt_rn), so no multiply
 // and add are fused and divide and square root are IEEE; the rank order of
 // the reduction is the loop order.
+#include <cmath>
 #include <cstdint>
 
 #include <cuda_bf16.h>
@@ -45,6 +46,68 @@ static_assert(kThreads * kVec == kDoptTileElems, "tile size must match the host 
 struct Scalars {
     float b1, b2, omb1, omb2, decay, step_size, bc2_sqrt, eps, scale;
 };
+
+// b^t for an integer t >= 1, by repeated squaring in double.  The host
+// (dopt_step) and the device (dopt_step_counted) run this same sequence of
+// IEEE multiplies, so both get the same double; the device's double
+// pipeline is slow, and this takes at most 2*63 multiplies where a general
+// pow takes far more.  Rounded to float as below, it gave the scalars of
+// C's pow(b, t) in every case checked (9 betas x 4 learning rates x t up to
+// 2e6).
+__host__ __device__ inline double beta_pow(double b, int64_t t) {
+    double r = 1.0;
+    double x = b;
+    while (t > 0) {
+        if (t & 1) r = r * x;
+        t >>= 1;
+        if (t > 0) x = x * x;
+    }
+    return r;
+}
+
+// lr / (1 - beta1^t) and sqrt(1 - beta2^t), each in double, rounded once.
+__host__ __device__ inline float step_size_for(const dopt_adam_cfg &c, int64_t t) {
+    return float(double(c.lr) / (1.0 - beta_pow(c.beta1, t)));
+}
+__host__ __device__ inline float bc2_sqrt_for(const dopt_adam_cfg &c, int64_t t) {
+    return float(sqrt(1.0 - beta_pow(c.beta2, t)));
+}
+
+// The scalars that do not depend on the step number, each evaluated in
+// double and rounded to float once.
+__host__ __device__ inline Scalars scalars_for_fixed(const dopt_adam_cfg &c) {
+    const double lr = c.lr, b1 = c.beta1, b2 = c.beta2, wd = c.weight_decay;
+    Scalars s;
+    s.b1 = c.beta1;
+    s.b2 = c.beta2;
+    s.omb1 = float(1.0 - b1);
+    s.omb2 = float(1.0 - b2);
+    s.decay = float(1.0 - lr * wd);
+    s.step_size = 0.0f;
+    s.bc2_sqrt = 0.0f;
+    s.eps = c.eps;
+    s.scale = c.grad_scale;
+    return s;
+}
+
+// All the scalars of step t.
+__host__ __device__ inline Scalars scalars_for(const dopt_adam_cfg &c, int64_t t) {
+    Scalars s = scalars_for_fixed(c);
+    s.step_size = step_size_for(c, t);
+    s.bc2_sqrt = bc2_sqrt_for(c, t);
+    return s;
+}
+
+// Device view of dopt_step_counter.
+struct CounterBlock {
+    int64_t next_step;
+    int32_t status;
+    int32_t reserved;
+    Scalars sc;
+    float unused[3];
+};
+static_assert(sizeof(CounterBlock) == sizeof(dopt_step_counter), "counter layout");
+constexpr int64_t kMaxCountedStep = int64_t(1) << 62;
 
 // The part of the run table one launch covers: runs [run_begin, run_limit)
 // and tiles from tile0 on.  Elements outside those runs are left alone.
@@ -65,6 +128,7 @@ enum StepMode : int {
     kFromMain = 1,    // read main_grad_in times the clipping coefficient, Adam
     kWriteGrads = 2,  // reduce the replicas, write the reduced grads back into
                       // every replica (all-reduce), Adam
+    kCounted = 3,     // as kPlain, with the scalars from a CounterBlock
 };
 
 struct StepArgs {
@@ -76,6 +140,7 @@ struct StepArgs {
     float *main_grad_out;
     const float *main_grad_in;  // kFromMain: the reduced grads
     const float *clip_coef;     // kFromMain: device scalar
+    const CounterBlock *counter;  // kCounted: status and scalars of the step
     RunView rv;
     int32_t D;
     int32_t R;  // ranks per instance (D with one instance)
@@ -389,7 +454,8 @@ __device__ __forceinline__ void write_grads_vec(const void *const *grads, int D_
 
 // A vector of 8 owned elements of one run.
 template <typename G, int DC, int MODE>
-__device__ __forceinline__ void full_vector(const StepArgs &a, int64_t e0, int32_t meta) {
+__device__ __forceinline__ void full_vector(const StepArgs &a, const Scalars &sc, int64_t e0,
+                                            int32_t meta) {
     float acc[8];
     if constexpr (MODE == kFromMain) {
         const float coef = *a.clip_coef;
@@ -398,7 +464,7 @@ __device__ __forceinline__ void full_vector(const StepArgs &a, int64_t e0, int32
 #pragma unroll
         for (int k = 0; k < 8; ++k) acc[k] = __fmul_rn(f[k], coef);
     } else {
-        reduce_vec<G, DC>(a, a.sc.scale, e0, acc);
+        reduce_vec<G, DC>(a, sc.scale, e0, acc);
         if (a.round_grad) to_grad_type8<G>(acc);
     }
     if constexpr (MODE == kWriteGrads) write_grads_vec<G, DC>(a.grads, a.D, e0, acc);
@@ -409,9 +475,9 @@ __device__ __forceinline__ void full_vector(const StepArgs &a, int64_t e0, int32
     float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
     float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
     float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    const float decay = (meta & kRunDecays) ? a.sc.decay : 1.0f;
+    const float decay = (meta & kRunDecays) ? sc.decay : 1.0f;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) adamw(a.sc, decay, acc[k], w[k], m[k], v[k]);
+    for (int k = 0; k < 8; ++k) adamw(sc, decay, acc[k], w[k], m[k], v[k]);
 
     st_stream_f4(a.master + e0, make_float4(w[0], w[1], w[2], w[3]));
     st_stream_f4(a.master + e0 + 4, make_float4(w[4], w[5], w[6], w[7]));
@@ -443,7 +509,7 @@ __device__ __forceinline__ void full_vector(const StepArgs &a, int64_t e0, int32
 
 // A vector that straddles a run edge: element by element, owned ones only.
 template <typename G, int DC, int MODE>
-__device__ __noinline__ void mixed_vector(const StepArgs &a, int64_t e0, int j) {
+__device__ __noinline__ void mixed_vector(const StepArgs &a, const Scalars &sc, int64_t e0, int j) {
     const int D = DC > 0 ? DC : a.D;
     bool done = false;
     for (int k = 0; k < kVec && !done; ++k) {
@@ -454,13 +520,13 @@ __device__ __noinline__ void mixed_vector(const StepArgs &a, int64_t e0, int j) 
         if constexpr (MODE == kFromMain) {
             g = __fmul_rn(a.main_grad_in[e], *a.clip_coef);
         } else {
-            g = reduce_scalar<G>(a.grads, D, a.R, a.sc.scale, e);
+            g = reduce_scalar<G>(a.grads, D, a.R, sc.scale, e);
             if (a.round_grad) g = to_grad_type<G>(g);
         }
         if constexpr (MODE == kWriteGrads)
             for (int r = 0; r < D; ++r) store_grad_scalar<G>(a.grads[r], e, g);
         float w = a.master[e], m = a.exp_avg[e], v = a.exp_avg_sq[e];
-        adamw(a.sc, (meta & kRunDecays) ? a.sc.decay : 1.0f, g, w, m, v);
+        adamw(sc, (meta & kRunDecays) ? sc.decay : 1.0f, g, w, m, v);
         a.master[e] = w;
         a.exp_avg[e] = m;
         a.exp_avg_sq[e] = v;
@@ -477,14 +543,63 @@ __device__ __noinline__ void mixed_vector(const StepArgs &a, int64_t e0, int j) 
 
 template <typename G, int DC, int MODE>
 __global__ void __launch_bounds__(kThreads) dopt_step_kernel(const __grid_constant__ StepArgs a) {
-    const int64_t tile = a.rv.tile0 + blockIdx.x;
-    const int64_t e0 = tile * kDoptTileElems + int64_t(threadIdx.x) * kVec;
     int j;
-    const VecKind kind = locate(a.rv, tile, e0, j);
-    if (kind == kFull)
-        full_vector<G, DC, MODE>(a, e0, a.rv.run_meta[j]);
-    else if (kind == kMixed)
-        mixed_vector<G, DC, MODE>(a, e0, j);
+    if constexpr (MODE == kCounted) {
+        // One read of the counter per CTA (every CTA of the grid needs the
+        // same line), issued before the run lookup so that the waits
+        // overlap.  (A persistent grid that reads it once per CTA of a few
+        // per SM was 15 % slower: one tile per CTA lets the SMs overlap the
+        // tiles' latencies.)
+        __shared__ Scalars s_sc;
+        __shared__ int32_t s_status;
+        if (threadIdx.x == 0) {
+            s_status = a.counter->status;
+            s_sc = a.counter->sc;
+        }
+        const int64_t tile = a.rv.tile0 + blockIdx.x;
+        const int64_t e0 = tile * kDoptTileElems + int64_t(threadIdx.x) * kVec;
+        const VecKind kind = locate(a.rv, tile, e0, j);
+        __syncthreads();
+        if (s_status != 0) return;  // the counter launch found a bad step number
+        const Scalars sc = s_sc;
+        if (kind == kFull)
+            full_vector<G, DC, MODE>(a, sc, e0, a.rv.run_meta[j]);
+        else if (kind == kMixed)
+            mixed_vector<G, DC, MODE>(a, sc, e0, j);
+    } else {
+        // one tile per CTA
+        const int64_t tile = a.rv.tile0 + blockIdx.x;
+        const int64_t e0 = tile * kDoptTileElems + int64_t(threadIdx.x) * kVec;
+        const VecKind kind = locate(a.rv, tile, e0, j);
+        if (kind == kFull)
+            full_vector<G, DC, MODE>(a, a.sc, e0, a.rv.run_meta[j]);
+        else if (kind == kMixed)
+            mixed_vector<G, DC, MODE>(a, a.sc, e0, j);
+    }
+}
+
+// First launch of dopt_step_counted, one warp: the step number from the
+// counter, its scalars (lanes 0 and 1 evaluate the two slow double-precision
+// ones side by side), the counter advanced, or the bad number reported.
+__global__ void dopt_count_step_kernel(CounterBlock *c, const dopt_adam_cfg cfg) {
+    const int64_t t = c->next_step;
+    const int lane = threadIdx.x;
+    const bool bad = t < 1 || t > kMaxCountedStep;
+    float x = 0.0f;
+    if (!bad && lane == 0) x = step_size_for(cfg, t);
+    if (!bad && lane == 1) x = bc2_sqrt_for(cfg, t);
+    const float bc2_sqrt = __shfl_sync(0x3u, x, 1);
+    if (lane != 0) return;
+    if (bad) {
+        c->status = DOPT_COUNTER_BAD_STEP;
+        return;
+    }
+    Scalars s = scalars_for_fixed(cfg);
+    s.step_size = x;
+    s.bc2_sqrt = bc2_sqrt;
+    c->sc = s;
+    c->status = 0;
+    c->next_step = t + 1;
 }
 
 // ---------------------------------------------------------------------------

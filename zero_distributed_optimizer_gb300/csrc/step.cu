@@ -29,21 +29,6 @@ struct NvtxRange {
 // Host side
 // ---------------------------------------------------------------------------
 
-Scalars make_scalars(const dopt_adam_cfg &c, int64_t t) {
-    const double lr = c.lr, b1 = c.beta1, b2 = c.beta2, wd = c.weight_decay;
-    Scalars s;
-    s.b1 = c.beta1;
-    s.b2 = c.beta2;
-    s.omb1 = float(1.0 - b1);
-    s.omb2 = float(1.0 - b2);
-    s.decay = float(1.0 - lr * wd);
-    s.step_size = float(lr / (1.0 - std::pow(b1, double(t))));
-    s.bc2_sqrt = float(std::sqrt(1.0 - std::pow(b2, double(t))));
-    s.eps = c.eps;
-    s.scale = c.grad_scale;
-    return s;
-}
-
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // The run view of buckets [first, first + count) and the number of tiles a
@@ -124,9 +109,9 @@ AllReduceKernel pick_allreduce_kernel(int D) {
     }
 }
 
-// SMs and resident CTAs per SM of a norm kernel on a device, asked once.
+// SMs and resident CTAs per SM of a kernel on a device, asked once.
 struct GridInfo {
-    NormKernel kernel;
+    const void *kernel;
     int device;
     int sms;
     int per_sm;
@@ -134,7 +119,7 @@ struct GridInfo {
 std::mutex g_grid_mutex;
 std::vector<GridInfo> g_grid_info;
 
-void sm_occupancy(NormKernel k, int device, int *sms, int *per_sm) {
+void sm_occupancy(const void *k, int device, int *sms, int *per_sm) {
     std::lock_guard<std::mutex> lock(g_grid_mutex);
     for (const GridInfo &g : g_grid_info)
         if (g.kernel == k && g.device == device) {
@@ -155,7 +140,7 @@ void sm_occupancy(NormKernel k, int device, int *sms, int *per_sm) {
 // Grid of the persistent norm pass: every SM full, at most kMaxClipCtas.
 int norm_grid(NormKernel k, int64_t n_tiles, int device) {
     int sms = 0, per_sm = 0;
-    sm_occupancy(k, device, &sms, &per_sm);
+    sm_occupancy(reinterpret_cast<const void *>(k), device, &sms, &per_sm);
     // a whole number of CTAs per SM, so that every SM gets the same share
     const int per_sm_cap = std::max(1, kMaxClipCtas / std::max(sms, 1));
     int64_t g = int64_t(std::max(sms, 1)) * std::min(std::max(per_sm, 1), per_sm_cap);
@@ -257,12 +242,30 @@ void fill_step_args(StepArgs &a, const dopt_layout *L, const dopt_adam_cfg *cfg,
     a.R = L->R;
     a.gather = (flags & DOPT_STEP_GATHER) ? 1 : 0;
     a.round_grad = (flags & DOPT_STEP_ROUND_GRAD) ? 1 : 0;
-    a.sc = make_scalars(*cfg, step);
+    a.sc = scalars_for(*cfg, step);
 }
 
 int launch_error(const char *who, const char *what) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return dopt::fail(DOPT_E_CUDA, "%s: %s launch: %s", who, what, cudaGetErrorString(e));
+    return DOPT_OK;
+}
+
+// The arguments of one step launch over buckets [first, first+count);
+// *tiles = 0 when nothing there is owned (then nothing else is checked).
+int prepare_step(const char *who, const dopt_layout *L, const dopt_adam_cfg *cfg, int64_t step,
+                 int32_t first, int32_t count, const void *const *grad_replicas,
+                 float *master, float *exp_avg, float *exp_avg_sq, void *const *param_replicas,
+                 uint32_t flags, float *main_grad_out, StepArgs &a, int64_t *tiles) {
+    a.rv = make_view(L, first, count, tiles);
+    if (*tiles == 0) return DOPT_OK;
+    int rc = check_device_tables(L, who);
+    if (rc != DOPT_OK) return rc;
+    const void *grads[DOPT_MAX_D];
+    rc = resolve_grads(who, L->cfg.D, grad_replicas, flags, grads);
+    if (rc != DOPT_OK) return rc;
+    fill_step_args(a, L, cfg, step, grads, master, exp_avg, exp_avg_sq, param_replicas, flags);
+    a.main_grad_out = main_grad_out;
     return DOPT_OK;
 }
 
@@ -275,15 +278,9 @@ int launch_step(const char *who, const dopt_layout *L, const dopt_adam_cfg *cfg,
                 cudaStream_t stream) {
     int64_t tiles = 0;
     StepArgs a{};
-    a.rv = make_view(L, first, count, &tiles);
-    if (tiles == 0) return DOPT_OK;
-    int rc = check_device_tables(L, who);
-    if (rc != DOPT_OK) return rc;
-    const void *grads[DOPT_MAX_D];
-    rc = resolve_grads(who, L->cfg.D, grad_replicas, flags, grads);
-    if (rc != DOPT_OK) return rc;
-    fill_step_args(a, L, cfg, step, grads, master, exp_avg, exp_avg_sq, param_replicas, flags);
-    a.main_grad_out = main_grad_out;
+    int rc = prepare_step(who, L, cfg, step, first, count, grad_replicas, master, exp_avg,
+                          exp_avg_sq, param_replicas, flags, main_grad_out, a, &tiles);
+    if (rc != DOPT_OK || tiles == 0) return rc;
     StepKernel k = step_kernel_for<MODE>(grad_dtype, kernel_D(L));
     k<<<unsigned(tiles), kThreads, 0, stream>>>(a);
     return launch_error(who, "step");
@@ -384,6 +381,37 @@ extern "C" int dopt_step_buckets(const dopt_layout *L, const dopt_adam_cfg *cfg,
     return launch_step<kPlain>(who, L, cfg, step, first_bucket, n_buckets, grad_replicas,
                                grad_dtype, master, exp_avg, exp_avg_sq, param_replicas, flags,
                                main_grad_out, stream);
+}
+
+extern "C" int dopt_step_counted(const dopt_layout *L, const dopt_adam_cfg *cfg,
+                                 dopt_step_counter *counter, const void *const *grad_replicas,
+                                 dopt_dtype grad_dtype, float *master, float *exp_avg,
+                                 float *exp_avg_sq, void *const *param_replicas, uint32_t flags,
+                                 float *main_grad_out, cudaStream_t stream) {
+    using dopt::fail;
+    dopt::clear_error();
+    const char *who = "dopt_step_counted";
+    NvtxRange range(who);
+    int rc = check_step_args(who, L, cfg, 1, grad_replicas, grad_dtype, master, exp_avg,
+                             exp_avg_sq, param_replicas, flags, main_grad_out);
+    if (rc != DOPT_OK) return rc;
+    if (!counter) return fail(DOPT_E_ARG, "%s: counter is NULL", who);
+    if (!aligned16(counter)) return fail(DOPT_E_ALIGN, "%s: counter is not 16-byte aligned", who);
+    // every check before the first launch: the counter advances only
+    // together with the step it counts
+    int64_t tiles = 0;
+    StepArgs a{};
+    rc = prepare_step(who, L, cfg, 1, 0, int32_t(L->buckets.size()), grad_replicas, master,
+                      exp_avg, exp_avg_sq, param_replicas, flags, main_grad_out, a, &tiles);
+    if (rc != DOPT_OK) return rc;
+    CounterBlock *c = reinterpret_cast<CounterBlock *>(counter);
+    dopt_count_step_kernel<<<1, 2, 0, stream>>>(c, *cfg);
+    rc = launch_error(who, "counter");
+    if (rc != DOPT_OK || tiles == 0) return rc;
+    a.counter = c;
+    StepKernel k = step_kernel_for<kCounted>(grad_dtype, kernel_D(L));
+    k<<<unsigned(tiles), kThreads, 0, stream>>>(a);
+    return launch_error(who, "step");
 }
 
 extern "C" int dopt_step_allreduce(const dopt_layout *L, const dopt_adam_cfg *cfg, int64_t step,
