@@ -119,6 +119,12 @@ def _declare(lib) -> None:
                                      ctypes.POINTER(ctypes.c_void_p), ctypes.c_int64,
                                      ctypes.c_int64, ctypes.c_int32,
                                      ctypes.POINTER(ctypes.c_double)]
+    lib.orc_count_nonfinite.restype = ctypes.c_int
+    lib.orc_count_nonfinite.argtypes = [i64p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                        ctypes.c_int64, ctypes.c_int32, ctypes.c_float,
+                                        ctypes.c_int32, ctypes.POINTER(ctypes.c_void_p),
+                                        ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
+                                        ctypes.POINTER(ctypes.c_int64)]
     lib.orc_allreduce.restype = ctypes.c_int
     lib.orc_allreduce.argtypes = [i64p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                   ctypes.c_int64,
@@ -310,6 +316,28 @@ def grad_norm_sq(sizes, D: int, bucket_elems: int, pad_unit: int, grad_scale: fl
     if rc != ORC_OK:
         raise OracleError(f"orc_grad_norm_sq failed: {rc}")
     return float(out.value)
+
+
+def count_nonfinite(sizes, D: int, bucket_elems: int, pad_unit: int, grad_scale: float, grads,
+                    window=None, instances: int = 1, round_grad: bool = False, lib=None) -> int:
+    """Owned elements of the window whose reduced grad is Inf or NaN (the
+    non-finite check, reading R13 of the C file; the tutorial's §8.2 notes
+    that FP16 overflows easily)."""
+    lib = lib or load()
+    sizes_a, sizes_p = _i64(sizes)
+    grad_is_f32 = grads[0].dtype == np.float32
+    span = len(grads[0])
+    w0, w1 = (0, span) if window is None else (int(window[0]), int(window[1]))
+    if w1 - w0 != span or len(grads) != D:
+        raise OracleError("grads must be D arrays of the window length")
+    gp = (ctypes.c_void_p * D)(*[g.ctypes.data for g in grads])
+    out = ctypes.c_int64(0)
+    rc = lib.orc_count_nonfinite(sizes_p, len(sizes_a), D, int(instances), bucket_elems,
+                                 pad_unit, float(grad_scale), int(grad_is_f32), gp, w0, w1,
+                                 int(bool(round_grad)), ctypes.byref(out))
+    if rc != ORC_OK:
+        raise OracleError(f"orc_count_nonfinite failed: {rc}")
+    return int(out.value)
 
 
 def allreduce(sizes, D: int, bucket_elems: int, pad_unit: int, grad_scale: float, grads,

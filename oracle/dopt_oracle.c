@@ -82,6 +82,15 @@
  *      main grads), so with that option the reduced grad is rounded to the
  *      grad type (bf16: R7) before clipping and Adam, and the norm is taken
  *      over the rounded grads.
+ *  R13 Non-finite check (off by default).  [P2] §8.2 notes that FP16
+ *      overflows easily; the pages give no rule for it, so the plain one is
+ *      taken: an owned element is non-finite when its reduced grad (after
+ *      the rounding of R12, when on) is Inf or NaN, counted once however
+ *      many replicas contributed; padding is never counted; with the check
+ *      on, a step with a non-zero count changes no state and no param (the
+ *      caller simply does not step).  Scaling comes first (R5), so finite
+ *      replicas whose unscaled sum would overflow are not counted when the
+ *      scaled sum is finite.
  *  R10 force_all_reduce ([P1] §5) leaves the optimizer step unchanged (each
  *      rank still updates its own shard from the same reduced grads) and
  *      additionally gives every replica's grad buffer the whole reduced grad,
@@ -528,6 +537,72 @@ int orc_step(const int64_t *sizes, int32_t n, const uint8_t *wd_mask, int32_t D,
 
 done:
     free(shard);
+    free(pieces);
+    free(pstart);
+    free(pend);
+    free(pbucket);
+    free(bstart);
+    free(bend);
+    return rc;
+}
+
+/*
+ * Number of owned elements of the window [w0, w1) whose reduced grad is Inf
+ * or NaN (R13), after the optional rounding to the grad type (R12).  Grad
+ * arrays are window-relative.
+ */
+int orc_count_nonfinite(const int64_t *sizes, int32_t n, int32_t D, int32_t instances,
+                        int64_t bucket_elems, int32_t pad_unit, float grad_scale,
+                        int32_t grad_is_f32, const void *const *grads, int64_t w0, int64_t w1,
+                        int32_t round_grad, int64_t *out)
+{
+    if (w0 < 0 || w1 < w0 || !out || instances < 1 || D % instances != 0)
+        return ORC_E_ARG;
+    int32_t R = D / instances;
+    int rc = ORC_OK;
+    size_t cap = (size_t)(n > 0 ? n : 1);
+    int64_t *pstart = (int64_t *)malloc(cap * sizeof *pstart);
+    int64_t *pend = (int64_t *)malloc(cap * sizeof *pend);
+    int32_t *pbucket = (int32_t *)malloc(cap * sizeof *pbucket);
+    int64_t *bstart = (int64_t *)malloc(cap * sizeof *bstart);
+    int64_t *bend = (int64_t *)malloc(cap * sizeof *bend);
+    orc_piece *pieces = NULL;
+    int32_t nb = 0, npieces = 0;
+    int64_t numel = 0;
+    int64_t count = 0;
+    if (!pstart || !pend || !pbucket || !bstart || !bend) {
+        rc = ORC_E_NOMEM;
+        goto done;
+    }
+    rc = orc_layout(sizes, n, R, bucket_elems, pad_unit, pstart, pend, pbucket, bstart, bend,
+                    &nb, &numel);
+    if (rc != ORC_OK)
+        goto done;
+    if (w1 > numel) {
+        rc = ORC_E_ARG;
+        goto done;
+    }
+    pieces = (orc_piece *)malloc(((size_t)n + (size_t)R * (size_t)nb + 1) * sizeof *pieces);
+    if (!pieces) {
+        rc = ORC_E_NOMEM;
+        goto done;
+    }
+    rc = orc_pieces(n, pstart, pend, pbucket, nb, bstart, bend, R, pieces, &npieces);
+    if (rc != ORC_OK)
+        goto done;
+    for (int32_t pi = 0; pi < npieces; ++pi) {
+        int64_t i_lo = orc_max(pieces[pi].gbuf_world.start, w0);
+        int64_t i_hi = orc_min(pieces[pi].gbuf_world.end, w1);
+        for (int64_t i = i_lo; i < i_hi; ++i) {
+            float r = orc_reduce_element(grads, grad_is_f32, D, instances, grad_scale, i - w0);
+            if (round_grad)
+                r = orc_round_to_grad_type(r, grad_is_f32);
+            if (isinf(r) || isnan(r))
+                ++count;
+        }
+    }
+    *out = count;
+done:
     free(pieces);
     free(pstart);
     free(pend);

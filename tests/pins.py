@@ -865,6 +865,74 @@ def pin_round_grad(lib):
     assert a == b
 
 
+def pin_nonfinite_count(lib):
+    """Reading R13 of the oracle: the count is over owned elements of the
+    reduced grad.  Closed cases: one Inf counts 1; +Inf and -Inf in two
+    replicas (a NaN sum) count 1, not 2; NaN at padding counts 0; scaling
+    comes first (page 1 §5), so 1.5*2^127 in two replicas counts 0 with a
+    factor of 1/2 and 1 with a factor of 1; a reduced grad that is finite in
+    fp32 but rounds to bf16 Inf (max bf16 + 2^119, a tie rounded to even)
+    counts only with the rounding of R12; across two instances the
+    instance sums Inf and -Inf give a NaN that counts 1.  Random layouts:
+    the count equals the number of non-finite owned main grads a step
+    reports."""
+    sizes, D = [5, 6], 4  # 11 owned elements, padded to 12
+    N = oracle.range_map(sizes, D, 0, 1, lib=lib).numel
+    assert N == 12
+
+    def f32(entries):
+        g = [np.zeros(N, np.float32) for _ in range(D)]
+        for r, i, x in entries:
+            g[r][i] = x
+        return g
+
+    def count(g, scale=1.0, **kw):
+        return oracle.count_nonfinite(sizes, D, 0, 1, scale, g, lib=lib, **kw)
+
+    inf, nan = np.float32(np.inf), np.float32(np.nan)
+    assert count(f32([])) == 0
+    assert count(f32([(1, 3, inf)])) == 1
+    assert count(f32([(0, 7, inf), (2, 7, -inf)])) == 1
+    assert count(f32([(3, 11, nan)])) == 0
+    assert count(f32([(3, 11, nan), (1, 10, nan), (0, 0, -inf)])) == 2
+    big = np.float32(1.5 * 2.0 ** 127)
+    assert count(f32([(0, 4, big), (1, 4, big)]), scale=0.5) == 0
+    assert count(f32([(0, 4, big), (1, 4, big)]), scale=1.0) == 1
+    # bf16 grads: max bf16 (0x7F7F) + 2^119 (0x7B00) is finite in fp32 and
+    # a tie between max bf16 and Inf in bf16, which goes to the even Inf
+    g = [np.zeros(N, np.uint16) for _ in range(D)]
+    g[0][2], g[1][2] = 0x7F7F, 0x7B00
+    assert count(g) == 0
+    assert count(g, round_grad=True) == 1
+    # two instances of two ranks: Inf + 0 | -Inf + 0 -> NaN
+    gi = f32([(0, 5, inf), (3, 5, -inf)])
+    assert oracle.count_nonfinite(sizes, D, 0, 1, 1.0, gi, instances=2, lib=lib) == 1
+    # random layouts with scattered Inf/NaN, against the step's main grads
+    rng = np.random.default_rng(17)
+    for _ in range(20):
+        n = int(rng.integers(1, 6))
+        sz = [int(x) for x in rng.integers(0, 40, n)]
+        Dr = int(rng.integers(1, 6))
+        pad = int(rng.integers(1, 5))
+        Nr = oracle.range_map(sz, Dr, 0, pad, lib=lib).numel
+        if Nr == 0:
+            continue
+        gr = [rng.normal(0, 1, Nr).astype(np.float32) for _ in range(Dr)]
+        for _ in range(int(rng.integers(0, 6))):
+            gr[int(rng.integers(0, Dr))][int(rng.integers(0, Nr))] = rng.choice([inf, -inf, nan])
+        master, m, v = _state(Nr, 3)
+        params = _params_from(master, Dr)
+        mg = np.zeros(Nr, np.float32)
+        oracle.step(sz, None, Dr, 0, pad, oracle.make_adam(grad_scale=0.5), 1, gr, master, m, v,
+                    params, main_grad_out=mg, lib=lib)
+        L = oracle.range_map(sz, Dr, 0, pad, lib=lib)
+        owned = np.zeros(Nr, bool)
+        for p in range(n):
+            owned[L.param_start[p]:L.param_end[p]] = True
+        want = int(np.count_nonzero(~np.isfinite(mg[owned])))
+        assert oracle.count_nonfinite(sz, Dr, 0, pad, 0.5, gr, lib=lib) == want
+
+
 ALL_PINS = [
     pin_page1_ownership,
     pin_brute_force_range_maps,
@@ -889,4 +957,5 @@ ALL_PINS = [
     pin_instances_factorizations,
     pin_instances_write_back_and_gather,
     pin_round_grad,
+    pin_nonfinite_count,
 ]

@@ -75,6 +75,21 @@ MUTANTS = [
     ("bf16_truncates", "if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u)))", "if (0)"),
     ("bf16_ties_away", "if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u)))",
      "if (lower >= 0x8000u)"),
+    ("nonfinite_misses_nan", "if (isinf(r) || isnan(r))\n                ++count;",
+     "if (isinf(r))\n                ++count;"),
+    ("nonfinite_ignores_rounding",
+     "r = orc_round_to_grad_type(r, grad_is_f32);\n            if (isinf(r) || isnan(r))",
+     "(void)0;\n            if (isinf(r) || isnan(r))"),
+    ("nonfinite_counts_replicas", "if (isinf(r) || isnan(r))\n                ++count;",
+     "for (int32_t q = 0; q < D; ++q) {\n                float x = orc_grad(grads, grad_is_f32, q, i - w0);\n"
+     "                if (isinf(x) || isnan(x))\n                    ++count;\n            }"),
+    ("nonfinite_counts_past_piece_end",
+     "int64_t i_hi = orc_min(pieces[pi].gbuf_world.end, w1);\n        for (int64_t i = i_lo; i < i_hi; ++i) {\n"
+     "            float r = orc_reduce_element(grads, grad_is_f32, D, instances, grad_scale, i - w0);\n"
+     "            if (round_grad)\n                r = orc_round_to_grad_type(r, grad_is_f32);\n            if (isinf",
+     "int64_t i_hi = orc_min(pieces[pi].gbuf_world.end + 1, w1);\n        for (int64_t i = i_lo; i < i_hi; ++i) {\n"
+     "            float r = orc_reduce_element(grads, grad_is_f32, D, instances, grad_scale, i - w0);\n"
+     "            if (round_grad)\n                r = orc_round_to_grad_type(r, grad_is_f32);\n            if (isinf"),
 ]
 
 RUNNER = r"""
