@@ -62,8 +62,9 @@ MUTANTS = [
      "float reduced = shard[pc->gbuf_world_in_bucket.start + t];"),
     ("round_grad_ignored", "if (round_grad)\n                        g = orc_round_to_grad_type(g, grad_is_f32);",
      "if (0)\n                        g = orc_round_to_grad_type(g, grad_is_f32);"),
-    ("round_grad_norm_unrounded", "if (round_grad)\n                r = orc_round_to_grad_type(r, grad_is_f32);",
-     "if (0)\n                r = orc_round_to_grad_type(r, grad_is_f32);"),
+    ("round_grad_norm_unrounded",
+     "if (round_grad)\n                r = orc_round_to_grad_type(r, grad_is_f32);\n            double g",
+     "if (0)\n                r = orc_round_to_grad_type(r, grad_is_f32);\n            double g"),
     ("round_grad_truncates", "return grad_is_f32 ? g : orc_bf16_to_f32(orc_f32_to_bf16(g));",
      "return grad_is_f32 ? g : orc_bits_to_f32(orc_f32_to_bits(g) & 0xffff0000u);"),
     ("clip_not_applied", "float gc = g * clip_coef;", "float gc = g;"),
