@@ -344,6 +344,30 @@ int dopt_gather(const dopt_layout *layout, void *const *param_replicas, cudaStre
 #define DOPT_CLIP_WORKSPACE_BYTES 16384
 
 /*
+ * dopt_step_clipped flag: skip the update when any owned element's reduced
+ * grad (after DOPT_STEP_ROUND_GRAD's rounding, when set) is Inf or NaN.
+ * The first launch counts such elements; when the count is not 0 the
+ * second launch stores nothing (master, exp_avg, exp_avg_sq and every param
+ * replica keep their values), the coefficient is reported as NaN, and the
+ * count is reported in the dopt_clip_report.  The pages give no rule for
+ * non-finite grads (the tutorial's §8.2 only notes that FP16 overflows
+ * easily); this is the usual mixed-precision practice of dropping a step
+ * whose grads overflowed.  Refused (DOPT_E_ARG) by every other entry point.
+ */
+#define DOPT_STEP_SKIP_NONFINITE 8u
+
+/*
+ * What dopt_step_clipped reports through norm_out.  Without
+ * DOPT_STEP_SKIP_NONFINITE only norm and coef are written (norm_out may
+ * then point to just 2 floats); with it, the whole 16-byte report.
+ */
+typedef struct {
+    float norm;         /* global norm of the reduced grads */
+    float coef;         /* clipping coefficient; NaN when the step was skipped */
+    uint64_t nonfinite; /* owned elements whose reduced grad is Inf or NaN */
+} dopt_clip_report;
+
+/*
  * The step with global grad-norm clipping (distributed-training tutorial,
  * §8.3: the norm sqrt(sum ||g||^2) over every rank's shard is needed before
  * the optimizer update).  Two launches on `stream`:
@@ -363,7 +387,11 @@ int dopt_gather(const dopt_layout *layout, void *const *param_replicas, cudaStre
  *   workspace   device, DOPT_CLIP_WORKSPACE_BYTES, 16-byte aligned, owned by
  *               the caller; holds per-CTA partial sums between the launches;
  *               calls that share a workspace must not overlap on the GPU
- *   norm_out    nullable device float[2]: [0] = global norm, [1] = c
+ *   norm_out    nullable device pointer, 8-byte aligned, to a
+ *               dopt_clip_report: norm and c (and, with
+ *               DOPT_STEP_SKIP_NONFINITE, the count of non-finite reduced
+ *               grads)
+ *   flags       as in dopt_step, plus DOPT_STEP_SKIP_NONFINITE
  *   other arguments as in dopt_step.
  *
  * The norm's fp32 squares and pairwise sums differ from an exact sum by at
@@ -415,7 +443,7 @@ int dopt_step_clipped(const dopt_layout *layout, const dopt_adam_cfg *cfg, int64
  * more than DOPT_NOALLOC_SCRATCH_BYTES is refused with DOPT_E_ARG.
  *
  * Arguments, results and errors otherwise as dopt_step_clipped (without
- * `workspace`).
+ * `workspace`, and without DOPT_STEP_SKIP_NONFINITE, which it refuses).
  */
 int dopt_step_clipped_noalloc(const dopt_layout *layout, const dopt_adam_cfg *cfg, int64_t step,
                               float max_norm, const void *const *grad_replicas,

@@ -260,3 +260,24 @@ def test_counted_step_argument_checks_before_cuda(lib):
     assert call(flags=8) == B.DOPT_E_ARG
     assert call() in (B.DOPT_E_STATE, B.DOPT_E_CUDA)  # nothing was launched
     assert ctypes.sizeof(ctypes.c_int64) * 8 == B.DOPT_STEP_COUNTER_BYTES
+
+
+def test_skip_nonfinite_only_on_the_clipped_step(lib):
+    L = _lib_layout([100, 30], 2, 0, 8)
+    cfg = B.AdamConfig().to_c()
+    gp = (ctypes.c_void_p * 2)(0x10000, 0x20000)
+    skip = B.DOPT_STEP_GATHER | B.DOPT_STEP_SKIP_NONFINITE
+    st = (0x30000, 0x40000, 0x50000)
+    assert B.lib().dopt_step(L.handle, ctypes.byref(cfg), 1, gp, 0, *st, gp, skip, None,
+                             None) == B.DOPT_E_ARG
+    assert B.lib().dopt_step_buckets(L.handle, ctypes.byref(cfg), 1, 0, 1, gp, 0, *st, gp, skip,
+                                     None, None) == B.DOPT_E_ARG
+    assert B.lib().dopt_step_allreduce(L.handle, ctypes.byref(cfg), 1, gp, 0, *st, gp, skip,
+                                       None, None) == B.DOPT_E_ARG
+    assert B.lib().dopt_step_counted(L.handle, ctypes.byref(cfg), 0x90000, gp, 0, *st, gp, skip,
+                                     None, None) == B.DOPT_E_ARG
+    assert B.lib().dopt_step_clipped_noalloc(L.handle, ctypes.byref(cfg), 1, 1.0, gp, 0, *st, gp,
+                                             skip, 0x70000, None, None) == B.DOPT_E_ARG
+    assert B.lib().dopt_step_clipped(L.handle, ctypes.byref(cfg), 1, 1.0, gp, 0, *st, gp, skip,
+                                     0x70000, 0x80000, None, None) in (B.DOPT_E_STATE,
+                                                                       B.DOPT_E_CUDA)

@@ -31,6 +31,7 @@ DOPT_FP32 = 1
 DOPT_STEP_GATHER = 1
 DOPT_STEP_HOST_GRADS = 2
 DOPT_STEP_ROUND_GRAD = 4
+DOPT_STEP_SKIP_NONFINITE = 8
 DOPT_CLIP_WORKSPACE_BYTES = 16384
 DOPT_STEP_COUNTER_BYTES = 64  # sizeof(dopt_step_counter)
 DOPT_COUNTER_BAD_STEP = 1
@@ -544,15 +545,35 @@ def clip_workspace(device=None):
                        device=device if device is not None else "cuda")
 
 
+def clip_report(device=None):
+    """A device buffer for the dopt_clip_report of dopt_step_clipped (16
+    bytes: norm, coefficient, count of non-finite reduced grads)."""
+    import torch
+
+    return torch.zeros(4, dtype=torch.float32, device=device if device is not None else "cuda")
+
+
+def read_clip_report(report):
+    """(norm, coef, nonfinite) of a :func:`clip_report` buffer
+    (synchronises with the device)."""
+    import torch
+
+    h = report.cpu()
+    return float(h[0]), float(h[1]), int(h[2:4].view(torch.int64)[0])
+
+
 def dopt_step_clipped(layout: Layout, adam: AdamConfig, step: int, max_norm: float,
                       grad_replicas, master, exp_avg, exp_avg_sq, param_replicas, main_grad,
                       workspace, gather: bool = True, norm_out=None, stream=None,
-                      round_grad: bool = False) -> None:
+                      round_grad: bool = False, skip_nonfinite: bool = False) -> None:
     """The step with global grad-norm clipping (two launches).
 
     main_grad: fp32 CUDA tensor of >= padded_numel elements (receives the
     reduced grads before clipping); workspace: from :func:`clip_workspace`;
-    norm_out: optional fp32 CUDA tensor of 2 elements (norm, coefficient).
+    norm_out: optional fp32 CUDA tensor of 2 elements (norm, coefficient),
+    or a :func:`clip_report` (required size with skip_nonfinite).
+    skip_nonfinite: store nothing when any reduced grad is Inf or NaN (the
+    report then holds the count and a NaN coefficient).
     """
     import torch
 
@@ -575,7 +596,7 @@ def dopt_step_clipped(layout: Layout, adam: AdamConfig, step: int, max_norm: flo
         _check_tensor(p, f"param_replicas[{i}]", torch.bfloat16, N, device)
     _check_tensor(workspace, "workspace", torch.uint8, DOPT_CLIP_WORKSPACE_BYTES, device)
     if norm_out is not None:
-        _check_tensor(norm_out, "norm_out", torch.float32, 2, device)
+        _check_tensor(norm_out, "norm_out", torch.float32, 4 if skip_nonfinite else 2, device)
     gp = (ctypes.c_void_p * D)(*[g.data_ptr() for g in grad_replicas])
     pp = (ctypes.c_void_p * D)(*[p.data_ptr() for p in param_replicas])
     cfg = adam.to_c()
@@ -583,7 +604,9 @@ def dopt_step_clipped(layout: Layout, adam: AdamConfig, step: int, max_norm: flo
         _check(lib().dopt_step_clipped(
             layout.handle, ctypes.byref(cfg), int(step), float(max_norm), gp,
             DOPT_BF16 if gdt == torch.bfloat16 else DOPT_FP32, master.data_ptr(),
-            exp_avg.data_ptr(), exp_avg_sq.data_ptr(), pp, _flags(gather, round_grad=round_grad),
+            exp_avg.data_ptr(), exp_avg_sq.data_ptr(), pp,
+            _flags(gather, round_grad=round_grad)
+            | (DOPT_STEP_SKIP_NONFINITE if skip_nonfinite else 0),
             main_grad.data_ptr(), workspace.data_ptr(),
             None if norm_out is None else norm_out.data_ptr(), _stream_handle(stream)))
 

@@ -29,6 +29,7 @@
 // and add are fused and divide and square root are IEEE; the rank order of
 // the reduction is the loop order.
 #include <cmath>
+#include <cstddef>
 #include <cstdint>
 
 #include <cuda_bf16.h>
@@ -146,19 +147,25 @@ struct StepArgs {
     int32_t R;  // ranks per instance (D with one instance)
     int32_t gather;
     int32_t round_grad;  // round the reduced grad to the grad type first
+    int32_t skip_nonfinite;  // kFromMain: a NaN coefficient means store nothing
     Scalars sc;
 };
 
 // Workspace of the clipped step (device memory, DOPT_CLIP_WORKSPACE_BYTES).
 struct ClipWorkspace {
-    unsigned int ticket;  // CTAs done; zeroed before every launch
+    unsigned int ticket;           // CTAs done; zeroed before every launch
     unsigned int pad0;
+    unsigned long long nonfinite;  // non-finite reduced grads; zeroed likewise
     double norm_sq;
     float norm;
     float coef;
-    unsigned char pad1[40];
+    unsigned char pad1[32];
     double partial[kMaxClipCtas];
 };
+constexpr size_t kClipResetBytes = 16;  // ticket, pad0, nonfinite
+static_assert(offsetof(ClipWorkspace, norm_sq) == kClipResetBytes, "reset prefix");
+static_assert(offsetof(ClipWorkspace, partial) == 64, "workspace header");
+static_assert(sizeof(dopt_clip_report) == 16, "report layout");
 static_assert(sizeof(ClipWorkspace) <= DOPT_CLIP_WORKSPACE_BYTES, "workspace size");
 static_assert(sizeof(ClipWorkspace) <= DOPT_NOALLOC_SCRATCH_BYTES, "scratch size");
 
@@ -172,6 +179,7 @@ struct NormArgs {
     int32_t D;
     int32_t R;
     int32_t round_grad;
+    int32_t skip_nonfinite;  // report a NaN coefficient (skip) if any grad is Inf/NaN
     float scale;
     float max_norm;
 };
@@ -459,6 +467,7 @@ __device__ __forceinline__ void full_vector(const StepArgs &a, const Scalars &sc
     float acc[8];
     if constexpr (MODE == kFromMain) {
         const float coef = *a.clip_coef;
+        if (a.skip_nonfinite && isnan(coef)) return;  // the step is skipped
         const float4 g0 = ld_stream_f4(a.main_grad_in + e0), g1 = ld_stream_f4(a.main_grad_in + e0 + 4);
         const float f[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
@@ -510,6 +519,9 @@ __device__ __forceinline__ void full_vector(const StepArgs &a, const Scalars &sc
 // A vector that straddles a run edge: element by element, owned ones only.
 template <typename G, int DC, int MODE>
 __device__ __noinline__ void mixed_vector(const StepArgs &a, const Scalars &sc, int64_t e0, int j) {
+    if constexpr (MODE == kFromMain) {
+        if (a.skip_nonfinite && isnan(*a.clip_coef)) return;  // the step is skipped
+    }
     const int D = DC > 0 ? DC : a.D;
     bool done = false;
     for (int k = 0; k < kVec && !done; ++k) {
@@ -649,6 +661,7 @@ template <typename G, int DC>
 __global__ void __launch_bounds__(kThreads) dopt_rs_norm_kernel(const __grid_constant__ NormArgs a) {
     const int lane = threadIdx.x & 31;
     double local = 0.0;
+    unsigned int bad = 0;  // non-finite reduced grads seen by this thread
     for (int64_t t = blockIdx.x; t < a.n_tiles; t += gridDim.x) {
         const int64_t tile = a.rv.tile0 + t;
         const int64_t e0 = tile * kDoptTileElems + int64_t(threadIdx.x) * kVec;
@@ -662,7 +675,10 @@ __global__ void __launch_bounds__(kThreads) dopt_rs_norm_kernel(const __grid_con
             st_stream_f4(a.main_grad + e0 + 4, make_float4(acc[4], acc[5], acc[6], acc[7]));
             float sq[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) sq[k] = __fmul_rn(acc[k], acc[k]);
+            for (int k = 0; k < 8; ++k) {
+                sq[k] = __fmul_rn(acc[k], acc[k]);
+                bad += isfinite(acc[k]) ? 0u : 1u;
+            }
             const float s01 = __fadd_rn(sq[0], sq[1]), s23 = __fadd_rn(sq[2], sq[3]);
             const float s45 = __fadd_rn(sq[4], sq[5]), s67 = __fadd_rn(sq[6], sq[7]);
             local += double(__fadd_rn(__fadd_rn(s01, s23), __fadd_rn(s45, s67)));
@@ -676,18 +692,29 @@ __global__ void __launch_bounds__(kThreads) dopt_rs_norm_kernel(const __grid_con
                 if (a.round_grad) g = to_grad_type<G>(g);
                 a.main_grad[e] = g;
                 local += double(__fmul_rn(g, g));
+                bad += isfinite(g) ? 0u : 1u;
             }
         }
     }
     __shared__ double warp_part[kThreads / 32];
+    __shared__ unsigned int warp_bad[kThreads / 32];
     __shared__ bool last;
     local = warp_sum(local);
-    if (lane == 0) warp_part[threadIdx.x >> 5] = local;
+    bad = __reduce_add_sync(0xffffffffu, bad);
+    if (lane == 0) {
+        warp_part[threadIdx.x >> 5] = local;
+        warp_bad[threadIdx.x >> 5] = bad;
+    }
     __syncthreads();
     if (threadIdx.x == 0) {
         double cta = 0.0;
-        for (int w = 0; w < kThreads / 32; ++w) cta += warp_part[w];
+        unsigned long long cta_bad = 0;
+        for (int w = 0; w < kThreads / 32; ++w) {
+            cta += warp_part[w];
+            cta_bad += warp_bad[w];
+        }
         a.ws->partial[blockIdx.x] = cta;
+        if (cta_bad) atomicAdd(&a.ws->nonfinite, cta_bad);  // integer: order-free
         __threadfence();
         last = atomicAdd(&a.ws->ticket, 1u) == gridDim.x - 1;
     }
@@ -701,12 +728,17 @@ __global__ void __launch_bounds__(kThreads) dopt_rs_norm_kernel(const __grid_con
         const double norm = sqrt(v);
         double coef = double(a.max_norm) / (norm + 1e-6);
         if (coef > 1.0) coef = 1.0;
+        const unsigned long long nonfinite = __ldcg(&a.ws->nonfinite);
+        float c = float(coef);
+        if (a.skip_nonfinite && nonfinite != 0) c = __int_as_float(0x7fc00000);  // skip
         a.ws->norm_sq = v;
         a.ws->norm = float(norm);
-        a.ws->coef = float(coef);
+        a.ws->coef = c;
         if (a.norm_out) {
-            a.norm_out[0] = float(norm);
-            a.norm_out[1] = float(coef);
+            dopt_clip_report *rep = reinterpret_cast<dopt_clip_report *>(a.norm_out);
+            rep->norm = float(norm);
+            rep->coef = c;
+            if (a.skip_nonfinite) rep->nonfinite = nonfinite;
         }
     }
 }

@@ -175,14 +175,16 @@ int check_replicas(const char *who, int D, const void *const *ptrs) {
 int check_step_args(const char *who, const dopt_layout *L, const dopt_adam_cfg *cfg,
                     int64_t step, const void *const *grad_replicas, dopt_dtype grad_dtype,
                     const float *master, const float *exp_avg, const float *exp_avg_sq,
-                    void *const *param_replicas, uint32_t flags, const float *main_grad) {
+                    void *const *param_replicas, uint32_t flags, const float *main_grad,
+                    uint32_t extra_flags = 0) {
     using dopt::fail;
     if (!L || !cfg || !grad_replicas || !param_replicas || !master || !exp_avg || !exp_avg_sq)
         return fail(DOPT_E_ARG, "%s: NULL argument", who);
     if (step < 1) return fail(DOPT_E_ARG, "%s: step=%lld < 1", who, (long long)step);
     if (grad_dtype != DOPT_BF16 && grad_dtype != DOPT_FP32)
         return fail(DOPT_E_ARG, "%s: unknown grad dtype %d", who, int(grad_dtype));
-    if (flags & ~uint32_t(DOPT_STEP_GATHER | DOPT_STEP_HOST_GRADS | DOPT_STEP_ROUND_GRAD))
+    if (flags & ~(uint32_t(DOPT_STEP_GATHER | DOPT_STEP_HOST_GRADS | DOPT_STEP_ROUND_GRAD) |
+                  extra_flags))
         return fail(DOPT_E_ARG, "%s: unknown flags 0x%x", who, flags);
     if (!(cfg->lr >= 0.0f) || !std::isfinite(cfg->lr) || !(cfg->beta1 >= 0.0f && cfg->beta1 < 1.0f) ||
         !(cfg->beta2 >= 0.0f && cfg->beta2 < 1.0f) || !(cfg->eps >= 0.0f) || !std::isfinite(cfg->eps) ||
@@ -307,11 +309,12 @@ int launch_clipped(const char *who, const dopt_layout *L, const dopt_adam_cfg *c
     na.D = D;
     na.R = L->R;
     na.round_grad = (flags & DOPT_STEP_ROUND_GRAD) ? 1 : 0;
+    na.skip_nonfinite = (flags & DOPT_STEP_SKIP_NONFINITE) ? 1 : 0;
     na.scale = cfg->grad_scale;
     na.max_norm = max_norm;
     NormKernel nk = norm_kernel_for(grad_dtype, kernel_D(L));
     const int grid_a = norm_grid(nk, na.n_tiles, L->device);
-    cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(unsigned int), stream);
+    cudaError_t e = cudaMemsetAsync(ws, 0, kClipResetBytes, stream);
     if (e != cudaSuccess) return fail(DOPT_E_CUDA, "%s: workspace reset: %s", who, cudaGetErrorString(e));
     nk<<<grid_a, kThreads, 0, stream>>>(na);
     rc = launch_error(who, "norm");
@@ -323,6 +326,7 @@ int launch_clipped(const char *who, const dopt_layout *L, const dopt_adam_cfg *c
     fill_step_args(a, L, cfg, step, grads, master, exp_avg, exp_avg_sq, param_replicas, flags);
     a.main_grad_in = main_grad;
     a.clip_coef = &ws->coef;
+    a.skip_nonfinite = na.skip_nonfinite;
     StepKernel k = pick_step_kernel<float, kFromMain>(kernel_D(L));
     k<<<unsigned(tiles), kThreads, 0, stream>>>(a);
     return launch_error(who, "step");
@@ -471,7 +475,8 @@ extern "C" int dopt_step_clipped(const dopt_layout *L, const dopt_adam_cfg *cfg,
     const char *who = "dopt_step_clipped";
     NvtxRange range(who);
     int rc = check_step_args(who, L, cfg, step, grad_replicas, grad_dtype, master, exp_avg,
-                             exp_avg_sq, param_replicas, flags, main_grad);
+                             exp_avg_sq, param_replicas, flags, main_grad,
+                             DOPT_STEP_SKIP_NONFINITE);
     if (rc != DOPT_OK) return rc;
     rc = check_clip_args(who, main_grad, norm_out, max_norm);
     if (rc != DOPT_OK) return rc;
