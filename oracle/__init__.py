@@ -110,7 +110,7 @@ def _declare(lib) -> None:
         ctypes.POINTER(Adam), ctypes.c_int64, ctypes.c_int32, ctypes.POINTER(ctypes.c_void_p),
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p),
         ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_float,
-        ctypes.c_int32,
+        ctypes.c_int32, ctypes.c_int32,
     ]
     lib.orc_grad_norm_sq.restype = ctypes.c_int
     lib.orc_grad_norm_sq.argtypes = [i64p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
@@ -134,6 +134,10 @@ def _declare(lib) -> None:
     lib.orc_clip_coef.argtypes = [ctypes.c_double, ctypes.c_float]
     lib.orc_f32_to_bf16.restype = ctypes.c_uint16
     lib.orc_f32_to_bf16.argtypes = [ctypes.c_float]
+    lib.orc_f32_to_f16.restype = ctypes.c_uint16
+    lib.orc_f32_to_f16.argtypes = [ctypes.c_float]
+    lib.orc_f16_to_f32.restype = ctypes.c_float
+    lib.orc_f16_to_f32.argtypes = [ctypes.c_uint16]
     lib.orc_bf16_to_f32.restype = ctypes.c_float
     lib.orc_bf16_to_f32.argtypes = [ctypes.c_uint16]
     lib.orc_step_scalars.restype = None
@@ -154,6 +158,23 @@ def load(path: str | None = None):
             _declare(lib)
             _lib = lib
         return _lib
+
+
+GRAD_BF16, GRAD_F32, GRAD_F16 = 0, 1, 2
+
+
+def _grad_type(grads) -> int:
+    """Grad element type of the replicas: uint16 arrays hold bf16 bits,
+    float16 arrays are IEEE binary16, float32 arrays fp32."""
+    dt = grads[0].dtype
+    code = {np.dtype(np.uint16): GRAD_BF16, np.dtype(np.float32): GRAD_F32,
+            np.dtype(np.float16): GRAD_F16}.get(np.dtype(dt))
+    if code is None:
+        raise OracleError(f"grad dtype {dt}: use uint16 (bf16 bits), float16 or float32")
+    for g in grads:
+        if g.dtype != dt or not g.flags.c_contiguous:
+            raise OracleError("grads must be contiguous and all of one dtype")
+    return code
 
 
 def _i64(a):
@@ -261,16 +282,15 @@ def step(sizes, wd_mask, D: int, bucket_elems: int, pad_unit: int, adam: Adam, t
     n = len(sizes_a)
     if len(grads) != D or len(params) != D:
         raise OracleError("need D grad and D param arrays")
-    grad_is_f32 = grads[0].dtype == np.float32
-    for g in grads:
-        if g.dtype != (np.float32 if grad_is_f32 else np.uint16) or not g.flags.c_contiguous:
-            raise OracleError("grads must be contiguous, all uint16 (bf16 bits) or all float32")
+    grad_type = _grad_type(grads)
     for a in (master, exp_avg, exp_avg_sq):
         if a.dtype != np.float32 or not a.flags.c_contiguous:
             raise OracleError("state arrays must be contiguous float32")
+    param_is_f16 = params[0].dtype == np.float16
     for p in params:
-        if p.dtype != np.uint16 or not p.flags.c_contiguous:
-            raise OracleError("params must be contiguous uint16 (bf16 bits)")
+        if p.dtype != params[0].dtype or p.dtype not in (np.uint16, np.float16) \
+                or not p.flags.c_contiguous:
+            raise OracleError("params must be contiguous, all uint16 (bf16 bits) or all float16")
     if window is None:
         w0, w1 = 0, len(master)
     else:
@@ -288,11 +308,11 @@ def step(sizes, wd_mask, D: int, bucket_elems: int, pad_unit: int, adam: Adam, t
     pp = (ctypes.c_void_p * D)(*[p.ctypes.data for p in params])
     rc = lib.orc_step(sizes_p, n, None if wd is None else wd.ctypes.data, D, int(instances),
                       bucket_elems,
-                      pad_unit, ctypes.byref(adam), t, int(grad_is_f32), gp,
+                      pad_unit, ctypes.byref(adam), t, grad_type, gp,
                       master.ctypes.data, exp_avg.ctypes.data, exp_avg_sq.ctypes.data, pp,
                       int(bool(gather)),
                       None if main_grad_out is None else main_grad_out.ctypes.data, w0, w1,
-                      float(clip_coef), int(bool(round_grad)))
+                      float(clip_coef), int(bool(round_grad)), int(param_is_f16))
     if rc != ORC_OK:
         raise OracleError(f"orc_step failed: {rc}")
 
@@ -303,7 +323,7 @@ def grad_norm_sq(sizes, D: int, bucket_elems: int, pad_unit: int, grad_scale: fl
     window (tutorial §8.3 global norm), accumulated in double."""
     lib = lib or load()
     sizes_a, sizes_p = _i64(sizes)
-    grad_is_f32 = grads[0].dtype == np.float32
+    grad_type = _grad_type(grads)
     span = len(grads[0])
     w0, w1 = (0, span) if window is None else (int(window[0]), int(window[1]))
     if w1 - w0 != span or len(grads) != D:
@@ -311,7 +331,7 @@ def grad_norm_sq(sizes, D: int, bucket_elems: int, pad_unit: int, grad_scale: fl
     gp = (ctypes.c_void_p * D)(*[g.ctypes.data for g in grads])
     out = ctypes.c_double(0.0)
     rc = lib.orc_grad_norm_sq(sizes_p, len(sizes_a), D, int(instances), bucket_elems, pad_unit,
-                              float(grad_scale), int(grad_is_f32), gp, w0, w1,
+                              float(grad_scale), grad_type, gp, w0, w1,
                               int(bool(round_grad)), ctypes.byref(out))
     if rc != ORC_OK:
         raise OracleError(f"orc_grad_norm_sq failed: {rc}")
@@ -325,7 +345,7 @@ def count_nonfinite(sizes, D: int, bucket_elems: int, pad_unit: int, grad_scale:
     that FP16 overflows easily)."""
     lib = lib or load()
     sizes_a, sizes_p = _i64(sizes)
-    grad_is_f32 = grads[0].dtype == np.float32
+    grad_type = _grad_type(grads)
     span = len(grads[0])
     w0, w1 = (0, span) if window is None else (int(window[0]), int(window[1]))
     if w1 - w0 != span or len(grads) != D:
@@ -333,7 +353,7 @@ def count_nonfinite(sizes, D: int, bucket_elems: int, pad_unit: int, grad_scale:
     gp = (ctypes.c_void_p * D)(*[g.ctypes.data for g in grads])
     out = ctypes.c_int64(0)
     rc = lib.orc_count_nonfinite(sizes_p, len(sizes_a), D, int(instances), bucket_elems,
-                                 pad_unit, float(grad_scale), int(grad_is_f32), gp, w0, w1,
+                                 pad_unit, float(grad_scale), grad_type, gp, w0, w1,
                                  int(bool(round_grad)), ctypes.byref(out))
     if rc != ORC_OK:
         raise OracleError(f"orc_count_nonfinite failed: {rc}")
@@ -347,18 +367,15 @@ def allreduce(sizes, D: int, bucket_elems: int, pad_unit: int, grad_scale: float
     the reduced grad at every owned element, rounded to the grad type."""
     lib = lib or load()
     sizes_a, sizes_p = _i64(sizes)
-    grad_is_f32 = grads[0].dtype == np.float32
+    grad_type = _grad_type(grads)
     span = len(grads[0])
     w0, w1 = (0, span) if window is None else (int(window[0]), int(window[1]))
     if w1 - w0 != span or len(grads) != D:
         raise OracleError("grads must be D arrays of the window length")
-    for g in grads:
-        if g.dtype != (np.float32 if grad_is_f32 else np.uint16) or not g.flags.c_contiguous:
-            raise OracleError("grads must be contiguous, all uint16 or all float32")
     gp = (ctypes.c_void_p * D)(*[g.ctypes.data for g in grads])
     rc = lib.orc_allreduce(sizes_p, len(sizes_a), D, int(instances), bucket_elems, pad_unit,
                            float(grad_scale),
-                           int(grad_is_f32), gp, w0, w1)
+                           grad_type, gp, w0, w1)
     if rc != ORC_OK:
         raise OracleError(f"orc_allreduce failed: {rc}")
 
@@ -367,6 +384,20 @@ def clip_coef(norm_sq: float, max_norm: float, lib=None) -> float:
     """min(1, max_norm / (sqrt(norm_sq) + 1e-6)), rounded to float once."""
     lib = lib or load()
     return float(lib.orc_clip_coef(float(norm_sq), float(max_norm)))
+
+
+def f32_to_f16(x, lib=None) -> np.ndarray:
+    """Round fp32 values to IEEE binary16 bits (nearest, ties to even)."""
+    lib = lib or load()
+    x = np.asarray(x, np.float32).ravel()
+    return np.array([lib.orc_f32_to_f16(float(v)) for v in x], np.uint16)
+
+
+def f16_to_f32(bits, lib=None) -> np.ndarray:
+    """Widen IEEE binary16 bits to fp32 (exact)."""
+    lib = lib or load()
+    bits = np.asarray(bits, np.uint16).ravel()
+    return np.array([lib.orc_f16_to_f32(int(b)) for b in bits], np.float32)
 
 
 def f32_to_bf16(x, lib=None) -> np.ndarray:

@@ -59,6 +59,12 @@
  *      float once.
  *  R7  Model params are bf16; fp32 -> bf16 is round-to-nearest-even, NaN
  *      stays a quiet NaN.
+ *  R7b FP16 ([P2] §8.2 names FP16/BF16 for forward and backward; [P3]'s
+ *      state table lists FP16 params and grads): grads may be IEEE binary16
+ *      (widened exactly) and the model params binary16 too; fp32 -> fp16
+ *      rounds to nearest even, overflows to Inf from 65520 on, and keeps
+ *      subnormals.  Rounding the reduced grad (R12) and the all-reduce
+ *      (R10) use the grads' type.
  *  R8  The all-gather copies every rank's owned elements (its pieces) from
  *      its own replica into all other replicas; padding is not copied.
  *  R9  Global-norm clipping ([P2] §8.3: the norm sqrt(sum ||g||^2) over all
@@ -105,6 +111,11 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+
+/* Grad element types (the grad_type arguments). */
+#define ORC_GRAD_BF16 0
+#define ORC_GRAD_F32 1
+#define ORC_GRAD_F16 2
 
 #define ORC_OK 0
 #define ORC_E_ARG (-1)
@@ -276,6 +287,63 @@ static uint32_t orc_f32_to_bits(float f)
 
 float orc_bf16_to_f32(uint16_t h) { return orc_bits_to_f32((uint32_t)h << 16); }
 
+/*
+ * IEEE 754 binary16 (R7b): 1 sign bit, 5 exponent bits (bias 15), 10
+ * fraction bits; exponent 0 holds zero and the subnormals (fraction *
+ * 2^-24), exponent 31 Inf and NaN.  Widening to fp32 is exact.
+ */
+float orc_f16_to_f32(uint16_t h)
+{
+    uint32_t sign = (uint32_t)(h >> 15) << 31;
+    uint32_t e = (h >> 10) & 0x1fu;
+    uint32_t frac = h & 0x3ffu;
+    if (e == 0x1fu)
+        return orc_bits_to_f32(sign | 0x7f800000u | (frac << 13));
+    if (e == 0) {
+        float v = (float)frac * 0x1p-24f; /* exact: frac < 2^10 */
+        return sign ? -v : v;
+    }
+    return orc_bits_to_f32(sign | ((e - 15u + 127u) << 23) | (frac << 13));
+}
+
+/*
+ * fp32 -> binary16, round to nearest, ties to even; magnitudes from 65520
+ * (the midpoint above the largest finite 65504, whose even neighbour is the
+ * overflow) give Inf; NaN gives the quiet NaN 0x7e00 with the sign.  The
+ * magnitude is divided by the quantum of its binade (a power of two, so
+ * exactly, in double) and rounded with rint, which rounds ties to even in
+ * the default rounding mode.
+ */
+uint16_t orc_f32_to_f16(float f)
+{
+    uint32_t u = orc_f32_to_bits(f);
+    uint16_t sign = (uint16_t)((u >> 16) & 0x8000u);
+    uint32_t a = u & 0x7fffffffu;
+    if (a > 0x7f800000u)
+        return (uint16_t)(sign | 0x7e00u);
+    double ax = (double)orc_bits_to_f32(a);
+    if (ax >= 65520.0)
+        return (uint16_t)(sign | 0x7c00u);
+    if (ax == 0.0)
+        return sign;
+    int e2 = 0;
+    (void)frexp(ax, &e2); /* ax = m * 2^e2, 0.5 <= m < 1 */
+    int ex = e2 - 1;      /* floor(log2 ax) */
+    if (ex < -14)
+        ex = -14;         /* the subnormals share the quantum 2^-24 */
+    double n = rint(ldexp(ax, 10 - ex));
+    if (n >= 2048.0) {
+        n *= 0.5;
+        ex += 1;
+    }
+    uint32_t bits;
+    if (n >= 1024.0)
+        bits = ((uint32_t)(ex + 15) << 10) | ((uint32_t)n - 1024u);
+    else
+        bits = (uint32_t)n; /* subnormal (ex == -14) */
+    return (uint16_t)(sign | bits);
+}
+
 /* Round to nearest, ties to even, on the 16 dropped bits; NaN -> quiet NaN. */
 uint16_t orc_f32_to_bf16(float f)
 {
@@ -319,10 +387,12 @@ static orc_scalars orc_make_scalars(const orc_adam *c, int64_t t)
 }
 
 /* Element i of replica r, widened to fp32. */
-static float orc_grad(const void *const *grads, int32_t grad_is_f32, int32_t r, int64_t idx)
+static float orc_grad(const void *const *grads, int32_t grad_type, int32_t r, int64_t idx)
 {
-    if (grad_is_f32)
+    if (grad_type == ORC_GRAD_F32)
         return ((const float *)grads[r])[idx];
+    if (grad_type == ORC_GRAD_F16)
+        return orc_f16_to_f32(((const uint16_t *)grads[r])[idx]);
     return orc_bf16_to_f32(((const uint16_t *)grads[r])[idx]);
 }
 
@@ -331,16 +401,16 @@ static float orc_grad(const void *const *grads, int32_t grad_is_f32, int32_t r, 
  * reduce-scatter within the instance); then the instances' sums added in
  * instance order (the all-reduce across instances).  With one instance this
  * is the plain rank-order sum.  `idx` is window-relative. */
-static float orc_reduce_element(const void *const *grads, int32_t grad_is_f32, int32_t D,
+static float orc_reduce_element(const void *const *grads, int32_t grad_type, int32_t D,
                                 int32_t instances, float scale, int64_t idx)
 {
     int32_t R = D / instances;
     float acc = 0.0f;
     for (int32_t inst = 0; inst < instances; ++inst) {
         int32_t first = inst * R;
-        float part = scale * orc_grad(grads, grad_is_f32, first, idx);
+        float part = scale * orc_grad(grads, grad_type, first, idx);
         for (int32_t q = first + 1; q < first + R; ++q) {
-            float x = scale * orc_grad(grads, grad_is_f32, q, idx);
+            float x = scale * orc_grad(grads, grad_type, q, idx);
             part = part + x;
         }
         acc = (inst == 0) ? part : acc + part;
@@ -350,9 +420,11 @@ static float orc_reduce_element(const void *const *grads, int32_t grad_is_f32, i
 
 /* The reduced grad rounded to the grad buffer's type (R12): bf16 rounds to
  * nearest even (R7), fp32 stays as is. */
-static float orc_round_to_grad_type(float g, int32_t grad_is_f32)
+static float orc_round_to_grad_type(float g, int32_t grad_type)
 {
-    return grad_is_f32 ? g : orc_bf16_to_f32(orc_f32_to_bf16(g));
+    if (grad_type == ORC_GRAD_F16)
+        return orc_f16_to_f32(orc_f32_to_f16(g));
+    return grad_type == ORC_GRAD_F32 ? g : orc_bf16_to_f32(orc_f32_to_bf16(g));
 }
 
 /* One AdamW update of a single element (R6), fp32, one rounding per op. */
@@ -404,10 +476,10 @@ static void orc_adamw(const orc_scalars *s, int decays, float g, float *w, float
 int orc_step(const int64_t *sizes, int32_t n, const uint8_t *wd_mask, int32_t D,
              int32_t instances, int64_t bucket_elems, int32_t pad_unit,
              const orc_adam *cfg, int64_t step,
-             int32_t grad_is_f32, const void *const *grads, float *master, float *exp_avg,
+             int32_t grad_type, const void *const *grads, float *master, float *exp_avg,
              float *exp_avg_sq, uint16_t *const *params, int32_t gather,
              float *main_grad_out, int64_t w0, int64_t w1, float clip_coef,
-             int32_t round_grad)
+             int32_t round_grad, int32_t param_is_f16)
 {
     if (step < 1 || w0 < 0 || w1 < w0 || instances < 1 || D % instances != 0)
         return ORC_E_ARG;
@@ -472,7 +544,7 @@ int orc_step(const int64_t *sizes, int32_t n, const uint8_t *wd_mask, int32_t D,
             int64_t j_hi = orc_min(S, w1 - mine.start);
             for (int64_t j = j_lo; j < j_hi; ++j) {
                 int64_t i = mine.start + j;
-                shard[j] = orc_reduce_element(grads, grad_is_f32, D, instances, sc.scale,
+                shard[j] = orc_reduce_element(grads, grad_type, D, instances, sc.scale,
                                               i - w0);
             }
 
@@ -494,7 +566,7 @@ int orc_step(const int64_t *sizes, int32_t n, const uint8_t *wd_mask, int32_t D,
                     float g = shard[pc->gbuf_local.start + t];
                     /* the reduced grad in the grad buffer's type (R12) */
                     if (round_grad)
-                        g = orc_round_to_grad_type(g, grad_is_f32);
+                        g = orc_round_to_grad_type(g, grad_type);
                     /* global-norm clipping (R9): one fp32 multiply; a
                      * coefficient of exactly 1 leaves g unchanged */
                     float gc = g * clip_coef;
@@ -507,7 +579,8 @@ int orc_step(const int64_t *sizes, int32_t n, const uint8_t *wd_mask, int32_t D,
                      * gbuf_world_in_bucket ([P1] §4.3); rank r of every
                      * instance holds the same update (R11) */
                     int64_t bi = bstart[k] + pc->gbuf_world_in_bucket.start + t;
-                    uint16_t updated = orc_f32_to_bf16(master[mi - w0]);
+                    uint16_t updated = param_is_f16 ? orc_f32_to_f16(master[mi - w0])
+                                                    : orc_f32_to_bf16(master[mi - w0]);
                     for (int32_t inst = 0; inst < instances; ++inst)
                         params[inst * R + r][bi - w0] = updated;
                     if (main_grad_out)
@@ -553,7 +626,7 @@ done:
  */
 int orc_count_nonfinite(const int64_t *sizes, int32_t n, int32_t D, int32_t instances,
                         int64_t bucket_elems, int32_t pad_unit, float grad_scale,
-                        int32_t grad_is_f32, const void *const *grads, int64_t w0, int64_t w1,
+                        int32_t grad_type, const void *const *grads, int64_t w0, int64_t w1,
                         int32_t round_grad, int64_t *out)
 {
     if (w0 < 0 || w1 < w0 || !out || instances < 1 || D % instances != 0)
@@ -594,9 +667,9 @@ int orc_count_nonfinite(const int64_t *sizes, int32_t n, int32_t D, int32_t inst
         int64_t i_lo = orc_max(pieces[pi].gbuf_world.start, w0);
         int64_t i_hi = orc_min(pieces[pi].gbuf_world.end, w1);
         for (int64_t i = i_lo; i < i_hi; ++i) {
-            float r = orc_reduce_element(grads, grad_is_f32, D, instances, grad_scale, i - w0);
+            float r = orc_reduce_element(grads, grad_type, D, instances, grad_scale, i - w0);
             if (round_grad)
-                r = orc_round_to_grad_type(r, grad_is_f32);
+                r = orc_round_to_grad_type(r, grad_type);
             if (isinf(r) || isnan(r))
                 ++count;
         }
@@ -620,7 +693,7 @@ done:
  */
 int orc_grad_norm_sq(const int64_t *sizes, int32_t n, int32_t D, int32_t instances,
                      int64_t bucket_elems, int32_t pad_unit, float grad_scale,
-                     int32_t grad_is_f32, const void *const *grads, int64_t w0, int64_t w1,
+                     int32_t grad_type, const void *const *grads, int64_t w0, int64_t w1,
                      int32_t round_grad, double *out)
 {
     if (w0 < 0 || w1 < w0 || !out || instances < 1 || D % instances != 0)
@@ -661,9 +734,9 @@ int orc_grad_norm_sq(const int64_t *sizes, int32_t n, int32_t D, int32_t instanc
         int64_t i_lo = orc_max(pieces[pi].gbuf_world.start, w0);
         int64_t i_hi = orc_min(pieces[pi].gbuf_world.end, w1);
         for (int64_t i = i_lo; i < i_hi; ++i) {
-            float r = orc_reduce_element(grads, grad_is_f32, D, instances, grad_scale, i - w0);
+            float r = orc_reduce_element(grads, grad_type, D, instances, grad_scale, i - w0);
             if (round_grad)
-                r = orc_round_to_grad_type(r, grad_is_f32);
+                r = orc_round_to_grad_type(r, grad_type);
             double g = (double)r;
             sum += g * g;
         }
@@ -689,7 +762,7 @@ done:
  * grads are window-relative and are overwritten.
  */
 int orc_allreduce(const int64_t *sizes, int32_t n, int32_t D, int32_t instances,
-                  int64_t bucket_elems, int32_t pad_unit, float grad_scale, int32_t grad_is_f32,
+                  int64_t bucket_elems, int32_t pad_unit, float grad_scale, int32_t grad_type,
                   void *const *grads, int64_t w0, int64_t w1)
 {
     if (w0 < 0 || w1 < w0 || instances < 1 || D % instances != 0)
@@ -744,7 +817,7 @@ int orc_allreduce(const int64_t *sizes, int32_t n, int32_t D, int32_t instances,
             int64_t j_lo = orc_max(0, w0 - mine.start);
             int64_t j_hi = orc_min(S, w1 - mine.start);
             for (int64_t j = j_lo; j < j_hi; ++j)
-                shard[j] = orc_reduce_element((const void *const *)grads, grad_is_f32, D,
+                shard[j] = orc_reduce_element((const void *const *)grads, grad_type, D,
                                               instances, grad_scale, mine.start + j - w0);
             int32_t last_piece = first_piece;
             while (last_piece < npieces && pieces[last_piece].bucket_id == k &&
@@ -759,8 +832,10 @@ int orc_allreduce(const int64_t *sizes, int32_t n, int32_t D, int32_t instances,
                     int64_t i = pc->gbuf_world.start + t;
                     float reduced = shard[pc->gbuf_local.start + t];
                     for (int32_t q = 0; q < D; ++q) {
-                        if (grad_is_f32)
+                        if (grad_type == ORC_GRAD_F32)
                             ((float *)grads[q])[i - w0] = reduced;
+                        else if (grad_type == ORC_GRAD_F16)
+                            ((uint16_t *)grads[q])[i - w0] = orc_f32_to_f16(reduced);
                         else
                             ((uint16_t *)grads[q])[i - w0] = orc_f32_to_bf16(reduced);
                     }

@@ -933,6 +933,105 @@ def pin_nonfinite_count(lib):
         assert oracle.count_nonfinite(sz, Dr, 0, pad, 0.5, gr, lib=lib) == want
 
 
+def pin_f16_conversions(lib):
+    """IEEE binary16 (reading R7b), against numpy's float16, which
+    implements the standard's conversions: widening every one of the 65536
+    bit patterns; narrowing every finite half, every midpoint between
+    neighbouring halves (ties go to the even one), the floats just beside
+    those midpoints, the overflow edge, subnormals and random floats."""
+    allbits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    want = allbits.view(np.float16).astype(np.float32)
+    got = np.array([lib.orc_f16_to_f32(int(b)) for b in allbits], np.float32)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan].view(np.uint32), want[~nan].view(np.uint32))
+
+    finite = want[np.isfinite(want)]
+    pos = np.unique(np.abs(finite.astype(np.float64)))
+    mids = (pos[:-1] + pos[1:]) / 2  # exact in fp32 for binary16 neighbours
+    mids32 = mids.astype(np.float32)
+    assert np.array_equal(mids32.astype(np.float64), mids)
+    rng = np.random.default_rng(23)
+    rand = (rng.standard_normal(20000) * np.exp(rng.uniform(-20, 12, 20000))).astype(np.float32)
+    edge = np.array([0.0, -0.0, 65504.0, 65519.996, 65520.0, 65536.0, 1e30, 2.0 ** -24,
+                     2.0 ** -25, 3 * 2.0 ** -26, 2.0 ** -26, 2.0 ** -14, 6.1e-5, 1e-8,
+                     np.inf, -np.inf, np.nan], np.float32)
+    xs = np.concatenate([finite, -finite, mids32, -mids32,
+                         np.nextafter(mids32, np.float32(np.inf)),
+                         np.nextafter(mids32, np.float32(0)), rand, edge])
+    with np.errstate(over="ignore"):
+        want16 = xs.astype(np.float16).view(np.uint16)
+    got16 = np.array([lib.orc_f32_to_f16(float(x)) for x in xs], np.uint16)
+    wnan = np.isnan(want16.view(np.float16))
+    assert np.array_equal(np.isnan(got16.view(np.float16)), wnan)
+    bad = np.flatnonzero(got16[~wnan] != want16[~wnan])
+    assert bad.size == 0, (xs[~wnan][bad[:5]], got16[~wnan][bad[:5]], want16[~wnan][bad[:5]])
+
+
+def pin_f16_grads_and_params(lib):
+    """FP16 grads whose values are exact in both fp16 and bf16 give the bf16
+    path's step, main grads and all-reduce bit for bit; fp16 params are
+    numpy's float16 rounding of the updated master; with the rounding of
+    R12 the main grads are numpy's float16 of the unrounded ones; and
+    60000 + 60000 (finite in fp32, beyond fp16's 65504) is non-finite only
+    once rounded to fp16."""
+    sizes, wd, D, pad = [300, 41, 129], [1, 0, 1], 4, 2
+    L = oracle.range_map(sizes, D, 0, pad, lib=lib)
+    N = L.numel
+    owned = np.zeros(N, bool)
+    for p in range(len(sizes)):
+        owned[L.param_start[p]:L.param_end[p]] = True
+    rng = np.random.default_rng(29)
+    vals = [(rng.integers(-64, 65, N) * 2.0 ** -10).astype(np.float32) for _ in range(D)]
+    g16 = [v.astype(np.float16) for v in vals]
+    gbf = [(v.view(np.uint32) >> 16).astype(np.uint16) for v in vals]  # exact
+    adam = oracle.make_adam(grad_scale=0.25)
+    master0, m0, v0 = _state(N, 31, 1e-4, 1e-6)
+    out = {}
+    for name, g in (("f16", g16), ("bf16", gbf)):
+        master, m, v = master0.copy(), m0.copy(), v0.copy()
+        params = _params_from(master0, D)
+        mg = np.zeros(N, np.float32)
+        oracle.step(sizes, wd, D, 0, pad, adam, 1, [x.copy() for x in g], master, m, v, params,
+                    main_grad_out=mg, lib=lib)
+        ar = [x.copy() for x in g]
+        oracle.allreduce(sizes, D, 0, pad, 0.25, ar, lib=lib)
+        arf = [x.astype(np.float32) if name == "f16" else
+               (x.astype(np.uint32) << 16).view(np.float32) for x in ar]
+        out[name] = (master, m, v, params, mg, arf)
+    for a, b in zip(out["f16"][:3] + (out["f16"][4],), out["bf16"][:3] + (out["bf16"][4],)):
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    for a, b in zip(out["f16"][5], out["bf16"][5]):
+        assert np.array_equal(a[owned], b[owned])
+    # fp16 params
+    master, m, v = master0.copy(), m0.copy(), v0.copy()
+    p16 = [master0.astype(np.float16) for _ in range(D)]
+    p_before = [p.copy() for p in p16]
+    oracle.step(sizes, wd, D, 0, pad, adam, 1, [x.copy() for x in g16], master, m, v, p16,
+                lib=lib)
+    assert np.array_equal(master.view(np.uint32), out["f16"][0].view(np.uint32))
+    for p, p0 in zip(p16, p_before):
+        assert np.array_equal(p[owned].view(np.uint16), master[owned].astype(np.float16).view(np.uint16))
+        assert np.array_equal(p[~owned].view(np.uint16), p0[~owned].view(np.uint16))
+    # the rounding of R12 in fp16
+    gr = [rng.normal(0, 1, N).astype(np.float16) for _ in range(D)]
+    runs = {}
+    for rg in (False, True):
+        mg = np.zeros(N, np.float32)
+        master, m, v = master0.copy(), m0.copy(), v0.copy()
+        oracle.step(sizes, wd, D, 0, pad, oracle.make_adam(grad_scale=0.3), 1, gr, master, m, v,
+                    _params_from(master0, D), main_grad_out=mg, round_grad=rg, lib=lib)
+        runs[rg] = mg
+    want = runs[False].astype(np.float16).astype(np.float32)
+    assert np.array_equal(runs[True][owned], want[owned])
+    assert np.count_nonzero(want[owned] != runs[False][owned]) > owned.sum() // 2
+    # overflow only once rounded to fp16
+    go = [np.zeros(N, np.float16) for _ in range(D)]
+    go[0][3] = go[1][3] = np.float16(60000.0)
+    assert oracle.count_nonfinite(sizes, D, 0, pad, 1.0, go, lib=lib) == 0
+    assert oracle.count_nonfinite(sizes, D, 0, pad, 1.0, go, round_grad=True, lib=lib) == 1
+
+
 ALL_PINS = [
     pin_page1_ownership,
     pin_brute_force_range_maps,
@@ -958,4 +1057,6 @@ ALL_PINS = [
     pin_instances_write_back_and_gather,
     pin_round_grad,
     pin_nonfinite_count,
+    pin_f16_conversions,
+    pin_f16_grads_and_params,
 ]

@@ -15,8 +15,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 # (name, text in dopt_oracle.c, replacement)
 MUTANTS = [
-    ("no_scale_first_rank", "float part = scale * orc_grad(grads, grad_is_f32, first, idx);",
-     "float part = orc_grad(grads, grad_is_f32, first, idx);"),
+    ("no_scale_first_rank", "float part = scale * orc_grad(grads, grad_type, first, idx);",
+     "float part = orc_grad(grads, grad_type, first, idx);"),
     ("skip_last_rank", "for (int32_t q = first + 1; q < first + R; ++q) {",
      "for (int32_t q = first + 1; q < first + R - 1; ++q) {"),
     ("skip_last_instance", "for (int32_t inst = 0; inst < instances; ++inst) {\n        int32_t first",
@@ -54,19 +54,22 @@ MUTANTS = [
     ("local_range_from_bucket", "pc.gbuf_local = orc_normalize(pc.gbuf_world, x - mine.start);",
      "pc.gbuf_local = orc_normalize(pc.gbuf_world, x - bucket_start[k]);"),
     ("no_gather", "if (gather) {", "if (0) {"),
-    ("allreduce_skips_own_rank", "for (int32_t q = 0; q < D; ++q) {\n                        if (grad_is_f32)",
-     "for (int32_t q = 0; q < D; ++q) {\n                        if (q == r) continue;\n                        if (grad_is_f32)"),
+    ("allreduce_skips_own_rank",
+     "for (int32_t q = 0; q < D; ++q) {\n                        if (grad_type == ORC_GRAD_F32)",
+     "for (int32_t q = 0; q < D; ++q) {\n                        if (q == r) continue;\n"
+     "                        if (grad_type == ORC_GRAD_F32)"),
     ("allreduce_truncates_bf16", "((uint16_t *)grads[q])[i - w0] = orc_f32_to_bf16(reduced);",
      "((uint16_t *)grads[q])[i - w0] = (uint16_t)(orc_f32_to_bits(reduced) >> 16);"),
     ("allreduce_via_bucket_range", "float reduced = shard[pc->gbuf_local.start + t];",
      "float reduced = shard[pc->gbuf_world_in_bucket.start + t];"),
-    ("round_grad_ignored", "if (round_grad)\n                        g = orc_round_to_grad_type(g, grad_is_f32);",
-     "if (0)\n                        g = orc_round_to_grad_type(g, grad_is_f32);"),
+    ("round_grad_ignored", "if (round_grad)\n                        g = orc_round_to_grad_type(g, grad_type);",
+     "if (0)\n                        g = orc_round_to_grad_type(g, grad_type);"),
     ("round_grad_norm_unrounded",
-     "if (round_grad)\n                r = orc_round_to_grad_type(r, grad_is_f32);\n            double g",
-     "if (0)\n                r = orc_round_to_grad_type(r, grad_is_f32);\n            double g"),
-    ("round_grad_truncates", "return grad_is_f32 ? g : orc_bf16_to_f32(orc_f32_to_bf16(g));",
-     "return grad_is_f32 ? g : orc_bits_to_f32(orc_f32_to_bits(g) & 0xffff0000u);"),
+     "if (round_grad)\n                r = orc_round_to_grad_type(r, grad_type);\n            double g",
+     "if (0)\n                r = orc_round_to_grad_type(r, grad_type);\n            double g"),
+    ("round_grad_truncates",
+     "return grad_type == ORC_GRAD_F32 ? g : orc_bf16_to_f32(orc_f32_to_bf16(g));",
+     "return grad_type == ORC_GRAD_F32 ? g : orc_bits_to_f32(orc_f32_to_bits(g) & 0xffff0000u);"),
     ("clip_not_applied", "float gc = g * clip_coef;", "float gc = g;"),
     ("norm_not_squared", "sum += g * g;", "sum += g < 0 ? -g : g;"),
     ("clip_no_sqrt", "double norm = sqrt(norm_sq);", "double norm = norm_sq;"),
@@ -79,18 +82,34 @@ MUTANTS = [
     ("nonfinite_misses_nan", "if (isinf(r) || isnan(r))\n                ++count;",
      "if (isinf(r))\n                ++count;"),
     ("nonfinite_ignores_rounding",
-     "r = orc_round_to_grad_type(r, grad_is_f32);\n            if (isinf(r) || isnan(r))",
+     "r = orc_round_to_grad_type(r, grad_type);\n            if (isinf(r) || isnan(r))",
      "(void)0;\n            if (isinf(r) || isnan(r))"),
     ("nonfinite_counts_replicas", "if (isinf(r) || isnan(r))\n                ++count;",
-     "for (int32_t q = 0; q < D; ++q) {\n                float x = orc_grad(grads, grad_is_f32, q, i - w0);\n"
+     "for (int32_t q = 0; q < D; ++q) {\n                float x = orc_grad(grads, grad_type, q, i - w0);\n"
      "                if (isinf(x) || isnan(x))\n                    ++count;\n            }"),
     ("nonfinite_counts_past_piece_end",
      "int64_t i_hi = orc_min(pieces[pi].gbuf_world.end, w1);\n        for (int64_t i = i_lo; i < i_hi; ++i) {\n"
-     "            float r = orc_reduce_element(grads, grad_is_f32, D, instances, grad_scale, i - w0);\n"
-     "            if (round_grad)\n                r = orc_round_to_grad_type(r, grad_is_f32);\n            if (isinf",
+     "            float r = orc_reduce_element(grads, grad_type, D, instances, grad_scale, i - w0);\n"
+     "            if (round_grad)\n                r = orc_round_to_grad_type(r, grad_type);\n            if (isinf",
      "int64_t i_hi = orc_min(pieces[pi].gbuf_world.end + 1, w1);\n        for (int64_t i = i_lo; i < i_hi; ++i) {\n"
-     "            float r = orc_reduce_element(grads, grad_is_f32, D, instances, grad_scale, i - w0);\n"
-     "            if (round_grad)\n                r = orc_round_to_grad_type(r, grad_is_f32);\n            if (isinf"),
+     "            float r = orc_reduce_element(grads, grad_type, D, instances, grad_scale, i - w0);\n"
+     "            if (round_grad)\n                r = orc_round_to_grad_type(r, grad_type);\n            if (isinf"),
+    ("f16_widen_bias", "return orc_bits_to_f32(sign | ((e - 15u + 127u) << 23) | (frac << 13));",
+     "return orc_bits_to_f32(sign | ((e - 14u + 127u) << 23) | (frac << 13));"),
+    ("f16_widen_flushes_subnormals", "float v = (float)frac * 0x1p-24f;", "float v = 0.0f;"),
+    ("f16_narrow_truncates", "double n = rint(ldexp(ax, 10 - ex));",
+     "double n = floor(ldexp(ax, 10 - ex));"),
+    ("f16_narrow_flushes_subnormals", "bits = (uint32_t)n; /* subnormal (ex == -14) */",
+     "bits = 0u;"),
+    ("f16_grads_read_as_bf16",
+     "if (grad_type == ORC_GRAD_F16)\n        return orc_f16_to_f32(((const uint16_t *)grads[r])[idx]);",
+     "if (0)\n        return orc_f16_to_f32(((const uint16_t *)grads[r])[idx]);"),
+    ("f16_params_written_as_bf16", "uint16_t updated = param_is_f16 ? orc_f32_to_f16(",
+     "uint16_t updated = 0 ? orc_f32_to_f16("),
+    ("f16_round_grad_as_bf16", "if (grad_type == ORC_GRAD_F16)\n        return orc_f16_to_f32(orc_f32_to_f16(g));",
+     "if (0)\n        return orc_f16_to_f32(orc_f32_to_f16(g));"),
+    ("f16_allreduce_as_bf16", "else if (grad_type == ORC_GRAD_F16)\n                            ((uint16_t *)grads[q])[i - w0] = orc_f32_to_f16(reduced);",
+     "else if (0)\n                            ((uint16_t *)grads[q])[i - w0] = orc_f32_to_f16(reduced);"),
 ]
 
 RUNNER = r"""
