@@ -118,8 +118,15 @@ typedef struct {
     float grad_scale;
 } dopt_adam_cfg;
 
-/* Gradient element type of the replica buffers. */
-typedef enum { DOPT_BF16 = 0, DOPT_FP32 = 1 } dopt_dtype;
+/*
+ * Gradient element type of the replica buffers.  DOPT_FP16 is IEEE
+ * binary16 (the tutorial's mixed-precision section and the ZeRO page's
+ * state table list FP16 grads next to BF16): widened exactly; where a
+ * reduced grad goes back into the grad type (DOPT_STEP_ROUND_GRAD, the
+ * all-reduce) it is rounded to nearest even and overflows to Inf beyond
+ * 65504.
+ */
+typedef enum { DOPT_BF16 = 0, DOPT_FP32 = 1, DOPT_FP16 = 2 } dopt_dtype;
 
 /* dopt_step flags. */
 #define DOPT_STEP_GATHER 1u /* fuse the all-gather: write all D replicas */
@@ -135,14 +142,20 @@ typedef enum { DOPT_BF16 = 0, DOPT_FP32 = 1 } dopt_dtype;
  */
 #define DOPT_STEP_HOST_GRADS 2u
 /*
- * Round each reduced grad to the grad type before clipping and Adam (bf16:
- * nearest even; fp32 grads are unchanged), as when the reduce-scatter writes
+ * Round each reduced grad to the grad type before clipping and Adam (bf16
+ * and fp16: nearest even; fp32 grads are unchanged), as when the reduce-scatter writes
  * into the grad buffer and the optimizer copies the shard from there (page
  * 1, §4.2-§4.3).  main_grad_out / main_grad then hold the rounded values and
  * the clipped step's norm is taken over them.  Without the flag the fp32
  * sum feeds Adam directly.  Accepted by every step entry point.
  */
 #define DOPT_STEP_ROUND_GRAD 4u
+/*
+ * The param replicas hold IEEE fp16 instead of bf16: the write-back rounds
+ * the fp32 master to fp16 (nearest even, Inf beyond 65504).  The all-gather
+ * copies 16-bit values and is the same for both types.
+ */
+#define DOPT_STEP_PARAMS_FP16 16u
 
 typedef struct dopt_layout dopt_layout;
 
@@ -210,7 +223,8 @@ void dopt_layout_free(dopt_layout *layout);
  *     v      = beta2*v + (1-beta2)*(g*g)
  *     w      = w * (1 - lr*weight_decay)          (only if p decays)
  *     w      = w - step_size * (m / (sqrt(v)/bc2_sqrt + eps))
- *     param_replicas[r][i] = bf16_rne(w)   for every r (DOPT_STEP_GATHER)
+ *     param_replicas[r][i] = bf16_rne(w)   for every r (DOPT_STEP_GATHER;
+ *                                          fp16_rne(w) with DOPT_STEP_PARAMS_FP16)
  *                                          or, without the flag, for the
  *                                          replica of rank q in every
  *                                          instance
@@ -229,8 +243,10 @@ void dopt_layout_free(dopt_layout *layout);
  *   master, exp_avg, exp_avg_sq
  *                   device fp32, padded_numel elements each, buffer-indexed
  *                   (the union of all D ranks' shards); updated in place
- *   param_replicas  host array of D device pointers, bf16, padded_numel each
- *   flags           DOPT_STEP_GATHER, DOPT_STEP_HOST_GRADS, DOPT_STEP_ROUND_GRAD
+ *   param_replicas  host array of D device pointers, bf16 (fp16 with
+ *                   DOPT_STEP_PARAMS_FP16), padded_numel each
+ *   flags           DOPT_STEP_GATHER, DOPT_STEP_HOST_GRADS, DOPT_STEP_ROUND_GRAD,
+ *                   DOPT_STEP_PARAMS_FP16
  *   main_grad_out   nullable device fp32[padded_numel]: the reduce-scattered
  *                   fp32 main grad of every owned element
  *   stream          CUDA stream to launch on

@@ -75,6 +75,55 @@ def assert_bf16_close(gpu_bits, orc_bits, what, ulps=1) -> int:
     return int(np.count_nonzero(gpu_bits[ok] != orc_bits[ok]))
 
 
+def f16_is_nan(bits):
+    bits = np.asarray(bits, np.uint16)
+    return ((bits & 0x7C00) == 0x7C00) & ((bits & 0x3FF) != 0)
+
+
+def assert_f16_close(gpu, orc, what, ulps=1) -> int:
+    """IEEE fp16 arrays (float16 or their uint16 bits) within `ulps` units
+    in the last place; NaN where the other side has NaN."""
+    gpu_bits = np.asarray(gpu).view(np.uint16) if np.asarray(gpu).dtype == np.float16 \
+        else np.asarray(gpu, np.uint16)
+    orc_bits = np.asarray(orc).view(np.uint16) if np.asarray(orc).dtype == np.float16 \
+        else np.asarray(orc, np.uint16)
+    assert gpu_bits.shape == orc_bits.shape, what
+    ng, no = f16_is_nan(gpu_bits), f16_is_nan(orc_bits)
+    assert np.array_equal(ng, no), f"{what}: NaN positions differ"
+    ok = ~no
+    d = np.abs(bf16_order_key(gpu_bits[ok]) - bf16_order_key(orc_bits[ok]))  # same sign layout
+    if (d > ulps).any():
+        idx = np.flatnonzero(ok)[d > ulps][:5]
+        raise AssertionError(f"{what}: {int((d > ulps).sum())} elements beyond {ulps} ulp, e.g. "
+                             f"index {idx.tolist()} gpu {gpu_bits[idx].tolist()} "
+                             f"oracle {orc_bits[idx].tolist()}")
+    return int(np.count_nonzero(gpu_bits[ok] != orc_bits[ok]))
+
+
+def t2np_grad(t):
+    """A grad tensor as the oracle takes it: bf16 as uint16 bits, fp16 as
+    float16, fp32 as float32 (copies)."""
+    import torch
+
+    if t.dtype == torch.bfloat16:
+        return t2np_bf16(t).copy()
+    return t.detach().cpu().numpy().copy()
+
+
+def t2np_param(t):
+    """A param replica as the oracle takes it: bf16 bits or float16."""
+    return t2np_grad(t)
+
+
+def assert_param_close(gpu_t, orc, what) -> int:
+    """A device param replica (bf16 or fp16) against the oracle's, 1 ulp."""
+    import torch
+
+    if gpu_t.dtype == torch.float16:
+        return assert_f16_close(gpu_t.detach().cpu().numpy(), orc, what)
+    return assert_bf16_close(t2np_bf16(gpu_t), orc, what)
+
+
 def merge_windows(wins, numel):
     wins = sorted((max(0, a), min(numel, b)) for a, b in wins if min(numel, b) > max(0, a))
     out = []

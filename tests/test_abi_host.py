@@ -281,3 +281,19 @@ def test_skip_nonfinite_only_on_the_clipped_step(lib):
     assert B.lib().dopt_step_clipped(L.handle, ctypes.byref(cfg), 1, 1.0, gp, 0, *st, gp, skip,
                                      0x70000, 0x80000, None, None) in (B.DOPT_E_STATE,
                                                                        B.DOPT_E_CUDA)
+
+
+def test_fp16_dtype_and_param_flag_accepted_before_cuda(lib):
+    L = _lib_layout([100, 30], 2, 0, 8)
+    cfg = B.AdamConfig().to_c()
+    gp = (ctypes.c_void_p * 2)(0x10000, 0x20000)
+    st = (0x30000, 0x40000, 0x50000)
+    flags = B.DOPT_STEP_GATHER | B.DOPT_STEP_PARAMS_FP16
+    assert B.lib().dopt_step(L.handle, ctypes.byref(cfg), 1, gp, B.DOPT_FP16, *st, gp, flags,
+                             None, None) in (B.DOPT_E_STATE, B.DOPT_E_CUDA)
+    assert B.lib().dopt_step(L.handle, ctypes.byref(cfg), 1, gp, 3, *st, gp, flags, None,
+                             None) == B.DOPT_E_ARG
+    assert B.lib().dopt_allreduce(L.handle, gp, B.DOPT_FP16, 1.0, None) in (B.DOPT_E_STATE,
+                                                                           B.DOPT_E_CUDA)
+    assert B.lib().dopt_step(L.handle, ctypes.byref(cfg), 1, gp, 0, *st, gp, 32, None,
+                             None) == B.DOPT_E_ARG

@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import oracle
-from parity import assert_bf16_close, assert_f32_close, t2np_bf16, t2np_f32
+from parity import assert_f32_close, assert_param_close, t2np_f32, t2np_grad, t2np_param
 from zero_distributed_optimizer_gb300 import binding as B
 from zero_distributed_optimizer_gb300 import workloads as W
 
@@ -36,20 +36,28 @@ def random_config(seed):
     round_grad = bool(rng.integers(0, 2))
     steps = int(rng.integers(1, 4))
     scale = float(rng.choice([1.0, 1.0 / D, 0.3]))
-    return sizes, wd, D, instances, bucket, pad, dtype, gather, round_grad, steps, scale
+    param_dtype = "bf16"
+    if seed >= 40:  # later seeds draw the 16-bit types from all of them
+        more = np.random.default_rng(20_000 + seed)
+        dtype = str(more.choice(["bf16", "fp16", "fp32"]))
+        param_dtype = str(more.choice(["bf16", "fp16"]))
+    return sizes, wd, D, instances, bucket, pad, dtype, gather, round_grad, steps, scale, \
+        param_dtype
 
 
-@pytest.mark.parametrize("seed", range(40))
+@pytest.mark.parametrize("seed", range(70))
 def test_random_parity(seed):
-    sizes, wd, D, inst, bucket, pad, dtype, gather, rg, steps, scale = random_config(seed)
+    sizes, wd, D, inst, bucket, pad, dtype, gather, rg, steps, scale, pdt = random_config(seed)
     L = B.dopt_build_range_map(sizes, D, bucket, pad, wd, instances=inst).to_device()
     N = L.padded_numel
     assert N == oracle.range_map(sizes, D // inst, bucket, pad).numel
     if N == 0:
         return
     master, m, v, params, grads = W.random_case(N, D, steps, dtype, seed)
+    if pdt == "fp16":
+        params = [p.float().half() for p in params]
     h = [master.numpy().copy(), m.numpy().copy(), v.numpy().copy()]
-    hp = [t2np_bf16(p).copy() for p in params]
+    hp = [t2np_param(p) for p in params]
     hmg = np.full(N, -3.0, np.float32)
     d = [master.to(DEV), m.to(DEV), v.to(DEV)]
     dp = [p.to(DEV) for p in params]
@@ -57,7 +65,7 @@ def test_random_parity(seed):
     adam = B.AdamConfig(grad_scale=scale)
     oadam = oracle.make_adam(**asdict(adam))
     for i in range(steps):
-        hg = [t2np_bf16(g).copy() if dtype == "bf16" else g.numpy().copy() for g in grads[i]]
+        hg = [t2np_grad(g) for g in grads[i]]
         B.dopt_step(L, adam, i + 1, [g.to(DEV) for g in grads[i]], *d, dp, gather=gather,
                     main_grad_out=dmg, round_grad=rg)
         oracle.step(sizes, wd, D, bucket, pad, oadam, i + 1, hg, *h, hp, gather=gather,
@@ -67,4 +75,4 @@ def test_random_parity(seed):
         assert_f32_close(t2np_f32(x), y, name)
     assert_f32_close(t2np_f32(dmg), hmg, "main_grad")
     for r in range(D):
-        assert_bf16_close(t2np_bf16(dp[r]), hp[r], f"param{r}")
+        assert_param_close(dp[r], hp[r], f"param{r}")

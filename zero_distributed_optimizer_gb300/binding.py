@@ -28,10 +28,12 @@ DOPT_E_NOMEM = -6
 DOPT_MAX_D = 64
 DOPT_BF16 = 0
 DOPT_FP32 = 1
+DOPT_FP16 = 2
 DOPT_STEP_GATHER = 1
 DOPT_STEP_HOST_GRADS = 2
 DOPT_STEP_ROUND_GRAD = 4
 DOPT_STEP_SKIP_NONFINITE = 8
+DOPT_STEP_PARAMS_FP16 = 16
 DOPT_CLIP_WORKSPACE_BYTES = 16384
 DOPT_STEP_COUNTER_BYTES = 64  # sizeof(dopt_step_counter)
 DOPT_COUNTER_BAD_STEP = 1
@@ -271,6 +273,29 @@ def _flags(gather: bool, host_grads: bool = False, round_grad: bool = False) -> 
             | (DOPT_STEP_ROUND_GRAD if round_grad else 0))
 
 
+def _grad_code(gdt) -> int:
+    """dopt_dtype of a torch grad dtype."""
+    import torch
+
+    codes = {torch.bfloat16: DOPT_BF16, torch.float32: DOPT_FP32, torch.float16: DOPT_FP16}
+    if gdt not in codes:
+        raise DoptError(DOPT_E_ARG, f"grad dtype {gdt} is not bf16, fp16 or fp32")
+    return codes[gdt]
+
+
+def _param_flag(param_replicas, N, device) -> int:
+    """Check the param replicas (all bf16 or all fp16) and return the flag
+    for their type."""
+    import torch
+
+    pdt = param_replicas[0].dtype
+    if pdt not in (torch.bfloat16, torch.float16):
+        raise DoptError(DOPT_E_ARG, f"param dtype {pdt} is not bf16 or fp16")
+    for i, p in enumerate(param_replicas):
+        _check_tensor(p, f"param_replicas[{i}]", pdt, N, device)
+    return DOPT_STEP_PARAMS_FP16 if pdt == torch.float16 else 0
+
+
 def _check_grads(grad_replicas, gdt, N, device, host_grads):
     """Device grads on the step's device, or (host_grads) pinned CPU tensors
     that the library reads in place."""
@@ -295,20 +320,17 @@ def _step_pointers(layout: Layout, grad_replicas, master, exp_avg, exp_avg_sq, p
     if device.type != "cuda":
         raise DoptError(DOPT_E_ARG, "the step needs CUDA tensors (no CPU path exists)")
     gdt = grad_replicas[0].dtype
-    if gdt not in (torch.bfloat16, torch.float32):
-        raise DoptError(DOPT_E_ARG, f"grad dtype {gdt} is not bf16 or fp32")
+    dt = _grad_code(gdt)
     _check_grads(grad_replicas, gdt, N, device, host_grads)
     for name, t in (("master", master), ("exp_avg", exp_avg), ("exp_avg_sq", exp_avg_sq)):
         _check_tensor(t, name, torch.float32, N, device)
-    for i, p in enumerate(param_replicas):
-        _check_tensor(p, f"param_replicas[{i}]", torch.bfloat16, N, device)
+    pflag = _param_flag(param_replicas, N, device)
     if main_grad_out is not None:
         _check_tensor(main_grad_out, "main_grad_out", torch.float32, N, device)
     gp = (ctypes.c_void_p * D)(*[g.data_ptr() for g in grad_replicas])
     pp = (ctypes.c_void_p * D)(*[p.data_ptr() for p in param_replicas])
-    dt = DOPT_BF16 if gdt == torch.bfloat16 else DOPT_FP32
     mg = None if main_grad_out is None else main_grad_out.data_ptr()
-    return device, gp, pp, dt, mg
+    return device, gp, pp, dt, mg, pflag
 
 
 def dopt_step_buckets(layout: Layout, adam: AdamConfig, step: int, first_bucket: int,
@@ -318,9 +340,9 @@ def dopt_step_buckets(layout: Layout, adam: AdamConfig, step: int, first_bucket:
     """The step over buckets [first_bucket, first_bucket + n_buckets) only."""
     import torch
 
-    device, gp, pp, dt, mg = _step_pointers(layout, grad_replicas, master, exp_avg, exp_avg_sq,
+    device, gp, pp, dt, mg, pflag = _step_pointers(layout, grad_replicas, master, exp_avg, exp_avg_sq,
                                             param_replicas, main_grad_out, host_grads)
-    flags = _flags(gather, host_grads, round_grad)
+    flags = _flags(gather, host_grads, round_grad) | pflag
     cfg = adam.to_c()
     with torch.cuda.device(device):
         _check(lib().dopt_step_buckets(
@@ -335,13 +357,14 @@ def dopt_step_allreduce(layout: Layout, adam: AdamConfig, step: int, grad_replic
     """The step that also all-reduces the grads in place (force_all_reduce)."""
     import torch
 
-    device, gp, pp, dt, mg = _step_pointers(layout, grad_replicas, master, exp_avg, exp_avg_sq,
+    device, gp, pp, dt, mg, pflag = _step_pointers(layout, grad_replicas, master, exp_avg, exp_avg_sq,
                                             param_replicas, main_grad_out)
     cfg = adam.to_c()
     with torch.cuda.device(device):
         _check(lib().dopt_step_allreduce(
             layout.handle, ctypes.byref(cfg), int(step), gp, dt, master.data_ptr(),
-            exp_avg.data_ptr(), exp_avg_sq.data_ptr(), pp, _flags(gather, round_grad=round_grad),
+            exp_avg.data_ptr(), exp_avg_sq.data_ptr(), pp,
+            _flags(gather, round_grad=round_grad) | pflag,
             mg, _stream_handle(stream)))
 
 
@@ -357,15 +380,13 @@ def dopt_allreduce(layout: Layout, grad_replicas, grad_scale: float, stream=None
     if device.type != "cuda":
         raise DoptError(DOPT_E_ARG, "dopt_allreduce needs CUDA tensors")
     gdt = grad_replicas[0].dtype
-    if gdt not in (torch.bfloat16, torch.float32):
-        raise DoptError(DOPT_E_ARG, f"grad dtype {gdt} is not bf16 or fp32")
+    dt = _grad_code(gdt)
     for i, g in enumerate(grad_replicas):
         _check_tensor(g, f"grad_replicas[{i}]", gdt, layout.padded_numel, device)
     gp = (ctypes.c_void_p * D)(*[g.data_ptr() for g in grad_replicas])
     with torch.cuda.device(device):
-        _check(lib().dopt_allreduce(layout.handle, gp,
-                                    DOPT_BF16 if gdt == torch.bfloat16 else DOPT_FP32,
-                                    float(grad_scale), _stream_handle(stream)))
+        _check(lib().dopt_allreduce(layout.handle, gp, dt, float(grad_scale),
+                                    _stream_handle(stream)))
 
 
 def dopt_step(layout: Layout, adam: AdamConfig, step: int, grad_replicas, master, exp_avg,
@@ -381,9 +402,9 @@ def dopt_step(layout: Layout, adam: AdamConfig, step: int, grad_replicas, master
     """
     import torch
 
-    device, gp, pp, dt, mg = _step_pointers(layout, grad_replicas, master, exp_avg, exp_avg_sq,
+    device, gp, pp, dt, mg, pflag = _step_pointers(layout, grad_replicas, master, exp_avg, exp_avg_sq,
                                             param_replicas, main_grad_out, host_grads)
-    flags = _flags(gather, host_grads, round_grad)
+    flags = _flags(gather, host_grads, round_grad) | pflag
     cfg = adam.to_c()
     with torch.cuda.device(device):
         _check(lib().dopt_step(layout.handle, ctypes.byref(cfg), int(step), gp, dt,
@@ -429,10 +450,10 @@ def dopt_step_counted(layout: Layout, adam: AdamConfig, counter, grad_replicas, 
     so they can be captured once in a CUDA graph and replayed every step."""
     import torch
 
-    device, gp, pp, dt, mg = _step_pointers(layout, grad_replicas, master, exp_avg, exp_avg_sq,
+    device, gp, pp, dt, mg, pflag = _step_pointers(layout, grad_replicas, master, exp_avg, exp_avg_sq,
                                             param_replicas, main_grad_out, host_grads)
     _check_counter(counter, master.device)
-    flags = _flags(gather, host_grads, round_grad)
+    flags = _flags(gather, host_grads, round_grad) | pflag
     cfg = adam.to_c()
     with torch.cuda.device(device):
         _check(lib().dopt_step_counted(layout.handle, ctypes.byref(cfg), counter.data_ptr(), gp,
@@ -453,14 +474,14 @@ class StepPlan:
                  host_grads: bool = False, round_grad: bool = False, stream=None):
         import torch
 
-        self.device, self._gp, self._pp, self._dt, self._mg = _step_pointers(
+        self.device, self._gp, self._pp, self._dt, self._mg, pflag = _step_pointers(
             layout, grad_replicas, master, exp_avg, exp_avg_sq, param_replicas, main_grad_out,
             host_grads)
         self.layout = layout
         self._keep = (list(grad_replicas), master, exp_avg, exp_avg_sq, list(param_replicas),
                       main_grad_out)
         self._state = (master.data_ptr(), exp_avg.data_ptr(), exp_avg_sq.data_ptr())
-        self._flags = _flags(gather, host_grads, round_grad)
+        self._flags = _flags(gather, host_grads, round_grad) | pflag
         self._cfg = adam.to_c()
         with torch.cuda.device(self.device):
             self._stream = _stream_handle(stream)
@@ -502,8 +523,8 @@ class HostStepper:
 
         if host_params_out.device.type != "cpu" or not host_params_out.is_pinned():
             raise DoptError(DOPT_E_ARG, "host_params_out must be a pinned CPU tensor")
-        _check_tensor(host_params_out, "host_params_out", torch.bfloat16, layout.padded_numel,
-                      host_params_out.device)
+        _check_tensor(host_params_out, "host_params_out", param_replicas[0].dtype,
+                      layout.padded_numel, host_params_out.device)
         self.layout, self.adam = layout, adam
         self.state = (master, exp_avg, exp_avg_sq)
         self.params = list(param_replicas)
@@ -585,15 +606,13 @@ def dopt_step_clipped(layout: Layout, adam: AdamConfig, step: int, max_norm: flo
     if device.type != "cuda":
         raise DoptError(DOPT_E_ARG, "dopt_step_clipped needs CUDA tensors (no CPU path exists)")
     gdt = grad_replicas[0].dtype
-    if gdt not in (torch.bfloat16, torch.float32):
-        raise DoptError(DOPT_E_ARG, f"grad dtype {gdt} is not bf16 or fp32")
+    dt = _grad_code(gdt)
     for i, g in enumerate(grad_replicas):
         _check_tensor(g, f"grad_replicas[{i}]", gdt, N, device)
     for name, t in (("master", master), ("exp_avg", exp_avg), ("exp_avg_sq", exp_avg_sq),
                     ("main_grad", main_grad)):
         _check_tensor(t, name, torch.float32, N, device)
-    for i, p in enumerate(param_replicas):
-        _check_tensor(p, f"param_replicas[{i}]", torch.bfloat16, N, device)
+    pflag = _param_flag(param_replicas, N, device)
     _check_tensor(workspace, "workspace", torch.uint8, DOPT_CLIP_WORKSPACE_BYTES, device)
     if norm_out is not None:
         _check_tensor(norm_out, "norm_out", torch.float32, 4 if skip_nonfinite else 2, device)
@@ -603,9 +622,9 @@ def dopt_step_clipped(layout: Layout, adam: AdamConfig, step: int, max_norm: flo
     with torch.cuda.device(device):
         _check(lib().dopt_step_clipped(
             layout.handle, ctypes.byref(cfg), int(step), float(max_norm), gp,
-            DOPT_BF16 if gdt == torch.bfloat16 else DOPT_FP32, master.data_ptr(),
+            dt, master.data_ptr(),
             exp_avg.data_ptr(), exp_avg_sq.data_ptr(), pp,
-            _flags(gather, round_grad=round_grad)
+            _flags(gather, round_grad=round_grad) | pflag
             | (DOPT_STEP_SKIP_NONFINITE if skip_nonfinite else 0),
             main_grad.data_ptr(), workspace.data_ptr(),
             None if norm_out is None else norm_out.data_ptr(), _stream_handle(stream)))
@@ -629,15 +648,13 @@ def dopt_step_clipped_noalloc(layout: Layout, adam: AdamConfig, step: int, max_n
     if device.type != "cuda":
         raise DoptError(DOPT_E_ARG, "dopt_step_clipped_noalloc needs CUDA tensors")
     gdt = grad_replicas[0].dtype
-    if gdt not in (torch.bfloat16, torch.float32):
-        raise DoptError(DOPT_E_ARG, f"grad dtype {gdt} is not bf16 or fp32")
+    dt = _grad_code(gdt)
     for i, g in enumerate(grad_replicas):
         _check_tensor(g, f"grad_replicas[{i}]", gdt, N, device)
     for name, t in (("master", master), ("exp_avg", exp_avg), ("exp_avg_sq", exp_avg_sq),
                     ("main_grad", main_grad)):
         _check_tensor(t, name, torch.float32, N, device)
-    for i, p in enumerate(param_replicas):
-        _check_tensor(p, f"param_replicas[{i}]", torch.bfloat16, N, device)
+    pflag = _param_flag(param_replicas, N, device)
     if norm_out is not None:
         _check_tensor(norm_out, "norm_out", torch.float32, 2, device)
     gp = (ctypes.c_void_p * D)(*[g.data_ptr() for g in grad_replicas])
@@ -646,8 +663,9 @@ def dopt_step_clipped_noalloc(layout: Layout, adam: AdamConfig, step: int, max_n
     with torch.cuda.device(device):
         _check(lib().dopt_step_clipped_noalloc(
             layout.handle, ctypes.byref(cfg), int(step), float(max_norm), gp,
-            DOPT_BF16 if gdt == torch.bfloat16 else DOPT_FP32, master.data_ptr(),
-            exp_avg.data_ptr(), exp_avg_sq.data_ptr(), pp, DOPT_STEP_GATHER if gather else 0,
+            dt, master.data_ptr(),
+            exp_avg.data_ptr(), exp_avg_sq.data_ptr(), pp,
+            (DOPT_STEP_GATHER if gather else 0) | pflag,
             main_grad.data_ptr(), None if norm_out is None else norm_out.data_ptr(),
             _stream_handle(stream)))
 
@@ -662,8 +680,7 @@ def dopt_gather(layout: Layout, param_replicas, stream=None) -> None:
     device = param_replicas[0].device
     if device.type != "cuda":
         raise DoptError(DOPT_E_ARG, "dopt_gather needs CUDA tensors")
-    for i, p in enumerate(param_replicas):
-        _check_tensor(p, f"param_replicas[{i}]", torch.bfloat16, layout.padded_numel, device)
+    _param_flag(param_replicas, layout.padded_numel, device)  # bf16 or fp16: 16-bit copies
     pp = (ctypes.c_void_p * D)(*[p.data_ptr() for p in param_replicas])
     with torch.cuda.device(device):
         _check(lib().dopt_gather(layout.handle, pp, _stream_handle(stream)))

@@ -32,7 +32,10 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <type_traits>
+
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "dopt_internal.h"
@@ -148,6 +151,7 @@ struct StepArgs {
     int32_t gather;
     int32_t round_grad;  // round the reduced grad to the grad type first
     int32_t skip_nonfinite;  // kFromMain: a NaN coefficient means store nothing
+    int32_t param_f16;       // the param replicas hold fp16 (else bf16)
     Scalars sc;
 };
 
@@ -236,12 +240,39 @@ __device__ __forceinline__ uint16_t to_bf16_bits(float x) {
     return *reinterpret_cast<uint16_t *>(&h);
 }
 
-// A reduced grad in the grad buffer's type: bf16 rounds to nearest even,
-// fp32 is already in its type.
+// IEEE fp16: conversions to and from fp32 (round to nearest even, Inf on
+// overflow; widening is exact).
+__device__ __forceinline__ uint16_t to_f16_bits(float x) { return __half_as_ushort(__float2half_rn(x)); }
+__device__ __forceinline__ float f16_to_float(uint16_t h) { return __half2float(__ushort_as_half(h)); }
+
+__device__ __forceinline__ void unpack_f16x8(const uint4 &raw, float (&f)[8]) {
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float2 p = __half22float2(*reinterpret_cast<const __half2 *>(&w[k]));
+        f[2 * k] = p.x;
+        f[2 * k + 1] = p.y;
+    }
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ uint4 pack_f16x8(const float (&f)[8]) {
+    return make_uint4(pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]), pack_f16x2(f[4], f[5]),
+                      pack_f16x2(f[6], f[7]));
+}
+
+// A reduced grad in the grad buffer's type: bf16 and fp16 round to nearest
+// even, fp32 is already in its type.
 template <typename G>
 __device__ __forceinline__ float to_grad_type(float g) {
-    if constexpr (sizeof(G) == 2)
+    if constexpr (std::is_same_v<G, __nv_bfloat16>)
         return __uint_as_float(uint32_t(to_bf16_bits(g)) << 16);
+    else if constexpr (std::is_same_v<G, __half>)
+        return f16_to_float(to_f16_bits(g));
     else
         return g;
 }
@@ -325,23 +356,40 @@ __device__ __forceinline__ bool owned_at(const RunView &v, int64_t e, int &j, bo
 
 template <typename G>
 __device__ __forceinline__ float load_grad_scalar(const void *base, int64_t i) {
-    if constexpr (sizeof(G) == 2)
+    if constexpr (std::is_same_v<G, __nv_bfloat16>)
         return __uint_as_float(uint32_t(__ldcs(static_cast<const unsigned short *>(base) + i)) << 16);
+    else if constexpr (std::is_same_v<G, __half>)
+        return f16_to_float(__ldcs(static_cast<const unsigned short *>(base) + i));
     else
         return __ldcs(static_cast<const float *>(base) + i);
 }
 
 template <typename G>
 __device__ __forceinline__ void store_grad_scalar(const void *base, int64_t i, float g) {
-    if constexpr (sizeof(G) == 2)
+    if constexpr (std::is_same_v<G, __nv_bfloat16>)
         static_cast<uint16_t *>(const_cast<void *>(base))[i] = to_bf16_bits(g);
+    else if constexpr (std::is_same_v<G, __half>)
+        static_cast<uint16_t *>(const_cast<void *>(base))[i] = to_f16_bits(g);
     else
         static_cast<float *>(const_cast<void *>(base))[i] = g;
 }
 
-// Load the 8 grads of replica r at e0 (bf16: one 16-byte load; fp32: two).
+// Load the 8 grads of replica r at e0 (16-bit types: one 16-byte load; fp32:
+// two).
 template <typename G>
 struct GradVec;
+
+template <>
+struct GradVec<__half> {
+    uint4 a;
+    __device__ __forceinline__ void load(const void *base, int64_t e0) {
+        a = ld_stream(static_cast<const __half *>(base) + e0);
+    }
+    __device__ __forceinline__ void get(float (&f)[8]) const { unpack_f16x8(a, f); }
+    __device__ __forceinline__ static void store(const void *base, int64_t e0, const float (&f)[8]) {
+        st_stream(static_cast<__half *>(const_cast<void *>(base)) + e0, pack_f16x8(f));
+    }
+};
 
 template <>
 struct GradVec<__nv_bfloat16> {
@@ -499,7 +547,7 @@ __device__ __forceinline__ void full_vector(const StepArgs &a, const Scalars &sc
         st_stream_f4(a.main_grad_out + e0 + 4, make_float4(acc[4], acc[5], acc[6], acc[7]));
     }
 
-    const uint4 packed = pack_bf16x8(w);
+    const uint4 packed = a.param_f16 ? pack_f16x8(w) : pack_bf16x8(w);
     if (a.gather) {
         if constexpr (DC > 0) {
 #pragma unroll
@@ -543,7 +591,7 @@ __device__ __noinline__ void mixed_vector(const StepArgs &a, const Scalars &sc, 
         a.exp_avg[e] = m;
         a.exp_avg_sq[e] = v;
         if (MODE != kFromMain && a.main_grad_out) a.main_grad_out[e] = g;
-        const uint16_t bits = to_bf16_bits(w);
+        const uint16_t bits = a.param_f16 ? to_f16_bits(w) : to_bf16_bits(w);
         if (a.gather) {
             for (int r = 0; r < D; ++r) static_cast<uint16_t *>(a.params[r])[e] = bits;
         } else {

@@ -9,6 +9,7 @@
 #include <vector>
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <nvtx3/nvToolsExt.h>
 
@@ -77,8 +78,11 @@ int kernel_D(const dopt_layout *L) { return L->cfg.instances > 1 ? 0 : L->cfg.D;
 
 template <int MODE>
 StepKernel step_kernel_for(dopt_dtype grad_dtype, int D) {
-    return grad_dtype == DOPT_BF16 ? pick_step_kernel<__nv_bfloat16, MODE>(D)
-                                   : pick_step_kernel<float, MODE>(D);
+    switch (grad_dtype) {
+        case DOPT_BF16: return pick_step_kernel<__nv_bfloat16, MODE>(D);
+        case DOPT_FP16: return pick_step_kernel<__half, MODE>(D);
+        default: return pick_step_kernel<float, MODE>(D);
+    }
 }
 
 template <typename G>
@@ -94,7 +98,11 @@ NormKernel pick_norm_kernel(int D) {
 }
 
 NormKernel norm_kernel_for(dopt_dtype grad_dtype, int D) {
-    return grad_dtype == DOPT_BF16 ? pick_norm_kernel<__nv_bfloat16>(D) : pick_norm_kernel<float>(D);
+    switch (grad_dtype) {
+        case DOPT_BF16: return pick_norm_kernel<__nv_bfloat16>(D);
+        case DOPT_FP16: return pick_norm_kernel<__half>(D);
+        default: return pick_norm_kernel<float>(D);
+    }
 }
 
 template <typename G>
@@ -181,9 +189,10 @@ int check_step_args(const char *who, const dopt_layout *L, const dopt_adam_cfg *
     if (!L || !cfg || !grad_replicas || !param_replicas || !master || !exp_avg || !exp_avg_sq)
         return fail(DOPT_E_ARG, "%s: NULL argument", who);
     if (step < 1) return fail(DOPT_E_ARG, "%s: step=%lld < 1", who, (long long)step);
-    if (grad_dtype != DOPT_BF16 && grad_dtype != DOPT_FP32)
+    if (grad_dtype != DOPT_BF16 && grad_dtype != DOPT_FP32 && grad_dtype != DOPT_FP16)
         return fail(DOPT_E_ARG, "%s: unknown grad dtype %d", who, int(grad_dtype));
-    if (flags & ~(uint32_t(DOPT_STEP_GATHER | DOPT_STEP_HOST_GRADS | DOPT_STEP_ROUND_GRAD) |
+    if (flags & ~(uint32_t(DOPT_STEP_GATHER | DOPT_STEP_HOST_GRADS | DOPT_STEP_ROUND_GRAD |
+                           DOPT_STEP_PARAMS_FP16) |
                   extra_flags))
         return fail(DOPT_E_ARG, "%s: unknown flags 0x%x", who, flags);
     if (!(cfg->lr >= 0.0f) || !std::isfinite(cfg->lr) || !(cfg->beta1 >= 0.0f && cfg->beta1 < 1.0f) ||
@@ -244,6 +253,7 @@ void fill_step_args(StepArgs &a, const dopt_layout *L, const dopt_adam_cfg *cfg,
     a.R = L->R;
     a.gather = (flags & DOPT_STEP_GATHER) ? 1 : 0;
     a.round_grad = (flags & DOPT_STEP_ROUND_GRAD) ? 1 : 0;
+    a.param_f16 = (flags & DOPT_STEP_PARAMS_FP16) ? 1 : 0;
     a.sc = scalars_for(*cfg, step);
 }
 
@@ -442,7 +452,7 @@ extern "C" int dopt_allreduce(const dopt_layout *L, void *const *grad_replicas,
     const char *who = "dopt_allreduce";
     NvtxRange range(who);
     if (!L || !grad_replicas) return fail(DOPT_E_ARG, "%s: NULL argument", who);
-    if (grad_dtype != DOPT_BF16 && grad_dtype != DOPT_FP32)
+    if (grad_dtype != DOPT_BF16 && grad_dtype != DOPT_FP32 && grad_dtype != DOPT_FP16)
         return fail(DOPT_E_ARG, "%s: unknown grad dtype %d", who, int(grad_dtype));
     if (!std::isfinite(grad_scale)) return fail(DOPT_E_ARG, "%s: grad_scale not finite", who);
     const int D = L->cfg.D;
@@ -458,8 +468,9 @@ extern "C" int dopt_allreduce(const dopt_layout *L, void *const *grad_replicas,
     a.D = D;
     a.R = L->R;
     a.scale = grad_scale;
-    AllReduceKernel k = grad_dtype == DOPT_BF16 ? pick_allreduce_kernel<__nv_bfloat16>(kernel_D(L))
-                                                : pick_allreduce_kernel<float>(kernel_D(L));
+    AllReduceKernel k = grad_dtype == DOPT_BF16   ? pick_allreduce_kernel<__nv_bfloat16>(kernel_D(L))
+                        : grad_dtype == DOPT_FP16 ? pick_allreduce_kernel<__half>(kernel_D(L))
+                                                  : pick_allreduce_kernel<float>(kernel_D(L));
     k<<<unsigned(tiles), kThreads, 0, stream>>>(a);
     return launch_error(who, "all-reduce");
 }

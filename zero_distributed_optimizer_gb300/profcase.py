@@ -60,6 +60,9 @@ def main(argv=None):
                     help="buckets mode: bucket k is launched on stream k mod STREAMS")
     ap.add_argument("--plan", action="store_true",
                     help="step and buckets modes: launch through a StepPlan")
+    ap.add_argument("--grad-dtype", choices=["bf16", "fp16", "fp32"], default=None,
+                    help="override the workload's grad type")
+    ap.add_argument("--param-dtype", choices=["bf16", "fp16"], default="bf16")
     args = ap.parse_args(argv)
 
     libbuild.build()
@@ -68,6 +71,8 @@ def main(argv=None):
     else:
         w = getattr(W, args.workload)()
     w = truncated(w, args.max_elems)
+    if args.grad_dtype:
+        w = w.with_(grad_dtype=args.grad_dtype)
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     L = B.dopt_build_range_map(list(w.sizes), w.D, w.bucket_elems, w.pad_unit,
@@ -75,6 +80,8 @@ def main(argv=None):
     N = L.padded_numel
     master, m, v = W.make_state(w, N, dev)
     params = W.make_params(master, w.D)
+    if args.param_dtype == "fp16":
+        params = [p.float().half() for p in params]
     grads = W.make_grads(w, N, 1, dev)
     adam = B.AdamConfig(**w.adam_kwargs())
     if args.mode == "clipped":
@@ -148,7 +155,8 @@ def main(argv=None):
                 "step_allreduce": step_bytes + w.D * w.grad_bytes}[args.mode]
     bytes_per = w.numel * per_elem
     print(json.dumps({"workload": w.name, "N": w.numel, "padded_numel": N, "D": w.D,
-                      "mode": args.mode, "n_buckets": L.n_buckets, "streams": args.streams, "plan": args.plan,
+                      "mode": args.mode, "grad_dtype": w.grad_dtype, "param_dtype": args.param_dtype,
+                      "n_buckets": L.n_buckets, "streams": args.streams, "plan": args.plan,
                       "launches": args.launches, "ms_per_launch": ms,
                       "algorithmic_bytes_per_launch": bytes_per,
                       "gbs": bytes_per / (ms / 1e3) / 1e9}))

@@ -40,7 +40,7 @@ class Workload:
     D: int
     bucket_elems: int       # 0: one bucket
     pad_unit: int
-    grad_dtype: str         # "bf16" or "fp32"
+    grad_dtype: str         # "bf16", "fp16" or "fp32"
     grad_dist: str          # "uniform1", "normal1e-3", "normal1e-3_outliers"
     m_init: str             # "zero" or "normal1e-4"
     v_init: str             # "zero" or "absnormal1e-6"
@@ -60,7 +60,7 @@ class Workload:
 
     @property
     def grad_bytes(self) -> int:
-        return 2 if self.grad_dtype == "bf16" else 4
+        return 4 if self.grad_dtype == "fp32" else 2
 
     def adam_kwargs(self) -> dict:
         return dict(lr=self.lr, beta1=self.beta1, beta2=self.beta2, eps=self.eps,
@@ -68,7 +68,7 @@ class Workload:
 
     def algorithmic_bytes_per_element(self) -> int:
         """Bytes one element moves: D grads read, master/m/v read+written,
-        D bf16 params written."""
+        D 16-bit params written."""
         return self.D * self.grad_bytes + 24 + 2 * self.D
 
     def with_(self, **kw) -> "Workload":
@@ -228,7 +228,7 @@ def make_grads(w: Workload, numel: int, t: int, device="cpu", ranks=None):
             if w.grad_dist == "normal1e-3_outliers":
                 hit = torch.rand(numel, generator=g, device=device, dtype=torch.float32) < 0.01
                 x = torch.where(hit, x * 100, x)
-        out.append(x.to(torch.bfloat16) if w.grad_dtype == "bf16" else x)
+        out.append(_to_grad_dtype(torch, x, w.grad_dtype))
         del x
     return out
 
@@ -258,6 +258,11 @@ def make_params(master, D: int):
     return [p.clone() for _ in range(D)]
 
 
+def _to_grad_dtype(torch, x, grad_dtype: str):
+    """fp32 draws cast to the grads' type ("bf16", "fp16" or "fp32")."""
+    return x.to({"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}[grad_dtype])
+
+
 def random_case(numel: int, D: int, steps: int, grad_dtype: str = "bf16", seed: int = 0):
     """Seeded inputs for a small parity case (CPU tensors): fp32 master/m/v,
     D distinct random bf16 replicas (so untouched padding is visible) and
@@ -279,6 +284,6 @@ def random_case(numel: int, D: int, steps: int, grad_dtype: str = "bf16", seed: 
             x = torch.where(u < 0.01, x * 1000, x)
             x = torch.where((u >= 0.01) & (u < 0.02), torch.zeros_like(x), x)
             x = torch.where((u >= 0.02) & (u < 0.03), x * 1e-7, x)
-            per_rank.append(x.to(torch.bfloat16) if grad_dtype == "bf16" else x)
+            per_rank.append(_to_grad_dtype(torch, x, grad_dtype))
         grads.append(per_rank)
     return master, m, v, params, grads
