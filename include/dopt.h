@@ -325,7 +325,8 @@ int dopt_step_counted(const dopt_layout *layout, const dopt_adam_cfg *cfg,
  * distributed-training tutorial, "AllReduce" = reduce-scatter followed by
  * all-gather).  For every owned element i:
  *     g = fp32 sum over r in rank order of grad_scale * float(grad_replicas[r][i])
- *     grad_replicas[r][i] = g rounded to the grad type (bf16: nearest even)
+ *     grad_replicas[r][i] = g rounded to the grad type (bf16, fp16: nearest
+ *                           even)
  * for every r, in place.  Padding is not written.
  *   grad_replicas  host array of D device pointers (16-byte aligned),
  *                  padded_numel elements of grad_dtype each; read and written
@@ -350,8 +351,9 @@ int dopt_step_allreduce(const dopt_layout *layout, const dopt_adam_cfg *cfg, int
 /*
  * The all-gather of the params on its own (page 1, §4.4): for every rank q
  * and every element q owns, copy param_replicas[q][i] into every other
- * replica of q's instance.  Padding is not copied.  param_replicas: host array of D device
- * bf16 pointers (16-byte aligned).  Asynchronous on `stream`.
+ * replica of q's instance.  Padding is not copied.  param_replicas: host
+ * array of D device pointers to 16-bit params (bf16 or fp16: the copy does
+ * not look at the values), 16-byte aligned.  Asynchronous on `stream`.
  * Errors: DOPT_E_ARG, DOPT_E_ALIGN, DOPT_E_STATE, DOPT_E_CUDA.
  */
 int dopt_gather(const dopt_layout *layout, void *const *param_replicas, cudaStream_t stream);
