@@ -299,11 +299,14 @@ typedef struct {
 
 /*
  * dopt_step with the step number taken from a counter in device memory
- * instead of a host argument, and the counter advanced on the device.  One
- * kernel of one thread reads counter->next_step = t, evaluates the step's
- * scalars (the same double-precision expressions as dopt_step, there with
- * the device's pow and sqrt) into counter->scratch and stores t + 1; then
- * the step kernel of dopt_step runs with those scalars.  The launches and
+ * instead of a host argument, and the counter advanced on the device.  A
+ * kernel of two threads reads counter->next_step = t, evaluates the step's
+ * scalars (the same double-precision operations as dopt_step, on the
+ * device) into counter->scratch and stores t + 1; then the step kernel of
+ * dopt_step runs with those scalars.  The first kernel is launched as a
+ * programmatic dependent of the kernel before it on the stream: it may start
+ * early, but it reads the final counter and writes only after that kernel
+ * has completed.  The launches and
  * their arguments do not depend on t, so a sequence captured once (a CUDA
  * graph) replays every later step.  The pages describe no such counter:
  * it is an addition of this library for graph replay.

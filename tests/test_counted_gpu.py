@@ -226,3 +226,48 @@ def test_counted_capture_as_first_use():
     out = subprocess.run([sys.executable, "-c", FIRST_USE], capture_output=True, text=True,
                          timeout=300, cwd=root)
     assert out.returncode == 0 and out.stdout.strip().endswith("ok"), out.stdout + out.stderr
+
+
+def test_several_counted_steps_in_one_graph():
+    """Four counted steps captured in one graph (each counter kernel a
+    programmatic dependent of the step kernel before it), replayed three
+    times, with the counter moved by the caller between replays, equal host
+    steps at the same step numbers."""
+    L, s, p, g, _ = _case([65536, 1000, 65536, 3], [1, 0, 1, 0], 8, 0, 64, steps=1, seed=18)
+    s2, p2 = _clone(s, p)
+    adam = B.AdamConfig(grad_scale=1.0 / 8)
+    ws, wp = _clone(s, p)
+    B.dopt_step_counted(L, adam, B.step_counter(1), g[0], *ws, wp)  # kernels loaded
+    torch.cuda.synchronize()
+    counter = B.step_counter(1)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(4):
+            B.dopt_step_counted(L, adam, counter, g[0], *s2, p2)
+    numbers = []
+    for start in (1, 100, 5):
+        counter[0] = start
+        graph.replay()
+        numbers += list(range(start, start + 4))
+    for t in numbers:
+        B.dopt_step(L, adam, t, g[0], *s, p)
+    torch.cuda.synchronize()
+    _equal(s + p, s2 + p2)
+    assert B.counter_state(counter) == (9, 0)
+
+
+def test_counted_after_a_counter_write_on_the_stream():
+    """A caller's kernel that rewrites the counter right before the counted
+    step: the counter kernel, started early, must use the rewritten number."""
+    L, s, p, g, _ = _case([3000, 17, 2500], [1, 0, 1], 2, 0, 8, steps=1, seed=21)
+    s2, p2 = _clone(s, p)
+    adam = B.AdamConfig(lr=2e-3, grad_scale=0.5)
+    counter = B.step_counter(1)
+    for t in (7, 8, 1234, 3):
+        counter.fill_(t)  # the last 7 elements are scratch: zeroed or rewritten by the step
+        counter[1:].zero_()
+        B.dopt_step_counted(L, adam, counter, g[0], *s2, p2)
+        B.dopt_step(L, adam, t, g[0], *s, p)
+    torch.cuda.synchronize()
+    _equal(s + p, s2 + p2)
+    assert B.counter_state(counter) == (4, 0)

@@ -605,6 +605,9 @@ template <typename G, int DC, int MODE>
 __global__ void __launch_bounds__(kThreads) dopt_step_kernel(const __grid_constant__ StepArgs a) {
     int j;
     if constexpr (MODE == kCounted) {
+        // let the next counted step's counter kernel start (it waits for this
+        // grid to complete before it writes the counter)
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         // One read of the counter per CTA (every CTA of the grid needs the
         // same line), issued before the run lookup so that the waits
         // overlap.  (A persistent grid that reads it once per CTA of a few
@@ -638,16 +641,30 @@ __global__ void __launch_bounds__(kThreads) dopt_step_kernel(const __grid_consta
     }
 }
 
-// First launch of dopt_step_counted, one warp: the step number from the
-// counter, its scalars (lanes 0 and 1 evaluate the two slow double-precision
-// ones side by side), the counter advanced, or the bad number reported.
+// The slow double-precision scalar of lane 0 (step size) or lane 1
+// (sqrt of the second bias correction) for step t.
+__device__ __forceinline__ float counted_scalar(const dopt_adam_cfg &cfg, int64_t t, int lane) {
+    if (t < 1 || t > kMaxCountedStep) return 0.0f;
+    return lane == 0 ? step_size_for(cfg, t) : bc2_sqrt_for(cfg, t);
+}
+
+// First launch of dopt_step_counted, one warp of two lanes: the step number
+// from the counter, its scalars (the lanes evaluate the two slow
+// double-precision ones side by side), the counter advanced, or the bad
+// number reported.  It is launched as a programmatic dependent of the
+// previous kernel on the stream (the step kernel of the step before, which
+// lets it start once all its CTAs run): it evaluates the scalars for the
+// number it reads then, waits for the previous grid to complete, reads the
+// number again and evaluates once more only if it changed, so the slow part
+// overlaps the previous step's last wave.
 __global__ void dopt_count_step_kernel(CounterBlock *c, const dopt_adam_cfg cfg) {
-    const int64_t t = c->next_step;
     const int lane = threadIdx.x;
+    const int64_t guess = __ldcg(&c->next_step);
+    float x = counted_scalar(cfg, guess, lane);
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the grids before: complete, visible
+    const int64_t t = __ldcg(&c->next_step);
+    if (t != guess) x = counted_scalar(cfg, t, lane);
     const bool bad = t < 1 || t > kMaxCountedStep;
-    float x = 0.0f;
-    if (!bad && lane == 0) x = step_size_for(cfg, t);
-    if (!bad && lane == 1) x = bc2_sqrt_for(cfg, t);
     const float bc2_sqrt = __shfl_sync(0x3u, x, 1);
     if (lane != 0) return;
     if (bad) {

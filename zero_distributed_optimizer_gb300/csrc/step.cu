@@ -419,7 +419,24 @@ extern "C" int dopt_step_counted(const dopt_layout *L, const dopt_adam_cfg *cfg,
                       exp_avg, exp_avg_sq, param_replicas, flags, main_grad_out, a, &tiles);
     if (rc != DOPT_OK) return rc;
     CounterBlock *c = reinterpret_cast<CounterBlock *>(counter);
-    dopt_count_step_kernel<<<1, 2, 0, stream>>>(c, *cfg);
+    // a programmatic dependent of the kernel before it on the stream (see
+    // dopt_count_step_kernel)
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(1);
+    lc.blockDim = dim3(2);
+    lc.dynamicSmemBytes = 0;
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    const dopt_adam_cfg cfg_copy = *cfg;
+    cudaError_t le = cudaLaunchKernelEx(&lc, dopt_count_step_kernel, c, cfg_copy);
+    if (le != cudaSuccess) {
+        cudaGetLastError();
+        return fail(DOPT_E_CUDA, "%s: counter launch: %s", who, cudaGetErrorString(le));
+    }
     rc = launch_error(who, "counter");
     if (rc != DOPT_OK || tiles == 0) return rc;
     a.counter = c;
