@@ -688,8 +688,11 @@ __global__ void dopt_count_step_kernel(CounterBlock *c, const dopt_adam_cfg cfg)
 // replica, rounded to the grad type.
 // ---------------------------------------------------------------------------
 
+// The same launch bounds as the step kernel: 0.6 % faster at D = 8 and
+// 0.3 % at D = 16.  (The gather kernel keeps the default: 3 CTAs per SM
+// helped at D = 8 by 0.5 % and cost 4 % at D = 4.)
 template <typename G, int DC>
-__global__ void __launch_bounds__(kThreads) dopt_allreduce_kernel(const __grid_constant__ AllReduceArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) dopt_allreduce_kernel(const __grid_constant__ AllReduceArgs a) {
     const int64_t tile = a.rv.tile0 + blockIdx.x;
     const int64_t e0 = tile * kDoptTileElems + int64_t(threadIdx.x) * kVec;
     int j;
