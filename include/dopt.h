@@ -286,7 +286,8 @@ int dopt_step_buckets(const dopt_layout *layout, const dopt_adam_cfg *cfg, int64
  *   status     written by every launch: 0, or DOPT_COUNTER_BAD_STEP when
  *              next_step was outside 1 .. 2^62; such a launch changes
  *              nothing else (not the counter, the state or the params).
- *   scratch    the library's: the Adam scalars of the step last taken.
+ *   scratch    the library's: the two Adam scalars that depend on the step
+ *              number, for the step last taken, and a copy of the status.
  */
 typedef struct {
     int64_t next_step;
@@ -301,9 +302,9 @@ typedef struct {
  * dopt_step with the step number taken from a counter in device memory
  * instead of a host argument, and the counter advanced on the device.  A
  * kernel of two threads reads counter->next_step = t, evaluates the step's
- * scalars (the same double-precision operations as dopt_step, on the
- * device) into counter->scratch and stores t + 1; then the step kernel of
- * dopt_step runs with those scalars.  The first kernel is launched as a
+ * scalars that depend on t (the same double-precision operations as
+ * dopt_step, on the device) into counter->scratch and stores t + 1; then
+ * the step kernel of dopt_step runs with those scalars.  The first kernel is launched as a
  * programmatic dependent of the kernel before it on the stream: it may start
  * early, but it reads the final counter and writes only after that kernel
  * has completed.  The launches and
