@@ -132,6 +132,7 @@ struct RunView {
     const int32_t *tile_run;
     int64_t numel;
     int64_t tile0;
+    int64_t lo, hi;  // [start of the first run, end of the last run) of the view
     int32_t run_begin;
     int32_t run_limit;
 };
@@ -438,6 +439,22 @@ struct GradVec<float> {
 // group of R consecutive replicas in rank order and adds the groups' sums in
 // group order (several optimizer instances; with R = D the last group's sum
 // is copied, so the result is the plain rank-order sum).
+// The compile-time-D reduction of 8 elements from replicas already loaded.
+template <typename G, int DC>
+__device__ __forceinline__ void reduce_loaded(const GradVec<G> (&g)[DC], float scale,
+                                              float (&acc)[8]) {
+#pragma unroll
+    for (int r = 0; r < DC; ++r) {
+        float f[8];
+        g[r].get(f);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float x = __fmul_rn(scale, f[k]);
+            acc[k] = r == 0 ? x : __fadd_rn(acc[k], x);
+        }
+    }
+}
+
 template <typename G, int DC, typename Args>
 __device__ __forceinline__ void reduce_vec(const Args &a, float scale, int64_t e0,
                                            float (&acc)[8]) {
@@ -445,16 +462,7 @@ __device__ __forceinline__ void reduce_vec(const Args &a, float scale, int64_t e
         GradVec<G> g[DC];
 #pragma unroll
         for (int r = 0; r < DC; ++r) g[r].load(a.grads[r], e0);
-#pragma unroll
-        for (int r = 0; r < DC; ++r) {
-            float f[8];
-            g[r].get(f);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const float x = __fmul_rn(scale, f[k]);
-                acc[k] = r == 0 ? x : __fadd_rn(acc[k], x);
-            }
-        }
+        reduce_loaded<G, DC>(g, scale, acc);
     } else {
         constexpr int kBatch = 4;
         float part[8];
@@ -518,27 +526,14 @@ __device__ __forceinline__ void write_grads_vec(const void *const *grads, int D_
 // The step kernel
 // ---------------------------------------------------------------------------
 
-// A vector of 8 owned elements of one run.
+// The Adam update of a vector of 8 owned elements of one run and all its
+// stores, from its reduced grads and its loaded master/m/v.
 template <typename G, int DC, int MODE>
-__device__ __forceinline__ void full_vector(const StepArgs &a, const Scalars &sc, int64_t e0,
-                                            int32_t meta, int32_t status = 0) {
-    float acc[8];
-    if constexpr (MODE == kFromMain) {
-        const float coef = *a.clip_coef;
-        if (a.skip_nonfinite && isnan(coef)) return;  // the step is skipped
-        const float4 g0 = ld_stream_f4(a.main_grad_in + e0), g1 = ld_stream_f4(a.main_grad_in + e0 + 4);
-        const float f[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-#pragma unroll
-        for (int k = 0; k < 8; ++k) acc[k] = __fmul_rn(f[k], coef);
-    } else {
-        reduce_vec<G, DC>(a, sc.scale, e0, acc);
-        if (a.round_grad) to_grad_type8<G>(acc);
-    }
-    if constexpr (MODE == kWriteGrads) write_grads_vec<G, DC>(a.grads, a.D, e0, acc);
-
-    const float4 w0 = ld_stream_f4(a.master + e0), w1 = ld_stream_f4(a.master + e0 + 4);
-    const float4 m0 = ld_stream_f4(a.exp_avg + e0), m1 = ld_stream_f4(a.exp_avg + e0 + 4);
-    const float4 v0 = ld_stream_f4(a.exp_avg_sq + e0), v1 = ld_stream_f4(a.exp_avg_sq + e0 + 4);
+__device__ __forceinline__ void update_and_store(const StepArgs &a, const Scalars &sc, int64_t e0,
+                                                 int32_t meta, int32_t status, float (&acc)[8],
+                                                 const float4 &w0, const float4 &w1,
+                                                 const float4 &m0, const float4 &m1,
+                                                 const float4 &v0, const float4 &v1) {
     float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
     float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
     float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
@@ -575,6 +570,65 @@ __device__ __forceinline__ void full_vector(const StepArgs &a, const Scalars &sc
         for (int r = q; r < a.D; r += a.R)
             st_stream(static_cast<__nv_bfloat16 *>(a.params[r]) + e0, packed);
     }
+}
+
+// A vector of 8 owned elements of one run, loading as it goes.
+template <typename G, int DC, int MODE>
+__device__ __forceinline__ void full_vector(const StepArgs &a, const Scalars &sc, int64_t e0,
+                                            int32_t meta, int32_t status = 0) {
+    float acc[8];
+    if constexpr (MODE == kFromMain) {
+        const float coef = *a.clip_coef;
+        if (a.skip_nonfinite && isnan(coef)) return;  // the step is skipped
+        const float4 g0 = ld_stream_f4(a.main_grad_in + e0), g1 = ld_stream_f4(a.main_grad_in + e0 + 4);
+        const float f[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc[k] = __fmul_rn(f[k], coef);
+    } else {
+        reduce_vec<G, DC>(a, sc.scale, e0, acc);
+        if (a.round_grad) to_grad_type8<G>(acc);
+    }
+    if constexpr (MODE == kWriteGrads) write_grads_vec<G, DC>(a.grads, a.D, e0, acc);
+    const float4 w0 = ld_stream_f4(a.master + e0), w1 = ld_stream_f4(a.master + e0 + 4);
+    const float4 m0 = ld_stream_f4(a.exp_avg + e0), m1 = ld_stream_f4(a.exp_avg + e0 + 4);
+    const float4 v0 = ld_stream_f4(a.exp_avg_sq + e0), v1 = ld_stream_f4(a.exp_avg_sq + e0 + 4);
+    update_and_store<G, DC, MODE>(a, sc, e0, meta, status, acc, w0, w1, m0, m1, v0, v1);
+}
+
+// The loads of a vector issued before the thread knows whether it is a
+// whole vector of one run (its run lookup is a chain of dependent loads): the
+// D grad replicas and master/m/v at e0, all inside the launch's own range.
+template <typename G, int DC>
+struct Preloaded {
+    GradVec<G> g[DC];
+    float4 w0, w1, m0, m1, v0, v1;
+    __device__ __forceinline__ void load(const StepArgs &a, int64_t e0) {
+#pragma unroll
+        for (int r = 0; r < DC; ++r) g[r].load(a.grads[r], e0);
+        w0 = ld_stream_f4(a.master + e0), w1 = ld_stream_f4(a.master + e0 + 4);
+        m0 = ld_stream_f4(a.exp_avg + e0), m1 = ld_stream_f4(a.exp_avg + e0 + 4);
+        v0 = ld_stream_f4(a.exp_avg_sq + e0), v1 = ld_stream_f4(a.exp_avg_sq + e0 + 4);
+    }
+};
+
+// Which instantiations preload: D = 1 with 16-bit grads, where it made the
+// 256 Mi sweep's step 1.8 % faster.  With more replicas enough other warps
+// cover the lookup, and holding the preloaded vectors across it cost 0.5 %
+// (D = 2) to 4.7 % (D = 8, 1 Mi buckets); they load as they go.
+template <typename G, int DC, int MODE>
+constexpr bool kPreload = DC == 1 && sizeof(G) == 2 && MODE != kFromMain;
+
+// A whole vector of one run from its preloaded grads and state.
+template <typename G, int DC, int MODE>
+__device__ __forceinline__ void full_vector_preloaded(const StepArgs &a, const Scalars &sc,
+                                                      int64_t e0, int32_t meta, int32_t status,
+                                                      const Preloaded<G, DC> &p) {
+    float acc[8];
+    reduce_loaded<G, DC>(p.g, sc.scale, acc);
+    if (a.round_grad) to_grad_type8<G>(acc);
+    if constexpr (MODE == kWriteGrads) write_grads_vec<G, DC>(a.grads, a.D, e0, acc);
+    update_and_store<G, DC, MODE>(a, sc, e0, meta, status, acc, p.w0, p.w1, p.m0, p.m1, p.v0,
+                                  p.v1);
 }
 
 // A vector that straddles a run edge: element by element, owned ones only.
@@ -618,9 +672,40 @@ __device__ __noinline__ void mixed_vector(const StepArgs &a, const Scalars &sc, 
 // would otherwise stop near 56-64, and the extra registers keep more loads in
 // flight per thread (D = 4: 2.5 % faster, D = 8 and 16: 0.2-0.4 %; forcing 6
 // or 8 CTAs per SM spilled and lost 15-40 %).
+// One tile per CTA: this thread's vector of 8 elements.  `sc` is the
+// launch's own scalars (read from the constant bank) except in the counted
+// step, whose two step-dependent scalars come from the counter.
+template <typename G, int DC, int MODE>
+__device__ __forceinline__ void step_vector(const StepArgs &a, const Scalars &sc, int32_t status) {
+    const int64_t tile = a.rv.tile0 + blockIdx.x;
+    const int64_t e0 = tile * kDoptTileElems + int64_t(threadIdx.x) * kVec;
+    int j;
+    if constexpr (kPreload<G, DC, MODE>) {
+        // A whole vector of one run lies inside [lo, hi), so every vector
+        // that turns out whole has its loads in flight before the lookup.
+        Preloaded<G, DC> p;
+        const bool inside = e0 >= a.rv.lo && e0 + kVec <= a.rv.hi;
+        if (inside) p.load(a, e0);
+        const VecKind kind = locate(a.rv, tile, e0, j);
+        if (kind == kFull) {
+            full_vector_preloaded<G, DC, MODE>(a, sc, e0, a.rv.run_meta[j], status, p);
+        } else if (kind == kMixed) {
+            if (status != 0) return;
+            mixed_vector<G, DC, MODE>(a, sc, e0, j);
+        }
+    } else {
+        const VecKind kind = locate(a.rv, tile, e0, j);
+        if (kind == kFull) {
+            full_vector<G, DC, MODE>(a, sc, e0, a.rv.run_meta[j], status);
+        } else if (kind == kMixed) {
+            if (status != 0) return;
+            mixed_vector<G, DC, MODE>(a, sc, e0, j);
+        }
+    }
+}
+
 template <typename G, int DC, int MODE>
 __global__ void __launch_bounds__(kThreads, 3) dopt_step_kernel(const __grid_constant__ StepArgs a) {
-    int j;
     if constexpr (MODE == kCounted) {
         // let the next counted step's counter kernel start (it waits for this
         // grid to complete before it writes the counter)
@@ -635,25 +720,11 @@ __global__ void __launch_bounds__(kThreads, 3) dopt_step_kernel(const __grid_con
         Scalars sc = a.sc;
         sc.step_size = __uint_as_float(hot.x);
         sc.bc2_sqrt = __uint_as_float(hot.y);
-        const int32_t status = int32_t(hot.z);
-        const int64_t tile = a.rv.tile0 + blockIdx.x;
-        const int64_t e0 = tile * kDoptTileElems + int64_t(threadIdx.x) * kVec;
-        const VecKind kind = locate(a.rv, tile, e0, j);
-        if (kind == kFull) {
-            full_vector<G, DC, MODE>(a, sc, e0, a.rv.run_meta[j], status);
-        } else if (kind == kMixed) {
-            if (status != 0) return;
-            mixed_vector<G, DC, MODE>(a, sc, e0, j);
-        }
+        step_vector<G, DC, MODE>(a, sc, int32_t(hot.z));
     } else {
-        // one tile per CTA
-        const int64_t tile = a.rv.tile0 + blockIdx.x;
-        const int64_t e0 = tile * kDoptTileElems + int64_t(threadIdx.x) * kVec;
-        const VecKind kind = locate(a.rv, tile, e0, j);
-        if (kind == kFull)
-            full_vector<G, DC, MODE>(a, a.sc, e0, a.rv.run_meta[j]);
-        else if (kind == kMixed)
-            mixed_vector<G, DC, MODE>(a, a.sc, e0, j);
+        // the scalars stay in the constant bank (a copy in registers cost
+        // the D = 2 step 4 %)
+        step_vector<G, DC, MODE>(a, a.sc, 0);
     }
 }
 

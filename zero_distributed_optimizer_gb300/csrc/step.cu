@@ -47,6 +47,8 @@ RunView make_view(const dopt_layout *L, int32_t first, int32_t count, int64_t *t
     if (v.run_begin >= v.run_limit) return v;
     const int64_t lo = L->run_start[size_t(v.run_begin)];
     const int64_t hi = L->run_end[size_t(v.run_limit - 1)];
+    v.lo = lo;
+    v.hi = hi;
     v.tile0 = lo / kDoptTileElems;
     *tiles = (hi + kDoptTileElems - 1) / kDoptTileElems - v.tile0;
     return v;
