@@ -1,12 +1,15 @@
 #!/usr/bin/env python3
 """Benchmark of the fused ZeRO-1 distributed-optimizer step on GB300.
 
-One step = one dopt_step launch: reduce-scatter of the D bf16 grad replicas
-(scaled, fp32, rank order), fp32 main grads through the range map, AdamW
-with bias correction on fp32 master/m/v, bf16 write-back and all-gather into
-the D param replicas, over every bucket of the GPT-2-small-shaped flat
-buffer (124,439,808 elements, D=8, 40 Mi buckets padded to multiples of
-D*64).  Prints one JSON line.
+One step = the whole fused step over every bucket of the GPT-2-small-shaped
+flat buffer (124,439,808 elements, D=8, 40 Mi buckets padded to multiples
+of D*64): reduce-scatter of the D bf16 grad replicas (scaled, fp32, rank
+order), fp32 main grads through the range map, AdamW with bias correction
+on fp32 master/m/v, bf16 write-back and all-gather into the D param
+replicas.  The timed steps are dopt_step_counted calls (step number in a
+device counter) captured in CUDA graphs and replayed; the same steps as
+plain dopt_step calls (one launch each) are timed too and reported under
+"direct".  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -327,13 +330,35 @@ def run_ours(args):
         step(t)
     torch.cuda.synchronize()
 
+    # The timed path: dopt_step_counted (the step number lives in a device
+    # counter, so the launches do not depend on it) captured GRAPH_STEPS at a
+    # time in a CUDA graph, plus one graph for the remainder of K, replayed
+    # until exactly K steps are done.  Each step is two launches: a counter
+    # kernel of two threads, then the step kernel.
+    per = GRAPH_STEPS
+    counter = B.step_counter(t + 1, device)
+    B.dopt_step_counted(L, adam, counter, grads, master, m, v, params)  # kernels loaded
+    torch.cuda.synchronize()
+    graphs = {}
+    for n in sorted({per, args.steps % per} - {0}):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(n):
+                B.dopt_step_counted(L, adam, counter, grads, master, m, v, params)
+        graphs[n] = g
+    taken = 1
+    for _ in range(max(args.warmup, 3)):
+        graphs[per].replay()
+        taken += per
+    torch.cuda.synchronize()
+
     sampler = ClockSampler(torch.cuda.current_device())
     sampler.start()
     # let the sampler come up and the clocks settle under the same load
     settle_end = time.time() + 0.4
     while time.time() < settle_end:
-        t += 1
-        step(t)
+        graphs[per].replay()
+        taken += per
         torch.cuda.synchronize()
 
     if world > 1:
@@ -342,15 +367,21 @@ def run_ours(args):
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     h0 = time.time()
     ev0.record(stream)
-    for _ in range(args.steps):
-        t += 1
-        step(t)
+    for _ in range(args.steps // per):
+        graphs[per].replay()
+    if args.steps % per:
+        graphs[args.steps % per].replay()
     ev1.record(stream)
     torch.cuda.synchronize()
     h1 = time.time()
     if world > 1:
         torch.distributed.barrier()
     sampler.stop()
+    taken += args.steps
+    next_step, status = B.counter_state(counter)
+    assert status == 0 and next_step == t + 1 + taken, (next_step, status, t, taken)
+    t = next_step - 1
+    del graphs
     ms_local = ev0.elapsed_time(ev1)
     ms_total = max_over_ranks(ms_local, world, device)
     ms_per_step = ms_total / args.steps
@@ -362,40 +393,22 @@ def run_ours(args):
     peak, peak_kind = measured_hbm_peak()
     traffic = read_profile_traffic()
 
-    # the same steps replayed from a CUDA graph: GRAPH_STEPS dopt_step_counted
-    # calls (the step number lives in a device counter) captured once, the
-    # graph replayed until K steps are done
-    graph = None
-    if not args.no_graph:
-        per = GRAPH_STEPS
-        replays = max(1, args.steps // per)
-        counter = B.step_counter(t + 1, device)
-        B.dopt_step_counted(L, adam, counter, grads, master, m, v, params)  # kernels loaded
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for _ in range(per):
-                B.dopt_step_counted(L, adam, counter, grads, master, m, v, params)
-        for _ in range(3):
-            g.replay()
-        torch.cuda.synchronize()
-        if world > 1:
-            torch.distributed.barrier()
-        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        g0.record(stream)
-        for _ in range(replays):
-            g.replay()
-        g1.record(stream)
-        torch.cuda.synchronize()
-        g_ms = max_over_ranks(g0.elapsed_time(g1), world, device) / (replays * per)
-        next_step, status = B.counter_state(counter)
-        assert status == 0 and next_step == t + 2 + per * (3 + replays)
-        t = next_step - 1
-        graph = {"ms_per_step": g_ms, "value": world * elems / (g_ms / 1e3), "unit": UNIT,
-                 "steps": replays * per, "steps_per_graph": per, "launches_per_step": 2,
-                 "path": "binding.dopt_step_counted captured in a CUDA graph and replayed "
-                         "(per step a counter kernel of two threads, then the step kernel)"}
-        del g
+    # the same K steps as one dopt_step call each (one launch per step, the
+    # step number a host argument)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    d0.record(stream)
+    for _ in range(args.steps):
+        t += 1
+        step(t)
+    d1.record(stream)
+    torch.cuda.synchronize()
+    d_ms = max_over_ranks(d0.elapsed_time(d1), world, device) / args.steps
+    direct = {"ms_per_step": d_ms, "value": world * elems / (d_ms / 1e3), "unit": UNIT,
+              "launches_per_step": 1,
+              "path": "binding.dopt_step, one call (one kernel launch) per step"}
 
     # end to end through the public API: grads from pinned host memory,
     # updated params (replica 0) back to pinned host memory, every step
@@ -477,16 +490,21 @@ def run_ours(args):
                        "state_dtype": "f32", "param_dtype": "bf16",
                        "bytes_per_element": w.algorithmic_bytes_per_element(),
                        "l2": l2_note(N * (w.D * w.grad_bytes + 12 + 2 * w.D)),
+                       "path": f"binding.dopt_step_counted, {GRAPH_STEPS} steps per CUDA "
+                               "graph, replayed (a counter kernel and the step kernel per "
+                               "step)",
                        "parallelism": "replicas" if world > 1 else "single"},
             "hbm_gbs": gbs, "pct_of_8tbs": gbs / NOMINAL_HBM_GBS,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                          "frac": gbs / peak, "peak_kind": peak_kind,
                          "traffic": traffic,
+                         "kernel": "dopt_step_kernel (the counter kernel's time is "
+                                   "included in the step time it divides by)",
                          "algorithmic_bytes_per_launch": bytes_per_launch},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "graph_replay": graph,
-            "gpu_launches": args.steps,
+            "direct": direct,
+            "gpu_launches": 2 * args.steps,
             "clocks": sampler.summary(h0, h1),
             "torch": torch.__version__,
         }
@@ -505,8 +523,6 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-graph", action="store_true",
-                    help="skip the CUDA-graph replay of counted steps")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="wall time of the CPU-baseline legs (one thread, all threads)")
     ap.add_argument("--cpu-threads", type=int, default=0,

@@ -307,15 +307,23 @@ __device__ __forceinline__ void st_stream_f4(float *p, const float4 &v) {
     __stcs(reinterpret_cast<float4 *>(p), v);
 }
 
+// The two scalars that depend on the step number, passed apart from the
+// others: the counted step takes them from its counter and every other
+// scalar from the constant bank, like the other steps.
+struct StepDep {
+    float step_size;
+    float bc2_sqrt;
+};
+
 // One AdamW update of one element, each operation rounded on its own.
-__device__ __forceinline__ void adamw(const Scalars &s, float decay, float g, float &w, float &m,
-                                      float &v) {
+__device__ __forceinline__ void adamw(const Scalars &s, StepDep dep, float decay, float g,
+                                      float &w, float &m, float &v) {
     m = __fadd_rn(__fmul_rn(s.b1, m), __fmul_rn(s.omb1, g));
     const float gg = __fmul_rn(g, g);
     v = __fadd_rn(__fmul_rn(s.b2, v), __fmul_rn(s.omb2, gg));
     w = __fmul_rn(w, decay);
-    const float denom = __fadd_rn(__fdiv_rn(__fsqrt_rn(v), s.bc2_sqrt), s.eps);
-    w = __fsub_rn(w, __fmul_rn(s.step_size, __fdiv_rn(m, denom)));
+    const float denom = __fadd_rn(__fdiv_rn(__fsqrt_rn(v), dep.bc2_sqrt), s.eps);
+    w = __fsub_rn(w, __fmul_rn(dep.step_size, __fdiv_rn(m, denom)));
 }
 
 // First run (index >= j, < limit) whose end lies beyond `pos`: one ballot
@@ -529,7 +537,8 @@ __device__ __forceinline__ void write_grads_vec(const void *const *grads, int D_
 // The Adam update of a vector of 8 owned elements of one run and all its
 // stores, from its reduced grads and its loaded master/m/v.
 template <typename G, int DC, int MODE>
-__device__ __forceinline__ void update_and_store(const StepArgs &a, const Scalars &sc, int64_t e0,
+__device__ __forceinline__ void update_and_store(const StepArgs &a, const Scalars &sc, StepDep dep,
+                                                 int64_t e0,
                                                  int32_t meta, int32_t status, float (&acc)[8],
                                                  const float4 &w0, const float4 &w1,
                                                  const float4 &m0, const float4 &m1,
@@ -539,7 +548,7 @@ __device__ __forceinline__ void update_and_store(const StepArgs &a, const Scalar
     float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
     const float decay = (meta & kRunDecays) ? sc.decay : 1.0f;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) adamw(sc, decay, acc[k], w[k], m[k], v[k]);
+    for (int k = 0; k < 8; ++k) adamw(sc, dep, decay, acc[k], w[k], m[k], v[k]);
     if constexpr (MODE == kCounted) {
         if (status != 0) return;  // the counter launch found a bad step number
     }
@@ -574,7 +583,7 @@ __device__ __forceinline__ void update_and_store(const StepArgs &a, const Scalar
 
 // A vector of 8 owned elements of one run, loading as it goes.
 template <typename G, int DC, int MODE>
-__device__ __forceinline__ void full_vector(const StepArgs &a, const Scalars &sc, int64_t e0,
+__device__ __forceinline__ void full_vector(const StepArgs &a, const Scalars &sc, StepDep dep, int64_t e0,
                                             int32_t meta, int32_t status = 0) {
     float acc[8];
     if constexpr (MODE == kFromMain) {
@@ -592,7 +601,7 @@ __device__ __forceinline__ void full_vector(const StepArgs &a, const Scalars &sc
     const float4 w0 = ld_stream_f4(a.master + e0), w1 = ld_stream_f4(a.master + e0 + 4);
     const float4 m0 = ld_stream_f4(a.exp_avg + e0), m1 = ld_stream_f4(a.exp_avg + e0 + 4);
     const float4 v0 = ld_stream_f4(a.exp_avg_sq + e0), v1 = ld_stream_f4(a.exp_avg_sq + e0 + 4);
-    update_and_store<G, DC, MODE>(a, sc, e0, meta, status, acc, w0, w1, m0, m1, v0, v1);
+    update_and_store<G, DC, MODE>(a, sc, dep, e0, meta, status, acc, w0, w1, m0, m1, v0, v1);
 }
 
 // The loads of a vector issued before the thread knows whether it is a
@@ -620,20 +629,21 @@ constexpr bool kPreload = DC == 1 && sizeof(G) == 2 && MODE != kFromMain;
 
 // A whole vector of one run from its preloaded grads and state.
 template <typename G, int DC, int MODE>
-__device__ __forceinline__ void full_vector_preloaded(const StepArgs &a, const Scalars &sc,
+__device__ __forceinline__ void full_vector_preloaded(const StepArgs &a, const Scalars &sc, StepDep dep,
                                                       int64_t e0, int32_t meta, int32_t status,
                                                       const Preloaded<G, DC> &p) {
     float acc[8];
     reduce_loaded<G, DC>(p.g, sc.scale, acc);
     if (a.round_grad) to_grad_type8<G>(acc);
     if constexpr (MODE == kWriteGrads) write_grads_vec<G, DC>(a.grads, a.D, e0, acc);
-    update_and_store<G, DC, MODE>(a, sc, e0, meta, status, acc, p.w0, p.w1, p.m0, p.m1, p.v0,
-                                  p.v1);
+    update_and_store<G, DC, MODE>(a, sc, dep, e0, meta, status, acc, p.w0, p.w1, p.m0, p.m1,
+                                  p.v0, p.v1);
 }
 
 // A vector that straddles a run edge: element by element, owned ones only.
 template <typename G, int DC, int MODE>
-__device__ __noinline__ void mixed_vector(const StepArgs &a, const Scalars &sc, int64_t e0, int j) {
+__device__ __noinline__ void mixed_vector(const StepArgs &a, const Scalars &sc, StepDep dep, int64_t e0,
+                                         int j) {
     if constexpr (MODE == kFromMain) {
         if (a.skip_nonfinite && isnan(*a.clip_coef)) return;  // the step is skipped
     }
@@ -653,7 +663,7 @@ __device__ __noinline__ void mixed_vector(const StepArgs &a, const Scalars &sc, 
         if constexpr (MODE == kWriteGrads)
             for (int r = 0; r < D; ++r) store_grad_scalar<G>(a.grads[r], e, g);
         float w = a.master[e], m = a.exp_avg[e], v = a.exp_avg_sq[e];
-        adamw(sc, (meta & kRunDecays) ? sc.decay : 1.0f, g, w, m, v);
+        adamw(sc, dep, (meta & kRunDecays) ? sc.decay : 1.0f, g, w, m, v);
         a.master[e] = w;
         a.exp_avg[e] = m;
         a.exp_avg_sq[e] = v;
@@ -673,10 +683,11 @@ __device__ __noinline__ void mixed_vector(const StepArgs &a, const Scalars &sc, 
 // flight per thread (D = 4: 2.5 % faster, D = 8 and 16: 0.2-0.4 %; forcing 6
 // or 8 CTAs per SM spilled and lost 15-40 %).
 // One tile per CTA: this thread's vector of 8 elements.  `sc` is the
-// launch's own scalars (read from the constant bank) except in the counted
-// step, whose two step-dependent scalars come from the counter.
+// launch's own scalars (read from the constant bank); `dep` holds the two
+// step-dependent ones, which the counted step takes from its counter.
 template <typename G, int DC, int MODE>
-__device__ __forceinline__ void step_vector(const StepArgs &a, const Scalars &sc, int32_t status) {
+__device__ __forceinline__ void step_vector(const StepArgs &a, const Scalars &sc, StepDep dep,
+                                            int32_t status) {
     const int64_t tile = a.rv.tile0 + blockIdx.x;
     const int64_t e0 = tile * kDoptTileElems + int64_t(threadIdx.x) * kVec;
     int j;
@@ -688,18 +699,18 @@ __device__ __forceinline__ void step_vector(const StepArgs &a, const Scalars &sc
         if (inside) p.load(a, e0);
         const VecKind kind = locate(a.rv, tile, e0, j);
         if (kind == kFull) {
-            full_vector_preloaded<G, DC, MODE>(a, sc, e0, a.rv.run_meta[j], status, p);
+            full_vector_preloaded<G, DC, MODE>(a, sc, dep, e0, a.rv.run_meta[j], status, p);
         } else if (kind == kMixed) {
             if (status != 0) return;
-            mixed_vector<G, DC, MODE>(a, sc, e0, j);
+            mixed_vector<G, DC, MODE>(a, sc, dep, e0, j);
         }
     } else {
         const VecKind kind = locate(a.rv, tile, e0, j);
         if (kind == kFull) {
-            full_vector<G, DC, MODE>(a, sc, e0, a.rv.run_meta[j], status);
+            full_vector<G, DC, MODE>(a, sc, dep, e0, a.rv.run_meta[j], status);
         } else if (kind == kMixed) {
             if (status != 0) return;
-            mixed_vector<G, DC, MODE>(a, sc, e0, j);
+            mixed_vector<G, DC, MODE>(a, sc, dep, e0, j);
         }
     }
 }
@@ -717,14 +728,12 @@ __global__ void __launch_bounds__(kThreads, 3) dopt_step_kernel(const __grid_con
         // memory behind a CTA barrier cost 1.7 %; a persistent grid that
         // reads it once per resident CTA cost 15 %.)
         const uint4 hot = *reinterpret_cast<const uint4 *>(&a.counter->hot);
-        Scalars sc = a.sc;
-        sc.step_size = __uint_as_float(hot.x);
-        sc.bc2_sqrt = __uint_as_float(hot.y);
-        step_vector<G, DC, MODE>(a, sc, int32_t(hot.z));
+        step_vector<G, DC, MODE>(a, a.sc, StepDep{__uint_as_float(hot.x), __uint_as_float(hot.y)},
+                                 int32_t(hot.z));
     } else {
-        // the scalars stay in the constant bank (a copy in registers cost
-        // the D = 2 step 4 %)
-        step_vector<G, DC, MODE>(a, a.sc, 0);
+        // every scalar stays in the constant bank (a copy of them in
+        // registers cost the D = 2 step 4 %)
+        step_vector<G, DC, MODE>(a, a.sc, StepDep{a.sc.step_size, a.sc.bc2_sqrt}, 0);
     }
 }
 

@@ -52,10 +52,10 @@ def main(argv=None):
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--mode", default="step",
                     choices=["step", "gather", "clipped", "buckets", "buckets_graph", "allreduce",
-                             "step_allreduce"],
+                             "step_allreduce", "counted"],
                     help="the fused step, dopt_gather alone, the clipped step, the step as "
-                         "one launch per bucket, dopt_allreduce alone, or the step with "
-                         "force_all_reduce")
+                         "one launch per bucket, dopt_allreduce alone, the step with "
+                         "force_all_reduce, or the counted step (step number on the device)")
     ap.add_argument("--streams", type=int, default=1,
                     help="buckets mode: bucket k is launched on stream k mod STREAMS")
     ap.add_argument("--plan", action="store_true",
@@ -107,6 +107,7 @@ def main(argv=None):
             join.record(s_)
             streams[0].wait_event(join)
 
+    counter = B.step_counter(1, dev) if args.mode == "counted" else None
     graph = None
     if args.mode == "buckets_graph":
         # the per-bucket launches of one step recorded once and replayed: the
@@ -141,6 +142,8 @@ def main(argv=None):
             B.dopt_step_allreduce(L, adam, t, grads, master, m, v, params)
         elif args.mode == "clipped":
             B.dopt_step_clipped(L, adam, t, 1.0, grads, master, m, v, params, main_grad, ws)
+        elif args.mode == "counted":
+            B.dopt_step_counted(L, adam, counter, grads, master, m, v, params)
         elif plan is not None:
             plan.step(t)
         else:
@@ -150,7 +153,7 @@ def main(argv=None):
     ms = ev[0].elapsed_time(ev[1]) / max(args.launches, 1)
     step_bytes = w.algorithmic_bytes_per_element()
     per_elem = {"gather": 2 * w.D, "step": step_bytes, "buckets": step_bytes,
-                "buckets_graph": step_bytes,
+                "buckets_graph": step_bytes, "counted": step_bytes,
                 "clipped": step_bytes + 8, "allreduce": 2 * w.D * w.grad_bytes,
                 "step_allreduce": step_bytes + w.D * w.grad_bytes}[args.mode]
     bytes_per = w.numel * per_elem
