@@ -430,6 +430,27 @@ int dopt_step_clipped(const dopt_layout *layout, const dopt_adam_cfg *cfg, int64
 #define DOPT_NOALLOC_SCRATCH_BYTES 16384
 
 /*
+ * dopt_step_clipped with the step number taken from, and advanced in, a
+ * device counter, as dopt_step_counted does for dopt_step: the counter
+ * kernel, then the two launches of dopt_step_clipped, whose second one takes
+ * the two step-dependent scalars and the status from the counter.  The
+ * launches do not depend on the step number, so a captured sequence replays
+ * every later step.  With a bad next_step (see dopt_step_counter) the norm
+ * pass still writes main_grad and norm_out; master, exp_avg, exp_avg_sq and
+ * the params are not written.  A step that DOPT_STEP_SKIP_NONFINITE skips
+ * is not counted: next_step is left as it was before the call.  The pages
+ * describe no such counter: it is an
+ * addition of this library for graph replay.  Arguments and errors as
+ * dopt_step_clipped, plus those of dopt_step_counted for `counter`.
+ */
+int dopt_step_clipped_counted(const dopt_layout *layout, const dopt_adam_cfg *cfg,
+                              dopt_step_counter *counter, float max_norm,
+                              const void *const *grad_replicas, dopt_dtype grad_dtype,
+                              float *master, float *exp_avg, float *exp_avg_sq,
+                              void *const *param_replicas, uint32_t flags, float *main_grad,
+                              void *workspace, float *norm_out, cudaStream_t stream);
+
+/*
  * dopt_step_clipped for callers that cannot allocate device memory on the
  * step's path.  The pages have no counterpart: this entry point exists for
  * such callers, not for the method.

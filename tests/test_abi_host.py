@@ -297,3 +297,21 @@ def test_fp16_dtype_and_param_flag_accepted_before_cuda(lib):
                                                                            B.DOPT_E_CUDA)
     assert B.lib().dopt_step(L.handle, ctypes.byref(cfg), 1, gp, 0, *st, gp, 32, None,
                              None) == B.DOPT_E_ARG
+
+
+def test_clipped_counted_argument_checks_before_cuda(lib):
+    L = _lib_layout([100, 30], 2, 0, 8)
+    cfg = B.AdamConfig().to_c()
+    gp = (ctypes.c_void_p * 2)(0x10000, 0x20000)
+    st = (0x30000, 0x40000, 0x50000)
+
+    def call(counter=0x90000, ws=0x80000, main=0x70000, flags=1):
+        return B.lib().dopt_step_clipped_counted(L.handle, ctypes.byref(cfg), counter, 1.0, gp,
+                                                 0, *st, gp, flags, main, ws, None, None)
+
+    assert call(counter=None) == B.DOPT_E_ARG
+    assert call(counter=0x90004) == B.DOPT_E_ALIGN
+    assert call(ws=None) == B.DOPT_E_ARG
+    assert call(main=None) == B.DOPT_E_ARG
+    assert call(flags=64) == B.DOPT_E_ARG
+    assert call(flags=1 | B.DOPT_STEP_SKIP_NONFINITE) in (B.DOPT_E_STATE, B.DOPT_E_CUDA)

@@ -271,3 +271,80 @@ def test_counted_after_a_counter_write_on_the_stream():
     torch.cuda.synchronize()
     _equal(s + p, s2 + p2)
     assert B.counter_state(counter) == (4, 0)
+
+
+def _clip_case(seed=31):
+    return _case([5000, 1, 7, 300, 20000, 3, 9999], [1, 0, 1, 0, 1, 1, 0], 8, 0, 1, "bf16",
+                 steps=3, seed=seed)
+
+
+def test_clipped_counted_equals_clipped_in_a_graph():
+    """Three counted clipped steps replayed from one graph equal three
+    clipped steps with host step numbers: state, params, main grads and
+    the norm report, bit for bit."""
+    L, s, p, g, _ = _clip_case()
+    N = L.padded_numel
+    s2, p2 = _clone(s, p)
+    adam = B.AdamConfig(grad_scale=1.0 / 8)
+    mg, mg2 = (torch.full((N,), -1.0, device=DEV) for _ in range(2))  # padding stays -1
+    ws, ws2 = B.clip_workspace(DEV), B.clip_workspace(DEV)
+    rep, rep2 = B.clip_report(DEV), B.clip_report(DEV)
+    gsrc = [[x.clone() for x in gs] for gs in g]
+    gbuf = [x.clone() for x in g[0]]
+    # warm-up on copies
+    ws_, wp_ = _clone(s, p)
+    B.dopt_step_clipped_counted(L, adam, B.step_counter(1), 0.05, gbuf, *ws_, wp_,
+                                torch.empty(N, device=DEV), B.clip_workspace(DEV))
+    torch.cuda.synchronize()
+    counter = B.step_counter(1)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        B.dopt_step_clipped_counted(L, adam, counter, 0.05, gbuf, *s2, p2, mg2, ws2,
+                                    norm_out=rep2, skip_nonfinite=True)
+    for t in range(1, 4):
+        for x, y in zip(gbuf, gsrc[t - 1]):
+            x.copy_(y)
+        graph.replay()
+        B.dopt_step_clipped(L, adam, t, 0.05, gsrc[t - 1], *s, p, mg, ws, norm_out=rep,
+                            skip_nonfinite=True)
+        torch.cuda.synchronize()
+        assert torch.equal(rep, rep2)
+    _equal(s + p + [mg], s2 + p2 + [mg2])
+    assert B.counter_state(counter) == (4, 0)
+
+
+def test_clipped_counted_bad_step_and_skip():
+    """A bad step number stores nothing but the main grads and the report; a
+    step that the non-finite check skips gives its number back."""
+    L, s, p, g, _ = _clip_case(seed=32)
+    N = L.padded_numel
+    adam = B.AdamConfig(grad_scale=1.0 / 8)
+    before = [x.clone() for x in s + p]
+    mg = torch.full((N,), -1.0, device=DEV)
+    counter = B.step_counter(0)
+    B.dopt_step_clipped_counted(L, adam, counter, 0.05, g[0], *s, p, mg, B.clip_workspace(DEV))
+    torch.cuda.synchronize()
+    _equal(before, s + p)
+    assert B.counter_state(counter) == (0, B.DOPT_COUNTER_BAD_STEP)
+    assert not torch.all(mg == -1.0)  # the norm pass ran
+    # a NaN grad: skipped, and the step number is given back
+    counter[0] = 5
+    bad = [x.clone() for x in g[0]]
+    bad[3][1234] = float("nan")
+    rep = B.clip_report(DEV)
+    B.dopt_step_clipped_counted(L, adam, counter, 0.05, bad, *s, p, mg, B.clip_workspace(DEV),
+                                norm_out=rep, skip_nonfinite=True)
+    torch.cuda.synchronize()
+    _equal(before, s + p)
+    norm, coef, nonfinite = B.read_clip_report(rep)
+    assert nonfinite == 1 and np.isnan(coef)
+    assert B.counter_state(counter) == (5, 0)
+    # the same number then steps with clean grads
+    ref = [x.clone() for x in before]
+    B.dopt_step_clipped_counted(L, adam, counter, 0.05, g[0], *s, p, mg, B.clip_workspace(DEV),
+                                skip_nonfinite=True)
+    B.dopt_step_clipped(L, adam, 5, 0.05, g[0], *ref[:3], ref[3:], torch.empty(N, device=DEV),
+                        B.clip_workspace(DEV))
+    torch.cuda.synchronize()
+    _equal(ref, s + p)
+    assert B.counter_state(counter) == (6, 0)

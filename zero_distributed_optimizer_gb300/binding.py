@@ -104,6 +104,10 @@ def _declare(lib):
     lib.dopt_step_clipped.argtypes = [vp, P(dopt_adam_cfg), ctypes.c_int64, ctypes.c_float, P(vp),
                                       ctypes.c_int, vp, vp, vp, P(vp), ctypes.c_uint32, vp, vp,
                                       vp, vp]
+    lib.dopt_step_clipped_counted.restype = ctypes.c_int
+    lib.dopt_step_clipped_counted.argtypes = [vp, P(dopt_adam_cfg), vp, ctypes.c_float, P(vp),
+                                              ctypes.c_int, vp, vp, vp, P(vp), ctypes.c_uint32,
+                                              vp, vp, vp, vp]
     lib.dopt_step_clipped_noalloc.restype = ctypes.c_int
     lib.dopt_step_clipped_noalloc.argtypes = [vp, P(dopt_adam_cfg), ctypes.c_int64, ctypes.c_float,
                                               P(vp), ctypes.c_int, vp, vp, vp, P(vp),
@@ -628,6 +632,34 @@ def dopt_step_clipped(layout: Layout, adam: AdamConfig, step: int, max_norm: flo
             | (DOPT_STEP_SKIP_NONFINITE if skip_nonfinite else 0),
             main_grad.data_ptr(), workspace.data_ptr(),
             None if norm_out is None else norm_out.data_ptr(), _stream_handle(stream)))
+
+
+def dopt_step_clipped_counted(layout: Layout, adam: AdamConfig, counter, max_norm: float,
+                              grad_replicas, master, exp_avg, exp_avg_sq, param_replicas,
+                              main_grad, workspace, gather: bool = True, norm_out=None,
+                              stream=None, round_grad: bool = False,
+                              skip_nonfinite: bool = False) -> None:
+    """dopt_step_clipped with the step number read from, and advanced in, a
+    device counter (:func:`step_counter`), for graph capture."""
+    import torch
+
+    device, gp, pp, dt, mg, pflag = _step_pointers(layout, grad_replicas, master, exp_avg,
+                                                   exp_avg_sq, param_replicas, main_grad)
+    if main_grad is None:
+        raise DoptError(DOPT_E_ARG, "main_grad is required")
+    _check_counter(counter, device)
+    _check_tensor(workspace, "workspace", torch.uint8, DOPT_CLIP_WORKSPACE_BYTES, device)
+    if norm_out is not None:
+        _check_tensor(norm_out, "norm_out", torch.float32, 4 if skip_nonfinite else 2, device)
+    flags = (_flags(gather, round_grad=round_grad) | pflag
+             | (DOPT_STEP_SKIP_NONFINITE if skip_nonfinite else 0))
+    cfg = adam.to_c()
+    with torch.cuda.device(device):
+        _check(lib().dopt_step_clipped_counted(
+            layout.handle, ctypes.byref(cfg), counter.data_ptr(), float(max_norm), gp, dt,
+            master.data_ptr(), exp_avg.data_ptr(), exp_avg_sq.data_ptr(), pp, flags, mg,
+            workspace.data_ptr(), None if norm_out is None else norm_out.data_ptr(),
+            _stream_handle(stream)))
 
 
 def dopt_step_clipped_noalloc(layout: Layout, adam: AdamConfig, step: int, max_norm: float,

@@ -155,7 +155,8 @@ struct StepArgs {
     float *main_grad_out;
     const float *main_grad_in;  // kFromMain: the reduced grads
     const float *clip_coef;     // kFromMain: device scalar
-    const CounterBlock *counter;  // kCounted: status and t-dependent scalars
+    const CounterBlock *counter;  // kCounted, and kFromMain when not NULL: status and
+                                  // t-dependent scalars
     RunView rv;
     int32_t D;
     int32_t R;  // ranks per instance (D with one instance)
@@ -196,6 +197,7 @@ struct NormArgs {
     int32_t round_grad;
     int32_t skip_nonfinite;  // report a NaN coefficient (skip) if any grad is Inf/NaN
     float scale;
+    CounterBlock *counter;   // the counted clipped step: a skipped step gives its number back
     float max_norm;
 };
 
@@ -549,7 +551,7 @@ __device__ __forceinline__ void update_and_store(const StepArgs &a, const Scalar
     const float decay = (meta & kRunDecays) ? sc.decay : 1.0f;
 #pragma unroll
     for (int k = 0; k < 8; ++k) adamw(sc, dep, decay, acc[k], w[k], m[k], v[k]);
-    if constexpr (MODE == kCounted) {
+    if constexpr (MODE == kCounted || MODE == kFromMain) {
         if (status != 0) return;  // the counter launch found a bad step number
     }
 
@@ -717,7 +719,9 @@ __device__ __forceinline__ void step_vector(const StepArgs &a, const Scalars &sc
 
 template <typename G, int DC, int MODE>
 __global__ void __launch_bounds__(kThreads, 3) dopt_step_kernel(const __grid_constant__ StepArgs a) {
-    if constexpr (MODE == kCounted) {
+    bool counted = MODE == kCounted;
+    if constexpr (MODE == kFromMain) counted = a.counter != nullptr;  // the counted clipped step
+    if (counted) {
         // let the next counted step's counter kernel start (it waits for this
         // grid to complete before it writes the counter)
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -892,7 +896,13 @@ __global__ void __launch_bounds__(kThreads) dopt_rs_norm_kernel(const __grid_con
         if (coef > 1.0) coef = 1.0;
         const unsigned long long nonfinite = __ldcg(&a.ws->nonfinite);
         float c = float(coef);
-        if (a.skip_nonfinite && nonfinite != 0) c = __int_as_float(0x7fc00000);  // skip
+        if (a.skip_nonfinite && nonfinite != 0) {
+            c = __int_as_float(0x7fc00000);  // skip
+            // a skipped step is not counted (the counter kernel before this
+            // grid advanced the counter; nothing else reads it until this
+            // step's kernels are done)
+            if (a.counter && a.counter->hot.status == 0) a.counter->next_step -= 1;
+        }
         a.ws->norm_sq = v;
         a.ws->norm = float(norm);
         a.ws->coef = c;

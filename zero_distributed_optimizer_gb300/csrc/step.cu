@@ -306,7 +306,8 @@ int launch_clipped(const char *who, const dopt_layout *L, const dopt_adam_cfg *c
                    int64_t step, float max_norm, const void *const *grad_replicas,
                    dopt_dtype grad_dtype, float *master, float *exp_avg, float *exp_avg_sq,
                    void *const *param_replicas, uint32_t flags, float *main_grad,
-                   ClipWorkspace *ws, float *norm_out, cudaStream_t stream) {
+                   ClipWorkspace *ws, float *norm_out, cudaStream_t stream,
+                   const CounterBlock *counter = nullptr) {
     using dopt::fail;
     NormArgs na{};
     const int D = L->cfg.D;
@@ -324,6 +325,7 @@ int launch_clipped(const char *who, const dopt_layout *L, const dopt_adam_cfg *c
     na.skip_nonfinite = (flags & DOPT_STEP_SKIP_NONFINITE) ? 1 : 0;
     na.scale = cfg->grad_scale;
     na.max_norm = max_norm;
+    na.counter = const_cast<CounterBlock *>(counter);
     NormKernel nk = norm_kernel_for(grad_dtype, kernel_D(L));
     const int grid_a = norm_grid(nk, na.n_tiles, L->device);
     cudaError_t e = cudaMemsetAsync(ws, 0, kClipResetBytes, stream);
@@ -339,9 +341,41 @@ int launch_clipped(const char *who, const dopt_layout *L, const dopt_adam_cfg *c
     a.main_grad_in = main_grad;
     a.clip_coef = &ws->coef;
     a.skip_nonfinite = na.skip_nonfinite;
+    a.counter = counter;  // the counted clipped step: scalars and status from the counter
     StepKernel k = pick_step_kernel<float, kFromMain>(kernel_D(L));
     k<<<unsigned(tiles), kThreads, 0, stream>>>(a);
     return launch_error(who, "step");
+}
+
+// The counter kernel of a counted step, launched as a programmatic dependent
+// of the kernel before it on the stream (see dopt_count_step_kernel).
+int launch_counter(const char *who, CounterBlock *c, const dopt_adam_cfg *cfg,
+                   cudaStream_t stream) {
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(1);
+    lc.blockDim = dim3(2);
+    lc.dynamicSmemBytes = 0;
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    const dopt_adam_cfg cfg_copy = *cfg;
+    cudaError_t le = cudaLaunchKernelEx(&lc, dopt_count_step_kernel, c, cfg_copy);
+    if (le != cudaSuccess) {
+        cudaGetLastError();
+        return dopt::fail(DOPT_E_CUDA, "%s: counter launch: %s", who, cudaGetErrorString(le));
+    }
+    return launch_error(who, "counter");
+}
+
+// Checks of a step counter argument.
+int check_counter(const char *who, const dopt_step_counter *counter) {
+    if (!counter) return dopt::fail(DOPT_E_ARG, "%s: counter is NULL", who);
+    if (!aligned16(counter))
+        return dopt::fail(DOPT_E_ALIGN, "%s: counter is not 16-byte aligned", who);
+    return DOPT_OK;
 }
 
 // Checks of the clipped entry points beyond the step's own.
@@ -411,8 +445,8 @@ extern "C" int dopt_step_counted(const dopt_layout *L, const dopt_adam_cfg *cfg,
     int rc = check_step_args(who, L, cfg, 1, grad_replicas, grad_dtype, master, exp_avg,
                              exp_avg_sq, param_replicas, flags, main_grad_out);
     if (rc != DOPT_OK) return rc;
-    if (!counter) return fail(DOPT_E_ARG, "%s: counter is NULL", who);
-    if (!aligned16(counter)) return fail(DOPT_E_ALIGN, "%s: counter is not 16-byte aligned", who);
+    rc = check_counter(who, counter);
+    if (rc != DOPT_OK) return rc;
     // every check before the first launch: the counter advances only
     // together with the step it counts
     int64_t tiles = 0;
@@ -421,25 +455,7 @@ extern "C" int dopt_step_counted(const dopt_layout *L, const dopt_adam_cfg *cfg,
                       exp_avg, exp_avg_sq, param_replicas, flags, main_grad_out, a, &tiles);
     if (rc != DOPT_OK) return rc;
     CounterBlock *c = reinterpret_cast<CounterBlock *>(counter);
-    // a programmatic dependent of the kernel before it on the stream (see
-    // dopt_count_step_kernel)
-    cudaLaunchConfig_t lc = {};
-    lc.gridDim = dim3(1);
-    lc.blockDim = dim3(2);
-    lc.dynamicSmemBytes = 0;
-    lc.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    lc.attrs = attr;
-    lc.numAttrs = 1;
-    const dopt_adam_cfg cfg_copy = *cfg;
-    cudaError_t le = cudaLaunchKernelEx(&lc, dopt_count_step_kernel, c, cfg_copy);
-    if (le != cudaSuccess) {
-        cudaGetLastError();
-        return fail(DOPT_E_CUDA, "%s: counter launch: %s", who, cudaGetErrorString(le));
-    }
-    rc = launch_error(who, "counter");
+    rc = launch_counter(who, c, cfg, stream);
     if (rc != DOPT_OK || tiles == 0) return rc;
     a.counter = c;
     StepKernel k = step_kernel_for<kCounted>(grad_dtype, kernel_D(L));
@@ -518,6 +534,45 @@ extern "C" int dopt_step_clipped(const dopt_layout *L, const dopt_adam_cfg *cfg,
     return launch_clipped(who, L, cfg, step, max_norm, grad_replicas, grad_dtype, master,
                           exp_avg, exp_avg_sq, param_replicas, flags, main_grad,
                           static_cast<ClipWorkspace *>(workspace), norm_out, stream);
+}
+
+extern "C" int dopt_step_clipped_counted(const dopt_layout *L, const dopt_adam_cfg *cfg,
+                                         dopt_step_counter *counter, float max_norm,
+                                         const void *const *grad_replicas, dopt_dtype grad_dtype,
+                                         float *master, float *exp_avg, float *exp_avg_sq,
+                                         void *const *param_replicas, uint32_t flags,
+                                         float *main_grad, void *workspace, float *norm_out,
+                                         cudaStream_t stream) {
+    using dopt::fail;
+    dopt::clear_error();
+    const char *who = "dopt_step_clipped_counted";
+    NvtxRange range(who);
+    int rc = check_step_args(who, L, cfg, 1, grad_replicas, grad_dtype, master, exp_avg,
+                             exp_avg_sq, param_replicas, flags, main_grad,
+                             DOPT_STEP_SKIP_NONFINITE);
+    if (rc != DOPT_OK) return rc;
+    rc = check_clip_args(who, main_grad, norm_out, max_norm);
+    if (rc != DOPT_OK) return rc;
+    rc = check_counter(who, counter);
+    if (rc != DOPT_OK) return rc;
+    if (!workspace) return fail(DOPT_E_ARG, "%s: workspace is required", who);
+    if (!aligned16(workspace)) return fail(DOPT_E_ALIGN, "%s: workspace misaligned", who);
+    const bool empty = L->run_start.empty();
+    if (!empty) {
+        rc = check_device_tables(L, who);
+        if (rc != DOPT_OK) return rc;
+        const void *grads[DOPT_MAX_D];
+        rc = resolve_grads(who, L->cfg.D, grad_replicas, flags, grads);
+        if (rc != DOPT_OK) return rc;
+    }
+    // every check before the first launch: the counter advances only
+    // together with the step it counts
+    CounterBlock *c = reinterpret_cast<CounterBlock *>(counter);
+    rc = launch_counter(who, c, cfg, stream);
+    if (rc != DOPT_OK || empty) return rc;
+    return launch_clipped(who, L, cfg, 1, max_norm, grad_replicas, grad_dtype, master, exp_avg,
+                          exp_avg_sq, param_replicas, flags, main_grad,
+                          static_cast<ClipWorkspace *>(workspace), norm_out, stream, c);
 }
 
 // ---------------------------------------------------------------------------
