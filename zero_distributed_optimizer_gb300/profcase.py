@@ -63,6 +63,8 @@ def main(argv=None):
     ap.add_argument("--grad-dtype", choices=["bf16", "fp16", "fp32"], default=None,
                     help="override the workload's grad type")
     ap.add_argument("--param-dtype", choices=["bf16", "fp16"], default="bf16")
+    ap.add_argument("--instances", type=int, default=1,
+                    help="distributed-optimizer instances (D must divide by it)")
     args = ap.parse_args(argv)
 
     libbuild.build()
@@ -76,7 +78,7 @@ def main(argv=None):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     L = B.dopt_build_range_map(list(w.sizes), w.D, w.bucket_elems, w.pad_unit,
-                               list(w.wd_mask)).to_device(dev)
+                               list(w.wd_mask), instances=args.instances).to_device(dev)
     N = L.padded_numel
     master, m, v = W.make_state(w, N, dev)
     params = W.make_params(master, w.D)
@@ -159,6 +161,7 @@ def main(argv=None):
     bytes_per = w.numel * per_elem
     print(json.dumps({"workload": w.name, "N": w.numel, "padded_numel": N, "D": w.D,
                       "mode": args.mode, "grad_dtype": w.grad_dtype, "param_dtype": args.param_dtype,
+                      "instances": args.instances,
                       "n_buckets": L.n_buckets, "streams": args.streams, "plan": args.plan,
                       "launches": args.launches, "ms_per_launch": ms,
                       "algorithmic_bytes_per_launch": bytes_per,
