@@ -123,29 +123,55 @@ for pin in pins.ALL_PINS:
         pin(lib)
     except BaseException as e:
         failed.append(pin.__name__)
+        if {first_only!r}:
+            break  # a mutant is caught by its first failing pin
 print("FAILED_PINS", ",".join(failed))
 sys.exit(1 if failed else 0)
 """
 
 
-@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
-def test_mutant_is_caught(name, old, new, tmp_path):
+def _run_mutant(name, old, new, workdir):
+    """Compile the oracle with one planted mistake and run the pins on it in
+    a subprocess; returns (site found once, caught, output)."""
     with open(os.path.join(ROOT, "oracle", "dopt_oracle.c")) as f:
         src = f.read()
-    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
-    mutated = tmp_path / "mutant.c"
-    mutated.write_text(src.replace(old, new))
-    so = tmp_path / "libmutant.so"
-    oracle._compile(str(mutated), str(so))
-    code = RUNNER.format(root=ROOT, tests=os.path.join(ROOT, "tests"), path=str(so))
+    if src.count(old) != 1:
+        return False, False, f"mutation site for {name} not found exactly once"
+    mutated = os.path.join(workdir, f"{name}.c")
+    with open(mutated, "w") as f:
+        f.write(src.replace(old, new))
+    so = os.path.join(workdir, f"lib{name}.so")
+    oracle._compile(mutated, so)
+    code = RUNNER.format(root=ROOT, tests=os.path.join(ROOT, "tests"), path=so, first_only=True)
     res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True,
                          timeout=600)
-    assert res.returncode != 0, f"mutant {name} passed every pin:\n{res.stdout}\n{res.stderr}"
+    return True, res.returncode != 0, res.stdout + res.stderr
+
+
+@pytest.fixture(scope="module")
+def mutant_results(tmp_path_factory):
+    """Every mutant compiled and run at once (subprocesses in parallel: each
+    is independent, and one that crashes takes only itself down)."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    workdir = str(tmp_path_factory.mktemp("mutants"))
+    workers = max(1, min(len(MUTANTS), os.cpu_count() or 1))
+    with ThreadPoolExecutor(workers) as ex:
+        futures = {m[0]: ex.submit(_run_mutant, *m, workdir) for m in MUTANTS}
+    return {name: f.result() for name, f in futures.items()}
+
+
+@pytest.mark.parametrize("name", [m[0] for m in MUTANTS])
+def test_mutant_is_caught(name, mutant_results):
+    found, caught, output = mutant_results[name]
+    assert found, output
+    assert caught, f"mutant {name} passed every pin:\n{output}"
 
 
 def test_runner_passes_unmutated_oracle():
     """Control: the same runner on the unmodified oracle reports no failure."""
-    code = RUNNER.format(root=ROOT, tests=os.path.join(ROOT, "tests"), path=oracle.build())
+    code = RUNNER.format(root=ROOT, tests=os.path.join(ROOT, "tests"), path=oracle.build(),
+                         first_only=False)
     res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True,
                          timeout=600)
     assert res.returncode == 0, res.stdout + res.stderr
