@@ -37,7 +37,8 @@ def _equal(a, b):
 
 
 @pytest.mark.parametrize("D,instances,grad_dtype", [(4, 1, "bf16"), (8, 2, "fp32"), (3, 1, "bf16"),
-                                                     (16, 1, "fp32")])
+                                                     (16, 1, "fp32"), (8, 2, "bf16"),
+                                                     (16, 4, "fp16")])
 def test_counted_equals_host_step(D, instances, grad_dtype):
     L, s, p, g, _ = _case([5000, 1, 7, 300, 20000, 3, 9999], [1, 0, 1, 0, 1, 1, 0], D, 9000, 8,
                           grad_dtype, seed=D, instances=instances)
@@ -273,16 +274,17 @@ def test_counted_after_a_counter_write_on_the_stream():
     assert B.counter_state(counter) == (4, 0)
 
 
-def _clip_case(seed=31):
-    return _case([5000, 1, 7, 300, 20000, 3, 9999], [1, 0, 1, 0, 1, 1, 0], 8, 0, 1, "bf16",
-                 steps=3, seed=seed)
+def _clip_case(seed=31, grad_dtype="bf16", instances=1):
+    return _case([5000, 1, 7, 300, 20000, 3, 9999], [1, 0, 1, 0, 1, 1, 0], 8, 0, 1, grad_dtype,
+                 steps=3, seed=seed, instances=instances)
 
 
-def test_clipped_counted_equals_clipped_in_a_graph():
+@pytest.mark.parametrize("grad_dtype,instances", [("bf16", 1), ("fp16", 2), ("fp32", 4)])
+def test_clipped_counted_equals_clipped_in_a_graph(grad_dtype, instances):
     """Three counted clipped steps replayed from one graph equal three
     clipped steps with host step numbers: state, params, main grads and
     the norm report, bit for bit."""
-    L, s, p, g, _ = _clip_case()
+    L, s, p, g, _ = _clip_case(grad_dtype=grad_dtype, instances=instances)
     N = L.padded_numel
     s2, p2 = _clone(s, p)
     adam = B.AdamConfig(grad_scale=1.0 / 8)
