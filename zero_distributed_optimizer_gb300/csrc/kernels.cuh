@@ -444,20 +444,18 @@ struct GradVec<float> {
     }
 };
 
-// Scaled rank-order fp32 reduction of 8 elements over the D replicas.  The
-// compile-time-D form serves one instance; the run-time form reduces each
-// group of R consecutive replicas in rank order and adds the groups' sums in
-// group order (several optimizer instances; with R = D the last group's sum
-// is copied, so the result is the plain rank-order sum).
 // The compile-time-D reduction of 8 elements from replicas already loaded:
-// the rank-order sum (one instance), or with HIER each group of R
+// the rank-order sum (one instance, GR = DC), or each group of GR
 // consecutive replicas in rank order and then the groups' sums in group
-// order (several instances, R a run-time divisor of D).  HIER is a separate
-// instantiation so that the one-instance kernels stay as they are.
-template <typename G, int DC, bool HIER>
-__device__ __forceinline__ void reduce_loaded(const GradVec<G> (&g)[DC], float scale, int R,
-                                              float (&acc)[8]) {
-    if constexpr (!HIER) {
+// order (DC / GR instances).  The group size is a template argument so that
+// the grouped sum unrolls into the same straight-line code as the plain one.
+// (With the group size read at run time, the branch at each group's end
+// kept the state loads behind the whole reduction: 1.3 % slower at D = 8 as
+// 2 instances and 8 % at D = 2 as 2.)
+template <typename G, int DC, int GR>
+__device__ __forceinline__ void reduce_loaded(const GradVec<G> (&g)[DC], float scale, float (&acc)[8]) {
+    static_assert(GR > 0 && DC % GR == 0, "the group size divides the replica count");
+    if constexpr (GR == DC) {
 #pragma unroll
         for (int r = 0; r < DC; ++r) {
             float f[8];
@@ -470,7 +468,6 @@ __device__ __forceinline__ void reduce_loaded(const GradVec<G> (&g)[DC], float s
         }
     } else {
         float part[8];
-        int in_group = 0;  // position of replica r inside its group
 #pragma unroll
         for (int r = 0; r < DC; ++r) {
             float f[8];
@@ -478,26 +475,27 @@ __device__ __forceinline__ void reduce_loaded(const GradVec<G> (&g)[DC], float s
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const float x = __fmul_rn(scale, f[k]);
-                part[k] = in_group == 0 ? x : __fadd_rn(part[k], x);
-            }
-            if (++in_group == R) {
-                in_group = 0;
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    acc[k] = r + 1 == R ? part[k] : __fadd_rn(acc[k], part[k]);
+                part[k] = r % GR == 0 ? x : __fadd_rn(part[k], x);
+                if (r % GR == GR - 1) acc[k] = r == GR - 1 ? part[k] : __fadd_rn(acc[k], part[k]);
             }
         }
     }
 }
 
-template <typename G, int DC, bool HIER = false, typename Args>
+// Scaled rank-order fp32 reduction of 8 elements over the D replicas.  The
+// compile-time-D form loads every replica first (one instance, or groups of
+// GR); the run-time form loads 4 replicas at a time and reduces each
+// group of R consecutive replicas in rank order, adding the groups' sums in
+// group order (several optimizer instances; with R = D the last group's sum
+// is copied, so the result is the plain rank-order sum).
+template <typename G, int DC, int GR = DC, typename Args>
 __device__ __forceinline__ void reduce_vec(const Args &a, float scale, int64_t e0,
                                            float (&acc)[8]) {
     if constexpr (DC > 0) {
         GradVec<G> g[DC];
 #pragma unroll
         for (int r = 0; r < DC; ++r) g[r].load(a.grads[r], e0);
-        reduce_loaded<G, DC, HIER>(g, scale, a.R, acc);
+        reduce_loaded<G, DC, GR>(g, scale, acc);
     } else {
         constexpr int kBatch = 4;
         float part[8];
@@ -609,7 +607,7 @@ __device__ __forceinline__ void update_and_store(const StepArgs &a, const Scalar
 }
 
 // A vector of 8 owned elements of one run, loading as it goes.
-template <typename G, int DC, int MODE, bool HIER>
+template <typename G, int DC, int MODE, int GR>
 __device__ __forceinline__ void full_vector(const StepArgs &a, const Scalars &sc, StepDep dep, int64_t e0,
                                             int32_t meta, int32_t status = 0) {
     float acc[8];
@@ -621,7 +619,7 @@ __device__ __forceinline__ void full_vector(const StepArgs &a, const Scalars &sc
 #pragma unroll
         for (int k = 0; k < 8; ++k) acc[k] = __fmul_rn(f[k], coef);
     } else {
-        reduce_vec<G, DC, HIER>(a, sc.scale, e0, acc);
+        reduce_vec<G, DC, GR>(a, sc.scale, e0, acc);
         if (a.round_grad) to_grad_type8<G>(acc);
     }
     if constexpr (MODE == kWriteGrads) write_grads_vec<G, DC>(a.grads, a.D, e0, acc);
@@ -660,7 +658,7 @@ __device__ __forceinline__ void full_vector_preloaded(const StepArgs &a, const S
                                                       int64_t e0, int32_t meta, int32_t status,
                                                       const Preloaded<G, DC> &p) {
     float acc[8];
-    reduce_loaded<G, DC, false>(p.g, sc.scale, a.R, acc);
+    reduce_loaded<G, DC, DC>(p.g, sc.scale, acc);
     if (a.round_grad) to_grad_type8<G>(acc);
     if constexpr (MODE == kWriteGrads) write_grads_vec<G, DC>(a.grads, a.D, e0, acc);
     update_and_store<G, DC, MODE>(a, sc, dep, e0, meta, status, acc, p.w0, p.w1, p.m0, p.m1,
@@ -712,7 +710,7 @@ __device__ __noinline__ void mixed_vector(const StepArgs &a, const Scalars &sc, 
 // One tile per CTA: this thread's vector of 8 elements.  `sc` is the
 // launch's own scalars (read from the constant bank); `dep` holds the two
 // step-dependent ones, which the counted step takes from its counter.
-template <typename G, int DC, int MODE, bool HIER>
+template <typename G, int DC, int MODE, int GR>
 __device__ __forceinline__ void step_vector(const StepArgs &a, const Scalars &sc, StepDep dep,
                                             int32_t status) {
     const int64_t tile = a.rv.tile0 + blockIdx.x;
@@ -734,7 +732,7 @@ __device__ __forceinline__ void step_vector(const StepArgs &a, const Scalars &sc
     } else {
         const VecKind kind = locate(a.rv, tile, e0, j);
         if (kind == kFull) {
-            full_vector<G, DC, MODE, HIER>(a, sc, dep, e0, a.rv.run_meta[j], status);
+            full_vector<G, DC, MODE, GR>(a, sc, dep, e0, a.rv.run_meta[j], status);
         } else if (kind == kMixed) {
             if (status != 0) return;
             mixed_vector<G, DC, MODE>(a, sc, dep, e0, j);
@@ -742,7 +740,8 @@ __device__ __forceinline__ void step_vector(const StepArgs &a, const Scalars &sc
     }
 }
 
-template <typename G, int DC, int MODE, bool HIER = false>
+// GR: the replicas of one optimizer instance (GR = DC: one instance).
+template <typename G, int DC, int MODE, int GR = DC>
 __global__ void __launch_bounds__(kThreads, 3) dopt_step_kernel(const __grid_constant__ StepArgs a) {
     bool counted = MODE == kCounted;
     if constexpr (MODE == kFromMain) counted = a.counter != nullptr;  // the counted clipped step
@@ -757,13 +756,12 @@ __global__ void __launch_bounds__(kThreads, 3) dopt_step_kernel(const __grid_con
         // memory behind a CTA barrier cost 1.7 %; a persistent grid that
         // reads it once per resident CTA cost 15 %.)
         const uint4 hot = *reinterpret_cast<const uint4 *>(&a.counter->hot);
-        step_vector<G, DC, MODE, HIER>(a, a.sc,
-                                       StepDep{__uint_as_float(hot.x), __uint_as_float(hot.y)},
-                                 int32_t(hot.z));
+        step_vector<G, DC, MODE, GR>(a, a.sc, StepDep{__uint_as_float(hot.x), __uint_as_float(hot.y)},
+                                     int32_t(hot.z));
     } else {
         // every scalar stays in the constant bank (a copy of them in
         // registers cost the D = 2 step 4 %)
-        step_vector<G, DC, MODE, HIER>(a, a.sc, StepDep{a.sc.step_size, a.sc.bc2_sqrt}, 0);
+        step_vector<G, DC, MODE, GR>(a, a.sc, StepDep{a.sc.step_size, a.sc.bc2_sqrt}, 0);
     }
 }
 
@@ -811,7 +809,7 @@ __global__ void dopt_count_step_kernel(CounterBlock *c, const dopt_adam_cfg cfg)
 // The same launch bounds as the step kernel: 0.6 % faster at D = 8 and
 // 0.3 % at D = 16.  (The gather kernel keeps the default: 3 CTAs per SM
 // helped at D = 8 by 0.5 % and cost 4 % at D = 4.)
-template <typename G, int DC, bool HIER = false>
+template <typename G, int DC, int GR = DC>
 __global__ void __launch_bounds__(kThreads, 3) dopt_allreduce_kernel(const __grid_constant__ AllReduceArgs a) {
     const int64_t tile = a.rv.tile0 + blockIdx.x;
     const int64_t e0 = tile * kDoptTileElems + int64_t(threadIdx.x) * kVec;
@@ -819,7 +817,7 @@ __global__ void __launch_bounds__(kThreads, 3) dopt_allreduce_kernel(const __gri
     const VecKind kind = locate(a.rv, tile, e0, j);
     if (kind == kFull) {
         float acc[8];
-        reduce_vec<G, DC, HIER>(a, a.scale, e0, acc);
+        reduce_vec<G, DC, GR>(a, a.scale, e0, acc);
         write_grads_vec<G, DC>(a.grads, a.D, e0, acc);
     } else if (kind == kMixed) {
         const int D = DC > 0 ? DC : a.D;

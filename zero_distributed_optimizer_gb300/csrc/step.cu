@@ -74,40 +74,47 @@ StepKernel pick_step_kernel(int D) {
     }
 }
 
+// The grouped kernels: D replicas in instances of R (1 < R < D).
 template <typename G, int MODE>
-StepKernel pick_step_kernel_hier(int D) {
-    switch (D) {
-        case 2: return dopt_step_kernel<G, 2, MODE, true>;
-        case 4: return dopt_step_kernel<G, 4, MODE, true>;
-        case 8: return dopt_step_kernel<G, 8, MODE, true>;
-        case 16: return dopt_step_kernel<G, 16, MODE, true>;
+StepKernel pick_step_kernel_grouped(int D, int R) {
+    switch (D * 100 + R) {
+        case 402: return dopt_step_kernel<G, 4, MODE, 2>;
+        case 802: return dopt_step_kernel<G, 8, MODE, 2>;
+        case 804: return dopt_step_kernel<G, 8, MODE, 4>;
+        case 1602: return dopt_step_kernel<G, 16, MODE, 2>;
+        case 1604: return dopt_step_kernel<G, 16, MODE, 4>;
+        case 1608: return dopt_step_kernel<G, 16, MODE, 8>;
         default: return dopt_step_kernel<G, 0, MODE>;
     }
 }
 
 // The kernels a layout takes.  D in {1, 2, 4, 8, 16} has compile-time
-// forms; with several optimizer instances the step and all-reduce kernels
-// of 16-bit grads have forms that reduce group by group (HIER: 2.6 % faster
-// than the run-time form at D = 8 as 2 instances, 3.4 % at D = 2 as 2),
-// while fp32 grads (whose unrolled grouped reduction spills) and any other
-// D take the run-time form.
-bool use_hier(const dopt_layout *L, dopt_dtype grad_dtype) {
+// forms.  With several optimizer instances of R ranks each, the step and
+// all-reduce kernels of 16-bit grads have compile-time forms for every
+// (D, R) with D in {4, 8, 16} (the grouped sum unrolled like the plain
+// one); fp32 grads (whose unrolled grouped reduction spills) and any other
+// D take the run-time form.  Groups of one replica each (as many instances
+// as ranks) add up exactly like one group, in rank order, so that layout
+// takes the one-instance kernels; only the ranks' write-back stride (R = 1)
+// differs, and the kernels read it at run time.
+bool grouped(const dopt_layout *L) { return L->cfg.instances > 1 && L->cfg.instances < L->cfg.D; }
+int group_size(const dopt_layout *L) { return L->cfg.D / L->cfg.instances; }
+bool use_grouped_kernel(const dopt_layout *L, dopt_dtype grad_dtype) {
     const int D = L->cfg.D;
-    return L->cfg.instances > 1 && grad_dtype != DOPT_FP32 &&
-           (D == 2 || D == 4 || D == 8 || D == 16);
+    return grouped(L) && grad_dtype != DOPT_FP32 && (D == 4 || D == 8 || D == 16);
 }
-int kernel_D(const dopt_layout *L) { return L->cfg.instances > 1 ? 0 : L->cfg.D; }
+int kernel_D(const dopt_layout *L) { return grouped(L) ? 0 : L->cfg.D; }
 
 template <int MODE>
 StepKernel step_kernel_for(const dopt_layout *L, dopt_dtype grad_dtype) {
-    const bool hier = use_hier(L, grad_dtype);
+    const bool g = use_grouped_kernel(L, grad_dtype);
     switch (grad_dtype) {
         case DOPT_BF16:
-            return hier ? pick_step_kernel_hier<__nv_bfloat16, MODE>(L->cfg.D)
-                        : pick_step_kernel<__nv_bfloat16, MODE>(kernel_D(L));
+            return g ? pick_step_kernel_grouped<__nv_bfloat16, MODE>(L->cfg.D, group_size(L))
+                     : pick_step_kernel<__nv_bfloat16, MODE>(kernel_D(L));
         case DOPT_FP16:
-            return hier ? pick_step_kernel_hier<__half, MODE>(L->cfg.D)
-                        : pick_step_kernel<__half, MODE>(kernel_D(L));
+            return g ? pick_step_kernel_grouped<__half, MODE>(L->cfg.D, group_size(L))
+                     : pick_step_kernel<__half, MODE>(kernel_D(L));
         default: return pick_step_kernel<float, MODE>(kernel_D(L));
     }
 }
@@ -135,28 +142,41 @@ NormKernel norm_kernel_for(const dopt_layout *L, dopt_dtype grad_dtype) {
     }
 }
 
-template <typename G, bool HIER>
+template <typename G>
 AllReduceKernel pick_allreduce_kernel(int D) {
     switch (D) {
-        case 1: return HIER ? dopt_allreduce_kernel<G, 0> : dopt_allreduce_kernel<G, 1>;
-        case 2: return dopt_allreduce_kernel<G, 2, HIER>;
-        case 4: return dopt_allreduce_kernel<G, 4, HIER>;
-        case 8: return dopt_allreduce_kernel<G, 8, HIER>;
-        case 16: return dopt_allreduce_kernel<G, 16, HIER>;
+        case 1: return dopt_allreduce_kernel<G, 1>;
+        case 2: return dopt_allreduce_kernel<G, 2>;
+        case 4: return dopt_allreduce_kernel<G, 4>;
+        case 8: return dopt_allreduce_kernel<G, 8>;
+        case 16: return dopt_allreduce_kernel<G, 16>;
+        default: return dopt_allreduce_kernel<G, 0>;
+    }
+}
+
+template <typename G>
+AllReduceKernel pick_allreduce_kernel_grouped(int D, int R) {
+    switch (D * 100 + R) {
+        case 402: return dopt_allreduce_kernel<G, 4, 2>;
+        case 802: return dopt_allreduce_kernel<G, 8, 2>;
+        case 804: return dopt_allreduce_kernel<G, 8, 4>;
+        case 1602: return dopt_allreduce_kernel<G, 16, 2>;
+        case 1604: return dopt_allreduce_kernel<G, 16, 4>;
+        case 1608: return dopt_allreduce_kernel<G, 16, 8>;
         default: return dopt_allreduce_kernel<G, 0>;
     }
 }
 
 AllReduceKernel allreduce_kernel_for(const dopt_layout *L, dopt_dtype grad_dtype) {
-    const bool hier = use_hier(L, grad_dtype);
+    const bool g = use_grouped_kernel(L, grad_dtype);
     switch (grad_dtype) {
         case DOPT_BF16:
-            return hier ? pick_allreduce_kernel<__nv_bfloat16, true>(L->cfg.D)
-                        : pick_allreduce_kernel<__nv_bfloat16, false>(kernel_D(L));
+            return g ? pick_allreduce_kernel_grouped<__nv_bfloat16>(L->cfg.D, group_size(L))
+                     : pick_allreduce_kernel<__nv_bfloat16>(kernel_D(L));
         case DOPT_FP16:
-            return hier ? pick_allreduce_kernel<__half, true>(L->cfg.D)
-                        : pick_allreduce_kernel<__half, false>(kernel_D(L));
-        default: return pick_allreduce_kernel<float, false>(kernel_D(L));
+            return g ? pick_allreduce_kernel_grouped<__half>(L->cfg.D, group_size(L))
+                     : pick_allreduce_kernel<__half>(kernel_D(L));
+        default: return pick_allreduce_kernel<float>(kernel_D(L));
     }
 }
 
