@@ -15,6 +15,10 @@ from zero_distributed_optimizer_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
+# Every group size the compile-time grouped kernels take (D = 4 in 2; 8 in
+# 2, 4; 16 in 2, 4, 8, where fp32 grads take the run-time form), the
+# run-time form (D = 6 in 3), and groups of one rank (D = 8 in 8, D = 4 in
+# 4), which take the one-instance kernels.
 CASES = [
     # sizes, wd, D, instances, bucket, pad
     ([130, 260, 90, 310, 210], None, 4, 2, 0, 1),
@@ -23,6 +27,9 @@ CASES = [
     ([65536, 1000, 65536], [1, 0, 1], 16, 4, 0, 64),
     ([123457, 99], [1, 0], 8, 8, 0, 1),
     ([31000, 17, 64000, 5], [1, 0, 1, 0], 8, 4, 30000, 3),
+    ([40000, 3, 24000, 77], [1, 0, 1, 1], 16, 2, 0, 1),
+    ([40000, 3, 24000, 77], [0, 1, 1, 0], 16, 8, 30000, 2),
+    ([999, 1001, 64], None, 4, 4, 0, 1),
 ]
 
 

@@ -74,26 +74,35 @@ StepKernel pick_step_kernel(int D) {
     }
 }
 
-// The grouped kernels: D replicas in instances of R (1 < R < D).
+// The grouped kernels: D replicas in instances of R (1 < R < D); fp32
+// grads at D = 16 take the run-time form.
 template <typename G, int MODE>
 StepKernel pick_step_kernel_grouped(int D, int R) {
     switch (D * 100 + R) {
         case 402: return dopt_step_kernel<G, 4, MODE, 2>;
         case 802: return dopt_step_kernel<G, 8, MODE, 2>;
         case 804: return dopt_step_kernel<G, 8, MODE, 4>;
-        case 1602: return dopt_step_kernel<G, 16, MODE, 2>;
-        case 1604: return dopt_step_kernel<G, 16, MODE, 4>;
-        case 1608: return dopt_step_kernel<G, 16, MODE, 8>;
-        default: return dopt_step_kernel<G, 0, MODE>;
+        case 1602:
+            if constexpr (sizeof(G) == 2) return dopt_step_kernel<G, 16, MODE, 2>;
+            break;
+        case 1604:
+            if constexpr (sizeof(G) == 2) return dopt_step_kernel<G, 16, MODE, 4>;
+            break;
+        case 1608:
+            if constexpr (sizeof(G) == 2) return dopt_step_kernel<G, 16, MODE, 8>;
+            break;
+        default: break;
     }
+    return dopt_step_kernel<G, 0, MODE>;
 }
 
 // The kernels a layout takes.  D in {1, 2, 4, 8, 16} has compile-time
 // forms.  With several optimizer instances of R ranks each, the step and
-// all-reduce kernels of 16-bit grads have compile-time forms for every
-// (D, R) with D in {4, 8, 16} (the grouped sum unrolled like the plain
-// one); fp32 grads (whose unrolled grouped reduction spills) and any other
-// D take the run-time form.  Groups of one replica each (as many instances
+// all-reduce kernels have compile-time forms for every (D, R) with D in
+// {4, 8, 16} (the grouped sum unrolled like the plain one, with the same
+// registers); fp32 grads use them for D up to 8 (D = 16 as 2 instances ran
+// 0.3 % slower than the run-time form).  Any other layout takes the
+// run-time form.  Groups of one replica each (as many instances
 // as ranks) add up exactly like one group, in rank order, so that layout
 // takes the one-instance kernels; only the ranks' write-back stride (R = 1)
 // differs, and the kernels read it at run time.
@@ -101,7 +110,7 @@ bool grouped(const dopt_layout *L) { return L->cfg.instances > 1 && L->cfg.insta
 int group_size(const dopt_layout *L) { return L->cfg.D / L->cfg.instances; }
 bool use_grouped_kernel(const dopt_layout *L, dopt_dtype grad_dtype) {
     const int D = L->cfg.D;
-    return grouped(L) && grad_dtype != DOPT_FP32 && (D == 4 || D == 8 || D == 16);
+    return grouped(L) && (D == 4 || D == 8 || (D == 16 && grad_dtype != DOPT_FP32));
 }
 int kernel_D(const dopt_layout *L) { return grouped(L) ? 0 : L->cfg.D; }
 
@@ -115,7 +124,9 @@ StepKernel step_kernel_for(const dopt_layout *L, dopt_dtype grad_dtype) {
         case DOPT_FP16:
             return g ? pick_step_kernel_grouped<__half, MODE>(L->cfg.D, group_size(L))
                      : pick_step_kernel<__half, MODE>(kernel_D(L));
-        default: return pick_step_kernel<float, MODE>(kernel_D(L));
+        default:
+            return g ? pick_step_kernel_grouped<float, MODE>(L->cfg.D, group_size(L))
+                     : pick_step_kernel<float, MODE>(kernel_D(L));
     }
 }
 
@@ -132,8 +143,9 @@ NormKernel pick_norm_kernel(int D) {
 }
 
 // The norm pass keeps the run-time form for several instances: its grouped
-// compile-time form held 60 registers instead of 32, which cost the
-// persistent grid residency and the clipped step 0.2 %.
+// compile-time forms (one per (D, R), 34-74 registers against 64-80 for the
+// run-time form) made the clipped step 0.2 % slower at D = 8 as 2 instances
+// and 6 % with fp32 grads, for 0.5 % at D = 8 as 4.
 NormKernel norm_kernel_for(const dopt_layout *L, dopt_dtype grad_dtype) {
     switch (grad_dtype) {
         case DOPT_BF16: return pick_norm_kernel<__nv_bfloat16>(kernel_D(L));
@@ -160,11 +172,18 @@ AllReduceKernel pick_allreduce_kernel_grouped(int D, int R) {
         case 402: return dopt_allreduce_kernel<G, 4, 2>;
         case 802: return dopt_allreduce_kernel<G, 8, 2>;
         case 804: return dopt_allreduce_kernel<G, 8, 4>;
-        case 1602: return dopt_allreduce_kernel<G, 16, 2>;
-        case 1604: return dopt_allreduce_kernel<G, 16, 4>;
-        case 1608: return dopt_allreduce_kernel<G, 16, 8>;
-        default: return dopt_allreduce_kernel<G, 0>;
+        case 1602:
+            if constexpr (sizeof(G) == 2) return dopt_allreduce_kernel<G, 16, 2>;
+            break;
+        case 1604:
+            if constexpr (sizeof(G) == 2) return dopt_allreduce_kernel<G, 16, 4>;
+            break;
+        case 1608:
+            if constexpr (sizeof(G) == 2) return dopt_allreduce_kernel<G, 16, 8>;
+            break;
+        default: break;
     }
+    return dopt_allreduce_kernel<G, 0>;
 }
 
 AllReduceKernel allreduce_kernel_for(const dopt_layout *L, dopt_dtype grad_dtype) {
@@ -176,7 +195,9 @@ AllReduceKernel allreduce_kernel_for(const dopt_layout *L, dopt_dtype grad_dtype
         case DOPT_FP16:
             return g ? pick_allreduce_kernel_grouped<__half>(L->cfg.D, group_size(L))
                      : pick_allreduce_kernel<__half>(kernel_D(L));
-        default: return pick_allreduce_kernel<float>(kernel_D(L));
+        default:
+            return g ? pick_allreduce_kernel_grouped<float>(L->cfg.D, group_size(L))
+                     : pick_allreduce_kernel<float>(kernel_D(L));
     }
 }
 
