@@ -375,6 +375,34 @@ __device__ __forceinline__ bool owned_at(const RunView &v, int64_t e, int &j, bo
     return v.run_start[j] <= e;
 }
 
+// The vectors of a warp that straddle a run edge (padding, another decay
+// flag or owner in them), shared out over the warp's lanes: `mixed` holds
+// the lanes whose vector straddles (the same in every lane, so every lane
+// must call this); in each round the four octets of lanes take one such
+// vector each, one element per lane, and f(e, run meta) runs for each owned
+// element.  (One lane per vector, element after element with each
+// element's loads waited on in turn, the step of a 1000-element layout took
+// 11.3 us a step against 6.4 us.)  The warp's first run is looked up again
+// here so that the vector path keeps no run index alive.
+template <typename F>
+__device__ __forceinline__ void for_straddling_elements(const RunView &v, int64_t tile, unsigned mixed,
+                                                        F &&f) {
+    const int lane = threadIdx.x & 31;
+    const int octet = lane >> 3;
+    const int64_t warp_e0 = tile * kDoptTileElems + int64_t(threadIdx.x & ~31) * kVec;
+    const int jw = warp_first_run(v.run_end, v.run_limit, max(v.tile_run[tile], v.run_begin), warp_e0, lane);
+    while (mixed != 0) {
+        unsigned mine = mixed;  // this octet's vector: the octet-th lane left in `mixed`
+        for (int s = 0; s < octet && mine != 0; ++s) mine &= mine - 1;
+        for (int s = 0; s < 4 && mixed != 0; ++s) mixed &= mixed - 1;
+        if (mine == 0) continue;
+        const int64_t e = warp_e0 + int64_t(__ffs(mine) - 1) * kVec + (lane & 7);
+        int j = jw;
+        bool done = false;
+        if (owned_at(v, e, j, done)) f(e, v.run_meta[j]);
+    }
+}
+
 template <typename G>
 __device__ __forceinline__ float load_grad_scalar(const void *base, int64_t i) {
     if constexpr (std::is_same_v<G, __nv_bfloat16>)
@@ -665,14 +693,8 @@ __device__ __forceinline__ void full_vector_preloaded(const StepArgs &a, const S
                                   p.v0, p.v1);
 }
 
-// The vectors of a warp that straddle a run edge (padding, another decay
-// flag or owner in them), shared out over the warp's lanes: in each round
-// the four octets of lanes take one such vector each, one element per lane,
-// and each lane updates its element if it is owned.  (One lane per vector,
-// element after element with each element's loads waited on in turn, the
-// step of a 1000-element layout took about 12 us.)  `mixed` holds the lanes
-// whose vector straddles (the same in every lane).  The warp's first run is
-// looked up again here so that the hot path keeps no run index alive.
+// The step of the warp's vectors that straddle a run edge, element by
+// element over the warp's lanes (for_straddling_elements).
 template <typename G, int DC, int MODE>
 __device__ __noinline__ void mixed_elements(const StepArgs &a, const Scalars &sc, StepDep dep,
                                             unsigned mixed) {
@@ -680,22 +702,7 @@ __device__ __noinline__ void mixed_elements(const StepArgs &a, const Scalars &sc
         if (a.skip_nonfinite && isnan(*a.clip_coef)) return;  // the step is skipped
     }
     const int D = DC > 0 ? DC : a.D;
-    const int lane = threadIdx.x & 31;
-    const int octet = lane >> 3;
-    const int64_t tile = a.rv.tile0 + blockIdx.x;
-    const int64_t warp_e0 = tile * kDoptTileElems + int64_t(threadIdx.x & ~31) * kVec;
-    const int jw = warp_first_run(a.rv.run_end, a.rv.run_limit, max(a.rv.tile_run[tile], a.rv.run_begin),
-                                  warp_e0, lane);
-    while (mixed != 0) {
-        unsigned mine = mixed;  // this octet's vector: the octet-th lane left in `mixed`
-        for (int s = 0; s < octet && mine != 0; ++s) mine &= mine - 1;
-        for (int s = 0; s < 4 && mixed != 0; ++s) mixed &= mixed - 1;
-        if (mine == 0) continue;
-        const int64_t e = warp_e0 + int64_t(__ffs(mine) - 1) * kVec + (lane & 7);
-        int jr = jw;
-        bool done = false;
-        if (!owned_at(a.rv, e, jr, done)) continue;
-        const int32_t meta = a.rv.run_meta[jr];
+    for_straddling_elements(a.rv, a.rv.tile0 + blockIdx.x, mixed, [&](int64_t e, int32_t meta) {
         float g;
         if constexpr (MODE == kFromMain) {
             g = __fmul_rn(a.main_grad_in[e], *a.clip_coef);
@@ -718,7 +725,7 @@ __device__ __noinline__ void mixed_elements(const StepArgs &a, const Scalars &sc
             for (int r = meta >> kRunRankShift; r < D; r += a.R)
                 static_cast<uint16_t *>(a.params[r])[e] = bits;
         }
-    }
+    });
 }
 
 // At least 3 CTAs per SM: this lets ptxas use up to 85 registers where it
@@ -818,6 +825,17 @@ __global__ void dopt_count_step_kernel(CounterBlock *c, const dopt_adam_cfg cfg)
 // replica, rounded to the grad type.
 // ---------------------------------------------------------------------------
 
+// The all-reduce of the warp's vectors that straddle a run edge, element by
+// element over the warp's lanes.
+template <typename G, int DC>
+__device__ __noinline__ void allreduce_mixed(const AllReduceArgs &a, unsigned mixed) {
+    const int D = DC > 0 ? DC : a.D;
+    for_straddling_elements(a.rv, a.rv.tile0 + blockIdx.x, mixed, [&](int64_t e, int32_t) {
+        const float g = reduce_scalar<G>(a.grads, D, a.R, a.scale, e);
+        for (int r = 0; r < D; ++r) store_grad_scalar<G>(a.grads[r], e, g);
+    });
+}
+
 // The same launch bounds as the step kernel: 0.6 % faster at D = 8 and
 // 0.3 % at D = 16.  (The gather kernel keeps the default: 3 CTAs per SM
 // helped at D = 8 by 0.5 % and cost 4 % at D = 4.)
@@ -831,16 +849,9 @@ __global__ void __launch_bounds__(kThreads, 3) dopt_allreduce_kernel(const __gri
         float acc[8];
         reduce_vec<G, DC, GR>(a, a.scale, e0, acc);
         write_grads_vec<G, DC>(a.grads, a.D, e0, acc);
-    } else if (kind == kMixed) {
-        const int D = DC > 0 ? DC : a.D;
-        bool done = false;
-        for (int k = 0; k < kVec && !done; ++k) {
-            const int64_t e = e0 + k;
-            if (!owned_at(a.rv, e, j, done)) continue;
-            const float g = reduce_scalar<G>(a.grads, D, a.R, a.scale, e);
-            for (int r = 0; r < D; ++r) store_grad_scalar<G>(a.grads[r], e, g);
-        }
     }
+    const unsigned mixed = __ballot_sync(0xffffffffu, kind == kMixed);
+    if (mixed != 0) allreduce_mixed<G, DC>(a, mixed);
 }
 
 // ---------------------------------------------------------------------------
@@ -885,6 +896,9 @@ __global__ void __launch_bounds__(kThreads) dopt_rs_norm_kernel(const __grid_con
             const float s45 = __fadd_rn(sq[4], sq[5]), s67 = __fadd_rn(sq[6], sq[7]);
             local += double(__fadd_rn(__fadd_rn(s01, s23), __fadd_rn(s45, s67)));
         } else if (kind == kMixed) {
+            // one lane per straddling vector: sharing them out over the warp
+            // (as the other kernels do) made this persistent loop, and the
+            // clipped step, 1.7 % slower
             const int D = DC > 0 ? DC : a.D;
             bool done = false;
             for (int k = 0; k < kVec && !done; ++k) {
@@ -955,6 +969,19 @@ __global__ void __launch_bounds__(kThreads) dopt_rs_norm_kernel(const __grid_con
 // The gather kernel: each rank's owned elements from its replica to all.
 // ---------------------------------------------------------------------------
 
+// The gather of the warp's vectors that straddle a run edge, element by
+// element over the warp's lanes.
+__device__ __noinline__ void gather_mixed(const GatherArgs &a, unsigned mixed) {
+    for_straddling_elements(a.rv, a.rv.tile0 + blockIdx.x, mixed, [&](int64_t e, int32_t meta) {
+        const int q = meta >> kRunRankShift;
+        for (int base = 0; base < a.D; base += a.R) {
+            const uint16_t bits = static_cast<const uint16_t *>(a.params[base + q])[e];
+            for (int r = base; r < base + a.R; ++r)
+                if (r != base + q) static_cast<uint16_t *>(a.params[r])[e] = bits;
+        }
+    });
+}
+
 __global__ void __launch_bounds__(kThreads) dopt_gather_kernel(const __grid_constant__ GatherArgs a) {
     const int64_t tile = a.rv.tile0 + blockIdx.x;
     const int64_t e0 = tile * kDoptTileElems + int64_t(threadIdx.x) * kVec;
@@ -967,19 +994,9 @@ __global__ void __launch_bounds__(kThreads) dopt_gather_kernel(const __grid_cons
             for (int r = base; r < base + a.R; ++r)
                 if (r != base + q) st_stream(static_cast<__nv_bfloat16 *>(a.params[r]) + e0, val);
         }
-    } else if (kind == kMixed) {
-        bool done = false;
-        for (int k = 0; k < kVec && !done; ++k) {
-            const int64_t e = e0 + k;
-            if (!owned_at(a.rv, e, j, done)) continue;
-            const int q = a.rv.run_meta[j] >> kRunRankShift;
-            for (int base = 0; base < a.D; base += a.R) {
-                const uint16_t bits = static_cast<const uint16_t *>(a.params[base + q])[e];
-                for (int r = base; r < base + a.R; ++r)
-                    if (r != base + q) static_cast<uint16_t *>(a.params[r])[e] = bits;
-            }
-        }
     }
+    const unsigned mixed = __ballot_sync(0xffffffffu, kind == kMixed);
+    if (mixed != 0) gather_mixed(a, mixed);
 }
 
 }  // namespace
