@@ -1,6 +1,7 @@
 """The benchmark's reference arm runs on the CPU (it times the oracle): its
 JSON line carries the contract's keys, and under torchrun only rank 0
-prints."""
+prints.  The hash that ties the stored ncu counters to the device code
+ignores comments only."""
 import json
 import os
 import subprocess
@@ -37,3 +38,19 @@ def test_reference_arm_only_rank_zero_prints():
                "--workload", "toy_1000", "--cpu-threads", "1")
     assert out.returncode == 0, out.stderr
     assert not [l for l in out.stdout.splitlines() if l.startswith("{")]
+
+
+def test_kernel_hash_ignores_comments_only():
+    """The stored ncu counters stay valid across comment edits of the device
+    code and are voided by any code change."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    code = 'int f(int x) { return x + 1; }  // one\n/* two */ const char *s = "a // b";\n'
+    same = '// header\nint f(int x)\n{\n    return x + 1;  /* inline */\n}\nconst char *s = "a // b";'
+    other = 'int f(int x) { return x + 2; }\nconst char *s = "a // b";'
+    strip = bench.strip_c_comments
+    assert strip(code) == strip(same)
+    assert strip(code) != strip(other)
+    assert '"a // b"' in strip(code)
+    assert len(bench.kernel_source_hash()) == 16

@@ -22,7 +22,7 @@
 // through 128-bit loads and stores; a vector that straddles a run edge
 // (param with another decay flag, a rank edge, padding, the edge of the
 // launch's range) is done element by element and touches owned elements of
-// the range only.
+// the range only, the warp's such vectors shared out over its lanes.
 //
 // Arithmetic.  Every fp32 operation uses the round-to-nearest intrinsics
 // (__fmul_rn, __fadd_rn, __fsub_rn, __fdiv_rn, __fsqrt_rn), so no multiply
