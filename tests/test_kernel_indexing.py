@@ -4,8 +4,11 @@ The model follows the kernels' decomposition: a launch covers a run view
 (runs [run_begin, run_limit) and the tiles from tile0 that span them),
 2048-element tiles, a per-tile first-run index, a per-warp ballot over 32 run
 ends, a per-thread walk, the 8-element vector path inside one run and the
-element path at run edges.  It checks that every owned element of the view
-is visited exactly once, that nothing outside it is visited, and that every
+element path at run edges, in both of its forms: the warp's straddling
+vectors shared out over its lanes (four per round, one element per lane:
+the step, all-reduce and gather kernels) and one lane per straddling vector
+(the norm pass).  It checks that every owned element of the view is
+visited exactly once, that nothing outside it is visited, and that every
 8-element vector access lies inside the buffer.  The run table is rebuilt
 here from the pieces with the library's rule (touching pieces of one bucket
 with the same owner rank and decay flag merge)."""
@@ -54,7 +57,16 @@ def view(runs, bucket_run, first, count):
     return lo_run, hi_run, tile0, tiles
 
 
-def simulate(numel, runs, tile_run, run_begin, run_limit, tile0, tiles, visits):
+def owned_at(e, j, numel, start, end, run_limit):
+    """The element path's lookup: (owned, run index) walking from run j."""
+    if e >= numel:
+        return False, j
+    while j < run_limit and end[j] <= e:
+        j += 1
+    return j < run_limit and start[j] <= e, j
+
+
+def simulate(numel, runs, tile_run, run_begin, run_limit, tile0, tiles, visits, shared=True):
     start = [r[0] for r in runs]
     end = [r[1] for r in runs]
     vector_accesses = 0
@@ -70,6 +82,7 @@ def simulate(numel, runs, tile_run, run_begin, run_limit, tile0, tiles, visits):
                 j += c
                 if c < 32:
                     break
+            mixed = []  # lanes whose vector straddles a run edge (the ballot)
             for lane in range(32):
                 e0 = wb + lane * VEC
                 if e0 >= numel:
@@ -84,17 +97,26 @@ def simulate(numel, runs, tile_run, run_begin, run_limit, tile0, tiles, visits):
                     visits[e0:e0 + VEC] += 1
                     vector_accesses += 1
                     continue
-                for k in range(VEC):
-                    e = e0 + k
-                    if e >= numel:
-                        break
-                    while jj < run_limit and end[jj] <= e:
-                        jj += 1
-                    if jj >= run_limit:
-                        break
-                    if start[jj] > e:
+                if not shared:  # one lane per vector, element after element
+                    for k in range(VEC):
+                        owned, jj = owned_at(e0 + k, jj, numel, start, end, run_limit)
+                        if owned:
+                            visits[e0 + k] += 1
+                    continue
+                mixed.append(lane)
+            # rounds of 4 straddling vectors, octet o taking the o-th one left,
+            # lane k of the octet element k, each walking from the warp's run j
+            for r0 in range(0, len(mixed), 4):
+                for octet in range(4):
+                    if r0 + octet >= len(mixed):
                         continue
-                    visits[e] += 1
+                    src = mixed[r0 + octet]
+                    for k in range(VEC):
+                        e = wb + src * VEC + k
+                        assert wb <= e < wb + 32 * VEC
+                        owned, _ = owned_at(e, j, numel, start, end, run_limit)
+                        if owned:
+                            visits[e] += 1
     return vector_accesses
 
 
@@ -109,10 +131,11 @@ def check_layout(sizes, D, bucket, pad, wd=None, instances=1):
     owned = np.zeros(N, np.int32)
     for a, b in L.param_ranges():
         owned[a:b] = 1
-    # one launch over every bucket
-    visits = np.zeros(N, np.int32)
-    nvec = simulate(N, runs, tr, *view(runs, bucket_run, 0, L.n_buckets), visits)
-    assert np.array_equal(visits, owned)
+    # one launch over every bucket, with either element path
+    for shared in (True, False):
+        visits = np.zeros(N, np.int32)
+        nvec = simulate(N, runs, tr, *view(runs, bucket_run, 0, L.n_buckets), visits, shared)
+        assert np.array_equal(visits, owned)
     # one launch per bucket, and one over a middle range of buckets
     visits = np.zeros(N, np.int32)
     for k in range(L.n_buckets):
