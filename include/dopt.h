@@ -494,6 +494,26 @@ int dopt_step_clipped_noalloc(const dopt_layout *layout, const dopt_adam_cfg *cf
                               float *exp_avg_sq, void *const *param_replicas, uint32_t flags,
                               float *main_grad, float *norm_out, cudaStream_t stream);
 
+/* Device-side checks (a test build of the library, compiled with
+ * DOPT_DEVICE_CHECKS defined; built by build(checked=True) as
+ * libdopt_checked.so).  In that build every kernel checks, before each
+ * vector or element access, that the index lies inside the buffers (all of
+ * a launch's buffers are padded_numel long) and that a vector starts on an
+ * 8-element boundary; a failed check sets its DOPT_CHECK_* bit, records the
+ * first bad element index and skips the access instead of making it.
+ * These are the kernels' own guards against a wrong run table or index
+ * arithmetic; valid inputs never fail them.
+ *
+ * Reads the current device's record: *flags (DOPT_CHECK_* bits, 0 if no
+ * check failed) and *first_bad (the first failing element index, -1 if
+ * none); with reset != 0 it then clears the record.  Synchronous (it waits
+ * for the device's work to finish).  Errors: DOPT_E_ARG (NULL output),
+ * DOPT_E_STATE in a build without the checks (the product library),
+ * DOPT_E_CUDA. */
+#define DOPT_CHECK_INDEX 1u /* an element or vector index outside the buffers */
+#define DOPT_CHECK_ALIGN 2u /* a vector not on an 8-element boundary */
+int dopt_device_checks(int reset, uint32_t *flags, int64_t *first_bad);
+
 /* Text of the last error raised on the calling thread ("" if none). */
 const char *dopt_last_error(void);
 

@@ -315,3 +315,15 @@ def test_clipped_counted_argument_checks_before_cuda(lib):
     assert call(main=None) == B.DOPT_E_ARG
     assert call(flags=64) == B.DOPT_E_ARG
     assert call(flags=1 | B.DOPT_STEP_SKIP_NONFINITE) in (B.DOPT_E_STATE, B.DOPT_E_CUDA)
+
+
+def test_product_build_has_no_device_checks(lib):
+    """dopt_device_checks answers DOPT_E_STATE in the product library (the
+    checks exist only in the libdopt_checked.so test build) and needs no
+    device to say so."""
+    if B.LIB_PATH.endswith("libdopt_checked.so"):
+        pytest.skip("this process runs the checked build")
+    with pytest.raises(B.DoptError) as e:
+        B.device_checks()
+    assert e.value.code == B.DOPT_E_STATE
+    assert "DOPT_DEVICE_CHECKS" in str(e.value)

@@ -16,7 +16,10 @@ import threading
 from dataclasses import dataclass
 
 PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(PKG, "libdopt.so")
+# DOPT_CHECKED=1 loads the test build with the kernels' device-side index
+# checks (libdopt_checked.so, see dopt_device_checks in dopt.h) instead.
+LIB_PATH = os.path.join(PKG, "libdopt_checked.so" if os.environ.get("DOPT_CHECKED") == "1"
+                        else "libdopt.so")
 
 DOPT_OK = 0
 DOPT_E_ARG = -1
@@ -25,6 +28,8 @@ DOPT_E_ALIGN = -3
 DOPT_E_CUDA = -4
 DOPT_E_STATE = -5
 DOPT_E_NOMEM = -6
+DOPT_CHECK_INDEX = 1
+DOPT_CHECK_ALIGN = 2
 DOPT_MAX_D = 64
 DOPT_BF16 = 0
 DOPT_FP32 = 1
@@ -123,6 +128,8 @@ def _declare(lib):
     lib.dopt_allreduce.argtypes = [vp, P(vp), ctypes.c_int, ctypes.c_float, vp]
     lib.dopt_gather.restype = ctypes.c_int
     lib.dopt_gather.argtypes = [vp, P(vp), vp]
+    lib.dopt_device_checks.restype = ctypes.c_int
+    lib.dopt_device_checks.argtypes = [ctypes.c_int, P(ctypes.c_uint32), P(ctypes.c_int64)]
     lib.dopt_last_error.restype = ctypes.c_char_p
     lib.dopt_last_error.argtypes = []
     lib.dopt_version.restype = ctypes.c_char_p
@@ -142,6 +149,16 @@ def lib():
             _declare(handle)
             _lib = handle
         return _lib
+
+
+def device_checks(reset: bool = False):
+    """(flags, first_bad) of the device-side checks in the checked test
+    build (DOPT_CHECK_* bits, 0 if every check passed; the first failing
+    element index, -1 if none); reset clears them.  Raises DoptError with
+    DOPT_E_STATE in the product build, which has no checks."""
+    flags, first = ctypes.c_uint32(0), ctypes.c_int64(0)
+    _check(lib().dopt_device_checks(1 if reset else 0, ctypes.byref(flags), ctypes.byref(first)))
+    return flags.value, first.value
 
 
 def _check(rc: int):

@@ -375,6 +375,46 @@ __device__ __forceinline__ bool owned_at(const RunView &v, int64_t e, int &j, bo
     return v.run_start[j] <= e;
 }
 
+// Device-side checks, compiled in only with DOPT_DEVICE_CHECKS (a separate
+// build of the library for testing): before a vector or element access each
+// kernel checks the index against the buffer (every buffer of a launch is
+// padded_numel long) and the vector's alignment; a failed check records its
+// kind and the first bad index and skips the access.  In the product build
+// both checks are constant true.
+#ifdef DOPT_DEVICE_CHECKS
+__device__ unsigned int g_check_flags;              // DOPT_CHECK_* bits
+__device__ unsigned long long g_check_first = ~0ull;  // first bad index, ~0 if none
+
+__device__ __noinline__ void record_check(unsigned int flag, int64_t index) {
+    atomicOr(&g_check_flags, flag);
+    atomicCAS(&g_check_first, ~0ull, static_cast<unsigned long long>(index));
+}
+#endif
+
+__device__ __forceinline__ bool vector_in_buffer(const RunView &v, int64_t e0) {
+#ifdef DOPT_DEVICE_CHECKS
+    if (e0 < 0 || e0 + kVec > v.numel) {
+        record_check(DOPT_CHECK_INDEX, e0);
+        return false;
+    }
+    if (e0 % kVec != 0) {
+        record_check(DOPT_CHECK_ALIGN, e0);
+        return false;
+    }
+#endif
+    return true;
+}
+
+__device__ __forceinline__ bool element_in_buffer(const RunView &v, int64_t e) {
+#ifdef DOPT_DEVICE_CHECKS
+    if (e < 0 || e >= v.numel) {
+        record_check(DOPT_CHECK_INDEX, e);
+        return false;
+    }
+#endif
+    return true;
+}
+
 // The vectors of a warp that straddle a run edge (padding, another decay
 // flag or owner in them), shared out over the warp's lanes: `mixed` holds
 // the lanes whose vector straddles (the same in every lane, so every lane
@@ -399,7 +439,7 @@ __device__ __forceinline__ void for_straddling_elements(const RunView &v, int64_
         const int64_t e = warp_e0 + int64_t(__ffs(mine) - 1) * kVec + (lane & 7);
         int j = jw;
         bool done = false;
-        if (owned_at(v, e, j, done)) f(e, v.run_meta[j]);
+        if (owned_at(v, e, j, done) && element_in_buffer(v, e)) f(e, v.run_meta[j]);
     }
 }
 
@@ -746,13 +786,15 @@ __device__ __forceinline__ void step_vector(const StepArgs &a, const Scalars &sc
         // A whole vector of one run lies inside [lo, hi), so every vector
         // that turns out whole has its loads in flight before the lookup.
         Preloaded<G, DC> p;
-        const bool inside = e0 >= a.rv.lo && e0 + kVec <= a.rv.hi;
+        const bool inside = e0 >= a.rv.lo && e0 + kVec <= a.rv.hi && vector_in_buffer(a.rv, e0);
         if (inside) p.load(a, e0);
         kind = locate(a.rv, tile, e0, j);
-        if (kind == kFull) full_vector_preloaded<G, DC, MODE>(a, sc, dep, e0, a.rv.run_meta[j], status, p);
+        if (kind == kFull && vector_in_buffer(a.rv, e0))
+            full_vector_preloaded<G, DC, MODE>(a, sc, dep, e0, a.rv.run_meta[j], status, p);
     } else {
         kind = locate(a.rv, tile, e0, j);
-        if (kind == kFull) full_vector<G, DC, MODE, GR>(a, sc, dep, e0, a.rv.run_meta[j], status);
+        if (kind == kFull && vector_in_buffer(a.rv, e0))
+            full_vector<G, DC, MODE, GR>(a, sc, dep, e0, a.rv.run_meta[j], status);
     }
     // every lane of the warp is here (no lane returns before this point)
     const unsigned mixed = __ballot_sync(0xffffffffu, kind == kMixed);
@@ -845,7 +887,7 @@ __global__ void __launch_bounds__(kThreads, 3) dopt_allreduce_kernel(const __gri
     const int64_t e0 = tile * kDoptTileElems + int64_t(threadIdx.x) * kVec;
     int j;
     const VecKind kind = locate(a.rv, tile, e0, j);
-    if (kind == kFull) {
+    if (kind == kFull && vector_in_buffer(a.rv, e0)) {
         float acc[8];
         reduce_vec<G, DC, GR>(a, a.scale, e0, acc);
         write_grads_vec<G, DC>(a.grads, a.D, e0, acc);
@@ -880,7 +922,7 @@ __global__ void __launch_bounds__(kThreads) dopt_rs_norm_kernel(const __grid_con
         const int64_t e0 = tile * kDoptTileElems + int64_t(threadIdx.x) * kVec;
         int j;
         const VecKind kind = locate(a.rv, tile, e0, j);
-        if (kind == kFull) {
+        if (kind == kFull && vector_in_buffer(a.rv, e0)) {
             float acc[8];
             reduce_vec<G, DC>(a, a.scale, e0, acc);
             if (a.round_grad) to_grad_type8<G>(acc);
@@ -903,7 +945,7 @@ __global__ void __launch_bounds__(kThreads) dopt_rs_norm_kernel(const __grid_con
             bool done = false;
             for (int k = 0; k < kVec && !done; ++k) {
                 const int64_t e = e0 + k;
-                if (!owned_at(a.rv, e, j, done)) continue;
+                if (!owned_at(a.rv, e, j, done) || !element_in_buffer(a.rv, e)) continue;
                 float g = reduce_scalar<G>(a.grads, D, a.R, a.scale, e);
                 if (a.round_grad) g = to_grad_type<G>(g);
                 a.main_grad[e] = g;
@@ -987,7 +1029,7 @@ __global__ void __launch_bounds__(kThreads) dopt_gather_kernel(const __grid_cons
     const int64_t e0 = tile * kDoptTileElems + int64_t(threadIdx.x) * kVec;
     int j;
     const VecKind kind = locate(a.rv, tile, e0, j);
-    if (kind == kFull) {
+    if (kind == kFull && vector_in_buffer(a.rv, e0)) {
         const int q = a.rv.run_meta[j] >> kRunRankShift;
         for (int base = 0; base < a.D; base += a.R) {
             const uint4 val = ld_stream(static_cast<const __nv_bfloat16 *>(a.params[base + q]) + e0);

@@ -478,6 +478,31 @@ int check_clip_args(const char *who, const float *main_grad, const float *norm_o
 // Entry points
 // ---------------------------------------------------------------------------
 
+extern "C" int dopt_device_checks(int reset, uint32_t *flags, int64_t *first_bad) {
+    using dopt::fail;
+    if (!flags || !first_bad) return fail(DOPT_E_ARG, "dopt_device_checks: NULL output");
+#ifdef DOPT_DEVICE_CHECKS
+    unsigned int f = 0;
+    unsigned long long first = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&f, g_check_flags, sizeof f);
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&first, g_check_first, sizeof first);
+    if (e == cudaSuccess && reset) {
+        const unsigned int zero = 0;
+        const unsigned long long none = ~0ull;
+        e = cudaMemcpyToSymbol(g_check_flags, &zero, sizeof zero);
+        if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_check_first, &none, sizeof none);
+    }
+    if (e != cudaSuccess)
+        return fail(DOPT_E_CUDA, "dopt_device_checks: %s", cudaGetErrorString(e));
+    *flags = f;
+    *first_bad = static_cast<int64_t>(first);
+    return DOPT_OK;
+#else
+    (void)reset;
+    return fail(DOPT_E_STATE, "dopt_device_checks: this library was built without DOPT_DEVICE_CHECKS");
+#endif
+}
+
 extern "C" int dopt_step(const dopt_layout *L, const dopt_adam_cfg *cfg, int64_t step,
                          const void *const *grad_replicas, dopt_dtype grad_dtype, float *master,
                          float *exp_avg, float *exp_avg_sq, void *const *param_replicas,
