@@ -327,3 +327,27 @@ def test_product_build_has_no_device_checks(lib):
         B.device_checks()
     assert e.value.code == B.DOPT_E_STATE
     assert "DOPT_DEVICE_CHECKS" in str(e.value)
+
+
+def test_checked_build_compiles_and_exports_the_same_symbols():
+    """The test build with device-side checks compiles for sm_103a, exports
+    every symbol the header declares, and its dopt_device_checks reaches the
+    CUDA runtime (an error without a device, not DOPT_E_STATE)."""
+    import subprocess
+    import sys
+
+    path = libbuild.build(checked=True)
+    assert path.endswith("libdopt_checked.so")
+    checked = ctypes.CDLL(path)
+    missing = [n for n in declared_functions() if not hasattr(checked, n)]
+    assert not missing, missing
+    import torch
+
+    if torch.cuda.is_available():
+        return
+    code = ("import zero_distributed_optimizer_gb300.binding as B\n"
+            "assert B.LIB_PATH.endswith('libdopt_checked.so')\n"
+            "try:\n    B.device_checks()\nexcept B.DoptError as e:\n    print('CODE', e.code)\n")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True,
+                       env=dict(os.environ, DOPT_CHECKED="1"), timeout=300)
+    assert f"CODE {B.DOPT_E_CUDA}" in r.stdout, r.stdout + r.stderr
