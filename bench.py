@@ -517,6 +517,11 @@ def run_ours(args):
                        "state_dtype": "f32", "param_dtype": "bf16",
                        "bytes_per_element": w.algorithmic_bytes_per_element(),
                        "l2": l2_note(N * (w.D * w.grad_bytes + 12 + 2 * w.D)),
+                       # device memory of the step's buffers, and the fp32
+                       # master/m/v shard each simulated rank owns (12 bytes
+                       # per element over D ranks: ZeRO-1's optimizer state)
+                       "resident_bytes": N * (w.D * w.grad_bytes + 12 + 2 * w.D),
+                       "optimizer_state_bytes_per_rank": 12 * N // w.D,
                        "path": f"binding.dopt_step_counted, {GRAPH_STEPS} steps per CUDA "
                                "graph, replayed (a counter kernel and the step kernel per "
                                "step)",
