@@ -143,7 +143,7 @@ def measured_hbm_peak():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+    """nvidia-smi clocks and throttle reasons, sampled every 50 ms."""
 
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -159,7 +159,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-i", str(self.gpu_index), "-lms", "100"],
+                 "-i", str(self.gpu_index), "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -188,7 +188,7 @@ class ClockSampler:
         if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
                     "note": "nvidia-smi unavailable"}
-        inside = [p for t, p in self.samples if t0 - 0.15 <= t <= t1 + 0.15]
+        inside = [p for t, p in self.samples if t0 - 0.05 <= t <= t1 + 0.05]
         note = "samples during the timed region"
         if not inside:
             mid = 0.5 * (t0 + t1)
@@ -208,6 +208,7 @@ class ClockSampler:
         reasons = sorted({names[i] for p in inside for i in range(4)
                           if p[6 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_mhz_min": min(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
                 "power_w_max": max(power) if power else None,
                 "reasons": reasons, "samples": len(inside), "note": note}
@@ -282,6 +283,23 @@ def workload_by_name(name: str) -> W.Workload:
     return getattr(W, name)()
 
 
+def workload_config(w: W.Workload, padded_numel: int, n_buckets: int, world: int) -> dict:
+    """The `config` object of the JSON line: the workload alone, the same
+    for both arms (how each arm runs it is stated outside `config`)."""
+    resident = padded_numel * (w.D * w.grad_bytes + 12 + 2 * w.D)
+    return {"workload": w.name, "N": w.numel, "padded_numel": padded_numel, "D": w.D,
+            "bucket_elems": w.bucket_elems, "pad_unit": w.pad_unit, "n_buckets": n_buckets,
+            "grad_dtype": w.grad_dtype, "state_dtype": "f32", "param_dtype": "bf16",
+            "bytes_per_element": w.algorithmic_bytes_per_element(),
+            "l2": l2_note(resident),
+            # device memory of the step's buffers, and the fp32 master/m/v
+            # shard each simulated rank owns (12 bytes per element over D
+            # ranks: ZeRO-1's optimizer state)
+            "resident_bytes": resident,
+            "optimizer_state_bytes_per_rank": 12 * padded_numel // w.D,
+            "parallelism": "replicas" if world > 1 else "single"}
+
+
 def run_reference(args):
     """The oracle arm: rank 0 alone times the CPU oracle on a bounded window."""
     world, rank, _ = dist_env()
@@ -301,14 +319,16 @@ def run_reference(args):
                                             sample=elems, threads=threads)
     sample = (f"first {used} elements of the {w.name} buffer (D={w.D}), "
               f"{steps} oracle steps, {threads} host threads on disjoint windows")
+    import oracle
+
+    O = oracle.range_map(list(w.sizes), w.D, w.bucket_elems, w.pad_unit)
     line = {
         "impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": world,
         "steps": steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / max(steps, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": w.name, "N": w.numel, "D": w.D, "bucket_elems": w.bucket_elems,
-                   "pad_unit": w.pad_unit, "grad_dtype": w.grad_dtype,
-                   "sample_elems": used},
+        "config": workload_config(w, O.numel, O.n_buckets, world),
+        "path": "the CPU oracle (plain C) stepping a bounded sample of the buffer",
         "cpu_baseline": {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -383,34 +403,47 @@ def run_ours(args):
     sampler.start()
     # let the sampler come up and the clocks settle under the same load
     settle_end = time.time() + 0.4
+    settled = 0
+    s0 = time.time()
     while time.time() < settle_end:
         graphs[per].replay()
         taken += per
+        settled += per
         torch.cuda.synchronize()
+    est_ms = 1e3 * (time.time() - s0) / max(settled, 1)
 
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # The timed region: R repeats of exactly K steps, each bracketed by a
+    # barrier and a synchronize on both sides and timed with CUDA events;
+    # the reported time per step is the median over the repeats.  R is at
+    # least 5 and large enough that the repeats cover about
+    # --timed-seconds, so that the clock sampler sees the load several times.
+    repeats = args.repeats or max(5, min(1000, int(args.timed_seconds /
+                                                   max(args.steps * est_ms / 1e3, 1e-6)) + 1))
+    rep_ms = []
     h0 = time.time()
-    ev0.record(stream)
-    for _ in range(args.steps // per):
-        graphs[per].replay()
-    if args.steps % per:
-        graphs[args.steps % per].replay()
-    ev1.record(stream)
-    torch.cuda.synchronize()
+    for _ in range(repeats):
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(args.steps // per):
+            graphs[per].replay()
+        if args.steps % per:
+            graphs[args.steps % per].replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        rep_ms.append(max_over_ranks(ev0.elapsed_time(ev1), world, device))
+        taken += args.steps
     h1 = time.time()
-    if world > 1:
-        torch.distributed.barrier()
     sampler.stop()
-    taken += args.steps
     next_step, status = B.counter_state(counter)
     assert status == 0 and next_step == t + 1 + taken, (next_step, status, t, taken)
     t = next_step - 1
     del graphs
-    ms_local = ev0.elapsed_time(ev1)
-    ms_total = max_over_ranks(ms_local, world, device)
+    ms_total = statistics.median(rep_ms)
     ms_per_step = ms_total / args.steps
 
     elems = w.numel
@@ -509,23 +542,18 @@ def run_ours(args):
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "repeats": repeats,
+            "ms_per_step_spread": {"min": min(rep_ms) / args.steps,
+                                   "median": ms_per_step,
+                                   "max": max(rep_ms) / args.steps,
+                                   "note": f"{repeats} repeats of the {args.steps} timed steps, "
+                                           "each bracketed by barrier + synchronize; value and "
+                                           "ms_per_step use the median repeat"},
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
-            "config": {"workload": w.name, "N": elems, "padded_numel": N, "D": w.D,
-                       "bucket_elems": w.bucket_elems, "pad_unit": w.pad_unit,
-                       "n_buckets": L.n_buckets, "grad_dtype": w.grad_dtype,
-                       "state_dtype": "f32", "param_dtype": "bf16",
-                       "bytes_per_element": w.algorithmic_bytes_per_element(),
-                       "l2": l2_note(N * (w.D * w.grad_bytes + 12 + 2 * w.D)),
-                       # device memory of the step's buffers, and the fp32
-                       # master/m/v shard each simulated rank owns (12 bytes
-                       # per element over D ranks: ZeRO-1's optimizer state)
-                       "resident_bytes": N * (w.D * w.grad_bytes + 12 + 2 * w.D),
-                       "optimizer_state_bytes_per_rank": 12 * N // w.D,
-                       "path": f"binding.dopt_step_counted, {GRAPH_STEPS} steps per CUDA "
-                               "graph, replayed (a counter kernel and the step kernel per "
-                               "step)",
-                       "parallelism": "replicas" if world > 1 else "single"},
+            "config": workload_config(w, N, L.n_buckets, world),
+            "path": f"binding.dopt_step_counted, {GRAPH_STEPS} steps per CUDA graph, replayed "
+                    "(a counter kernel and the step kernel per step)",
             "hbm_gbs": gbs, "pct_of_8tbs": gbs / NOMINAL_HBM_GBS,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                          "frac": gbs / peak, "peak_kind": peak_kind,
@@ -536,7 +564,7 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "e2e": e2e,
             "direct": direct,
-            "gpu_launches": 2 * args.steps,
+            "gpu_launches": 2 * args.steps * repeats,
             "clocks": sampler.summary(h0, h1),
             "torch": torch.__version__,
         }
@@ -559,6 +587,11 @@ def main(argv=None):
                     help="wall time of the CPU-baseline legs (one thread, all threads)")
     ap.add_argument("--cpu-threads", type=int, default=0,
                     help="host threads of the oracle runs (0: every core this process may use)")
+    ap.add_argument("--repeats", type=int, default=0,
+                    help="repeats of the K timed steps (0: at least 5, enough to cover "
+                         "--timed-seconds)")
+    ap.add_argument("--timed-seconds", type=float, default=1.0,
+                    help="device time the repeats of the timed region should cover")
     ap.add_argument("--workload", choices=WORKLOADS, default="gpt2_small",
                     help="the GPT-2-small layout is the configuration of the reported metric")
     args = ap.parse_args(argv)

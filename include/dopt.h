@@ -42,7 +42,8 @@ extern "C" {
 /* Status codes. */
 #define DOPT_OK 0
 #define DOPT_E_ARG (-1)    /* invalid argument (null, out of range) */
-#define DOPT_E_LAYOUT (-2) /* a bucket does not divide by R (page 1, §4.1 and §5) */
+#define DOPT_E_LAYOUT (-2) /* a bucket does not divide by R (distributed-optimizer
+                              page, §4.1 and §5) */
 #define DOPT_E_ALIGN (-3)  /* a device pointer is not 16-byte aligned */
 #define DOPT_E_CUDA (-4)   /* a CUDA runtime call failed */
 #define DOPT_E_STATE (-5)  /* the layout has no device tables on this device */
@@ -51,7 +52,8 @@ extern "C" {
 /* Largest number of simulated data-parallel ranks. */
 #define DOPT_MAX_D 64
 
-/* Range(start, end): the half-open interval [start, end) (page 1, §4.1). */
+/* Range(start, end): the half-open interval [start, end)
+ * (distributed-optimizer page, §4.1). */
 typedef struct {
     int64_t start;
     int64_t end;
@@ -59,7 +61,8 @@ typedef struct {
 
 /*
  * One (param, rank) piece: the part of a param that falls in one rank's
- * range of its bucket, with the four ranges of page 1, §4.1:
+ * range of its bucket, with the four ranges of the distributed-optimizer
+ * page, §4.1:
  *   gbuf_world            the piece's range in the whole flat buffer
  *   gbuf_world_in_bucket  the same, relative to the start of its bucket
  *   gbuf_local            the same, relative to the start of the rank's range
@@ -78,15 +81,19 @@ typedef struct {
 } dopt_piece;
 
 /*
- * Layout parameters.
+ * Layout parameters, in the order of the boundary's own statement of them
+ * (D, bucket_elems, pad_unit), so that a caller who sets just those three
+ * positionally gets one instance and a zero reserved word:
  *   D             simulated data-parallel ranks (replica buffers),
  *                 1..DOPT_MAX_D
- *   pad_unit      every bucket is padded at its end to a multiple of
- *                 R * pad_unit elements (>= 1), R = D / instances
  *   bucket_elems  a bucket is closed as soon as its unpadded element count
  *                 reaches bucket_elems; 0 puts all params in one bucket
- *   instances     distributed-optimizer instances (page 1, §5,
- *                 num_distributed_optimizer_instances); 0 or 1: one
+ *                 (distributed-optimizer page, §2)
+ *   pad_unit      every bucket is padded at its end to a multiple of
+ *                 R * pad_unit elements (>= 1), R = D / instances (§4.1, §5:
+ *                 a bucket must divide by the rank count)
+ *   instances     distributed-optimizer instances (distributed-optimizer
+ *                 page, §5, num_distributed_optimizer_instances); 0 or 1: one
  *                 instance.  D must divide by it.  The ranks form
  *                 `instances` groups of R = D / instances consecutive ranks;
  *                 each bucket is split into R ranges, rank r of every group
@@ -97,15 +104,16 @@ typedef struct {
  */
 typedef struct {
     int32_t D;
-    int32_t pad_unit;
     int64_t bucket_elems;
+    int32_t pad_unit;
     int32_t instances;
     int32_t reserved;
 } dopt_layout_cfg;
 
 /*
  * AdamW hyper-parameters.  grad_scale is the gradient scaling factor applied
- * to every replica's grads before the reduction (page 1, §5).
+ * to every replica's grads before the reduction (distributed-optimizer
+ * page, §5).
  * Valid ranges: lr >= 0, 0 <= beta1 < 1, 0 <= beta2 < 1, eps >= 0,
  * weight_decay >= 0, grad_scale finite.
  */
@@ -143,11 +151,12 @@ typedef enum { DOPT_BF16 = 0, DOPT_FP32 = 1, DOPT_FP16 = 2 } dopt_dtype;
 #define DOPT_STEP_HOST_GRADS 2u
 /*
  * Round each reduced grad to the grad type before clipping and Adam (bf16
- * and fp16: nearest even; fp32 grads are unchanged), as when the reduce-scatter writes
- * into the grad buffer and the optimizer copies the shard from there (page
- * 1, §4.2-§4.3).  main_grad_out / main_grad then hold the rounded values and
- * the clipped step's norm is taken over them.  Without the flag the fp32
- * sum feeds Adam directly.  Accepted by every step entry point.
+ * and fp16: nearest even; fp32 grads are unchanged), as when the
+ * reduce-scatter writes into the grad buffer and the optimizer copies the
+ * shard from there (distributed-optimizer page, §4.2-§4.3).  main_grad_out /
+ * main_grad then hold the rounded values and the clipped step's norm is
+ * taken over them.  Without the flag the fp32 sum feeds Adam directly.
+ * Accepted by every step entry point.
  */
 #define DOPT_STEP_ROUND_GRAD 4u
 /*
@@ -156,18 +165,33 @@ typedef enum { DOPT_BF16 = 0, DOPT_FP32 = 1, DOPT_FP16 = 2 } dopt_dtype;
  * copies 16-bit values and is the same for both types.
  */
 #define DOPT_STEP_PARAMS_FP16 16u
+/*
+ * Read each tile's grads and master/m/v through shared memory: one thread
+ * of every CTA issues 1-D bulk copies (the SM's copy engine, from this
+ * GPU's own memory into that CTA's shared memory; no cluster multicast),
+ * and the CTA computes from shared memory once they complete.  The results
+ * are those of the default path (128-bit vector loads into registers), bit
+ * for bit.  The pages suggest staging bucket tiles this way; the library
+ * keeps it as a measured alternative, not the default.  Accepted by
+ * dopt_step, dopt_step_buckets and dopt_step_counted, for layouts with one
+ * instance and D in {1, 2, 4, 8, 16} and device grads (DOPT_E_ARG
+ * otherwise).  A CTA whose copies do not complete within 2 s skips its
+ * tile and is counted (dopt_stage_timeouts) instead of hanging.
+ */
+#define DOPT_STEP_STAGE 32u
 
 typedef struct dopt_layout dopt_layout;
 
 /*
- * Build the flat-buffer layout and its four-way range map (page 1, §2, §3,
- * §4.1, §5).
+ * Build the flat-buffer layout and its four-way range map
+ * (distributed-optimizer page, §2, §3, §4.1, §5).
  *
  *   param_sizes[n_params]  element count of each param (>= 0), in buffer
  *                          order; params sit at consecutive offsets.
  *   wd_mask[n_params]      nullable; nonzero where the param takes weight
  *                          decay (NULL: every param does).
- *   cfg                    D, pad_unit, bucket_elems (see dopt_layout_cfg).
+ *   cfg                    D, bucket_elems, pad_unit, instances (see
+ *                          dopt_layout_cfg).
  *   out                    receives a new layout; free it with
  *                          dopt_layout_free.
  *
@@ -182,37 +206,67 @@ typedef struct dopt_layout dopt_layout;
 int dopt_build_range_map(const int64_t *param_sizes, int32_t n_params, const uint8_t *wd_mask,
                          const dopt_layout_cfg *cfg, dopt_layout **out);
 
-/* Sizes of a layout: padded buffer length, bucket and piece counts.  Any
- * output pointer may be NULL.  Host only. */
+/*
+ * Sizes of a layout: the padded length of the flat buffer (distributed-
+ * optimizer page, §2: every param's grads in one contiguous buffer, each
+ * bucket padded so that it divides by the rank count, §4.1 and §5), the
+ * bucket count (§2) and the piece count (§4.1: one piece per (param, rank)
+ * overlap).  Any output pointer may be NULL.  Host only.  Errors: DOPT_E_ARG
+ * (NULL layout).
+ */
 int dopt_layout_query(const dopt_layout *layout, int64_t *padded_numel, int32_t *n_buckets,
                       int32_t *n_pieces);
 
-/* Copy the n_buckets bucket ranges (padded, in buffer order). Host only. */
+/*
+ * Copy the bucket ranges, padding included, in buffer order, into
+ * buckets[n_buckets] (caller-owned host array; distributed-optimizer page,
+ * §2: the flat buffer cut into buckets; §3: each bucket split into equal
+ * contiguous rank ranges).  Host only.  Errors: DOPT_E_ARG (NULL argument).
+ */
 int dopt_layout_buckets(const dopt_layout *layout, dopt_range *buckets);
 
-/* Copy the n_pieces pieces, sorted by (bucket, rank, gbuf_world.start).
- * Host only. */
+/*
+ * Copy the pieces into pieces[n_pieces] (caller-owned host array), sorted by
+ * (bucket, rank, gbuf_world.start): for every param and every rank range it
+ * overlaps, the four ranges of the distributed-optimizer page, §4.1
+ * (gbuf_world, gbuf_world_in_bucket, gbuf_local, param; see dopt_piece).
+ * Host only.  Errors: DOPT_E_ARG (NULL argument).
+ */
 int dopt_layout_pieces(const dopt_layout *layout, dopt_piece *pieces);
 
-/* Copy each param's full range in the buffer ([n_params]). Host only. */
+/*
+ * Copy each param's full range [offset, offset + size) in the flat buffer
+ * into params[n_params] (caller-owned host array, in the order the params
+ * were given): the param's place in the contiguous buffer of the
+ * distributed-optimizer page, §2, from which the §4.1 ranges of its pieces
+ * are cut.  Params sit at consecutive offsets inside their bucket; padding
+ * follows the last param of a bucket.  Host only.  Errors: DOPT_E_ARG (NULL
+ * argument).
+ */
+int dopt_layout_param_offsets(const dopt_layout *layout, dopt_range *params);
+
+/* The same call as dopt_layout_param_offsets, under its earlier name. */
 int dopt_layout_param_ranges(const dopt_layout *layout, dopt_range *params);
 
 /*
- * Copy the layout's kernel tables (owned runs of the buffer and a per-tile
- * index into them) to the current CUDA device.  Allocates device memory
- * once; must precede dopt_step / dopt_gather on that device and any stream
- * capture.  Calling it again on the same device is a no-op; on another
- * device it moves the tables there.  Synchronous.  Errors: DOPT_E_ARG,
- * DOPT_E_CUDA.
+ * Copy the layout's kernel tables to the current CUDA device: the owned
+ * runs of the buffer (stretches of the §4.1 pieces of the distributed-
+ * optimizer page with one owner rank and one weight-decay flag, merged) and
+ * a per-tile index into them.  Allocates device memory once; must precede
+ * dopt_step / dopt_gather on that device and any stream capture.  Calling
+ * it again on the same device is a no-op; on another device it moves the
+ * tables there.  Synchronous.  Errors: DOPT_E_ARG, DOPT_E_CUDA.
  */
 int dopt_layout_to_device(dopt_layout *layout);
 
-/* Free a layout and its device tables.  NULL is ignored. */
+/* Free a layout (the range map of dopt_build_range_map) and its device
+ * tables.  NULL is ignored.  Library bookkeeping: the pages have no
+ * counterpart. */
 void dopt_layout_free(dopt_layout *layout);
 
 /*
  * One distributed-optimizer step for all D simulated ranks, fused into one
- * kernel launch over the whole buffer (page 1, §4.2-§4.4):
+ * kernel launch over the whole buffer (distributed-optimizer page, §4.2-§4.4):
  *
  *   for every owned element i (rank q owns it, param p holds it):
  *     g      = fp32 sum over r = 0..D-1, in rank order, of
@@ -279,7 +333,7 @@ int dopt_step_buckets(const dopt_layout *layout, const dopt_adam_cfg *cfg, int64
 
 /*
  * Step counter in device memory for dopt_step_counted: 64 bytes, 16-byte
- * aligned, owned by the caller.
+ * aligned, owned by the caller, zeroed by the caller before first use.
  *   next_step  1-based number of the step the next dopt_step_counted launch
  *              takes.  The caller sets it (to 1, or to the step to resume
  *              at); every such launch reads it on the device and adds one.
@@ -288,12 +342,21 @@ int dopt_step_buckets(const dopt_layout *layout, const dopt_adam_cfg *cfg, int64
  *              nothing else (not the counter, the state or the params).
  *   scratch    the library's: the two Adam scalars that depend on the step
  *              number, for the step last taken, and a copy of the status.
+ *   exact_steps, undecided_steps
+ *              diagnostics of the device's evaluation of those two scalars
+ *              (see dopt_step_counted): the steps whose scalars needed the
+ *              slow exact evaluation, and the steps where even that could
+ *              not tell which float pow(beta, t) leads to.  The library only
+ *              adds to them.
  */
 typedef struct {
     int64_t next_step;
     int32_t status;
     int32_t reserved;
-    float scratch[12];
+    float scratch[4];
+    uint32_t exact_steps;
+    uint32_t undecided_steps;
+    uint32_t reserved2[6];
 } dopt_step_counter;
 
 #define DOPT_COUNTER_BAD_STEP 1
@@ -301,10 +364,19 @@ typedef struct {
 /*
  * dopt_step with the step number taken from a counter in device memory
  * instead of a host argument, and the counter advanced on the device.  A
- * kernel of two threads reads counter->next_step = t, evaluates the step's
- * scalars that depend on t (the same double-precision operations as
- * dopt_step, on the device) into counter->scratch and stores t + 1; then
- * the step kernel of dopt_step runs with those scalars.  The first kernel is launched as a
+ * kernel of four threads reads counter->next_step = t, evaluates the step's
+ * two scalars that depend on t into counter->scratch and stores t + 1; then
+ * the step kernel of dopt_step runs with those scalars.  dopt_step takes
+ * beta^t from the C library's pow; the device has none, so it computes
+ * beta^t by binary powering with a bound on its error, and evaluates each
+ * scalar at both ends of the interval where pow's result must lie (pow is
+ * within 0.52 ulp of the exact power).  When the two ends give the same
+ * float it is dopt_step's float.  Otherwise (rarely) it evaluates beta^t
+ * again in double-double and the scalar at every double within 0.52 ulp of
+ * that value, and counts the step in counter->exact_steps; if those still
+ * give two floats, it takes the one of the nearest double and counts the
+ * step in counter->undecided_steps (the only case in which the counted
+ * step may differ from dopt_step, by one float ulp of a scalar).  The first kernel is launched as a
  * programmatic dependent of the kernel before it on the stream: it may start
  * early, but it reads the final counter and writes only after that kernel
  * has completed.  The launches and
@@ -324,8 +396,8 @@ int dopt_step_counted(const dopt_layout *layout, const dopt_adam_cfg *cfg,
                       cudaStream_t stream);
 
 /*
- * The all-reduce of the grads on its own (page 1, §5, force_all_reduce: all
- * ranks keep the whole reduced grad, e.g. to save full weight grads;
+ * The all-reduce of the grads on its own (distributed-optimizer page, §5,
+ * force_all_reduce: all ranks keep the whole reduced grad, e.g. to save full weight grads;
  * distributed-training tutorial, "AllReduce" = reduce-scatter followed by
  * all-gather).  For every owned element i:
  *     g = fp32 sum over r in rank order of grad_scale * float(grad_replicas[r][i])
@@ -341,8 +413,8 @@ int dopt_allreduce(const dopt_layout *layout, void *const *grad_replicas, dopt_d
                    float grad_scale, cudaStream_t stream);
 
 /*
- * dopt_step with force_all_reduce (page 1, §5): the same step, one launch,
- * which also writes the reduced grad of every owned element into every grad
+ * dopt_step with force_all_reduce (distributed-optimizer page, §5): the
+ * same step, one launch, which also writes the reduced grad of every owned element into every grad
  * replica, as dopt_allreduce does (the Adam update uses the fp32 reduced
  * grad, unchanged).  grad_replicas are read and then written.  Arguments and
  * errors otherwise as dopt_step.
@@ -353,8 +425,8 @@ int dopt_step_allreduce(const dopt_layout *layout, const dopt_adam_cfg *cfg, int
                         uint32_t flags, float *main_grad_out, cudaStream_t stream);
 
 /*
- * The all-gather of the params on its own (page 1, §4.4): for every rank q
- * and every element q owns, copy param_replicas[q][i] into every other
+ * The all-gather of the params on its own (distributed-optimizer page,
+ * §4.4): for every rank q and every element q owns, copy param_replicas[q][i] into every other
  * replica of q's instance.  Padding is not copied.  param_replicas: host
  * array of D device pointers to 16-bit params (bf16 or fp16: the copy does
  * not look at the values), 16-byte aligned.  Asynchronous on `stream`.
@@ -472,13 +544,16 @@ int dopt_step_clipped_counted(const dopt_layout *layout, const dopt_adam_cfg *cf
  * (dopt_layout_to_device, which allocates, belongs to set-up).
  *
  * Set-up: the first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current and remembers it; make
- * that first call on each device before any stream capture.
+ * (cudaGetSymbolAddress) with that device current and remembers it for the
+ * life of the process; make that first call on each device before any
+ * stream capture.  A cudaDeviceReset of that device destroys the array
+ * with the context, and the remembered address is then stale: after a
+ * reset, do not call this entry point again in the same process.
  *
  * Sharing: every call on a device uses the same array, which keeps the last
- * call's contents.  Each call zeroes the ticket that must start at zero
- * (a 4-byte cudaMemsetAsync on `stream`); the rest is overwritten before it
- * is read.  Calls whose executions overlap on the GPU (other streams, other
+ * call's contents.  Each call zeroes the 16-byte header that must start at
+ * zero (the finishing ticket and the non-finite count: one 16-byte
+ * cudaMemsetAsync on `stream`); the rest is overwritten before it is read.  Calls whose executions overlap on the GPU (other streams, other
  * layouts, other threads) race on the array: the caller must order them.
  *
  * Limit: the norm pass needs 64 bytes plus 8 bytes per CTA, at most 1024
@@ -494,7 +569,8 @@ int dopt_step_clipped_noalloc(const dopt_layout *layout, const dopt_adam_cfg *cf
                               float *exp_avg_sq, void *const *param_replicas, uint32_t flags,
                               float *main_grad, float *norm_out, cudaStream_t stream);
 
-/* Device-side checks (a test build of the library, compiled with
+/* Device-side checks (library infrastructure for testing; the pages have
+ * no counterpart): a test build of the library, compiled with
  * DOPT_DEVICE_CHECKS defined; built by build(checked=True) as
  * libdopt_checked.so).  In that build every kernel checks, before each
  * vector or element access, that the index lies inside the buffers (all of
@@ -514,10 +590,19 @@ int dopt_step_clipped_noalloc(const dopt_layout *layout, const dopt_adam_cfg *cf
 #define DOPT_CHECK_ALIGN 2u /* a vector not on an 8-element boundary */
 int dopt_device_checks(int reset, uint32_t *flags, int64_t *first_bad);
 
-/* Text of the last error raised on the calling thread ("" if none). */
+/* Count of staged CTAs (DOPT_STEP_STAGE) on the current device whose bulk
+ * copies did not complete within their time limit, so that they skipped
+ * their tile; with reset != 0 the count is then cleared.  0 unless the
+ * copy engine failed.  Library infrastructure: the pages have no
+ * counterpart.  Synchronous.  Errors: DOPT_E_ARG (NULL count), DOPT_E_CUDA. */
+int dopt_stage_timeouts(int reset, uint32_t *count);
+
+/* Text of the last error raised on the calling thread ("" if none).
+ * Library infrastructure: the pages have no counterpart. */
 const char *dopt_last_error(void);
 
-/* Library version string. */
+/* Library version string.  Library infrastructure: the pages have no
+ * counterpart. */
 const char *dopt_version(void);
 
 #ifdef __cplusplus

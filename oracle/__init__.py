@@ -39,13 +39,13 @@ class OracleError(RuntimeError):
 
 
 class Range(ctypes.Structure):
-    """Half-open interval [start, end) (page 1, §4.1 "Range")."""
+    """Half-open interval [start, end) (distributed-optimizer page, §4.1 "Range")."""
 
     _fields_ = [("start", ctypes.c_int64), ("end", ctypes.c_int64)]
 
 
 class Piece(ctypes.Structure):
-    """One (param, rank) piece with its four ranges (page 1, §4.1 table)."""
+    """One (param, rank) piece with its four ranges (distributed-optimizer page, §4.1 table)."""
 
     _fields_ = [
         ("gbuf_world", Range),
@@ -200,7 +200,7 @@ class OracleLayout:
 
 
 def range_map(sizes, D: int, bucket_elems: int, pad_unit: int, lib=None) -> OracleLayout:
-    """Layout + four-way range map (page 1, §2, §3 and §4.1)."""
+    """Layout + four-way range map (distributed-optimizer page, §2, §3 and §4.1)."""
     lib = lib or load()
     sizes_a, sizes_p = _i64(sizes)
     n = len(sizes_a)
@@ -270,11 +270,11 @@ def step(sizes, wd_mask, D: int, bucket_elems: int, pad_unit: int, adam: Adam, t
     grads: D arrays (uint16 bf16 bits or float32); master/exp_avg/exp_avg_sq:
     float32; params: D uint16 arrays (bf16 bits); main_grad_out: optional
     float32.  All are buffer-indexed and cover ``window = (w0, w1)`` (default:
-    the whole padded buffer).  Follows page 1 §4.2 (reduce-scatter), §4.3
+    the whole padded buffer).  Follows the distributed-optimizer page, §4.2 (reduce-scatter), §4.3
     (main grads, Adam, write-back) and §4.4 (all-gather).  ``clip_coef``
     (from :func:`clip_coef`) multiplies every reduced grad before Adam.
     ``instances`` > 1 splits the D ranks into that many optimizer instances
-    (page 1 §5): reduce-scatter inside each, then a sum across instances.
+    (distributed-optimizer page, §5): reduce-scatter inside each, then a sum across instances.
     ``round_grad`` rounds every reduced grad to the grad type first.
     """
     lib = lib or load()
@@ -362,7 +362,7 @@ def count_nonfinite(sizes, D: int, bucket_elems: int, pad_unit: int, grad_scale:
 
 def allreduce(sizes, D: int, bucket_elems: int, pad_unit: int, grad_scale: float, grads,
               window=None, instances: int = 1, lib=None) -> None:
-    """All-reduce of the grads in place (page 1 §5 force_all_reduce; the
+    """All-reduce of the grads in place (distributed-optimizer page, §5 force_all_reduce; the
     tutorial's AllReduce = reduce-scatter + all-gather): every replica gets
     the reduced grad at every owned element, rounded to the grad type."""
     lib = lib or load()

@@ -436,7 +436,7 @@ def pin_bf16_rounding(lib):
 # ---------------------------------------------------------------------------
 
 def pin_gather_and_padding(lib):
-    """All-gather (page 1 §4.4): with the gather every replica holds the new
+    """All-gather (distributed-optimizer page, §4.4): with the gather every replica holds the new
     params; without it only the owning rank's replica changes on its range.
     Padding is never written."""
     sizes = [10, 27, 3]
@@ -645,7 +645,7 @@ def pin_clip_d_independence(lib):
 
 
 # ---------------------------------------------------------------------------
-# All-reduce pins (page 1 §5 force_all_reduce; tutorial "AllReduce")
+# All-reduce pins (distributed-optimizer page, §5 force_all_reduce; tutorial "AllReduce")
 # ---------------------------------------------------------------------------
 
 def pin_allreduce_every_rank(lib):
@@ -715,7 +715,7 @@ def pin_allreduce_rounds_to_nearest_even(lib):
 
 
 # ---------------------------------------------------------------------------
-# Optimizer instances (page 1 §5, num_distributed_optimizer_instances > 1)
+# Optimizer instances (distributed-optimizer page, §5, num_distributed_optimizer_instances > 1)
 # ---------------------------------------------------------------------------
 
 def pin_instances_hierarchical_order(lib):
@@ -869,7 +869,7 @@ def pin_nonfinite_count(lib):
     """Reading R13 of the oracle: the count is over owned elements of the
     reduced grad.  Closed cases: one Inf counts 1; +Inf and -Inf in two
     replicas (a NaN sum) count 1, not 2; NaN at padding counts 0; scaling
-    comes first (page 1 §5), so 1.5*2^127 in two replicas counts 0 with a
+    comes first (distributed-optimizer page, §5), so 1.5*2^127 in two replicas counts 0 with a
     factor of 1/2 and 1 with a factor of 1; a reduced grad that is finite in
     fp32 but rounds to bf16 Inf (max bf16 + 2^119, a tie rounded to even)
     counts only with the rounding of R12; across two instances the

@@ -37,8 +37,10 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for required in ("dopt_build_range_map", "dopt_step", "dopt_gather", "dopt_layout_free",
-                     "dopt_last_error"):
+    # the calls of the boundary as the scope table names them
+    for required in ("dopt_build_range_map", "dopt_layout_query", "dopt_layout_buckets",
+                     "dopt_layout_pieces", "dopt_layout_param_offsets", "dopt_layout_free",
+                     "dopt_step", "dopt_gather", "dopt_last_error"):
         assert required in names
 
 
@@ -58,7 +60,8 @@ def _compare_with_oracle(sizes, D, bucket, pad):
     O = oracle.range_map(sizes, D, bucket, pad)
     assert L.padded_numel == O.numel
     assert L.buckets() == list(zip(O.bucket_start.tolist(), O.bucket_end.tolist()))
-    assert L.param_ranges() == list(zip(O.param_start.tolist(), O.param_end.tolist()))
+    assert L.param_offsets() == list(zip(O.param_start.tolist(), O.param_end.tolist()))
+    assert L.param_ranges() == L.param_offsets()
     assert L.pieces() == O.pieces
     return L
 
@@ -237,7 +240,7 @@ def test_instances_errors(lib):
         with pytest.raises(B.DoptError) as e:
             B.dopt_build_range_map([10, 20], D, 0, 1, instances=instances)
         assert e.value.code == B.DOPT_E_ARG
-    cfg = B.dopt_layout_cfg(4, 1, 0, 1, 7)  # reserved must be 0
+    cfg = B.dopt_layout_cfg(4, 0, 1, 1, 7)  # reserved must be 0
     out = ctypes.c_void_p()
     sizes = (ctypes.c_int64 * 1)(10)
     assert B.lib().dopt_build_range_map(sizes, 1, None, ctypes.byref(cfg), ctypes.byref(out)) == B.DOPT_E_ARG
@@ -260,6 +263,39 @@ def test_counted_step_argument_checks_before_cuda(lib):
     assert call(flags=8) == B.DOPT_E_ARG
     assert call() in (B.DOPT_E_STATE, B.DOPT_E_CUDA)  # nothing was launched
     assert ctypes.sizeof(ctypes.c_int64) * 8 == B.DOPT_STEP_COUNTER_BYTES
+
+
+def test_stage_flag_checks_before_cuda(lib):
+    """DOPT_STEP_STAGE: taken by the plain, bucket-range and counted steps
+    for one-instance layouts with D in {1, 2, 4, 8, 16} and device grads,
+    refused otherwise before anything reaches CUDA."""
+    cfg = B.AdamConfig().to_c()
+    st = (0x30000, 0x40000, 0x50000)
+    stage = B.DOPT_STEP_GATHER | B.DOPT_STEP_STAGE
+    for D, inst, ok in ((2, 1, True), (8, 1, True), (16, 1, True), (3, 1, False), (8, 2, False),
+                        (32, 1, False)):
+        L = B.dopt_build_range_map([100, 30], D, 0, 8, instances=inst)
+        gp = (ctypes.c_void_p * D)(*[0x10000 * (r + 1) for r in range(D)])
+        rcs = [B.lib().dopt_step(L.handle, ctypes.byref(cfg), 1, gp, 0, *st, gp, stage, None,
+                                 None),
+               B.lib().dopt_step_buckets(L.handle, ctypes.byref(cfg), 1, 0, 1, gp, 0, *st, gp,
+                                         stage, None, None),
+               B.lib().dopt_step_counted(L.handle, ctypes.byref(cfg), 0x90000, gp, 0, *st, gp,
+                                         stage, None, None)]
+        for rc in rcs:
+            if ok:  # past the flag checks: the next check needs the device
+                assert rc in (B.DOPT_E_STATE, B.DOPT_E_CUDA), (D, inst, rc)
+            else:
+                assert rc == B.DOPT_E_ARG, (D, inst, rc)
+    L = _lib_layout([100, 30], 2, 0, 8)
+    gp = (ctypes.c_void_p * 2)(0x10000, 0x20000)
+    assert B.lib().dopt_step(L.handle, ctypes.byref(cfg), 1, gp, 0, *st, gp,
+                             stage | B.DOPT_STEP_HOST_GRADS, None, None) == B.DOPT_E_ARG
+    # the other entry points do not take it
+    assert B.lib().dopt_step_allreduce(L.handle, ctypes.byref(cfg), 1, gp, 0, *st, gp, stage,
+                                       None, None) == B.DOPT_E_ARG
+    assert B.lib().dopt_step_clipped(L.handle, ctypes.byref(cfg), 1, 1.0, gp, 0, *st, gp, stage,
+                                     0x70000, 0x80000, None, None) == B.DOPT_E_ARG
 
 
 def test_skip_nonfinite_only_on_the_clipped_step(lib):
@@ -295,7 +331,7 @@ def test_fp16_dtype_and_param_flag_accepted_before_cuda(lib):
                              None) == B.DOPT_E_ARG
     assert B.lib().dopt_allreduce(L.handle, gp, B.DOPT_FP16, 1.0, None) in (B.DOPT_E_STATE,
                                                                            B.DOPT_E_CUDA)
-    assert B.lib().dopt_step(L.handle, ctypes.byref(cfg), 1, gp, 0, *st, gp, 32, None,
+    assert B.lib().dopt_step(L.handle, ctypes.byref(cfg), 1, gp, 0, *st, gp, 64, None,
                              None) == B.DOPT_E_ARG
 
 

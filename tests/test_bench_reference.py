@@ -54,3 +54,20 @@ def test_kernel_hash_ignores_comments_only():
     assert strip(code) != strip(other)
     assert '"a // b"' in strip(code)
     assert len(bench.kernel_source_hash()) == 16
+
+
+def test_reference_arm_config_is_the_gpu_arms():
+    """Both arms print the same `config` object for a workload: the
+    reference arm's comes from the oracle's layout, the GPU arm's from the
+    library's (host-only calls), and the two layouts agree."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from zero_distributed_optimizer_gb300 import binding as B
+
+    out = _run({}, "--steps", "1", "--warmup", "3", "--workload", "toy_1000",
+               "--cpu-threads", "1")
+    assert out.returncode == 0, out.stderr
+    d = json.loads([l for l in out.stdout.splitlines() if l.startswith("{")][0])
+    w = bench.workload_by_name("toy_1000")
+    L = B.dopt_build_range_map(list(w.sizes), w.D, w.bucket_elems, w.pad_unit, list(w.wd_mask))
+    assert d["config"] == bench.workload_config(w, L.padded_numel, L.n_buckets, 1)

@@ -1,6 +1,8 @@
 """The boundary is plain C: a C11 program that includes include/dopt.h,
-links libdopt.so and calls the host-only entry points (layout and range
-map of the page-1 ownership demo) compiles without warnings and runs
+links libdopt.so and calls the host-only entry points as the boundary
+states them (dopt_build_range_map, dopt_layout_query, dopt_layout_buckets,
+dopt_layout_pieces, dopt_layout_param_offsets, dopt_layout_free; layout and range
+map of the ownership demo on the distributed-optimizer page, §3) compiles without warnings and runs
 without a GPU."""
 import os
 import subprocess
@@ -20,7 +22,7 @@ _Static_assert(sizeof(dopt_step_counter) == 64, "dopt_step_counter is 64 bytes")
 int main(void)
 {
     const int64_t sizes[5] = {130, 260, 90, 310, 210};
-    dopt_layout_cfg cfg = {4, 1, 0, 1, 0};
+    dopt_layout_cfg cfg = {.D = 4, .bucket_elems = 0, .pad_unit = 1};
     dopt_layout *L = NULL;
     if (dopt_build_range_map(sizes, 5, NULL, &cfg, &L) != DOPT_OK) {
         printf("build failed: %s\n", dopt_last_error());
@@ -39,7 +41,13 @@ int main(void)
                    (long long)pieces[i].gbuf_world.end, (long long)pieces[i].gbuf_local.start,
                    (long long)pieces[i].gbuf_local.end, (long long)pieces[i].param.start,
                    (long long)pieces[i].param.end);
-    dopt_layout_cfg bad = {0, 1, 0, 1, 0};
+    dopt_range buckets[1], params[5];
+    dopt_layout_buckets(L, buckets);
+    printf("bucket [%lld,%lld)\n", (long long)buckets[0].start, (long long)buckets[0].end);
+    if (dopt_layout_param_offsets(L, params) != DOPT_OK) return 1;
+    for (int p = 0; p < 5; ++p)
+        printf("param %d [%lld,%lld)\n", p, (long long)params[p].start, (long long)params[p].end);
+    dopt_layout_cfg bad = {.D = 0, .bucket_elems = 0, .pad_unit = 1};
     dopt_layout *L2 = NULL;
     printf("bad D -> %d\n", dopt_build_range_map(sizes, 5, NULL, &bad, &L2));
     dopt_layout_free(L);
@@ -67,5 +75,8 @@ def test_c11_program_uses_the_boundary(tmp_path):
     assert lines[1:4] == ["rank 1 param 1 world [250,390) local [0,140) param [120,260)",
                           "rank 1 param 2 world [390,480) local [140,230) param [0,90)",
                           "rank 1 param 3 world [480,500) local [230,250) param [0,20)"]
-    assert lines[4] == "bad D -> -1"
-    assert "sm_103a" in lines[5]
+    assert lines[4] == "bucket [0,1000)"
+    assert lines[5:10] == ["param 0 [0,130)", "param 1 [130,390)", "param 2 [390,480)",
+                           "param 3 [480,790)", "param 4 [790,1000)"]
+    assert lines[10] == "bad D -> -1"
+    assert "sm_103a" in lines[11]

@@ -32,7 +32,7 @@ int orc_step(const int64_t *sizes, int32_t n, const uint8_t *wd_mask, int32_t D,
              float *main_grad_out, int64_t w0, int64_t w1, float clip_coef, int32_t round_grad,
              int32_t param_is_f16);
 
-#define D 4
+#define NR 4
 #define CHECK(x) do { cudaError_t e_ = (x); if (e_ != cudaSuccess) { \
     printf("cuda error %s at %d\n", cudaGetErrorString(e_), __LINE__); return 1; } } while (0)
 
@@ -48,7 +48,7 @@ int main(void)
 {
     const int64_t sizes[7] = {130, 260, 90, 310, 210, 5003, 17};
     const uint8_t wd[7] = {1, 1, 0, 1, 1, 1, 0};
-    dopt_layout_cfg lc = {D, 8, 0, 1, 0};
+    dopt_layout_cfg lc = {.D = NR, .bucket_elems = 0, .pad_unit = 8};
     dopt_layout *L = NULL;
     if (dopt_build_range_map(sizes, 7, wd, &lc, &L) != DOPT_OK || dopt_layout_to_device(L) != DOPT_OK) {
         printf("layout: %s\n", dopt_last_error());
@@ -58,7 +58,23 @@ int main(void)
     int32_t nb = 0, np = 0;
     dopt_layout_query(L, &N, &nb, &np);
     size_t n = (size_t)N;
-    uint16_t *hg[2][D], *hp[D], *op[D];
+    /* each param's place in the flat buffer: consecutive offsets */
+    dopt_range po[7];
+    if (dopt_layout_param_offsets(L, po) != DOPT_OK) {
+        printf("param offsets: %s\n", dopt_last_error());
+        return 1;
+    }
+    int64_t at = 0;
+    for (int p = 0; p < 7; ++p) {
+        if (po[p].start != at || po[p].end != at + sizes[p]) {
+            printf("param %d at [%lld,%lld), expected start %lld\n", p, (long long)po[p].start,
+                   (long long)po[p].end, (long long)at);
+            return 1;
+        }
+        at = po[p].end;
+    }
+    printf("param offsets ok, %lld elements padded to %lld\n", (long long)at, (long long)N);
+    uint16_t *hg[2][NR], *hp[NR], *op[NR];
     float *hs[3], *os[3];
     for (int s = 0; s < 3; ++s) {
         hs[s] = malloc(n * 4);
@@ -67,7 +83,7 @@ int main(void)
             hs[s][i] = s == 0 ? 0.02f * next_unit() : (s == 1 ? 1e-4f * next_unit() : 1e-6f * (next_unit() + 1.0f));
         memcpy(os[s], hs[s], n * 4);
     }
-    for (int r = 0; r < D; ++r) {
+    for (int r = 0; r < NR; ++r) {
         hp[r] = malloc(n * 2);
         op[r] = malloc(n * 2);
         for (size_t i = 0; i < n; ++i) hp[r][i] = to_bf16_trunc(0.02f * next_unit());
@@ -77,9 +93,9 @@ int main(void)
             for (size_t i = 0; i < n; ++i) hg[t][r][i] = to_bf16_trunc(1e-3f * next_unit());
         }
     }
-    void *dg[D], *dp[D];
+    void *dg[NR], *dp[NR];
     float *ds[3];
-    for (int r = 0; r < D; ++r) {
+    for (int r = 0; r < NR; ++r) {
         CHECK(cudaMalloc(&dg[r], n * 2));
         CHECK(cudaMalloc(&dp[r], n * 2));
         CHECK(cudaMemcpy(dp[r], hp[r], n * 2, cudaMemcpyHostToDevice));
@@ -91,7 +107,7 @@ int main(void)
     dopt_adam_cfg cfg = {1e-3f, 0.9f, 0.95f, 1e-8f, 0.1f, 0.25f};
     orc_adam ocfg = {1e-3f, 0.9f, 0.95f, 1e-8f, 0.1f, 0.25f};
     for (int t = 0; t < 2; ++t) {
-        for (int r = 0; r < D; ++r)
+        for (int r = 0; r < NR; ++r)
             CHECK(cudaMemcpy(dg[r], hg[t][r], n * 2, cudaMemcpyHostToDevice));
         /* step 1 with the fused gather; step 2 without it, then dopt_gather */
         uint32_t flags = t == 0 ? DOPT_STEP_GATHER : 0u;
@@ -104,7 +120,7 @@ int main(void)
             printf("gather: %s\n", dopt_last_error());
             return 1;
         }
-        if (orc_step(sizes, 7, wd, D, 1, 0, 8, &ocfg, t + 1, 0, (const void *const *)hg[t], os[0],
+        if (orc_step(sizes, 7, wd, NR, 1, 0, 8, &ocfg, t + 1, 0, (const void *const *)hg[t], os[0],
                      os[1], os[2], op, 1, NULL, 0, N, 1.0f, 0, 0) != 0) {
             printf("oracle failed\n");
             return 1;
@@ -116,13 +132,13 @@ int main(void)
         CHECK(cudaMemcpy(hs[s], ds[s], n * 4, cudaMemcpyDeviceToHost));
         diff += memcmp(hs[s], os[s], n * 4) != 0;
     }
-    for (int r = 0; r < D; ++r) {
+    for (int r = 0; r < NR; ++r) {
         CHECK(cudaMemcpy(hp[r], dp[r], n * 2, cudaMemcpyDeviceToHost));
         diff += memcmp(hp[r], op[r], n * 2) != 0;
     }
     printf("elements %lld buffers differing %ld\n", (long long)N, diff);
     /* an error path: a replica pointer off its 16-byte alignment */
-    void *bad[D] = {dg[0], (char *)dg[1] + 2, dg[2], dg[3]};
+    void *bad[NR] = {dg[0], (char *)dg[1] + 2, dg[2], dg[3]};
     int rc = dopt_step(L, &cfg, 3, (const void *const *)bad, DOPT_BF16, ds[0], ds[1], ds[2], dp,
                        DOPT_STEP_GATHER, NULL, 0);
     printf("misaligned -> %d (%s)\n", rc, dopt_last_error());
@@ -154,5 +170,6 @@ def test_c_program_steps_on_the_device(tmp_path):
     assert res.returncode == 0, res.stderr
     out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=300)
     assert out.returncode == 0, out.stdout + out.stderr
+    assert "param offsets ok, 6020 elements padded to 6048" in out.stdout
     assert "buffers differing 0" in out.stdout
     assert "misaligned -> -3" in out.stdout

@@ -1,4 +1,4 @@
-"""Several distributed-optimizer instances (page 1 §5) on the device, against
+"""Several distributed-optimizer instances (distributed-optimizer page, §5) on the device, against
 the oracle: reduce-scatter inside each instance of R = D/I ranks, sums across
 instances in instance order, write-back and gather inside each instance."""
 from dataclasses import asdict

@@ -129,7 +129,7 @@ def check_layout(sizes, D, bucket, pad, wd=None, instances=1):
     N = L.padded_numel
     tr = tile_index(N, runs)
     owned = np.zeros(N, np.int32)
-    for a, b in L.param_ranges():
+    for a, b in L.param_offsets():
         owned[a:b] = 1
     # one launch over every bucket, with either element path
     for shared in (True, False):

@@ -29,7 +29,7 @@ INF_BF16, NINF_BF16, NAN_BF16 = 0x7F80, 0xFF80, 0x7FC0
 
 def _owned(L):
     mask = np.zeros(L.padded_numel, bool)
-    for a, b in L.param_ranges():
+    for a, b in L.param_offsets():
         mask[a:b] = True
     return mask
 

@@ -20,7 +20,7 @@ DEV = "cuda"
 
 def _owned_mask(L):
     mask = torch.zeros(L.padded_numel, dtype=torch.bool, device=DEV)
-    for a, b in L.param_ranges():
+    for a, b in L.param_offsets():
         mask[a:b] = True
     return mask
 

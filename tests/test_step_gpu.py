@@ -62,7 +62,7 @@ class Case:
 
     def padding_mask(self):
         owned = np.zeros(self.N, bool)
-        for a, b in self.L.param_ranges():
+        for a, b in self.L.param_offsets():
             owned[a:b] = True
         return ~owned
 

@@ -7,8 +7,10 @@ cause).  It keeps the norm pass's scratch in a static array inside the
 library instead of a caller workspace.  This file checks, through the C ABI,
 that two calls in a row give the same results as the workspace entry point
 within the parity tolerance, including the second call, which finds the
-first call's contents still in the shared scratch.  It is collected last and
-also passes alone in a fresh process."""
+first call's contents still in the shared scratch, and that this second
+call takes no device memory (the device's free memory, as the driver
+reports it, and the count of torch's allocations stay as they were).  It is
+collected last and also passes alone in a fresh process."""
 import pytest
 import torch
 
@@ -36,11 +38,22 @@ def test_noalloc_matches_workspace_entry_point(grad_dtype, D):
     nb = torch.zeros(2, device=DEV)
     ws = B.clip_workspace(DEV)
     adam = B.AdamConfig(grad_scale=1.0 / D)
+    dev_grads = [[x.to(DEV) for x in grads[i]] for i in range(2)]
+    torch.cuda.synchronize()
     for i, max_norm in enumerate((0.05, 1e9)):  # clipping engaged, then not
-        g = [x.to(DEV) for x in grads[i]]
+        g = dev_grads[i]
         B.dopt_step_clipped(L, adam, i + 1, max_norm, g, *a, pa, mga, ws, norm_out=na)
+        if i == 1:  # after the first call's set-up: nothing may allocate
+            torch.cuda.synchronize()
+            free_before = torch.cuda.mem_get_info()[0]
+            allocs_before = torch.cuda.memory_stats().get("allocation.all.allocated", 0)
         B.dopt_step_clipped_noalloc(L, adam, i + 1, max_norm, g, *b, pb, mgb, norm_out=nb)
         torch.cuda.synchronize()
+        if i == 1:
+            # no device memory taken by the call: not from the driver (free
+            # memory of the device unchanged), not from torch's allocator
+            assert torch.cuda.mem_get_info()[0] == free_before
+            assert torch.cuda.memory_stats().get("allocation.all.allocated", 0) == allocs_before
         assert_f32_close(t2np_f32(nb), t2np_f32(na), f"norm/coef call {i}")
         for name, x, y in zip(("master", "exp_avg", "exp_avg_sq"), b, a):
             assert_f32_close(t2np_f32(x), t2np_f32(y), f"{name} call {i}")

@@ -39,6 +39,7 @@ DOPT_STEP_HOST_GRADS = 2
 DOPT_STEP_ROUND_GRAD = 4
 DOPT_STEP_SKIP_NONFINITE = 8
 DOPT_STEP_PARAMS_FP16 = 16
+DOPT_STEP_STAGE = 32
 DOPT_CLIP_WORKSPACE_BYTES = 16384
 DOPT_STEP_COUNTER_BYTES = 64  # sizeof(dopt_step_counter)
 DOPT_COUNTER_BAD_STEP = 1
@@ -66,8 +67,8 @@ class dopt_piece(ctypes.Structure):
 
 
 class dopt_layout_cfg(ctypes.Structure):
-    _fields_ = [("D", ctypes.c_int32), ("pad_unit", ctypes.c_int32),
-                ("bucket_elems", ctypes.c_int64), ("instances", ctypes.c_int32),
+    _fields_ = [("D", ctypes.c_int32), ("bucket_elems", ctypes.c_int64),
+                ("pad_unit", ctypes.c_int32), ("instances", ctypes.c_int32),
                 ("reserved", ctypes.c_int32)]
 
 
@@ -93,6 +94,8 @@ def _declare(lib):
     lib.dopt_layout_buckets.argtypes = [vp, P(dopt_range)]
     lib.dopt_layout_pieces.restype = ctypes.c_int
     lib.dopt_layout_pieces.argtypes = [vp, P(dopt_piece)]
+    lib.dopt_layout_param_offsets.restype = ctypes.c_int
+    lib.dopt_layout_param_offsets.argtypes = [vp, P(dopt_range)]
     lib.dopt_layout_param_ranges.restype = ctypes.c_int
     lib.dopt_layout_param_ranges.argtypes = [vp, P(dopt_range)]
     lib.dopt_layout_to_device.restype = ctypes.c_int
@@ -128,6 +131,8 @@ def _declare(lib):
     lib.dopt_allreduce.argtypes = [vp, P(vp), ctypes.c_int, ctypes.c_float, vp]
     lib.dopt_gather.restype = ctypes.c_int
     lib.dopt_gather.argtypes = [vp, P(vp), vp]
+    lib.dopt_stage_timeouts.restype = ctypes.c_int
+    lib.dopt_stage_timeouts.argtypes = [ctypes.c_int, P(ctypes.c_uint32)]
     lib.dopt_device_checks.restype = ctypes.c_int
     lib.dopt_device_checks.argtypes = [ctypes.c_int, P(ctypes.c_uint32), P(ctypes.c_int64)]
     lib.dopt_last_error.restype = ctypes.c_char_p
@@ -159,6 +164,15 @@ def device_checks(reset: bool = False):
     flags, first = ctypes.c_uint32(0), ctypes.c_int64(0)
     _check(lib().dopt_device_checks(1 if reset else 0, ctypes.byref(flags), ctypes.byref(first)))
     return flags.value, first.value
+
+
+def stage_timeouts(reset: bool = False) -> int:
+    """Staged CTAs (DOPT_STEP_STAGE) on the current device whose bulk copies
+    ran past their time limit and skipped their tile (0 unless the copy
+    engine failed); reset clears the count."""
+    c = ctypes.c_uint32(0)
+    _check(lib().dopt_stage_timeouts(1 if reset else 0, ctypes.byref(c)))
+    return c.value
 
 
 def _check(rc: int):
@@ -210,7 +224,14 @@ class Layout:
         _check(lib().dopt_layout_buckets(self.handle, arr))
         return [(arr[i].start, arr[i].end) for i in range(self.n_buckets)]
 
+    def param_offsets(self) -> list:
+        """Each param's [start, end) in the flat buffer (dopt_layout_param_offsets)."""
+        arr = (dopt_range * max(self.n_params, 1))()
+        _check(lib().dopt_layout_param_offsets(self.handle, arr))
+        return [(arr[i].start, arr[i].end) for i in range(self.n_params)]
+
     def param_ranges(self) -> list:
+        """The same list through the call's earlier name, dopt_layout_param_ranges."""
         arr = (dopt_range * max(self.n_params, 1))()
         _check(lib().dopt_layout_param_ranges(self.handle, arr))
         return [(arr[i].start, arr[i].end) for i in range(self.n_params)]
@@ -256,7 +277,7 @@ def dopt_build_range_map(param_sizes, D: int, bucket_elems: int = 0, pad_unit: i
                          wd_mask=None, instances: int = 1) -> Layout:
     """Flat-buffer layout and four-way range map (host only, no CUDA call).
     ``instances`` > 1 groups the D ranks into that many optimizer instances
-    of D // instances ranks each (page 1 §5)."""
+    of D // instances ranks each (distributed-optimizer page, §5)."""
     n = len(param_sizes)
     sizes = (ctypes.c_int64 * max(n, 1))(*[int(s) for s in param_sizes])
     wd = None
@@ -264,7 +285,7 @@ def dopt_build_range_map(param_sizes, D: int, bucket_elems: int = 0, pad_unit: i
         if len(wd_mask) != n:
             raise DoptError(DOPT_E_ARG, "wd_mask length differs from param_sizes")
         wd = (ctypes.c_uint8 * max(n, 1))(*[1 if x else 0 for x in wd_mask])
-    cfg = dopt_layout_cfg(int(D), int(pad_unit), int(bucket_elems), int(instances), 0)
+    cfg = dopt_layout_cfg(int(D), int(bucket_elems), int(pad_unit), int(instances), 0)
     out = ctypes.c_void_p()
     _check(lib().dopt_build_range_map(sizes, n, wd, ctypes.byref(cfg), ctypes.byref(out)))
     return Layout(out.value, int(D), n, max(int(instances), 1))
@@ -289,9 +310,10 @@ def _check_tensor(t, name, dtype, numel, device):
         raise DoptError(DOPT_E_ARG, f"{name} must be contiguous with >= {numel} elements")
 
 
-def _flags(gather: bool, host_grads: bool = False, round_grad: bool = False) -> int:
+def _flags(gather: bool, host_grads: bool = False, round_grad: bool = False,
+           stage: bool = False) -> int:
     return ((DOPT_STEP_GATHER if gather else 0) | (DOPT_STEP_HOST_GRADS if host_grads else 0)
-            | (DOPT_STEP_ROUND_GRAD if round_grad else 0))
+            | (DOPT_STEP_ROUND_GRAD if round_grad else 0) | (DOPT_STEP_STAGE if stage else 0))
 
 
 def _grad_code(gdt) -> int:
@@ -357,13 +379,14 @@ def _step_pointers(layout: Layout, grad_replicas, master, exp_avg, exp_avg_sq, p
 def dopt_step_buckets(layout: Layout, adam: AdamConfig, step: int, first_bucket: int,
                       n_buckets: int, grad_replicas, master, exp_avg, exp_avg_sq,
                       param_replicas, gather: bool = True, main_grad_out=None,
-                      stream=None, host_grads: bool = False, round_grad: bool = False) -> None:
+                      stream=None, host_grads: bool = False, round_grad: bool = False,
+                      stage: bool = False) -> None:
     """The step over buckets [first_bucket, first_bucket + n_buckets) only."""
     import torch
 
     device, gp, pp, dt, mg, pflag = _step_pointers(layout, grad_replicas, master, exp_avg, exp_avg_sq,
                                             param_replicas, main_grad_out, host_grads)
-    flags = _flags(gather, host_grads, round_grad) | pflag
+    flags = _flags(gather, host_grads, round_grad, stage) | pflag
     cfg = adam.to_c()
     with torch.cuda.device(device):
         _check(lib().dopt_step_buckets(
@@ -412,20 +435,22 @@ def dopt_allreduce(layout: Layout, grad_replicas, grad_scale: float, stream=None
 
 def dopt_step(layout: Layout, adam: AdamConfig, step: int, grad_replicas, master, exp_avg,
               exp_avg_sq, param_replicas, gather: bool = True, main_grad_out=None,
-              stream=None, host_grads: bool = False, round_grad: bool = False) -> None:
+              stream=None, host_grads: bool = False, round_grad: bool = False,
+              stage: bool = False) -> None:
     """One fused ZeRO-1 step (reduce-scatter, AdamW, write-back, all-gather).
 
     grad_replicas: D bf16 or fp32 CUDA tensors (or, with host_grads, pinned
     CPU tensors the kernel reads in place); master/exp_avg/exp_avg_sq: fp32;
     param_replicas: D bf16; main_grad_out: optional fp32.  Each holds at
     least layout.padded_numel elements.  Asynchronous on `stream` (default:
-    torch's current stream).
+    torch's current stream).  stage: read through shared memory with bulk
+    copies (DOPT_STEP_STAGE).
     """
     import torch
 
     device, gp, pp, dt, mg, pflag = _step_pointers(layout, grad_replicas, master, exp_avg, exp_avg_sq,
                                             param_replicas, main_grad_out, host_grads)
-    flags = _flags(gather, host_grads, round_grad) | pflag
+    flags = _flags(gather, host_grads, round_grad, stage) | pflag
     cfg = adam.to_c()
     with torch.cuda.device(device):
         _check(lib().dopt_step(layout.handle, ctypes.byref(cfg), int(step), gp, dt,
@@ -452,6 +477,25 @@ def counter_state(counter):
     return int(h[0]), int(h[1:2].view(torch.int32)[0])
 
 
+def counter_scalars(counter):
+    """(step_size, bc2_sqrt): the two step-dependent Adam scalars the last
+    counted step took, as float32 bit patterns read back (synchronises)."""
+    import torch
+
+    h = counter.cpu()[2:3].view(torch.float32)
+    return float(h[0]), float(h[1])
+
+
+def counter_diagnostics(counter):
+    """(exact_steps, undecided_steps) of a step counter: the counted steps
+    whose two scalars needed the device's exact evaluation, and those where
+    even it could not decide (see dopt_step_counted; synchronises)."""
+    import torch
+
+    h = counter.cpu()[4:5].view(torch.int32)
+    return int(h[0]), int(h[1])
+
+
 def _check_counter(counter, device):
     import torch
 
@@ -465,7 +509,7 @@ def _check_counter(counter, device):
 def dopt_step_counted(layout: Layout, adam: AdamConfig, counter, grad_replicas, master,
                       exp_avg, exp_avg_sq, param_replicas, gather: bool = True,
                       main_grad_out=None, stream=None, host_grads: bool = False,
-                      round_grad: bool = False) -> None:
+                      round_grad: bool = False, stage: bool = False) -> None:
     """dopt_step with the step number read from, and advanced in, a device
     counter (:func:`step_counter`): the launches do not depend on the step,
     so they can be captured once in a CUDA graph and replayed every step."""
@@ -474,7 +518,7 @@ def dopt_step_counted(layout: Layout, adam: AdamConfig, counter, grad_replicas, 
     device, gp, pp, dt, mg, pflag = _step_pointers(layout, grad_replicas, master, exp_avg, exp_avg_sq,
                                             param_replicas, main_grad_out, host_grads)
     _check_counter(counter, master.device)
-    flags = _flags(gather, host_grads, round_grad) | pflag
+    flags = _flags(gather, host_grads, round_grad, stage) | pflag
     cfg = adam.to_c()
     with torch.cuda.device(device):
         _check(lib().dopt_step_counted(layout.handle, ctypes.byref(cfg), counter.data_ptr(), gp,
@@ -492,7 +536,8 @@ class StepPlan:
 
     def __init__(self, layout: Layout, adam: AdamConfig, grad_replicas, master, exp_avg,
                  exp_avg_sq, param_replicas, gather: bool = True, main_grad_out=None,
-                 host_grads: bool = False, round_grad: bool = False, stream=None):
+                 host_grads: bool = False, round_grad: bool = False, stream=None,
+                 stage: bool = False):
         import torch
 
         self.device, self._gp, self._pp, self._dt, self._mg, pflag = _step_pointers(
@@ -502,7 +547,7 @@ class StepPlan:
         self._keep = (list(grad_replicas), master, exp_avg, exp_avg_sq, list(param_replicas),
                       main_grad_out)
         self._state = (master.data_ptr(), exp_avg.data_ptr(), exp_avg_sq.data_ptr())
-        self._flags = _flags(gather, host_grads, round_grad) | pflag
+        self._flags = _flags(gather, host_grads, round_grad, stage) | pflag
         self._cfg = adam.to_c()
         with torch.cuda.device(self.device):
             self._stream = _stream_handle(stream)

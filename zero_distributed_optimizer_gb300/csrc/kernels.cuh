@@ -51,30 +51,18 @@ struct Scalars {
     float b1, b2, omb1, omb2, decay, step_size, bc2_sqrt, eps, scale;
 };
 
-// b^t for an integer t >= 1, by repeated squaring in double.  The host
-// (dopt_step) and the device (dopt_step_counted) run this same sequence of
-// IEEE multiplies, so both get the same double; the device's double
-// pipeline is slow, and this takes at most 2*63 multiplies where a general
-// pow takes far more.  Rounded to float as below, it gave the scalars of
-// C's pow(b, t) in every case checked (9 betas x 4 learning rates x t up to
-// 2e6).
-__host__ __device__ inline double beta_pow(double b, int64_t t) {
-    double r = 1.0;
-    double x = b;
-    while (t > 0) {
-        if (t & 1) r = r * x;
-        t >>= 1;
-        if (t > 0) x = x * x;
-    }
-    return r;
+// The two scalars that depend on the step number t: step_size =
+// lr / (1 - beta1^t) and bc2_sqrt = sqrt(1 - beta2^t), the bias corrections
+// of Adam.  Each is evaluated in double and rounded to float once, with
+// beta^t = pow(beta, t): the host entry points call the C library's pow
+// (step_size_host, bc2_sqrt_host), so their scalars are those of that
+// definition, bit for bit.  The device (the counter kernel of the counted
+// steps) has no such pow; counted_scalar below reaches the same floats.
+inline float step_size_host(const dopt_adam_cfg &c, int64_t t) {
+    return float(double(c.lr) / (1.0 - std::pow(double(c.beta1), double(t))));
 }
-
-// lr / (1 - beta1^t) and sqrt(1 - beta2^t), each in double, rounded once.
-__host__ __device__ inline float step_size_for(const dopt_adam_cfg &c, int64_t t) {
-    return float(double(c.lr) / (1.0 - beta_pow(c.beta1, t)));
-}
-__host__ __device__ inline float bc2_sqrt_for(const dopt_adam_cfg &c, int64_t t) {
-    return float(sqrt(1.0 - beta_pow(c.beta2, t)));
+inline float bc2_sqrt_host(const dopt_adam_cfg &c, int64_t t) {
+    return float(std::sqrt(1.0 - std::pow(double(c.beta2), double(t))));
 }
 
 // The scalars that do not depend on the step number, each evaluated in
@@ -94,11 +82,11 @@ __host__ __device__ inline Scalars scalars_for_fixed(const dopt_adam_cfg &c) {
     return s;
 }
 
-// All the scalars of step t.
-__host__ __device__ inline Scalars scalars_for(const dopt_adam_cfg &c, int64_t t) {
+// All the scalars of step t (host).
+inline Scalars scalars_for(const dopt_adam_cfg &c, int64_t t) {
     Scalars s = scalars_for_fixed(c);
-    s.step_size = step_size_for(c, t);
-    s.bc2_sqrt = bc2_sqrt_for(c, t);
+    s.step_size = step_size_host(c, t);
+    s.bc2_sqrt = bc2_sqrt_host(c, t);
     return s;
 }
 
@@ -117,10 +105,16 @@ struct CounterBlock {
     int32_t status;
     int32_t reserved;
     CounterHot hot;
-    float unused[8];
+    uint32_t exact_steps;      // steps whose scalars took the exact evaluation
+    uint32_t undecided_steps;  // steps where even that left the float open
+    uint32_t unused[6];
 };
 static_assert(sizeof(CounterBlock) == sizeof(dopt_step_counter), "counter layout");
 static_assert(offsetof(CounterBlock, hot) % 16 == 0, "one 16-byte load");
+static_assert(offsetof(CounterBlock, exact_steps) == offsetof(dopt_step_counter, exact_steps) &&
+                  offsetof(CounterBlock, undecided_steps) ==
+                      offsetof(dopt_step_counter, undecided_steps),
+              "counter layout");
 constexpr int64_t kMaxCountedStep = int64_t(1) << 62;
 
 // The part of the run table one launch covers: runs [run_begin, run_limit)
@@ -826,38 +820,335 @@ __global__ void __launch_bounds__(kThreads, 3) dopt_step_kernel(const __grid_con
     }
 }
 
-// The slow double-precision scalar of lane 0 (step size) or lane 1
-// (sqrt of the second bias correction) for step t.
-__device__ __forceinline__ float counted_scalar(const dopt_adam_cfg &cfg, int64_t t, int lane) {
-    if (t < 1 || t > kMaxCountedStep) return 0.0f;
-    return lane == 0 ? step_size_for(cfg, t) : bc2_sqrt_for(cfg, t);
+// ---------------------------------------------------------------------------
+// The staged step kernel: each tile's grads and state moved into shared
+// memory by bulk copies first (DOPT_STEP_STAGE)
+// ---------------------------------------------------------------------------
+//
+// The same step as dopt_step_kernel (one-instance layouts, D in {1, 2, 4, 8,
+// 16}, plain or counted), with a different way of reading: one thread of the
+// CTA issues one 1-D bulk copy (cp.async.bulk, the copy engine of the SM,
+// global -> this CTA's shared memory, no cluster multicast) per grad replica
+// and per state array for the tile's whole vectors, completing on an
+// mbarrier, while the CTA looks up its runs; the threads then read their
+// vectors from shared memory.  Stores go to global memory as in the plain
+// kernel.  The plain kernel loads with 128-bit vector loads straight into
+// registers; this one exists to measure the other design.
+
+// Bulk-copy waits that ran past their time limit (the copy engine never
+// completed them); the CTA then skipped its tile.  Read by
+// dopt_stage_timeouts.
+__device__ unsigned int g_stage_timeouts;
+
+constexpr unsigned long long kStageWaitNs = 2000000000ull;  // 2 s
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
 }
 
-// First launch of dopt_step_counted, one warp of two lanes: the step number
-// from the counter, its scalars (the lanes evaluate the two slow
-// double-precision ones side by side), the counter advanced, or the bad
-// number reported.  It is launched as a programmatic dependent of the
-// previous kernel on the stream (the step kernel of the step before, which
-// lets it start once all its CTAs run): it evaluates the scalars for the
-// number it reads then, waits for the previous grid to complete, reads the
-// number again and evaluates once more only if it changed, so the slow part
-// overlaps the previous step's last wave.
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Wait for phase `parity` of the mbarrier at `bar` for at most kStageWaitNs;
+// false if the time ran out.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    const unsigned long long t0 = globaltimer_ns();
+    for (;;) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (done) return true;
+        if (globaltimer_ns() - t0 > kStageWaitNs) return false;
+    }
+}
+
+// One 1-D bulk copy of `bytes` (a multiple of 16, both addresses 16-byte
+// aligned) from global memory into this CTA's shared memory, completing on
+// the mbarrier at `bar`.
+__device__ __forceinline__ void bulk_to_shared(uint32_t dst, const void *src, uint32_t bytes,
+                                               uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        :
+        : "r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// Shared-memory bytes of one staged tile: DC grad chunks and master/m/v.
+template <typename G, int DC>
+constexpr size_t staged_smem_bytes() {
+    return size_t(DC) * kDoptTileElems * sizeof(G) + 3 * kDoptTileElems * sizeof(float);
+}
+
+template <typename G>
+__device__ __forceinline__ void load_grad_shared(GradVec<G> &g, const unsigned char *p) {
+    if constexpr (sizeof(G) == 2) {
+        g.a = *reinterpret_cast<const uint4 *>(p);
+    } else {
+        g.a = *reinterpret_cast<const float4 *>(p);
+        g.b = *reinterpret_cast<const float4 *>(p + 16);
+    }
+}
+
+template <typename G, int DC, int MODE>
+__device__ __forceinline__ void staged_tile(const StepArgs &a, const Scalars &sc, StepDep dep,
+                                            int32_t status, unsigned char *stage,
+                                            unsigned long long *bar_ptr) {
+    constexpr int64_t kGradChunk = kDoptTileElems * int64_t(sizeof(G));
+    const int64_t tile = a.rv.tile0 + blockIdx.x;
+    const int64_t base = tile * kDoptTileElems;
+    const int64_t e0 = base + int64_t(threadIdx.x) * kVec;
+    // every whole vector of a run lies in [lo, hi) of the view: stage the
+    // tile's part of that span, cut to whole vectors (so that sizes and
+    // addresses are multiples of 16 bytes)
+    const int64_t s0 = max(base, a.rv.lo & ~int64_t(kVec - 1));
+    const int64_t s1 = min(base + kDoptTileElems, a.rv.hi & ~int64_t(kVec - 1));
+    const int64_t n = s1 - s0;
+    const uint32_t bar = smem_addr(bar_ptr);
+    if (threadIdx.x == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && n > 0) {
+        const uint32_t gbytes = uint32_t(n * int64_t(sizeof(G)));
+        const uint32_t sbytes = uint32_t(n * 4);
+        const uint32_t total = uint32_t(DC) * gbytes + 3 * sbytes;
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(total)
+                     : "memory");
+        const uint32_t sm = smem_addr(stage);
+        const int64_t goff = (s0 - base) * int64_t(sizeof(G)), soff = (s0 - base) * 4;
+#pragma unroll
+        for (int r = 0; r < DC; ++r)
+            bulk_to_shared(sm + uint32_t(r * kGradChunk + goff),
+                           static_cast<const G *>(a.grads[r]) + s0, gbytes, bar);
+        const uint32_t st = sm + uint32_t(DC * kGradChunk);
+        bulk_to_shared(st + uint32_t(soff), a.master + s0, sbytes, bar);
+        bulk_to_shared(st + uint32_t(kDoptTileElems * 4 + soff), a.exp_avg + s0, sbytes, bar);
+        bulk_to_shared(st + uint32_t(2 * kDoptTileElems * 4 + soff), a.exp_avg_sq + s0, sbytes, bar);
+    }
+    int j;
+    const VecKind kind = locate(a.rv, tile, e0, j);  // while the copies fly
+    const bool ok = n <= 0 || mbar_wait(bar, 0);
+    if (__syncthreads_or(!ok)) {
+        // the copy engine did not complete in time (for some thread: the
+        // whole CTA decides together): count it, give the copies one more
+        // bounded wait (they write this CTA's shared memory), and leave the
+        // tile alone
+        if (threadIdx.x == 0) atomicAdd(&g_stage_timeouts, 1u);
+        mbar_wait(bar, 0);
+        return;
+    }
+    if (kind == kFull && vector_in_buffer(a.rv, e0)) {
+        const int64_t off = e0 - base;
+        GradVec<G> g[DC];
+#pragma unroll
+        for (int r = 0; r < DC; ++r) load_grad_shared<G>(g[r], stage + r * kGradChunk + off * int64_t(sizeof(G)));
+        float acc[8];
+        reduce_loaded<G, DC, DC>(g, sc.scale, acc);
+        if (a.round_grad) to_grad_type8<G>(acc);
+        const float *sw = reinterpret_cast<const float *>(stage + DC * kGradChunk) + off;
+        const float *smv = sw + kDoptTileElems, *svv = sw + 2 * kDoptTileElems;
+        const float4 w0 = *reinterpret_cast<const float4 *>(sw), w1 = *reinterpret_cast<const float4 *>(sw + 4);
+        const float4 m0 = *reinterpret_cast<const float4 *>(smv), m1 = *reinterpret_cast<const float4 *>(smv + 4);
+        const float4 v0 = *reinterpret_cast<const float4 *>(svv), v1 = *reinterpret_cast<const float4 *>(svv + 4);
+        update_and_store<G, DC, MODE>(a, sc, dep, e0, a.rv.run_meta[j], status, acc, w0, w1, m0, m1,
+                                      v0, v1);
+    }
+    const unsigned mixed = __ballot_sync(0xffffffffu, kind == kMixed);
+    if (mixed != 0 && status == 0) mixed_elements<G, DC, MODE>(a, sc, dep, mixed);
+}
+
+template <typename G, int DC, int MODE>
+__global__ void __launch_bounds__(kThreads) dopt_step_staged_kernel(const __grid_constant__ StepArgs a) {
+    static_assert(MODE == kPlain || MODE == kCounted, "the staged kernel has the plain and counted modes");
+    extern __shared__ __align__(128) unsigned char stage[];
+    __shared__ __align__(8) unsigned long long bar;
+    if constexpr (MODE == kCounted) {
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        const uint4 hot = *reinterpret_cast<const uint4 *>(&a.counter->hot);
+        staged_tile<G, DC, MODE>(a, a.sc, StepDep{__uint_as_float(hot.x), __uint_as_float(hot.y)},
+                                 int32_t(hot.z), stage, &bar);
+    } else {
+        staged_tile<G, DC, MODE>(a, a.sc, StepDep{a.sc.step_size, a.sc.bc2_sqrt}, 0, stage, &bar);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// The counter kernel of the counted steps: the step number and its two
+// bias-correction scalars on the device
+// ---------------------------------------------------------------------------
+//
+// The host entry points take beta^t from the C library's pow.  The device
+// reaches the same floats as follows.  beta^t by binary powering in double
+// (at most 2*63 multiplies: this GPU's double pipeline is slow, and a
+// general pow costs far more) is within (t - 1) * 2^-53, relative, of the
+// exact power (each product rounds once; a chain of multiplications that
+// makes x^t lets at most t - 1 of those roundings count), unless it
+// underflows.  A correct pow is within 0.52 units in the last place of the
+// exact power (the C library's documented bound).  So pow's double lies in
+// [p - B, p + B] with p the powering's result and B = p * (t + 2) * 2^-52
+// (plus 2^-1000 for underflow).  Both scalars are monotone in beta^t (every
+// IEEE operation on the way, 1 - x, lr / x, sqrt, the rounding to float, is
+// monotone), so when the two ends of that interval give the same float, it
+// is pow's float.  Two lanes evaluate the two ends of each scalar side by
+// side.  Only when they differ (a float rounding boundary inside the
+// interval: about 2^-20 of the steps where t is small enough for the power
+// to matter) does the pair compute beta^t again in double-double, whose
+// error is far below an ulp, and evaluate the scalar at the smallest and at
+// the largest double within 0.52 ulp of it; the counter records such steps
+// (exact_steps), and the ones where those two still differ
+// (undecided_steps, which then take the double nearest the double-double
+// value).
+
+// beta^t by binary powering in double.
+__device__ __forceinline__ double beta_pow_fast(double b, int64_t t) {
+    double r = 1.0;
+    double x = b;
+    while (t > 0) {
+        if (t & 1) r = __dmul_rn(r, x);
+        t >>= 1;
+        if (t > 0) x = __dmul_rn(x, x);
+    }
+    return r;
+}
+
+// A double-double number hi + lo with |lo| at most half an ulp of hi.
+struct DoubleDouble {
+    double hi, lo;
+};
+
+// Product of two double-double numbers: the leading product's rounding
+// error exactly (fused multiply-add), the cross terms rounded, renormalised
+// with a fast two-sum (|p| >= |e|).  Relative error about 2^-104 unless
+// something underflows.
+__device__ __forceinline__ DoubleDouble dd_mul(DoubleDouble a, DoubleDouble b) {
+    const double p = __dmul_rn(a.hi, b.hi);
+    double e = __fma_rn(a.hi, b.hi, -p);
+    e = __dadd_rn(e, __dadd_rn(__dmul_rn(a.hi, b.lo), __dmul_rn(a.lo, b.hi)));
+    const double s = __dadd_rn(p, e);
+    return DoubleDouble{s, __dsub_rn(e, __dsub_rn(s, p))};
+}
+
+__device__ __noinline__ DoubleDouble beta_pow_dd(double b, int64_t t) {
+    DoubleDouble r{1.0, 0.0};
+    DoubleDouble x{b, 0.0};
+    while (t > 0) {
+        if (t & 1) r = dd_mul(r, x);
+        t >>= 1;
+        if (t > 0) x = dd_mul(x, x);
+    }
+    return r;
+}
+
+// Scalar `which` (0: lr / (1 - p), 1: sqrt(1 - p)) for beta^t = p: the
+// operations of the host's evaluation, each an IEEE round-to-nearest.
+__device__ __forceinline__ float scalar_at(const dopt_adam_cfg &cfg, int which, double p) {
+    const double d = __dsub_rn(1.0, p);
+    return which == 0 ? __double2float_rn(__ddiv_rn(double(cfg.lr), d))
+                      : __double2float_rn(__dsqrt_rn(d));
+}
+
+struct CountedScalar {
+    float x;
+    bool exact;      // the double-double evaluation ran
+    bool undecided;  // and the candidates still gave two floats
+};
+
+// The exact evaluation of a lane pair (side 0: smallest candidate double,
+// side 1: largest): the doubles within 0.52 ulp of beta^t, found from its
+// double-double value (whose own error, at most (t + 2) * 2^-100 of it, is
+// added to the margin).
+__device__ __noinline__ CountedScalar counted_scalar_exact(const dopt_adam_cfg &cfg, double b,
+                                                           int64_t t, int which, int side,
+                                                           unsigned pair) {
+    const DoubleDouble q = beta_pow_dd(b, t);
+    // the larger of the two ulps around hi: a conservative margin at a
+    // binade edge
+    const double up = __dsub_rn(nextafter(q.hi, 2.0), q.hi);
+    const double down = __dsub_rn(q.hi, nextafter(q.hi, -1.0));
+    const double ulp = fmax(up, down);
+    const double err = __dadd_rn(__dmul_rn(__dmul_rn(fabs(q.hi), double(t) + 2.0), 0x1p-100),
+                                 0x1p-1074);
+    const double margin = __dadd_rn(__dmul_rn(0.52, ulp), err);
+    const double lo_off = __dsub_rn(q.lo, margin);  // candidates d: lo_off <= d - hi <= hi_off
+    const double hi_off = __dadd_rn(q.lo, margin);
+    double d = q.hi;
+    if (side == 0) {
+        for (int k = 0; k < 4; ++k) {
+            const double prev = nextafter(d, -1.0);
+            if (prev < 0.0 || __dsub_rn(prev, q.hi) < lo_off) break;
+            d = prev;
+        }
+    } else {
+        for (int k = 0; k < 4; ++k) {
+            const double next = nextafter(d, 2.0);
+            if (__dsub_rn(next, q.hi) > hi_off) break;
+            d = next;
+        }
+    }
+    CountedScalar s{scalar_at(cfg, which, d), true, false};
+    const float other = __shfl_xor_sync(pair, s.x, 1);
+    if (other != s.x) {
+        s.undecided = true;
+        s.x = scalar_at(cfg, which, q.hi);  // the double nearest the double-double value
+    }
+    return s;
+}
+
+// Lane l of the counter kernel's four: scalar l >> 1 (0: step size, 1:
+// bc2_sqrt) of step t, the pair l, l ^ 1 evaluating the two ends of pow's
+// interval.  Every lane of the four must call it with the same t.
+__device__ __forceinline__ CountedScalar counted_scalar(const dopt_adam_cfg &cfg, int64_t t,
+                                                        int lane) {
+    if (t < 1 || t > kMaxCountedStep) return CountedScalar{0.0f, false, false};
+    const int which = lane >> 1, side = lane & 1;
+    const double b = which == 0 ? double(cfg.beta1) : double(cfg.beta2);
+    const double p = beta_pow_fast(b, t);
+    const double B = __dadd_rn(__dmul_rn(__dmul_rn(p, double(t) + 2.0), 0x1p-52), 0x1p-1000);
+    const double end = side == 0 ? fmax(__dsub_rn(p, B), 0.0) : __dadd_rn(p, B);
+    const float x = scalar_at(cfg, which, end);
+    const float other = __shfl_xor_sync(0xfu, x, 1);
+    if (other == x) return CountedScalar{x, false, false};
+    return counted_scalar_exact(cfg, b, t, which, side, 0x3u << (lane & 2));
+}
+
+// First launch of the counted steps, one warp of four lanes: the step
+// number from the counter, its two scalars (see above), the counter
+// advanced, or the bad number reported.  It is launched as a programmatic
+// dependent of the previous kernel on the stream (the step kernel of the
+// step before, which lets it start once all its CTAs run): it evaluates the
+// scalars for the number it reads then, waits for the previous grid to
+// complete, reads the number again and evaluates once more only if it
+// changed, so the slow part overlaps the previous step's last wave.
 __global__ void dopt_count_step_kernel(CounterBlock *c, const dopt_adam_cfg cfg) {
     const int lane = threadIdx.x;
     const int64_t guess = __ldcg(&c->next_step);
-    float x = counted_scalar(cfg, guess, lane);
+    CountedScalar s = counted_scalar(cfg, guess, lane);
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the grids before: complete, visible
     const int64_t t = __ldcg(&c->next_step);
-    if (t != guess) x = counted_scalar(cfg, t, lane);
+    if (t != guess) s = counted_scalar(cfg, t, lane);
     const bool bad = t < 1 || t > kMaxCountedStep;
-    const float bc2_sqrt = __shfl_sync(0x3u, x, 1);
+    const float bc2_sqrt = __shfl_sync(0xfu, s.x, 2);
+    const unsigned exact = __ballot_sync(0xfu, s.exact);
+    const unsigned undecided = __ballot_sync(0xfu, s.undecided);
     if (lane != 0) return;
     if (bad) {
         c->status = DOPT_COUNTER_BAD_STEP;
         c->hot.status = DOPT_COUNTER_BAD_STEP;
         return;
     }
-    c->hot = CounterHot{x, bc2_sqrt, 0, 0};
+    c->hot = CounterHot{s.x, bc2_sqrt, 0, 0};
+    if (exact) c->exact_steps += 1;
+    if (undecided) c->undecided_steps += 1;
     c->status = 0;
     c->next_step = t + 1;
 }

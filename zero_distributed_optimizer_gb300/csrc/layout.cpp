@@ -30,7 +30,7 @@ namespace {
 
 // Greedy buckets and padding: params at consecutive offsets; the open
 // bucket closes once its unpadded count reaches bucket_elems; each bucket
-// is padded to a multiple of R * pad_unit (page 1, §2 and §5).
+// is padded to a multiple of R * pad_unit (distributed-optimizer page, §2 and §5).
 void place_params(dopt_layout &L, const int64_t *sizes, int32_t n) {
     const int64_t unit = int64_t(L.R) * L.cfg.pad_unit;
     L.param_start.resize(n);
@@ -239,13 +239,17 @@ int dopt_layout_pieces(const dopt_layout *L, dopt_piece *pieces) {
     return DOPT_OK;
 }
 
-int dopt_layout_param_ranges(const dopt_layout *L, dopt_range *params) {
+int dopt_layout_param_offsets(const dopt_layout *L, dopt_range *params) {
     clear_error();
     if (!L || (!params && !L->param_start.empty()))
-        return fail(DOPT_E_ARG, "dopt_layout_param_ranges: NULL argument");
+        return fail(DOPT_E_ARG, "dopt_layout_param_offsets: NULL argument");
     for (size_t p = 0; p < L->param_start.size(); ++p)
         params[p] = dopt_range{L->param_start[p], L->param_end[p]};
     return DOPT_OK;
+}
+
+int dopt_layout_param_ranges(const dopt_layout *L, dopt_range *params) {
+    return dopt_layout_param_offsets(L, params);
 }
 
 int dopt_layout_to_device(dopt_layout *L) {

@@ -201,6 +201,71 @@ AllReduceKernel allreduce_kernel_for(const dopt_layout *L, dopt_dtype grad_dtype
     }
 }
 
+// The staged kernels (DOPT_STEP_STAGE): one-instance layouts with D in
+// {1, 2, 4, 8, 16}, plain or counted, and their shared-memory size.
+template <typename G, int MODE>
+StepKernel pick_staged_kernel(int D, size_t *smem) {
+    switch (D) {
+        case 1: *smem = staged_smem_bytes<G, 1>(); return dopt_step_staged_kernel<G, 1, MODE>;
+        case 2: *smem = staged_smem_bytes<G, 2>(); return dopt_step_staged_kernel<G, 2, MODE>;
+        case 4: *smem = staged_smem_bytes<G, 4>(); return dopt_step_staged_kernel<G, 4, MODE>;
+        case 8: *smem = staged_smem_bytes<G, 8>(); return dopt_step_staged_kernel<G, 8, MODE>;
+        case 16: *smem = staged_smem_bytes<G, 16>(); return dopt_step_staged_kernel<G, 16, MODE>;
+        default: *smem = 0; return nullptr;
+    }
+}
+
+template <int MODE>
+StepKernel staged_kernel_for(const dopt_layout *L, dopt_dtype grad_dtype, size_t *smem) {
+    if (L->cfg.instances > 1) {
+        *smem = 0;
+        return nullptr;
+    }
+    switch (grad_dtype) {
+        case DOPT_BF16: return pick_staged_kernel<__nv_bfloat16, MODE>(L->cfg.D, smem);
+        case DOPT_FP16: return pick_staged_kernel<__half, MODE>(L->cfg.D, smem);
+        default: return pick_staged_kernel<float, MODE>(L->cfg.D, smem);
+    }
+}
+
+// The staged kernels take more than the default 48 KB of dynamic shared
+// memory; the limit is raised once per kernel and device.
+std::mutex g_smem_mutex;
+std::vector<std::pair<const void *, int>> g_smem_set;
+
+int allow_smem(const char *who, const void *k, size_t bytes, int device) {
+    std::lock_guard<std::mutex> lock(g_smem_mutex);
+    for (const auto &e : g_smem_set)
+        if (e.first == k && e.second == device) return DOPT_OK;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return dopt::fail(DOPT_E_CUDA, "%s: shared-memory limit: %s", who, cudaGetErrorString(e));
+    }
+    g_smem_set.emplace_back(k, device);
+    return DOPT_OK;
+}
+
+// Launch the step kernel of a launch (or, with DOPT_STEP_STAGE, its staged
+// form) over `tiles` tiles.
+template <int MODE>
+int launch_step_kernel(const char *who, const dopt_layout *L, dopt_dtype grad_dtype,
+                       uint32_t flags, const StepArgs &a, int64_t tiles, cudaStream_t stream) {
+    if constexpr (MODE == kPlain || MODE == kCounted) {
+        if (flags & DOPT_STEP_STAGE) {
+            size_t smem = 0;
+            StepKernel k = staged_kernel_for<MODE>(L, grad_dtype, &smem);
+            int rc = allow_smem(who, reinterpret_cast<const void *>(k), smem, L->device);
+            if (rc != DOPT_OK) return rc;
+            k<<<unsigned(tiles), kThreads, smem, stream>>>(a);
+            return DOPT_OK;
+        }
+    }
+    StepKernel k = step_kernel_for<MODE>(L, grad_dtype);
+    k<<<unsigned(tiles), kThreads, 0, stream>>>(a);
+    return DOPT_OK;
+}
+
 // SMs and resident CTAs per SM of a kernel on a device, asked once.
 struct GridInfo {
     const void *kernel;
@@ -279,6 +344,14 @@ int check_step_args(const char *who, const dopt_layout *L, const dopt_adam_cfg *
                            DOPT_STEP_PARAMS_FP16) |
                   extra_flags))
         return fail(DOPT_E_ARG, "%s: unknown flags 0x%x", who, flags);
+    if (flags & DOPT_STEP_STAGE) {
+        const int D = L->cfg.D;
+        if (L->cfg.instances > 1 || (D != 1 && D != 2 && D != 4 && D != 8 && D != 16))
+            return fail(DOPT_E_ARG, "%s: DOPT_STEP_STAGE needs one instance and D in {1, 2, 4, 8, 16}",
+                        who);
+        if (flags & DOPT_STEP_HOST_GRADS)
+            return fail(DOPT_E_ARG, "%s: DOPT_STEP_STAGE reads device grads only", who);
+    }
     if (!(cfg->lr >= 0.0f) || !std::isfinite(cfg->lr) || !(cfg->beta1 >= 0.0f && cfg->beta1 < 1.0f) ||
         !(cfg->beta2 >= 0.0f && cfg->beta2 < 1.0f) || !(cfg->eps >= 0.0f) || !std::isfinite(cfg->eps) ||
         !(cfg->weight_decay >= 0.0f) || !std::isfinite(cfg->weight_decay) ||
@@ -377,8 +450,8 @@ int launch_step(const char *who, const dopt_layout *L, const dopt_adam_cfg *cfg,
     int rc = prepare_step(who, L, cfg, step, first, count, grad_replicas, master, exp_avg,
                           exp_avg_sq, param_replicas, flags, main_grad_out, a, &tiles);
     if (rc != DOPT_OK || tiles == 0) return rc;
-    StepKernel k = step_kernel_for<MODE>(L, grad_dtype);
-    k<<<unsigned(tiles), kThreads, 0, stream>>>(a);
+    rc = launch_step_kernel<MODE>(who, L, grad_dtype, flags, a, tiles, stream);
+    if (rc != DOPT_OK) return rc;
     return launch_error(who, "step");
 }
 
@@ -435,7 +508,7 @@ int launch_counter(const char *who, CounterBlock *c, const dopt_adam_cfg *cfg,
                    cudaStream_t stream) {
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(1);
-    lc.blockDim = dim3(2);
+    lc.blockDim = dim3(4);
     lc.dynamicSmemBytes = 0;
     lc.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -503,6 +576,20 @@ extern "C" int dopt_device_checks(int reset, uint32_t *flags, int64_t *first_bad
 #endif
 }
 
+extern "C" int dopt_stage_timeouts(int reset, uint32_t *count) {
+    using dopt::fail;
+    if (!count) return fail(DOPT_E_ARG, "dopt_stage_timeouts: NULL output");
+    unsigned int c = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&c, g_stage_timeouts, sizeof c);
+    if (e == cudaSuccess && reset) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_stage_timeouts, &zero, sizeof zero);
+    }
+    if (e != cudaSuccess) return fail(DOPT_E_CUDA, "dopt_stage_timeouts: %s", cudaGetErrorString(e));
+    *count = c;
+    return DOPT_OK;
+}
+
 extern "C" int dopt_step(const dopt_layout *L, const dopt_adam_cfg *cfg, int64_t step,
                          const void *const *grad_replicas, dopt_dtype grad_dtype, float *master,
                          float *exp_avg, float *exp_avg_sq, void *const *param_replicas,
@@ -511,7 +598,7 @@ extern "C" int dopt_step(const dopt_layout *L, const dopt_adam_cfg *cfg, int64_t
     const char *who = "dopt_step";
     NvtxRange range(who);
     int rc = check_step_args(who, L, cfg, step, grad_replicas, grad_dtype, master, exp_avg,
-                             exp_avg_sq, param_replicas, flags, main_grad_out);
+                             exp_avg_sq, param_replicas, flags, main_grad_out, DOPT_STEP_STAGE);
     if (rc != DOPT_OK) return rc;
     return launch_step<kPlain>(who, L, cfg, step, 0, int32_t(L->buckets.size()), grad_replicas,
                                grad_dtype, master, exp_avg, exp_avg_sq, param_replicas, flags,
@@ -529,7 +616,7 @@ extern "C" int dopt_step_buckets(const dopt_layout *L, const dopt_adam_cfg *cfg,
     const char *who = "dopt_step_buckets";
     NvtxRange range(who);
     int rc = check_step_args(who, L, cfg, step, grad_replicas, grad_dtype, master, exp_avg,
-                             exp_avg_sq, param_replicas, flags, main_grad_out);
+                             exp_avg_sq, param_replicas, flags, main_grad_out, DOPT_STEP_STAGE);
     if (rc != DOPT_OK) return rc;
     const int32_t nb = int32_t(L->buckets.size());
     if (first_bucket < 0 || n_buckets < 0 || first_bucket > nb || n_buckets > nb - first_bucket)
@@ -550,7 +637,7 @@ extern "C" int dopt_step_counted(const dopt_layout *L, const dopt_adam_cfg *cfg,
     const char *who = "dopt_step_counted";
     NvtxRange range(who);
     int rc = check_step_args(who, L, cfg, 1, grad_replicas, grad_dtype, master, exp_avg,
-                             exp_avg_sq, param_replicas, flags, main_grad_out);
+                             exp_avg_sq, param_replicas, flags, main_grad_out, DOPT_STEP_STAGE);
     if (rc != DOPT_OK) return rc;
     rc = check_counter(who, counter);
     if (rc != DOPT_OK) return rc;
@@ -565,8 +652,8 @@ extern "C" int dopt_step_counted(const dopt_layout *L, const dopt_adam_cfg *cfg,
     rc = launch_counter(who, c, cfg, stream);
     if (rc != DOPT_OK || tiles == 0) return rc;
     a.counter = c;
-    StepKernel k = step_kernel_for<kCounted>(L, grad_dtype);
-    k<<<unsigned(tiles), kThreads, 0, stream>>>(a);
+    rc = launch_step_kernel<kCounted>(who, L, grad_dtype, flags, a, tiles, stream);
+    if (rc != DOPT_OK) return rc;
     return launch_error(who, "step");
 }
 

@@ -65,6 +65,9 @@ def main(argv=None):
     ap.add_argument("--param-dtype", choices=["bf16", "fp16"], default="bf16")
     ap.add_argument("--instances", type=int, default=1,
                     help="distributed-optimizer instances (D must divide by it)")
+    ap.add_argument("--stage", action="store_true",
+                    help="step, counted and buckets modes: read through shared memory with "
+                         "bulk copies (DOPT_STEP_STAGE)")
     args = ap.parse_args(argv)
 
     libbuild.build()
@@ -90,7 +93,7 @@ def main(argv=None):
         main_grad = torch.empty(N, device=dev)
         ws = B.clip_workspace(dev)
     streams = [torch.cuda.current_stream()] + [torch.cuda.Stream(dev) for _ in range(args.streams - 1)]
-    plan = B.StepPlan(L, adam, grads, master, m, v, params) if args.plan else None
+    plan = B.StepPlan(L, adam, grads, master, m, v, params, stage=args.stage) if args.plan else None
 
     def bucket_launches(t):
         # fork the side streams off the main one, launch, join them back
@@ -103,7 +106,8 @@ def main(argv=None):
             if plan is not None:
                 plan.step_buckets(t, k, 1, stream=s_)
             else:
-                B.dopt_step_buckets(L, adam, t, k, 1, grads, master, m, v, params, stream=s_)
+                B.dopt_step_buckets(L, adam, t, k, 1, grads, master, m, v, params, stream=s_,
+                                    stage=args.stage)
         for s_ in streams[1:]:
             join = torch.cuda.Event()
             join.record(s_)
@@ -145,11 +149,11 @@ def main(argv=None):
         elif args.mode == "clipped":
             B.dopt_step_clipped(L, adam, t, 1.0, grads, master, m, v, params, main_grad, ws)
         elif args.mode == "counted":
-            B.dopt_step_counted(L, adam, counter, grads, master, m, v, params)
+            B.dopt_step_counted(L, adam, counter, grads, master, m, v, params, stage=args.stage)
         elif plan is not None:
             plan.step(t)
         else:
-            B.dopt_step(L, adam, t, grads, master, m, v, params)
+            B.dopt_step(L, adam, t, grads, master, m, v, params, stage=args.stage)
     ev[1].record()
     torch.cuda.synchronize()
     ms = ev[0].elapsed_time(ev[1]) / max(args.launches, 1)
@@ -161,7 +165,7 @@ def main(argv=None):
     bytes_per = w.numel * per_elem
     print(json.dumps({"workload": w.name, "N": w.numel, "padded_numel": N, "D": w.D,
                       "mode": args.mode, "grad_dtype": w.grad_dtype, "param_dtype": args.param_dtype,
-                      "instances": args.instances,
+                      "instances": args.instances, "stage": args.stage,
                       "n_buckets": L.n_buckets, "streams": args.streams, "plan": args.plan,
                       "launches": args.launches, "ms_per_launch": ms,
                       "algorithmic_bytes_per_launch": bytes_per,
