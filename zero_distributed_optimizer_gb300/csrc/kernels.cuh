@@ -672,18 +672,10 @@ __device__ __forceinline__ void update_and_store(const StepArgs &a, const Scalar
 template <typename G, int DC, int MODE, int GR>
 __device__ __forceinline__ void full_vector(const StepArgs &a, const Scalars &sc, StepDep dep, int64_t e0,
                                             int32_t meta, int32_t status = 0) {
+    static_assert(MODE != kFromMain, "the clipped step's vectors are done in step_vector");
     float acc[8];
-    if constexpr (MODE == kFromMain) {
-        const float coef = *a.clip_coef;
-        if (a.skip_nonfinite && isnan(coef)) return;  // the step is skipped
-        const float4 g0 = ld_stream_f4(a.main_grad_in + e0), g1 = ld_stream_f4(a.main_grad_in + e0 + 4);
-        const float f[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-#pragma unroll
-        for (int k = 0; k < 8; ++k) acc[k] = __fmul_rn(f[k], coef);
-    } else {
-        reduce_vec<G, DC, GR>(a, sc.scale, e0, acc);
-        if (a.round_grad) to_grad_type8<G>(acc);
-    }
+    reduce_vec<G, DC, GR>(a, sc.scale, e0, acc);
+    if (a.round_grad) to_grad_type8<G>(acc);
     if constexpr (MODE == kWriteGrads) write_grads_vec<G, DC>(a.grads, a.D, e0, acc);
     const float4 w0 = ld_stream_f4(a.master + e0), w1 = ld_stream_f4(a.master + e0 + 4);
     const float4 m0 = ld_stream_f4(a.exp_avg + e0), m1 = ld_stream_f4(a.exp_avg + e0 + 4);
@@ -731,12 +723,12 @@ __device__ __forceinline__ void full_vector_preloaded(const StepArgs &a, const S
 // element over the warp's lanes (for_straddling_elements).
 template <typename G, int DC, int MODE>
 __device__ __noinline__ void mixed_elements(const StepArgs &a, const Scalars &sc, StepDep dep,
-                                            unsigned mixed) {
+                                            unsigned mixed, int64_t tile) {
     if constexpr (MODE == kFromMain) {
         if (a.skip_nonfinite && isnan(*a.clip_coef)) return;  // the step is skipped
     }
     const int D = DC > 0 ? DC : a.D;
-    for_straddling_elements(a.rv, a.rv.tile0 + blockIdx.x, mixed, [&](int64_t e, int32_t meta) {
+    for_straddling_elements(a.rv, tile, mixed, [&](int64_t e, int32_t meta) {
         float g;
         if constexpr (MODE == kFromMain) {
             g = __fmul_rn(a.main_grad_in[e], *a.clip_coef);
@@ -785,6 +777,33 @@ __device__ __forceinline__ void step_vector(const StepArgs &a, const Scalars &sc
         kind = locate(a.rv, tile, e0, j);
         if (kind == kFull && vector_in_buffer(a.rv, e0))
             full_vector_preloaded<G, DC, MODE>(a, sc, dep, e0, a.rv.run_meta[j], status, p);
+    } else if constexpr (MODE == kFromMain) {
+        // The second launch of the clipped step starts (programmatic
+        // dependent launch) while the norm pass finishes: the run lookup and
+        // the master/m/v loads, which do not depend on that pass, go first;
+        // the main grads and the coefficient are read after the wait for
+        // the norm pass to complete.
+        kind = locate(a.rv, tile, e0, j);
+        const bool full = kind == kFull && vector_in_buffer(a.rv, e0);
+        float4 w0, w1, m0, m1, v0, v1;
+        if (full) {
+            w0 = ld_stream_f4(a.master + e0), w1 = ld_stream_f4(a.master + e0 + 4);
+            m0 = ld_stream_f4(a.exp_avg + e0), m1 = ld_stream_f4(a.exp_avg + e0 + 4);
+            v0 = ld_stream_f4(a.exp_avg_sq + e0), v1 = ld_stream_f4(a.exp_avg_sq + e0 + 4);
+        }
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        if (full) {
+            const float coef = *a.clip_coef;
+            if (!(a.skip_nonfinite && isnan(coef))) {  // else the step is skipped
+                const float4 g0 = ld_stream_f4(a.main_grad_in + e0);
+                const float4 g1 = ld_stream_f4(a.main_grad_in + e0 + 4);
+                float acc[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+                for (int k = 0; k < 8; ++k) acc[k] = __fmul_rn(acc[k], coef);
+                update_and_store<G, DC, MODE>(a, sc, dep, e0, a.rv.run_meta[j], status, acc, w0, w1,
+                                              m0, m1, v0, v1);
+            }
+        }
     } else {
         kind = locate(a.rv, tile, e0, j);
         if (kind == kFull && vector_in_buffer(a.rv, e0))
@@ -792,7 +811,7 @@ __device__ __forceinline__ void step_vector(const StepArgs &a, const Scalars &sc
     }
     // every lane of the warp is here (no lane returns before this point)
     const unsigned mixed = __ballot_sync(0xffffffffu, kind == kMixed);
-    if (mixed != 0 && status == 0) mixed_elements<G, DC, MODE>(a, sc, dep, mixed);
+    if (mixed != 0 && status == 0) mixed_elements<G, DC, MODE>(a, sc, dep, mixed, tile);
 }
 
 // GR: the replicas of one optimizer instance (GR = DC: one instance).
@@ -884,7 +903,7 @@ __device__ __forceinline__ void bulk_to_shared(uint32_t dst, const void *src, ui
 
 // Shared-memory bytes of one staged tile: DC grad chunks and master/m/v.
 template <typename G, int DC>
-constexpr size_t staged_smem_bytes() {
+__host__ __device__ constexpr size_t staged_smem_bytes() {
     return size_t(DC) * kDoptTileElems * sizeof(G) + 3 * kDoptTileElems * sizeof(float);
 }
 
@@ -964,7 +983,7 @@ __device__ __forceinline__ void staged_tile(const StepArgs &a, const Scalars &sc
                                       v0, v1);
     }
     const unsigned mixed = __ballot_sync(0xffffffffu, kind == kMixed);
-    if (mixed != 0 && status == 0) mixed_elements<G, DC, MODE>(a, sc, dep, mixed);
+    if (mixed != 0 && status == 0) mixed_elements<G, DC, MODE>(a, sc, dep, mixed, tile);
 }
 
 template <typename G, int DC, int MODE>
@@ -1205,6 +1224,9 @@ __device__ __forceinline__ double warp_sum(double v) {
 // norm and the clipping coefficient min(1, max_norm / (norm + 1e-6)).
 template <typename G, int DC>
 __global__ void __launch_bounds__(kThreads) dopt_rs_norm_kernel(const __grid_constant__ NormArgs a) {
+    // the step pass may be scheduled as soon as every CTA of this grid runs:
+    // it reads nothing of this pass before its griddepcontrol.wait
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int lane = threadIdx.x & 31;
     double local = 0.0;
     unsigned int bad = 0;  // non-finite reduced grads seen by this thread

@@ -246,6 +246,37 @@ int allow_smem(const char *who, const void *k, size_t bytes, int device) {
     return DOPT_OK;
 }
 
+// SMs and resident CTAs per SM of a kernel on a device, asked once.
+struct GridInfo {
+    const void *kernel;
+    int device;
+    int sms;
+    int per_sm;
+};
+std::mutex g_grid_mutex;
+std::vector<GridInfo> g_grid_info;
+
+// (A kernel is always launched with the same block size and dynamic shared
+// memory, so the kernel and the device are the key.)
+void sm_occupancy(const void *k, int device, int *sms, int *per_sm, int threads = kThreads,
+                  size_t smem = 0) {
+    std::lock_guard<std::mutex> lock(g_grid_mutex);
+    for (const GridInfo &g : g_grid_info)
+        if (g.kernel == k && g.device == device) {
+            *sms = g.sms;
+            *per_sm = g.per_sm;
+            return;
+        }
+    if (cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, k, threads, smem) != cudaSuccess) {
+        cudaGetLastError();
+        *sms = 1;
+        *per_sm = 1;
+        return;  // not cached: asked again next time
+    }
+    g_grid_info.push_back(GridInfo{k, device, *sms, *per_sm});
+}
+
 // Launch the step kernel of a launch (or, with DOPT_STEP_STAGE, its staged
 // form) over `tiles` tiles.
 template <int MODE>
@@ -266,33 +297,6 @@ int launch_step_kernel(const char *who, const dopt_layout *L, dopt_dtype grad_dt
     return DOPT_OK;
 }
 
-// SMs and resident CTAs per SM of a kernel on a device, asked once.
-struct GridInfo {
-    const void *kernel;
-    int device;
-    int sms;
-    int per_sm;
-};
-std::mutex g_grid_mutex;
-std::vector<GridInfo> g_grid_info;
-
-void sm_occupancy(const void *k, int device, int *sms, int *per_sm) {
-    std::lock_guard<std::mutex> lock(g_grid_mutex);
-    for (const GridInfo &g : g_grid_info)
-        if (g.kernel == k && g.device == device) {
-            *sms = g.sms;
-            *per_sm = g.per_sm;
-            return;
-        }
-    if (cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, k, kThreads, 0) != cudaSuccess) {
-        cudaGetLastError();
-        *sms = 1;
-        *per_sm = 1;
-        return;  // not cached: asked again next time
-    }
-    g_grid_info.push_back(GridInfo{k, device, *sms, *per_sm});
-}
 
 // Grid of the persistent norm pass: every SM full, at most kMaxClipCtas.
 int norm_grid(NormKernel k, int64_t n_tiles, int device) {
@@ -498,7 +502,24 @@ int launch_clipped(const char *who, const dopt_layout *L, const dopt_adam_cfg *c
     a.skip_nonfinite = na.skip_nonfinite;
     a.counter = counter;  // the counted clipped step: scalars and status from the counter
     StepKernel k = pick_step_kernel<float, kFromMain>(kernel_D(L));
-    k<<<unsigned(tiles), kThreads, 0, stream>>>(a);
+    // a programmatic dependent of the norm pass: its CTAs start as the norm
+    // pass's CTAs leave, load master/m/v and wait for the pass to complete
+    // before they read the main grads and the coefficient
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(unsigned(tiles));
+    lc.blockDim = dim3(kThreads);
+    lc.dynamicSmemBytes = 0;
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    cudaError_t le = cudaLaunchKernelEx(&lc, k, a);
+    if (le != cudaSuccess) {
+        cudaGetLastError();
+        return fail(DOPT_E_CUDA, "%s: step launch: %s", who, cudaGetErrorString(le));
+    }
     return launch_error(who, "step");
 }
 
