@@ -1290,12 +1290,21 @@ __global__ void __launch_bounds__(kThreads) dopt_rs_norm_kernel(const __grid_con
         last = atomicAdd(&a.ws->ticket, 1u) == gridDim.x - 1;
     }
     __syncthreads();
-    if (!last || threadIdx.x >= 32) return;
+    if (!last) return;
     __threadfence();
+    // The last CTA adds the partials: thread i those at i, i + 256, ...
+    // (independent loads, all in flight at once, where one warp walking the
+    // list made a chain of dependent L2 round trips at the end of the pass),
+    // then each warp's sum, then the 8 warps' sums in warp order: the same
+    // order at every call.
     double v = 0.0;
-    for (int i = lane; i < int(gridDim.x); i += 32) v += __ldcg(&a.ws->partial[i]);
+    for (int i = threadIdx.x; i < int(gridDim.x); i += kThreads) v += __ldcg(&a.ws->partial[i]);
     v = warp_sum(v);
-    if (lane == 0) {
+    if (lane == 0) warp_part[threadIdx.x >> 5] = v;  // thread 0 is done reading it
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        v = 0.0;
+        for (int w = 0; w < kThreads / 32; ++w) v += warp_part[w];
         const double norm = sqrt(v);
         double coef = double(a.max_norm) / (norm + 1e-6);
         if (coef > 1.0) coef = 1.0;
