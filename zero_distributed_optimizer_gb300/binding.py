@@ -10,7 +10,9 @@ Names follow the C entry points: ``dopt_build_range_map``, ``dopt_step``,
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
+import functools
 import os
 import threading
 from dataclasses import dataclass
@@ -144,6 +146,9 @@ def _declare(lib):
 def lib():
     """The loaded libdopt.so.  Raises if it has not been built."""
     global _lib
+    loaded = _lib
+    if loaded is not None:
+        return loaded
     with _lock:
         if _lib is None:
             if not os.path.exists(LIB_PATH):
@@ -190,8 +195,23 @@ class AdamConfig:
     grad_scale: float = 1.0
 
     def to_c(self) -> dopt_adam_cfg:
-        return dopt_adam_cfg(self.lr, self.beta1, self.beta2, self.eps, self.weight_decay,
-                             self.grad_scale)
+        """The C struct (one per distinct config, kept: the library only reads it)."""
+        return _adam_c(self)
+
+
+@functools.lru_cache(maxsize=256)
+def _adam_c(adam: AdamConfig) -> dopt_adam_cfg:
+    return dopt_adam_cfg(adam.lr, adam.beta1, adam.beta2, adam.eps, adam.weight_decay,
+                         adam.grad_scale)
+
+
+def _on(device):
+    """torch.cuda.device(device), or nothing when it is already current."""
+    import torch
+
+    if device.index == torch.cuda.current_device():
+        return contextlib.nullcontext()
+    return torch.cuda.device(device)
 
 
 class Layout:
@@ -302,6 +322,10 @@ def _stream_handle(stream):
 
 
 def _check_tensor(t, name, dtype, numel, device):
+    index = device.index if device.type == "cuda" else -1
+    if (index is not None and t.dtype is dtype and t.get_device() == index and t.is_contiguous()
+            and t.numel() >= numel):
+        return  # the common case, without building device objects
     if t.device != device:
         raise DoptError(DOPT_E_ARG, f"{name} is on {t.device}, expected {device}")
     if t.dtype != dtype:
@@ -388,7 +412,7 @@ def dopt_step_buckets(layout: Layout, adam: AdamConfig, step: int, first_bucket:
                                             param_replicas, main_grad_out, host_grads)
     flags = _flags(gather, host_grads, round_grad, stage) | pflag
     cfg = adam.to_c()
-    with torch.cuda.device(device):
+    with _on(device):
         _check(lib().dopt_step_buckets(
             layout.handle, ctypes.byref(cfg), int(step), int(first_bucket), int(n_buckets), gp,
             dt, master.data_ptr(), exp_avg.data_ptr(), exp_avg_sq.data_ptr(), pp, flags, mg,
@@ -404,7 +428,7 @@ def dopt_step_allreduce(layout: Layout, adam: AdamConfig, step: int, grad_replic
     device, gp, pp, dt, mg, pflag = _step_pointers(layout, grad_replicas, master, exp_avg, exp_avg_sq,
                                             param_replicas, main_grad_out)
     cfg = adam.to_c()
-    with torch.cuda.device(device):
+    with _on(device):
         _check(lib().dopt_step_allreduce(
             layout.handle, ctypes.byref(cfg), int(step), gp, dt, master.data_ptr(),
             exp_avg.data_ptr(), exp_avg_sq.data_ptr(), pp,
@@ -428,7 +452,7 @@ def dopt_allreduce(layout: Layout, grad_replicas, grad_scale: float, stream=None
     for i, g in enumerate(grad_replicas):
         _check_tensor(g, f"grad_replicas[{i}]", gdt, layout.padded_numel, device)
     gp = (ctypes.c_void_p * D)(*[g.data_ptr() for g in grad_replicas])
-    with torch.cuda.device(device):
+    with _on(device):
         _check(lib().dopt_allreduce(layout.handle, gp, dt, float(grad_scale),
                                     _stream_handle(stream)))
 
@@ -452,7 +476,7 @@ def dopt_step(layout: Layout, adam: AdamConfig, step: int, grad_replicas, master
                                             param_replicas, main_grad_out, host_grads)
     flags = _flags(gather, host_grads, round_grad, stage) | pflag
     cfg = adam.to_c()
-    with torch.cuda.device(device):
+    with _on(device):
         _check(lib().dopt_step(layout.handle, ctypes.byref(cfg), int(step), gp, dt,
                                master.data_ptr(), exp_avg.data_ptr(), exp_avg_sq.data_ptr(), pp,
                                flags, mg, _stream_handle(stream)))
@@ -520,7 +544,7 @@ def dopt_step_counted(layout: Layout, adam: AdamConfig, counter, grad_replicas, 
     _check_counter(counter, master.device)
     flags = _flags(gather, host_grads, round_grad, stage) | pflag
     cfg = adam.to_c()
-    with torch.cuda.device(device):
+    with _on(device):
         _check(lib().dopt_step_counted(layout.handle, ctypes.byref(cfg), counter.data_ptr(), gp,
                                        dt, master.data_ptr(), exp_avg.data_ptr(),
                                        exp_avg_sq.data_ptr(), pp, flags, mg,
@@ -685,7 +709,7 @@ def dopt_step_clipped(layout: Layout, adam: AdamConfig, step: int, max_norm: flo
     gp = (ctypes.c_void_p * D)(*[g.data_ptr() for g in grad_replicas])
     pp = (ctypes.c_void_p * D)(*[p.data_ptr() for p in param_replicas])
     cfg = adam.to_c()
-    with torch.cuda.device(device):
+    with _on(device):
         _check(lib().dopt_step_clipped(
             layout.handle, ctypes.byref(cfg), int(step), float(max_norm), gp,
             dt, master.data_ptr(),
@@ -716,7 +740,7 @@ def dopt_step_clipped_counted(layout: Layout, adam: AdamConfig, counter, max_nor
     flags = (_flags(gather, round_grad=round_grad) | pflag
              | (DOPT_STEP_SKIP_NONFINITE if skip_nonfinite else 0))
     cfg = adam.to_c()
-    with torch.cuda.device(device):
+    with _on(device):
         _check(lib().dopt_step_clipped_counted(
             layout.handle, ctypes.byref(cfg), counter.data_ptr(), float(max_norm), gp, dt,
             master.data_ptr(), exp_avg.data_ptr(), exp_avg_sq.data_ptr(), pp, flags, mg,
@@ -754,7 +778,7 @@ def dopt_step_clipped_noalloc(layout: Layout, adam: AdamConfig, step: int, max_n
     gp = (ctypes.c_void_p * D)(*[g.data_ptr() for g in grad_replicas])
     pp = (ctypes.c_void_p * D)(*[p.data_ptr() for p in param_replicas])
     cfg = adam.to_c()
-    with torch.cuda.device(device):
+    with _on(device):
         _check(lib().dopt_step_clipped_noalloc(
             layout.handle, ctypes.byref(cfg), int(step), float(max_norm), gp,
             dt, master.data_ptr(),
@@ -776,7 +800,7 @@ def dopt_gather(layout: Layout, param_replicas, stream=None) -> None:
         raise DoptError(DOPT_E_ARG, "dopt_gather needs CUDA tensors")
     _param_flag(param_replicas, layout.padded_numel, device)  # bf16 or fp16: 16-bit copies
     pp = (ctypes.c_void_p * D)(*[p.data_ptr() for p in param_replicas])
-    with torch.cuda.device(device):
+    with _on(device):
         _check(lib().dopt_gather(layout.handle, pp, _stream_handle(stream)))
 
 
