@@ -489,9 +489,11 @@ def run_ours(args):
                 stepper.step(t, host_grads)
             else:
                 B.step_from_host(L, adam, t, host_grads, dev_stage, master, m, v, params,
-                                 host_out, stream=stream, zero_copy=(name == "zero_copy"))
+                                 host_out, stream=stream,
+                                 zero_copy=name in ("zero_copy", "in_place_out"),
+                                 params_out_in_place=name == "in_place_out")
 
-        for name in ("staged", "zero_copy", "pipelined"):
+        for name in ("staged", "zero_copy", "pipelined", "in_place_out"):
             for _ in range(2):
                 t += 1
                 one(name, t)
@@ -519,7 +521,11 @@ def run_ours(args):
                                      "pinned host grads in place, D2H of param replica 0",
                         "pipelined": "binding.HostStepper: zero-copy step, param replica 0 "
                                      "staged on the device and copied to the host on a side "
-                                     "stream while the next step runs"}[best],
+                                     "stream while the next step runs",
+                        "in_place_out": "binding.step_from_host(zero_copy, params_out_in_place): "
+                                        "dopt_step reads the pinned host grads in place and "
+                                        "writes param replica 0 straight into pinned host "
+                                        "memory (the other 7 replicas on the device)"}[best],
                "ms_per_step_by_variant": variants}
         del host_grads, host_out, dev_stage
 

@@ -23,6 +23,14 @@
  *     arguments on the host before anything is queued, report launch errors
  *     through cudaGetLastError, and never allocate or synchronise.  Faults
  *     inside a kernel surface at the caller's next synchronisation.
+ *   - The step, all-reduce and gather kernels (but the counted step's,
+ *     which follows its counter kernel) are launched as programmatic
+ *     dependents of the kernel before them on the stream: when that kernel
+ *     lets its dependents start early (as the library's own kernels do),
+ *     their CTAs may become resident during its last wave and look up their
+ *     runs, but they read no grad, state or param, and write nothing,
+ *     before it has completed.  Stream order is unchanged for everything
+ *     else (copies, events, kernels that do not let dependents start).
  *   - Buffer-indexed arrays hold one element per position of the padded
  *     buffer (padded_numel elements).  Padding positions belong to no param;
  *     the step neither reads nor writes them in any buffer.
@@ -165,6 +173,19 @@ typedef enum { DOPT_BF16 = 0, DOPT_FP32 = 1, DOPT_FP16 = 2 } dopt_dtype;
  * copies 16-bit values and is the same for both types.
  */
 #define DOPT_STEP_PARAMS_FP16 16u
+/*
+ * The param replicas may be pinned host buffers (cudaHostAlloc, or
+ * cudaHostRegister'ed, with a device mapping) that the write-back and
+ * all-gather store into in place over the host link, each replica either
+ * that or device memory: a caller that needs one replica of the updated
+ * params on the host gets it without a device copy and a separate transfer.
+ * Each pointer is resolved with cudaPointerGetAttributes; anything that is
+ * neither device memory nor registered host memory with a device mapping is
+ * refused with DOPT_E_ARG before any launch.  Accepted by every step entry
+ * point (the pages store params on the devices; this is an addition of the
+ * library for callers whose grads and params cross the host link).
+ */
+#define DOPT_STEP_HOST_PARAMS 64u
 /*
  * Read each tile's grads and master/m/v through shared memory: one thread
  * of every CTA issues 1-D bulk copies (the SM's copy engine, from this
@@ -552,8 +573,9 @@ int dopt_step_clipped_counted(const dopt_layout *layout, const dopt_adam_cfg *cf
  *
  * Sharing: every call on a device uses the same array, which keeps the last
  * call's contents.  Each call zeroes the 16-byte header that must start at
- * zero (the finishing ticket and the non-finite count: one 16-byte
- * cudaMemsetAsync on `stream`); the rest is overwritten before it is read.  Calls whose executions overlap on the GPU (other streams, other
+ * zero (the finishing ticket and the non-finite count, with a one-thread
+ * kernel launched on `stream` before the norm pass); the rest is
+ * overwritten before it is read.  Calls whose executions overlap on the GPU (other streams, other
  * layouts, other threads) race on the array: the caller must order them.
  *
  * Limit: the norm pass needs 64 bytes plus 8 bytes per CTA, at most 1024

@@ -291,11 +291,34 @@ def test_stage_flag_checks_before_cuda(lib):
     gp = (ctypes.c_void_p * 2)(0x10000, 0x20000)
     assert B.lib().dopt_step(L.handle, ctypes.byref(cfg), 1, gp, 0, *st, gp,
                              stage | B.DOPT_STEP_HOST_GRADS, None, None) == B.DOPT_E_ARG
+    assert B.lib().dopt_step(L.handle, ctypes.byref(cfg), 1, gp, 0, *st, gp,
+                             stage | B.DOPT_STEP_HOST_PARAMS, None, None) == B.DOPT_E_ARG
     # the other entry points do not take it
     assert B.lib().dopt_step_allreduce(L.handle, ctypes.byref(cfg), 1, gp, 0, *st, gp, stage,
                                        None, None) == B.DOPT_E_ARG
     assert B.lib().dopt_step_clipped(L.handle, ctypes.byref(cfg), 1, 1.0, gp, 0, *st, gp, stage,
                                      0x70000, 0x80000, None, None) == B.DOPT_E_ARG
+
+
+def test_host_params_flag_accepted_before_cuda(lib):
+    """DOPT_STEP_HOST_PARAMS passes the flag checks of every step entry point
+    (the pointers are resolved only once the device is needed)."""
+    L = _lib_layout([100, 30], 2, 0, 8)
+    cfg = B.AdamConfig().to_c()
+    gp = (ctypes.c_void_p * 2)(0x10000, 0x20000)
+    st = (0x30000, 0x40000, 0x50000)
+    f = B.DOPT_STEP_GATHER | B.DOPT_STEP_HOST_PARAMS
+    rcs = [B.lib().dopt_step(L.handle, ctypes.byref(cfg), 1, gp, 0, *st, gp, f, None, None),
+           B.lib().dopt_step_buckets(L.handle, ctypes.byref(cfg), 1, 0, 1, gp, 0, *st, gp, f,
+                                     None, None),
+           B.lib().dopt_step_allreduce(L.handle, ctypes.byref(cfg), 1, gp, 0, *st, gp, f, None,
+                                       None),
+           B.lib().dopt_step_counted(L.handle, ctypes.byref(cfg), 0x90000, gp, 0, *st, gp, f,
+                                     None, None),
+           B.lib().dopt_step_clipped(L.handle, ctypes.byref(cfg), 1, 1.0, gp, 0, *st, gp, f,
+                                     0x70000, 0x80000, None, None)]
+    for rc in rcs:
+        assert rc in (B.DOPT_E_STATE, B.DOPT_E_CUDA), rc
 
 
 def test_skip_nonfinite_only_on_the_clipped_step(lib):
@@ -331,7 +354,7 @@ def test_fp16_dtype_and_param_flag_accepted_before_cuda(lib):
                              None) == B.DOPT_E_ARG
     assert B.lib().dopt_allreduce(L.handle, gp, B.DOPT_FP16, 1.0, None) in (B.DOPT_E_STATE,
                                                                            B.DOPT_E_CUDA)
-    assert B.lib().dopt_step(L.handle, ctypes.byref(cfg), 1, gp, 0, *st, gp, 64, None,
+    assert B.lib().dopt_step(L.handle, ctypes.byref(cfg), 1, gp, 0, *st, gp, 128, None,
                              None) == B.DOPT_E_ARG
 
 
@@ -349,7 +372,7 @@ def test_clipped_counted_argument_checks_before_cuda(lib):
     assert call(counter=0x90004) == B.DOPT_E_ALIGN
     assert call(ws=None) == B.DOPT_E_ARG
     assert call(main=None) == B.DOPT_E_ARG
-    assert call(flags=64) == B.DOPT_E_ARG
+    assert call(flags=128) == B.DOPT_E_ARG
     assert call(flags=1 | B.DOPT_STEP_SKIP_NONFINITE) in (B.DOPT_E_STATE, B.DOPT_E_CUDA)
 
 

@@ -155,3 +155,71 @@ def test_host_stepper_results():
         torch.cuda.synchronize()
         assert torch.equal(outa.view(torch.int16), outb.view(torch.int16))
     _eq(a + pa, b + pb)
+
+
+@pytest.mark.parametrize("host_replicas", [(0,), (0, 1, 2, 3)])
+def test_step_writes_pinned_host_params(host_replicas):
+    """DOPT_STEP_HOST_PARAMS: param replicas in pinned host memory (replica
+    0 alone, or all of them) are written in place by the step, with host
+    grads too; every buffer equals the all-device step bit for bit."""
+    D = 4
+    L, N, master, m, v, params, grads = _setup([300000, 5, 70001], [1, 0, 1], D, 100000, 64,
+                                               "bf16", seed=11)
+    a = [master.to(DEV), m.to(DEV), v.to(DEV)]
+    b = [x.clone() for x in a]
+    pa = [p.to(DEV) for p in params]
+    pb = [p.clone().pin_memory() if r in host_replicas else p.to(DEV)
+          for r, p in enumerate(params)]
+    adam = B.AdamConfig(grad_scale=1.0 / D)
+    for i in range(2):
+        B.dopt_step(L, adam, i + 1, [g.to(DEV) for g in grads[i]], *a, pa)
+        host = [g.contiguous().pin_memory() for g in grads[i]]
+        B.dopt_step(L, adam, i + 1, host, *b, pb, host_grads=True, host_params=True)
+        torch.cuda.synchronize()
+    _eq(a + pa, b + [p.to(DEV) for p in pb])
+
+
+def test_step_from_host_params_out_in_place():
+    """The end-to-end form: host grads read in place and param replica 0
+    written straight into the pinned output; it equals the staged form's
+    copy of replica 0."""
+    D = 8
+    L, N, master, m, v, params, grads = _setup([300000, 5, 70001], [1, 0, 1], D, 100000, 64,
+                                               "bf16", seed=12)
+    a = [master.to(DEV), m.to(DEV), v.to(DEV)]
+    b = [x.clone() for x in a]
+    pa = [p.to(DEV) for p in params]
+    pb = [p.clone() for p in pa]
+    # the in-place output is replica 0 itself, so it starts as replica 0 did
+    # (the step never writes padding); the staged form copies the whole
+    # replica, padding included
+    out_a = torch.empty(N, dtype=torch.bfloat16).pin_memory()
+    out_b = params[0].clone().pin_memory()
+    adam = B.AdamConfig(grad_scale=1.0 / D)
+    stage = [torch.empty(N, dtype=torch.bfloat16, device=DEV) for _ in range(D)]
+    for i in range(2):
+        host = [g.contiguous().pin_memory() for g in grads[i]]
+        B.step_from_host(L, adam, i + 1, host, stage, *a, pa, out_a)
+        B.step_from_host(L, adam, i + 1, host, None, *b, pb, out_b, zero_copy=True,
+                         params_out_in_place=True)
+        torch.cuda.synchronize()
+    _eq(a + pa[1:] + [out_a], b + pb[1:] + [out_b])
+
+
+def test_host_params_refuses_pageable_memory():
+    D = 2
+    L, N, master, m, v, params, grads = _setup([1000, 24], None, D, 0, 8, "bf16", seed=13)
+    d = [master.to(DEV), m.to(DEV), v.to(DEV)]
+    g = [x.to(DEV) for x in grads[0]]
+    pageable = torch.zeros(N, dtype=torch.bfloat16)  # not pinned
+    pp = (ctypes.c_void_p * D)(pageable.data_ptr(), params[1].to(DEV).data_ptr())
+    gp = (ctypes.c_void_p * D)(*[x.data_ptr() for x in g])
+    cfg = B.AdamConfig().to_c()
+    import zero_distributed_optimizer_gb300.binding as bb
+
+    rc = bb.lib().dopt_step(L.handle, ctypes.byref(cfg), 1, gp, B.DOPT_BF16, d[0].data_ptr(),
+                            d[1].data_ptr(), d[2].data_ptr(), pp,
+                            B.DOPT_STEP_GATHER | B.DOPT_STEP_HOST_PARAMS, None,
+                            torch.cuda.current_stream().cuda_stream)
+    assert rc == B.DOPT_E_ARG and "param replica 0" in bb.lib().dopt_last_error().decode()
+    torch.cuda.synchronize()  # the context is still usable

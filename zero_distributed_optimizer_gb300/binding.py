@@ -42,6 +42,7 @@ DOPT_STEP_ROUND_GRAD = 4
 DOPT_STEP_SKIP_NONFINITE = 8
 DOPT_STEP_PARAMS_FP16 = 16
 DOPT_STEP_STAGE = 32
+DOPT_STEP_HOST_PARAMS = 64
 DOPT_CLIP_WORKSPACE_BYTES = 16384
 DOPT_STEP_COUNTER_BYTES = 64  # sizeof(dopt_step_counter)
 DOPT_COUNTER_BAD_STEP = 1
@@ -350,17 +351,24 @@ def _grad_code(gdt) -> int:
     return codes[gdt]
 
 
-def _param_flag(param_replicas, N, device) -> int:
-    """Check the param replicas (all bf16 or all fp16) and return the flag
-    for their type."""
+def _param_flag(param_replicas, N, device, host_params: bool = False) -> int:
+    """Check the param replicas (all bf16 or all fp16; with host_params each
+    on the step's device or a pinned CPU tensor) and return the flags for
+    them."""
     import torch
 
     pdt = param_replicas[0].dtype
     if pdt not in (torch.bfloat16, torch.float16):
         raise DoptError(DOPT_E_ARG, f"param dtype {pdt} is not bf16 or fp16")
     for i, p in enumerate(param_replicas):
-        _check_tensor(p, f"param_replicas[{i}]", pdt, N, device)
-    return DOPT_STEP_PARAMS_FP16 if pdt == torch.float16 else 0
+        if host_params and p.device.type == "cpu":
+            if not p.is_pinned():
+                raise DoptError(DOPT_E_ARG, f"param_replicas[{i}] must be on {device} or pinned")
+            _check_tensor(p, f"param_replicas[{i}]", pdt, N, p.device)
+        else:
+            _check_tensor(p, f"param_replicas[{i}]", pdt, N, device)
+    return ((DOPT_STEP_PARAMS_FP16 if pdt == torch.float16 else 0)
+            | (DOPT_STEP_HOST_PARAMS if host_params else 0))
 
 
 def _check_grads(grad_replicas, gdt, N, device, host_grads):
@@ -376,7 +384,7 @@ def _check_grads(grad_replicas, gdt, N, device, host_grads):
 
 
 def _step_pointers(layout: Layout, grad_replicas, master, exp_avg, exp_avg_sq, param_replicas,
-                   main_grad_out, host_grads=False):
+                   main_grad_out, host_grads=False, host_params=False):
     import torch
 
     D = layout.D
@@ -391,7 +399,7 @@ def _step_pointers(layout: Layout, grad_replicas, master, exp_avg, exp_avg_sq, p
     _check_grads(grad_replicas, gdt, N, device, host_grads)
     for name, t in (("master", master), ("exp_avg", exp_avg), ("exp_avg_sq", exp_avg_sq)):
         _check_tensor(t, name, torch.float32, N, device)
-    pflag = _param_flag(param_replicas, N, device)
+    pflag = _param_flag(param_replicas, N, device, host_params)
     if main_grad_out is not None:
         _check_tensor(main_grad_out, "main_grad_out", torch.float32, N, device)
     gp = (ctypes.c_void_p * D)(*[g.data_ptr() for g in grad_replicas])
@@ -460,7 +468,7 @@ def dopt_allreduce(layout: Layout, grad_replicas, grad_scale: float, stream=None
 def dopt_step(layout: Layout, adam: AdamConfig, step: int, grad_replicas, master, exp_avg,
               exp_avg_sq, param_replicas, gather: bool = True, main_grad_out=None,
               stream=None, host_grads: bool = False, round_grad: bool = False,
-              stage: bool = False) -> None:
+              stage: bool = False, host_params: bool = False) -> None:
     """One fused ZeRO-1 step (reduce-scatter, AdamW, write-back, all-gather).
 
     grad_replicas: D bf16 or fp32 CUDA tensors (or, with host_grads, pinned
@@ -468,12 +476,15 @@ def dopt_step(layout: Layout, adam: AdamConfig, step: int, grad_replicas, master
     param_replicas: D bf16; main_grad_out: optional fp32.  Each holds at
     least layout.padded_numel elements.  Asynchronous on `stream` (default:
     torch's current stream).  stage: read through shared memory with bulk
-    copies (DOPT_STEP_STAGE).
+    copies (DOPT_STEP_STAGE).  host_params: any param replica may be a
+    pinned CPU tensor, which the kernel writes in place
+    (DOPT_STEP_HOST_PARAMS).
     """
     import torch
 
     device, gp, pp, dt, mg, pflag = _step_pointers(layout, grad_replicas, master, exp_avg, exp_avg_sq,
-                                            param_replicas, main_grad_out, host_grads)
+                                            param_replicas, main_grad_out, host_grads,
+                                            host_params)
     flags = _flags(gather, host_grads, round_grad, stage) | pflag
     cfg = adam.to_c()
     with _on(device):
@@ -810,19 +821,30 @@ def version() -> str:
 
 def step_from_host(layout: Layout, adam: AdamConfig, step: int, host_grads, dev_grads, master,
                    exp_avg, exp_avg_sq, param_replicas, host_params_out=None, stream=None,
-                   zero_copy: bool = False) -> None:
+                   zero_copy: bool = False, params_out_in_place: bool = False) -> None:
     """The step for a caller whose grads sit in pinned host memory.
 
     Staged (default): copy the D host grad replicas into the device buffers
     `dev_grads`, then run dopt_step.  zero_copy: the kernel reads the pinned
     host replicas in place over the host link (DOPT_STEP_HOST_GRADS);
     `dev_grads` is not used.  Either way replica 0 of the updated params is
-    copied back into `host_params_out` (if given).  Everything is queued on
-    `stream`; the caller synchronises before reading `host_params_out`."""
+    copied back into `host_params_out` (if given).  params_out_in_place
+    (with zero_copy): `host_params_out` (pinned) is itself param replica 0,
+    which the kernel writes over the host link (DOPT_STEP_HOST_PARAMS);
+    `param_replicas[0]` on the device is then not written.  Everything is
+    queued on `stream`; the caller synchronises before reading
+    `host_params_out`."""
     import torch
 
     s = torch.cuda.current_stream() if stream is None else stream
     with torch.cuda.stream(s):
+        if zero_copy and params_out_in_place:
+            if host_params_out is None:
+                raise DoptError(DOPT_E_ARG, "params_out_in_place needs host_params_out")
+            dopt_step(layout, adam, step, host_grads, master, exp_avg, exp_avg_sq,
+                      [host_params_out] + list(param_replicas[1:]), gather=True, stream=s,
+                      host_grads=True, host_params=True)
+            return
         if zero_copy:
             dopt_step(layout, adam, step, host_grads, master, exp_avg, exp_avg_sq, param_replicas,
                       gather=True, stream=s, host_grads=True)

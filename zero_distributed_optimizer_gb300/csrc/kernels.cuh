@@ -758,19 +758,64 @@ __device__ __noinline__ void mixed_elements(const StepArgs &a, const Scalars &sc
 // would otherwise stop near 56-64, and the extra registers keep more loads in
 // flight per thread (D = 4: 2.5 % faster, D = 8 and 16: 0.2-0.4 %; forcing 6
 // or 8 CTAs per SM spilled and lost 15-40 %).
+// Where the two step-dependent scalars and the status come from: the
+// launch's own scalars in the constant bank (a copy of them in registers
+// cost the D = 2 step 4 %), or the counter of the counted steps, read with
+// one 16-byte load per warp either before anything else (the counted step,
+// launched after its counter kernel has completed) or after the wait (the
+// counted clipped step).  Nothing waits for the counter's load until the
+// Adam arithmetic, and the status is checked only before the first store.
+// (Reading the whole counter through shared memory behind a CTA barrier
+// cost 1.7 %; a persistent grid that reads it once per resident CTA cost
+// 15 %; the counted step reading it after its run lookup, as a programmatic
+// dependent of the counter kernel, cost 0.15 % on GPT-2 small and 1.2 µs a
+// step on the 1000-element layout.)
+enum ScalarSource : int { kFromArgs = 0, kFromCounterAfterWait = 1, kFromCounterEarly = 2 };
+
+template <int SRC>
+__device__ __forceinline__ void step_scalars(const StepArgs &a, const Scalars &sc, const uint4 &early,
+                                             StepDep &dep, int32_t &status) {
+    if constexpr (SRC == kFromArgs) {
+        dep = StepDep{sc.step_size, sc.bc2_sqrt};
+        status = 0;
+    } else {
+        const uint4 hot = SRC == kFromCounterEarly ? early
+                                                   : *reinterpret_cast<const uint4 *>(&a.counter->hot);
+        dep = StepDep{__uint_as_float(hot.x), __uint_as_float(hot.y)};
+        status = int32_t(hot.z);
+    }
+}
+
+// The wait for the launch before (see dopt_step_kernel), then the scalars;
+// the counted step is launched after its counter kernel has completed, does
+// not wait, and has its scalars from the start.
+template <int SRC>
+__device__ __forceinline__ void wait_then_scalars(const StepArgs &a, const Scalars &sc,
+                                                  const uint4 &early, StepDep &dep,
+                                                  int32_t &status) {
+    if constexpr (SRC != kFromCounterEarly) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        step_scalars<SRC>(a, sc, early, dep, status);
+    }
+}
+
 // One tile per CTA: this thread's vector of 8 elements.  `sc` is the
-// launch's own scalars (read from the constant bank); `dep` holds the two
-// step-dependent ones, which the counted step takes from its counter.
-template <typename G, int DC, int MODE, int GR>
-__device__ __forceinline__ void step_vector(const StepArgs &a, const Scalars &sc, StepDep dep,
-                                            int32_t status) {
+// launch's own scalars (read from the constant bank); the two
+// step-dependent ones come from step_scalars.
+template <typename G, int DC, int MODE, int GR, int SRC>
+__device__ __forceinline__ void step_vector(const StepArgs &a, const Scalars &sc, const uint4 &early) {
     const int64_t tile = a.rv.tile0 + blockIdx.x;
     const int64_t e0 = tile * kDoptTileElems + int64_t(threadIdx.x) * kVec;
     int j;
     VecKind kind;
+    StepDep dep;
+    int32_t status;
+    if constexpr (SRC == kFromCounterEarly) step_scalars<SRC>(a, sc, early, dep, status);
     if constexpr (kPreload<G, DC, MODE>) {
         // A whole vector of one run lies inside [lo, hi), so every vector
-        // that turns out whole has its loads in flight before the lookup.
+        // that turns out whole has its loads in flight before the lookup
+        // (after the wait for the kernel before: see dopt_step_kernel).
+        wait_then_scalars<SRC>(a, sc, early, dep, status);
         Preloaded<G, DC> p;
         const bool inside = e0 >= a.rv.lo && e0 + kVec <= a.rv.hi && vector_in_buffer(a.rv, e0);
         if (inside) p.load(a, e0);
@@ -791,7 +836,7 @@ __device__ __forceinline__ void step_vector(const StepArgs &a, const Scalars &sc
             m0 = ld_stream_f4(a.exp_avg + e0), m1 = ld_stream_f4(a.exp_avg + e0 + 4);
             v0 = ld_stream_f4(a.exp_avg_sq + e0), v1 = ld_stream_f4(a.exp_avg_sq + e0 + 4);
         }
-        asm volatile("griddepcontrol.wait;" ::: "memory");
+        wait_then_scalars<SRC>(a, sc, early, dep, status);
         if (full) {
             const float coef = *a.clip_coef;
             if (!(a.skip_nonfinite && isnan(coef))) {  // else the step is skipped
@@ -806,6 +851,9 @@ __device__ __forceinline__ void step_vector(const StepArgs &a, const Scalars &sc
         }
     } else {
         kind = locate(a.rv, tile, e0, j);
+        // the run lookup reads only the layout's tables; grads and state
+        // may still be written by the kernel before (see dopt_step_kernel)
+        wait_then_scalars<SRC>(a, sc, early, dep, status);
         if (kind == kFull && vector_in_buffer(a.rv, e0))
             full_vector<G, DC, MODE, GR>(a, sc, dep, e0, a.rv.run_meta[j], status);
     }
@@ -815,27 +863,30 @@ __device__ __forceinline__ void step_vector(const StepArgs &a, const Scalars &sc
 }
 
 // GR: the replicas of one optimizer instance (GR = DC: one instance).
+//
+// Every step kernel but the counted one (which follows its counter kernel
+// in plain stream order) is launched as a programmatic dependent of the
+// kernel before it on the stream, and every one lets its own dependent
+// start as soon as all of its CTAs run: the next launch's first CTAs take the SMs that this
+// grid's last wave leaves, look up their runs, and wait
+// (griddepcontrol.wait: the grid before has completed and its writes are
+// visible) before they read grads or state or store anything.  Where the
+// kernel before does not let its dependents start early, the wait returns
+// at once and nothing changes.
 template <typename G, int DC, int MODE, int GR = DC>
 __global__ void __launch_bounds__(kThreads, 3) dopt_step_kernel(const __grid_constant__ StepArgs a) {
-    bool counted = MODE == kCounted;
-    if constexpr (MODE == kFromMain) counted = a.counter != nullptr;  // the counted clipped step
-    if (counted) {
-        // let the next counted step's counter kernel start (it waits for this
-        // grid to complete before it writes the counter)
-        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-        // The two scalars that depend on the step number, and the status,
-        // in one 16-byte load per warp issued first; nothing waits for it
-        // before the data loads are out, and the status is checked only
-        // before the first store.  (Reading the whole counter through shared
-        // memory behind a CTA barrier cost 1.7 %; a persistent grid that
-        // reads it once per resident CTA cost 15 %.)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const uint4 none = make_uint4(0, 0, 0, 0);
+    if constexpr (MODE == kCounted) {
         const uint4 hot = *reinterpret_cast<const uint4 *>(&a.counter->hot);
-        step_vector<G, DC, MODE, GR>(a, a.sc, StepDep{__uint_as_float(hot.x), __uint_as_float(hot.y)},
-                                     int32_t(hot.z));
+        step_vector<G, DC, MODE, GR, kFromCounterEarly>(a, a.sc, hot);
+    } else if constexpr (MODE == kFromMain) {
+        if (a.counter != nullptr)  // the counted clipped step
+            step_vector<G, DC, MODE, GR, kFromCounterAfterWait>(a, a.sc, none);
+        else
+            step_vector<G, DC, MODE, GR, kFromArgs>(a, a.sc, none);
     } else {
-        // every scalar stays in the constant bank (a copy of them in
-        // registers cost the D = 2 step 4 %)
-        step_vector<G, DC, MODE, GR>(a, a.sc, StepDep{a.sc.step_size, a.sc.bc2_sqrt}, 0);
+        step_vector<G, DC, MODE, GR, kFromArgs>(a, a.sc, none);
     }
 }
 
@@ -1191,12 +1242,16 @@ __device__ __noinline__ void allreduce_mixed(const AllReduceArgs &a, unsigned mi
 // The same launch bounds as the step kernel: 0.6 % faster at D = 8 and
 // 0.3 % at D = 16.  (The gather kernel keeps the default: 3 CTAs per SM
 // helped at D = 8 by 0.5 % and cost 4 % at D = 4.)
+// Launched like the step kernels: a programmatic dependent of the kernel
+// before it, reading and writing grads only after griddepcontrol.wait.
 template <typename G, int DC, int GR = DC>
 __global__ void __launch_bounds__(kThreads, 3) dopt_allreduce_kernel(const __grid_constant__ AllReduceArgs a) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t tile = a.rv.tile0 + blockIdx.x;
     const int64_t e0 = tile * kDoptTileElems + int64_t(threadIdx.x) * kVec;
     int j;
     const VecKind kind = locate(a.rv, tile, e0, j);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (kind == kFull && vector_in_buffer(a.rv, e0)) {
         float acc[8];
         reduce_vec<G, DC, GR>(a, a.scale, e0, acc);
@@ -1209,6 +1264,17 @@ __global__ void __launch_bounds__(kThreads, 3) dopt_allreduce_kernel(const __gri
 // ---------------------------------------------------------------------------
 // Pass 1 of the clipped step
 // ---------------------------------------------------------------------------
+
+// The clipped step's first launch: zero the workspace's header (the ticket
+// and the non-finite count) for the norm pass, which starts alongside it
+// (a programmatic dependent) and waits for it only before it touches the
+// workspace.
+__global__ void dopt_clip_reset_kernel(ClipWorkspace *ws) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    ws->ticket = 0;
+    ws->pad0 = 0;
+    ws->nonfinite = 0;
+}
 
 // Deterministic sum over a warp (fixed shuffle tree); the result is in lane 0.
 __device__ __forceinline__ double warp_sum(double v) {
@@ -1270,6 +1336,10 @@ __global__ void __launch_bounds__(kThreads) dopt_rs_norm_kernel(const __grid_con
     __shared__ double warp_part[kThreads / 32];
     __shared__ unsigned int warp_bad[kThreads / 32];
     __shared__ bool last;
+    // this pass is a programmatic dependent of the kernel that zeroes the
+    // workspace's header: its grads and tables it may read at once, the
+    // workspace only after that kernel has completed
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     local = warp_sum(local);
     bad = __reduce_add_sync(0xffffffffu, bad);
     if (lane == 0) {
@@ -1346,11 +1416,16 @@ __device__ __noinline__ void gather_mixed(const GatherArgs &a, unsigned mixed) {
     });
 }
 
+// Launched like the step kernels: a programmatic dependent of the kernel
+// before it (the step that wrote the owners' replicas), touching params only
+// after griddepcontrol.wait.
 __global__ void __launch_bounds__(kThreads) dopt_gather_kernel(const __grid_constant__ GatherArgs a) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t tile = a.rv.tile0 + blockIdx.x;
     const int64_t e0 = tile * kDoptTileElems + int64_t(threadIdx.x) * kVec;
     int j;
     const VecKind kind = locate(a.rv, tile, e0, j);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (kind == kFull && vector_in_buffer(a.rv, e0)) {
         const int q = a.rv.run_meta[j] >> kRunRankShift;
         for (int base = 0; base < a.D; base += a.R) {

@@ -305,6 +305,6 @@ void dopt_layout_free(dopt_layout *L) {
 
 const char *dopt_last_error(void) { return g_last_error.c_str(); }
 
-const char *dopt_version(void) { return "dopt 0.1.0 (sm_103a)"; }
+const char *dopt_version(void) { return "dopt 0.2.0 (sm_103a)"; }
 
 }  // extern "C"

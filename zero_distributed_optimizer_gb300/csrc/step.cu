@@ -59,6 +59,25 @@ RunView whole_view(const dopt_layout *L, int64_t *tiles) {
 }
 
 using StepKernel = void (*)(StepArgs);
+
+// A launch that may start while the kernel before it on the stream is still
+// running (programmatic dependent launch): the kernel waits for that one
+// with griddepcontrol.wait before it touches what it wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t stream,
+                             Args... args) {
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = grid;
+    lc.blockDim = block;
+    lc.dynamicSmemBytes = 0;
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    return cudaLaunchKernelEx(&lc, kernel, args...);
+}
 using NormKernel = void (*)(NormArgs);
 using AllReduceKernel = void (*)(AllReduceArgs);
 
@@ -293,7 +312,18 @@ int launch_step_kernel(const char *who, const dopt_layout *L, dopt_dtype grad_dt
         }
     }
     StepKernel k = step_kernel_for<MODE>(L, grad_dtype);
-    k<<<unsigned(tiles), kThreads, 0, stream>>>(a);
+    if constexpr (MODE == kCounted) {
+        // after its counter kernel in plain stream order: it reads the
+        // counter first thing (a programmatic dependent launch that reads it
+        // after its run lookup was slower, see step_scalars)
+        k<<<unsigned(tiles), kThreads, 0, stream>>>(a);
+        return DOPT_OK;
+    }
+    cudaError_t e = launch_dependent(k, dim3(unsigned(tiles)), dim3(kThreads), stream, a);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return dopt::fail(DOPT_E_CUDA, "%s: step launch: %s", who, cudaGetErrorString(e));
+    }
     return DOPT_OK;
 }
 
@@ -345,7 +375,7 @@ int check_step_args(const char *who, const dopt_layout *L, const dopt_adam_cfg *
     if (grad_dtype != DOPT_BF16 && grad_dtype != DOPT_FP32 && grad_dtype != DOPT_FP16)
         return fail(DOPT_E_ARG, "%s: unknown grad dtype %d", who, int(grad_dtype));
     if (flags & ~(uint32_t(DOPT_STEP_GATHER | DOPT_STEP_HOST_GRADS | DOPT_STEP_ROUND_GRAD |
-                           DOPT_STEP_PARAMS_FP16) |
+                           DOPT_STEP_PARAMS_FP16 | DOPT_STEP_HOST_PARAMS) |
                   extra_flags))
         return fail(DOPT_E_ARG, "%s: unknown flags 0x%x", who, flags);
     if (flags & DOPT_STEP_STAGE) {
@@ -353,8 +383,8 @@ int check_step_args(const char *who, const dopt_layout *L, const dopt_adam_cfg *
         if (L->cfg.instances > 1 || (D != 1 && D != 2 && D != 4 && D != 8 && D != 16))
             return fail(DOPT_E_ARG, "%s: DOPT_STEP_STAGE needs one instance and D in {1, 2, 4, 8, 16}",
                         who);
-        if (flags & DOPT_STEP_HOST_GRADS)
-            return fail(DOPT_E_ARG, "%s: DOPT_STEP_STAGE reads device grads only", who);
+        if (flags & (DOPT_STEP_HOST_GRADS | DOPT_STEP_HOST_PARAMS))
+            return fail(DOPT_E_ARG, "%s: DOPT_STEP_STAGE takes device buffers only", who);
     }
     if (!(cfg->lr >= 0.0f) || !std::isfinite(cfg->lr) || !(cfg->beta1 >= 0.0f && cfg->beta1 < 1.0f) ||
         !(cfg->beta2 >= 0.0f && cfg->beta2 < 1.0f) || !(cfg->eps >= 0.0f) || !std::isfinite(cfg->eps) ||
@@ -399,6 +429,34 @@ int resolve_grads(const char *who, int D, const void *const *grad_replicas, uint
     return DOPT_OK;
 }
 
+// With DOPT_STEP_HOST_PARAMS each param replica may be a pinned host buffer
+// (replaced by the device's mapping of it) or device memory (kept);
+// anything else is refused.
+int resolve_params(const char *who, int D, void *const *param_replicas, uint32_t flags,
+                   void **out) {
+    using dopt::fail;
+    for (int r = 0; r < D; ++r) out[r] = param_replicas[r];
+    if (!(flags & DOPT_STEP_HOST_PARAMS)) return DOPT_OK;
+    for (int r = 0; r < D; ++r) {
+        cudaPointerAttributes at{};
+        cudaError_t e = cudaPointerGetAttributes(&at, param_replicas[r]);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(DOPT_E_ARG, "%s: param replica %d: cudaPointerGetAttributes: %s", who, r,
+                        cudaGetErrorString(e));
+        }
+        if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) continue;
+        if (at.type != cudaMemoryTypeHost || !at.devicePointer)
+            return fail(DOPT_E_ARG, "%s: param replica %d is neither device memory nor pinned "
+                        "host memory mapped to the device", who, r);
+        char *base = static_cast<char *>(at.devicePointer);
+        out[r] = base + (static_cast<char *>(param_replicas[r]) - static_cast<char *>(at.hostPointer));
+        if (!aligned16(out[r]))
+            return fail(DOPT_E_ALIGN, "%s: param replica %d mapping is not 16-byte aligned", who, r);
+    }
+    return DOPT_OK;
+}
+
 void fill_step_args(StepArgs &a, const dopt_layout *L, const dopt_adam_cfg *cfg, int64_t step,
                     const void *const *grad_replicas, float *master, float *exp_avg,
                     float *exp_avg_sq, void *const *param_replicas, uint32_t flags) {
@@ -437,7 +495,10 @@ int prepare_step(const char *who, const dopt_layout *L, const dopt_adam_cfg *cfg
     const void *grads[DOPT_MAX_D];
     rc = resolve_grads(who, L->cfg.D, grad_replicas, flags, grads);
     if (rc != DOPT_OK) return rc;
-    fill_step_args(a, L, cfg, step, grads, master, exp_avg, exp_avg_sq, param_replicas, flags);
+    void *params[DOPT_MAX_D];
+    rc = resolve_params(who, L->cfg.D, param_replicas, flags, params);
+    if (rc != DOPT_OK) return rc;
+    fill_step_args(a, L, cfg, step, grads, master, exp_avg, exp_avg_sq, params, flags);
     a.main_grad_out = main_grad_out;
     return DOPT_OK;
 }
@@ -473,6 +534,9 @@ int launch_clipped(const char *who, const dopt_layout *L, const dopt_adam_cfg *c
     const void *grads[DOPT_MAX_D];
     int rc = resolve_grads(who, D, grad_replicas, flags, grads);
     if (rc != DOPT_OK) return rc;
+    void *params[DOPT_MAX_D];
+    rc = resolve_params(who, D, param_replicas, flags, params);
+    if (rc != DOPT_OK) return rc;
     for (int r = 0; r < D; ++r) na.grads[r] = grads[r];
     na.main_grad = main_grad;
     na.ws = ws;
@@ -487,16 +551,21 @@ int launch_clipped(const char *who, const dopt_layout *L, const dopt_adam_cfg *c
     na.counter = const_cast<CounterBlock *>(counter);
     NormKernel nk = norm_kernel_for(L, grad_dtype);
     const int grid_a = norm_grid(nk, na.n_tiles, L->device);
-    cudaError_t e = cudaMemsetAsync(ws, 0, kClipResetBytes, stream);
-    if (e != cudaSuccess) return fail(DOPT_E_CUDA, "%s: workspace reset: %s", who, cudaGetErrorString(e));
-    nk<<<grid_a, kThreads, 0, stream>>>(na);
+    dopt_clip_reset_kernel<<<1, 1, 0, stream>>>(ws);
+    rc = launch_error(who, "workspace reset");
+    if (rc != DOPT_OK) return rc;
+    cudaError_t e = launch_dependent(nk, dim3(unsigned(grid_a)), dim3(kThreads), stream, na);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(DOPT_E_CUDA, "%s: norm launch: %s", who, cudaGetErrorString(e));
+    }
     rc = launch_error(who, "norm");
     if (rc != DOPT_OK) return rc;
 
     StepArgs a{};
     int64_t tiles = 0;
     a.rv = whole_view(L, &tiles);
-    fill_step_args(a, L, cfg, step, grads, master, exp_avg, exp_avg_sq, param_replicas, flags);
+    fill_step_args(a, L, cfg, step, grads, master, exp_avg, exp_avg_sq, params, flags);
     a.main_grad_in = main_grad;
     a.clip_coef = &ws->coef;
     a.skip_nonfinite = na.skip_nonfinite;
@@ -505,17 +574,7 @@ int launch_clipped(const char *who, const dopt_layout *L, const dopt_adam_cfg *c
     // a programmatic dependent of the norm pass: its CTAs start as the norm
     // pass's CTAs leave, load master/m/v and wait for the pass to complete
     // before they read the main grads and the coefficient
-    cudaLaunchConfig_t lc = {};
-    lc.gridDim = dim3(unsigned(tiles));
-    lc.blockDim = dim3(kThreads);
-    lc.dynamicSmemBytes = 0;
-    lc.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    lc.attrs = attr;
-    lc.numAttrs = 1;
-    cudaError_t le = cudaLaunchKernelEx(&lc, k, a);
+    cudaError_t le = launch_dependent(k, dim3(unsigned(tiles)), dim3(kThreads), stream, a);
     if (le != cudaSuccess) {
         cudaGetLastError();
         return fail(DOPT_E_CUDA, "%s: step launch: %s", who, cudaGetErrorString(le));
@@ -719,7 +778,11 @@ extern "C" int dopt_allreduce(const dopt_layout *L, void *const *grad_replicas,
     a.R = L->R;
     a.scale = grad_scale;
     AllReduceKernel k = allreduce_kernel_for(L, grad_dtype);
-    k<<<unsigned(tiles), kThreads, 0, stream>>>(a);
+    cudaError_t e = launch_dependent(k, dim3(unsigned(tiles)), dim3(kThreads), stream, a);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(DOPT_E_CUDA, "%s: all-reduce launch: %s", who, cudaGetErrorString(e));
+    }
     return launch_error(who, "all-reduce");
 }
 
@@ -776,6 +839,9 @@ extern "C" int dopt_step_clipped_counted(const dopt_layout *L, const dopt_adam_c
         if (rc != DOPT_OK) return rc;
         const void *grads[DOPT_MAX_D];
         rc = resolve_grads(who, L->cfg.D, grad_replicas, flags, grads);
+        if (rc != DOPT_OK) return rc;
+        void *params[DOPT_MAX_D];
+        rc = resolve_params(who, L->cfg.D, param_replicas, flags, params);
         if (rc != DOPT_OK) return rc;
     }
     // every check before the first launch: the counter advances only
@@ -874,6 +940,11 @@ extern "C" int dopt_gather(const dopt_layout *L, void *const *param_replicas, cu
     for (int r = 0; r < D; ++r) a.params[r] = param_replicas[r];
     a.D = D;
     a.R = L->R;
-    dopt_gather_kernel<<<unsigned(tiles), kThreads, 0, stream>>>(a);
+    cudaError_t e = launch_dependent(dopt_gather_kernel, dim3(unsigned(tiles)), dim3(kThreads),
+                                     stream, a);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(DOPT_E_CUDA, "%s: gather launch: %s", who, cudaGetErrorString(e));
+    }
     return launch_error(who, "gather");
 }
