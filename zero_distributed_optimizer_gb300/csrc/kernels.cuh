@@ -762,8 +762,8 @@ __device__ __noinline__ void mixed_elements(const StepArgs &a, const Scalars &sc
 // launch's own scalars in the constant bank (a copy of them in registers
 // cost the D = 2 step 4 %), or the counter of the counted steps, read with
 // one 16-byte load per warp either before anything else (the counted step,
-// launched after its counter kernel has completed) or after the wait (the
-// counted clipped step).  Nothing waits for the counter's load until the
+// right after its wait for the counter kernel) or after the wait that
+// follows the run lookup (the counted clipped step).  Nothing waits for the counter's load until the
 // Adam arithmetic, and the status is checked only before the first store.
 // (Reading the whole counter through shared memory behind a CTA barrier
 // cost 1.7 %; a persistent grid that reads it once per resident CTA cost
@@ -787,8 +787,7 @@ __device__ __forceinline__ void step_scalars(const StepArgs &a, const Scalars &s
 }
 
 // The wait for the launch before (see dopt_step_kernel), then the scalars;
-// the counted step is launched after its counter kernel has completed, does
-// not wait, and has its scalars from the start.
+// the counted step has waited and read its scalars at its start.
 template <int SRC>
 __device__ __forceinline__ void wait_then_scalars(const StepArgs &a, const Scalars &sc,
                                                   const uint4 &early, StepDep &dep,
@@ -864,20 +863,24 @@ __device__ __forceinline__ void step_vector(const StepArgs &a, const Scalars &sc
 
 // GR: the replicas of one optimizer instance (GR = DC: one instance).
 //
-// Every step kernel but the counted one (which follows its counter kernel
-// in plain stream order) is launched as a programmatic dependent of the
-// kernel before it on the stream, and every one lets its own dependent
-// start as soon as all of its CTAs run: the next launch's first CTAs take the SMs that this
+// Every step kernel is launched as a programmatic dependent of the kernel
+// before it on the stream, and lets its own dependent start as soon as all
+// of its CTAs run: the next launch's first CTAs take the SMs that this
 // grid's last wave leaves, look up their runs, and wait
 // (griddepcontrol.wait: the grid before has completed and its writes are
-// visible) before they read grads or state or store anything.  Where the
-// kernel before does not let its dependents start early, the wait returns
-// at once and nothing changes.
+// visible) before they read grads or state or store anything.  The counted
+// step waits at its very start, before its run lookup: its counter kernel
+// lets it start only once the step before has completed, and reading the
+// counter after the lookup was slower.  Where the kernel before does not
+// let its dependents start early, the wait returns at once and nothing
+// changes.
 template <typename G, int DC, int MODE, int GR = DC>
 __global__ void __launch_bounds__(kThreads, 3) dopt_step_kernel(const __grid_constant__ StepArgs a) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const uint4 none = make_uint4(0, 0, 0, 0);
     if constexpr (MODE == kCounted) {
+        // the counter kernel before it wrote the counter: wait for it first
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         const uint4 hot = *reinterpret_cast<const uint4 *>(&a.counter->hot);
         step_vector<G, DC, MODE, GR, kFromCounterEarly>(a, a.sc, hot);
     } else if constexpr (MODE == kFromMain) {
@@ -1204,6 +1207,9 @@ __global__ void dopt_count_step_kernel(CounterBlock *c, const dopt_adam_cfg cfg)
     const int64_t guess = __ldcg(&c->next_step);
     CountedScalar s = counted_scalar(cfg, guess, lane);
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the grids before: complete, visible
+    // the step kernel after it may now take the SMs (it waits for this grid
+    // before it reads the counter)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t t = __ldcg(&c->next_step);
     if (t != guess) s = counted_scalar(cfg, t, lane);
     const bool bad = t < 1 || t > kMaxCountedStep;

@@ -312,13 +312,6 @@ int launch_step_kernel(const char *who, const dopt_layout *L, dopt_dtype grad_dt
         }
     }
     StepKernel k = step_kernel_for<MODE>(L, grad_dtype);
-    if constexpr (MODE == kCounted) {
-        // after its counter kernel in plain stream order: it reads the
-        // counter first thing (a programmatic dependent launch that reads it
-        // after its run lookup was slower, see step_scalars)
-        k<<<unsigned(tiles), kThreads, 0, stream>>>(a);
-        return DOPT_OK;
-    }
     cudaError_t e = launch_dependent(k, dim3(unsigned(tiles)), dim3(kThreads), stream, a);
     if (e != cudaSuccess) {
         cudaGetLastError();
