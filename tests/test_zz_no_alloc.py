@@ -8,7 +8,7 @@ library instead of a caller workspace.  This file checks, through the C ABI,
 that two calls in a row give the same results as the workspace entry point
 within the parity tolerance, including the second call, which finds the
 first call's contents still in the shared scratch, and that this second
-call takes no device memory (the device's free memory, as the driver
+call takes no device memory (the device's free memory, as cudaMemGetInfo
 reports it, and the count of torch's allocations stay as they were).  It is
 collected last and also passes alone in a fresh process."""
 import pytest
@@ -50,7 +50,7 @@ def test_noalloc_matches_workspace_entry_point(grad_dtype, D):
         B.dopt_step_clipped_noalloc(L, adam, i + 1, max_norm, g, *b, pb, mgb, norm_out=nb)
         torch.cuda.synchronize()
         if i == 1:
-            # no device memory taken by the call: not from the driver (free
+            # no device memory taken by the call: not from CUDA (free
             # memory of the device unchanged), not from torch's allocator
             assert torch.cuda.mem_get_info()[0] == free_before
             assert torch.cuda.memory_stats().get("allocation.all.allocated", 0) == allocs_before
