@@ -619,6 +619,22 @@ int dopt_device_checks(int reset, uint32_t *flags, int64_t *first_bad);
  * counterpart.  Synchronous.  Errors: DOPT_E_ARG (NULL count), DOPT_E_CUDA. */
 int dopt_stage_timeouts(int reset, uint32_t *count);
 
+/*
+ * The HBM bandwidth of a mix of streams, for measurement: one launch over
+ * n_vectors 16-byte vectors, one per thread, that reads vector i of each of
+ * the `reads` read buffers and writes the XOR of them with a seed made of i
+ * to vector i of each of the `writes` write buffers, with the streaming
+ * 128-bit loads and stores of the step kernels.  Timing it (the caller's
+ * CUDA events) gives the ceiling of a read/write mix, e.g. the step's 2D + 3
+ * read and D + 3 write streams, against which the step kernels are
+ * measured.  Buffers: device, 16-byte aligned, n_vectors * 16 bytes each,
+ * owned by the caller.  0 <= reads, writes <= 16, not both 0.  Library
+ * infrastructure for measurement: the pages have no counterpart.
+ * Asynchronous on `stream`.  Errors: DOPT_E_ARG, DOPT_E_ALIGN, DOPT_E_CUDA.
+ */
+int dopt_stream_probe(int32_t reads, int32_t writes, const void *const *read_buffers,
+                      void *const *write_buffers, int64_t n_vectors, cudaStream_t stream);
+
 /* Text of the last error raised on the calling thread ("" if none).
  * Library infrastructure: the pages have no counterpart. */
 const char *dopt_last_error(void);

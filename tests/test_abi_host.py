@@ -410,3 +410,21 @@ def test_checked_build_compiles_and_exports_the_same_symbols():
     r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True,
                        env=dict(os.environ, DOPT_CHECKED="1"), timeout=300)
     assert f"CODE {B.DOPT_E_CUDA}" in r.stdout, r.stdout + r.stderr
+
+
+def test_stream_probe_argument_checks_before_cuda(lib):
+    """The measurement probe refuses stream counts outside 0..16, no streams
+    at all, NULL or misaligned buffers before anything reaches CUDA; zero
+    vectors is a no-op."""
+    vp = ctypes.c_void_p
+    good = (vp * 2)(0x10000, 0x20000)
+    probe = B.lib().dopt_stream_probe
+    assert probe(17, 1, good, good, 16, None) == B.DOPT_E_ARG
+    assert probe(0, 0, good, good, 16, None) == B.DOPT_E_ARG
+    assert probe(-1, 1, good, good, 16, None) == B.DOPT_E_ARG
+    assert probe(1, 1, None, good, 16, None) == B.DOPT_E_ARG
+    assert probe(2, 0, (vp * 2)(0x10000, 0), None, 16, None) == B.DOPT_E_ARG
+    assert probe(1, 1, (vp * 1)(0x10008), good, 16, None) == B.DOPT_E_ALIGN
+    assert probe(1, 1, good, (vp * 1)(0x20004), 16, None) == B.DOPT_E_ALIGN
+    assert probe(1, 1, good, good, -1, None) == B.DOPT_E_ARG
+    assert probe(2, 2, good, good, 0, None) == B.DOPT_OK

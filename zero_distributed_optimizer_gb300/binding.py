@@ -134,6 +134,9 @@ def _declare(lib):
     lib.dopt_allreduce.argtypes = [vp, P(vp), ctypes.c_int, ctypes.c_float, vp]
     lib.dopt_gather.restype = ctypes.c_int
     lib.dopt_gather.argtypes = [vp, P(vp), vp]
+    lib.dopt_stream_probe.restype = ctypes.c_int
+    lib.dopt_stream_probe.argtypes = [ctypes.c_int32, ctypes.c_int32, P(vp), P(vp), ctypes.c_int64,
+                                      vp]
     lib.dopt_stage_timeouts.restype = ctypes.c_int
     lib.dopt_stage_timeouts.argtypes = [ctypes.c_int, P(ctypes.c_uint32)]
     lib.dopt_device_checks.restype = ctypes.c_int
@@ -170,6 +173,29 @@ def device_checks(reset: bool = False):
     flags, first = ctypes.c_uint32(0), ctypes.c_int64(0)
     _check(lib().dopt_device_checks(1 if reset else 0, ctypes.byref(flags), ctypes.byref(first)))
     return flags.value, first.value
+
+
+def dopt_stream_probe(read_buffers, write_buffers, stream=None) -> None:
+    """One launch of the stream probe (dopt_stream_probe in dopt.h): vector i
+    of every read buffer in, their XOR with a seed of i to vector i of every
+    write buffer.  Buffers: CUDA tensors of one device, contiguous, the same
+    byte size (a multiple of 16).  Time it with CUDA events."""
+    import torch
+
+    bufs = list(read_buffers) + list(write_buffers)
+    if not bufs:
+        raise DoptError(DOPT_E_ARG, "no buffers")
+    nbytes = bufs[0].numel() * bufs[0].element_size()
+    for b in bufs:
+        if (b.device.type != "cuda" or b.device != bufs[0].device or not b.is_contiguous()
+                or b.numel() * b.element_size() != nbytes or nbytes % 16):
+            raise DoptError(DOPT_E_ARG, "probe buffers must be contiguous CUDA tensors of one "
+                            "device and one byte size, a multiple of 16")
+    rp = (ctypes.c_void_p * max(len(read_buffers), 1))(*[b.data_ptr() for b in read_buffers])
+    wp = (ctypes.c_void_p * max(len(write_buffers), 1))(*[b.data_ptr() for b in write_buffers])
+    with _on(bufs[0].device):
+        _check(lib().dopt_stream_probe(len(read_buffers), len(write_buffers), rp, wp, nbytes // 16,
+                                       _stream_handle(stream)))
 
 
 def stage_timeouts(reset: bool = False) -> int:

@@ -16,6 +16,7 @@
 #include "dopt_internal.h"
 
 #include "kernels.cuh"
+#include "probe.cuh"
 
 namespace {
 
@@ -647,6 +648,46 @@ extern "C" int dopt_device_checks(int reset, uint32_t *flags, int64_t *first_bad
     (void)reset;
     return fail(DOPT_E_STATE, "dopt_device_checks: this library was built without DOPT_DEVICE_CHECKS");
 #endif
+}
+
+extern "C" int dopt_stream_probe(int32_t reads, int32_t writes, const void *const *read_buffers,
+                                 void *const *write_buffers, int64_t n_vectors,
+                                 cudaStream_t stream) {
+    using dopt::fail;
+    dopt::clear_error();
+    const char *who = "dopt_stream_probe";
+    if (reads < 0 || writes < 0 || reads > kMaxProbeStreams || writes > kMaxProbeStreams ||
+        reads + writes == 0)
+        return fail(DOPT_E_ARG, "%s: %d read and %d write streams (0..%d each, not both 0)", who,
+                    reads, writes, kMaxProbeStreams);
+    if (n_vectors < 0 || n_vectors > (int64_t(1) << 40))
+        return fail(DOPT_E_ARG, "%s: n_vectors out of range", who);
+    if ((reads && !read_buffers) || (writes && !write_buffers))
+        return fail(DOPT_E_ARG, "%s: NULL buffer array", who);
+    ProbeArgs a{};
+    for (int r = 0; r < reads; ++r) {
+        if (!read_buffers[r]) return fail(DOPT_E_ARG, "%s: read buffer %d is NULL", who, r);
+        if (!aligned16(read_buffers[r])) return fail(DOPT_E_ALIGN, "%s: read buffer %d misaligned", who, r);
+        a.in[r] = static_cast<const uint4 *>(read_buffers[r]);
+    }
+    for (int w = 0; w < writes; ++w) {
+        if (!write_buffers[w]) return fail(DOPT_E_ARG, "%s: write buffer %d is NULL", who, w);
+        if (!aligned16(write_buffers[w])) return fail(DOPT_E_ALIGN, "%s: write buffer %d misaligned", who, w);
+        a.out[w] = static_cast<uint4 *>(write_buffers[w]);
+    }
+    a.n = n_vectors;
+    a.reads = reads;
+    a.writes = writes;
+    if (n_vectors == 0) return DOPT_OK;
+    const int64_t blocks = (n_vectors + kThreads - 1) / kThreads;
+    if (blocks >= (int64_t(1) << 31)) return fail(DOPT_E_ARG, "%s: too many vectors", who);
+    void (*k)(ProbeArgs) = reads <= 1   ? dopt_stream_probe_kernel<1>
+                           : reads <= 2 ? dopt_stream_probe_kernel<2>
+                           : reads <= 4 ? dopt_stream_probe_kernel<4>
+                           : reads <= 8 ? dopt_stream_probe_kernel<8>
+                                        : dopt_stream_probe_kernel<16>;
+    k<<<unsigned(blocks), kThreads, 0, stream>>>(a);
+    return launch_error(who, "probe");
 }
 
 extern "C" int dopt_stage_timeouts(int reset, uint32_t *count) {

@@ -2,6 +2,10 @@
 
     python -m zero_distributed_optimizer_gb300.profcase --workload gpt2_small \
         [--max-elems N] [--warmup W] [--launches K] [--mode MODE]
+    python -m zero_distributed_optimizer_gb300.profcase --probe R,W[;R,W...] [--mib M]
+
+--probe times the stream probe (dopt_stream_probe) for each mix of R read
+and W write streams of M MiB each: the HBM's ceiling for that mix.
 
 --max-elems keeps the leading params of the workload whose total stays
 within N elements, so that a profiler capture can run on a smaller buffer of
@@ -65,12 +69,18 @@ def main(argv=None):
     ap.add_argument("--param-dtype", choices=["bf16", "fp16"], default="bf16")
     ap.add_argument("--instances", type=int, default=1,
                     help="distributed-optimizer instances (D must divide by it)")
+    ap.add_argument("--probe", default="",
+                    help="mixes 'R,W;R,W;...' of read and write streams for the stream probe "
+                         "(the workload is then not used)")
+    ap.add_argument("--mib", type=int, default=256, help="--probe: MiB per stream")
     ap.add_argument("--stage", action="store_true",
                     help="step, counted and buckets modes: read through shared memory with "
                          "bulk copies (DOPT_STEP_STAGE)")
     args = ap.parse_args(argv)
 
     libbuild.build()
+    if args.probe:
+        return probe(args)
     if args.workload == "sweep_256m":
         w = W.sweep_256m(args.D, args.bucket_mi)
     else:
@@ -170,6 +180,49 @@ def main(argv=None):
                       "launches": args.launches, "ms_per_launch": ms,
                       "algorithmic_bytes_per_launch": bytes_per,
                       "gbs": bytes_per / (ms / 1e3) / 1e9}))
+
+
+def probe(args):
+    """Bandwidth of each read/write stream mix: CUDA events around
+    `launches` probe launches captured in a CUDA graph (so that host
+    submission never limits short launches), after `warmup` direct ones,
+    best of three replays."""
+    import torch
+
+    from zero_distributed_optimizer_gb300 import binding as B
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    n = args.mib << 20
+    for mix in args.probe.split(";"):
+        reads, writes = (int(x) for x in mix.split(","))
+        rb = [torch.full((n // 4,), float(i + 1), device=dev) for i in range(reads)]
+        wb = [torch.empty(n // 4, device=dev) for _ in range(writes)]
+        for _ in range(args.warmup):
+            B.dopt_stream_probe(rb, wb)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side), torch.cuda.graph(graph, stream=side):
+            for _ in range(args.launches):
+                B.dopt_stream_probe(rb, wb)
+        torch.cuda.current_stream().wait_stream(side)
+        best = float("inf")
+        for _ in range(3):
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            ev[0].record()
+            graph.replay()
+            ev[1].record()
+            torch.cuda.synchronize()
+            best = min(best, ev[0].elapsed_time(ev[1]) / args.launches)
+        del graph
+        moved = (reads + writes) * n
+        print(json.dumps({"mode": "probe", "reads": reads, "writes": writes, "mib_per_stream": args.mib,
+                          "ms_per_launch": best, "bytes_per_launch": moved,
+                          "gbs": moved / (best / 1e3) / 1e9}), flush=True)
+        del rb, wb
+        torch.cuda.empty_cache()
 
 
 if __name__ == "__main__":
