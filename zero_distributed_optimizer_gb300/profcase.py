@@ -3,9 +3,14 @@
     python -m zero_distributed_optimizer_gb300.profcase --workload gpt2_small \
         [--max-elems N] [--warmup W] [--launches K] [--mode MODE]
     python -m zero_distributed_optimizer_gb300.profcase --probe R,W[;R,W...] [--mib M]
+    python -m zero_distributed_optimizer_gb300.profcase --workload gpt2_small --ab-stage ROUNDS
 
 --probe times the stream probe (dopt_stream_probe) for each mix of R read
 and W write streams of M MiB each: the HBM's ceiling for that mix.
+
+--ab-stage times the step (or the counted step) with direct loads and with
+DOPT_STEP_STAGE alternately in one process on the same buffers, ROUNDS
+rounds of --launches launches each, and prints the best of each.
 
 --max-elems keeps the leading params of the workload whose total stays
 within N elements, so that a profiler capture can run on a smaller buffer of
@@ -76,6 +81,9 @@ def main(argv=None):
     ap.add_argument("--stage", action="store_true",
                     help="step, counted and buckets modes: read through shared memory with "
                          "bulk copies (DOPT_STEP_STAGE)")
+    ap.add_argument("--ab-stage", type=int, default=0, metavar="ROUNDS",
+                    help="step and counted modes: alternate direct and staged launches for "
+                         "ROUNDS rounds and print the best time of each")
     args = ap.parse_args(argv)
 
     libbuild.build()
@@ -140,6 +148,8 @@ def main(argv=None):
         torch.cuda.current_stream().wait_stream(side)
         streams[0] = torch.cuda.current_stream()
     torch.cuda.synchronize()
+    if args.ab_stage:
+        return ab_stage(args, w, L, adam, grads, master, m, v, params, counter)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     t = 0
     for i in range(args.warmup + args.launches):
@@ -180,6 +190,51 @@ def main(argv=None):
                       "launches": args.launches, "ms_per_launch": ms,
                       "algorithmic_bytes_per_launch": bytes_per,
                       "gbs": bytes_per / (ms / 1e3) / 1e9}))
+
+
+def ab_stage(args, w, L, adam, grads, master, m, v, params, counter):
+    """Direct loads against DOPT_STEP_STAGE, alternating: `warmup` launches
+    of each, then `ab_stage` rounds of `launches` launches of each, CUDA
+    events around every round; the best round of each is reported."""
+    import torch
+
+    from zero_distributed_optimizer_gb300 import binding as B
+
+    if args.mode not in ("step", "counted"):
+        raise SystemExit("--ab-stage takes --mode step or counted")
+    t = 0
+
+    def launch(stage):
+        nonlocal t
+        t += 1
+        if args.mode == "counted":
+            B.dopt_step_counted(L, adam, counter, grads, master, m, v, params, stage=stage)
+        else:
+            B.dopt_step(L, adam, t, grads, master, m, v, params, stage=stage)
+
+    for stage in (False, True):
+        for _ in range(args.warmup):
+            launch(stage)
+    times = {False: [], True: []}
+    for _ in range(args.ab_stage):
+        for stage in (False, True):
+            torch.cuda.synchronize()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            ev[0].record()
+            for _ in range(args.launches):
+                launch(stage)
+            ev[1].record()
+            torch.cuda.synchronize()
+            times[stage].append(ev[0].elapsed_time(ev[1]) / args.launches)
+    bytes_per = w.numel * w.algorithmic_bytes_per_element()
+    out = {"workload": w.name, "N": w.numel, "D": w.D, "mode": args.mode, "grad_dtype": w.grad_dtype,
+           "launches": args.launches, "rounds": args.ab_stage}
+    for stage, name in ((False, "direct"), (True, "staged")):
+        best = min(times[stage])
+        out[name] = {"ms_per_launch": best, "gbs": bytes_per / (best / 1e3) / 1e9,
+                     "rounds_ms": times[stage]}
+    out["staged_over_direct"] = out["staged"]["ms_per_launch"] / out["direct"]["ms_per_launch"]
+    print(json.dumps(out), flush=True)
 
 
 def probe(args):
