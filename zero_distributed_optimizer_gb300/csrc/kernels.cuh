@@ -878,11 +878,17 @@ __device__ __forceinline__ void step_vector(const StepArgs &a, const Scalars &sc
 // CTAs per SM that the kernel's registers must allow: 3 (at most 85
 // registers), but 4 (64 registers, no spills) for the plain and counted
 // steps with D = 4 and 16-bit grads, which run 2-5 % faster with the fourth
-// CTA than with the 67-71 registers they take when allowed 3.  At D = 8 the
-// fourth CTA costs 0.2-0.4 %.
+// CTA than with the 67-71 registers they take when allowed 3, and 5 (48
+// registers; 32 bytes spilled) for the plain step with D = 1 and 16-bit
+// grads: 0.6-1.7 % faster than 4 CTAs of 50 registers.  Measured slower:
+// 4 CTAs at D = 8 (0.2-0.4 %), 4 with fp32 grads at D = 4 and 8 (0.4-12 %,
+// spills), 5 for the counted D = 1 step (6 %, 76 bytes spilled).
 template <typename G, int DC, int MODE>
 constexpr int step_min_ctas() {
-    return (DC == 4 && sizeof(G) == 2 && (MODE == kPlain || MODE == kCounted)) ? 4 : 3;
+    if (sizeof(G) != 2) return 3;
+    if (DC == 1 && MODE == kPlain) return 5;
+    if (DC == 4 && (MODE == kPlain || MODE == kCounted)) return 4;
+    return 3;
 }
 
 template <typename G, int DC, int MODE, int GR = DC>
