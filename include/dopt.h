@@ -188,7 +188,7 @@ typedef enum { DOPT_BF16 = 0, DOPT_FP32 = 1, DOPT_FP16 = 2 } dopt_dtype;
 #define DOPT_STEP_HOST_PARAMS 64u
 /*
  * Read each tile's grads and master/m/v through shared memory: one thread
- * of every CTA issues 1-D bulk copies (the SM's copy engine, from this
+ * of every CTA issues 1-D bulk copies (the SM's TMA unit, from this
  * GPU's own memory into that CTA's shared memory; no cluster multicast),
  * and the CTA computes from shared memory once they complete.  The results
  * are those of the default path (128-bit vector loads into registers), bit
@@ -614,8 +614,8 @@ int dopt_device_checks(int reset, uint32_t *flags, int64_t *first_bad);
 
 /* Count of staged CTAs (DOPT_STEP_STAGE) on the current device whose bulk
  * copies did not complete within their time limit, so that they skipped
- * their tile; with reset != 0 the count is then cleared.  0 unless the
- * copy engine failed.  Library infrastructure: the pages have no
+ * their tile; with reset != 0 the count is then cleared.  0 unless a bulk
+ * copy failed to complete.  Library infrastructure: the pages have no
  * counterpart.  Synchronous.  Errors: DOPT_E_ARG (NULL count), DOPT_E_CUDA. */
 int dopt_stage_timeouts(int reset, uint32_t *count);
 
@@ -625,10 +625,13 @@ int dopt_stage_timeouts(int reset, uint32_t *count);
  * the `reads` read buffers and writes the XOR of them with a seed made of i
  * to vector i of each of the `writes` write buffers, with the streaming
  * 128-bit loads and stores of the step kernels.  Timing it (the caller's
- * CUDA events) gives the ceiling of a read/write mix, e.g. the step's 2D + 3
- * read and D + 3 write streams, against which the step kernels are
- * measured.  Buffers: device, 16-byte aligned, n_vectors * 16 bytes each,
- * owned by the caller.  0 <= reads, writes <= 16, not both 0.  Library
+ * CUDA events) gives the ceiling of a read/write mix (the step at D reads
+ * D + 6 and writes D + 6 16-byte vectors per 8 elements: equal read and
+ * write streams), against which the step kernels are measured.  Buffers:
+ * device, 16-byte aligned, n_vectors * 16 bytes each, owned by the caller;
+ * with no write stream, a thread whose XOR equals one fixed 128-bit pattern
+ * stores it into read buffer 0 (this keeps the loads from being optimised
+ * away).  0 <= reads, writes <= 16, not both 0.  Library
  * infrastructure for measurement: the pages have no counterpart.
  * Asynchronous on `stream`.  Errors: DOPT_E_ARG, DOPT_E_ALIGN, DOPT_E_CUDA.
  */

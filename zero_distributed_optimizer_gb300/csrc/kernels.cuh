@@ -918,7 +918,7 @@ __global__ void __launch_bounds__(kThreads, step_min_ctas<G, DC, MODE>())
 //
 // The same step as dopt_step_kernel (one-instance layouts, D in {1, 2, 4, 8,
 // 16}, plain or counted), with a different way of reading: one thread of the
-// CTA issues one 1-D bulk copy (cp.async.bulk, the copy engine of the SM,
+// CTA issues one 1-D bulk copy (cp.async.bulk, the TMA unit of the SM,
 // global -> this CTA's shared memory, no cluster multicast) per grad replica
 // and per state array for the tile's whole vectors, completing on an
 // mbarrier, while the CTA looks up its runs; the threads then read their
@@ -926,7 +926,7 @@ __global__ void __launch_bounds__(kThreads, step_min_ctas<G, DC, MODE>())
 // kernel.  The plain kernel loads with 128-bit vector loads straight into
 // registers; this one exists to measure the other design.
 
-// Bulk-copy waits that ran past their time limit (the copy engine never
+// Bulk-copy waits that ran past their time limit (the TMA unit never
 // completed them); the CTA then skipped its tile.  Read by
 // dopt_stage_timeouts.
 __device__ unsigned int g_stage_timeouts;
@@ -1030,7 +1030,7 @@ __device__ __forceinline__ void staged_tile(const StepArgs &a, const Scalars &sc
     const VecKind kind = locate(a.rv, tile, e0, j);  // while the copies fly
     const bool ok = n <= 0 || mbar_wait(bar, 0);
     if (__syncthreads_or(!ok)) {
-        // the copy engine did not complete in time (for some thread: the
+        // the bulk copies did not complete in time (for some thread: the
         // whole CTA decides together): count it, give the copies one more
         // bounded wait (they write this CTA's shared memory), and leave the
         // tile alone
