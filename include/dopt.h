@@ -619,6 +619,18 @@ int dopt_device_checks(int reset, uint32_t *flags, int64_t *first_bad);
  * counterpart.  Synchronous.  Errors: DOPT_E_ARG (NULL count), DOPT_E_CUDA. */
 int dopt_stage_timeouts(int reset, uint32_t *count);
 
+/* Test build only (DOPT_DEVICE_CHECKS, libdopt_checked.so): every staged CTA
+ * launched after this call on the current device expects `extra_bytes`
+ * more from its bulk copies than they deliver, so its 2 s wait runs out
+ * and it takes the failure path described at DOPT_STEP_STAGE (counted by
+ * dopt_stage_timeouts, its tile left untouched, a second bounded wait,
+ * about 4 s in all) without any fault; 0 restores normal staging.
+ * 0 <= extra_bytes <= 65536.  Library infrastructure for testing the
+ * bounded wait: the pages have no counterpart.  Synchronous.  Errors:
+ * DOPT_E_STATE in the product build (which has no such hook), DOPT_E_ARG,
+ * DOPT_E_CUDA. */
+int dopt_stage_wait_test(uint32_t extra_bytes);
+
 /*
  * The HBM bandwidth of a mix of streams, for measurement: one launch over
  * n_vectors 16-byte vectors, one per thread, that reads vector i of each of

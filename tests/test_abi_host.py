@@ -386,6 +386,12 @@ def test_product_build_has_no_device_checks(lib):
         B.device_checks()
     assert e.value.code == B.DOPT_E_STATE
     assert "DOPT_DEVICE_CHECKS" in str(e.value)
+    # nor the hook that makes the staged wait run out
+    for extra in (0, 16):
+        with pytest.raises(B.DoptError) as e:
+            B.stage_wait_test(extra)
+        assert e.value.code == B.DOPT_E_STATE
+        assert "DOPT_DEVICE_CHECKS" in str(e.value)
 
 
 def test_checked_build_compiles_and_exports_the_same_symbols():

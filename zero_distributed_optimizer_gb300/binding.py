@@ -139,6 +139,8 @@ def _declare(lib):
                                       vp]
     lib.dopt_stage_timeouts.restype = ctypes.c_int
     lib.dopt_stage_timeouts.argtypes = [ctypes.c_int, P(ctypes.c_uint32)]
+    lib.dopt_stage_wait_test.restype = ctypes.c_int
+    lib.dopt_stage_wait_test.argtypes = [ctypes.c_uint32]
     lib.dopt_device_checks.restype = ctypes.c_int
     lib.dopt_device_checks.argtypes = [ctypes.c_int, P(ctypes.c_uint32), P(ctypes.c_int64)]
     lib.dopt_last_error.restype = ctypes.c_char_p
@@ -200,11 +202,19 @@ def dopt_stream_probe(read_buffers, write_buffers, stream=None) -> None:
 
 def stage_timeouts(reset: bool = False) -> int:
     """Staged CTAs (DOPT_STEP_STAGE) on the current device whose bulk copies
-    ran past their time limit and skipped their tile (0 unless the copy
-    engine failed); reset clears the count."""
+    ran past their time limit and skipped their tile (0 unless a bulk copy
+    failed to complete); reset clears the count."""
     c = ctypes.c_uint32(0)
     _check(lib().dopt_stage_timeouts(1 if reset else 0, ctypes.byref(c)))
     return c.value
+
+
+def stage_wait_test(extra_bytes: int) -> None:
+    """Test build only (dopt_stage_wait_test in dopt.h): staged CTAs
+    launched afterwards expect `extra_bytes` that no copy delivers, so their
+    bounded wait runs out; 0 restores normal staging.  Raises DoptError
+    with DOPT_E_STATE in the product build."""
+    _check(lib().dopt_stage_wait_test(ctypes.c_uint32(int(extra_bytes))))
 
 
 def _check(rc: int):

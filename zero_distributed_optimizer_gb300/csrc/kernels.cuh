@@ -933,6 +933,16 @@ __device__ unsigned int g_stage_timeouts;
 
 constexpr unsigned long long kStageWaitNs = 2000000000ull;  // 2 s
 
+#ifdef DOPT_DEVICE_CHECKS
+// Test build only: bytes added to every staged CTA's expected transaction
+// count that no copy delivers, so that its bounded wait runs out and the
+// failure path runs without any fault (dopt_stage_wait_test).
+__device__ unsigned int g_stage_phantom_bytes;
+__device__ __forceinline__ uint32_t stage_phantom_bytes() { return g_stage_phantom_bytes; }
+#else
+__device__ __forceinline__ uint32_t stage_phantom_bytes() { return 0u; }
+#endif
+
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -1012,7 +1022,7 @@ __device__ __forceinline__ void staged_tile(const StepArgs &a, const Scalars &sc
     if (threadIdx.x == 0 && n > 0) {
         const uint32_t gbytes = uint32_t(n * int64_t(sizeof(G)));
         const uint32_t sbytes = uint32_t(n * 4);
-        const uint32_t total = uint32_t(DC) * gbytes + 3 * sbytes;
+        const uint32_t total = uint32_t(DC) * gbytes + 3 * sbytes + stage_phantom_bytes();
         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(total)
                      : "memory");
         const uint32_t sm = smem_addr(stage);

@@ -692,6 +692,7 @@ extern "C" int dopt_stream_probe(int32_t reads, int32_t writes, const void *cons
 
 extern "C" int dopt_stage_timeouts(int reset, uint32_t *count) {
     using dopt::fail;
+    dopt::clear_error();
     if (!count) return fail(DOPT_E_ARG, "dopt_stage_timeouts: NULL output");
     unsigned int c = 0;
     cudaError_t e = cudaMemcpyFromSymbol(&c, g_stage_timeouts, sizeof c);
@@ -702,6 +703,26 @@ extern "C" int dopt_stage_timeouts(int reset, uint32_t *count) {
     if (e != cudaSuccess) return fail(DOPT_E_CUDA, "dopt_stage_timeouts: %s", cudaGetErrorString(e));
     *count = c;
     return DOPT_OK;
+}
+
+// The largest phantom count the test hook takes: well inside an mbarrier's
+// transaction-count range with the largest staged tile (D = 16 fp32).
+constexpr uint32_t kMaxStagePhantomBytes = 1u << 16;
+
+extern "C" int dopt_stage_wait_test(uint32_t extra_bytes) {
+    using dopt::fail;
+    dopt::clear_error();
+#ifdef DOPT_DEVICE_CHECKS
+    if (extra_bytes > kMaxStagePhantomBytes)
+        return fail(DOPT_E_ARG, "dopt_stage_wait_test: extra_bytes above %u", kMaxStagePhantomBytes);
+    const unsigned int v = extra_bytes;
+    const cudaError_t e = cudaMemcpyToSymbol(g_stage_phantom_bytes, &v, sizeof v);
+    if (e != cudaSuccess) return fail(DOPT_E_CUDA, "dopt_stage_wait_test: %s", cudaGetErrorString(e));
+    return DOPT_OK;
+#else
+    (void)extra_bytes;
+    return fail(DOPT_E_STATE, "dopt_stage_wait_test: this library was built without DOPT_DEVICE_CHECKS");
+#endif
 }
 
 extern "C" int dopt_step(const dopt_layout *L, const dopt_adam_cfg *cfg, int64_t step,
