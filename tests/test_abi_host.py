@@ -434,3 +434,15 @@ def test_stream_probe_argument_checks_before_cuda(lib):
     assert probe(1, 1, good, (vp * 1)(0x20004), 16, None) == B.DOPT_E_ALIGN
     assert probe(1, 1, good, good, -1, None) == B.DOPT_E_ARG
     assert probe(2, 2, good, good, 0, None) == B.DOPT_OK
+
+
+def test_package_exports_the_binding():
+    """Every public entry point and constant of the binding is importable
+    from the package itself."""
+    import zero_distributed_optimizer_gb300 as pkg
+
+    internal = {"lib", "dataclass", "dopt_adam_cfg", "dopt_layout_cfg", "dopt_piece", "dopt_range"}
+    public = [n for n in dir(B) if not n.startswith("_") and n not in internal
+              and (n.startswith("DOPT_") or callable(getattr(B, n)))]
+    missing = [n for n in public if not hasattr(pkg, n)]
+    assert not missing, missing
