@@ -705,14 +705,13 @@ extern "C" int dopt_stage_timeouts(int reset, uint32_t *count) {
     return DOPT_OK;
 }
 
-// The largest phantom count the test hook takes: well inside an mbarrier's
-// transaction-count range with the largest staged tile (D = 16 fp32).
-constexpr uint32_t kMaxStagePhantomBytes = 1u << 16;
-
 extern "C" int dopt_stage_wait_test(uint32_t extra_bytes) {
     using dopt::fail;
     dopt::clear_error();
 #ifdef DOPT_DEVICE_CHECKS
+    // the largest phantom count taken: well inside an mbarrier's
+    // transaction-count range with the largest staged tile (D = 16 fp32)
+    constexpr uint32_t kMaxStagePhantomBytes = 1u << 16;
     if (extra_bytes > kMaxStagePhantomBytes)
         return fail(DOPT_E_ARG, "dopt_stage_wait_test: extra_bytes above %u", kMaxStagePhantomBytes);
     const unsigned int v = extra_bytes;
