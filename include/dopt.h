@@ -485,12 +485,16 @@ typedef struct {
 /*
  * The step with global grad-norm clipping (distributed-training tutorial,
  * §8.3: the norm sqrt(sum ||g||^2) over every rank's shard is needed before
- * the optimizer update).  Two launches on `stream`:
+ * the optimizer update).  Two passes over memory on `stream` (four
+ * launches: a one-CTA reset of the workspace, the first pass, a one-CTA
+ * finalize kernel, the second pass):
  *
  *   1. the fused reduce-scatter writes every owned element's reduced fp32
  *      grad g (as in dopt_step) into main_grad, and the global
  *      norm^2 = sum of g^2 over all owned elements is accumulated (fp32
- *      squares summed per 8 elements, then in fp64); the coefficient
+ *      squares summed per 8 elements, then in fp64 within each CTA, the
+ *      CTAs' partials added exactly and rounded once, so the result does
+ *      not depend on the grid or on the order of the CTAs); the coefficient
  *      c = min(1, max_norm / (norm + 1e-6)) is evaluated in fp64 and rounded
  *      to float;
  *   2. the AdamW step, write-back and (with DOPT_STEP_GATHER) all-gather of
@@ -500,8 +504,9 @@ typedef struct {
  *   main_grad   device fp32[padded_numel], written: the reduced grads
  *               before clipping (padding untouched)
  *   workspace   device, DOPT_CLIP_WORKSPACE_BYTES, 16-byte aligned, owned by
- *               the caller; holds per-CTA partial sums between the launches;
- *               calls that share a workspace must not overlap on the GPU
+ *               the caller; holds the exact sum of squares between the
+ *               launches (zeroed by the call itself); calls that share a
+ *               workspace must not overlap on the GPU
  *   norm_out    nullable device pointer, 8-byte aligned, to a
  *               dopt_clip_report: norm and c (and, with
  *               DOPT_STEP_SKIP_NONFINITE, the count of non-finite reduced
@@ -525,7 +530,7 @@ int dopt_step_clipped(const dopt_layout *layout, const dopt_adam_cfg *cfg, int64
 /*
  * dopt_step_clipped with the step number taken from, and advanced in, a
  * device counter, as dopt_step_counted does for dopt_step: the counter
- * kernel, then the two launches of dopt_step_clipped, whose second one takes
+ * kernel, then the launches of dopt_step_clipped, whose step pass takes
  * the two step-dependent scalars and the status from the counter.  The
  * launches do not depend on the step number, so a captured sequence replays
  * every later step.  With a bad next_step (see dopt_step_counter) the norm
@@ -553,8 +558,8 @@ int dopt_step_clipped_counted(const dopt_layout *layout, const dopt_adam_cfg *cf
  * bookkeeping), and training loops that cannot take the device-wide
  * synchronisation that cudaFree, and a cudaMalloc that has to grow the
  * heap, can cause.  Such a caller cannot hand dopt_step_clipped a fresh
- * workspace, so this variant keeps the norm pass's scratch (per-CTA partial
- * sums, the finishing ticket, norm and coefficient) in a file-scope
+ * workspace, so this variant keeps the norm pass's scratch (the exact sum
+ * of squares, norm and coefficient) in a file-scope
  * `static __device__` array of DOPT_NOALLOC_SCRATCH_BYTES inside the
  * library.  Every GPU that loads the library holds that array until the
  * process exits.
@@ -572,15 +577,15 @@ int dopt_step_clipped_counted(const dopt_layout *layout, const dopt_adam_cfg *cf
  * reset, do not call this entry point again in the same process.
  *
  * Sharing: every call on a device uses the same array, which keeps the last
- * call's contents.  Each call zeroes the 16-byte header that must start at
- * zero (the finishing ticket and the non-finite count, with a one-thread
- * kernel launched on `stream` before the norm pass); the rest is
- * overwritten before it is read.  Calls whose executions overlap on the GPU (other streams, other
- * layouts, other threads) race on the array: the caller must order them.
+ * call's contents.  Each call zeroes what must start at zero (the
+ * accumulator, the special-value bits and the non-finite count, with a
+ * one-CTA kernel launched on `stream` before the norm pass); the rest is
+ * overwritten before it is read.  Calls whose executions overlap on the GPU
+ * (other streams, other layouts, other threads) race on the array: the
+ * caller must order them.
  *
- * Limit: the norm pass needs 64 bytes plus 8 bytes per CTA, at most 1024
- * CTAs (8,256 bytes), whatever the buffer size; a launch that would need
- * more than DOPT_NOALLOC_SCRATCH_BYTES is refused with DOPT_E_ARG.
+ * Size: the norm pass uses a fixed 1,856 bytes of the array, whatever the
+ * buffer size.
  *
  * Arguments, results and errors otherwise as dopt_step_clipped (without
  * `workspace`, and without DOPT_STEP_SKIP_NONFINITE, which it refuses).

@@ -9,6 +9,8 @@ to ~2e-7 relative, a clipped grad to an ulp or two, which keeps master/m/v
 inside the 1e-6 relative (+1e-7) tolerance and params inside 1 bf16 ulp."""
 from dataclasses import asdict
 
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -177,8 +179,9 @@ def test_clipped_gpt2_small_full_size():
 
 
 def test_clipped_step_is_deterministic():
-    """The norm's partial sums are added in a fixed order (per-CTA partials
-    in CTA order), so two runs from the same inputs are bitwise equal."""
+    """Each CTA adds its partial sum in a fixed order and the CTAs' partials
+    are summed exactly, so two runs from the same inputs are bitwise
+    equal."""
     sizes, wd, D = [700000, 5, 300001], [1, 0, 1], 8
     L = B.dopt_build_range_map(sizes, D, 0, 64, wd).to_device()
     N = L.padded_numel
@@ -198,3 +201,39 @@ def test_clipped_step_is_deterministic():
     for x, y in zip(*runs):
         assert torch.equal(x.view(torch.int16) if x.dtype == torch.bfloat16 else x.view(torch.int32),
                            y.view(torch.int16) if y.dtype == torch.bfloat16 else y.view(torch.int32))
+
+
+@pytest.mark.parametrize("D", [8, 2])  # 4 tiles per CTA; the persistent grid
+@pytest.mark.parametrize("log2_scale", [0, -60, 40])
+def test_norm_sum_is_exact(D, log2_scale):
+    """With grads k * 2^s (k integer below 256, in replica 0 only, the other
+    replicas zero, scaling 1) every square, every CTA's fp64 partial and the
+    total are exact, so the norm^2 the kernel leaves in the workspace (a
+    double at byte 16) must equal the integer sum of k^2, times 4^s, bit for
+    bit: thousands of CTAs' partials added through the digits and carries
+    of the exact accumulator, at scales that put them low, in the middle
+    and high in its range."""
+    sizes, wd = [700000, 5, 300001, 4096], [1, 0, 1, 1]
+    L = B.dopt_build_range_map(sizes, D, 0, 64, wd).to_device()
+    N = L.padded_numel
+    rng = np.random.default_rng(31 + D)
+    k = rng.integers(0, 256, size=N, dtype=np.int64)
+    g0 = torch.from_numpy(k.astype(np.float32) * np.float32(2.0 ** log2_scale)).to(torch.bfloat16)
+    assert torch.equal(g0.float(), torch.from_numpy(k.astype(np.float32) * np.float32(2.0 ** log2_scale)))
+    grads = [g0.to(DEV)] + [torch.zeros(N, dtype=torch.bfloat16, device=DEV) for _ in range(D - 1)]
+    master = torch.zeros(N, device=DEV)
+    m, v = torch.zeros(N, device=DEV), torch.zeros(N, device=DEV)
+    params = [torch.zeros(N, dtype=torch.bfloat16, device=DEV) for _ in range(D)]
+    ws = B.clip_workspace(DEV)
+    mg = torch.empty(N, device=DEV)
+    B.dopt_step_clipped(L, B.AdamConfig(grad_scale=1.0), 1, 3.0e38, grads, master, m, v, params,
+                        mg, ws)
+    torch.cuda.synchronize()
+    owned = np.zeros(N, dtype=bool)
+    for a, b in L.param_offsets():
+        owned[a:b] = True
+    exact = int((k[owned] ** 2).sum())
+    want = math.ldexp(float(exact), 2 * log2_scale)  # exact: the sum has < 53 bits
+    assert exact < 2 ** 53
+    got = ws[16:24].cpu().view(torch.float64).item()
+    assert got == want, (got, want)

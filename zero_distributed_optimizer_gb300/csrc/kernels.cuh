@@ -44,7 +44,6 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kVec = 8;
-constexpr int kMaxClipCtas = 1024;
 static_assert(kThreads * kVec == kDoptTileElems, "tile size must match the host table");
 
 struct Scalars {
@@ -162,19 +161,33 @@ struct StepArgs {
 };
 
 // Workspace of the clipped step (device memory, DOPT_CLIP_WORKSPACE_BYTES).
+// The norm pass adds its per-CTA partials exactly: every partial (a
+// non-negative double, a multiple of 2^-149 because every square is an fp32
+// product) is split into 32-bit digits of a fixed-point number whose lowest
+// bit weighs 2^-149, and each digit is added to a 64-bit word with an
+// integer atomic.  Integer sums do not depend on their order, so the norm
+// is the same at every call whatever the grid and the order in which CTAs
+// finish, and it is the exact sum of the partials rounded once.  kAccWords
+// digits reach 2^(32 * kAccWords - 149) = 2^299, beyond any finite sum of
+// fp32 squares of up to 2^40 elements; each word takes at most one digit
+// (< 2^32) per CTA, so it cannot overflow before 2^32 CTAs.  kAccCopies
+// copies, chosen by CTA index, spread the atomics over more addresses; the
+// finalize kernel adds them.
+constexpr int kAccWords = 14;
+constexpr int kAccLsb = -149;
+constexpr int kAccCopies = 16;
+
 struct ClipWorkspace {
-    unsigned int ticket;           // CTAs done; zeroed before every launch
+    unsigned int special;          // 1: some partial was +Inf, 2: NaN; zeroed before every launch
     unsigned int pad0;
     unsigned long long nonfinite;  // non-finite reduced grads; zeroed likewise
     double norm_sq;
     float norm;
     float coef;
     unsigned char pad1[32];
-    double partial[kMaxClipCtas];
+    unsigned long long acc[kAccCopies][kAccWords];  // zeroed likewise
 };
-constexpr size_t kClipResetBytes = 16;  // ticket, pad0, nonfinite
-static_assert(offsetof(ClipWorkspace, norm_sq) == kClipResetBytes, "reset prefix");
-static_assert(offsetof(ClipWorkspace, partial) == 64, "workspace header");
+static_assert(offsetof(ClipWorkspace, acc) == 64, "workspace header");
 static_assert(sizeof(dopt_clip_report) == 16, "report layout");
 static_assert(sizeof(ClipWorkspace) <= DOPT_CLIP_WORKSPACE_BYTES, "workspace size");
 static_assert(sizeof(ClipWorkspace) <= DOPT_NOALLOC_SCRATCH_BYTES, "scratch size");
@@ -1299,15 +1312,86 @@ __global__ void __launch_bounds__(kThreads, 3) dopt_allreduce_kernel(const __gri
 // Pass 1 of the clipped step
 // ---------------------------------------------------------------------------
 
-// The clipped step's first launch: zero the workspace's header (the ticket
-// and the non-finite count) for the norm pass, which starts alongside it
-// (a programmatic dependent) and waits for it only before it touches the
-// workspace.
+// The clipped step's first launch: zero the workspace's special-value bits,
+// non-finite count and accumulator for the norm pass, which starts
+// alongside it (a programmatic dependent) and waits for it only before it
+// touches the workspace.  One CTA of kThreads threads.
 __global__ void dopt_clip_reset_kernel(ClipWorkspace *ws) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    ws->ticket = 0;
-    ws->pad0 = 0;
-    ws->nonfinite = 0;
+    const int i = threadIdx.x;
+    if (i < kAccCopies * kAccWords) (&ws->acc[0][0])[i] = 0ull;
+    if (i == 0) {
+        ws->special = 0;
+        ws->nonfinite = 0;
+    }
+}
+
+// Add a CTA's partial p (>= 0, or +Inf, or NaN) to accumulator copy `acc`
+// exactly (see ClipWorkspace): p = m * 2^e with m < 2^53, and m shifted to
+// its place above 2^-149 is at most three 32-bit digits.  The atomics
+// return nothing (reductions), so no CTA waits for them.
+__device__ __forceinline__ void acc_add(unsigned long long *acc, unsigned int *special, double p) {
+    if (p == 0.0) return;
+    if (isnan(p)) {
+        atomicOr(special, 2u);
+        return;
+    }
+    const unsigned long long bits = static_cast<unsigned long long>(__double_as_longlong(p));
+    const int bexp = int((bits >> 52) & 0x7ff);
+    unsigned long long m = bits & ((1ull << 52) - 1);
+    int e = -1074;
+    if (bexp != 0) {
+        m |= 1ull << 52;
+        e = bexp - 1075;
+    }
+    int shift = e - kAccLsb;
+    if (shift < 0) {  // m carries trailing zeros down to 2^-149
+        m >>= -shift;
+        shift = 0;
+    }
+    if (bexp == 0x7ff || shift + 53 > 32 * kAccWords) {  // +Inf, or beyond the range
+        atomicOr(special, 1u);
+        return;
+    }
+    const int w = shift >> 5;
+    const unsigned __int128 v = static_cast<unsigned __int128>(m) << (shift & 31);
+    const unsigned long long d0 = static_cast<unsigned long long>(v) & 0xffffffffull;
+    const unsigned long long d1 = static_cast<unsigned long long>(v >> 32) & 0xffffffffull;
+    const unsigned long long d2 = static_cast<unsigned long long>(v >> 64);
+    if (d0) atomicAdd(&acc[w], d0);
+    if (d1) atomicAdd(&acc[w + 1], d1);
+    if (d2) atomicAdd(&acc[w + 2], d2);
+}
+
+// The exact sum held in kAccWords words (the copies already added), the
+// carries propagated, rounded once to the nearest double.
+__device__ double acc_value(const unsigned long long *words) {
+    unsigned long long digit[kAccWords];
+    unsigned long long carry = 0;
+    for (int k = 0; k < kAccWords; ++k) {
+        const unsigned long long t = words[k] + carry;
+        digit[k] = t & 0xffffffffull;
+        carry = t >> 32;
+    }
+    if (carry) return __longlong_as_double(0x7ff0000000000000ll);  // beyond the range: +Inf
+    int top = kAccWords - 1;
+    while (top >= 0 && digit[top] == 0) --top;
+    if (top < 0) return 0.0;
+    // the top three digits as one 96-bit window, left-justified, its top 64
+    // bits with every lower bit folded into a sticky bit, then one rounding
+    unsigned __int128 win = static_cast<unsigned __int128>(digit[top]) << 64;
+    if (top >= 1) win |= static_cast<unsigned __int128>(digit[top - 1]) << 32;
+    if (top >= 2) win |= digit[top - 2];
+    bool sticky = false;
+    for (int k = 0; k < top - 2; ++k) sticky |= digit[k] != 0;
+    const int lz = __clzll(static_cast<long long>(digit[top])) - 32;
+    win <<= 32 + lz;  // the top bit at bit 127
+    unsigned long long hi = static_cast<unsigned long long>(win >> 64);
+    sticky |= static_cast<unsigned long long>(win) != 0;
+    if (sticky) hi |= 1ull;
+    // window bit 95 - lz weighs 2^(32 * (top - 2) + 95 - lz - 149); it is hi's bit 63
+    const int scale = 32 * (top - 2) + 95 - lz + kAccLsb - 63;
+    return ldexp(__ull2double_rn(hi), scale);
 }
 
 // Deterministic sum over a warp (fixed shuffle tree); the result is in lane 0.
@@ -1319,9 +1403,10 @@ __device__ __forceinline__ double warp_sum(double v) {
 // The fused reduce-scatter writes the fp32 main grads and every CTA
 // accumulates the sum of their squares over the tiles it visits (fp32
 // squares summed pairwise per 8-element vector, then one fp64 add per
-// vector).  Each CTA leaves one fp64 partial; the CTA that finishes last
-// (atomic ticket, nobody waits) adds the partials in CTA order and writes the
-// norm and the clipping coefficient min(1, max_norm / (norm + 1e-6)).
+// vector, then the CTA's threads in a fixed order) and adds that partial to
+// the workspace's exact accumulator.  The grid is a few tiles per CTA, or a
+// persistent grid (see norm_grid on the host); the finalize kernel after it
+// turns the sum into the norm and the coefficient.
 template <typename G, int DC>
 __global__ void __launch_bounds__(kThreads) dopt_rs_norm_kernel(const __grid_constant__ NormArgs a) {
     // the step pass may be scheduled as soon as every CTA of this grid runs:
@@ -1369,10 +1454,9 @@ __global__ void __launch_bounds__(kThreads) dopt_rs_norm_kernel(const __grid_con
     }
     __shared__ double warp_part[kThreads / 32];
     __shared__ unsigned int warp_bad[kThreads / 32];
-    __shared__ bool last;
     // this pass is a programmatic dependent of the kernel that zeroes the
-    // workspace's header: its grads and tables it may read at once, the
-    // workspace only after that kernel has completed
+    // workspace: its grads and tables it may read at once, the workspace
+    // only after that kernel has completed
     asm volatile("griddepcontrol.wait;" ::: "memory");
     local = warp_sum(local);
     bad = __reduce_add_sync(0xffffffffu, bad);
@@ -1388,48 +1472,53 @@ __global__ void __launch_bounds__(kThreads) dopt_rs_norm_kernel(const __grid_con
             cta += warp_part[w];
             cta_bad += warp_bad[w];
         }
-        a.ws->partial[blockIdx.x] = cta;
+        acc_add(a.ws->acc[blockIdx.x % kAccCopies], &a.ws->special, cta);
         if (cta_bad) atomicAdd(&a.ws->nonfinite, cta_bad);  // integer: order-free
-        __threadfence();
-        last = atomicAdd(&a.ws->ticket, 1u) == gridDim.x - 1;
+    }
+}
+
+// The clipped step's third launch, one CTA: a programmatic dependent of the
+// norm pass (every partial added once that pass has completed), it rounds
+// the exact sum of squares once and writes the norm and the clipping
+// coefficient min(1, max_norm / (norm + 1e-6)) (NaN, a skip, when
+// non-finite grads were counted and the caller asked to skip).  The step
+// pass after it starts as soon as this kernel does and waits for it before
+// it reads the main grads and the coefficient.
+__global__ void __launch_bounds__(kThreads) dopt_clip_finalize_kernel(const __grid_constant__ NormArgs a) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    __shared__ unsigned long long words[kAccWords];
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (threadIdx.x < kAccWords) {  // the copies of one word (integers: any order)
+        unsigned long long t = 0;
+        for (int c = 0; c < kAccCopies; ++c) t += __ldcg(&a.ws->acc[c][threadIdx.x]);
+        words[threadIdx.x] = t;
     }
     __syncthreads();
-    if (!last) return;
-    __threadfence();
-    // The last CTA adds the partials: thread i those at i, i + 256, ...
-    // (independent loads, all in flight at once, where one warp walking the
-    // list made a chain of dependent L2 round trips at the end of the pass),
-    // then each warp's sum, then the 8 warps' sums in warp order: the same
-    // order at every call.
-    double v = 0.0;
-    for (int i = threadIdx.x; i < int(gridDim.x); i += kThreads) v += __ldcg(&a.ws->partial[i]);
-    v = warp_sum(v);
-    if (lane == 0) warp_part[threadIdx.x >> 5] = v;  // thread 0 is done reading it
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        v = 0.0;
-        for (int w = 0; w < kThreads / 32; ++w) v += warp_part[w];
-        const double norm = sqrt(v);
-        double coef = double(a.max_norm) / (norm + 1e-6);
-        if (coef > 1.0) coef = 1.0;
-        const unsigned long long nonfinite = __ldcg(&a.ws->nonfinite);
-        float c = float(coef);
-        if (a.skip_nonfinite && nonfinite != 0) {
-            c = __int_as_float(0x7fc00000);  // skip
-            // a skipped step is not counted (the counter kernel before this
-            // grid advanced the counter; nothing else reads it until this
-            // step's kernels are done)
-            if (a.counter && a.counter->hot.status == 0) a.counter->next_step -= 1;
-        }
-        a.ws->norm_sq = v;
-        a.ws->norm = float(norm);
-        a.ws->coef = c;
-        if (a.norm_out) {
-            dopt_clip_report *rep = reinterpret_cast<dopt_clip_report *>(a.norm_out);
-            rep->norm = float(norm);
-            rep->coef = c;
-            if (a.skip_nonfinite) rep->nonfinite = nonfinite;
-        }
+    if (threadIdx.x != 0) return;
+    const unsigned int special = __ldcg(&a.ws->special);
+    const double v = (special & 2u)   ? __longlong_as_double(0x7ff8000000000000ll)
+                     : (special & 1u) ? __longlong_as_double(0x7ff0000000000000ll)
+                                      : acc_value(words);
+    const double norm = sqrt(v);
+    double coef = double(a.max_norm) / (norm + 1e-6);
+    if (coef > 1.0) coef = 1.0;
+    const unsigned long long nonfinite = __ldcg(&a.ws->nonfinite);
+    float c = float(coef);
+    if (a.skip_nonfinite && nonfinite != 0) {
+        c = __int_as_float(0x7fc00000);  // skip
+        // a skipped step is not counted (the counter kernel before the norm
+        // pass advanced the counter; nothing else reads it until this step's
+        // kernels are done)
+        if (a.counter && a.counter->hot.status == 0) a.counter->next_step -= 1;
+    }
+    a.ws->norm_sq = v;
+    a.ws->norm = float(norm);
+    a.ws->coef = c;
+    if (a.norm_out) {
+        dopt_clip_report *rep = reinterpret_cast<dopt_clip_report *>(a.norm_out);
+        rep->norm = float(norm);
+        rep->coef = c;
+        if (a.skip_nonfinite) rep->nonfinite = nonfinite;
     }
 }
 

@@ -322,16 +322,23 @@ int launch_step_kernel(const char *who, const dopt_layout *L, dopt_dtype grad_dt
 }
 
 
-// Grid of the persistent norm pass: every SM full, at most kMaxClipCtas.
-int norm_grid(NormKernel k, int64_t n_tiles, int device) {
+// Grid of the norm pass.  With one instance and D >= 4, 4 tiles per CTA
+// (each CTA's stores and partial overlap the other CTAs' loads, as in the
+// step kernels); otherwise a persistent grid of at most 6 CTAs per SM (the
+// compile-time kernels at D < 4 keep few registers, and more resident CTAs
+// there, or fewer tiles per CTA, measured slower).  The partials are summed
+// exactly, so the grid changes nothing in the result.
+constexpr int64_t kNormTilesPerCta = 4;
+constexpr int kNormPersistentPerSm = 6;
+
+int norm_grid(NormKernel k, const dopt_layout *L, int64_t n_tiles) {
+    n_tiles = std::max<int64_t>(n_tiles, 1);
+    if (L->cfg.instances == 1 && L->cfg.D >= 4)
+        return int((n_tiles + kNormTilesPerCta - 1) / kNormTilesPerCta);
     int sms = 0, per_sm = 0;
-    sm_occupancy(reinterpret_cast<const void *>(k), device, &sms, &per_sm);
-    // a whole number of CTAs per SM, so that every SM gets the same share
-    const int per_sm_cap = std::max(1, kMaxClipCtas / std::max(sms, 1));
-    int64_t g = int64_t(std::max(sms, 1)) * std::min(std::max(per_sm, 1), per_sm_cap);
-    g = std::min<int64_t>(g, kMaxClipCtas);
-    g = std::min<int64_t>(g, std::max<int64_t>(n_tiles, 1));
-    return int(g);
+    sm_occupancy(reinterpret_cast<const void *>(k), L->device, &sms, &per_sm);
+    const int64_t g = int64_t(std::max(sms, 1)) * std::min(std::max(per_sm, 1), kNormPersistentPerSm);
+    return int(std::min(g, n_tiles));
 }
 
 int check_device_tables(const dopt_layout *L, const char *who) {
@@ -544,8 +551,8 @@ int launch_clipped(const char *who, const dopt_layout *L, const dopt_adam_cfg *c
     na.max_norm = max_norm;
     na.counter = const_cast<CounterBlock *>(counter);
     NormKernel nk = norm_kernel_for(L, grad_dtype);
-    const int grid_a = norm_grid(nk, na.n_tiles, L->device);
-    dopt_clip_reset_kernel<<<1, 1, 0, stream>>>(ws);
+    const int grid_a = norm_grid(nk, L, na.n_tiles);
+    dopt_clip_reset_kernel<<<1, kThreads, 0, stream>>>(ws);
     rc = launch_error(who, "workspace reset");
     if (rc != DOPT_OK) return rc;
     cudaError_t e = launch_dependent(nk, dim3(unsigned(grid_a)), dim3(kThreads), stream, na);
@@ -554,6 +561,13 @@ int launch_clipped(const char *who, const dopt_layout *L, const dopt_adam_cfg *c
         return fail(DOPT_E_CUDA, "%s: norm launch: %s", who, cudaGetErrorString(e));
     }
     rc = launch_error(who, "norm");
+    if (rc != DOPT_OK) return rc;
+    e = launch_dependent(dopt_clip_finalize_kernel, dim3(1), dim3(kThreads), stream, na);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(DOPT_E_CUDA, "%s: finalize launch: %s", who, cudaGetErrorString(e));
+    }
+    rc = launch_error(who, "finalize");
     if (rc != DOPT_OK) return rc;
 
     StepArgs a{};
@@ -565,9 +579,10 @@ int launch_clipped(const char *who, const dopt_layout *L, const dopt_adam_cfg *c
     a.skip_nonfinite = na.skip_nonfinite;
     a.counter = counter;  // the counted clipped step: scalars and status from the counter
     StepKernel k = pick_step_kernel<float, kFromMain>(kernel_D(L));
-    // a programmatic dependent of the norm pass: its CTAs start as the norm
-    // pass's CTAs leave, load master/m/v and wait for the pass to complete
-    // before they read the main grads and the coefficient
+    // a programmatic dependent of the finalize kernel: its CTAs start as the
+    // norm pass's CTAs leave, load master/m/v and wait for the finalize
+    // kernel (and so the norm pass) to complete before they read the main
+    // grads and the coefficient
     cudaError_t le = launch_dependent(k, dim3(unsigned(tiles)), dim3(kThreads), stream, a);
     if (le != cudaSuccess) {
         cudaGetLastError();
@@ -961,12 +976,7 @@ extern "C" int dopt_step_clipped_noalloc(const dopt_layout *L, const dopt_adam_c
     if (L->run_start.empty()) return DOPT_OK;
     rc = check_device_tables(L, who);
     if (rc != DOPT_OK) return rc;
-    const int64_t n_tiles = (L->numel + kDoptTileElems - 1) / kDoptTileElems;
-    const int grid_a = norm_grid(norm_kernel_for(L, grad_dtype), n_tiles, L->device);
-    const size_t need = offsetof(ClipWorkspace, partial) + size_t(grid_a) * sizeof(double);
-    if (need > sizeof(g_noalloc_scratch))
-        return fail(DOPT_E_ARG, "%s: the norm pass needs %zu bytes of scratch (%d CTAs), the "
-                    "static scratch holds %zu", who, need, grid_a, sizeof(g_noalloc_scratch));
+    static_assert(sizeof(ClipWorkspace) <= sizeof(g_noalloc_scratch), "scratch size");
     void *scratch = nullptr;
     rc = noalloc_scratch(L->device, &scratch);
     if (rc != DOPT_OK) return rc;
