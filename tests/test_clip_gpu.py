@@ -237,3 +237,33 @@ def test_norm_sum_is_exact(D, log2_scale):
     assert exact < 2 ** 53
     got = ws[16:24].cpu().view(torch.float64).item()
     assert got == want, (got, want)
+
+
+@pytest.mark.parametrize("D", [8, 2])  # 4 tiles per CTA; the persistent grid
+def test_norm_sum_is_rounded_once(D):
+    """Three CTAs' partials: 2^91 (tile 0, every grad 2^40) and twice
+    3 * 2^36 (tiles 1 and 2, three grads 2^18 each), each exact.  Their exact
+    sum, 2^91 + 0.75 ulp, rounds once to 2^91 + 2^39; added one after the
+    other in fp64 each small partial (0.375 ulp) would vanish and leave
+    2^91.  Tiles 0, 1 and 2 fall in three different CTAs both with 4 tiles
+    per CTA (12 tiles: 3 CTAs taking every third tile) and with the
+    persistent grid (one tile each)."""
+    tiles = 12
+    L = B.dopt_build_range_map([tiles * 2048], D, 0, 64).to_device()
+    N = L.padded_numel
+    assert N == tiles * 2048
+    g0 = torch.zeros(N, dtype=torch.bfloat16)
+    g0[:2048] = 2.0 ** 40
+    g0[2048:2048 + 3] = 2.0 ** 18
+    g0[4096:4096 + 3] = 2.0 ** 18
+    grads = [g0.to(DEV)] + [torch.zeros(N, dtype=torch.bfloat16, device=DEV) for _ in range(D - 1)]
+    master = torch.zeros(N, device=DEV)
+    m, v = torch.zeros(N, device=DEV), torch.zeros(N, device=DEV)
+    params = [torch.zeros(N, dtype=torch.bfloat16, device=DEV) for _ in range(D)]
+    ws = B.clip_workspace(DEV)
+    mg = torch.empty(N, device=DEV)
+    B.dopt_step_clipped(L, B.AdamConfig(grad_scale=1.0), 1, 3.0e38, grads, master, m, v, params,
+                        mg, ws)
+    torch.cuda.synchronize()
+    got = ws[16:24].cpu().view(torch.float64).item()
+    assert got == float(2 ** 91 + 6 * 2 ** 36) == 2.0 ** 91 + 2.0 ** 39, got
