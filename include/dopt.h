@@ -23,9 +23,10 @@
  *     arguments on the host before anything is queued, report launch errors
  *     through cudaGetLastError, and never allocate or synchronise.  Faults
  *     inside a kernel surface at the caller's next synchronisation.
- *   - The step, all-reduce and gather kernels are launched as
- *     programmatic dependents of the kernel before them on the stream (the
- *     counted step's kernel of its counter kernel): when that kernel
+ *   - The step, all-reduce, gather, norm and finalize kernels are launched
+ *     as programmatic dependents of the kernel before them on the stream
+ *     (the counted step's kernel of its counter kernel, the clipped step's
+ *     passes of the launch before each): when that kernel
  *     lets its dependents start early (as the library's own kernels do),
  *     their CTAs may become resident during its last wave and look up their
  *     runs, but they read no grad, state or param, and write nothing,
