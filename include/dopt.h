@@ -30,8 +30,12 @@
  *     lets its dependents start early (as the library's own kernels do),
  *     their CTAs may become resident during its last wave and look up their
  *     runs, but they read no grad, state or param, and write nothing,
- *     before it has completed.  Stream order is unchanged for everything
- *     else (copies, events, kernels that do not let dependents start).
+ *     before it has completed.  (The clipped step's second pass loads
+ *     master/m/v before its norm pass completes: neither of the call's
+ *     earlier kernels writes them, and the call's first launch is
+ *     stream-ordered, so everything queued before the call has completed
+ *     by then.)  Stream order is unchanged for everything else (copies,
+ *     events, kernels that do not let dependents start).
  *   - Buffer-indexed arrays hold one element per position of the padded
  *     buffer (padded_numel elements).  Padding positions belong to no param;
  *     the step neither reads nor writes them in any buffer.
