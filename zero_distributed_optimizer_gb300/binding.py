@@ -724,7 +724,8 @@ def dopt_step_clipped(layout: Layout, adam: AdamConfig, step: int, max_norm: flo
                       grad_replicas, master, exp_avg, exp_avg_sq, param_replicas, main_grad,
                       workspace, gather: bool = True, norm_out=None, stream=None,
                       round_grad: bool = False, skip_nonfinite: bool = False) -> None:
-    """The step with global grad-norm clipping (two launches).
+    """The step with global grad-norm clipping (two passes over memory: the
+    norm pass, then the step; see dopt_step_clipped in dopt.h).
 
     main_grad: fp32 CUDA tensor of >= padded_numel elements (receives the
     reduced grads before clipping); workspace: from :func:`clip_workspace`;
