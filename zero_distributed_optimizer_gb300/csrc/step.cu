@@ -322,18 +322,19 @@ int launch_step_kernel(const char *who, const dopt_layout *L, dopt_dtype grad_dt
 }
 
 
-// Grid of the norm pass.  With one instance and D >= 4, 4 tiles per CTA
-// (each CTA's stores and partial overlap the other CTAs' loads, as in the
-// step kernels); otherwise a persistent grid of at most 6 CTAs per SM (the
-// compile-time kernels at D < 4 keep few registers, and more resident CTAs
-// there, or fewer tiles per CTA, measured slower).  The partials are summed
-// exactly, so the grid changes nothing in the result.
+// Grid of the norm pass.  For the compile-time kernels at D = 4, 8 and 16
+// (one instance), 4 tiles per CTA: its CTAs leave the SMs one by one to the
+// step pass that follows, as step kernels do.  Otherwise a persistent grid
+// of at most 6 CTAs per SM: at D = 1 and 2, for the run-time-D kernel
+// (other D, several instances) and with more CTAs per SM, the tiled grid
+// measured slower.  The partials are summed exactly, so the grid changes
+// nothing in the result.
 constexpr int64_t kNormTilesPerCta = 4;
 constexpr int kNormPersistentPerSm = 6;
 
 int norm_grid(NormKernel k, const dopt_layout *L, int64_t n_tiles) {
     n_tiles = std::max<int64_t>(n_tiles, 1);
-    if (L->cfg.instances == 1 && L->cfg.D >= 4)
+    if (L->cfg.instances == 1 && (L->cfg.D == 4 || L->cfg.D == 8 || L->cfg.D == 16))
         return int((n_tiles + kNormTilesPerCta - 1) / kNormTilesPerCta);
     int sms = 0, per_sm = 0;
     sm_occupancy(reinterpret_cast<const void *>(k), L->device, &sms, &per_sm);
