@@ -267,3 +267,53 @@ def test_norm_sum_is_rounded_once(D):
     torch.cuda.synchronize()
     got = ws[16:24].cpu().view(torch.float64).item()
     assert got == float(2 ** 91 + 6 * 2 ** 36) == 2.0 ** 91 + 2.0 ** 39, got
+
+
+@pytest.mark.parametrize("D", [8, 2])
+def test_clipped_parity_huge_grads(D):
+    """Grads far beyond fp32's square root of its largest value (some
+    elements 2^70 and 2^100 times larger, bf16 still holds them): the norm is
+    a finite sum of fp64 squares, as in the oracle, not Inf from an fp32
+    square, and the clipped step matches the oracle, run edges included."""
+    sizes, wd, bucket, pad = [5000, 1, 7, 300, 20000, 3, 9999], [1, 0, 1, 0, 1, 1, 0], 0, 1
+    L = B.dopt_build_range_map(sizes, D, bucket, pad, wd).to_device()
+    N = L.padded_numel
+    master, m, v, params, grads = W.random_case(N, D, 1, "bf16", 77)
+    rng = np.random.default_rng(5)
+    g = [x.float() for x in grads[0]]
+    for r in range(D):
+        big = rng.random(N) < 0.01
+        huge = (rng.random(N) < 0.001) & ~big  # at most 2^100 times larger
+        g[r][torch.from_numpy(big)] *= 2.0 ** 70
+        g[r][torch.from_numpy(huge)] *= 2.0 ** 100
+    g = [x.to(torch.bfloat16) for x in g]
+    assert all(torch.isfinite(x.float()).all() for x in g)
+    hg = [t2np_bf16(x) for x in g]
+    adam = B.AdamConfig(grad_scale=1.0 / D)
+    oadam = oracle.make_adam(**asdict(adam))
+    nsq = oracle.grad_norm_sq(sizes, D, bucket, pad, adam.grad_scale, hg)
+    assert np.isfinite(nsq) and nsq > 2.0 ** 140  # some fp32 squares would overflow
+    max_norm = 0.5 * float(np.sqrt(nsq))
+    coef = oracle.clip_coef(nsq, max_norm)
+    h = [master.numpy().copy(), m.numpy().copy(), v.numpy().copy()]
+    hp = [t2np_bf16(p).copy() for p in params]
+    hmg = np.full(N, -9.0, np.float32)
+    d = [master.to(DEV), m.to(DEV), v.to(DEV)]
+    dp = [p.to(DEV) for p in params]
+    mg = torch.full((N,), -9.0, device=DEV)
+    ws = B.clip_workspace(DEV)
+    norm_out = torch.zeros(2, device=DEV)
+    B.dopt_step_clipped(L, adam, 1, max_norm, [x.to(DEV) for x in g], *d, dp, mg, ws,
+                        norm_out=norm_out)
+    oracle.step(sizes, wd, D, bucket, pad, oadam, 1, hg, *h, hp, main_grad_out=hmg, clip_coef=coef)
+    torch.cuda.synchronize()
+    got_norm, got_coef = norm_out.tolist()
+    assert np.isfinite(got_norm)
+    assert abs(got_norm - np.sqrt(nsq)) <= NORM_RTOL * np.sqrt(nsq)
+    assert abs(got_coef - coef) <= NORM_RTOL * coef
+    assert_f32_close(t2np_f32(d[0]), h[0], "master")
+    assert_f32_close(t2np_f32(d[1]), h[1], "exp_avg")
+    assert_f32_close(t2np_f32(d[2]), h[2], "exp_avg_sq")
+    assert_f32_close(t2np_f32(mg), hmg, "main_grad")
+    for r in range(D):
+        assert_bf16_close(t2np_bf16(dp[r]), hp[r], f"param{r}")

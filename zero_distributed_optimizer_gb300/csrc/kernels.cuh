@@ -163,7 +163,8 @@ struct StepArgs {
 // Workspace of the clipped step (device memory, DOPT_CLIP_WORKSPACE_BYTES).
 // The norm pass adds its per-CTA partials exactly: every partial (a
 // non-negative double, a multiple of 2^-149 because every square is an fp32
-// product) is split into 32-bit digits of a fixed-point number whose lowest
+// product, or an fp64 one of a sum of 2^120 or more) is split into 32-bit
+// digits of a fixed-point number whose lowest
 // bit weighs 2^-149, and each digit is added to a 64-bit word with an
 // integer atomic.  Integer sums do not depend on their order, so the norm
 // is the same at every call whatever the grid and the order in which CTAs
@@ -1403,7 +1404,10 @@ __device__ __forceinline__ double warp_sum(double v) {
 // The fused reduce-scatter writes the fp32 main grads and every CTA
 // accumulates the sum of their squares over the tiles it visits (fp32
 // squares summed pairwise per 8-element vector, then one fp64 add per
-// vector, then the CTA's threads in a fixed order) and adds that partial to
+// vector, then the CTA's threads in a fixed order; a vector whose fp32 sum
+// reaches 2^120 -- a grad of 2^60 or more, whose fp32 square may overflow
+// where the pages' sum of squares does not -- is summed in fp64 instead)
+// and adds that partial to
 // the workspace's exact accumulator.  The grid is a few tiles per CTA, or a
 // persistent grid (see norm_grid on the host); the finalize kernel after it
 // turns the sum into the norm and the coefficient.
@@ -1434,7 +1438,18 @@ __global__ void __launch_bounds__(kThreads) dopt_rs_norm_kernel(const __grid_con
             }
             const float s01 = __fadd_rn(sq[0], sq[1]), s23 = __fadd_rn(sq[2], sq[3]);
             const float s45 = __fadd_rn(sq[4], sq[5]), s67 = __fadd_rn(sq[6], sq[7]);
-            local += double(__fadd_rn(__fadd_rn(s01, s23), __fadd_rn(s45, s67)));
+            const float s = __fadd_rn(__fadd_rn(s01, s23), __fadd_rn(s45, s67));
+            if (s < 0x1p120f) {
+                local += double(s);
+            } else {
+                // a square or their sum overflowed fp32, or came near it
+                // (a grad of 2^60 or more), or a grad is NaN: the vector's
+                // squares again in fp64, where no finite fp32 grad overflows
+                double d = 0.0;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) d += double(acc[k]) * double(acc[k]);
+                local += d;
+            }
         } else if (kind == kMixed) {
             // one lane per straddling vector: sharing them out over the warp
             // (as the other kernels do) made this persistent loop, and the
@@ -1447,7 +1462,8 @@ __global__ void __launch_bounds__(kThreads) dopt_rs_norm_kernel(const __grid_con
                 float g = reduce_scalar<G>(a.grads, D, a.R, a.scale, e);
                 if (a.round_grad) g = to_grad_type<G>(g);
                 a.main_grad[e] = g;
-                local += double(__fmul_rn(g, g));
+                // fp32 square, or fp64 from 2^60 on (where fp32 overflows)
+                local += fabsf(g) < 0x1p60f ? double(__fmul_rn(g, g)) : double(g) * double(g);
                 bad += isfinite(g) ? 0u : 1u;
             }
         }
